@@ -1,0 +1,203 @@
+/*
+ * pbs.h — C ABI of the paged block-sparse attend (MiniMax-M3 style) for GB300 (sm_103a).
+ *
+ * The library computes, for every query token, attention over only the keys of
+ * the 128-token blocks its top-k list selects, read from a paged KV cache:
+ *
+ *   1. query position  (decode rows right-aligned to seq_len; prefill tokens
+ *      at context_len + offset in their request),
+ *   2. sparse block table build: causal filter, compaction, page-16 ids and
+ *      the attended context length,
+ *   3. gather + dequantise of the selected K/V rows (bf16, fp8-e4m3, NVFP4),
+ *   4. softmax(scale * q K^T) V per query head with GQA sharing,
+ *   5. index-cache insert (a side path that scatters index keys).
+ *
+ * Sources (vLLM API pages):
+ *   [flashinfer] vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer,
+ *                MiniMaxM3SparseFlashInferImpl.forward
+ *   [nvfp4]      vllm.models.minimax_m3.amd.sparse_attention_nvfp4,
+ *                customize_spec / MiniMaxM3SparseRocmNvfp4Impl.forward / metadata builder
+ *   [sparse_pa]  vllm.models.minimax_m3.amd.ops.sparse_pa,
+ *                _write_sparse_block_table_row_from_values,
+ *                minimax_m3_build_sparse_block_table_decode / _prefill,
+ *                minimax_m3_insert_index_cache, minimax_m3_sparse_block_page_stride
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - All pointers are DEVICE pointers owned by the caller, unless stated otherwise.
+ *   The library allocates no memory and keeps no state between calls.
+ * - Work is enqueued on `stream` (NULL = legacy default stream) and is
+ *   asynchronous; the return value only reports what the host could check
+ *   plus launch errors. Faults found by the kernels themselves are OR-ed into
+ *   `*err_word` (device int32, may be NULL) as PBS_DEVERR_* bits; the caller
+ *   zeroes it and reads it back when it wants to know.
+ * - Strides are in ELEMENTS of the pointed-to type except where the name ends
+ *   in `_bytes`.
+ * - Empty work (zero rows) returns PBS_OK without launching anything, as the
+ *   index-cache insert on [sparse_pa] returns early on empty tensors.
+ * - Constants fixed by the method: SPARSE_BLOCK_SIZE = 128 tokens per logical
+ *   block, 16 token rows per physical page, PAGES_PER_BLOCK = 8 pages per block.
+ *   A page-table entry is a physical BLOCK id b; its pages are
+ *   b * block_page_stride + j, j = 0..7 ([sparse_pa] row writer;
+ *   block_page_stride is 8 when K and V of a block share its pages, 16 when a
+ *   block holds separate K and V sides, [sparse_pa] minimax_m3_sparse_block_page_stride).
+ */
+#ifndef PBS_H
+#define PBS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PBS_API __attribute__((visibility("default")))
+#else
+#define PBS_API
+#endif
+
+/* Same object as cudaStream_t; kept opaque so this header needs no CUDA headers. */
+typedef struct CUstream_st* pbs_stream_t;
+
+/* ---- status codes (return values) ------------------------------------------------------ */
+#define PBS_OK              0
+#define PBS_ERR_ARG         1   /* null pointer where data is needed, bad enum, negative size */
+#define PBS_ERR_SHAPE       2   /* inconsistent sizes/strides ([sparse_pa] asserts and ValueErrors) */
+#define PBS_ERR_UNSUPPORTED 3   /* valid but not implemented here (head_dim != 128, GQA ratio, top-k > 64) */
+#define PBS_ERR_ALIGN       4   /* a pointer or stride breaks the 16-byte alignment the copy engine needs */
+#define PBS_ERR_CUDA        5   /* a CUDA runtime/driver call or a launch failed */
+
+/* ---- device error bits (OR-ed into *err_word by the kernels) ----------------------------- */
+#define PBS_DEVERR_BLOCK_OOB  1  /* a selected, causally valid block id >= max_blocks (row written as empty) */
+#define PBS_DEVERR_PAGE_OOB   2  /* a physical page id >= num_pages (row attends nothing) */
+#define PBS_DEVERR_SLOT_OOB   4  /* an index-cache slot >= num_blocks * block_tokens (row skipped) */
+#define PBS_DEVERR_TIMEOUT    8  /* a bounded wait on a copy gave up (output of that row is undefined) */
+
+/* ---- KV cache formats -------------------------------------------------------------------- */
+#define PBS_KV_BF16      0  /* page = [Hkv][16 rows][K(head_dim) | V(head_dim)] bf16 ([flashinfer]: K|V
+                               interleaved per row, head-major LBHNC; K = [..., :D], V = [..., D:]) */
+#define PBS_KV_FP8_E4M3  1  /* same layout, one e4m3 byte per element ([flashinfer] fp8 view) */
+#define PBS_KV_NVFP4     2  /* page = [2*Hkv slots][1152 B]; slot 2g = K of kv head g, 2g+1 = V
+                               ([nvfp4] customize_spec: two slots per head of packed data + block
+                               scales). A slot is 16 rows x 64 B of e2m1 codes (element 2i in the
+                               low nibble of byte i) then 16 rows x 8 B of e4m3 scales (scale j
+                               covers elements 16j..16j+15). head_dim must be 128. */
+
+/* Text for a status code (static storage; never NULL). */
+PBS_API const char* pbs_status_string(int status);
+
+/* ABI version, bumped on any incompatible change. */
+PBS_API int pbs_abi_version(void);
+
+/*
+ * Sparse block table, decode ([sparse_pa] minimax_m3_build_sparse_block_table_decode and
+ * _write_sparse_block_table_row_from_values; positions right-aligned per [flashinfer] forward).
+ *
+ *   topk        [num_rows, topk_k] int32 logical block ids, -1 padded; row r at topk + r*topk_row_stride
+ *   page_table  [batch, max_blocks] int32 physical block ids, row stride pt_row_stride
+ *   seq_lens    [batch] int32
+ *   num_rows    must equal batch * decode_query_len (PBS_ERR_SHAPE otherwise, as the page asserts);
+ *               row r belongs to request r / decode_query_len at
+ *               abs_pos = seq_lens[b] - decode_query_len + r % decode_query_len
+ *   sparse_bt   out [num_rows, topk_k * 8] int32 page-16 ids, row stride sbt_row_stride >= topk_k*8
+ *   sparse_ctx  out [num_rows] int32 attended keys per row
+ * Per row: a block b is valid iff abs_pos >= 0 and 0 <= b <= abs_pos / 128. Valid blocks
+ * below the own block are packed in top-k order, then the own block; each takes 8 ids
+ * page_table[b]*block_page_stride + j; the rest of the row is 0. ctx = 128*n_full +
+ * (abs_pos + 1 - 128*own) with the own block present, else min(128*n_valid, abs_pos + 1).
+ * 1 <= topk_k <= 64.
+ */
+PBS_API int pbs_build_sparse_block_table_decode(
+    const int32_t* topk, int64_t topk_row_stride, int32_t num_rows, int32_t topk_k,
+    const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+    const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
+    int32_t* sparse_bt, int64_t sbt_row_stride, int32_t* sparse_ctx,
+    int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Sparse block table, prefill ([sparse_pa] minimax_m3_build_sparse_block_table_prefill; the
+ * per-token request id and position of [nvfp4]'s metadata builder are derived here).
+ *
+ *   cu_seqlens_q [num_reqs + 1] int32, non-decreasing, cu_seqlens_q[0] = 0, cu_seqlens_q[num_reqs] = total_q
+ *   seq_lens     [num_reqs] int32 (context + query tokens)
+ * Token t of request r (cu_seqlens_q[r] <= t < cu_seqlens_q[r+1]) sits at
+ * abs_pos = seq_lens[r] - (cu_seqlens_q[r+1] - cu_seqlens_q[r]) + (t - cu_seqlens_q[r]).
+ * Other arguments and the row rule as for the decode table.
+ */
+PBS_API int pbs_build_sparse_block_table_prefill(
+    const int32_t* topk, int64_t topk_row_stride, int32_t total_q, int32_t topk_k,
+    const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+    const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs, int32_t block_page_stride,
+    int32_t* sparse_bt, int64_t sbt_row_stride, int32_t* sparse_ctx,
+    int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Sparse decode attention ([flashinfer] msa_sparse_decode_attention call in forward;
+ * [nvfp4] minimax_m3_nvfp4_sparse_decode_fly call). Builds each row's table itself
+ * (same rule as pbs_build_sparse_block_table_decode) and attends over it.
+ *
+ *   q           [num_rows, num_heads, head_dim] bf16; element (r, h, d) at
+ *               q + r*q_row_stride + h*q_head_stride + d
+ *   kv_cache    base of page 0 in the format `kv_dtype`; page p starts at
+ *               kv_cache + p*page_stride_bytes (16-byte aligned, as is the base)
+ *   num_pages   pages addressable from kv_cache (page ids >= num_pages set PBS_DEVERR_PAGE_OOB)
+ *   num_heads / num_kv_heads: GQA ratio G = num_heads / num_kv_heads; query head h reads kv head h / G.
+ *               Supported: head_dim 128, G in {1, 2, 4, 8}.
+ *   softmax_scale, k_scale, v_scale: fp32. The stored K is multiplied by k_scale and V by v_scale
+ *               (for NVFP4 these are the per-tensor global scales). As on [flashinfer] forward the
+ *               kernel folds k_scale into the softmax scale and v_scale into the output.
+ *   out         [num_rows, num_heads, head_dim] bf16, strides out_row_stride / out_head_stride.
+ *               A row that attends no key gets zeros.
+ */
+PBS_API int pbs_sparse_decode_attention(
+    const void* q, int64_t q_row_stride, int64_t q_head_stride,
+    const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
+    const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+    const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
+    float softmax_scale, float k_scale, float v_scale,
+    void* out, int64_t out_row_stride, int64_t out_head_stride,
+    int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Sparse prefill attention, varlen ([flashinfer] msa_sparse_attention call with cu_seqlens_q;
+ * [nvfp4] minimax_m3_nvfp4_sparse_prefill call). Token positions as in
+ * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention.
+ */
+PBS_API int pbs_sparse_prefill_attention(
+    const void* q, int64_t q_row_stride, int64_t q_head_stride,
+    const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
+    const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+    const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs, int32_t total_q,
+    int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
+    void* out, int64_t out_row_stride, int64_t out_head_stride,
+    int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Index-cache insert ([sparse_pa] minimax_m3_insert_index_cache): for n < num_tokens,
+ * index_cache[slot / block_tokens, slot % block_tokens, :] = index_k[n, :] with
+ * slot = slot_mapping[n * slot_stride]. A negative slot is padding and is skipped; a slot
+ * >= num_blocks*block_tokens sets PBS_DEVERR_SLOT_OOB and is skipped. Slots must be distinct
+ * (two rows writing one slot leave either row there).
+ *
+ *   index_k      [num_tokens, dim] elements of elem_bytes (1, 2 or 4) with strides k_stride0, k_stride1
+ *   index_cache  [num_blocks, block_tokens, dim], strides c_stride0, c_stride1, and a
+ *                contiguous last dimension (PBS_ERR_SHAPE otherwise, as the page raises)
+ *   slot_mapping [num_tokens] int64
+ */
+PBS_API int pbs_insert_index_cache(
+    const void* index_k, int64_t k_stride0, int64_t k_stride1, int32_t num_tokens, int32_t dim,
+    void* index_cache, int64_t c_stride0, int64_t c_stride1, int32_t num_blocks, int32_t block_tokens,
+    const int64_t* slot_mapping, int64_t slot_stride, int32_t elem_bytes,
+    int32_t* err_word, pbs_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* PBS_H */

@@ -1,0 +1,270 @@
+"""paged_block_sparse_gb300 — MiniMax-M3 paged block-sparse attend on GB300 (sm_103a).
+
+A thin ctypes binding over ``libpbs.so`` (C ABI in ``include/pbs.h``). Every function here only
+marshals torch tensors into pointers, strides and sizes, passes the current CUDA stream and
+turns a non-zero status into :class:`PbsError`; all computation runs in the library's CUDA
+kernels. There is no CPU fallback: without the built library every call raises.
+
+Sources (vLLM API pages): ``vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer``
+(forward), ``vllm.models.minimax_m3.amd.sparse_attention_nvfp4`` (forward, customize_spec) and
+``vllm.models.minimax_m3.amd.ops.sparse_pa`` (table builders, row writer, index-cache insert).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "PbsError", "KV_DTYPES", "SPARSE_BLOCK_SIZE", "PAGES_PER_BLOCK", "PAGE_ROWS", "library_path", "lib",
+    "abi_version", "status_string", "build_sparse_block_table_decode", "build_sparse_block_table_prefill",
+    "sparse_decode_attention", "sparse_prefill_attention", "insert_index_cache", "DEVERR",
+]
+
+SPARSE_BLOCK_SIZE = 128
+PAGE_ROWS = 16
+PAGES_PER_BLOCK = 8
+KV_DTYPES = {"bf16": 0, "fp8_e4m3": 1, "nvfp4": 2}
+DEVERR = {"block_oob": 1, "page_oob": 2, "slot_oob": 4, "timeout": 8}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+
+class PbsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status}: {status_string(status) if _lib else '?'}")
+
+
+def library_path() -> str:
+    return os.environ.get("PBS_LIBRARY", os.path.join(_HERE, "libpbs.so"))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpbs.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpbs.so is not built ({path} missing); run "
+                           "`python -m paged_block_sparse_gb300._build` (needs nvcc for sm_103a)")
+    L = ctypes.CDLL(path)
+    i32, i64, f32, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+    L.pbs_status_string.restype = ctypes.c_char_p
+    L.pbs_status_string.argtypes = [ctypes.c_int]
+    L.pbs_abi_version.restype = ctypes.c_int
+    L.pbs_abi_version.argtypes = []
+    table_common = [vp, i64, i32, i32, vp, i64, i32]
+    L.pbs_build_sparse_block_table_decode.restype = ctypes.c_int
+    L.pbs_build_sparse_block_table_decode.argtypes = table_common + [vp, i32, i32, i32, vp, i64, vp, vp, vp]
+    L.pbs_build_sparse_block_table_prefill.restype = ctypes.c_int
+    L.pbs_build_sparse_block_table_prefill.argtypes = table_common + [vp, vp, i32, i32, vp, i64, vp, vp, vp]
+    attend_head = [vp, i64, i64, vp, i64, i64, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32]
+    L.pbs_sparse_decode_attention.restype = ctypes.c_int
+    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp, vp]
+    L.pbs_sparse_prefill_attention.restype = ctypes.c_int
+    L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
+                                                             vp, vp]
+    L.pbs_insert_index_cache.restype = ctypes.c_int
+    L.pbs_insert_index_cache.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32, vp, i64, i32, vp, vp]
+    del sz
+    _lib = L
+    return L
+
+
+def abi_version() -> int:
+    return int(lib().pbs_abi_version())
+
+
+def status_string(status: int) -> str:
+    return lib().pbs_status_string(int(status)).decode()
+
+
+# --------------------------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------------------------
+
+def _dev(t: torch.Tensor, name: str, dtype=None, min_dim=1) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library reads device memory only)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() < min_dim:
+        raise ValueError(f"{name} must have at least {min_dim} dims")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PbsError(status, where)
+
+
+def _rows2d(t: torch.Tensor, name: str) -> torch.Tensor:
+    """[1, R, k] or [R, k] int32 with unit last stride -> [R, k] view."""
+    _dev(t, name, torch.int32, 2)
+    if t.dim() == 3:
+        if t.shape[0] != 1:
+            raise ValueError(f"{name} must be [1, rows, topk] or [rows, topk]")
+        t = t[0]
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must have a contiguous last dimension")
+    return t
+
+
+def _table2d(t: torch.Tensor, name: str) -> torch.Tensor:
+    _dev(t, name, torch.int32, 2)
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be [rows, cols] with a contiguous last dimension")
+    return t
+
+
+def _cache_geometry(kv_cache: torch.Tensor):
+    _dev(kv_cache, "kv_cache")
+    page_stride_bytes = kv_cache.stride(0) * kv_cache.element_size()
+    return int(kv_cache.shape[0]), int(page_stride_bytes)
+
+
+# --------------------------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------------------------
+
+def build_sparse_block_table_decode(topk, page_table, seq_lens, decode_query_len: int = 1,
+                                    block_page_stride: int = PAGES_PER_BLOCK, sparse_bt=None, sparse_ctx=None,
+                                    err_word=None, stream=None):
+    """Decode sparse block table (vLLM sparse_pa minimax_m3_build_sparse_block_table_decode).
+
+    Returns (sparse_bt [rows, topk*8] int32, sparse_ctx [rows] int32)."""
+    tk = _rows2d(topk, "topk")
+    pt = _table2d(page_table, "page_table")
+    sl = _dev(seq_lens, "seq_lens", torch.int32)
+    rows, k = tk.shape
+    if sparse_bt is None:
+        sparse_bt = torch.empty(rows, k * PAGES_PER_BLOCK, dtype=torch.int32, device=tk.device)
+    if sparse_ctx is None:
+        sparse_ctx = torch.empty(rows, dtype=torch.int32, device=tk.device)
+    _dev(sparse_bt, "sparse_bt", torch.int32, 2)
+    _dev(sparse_ctx, "sparse_ctx", torch.int32)
+    st = lib().pbs_build_sparse_block_table_decode(
+        _ptr(tk), tk.stride(0), rows, k, _ptr(pt), pt.stride(0), pt.shape[1], _ptr(sl), sl.shape[0],
+        int(decode_query_len), int(block_page_stride), _ptr(sparse_bt), sparse_bt.stride(0), _ptr(sparse_ctx),
+        _ptr(err_word), _stream(stream, tk.device))
+    _check(st, "pbs_build_sparse_block_table_decode")
+    return sparse_bt, sparse_ctx
+
+
+def build_sparse_block_table_prefill(topk, page_table, cu_seqlens_q, seq_lens,
+                                     block_page_stride: int = PAGES_PER_BLOCK, sparse_bt=None, sparse_ctx=None,
+                                     err_word=None, stream=None):
+    """Prefill sparse block table (vLLM sparse_pa minimax_m3_build_sparse_block_table_prefill)."""
+    tk = _rows2d(topk, "topk")
+    pt = _table2d(page_table, "page_table")
+    cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    sl = _dev(seq_lens, "seq_lens", torch.int32)
+    rows, k = tk.shape
+    if sparse_bt is None:
+        sparse_bt = torch.empty(rows, k * PAGES_PER_BLOCK, dtype=torch.int32, device=tk.device)
+    if sparse_ctx is None:
+        sparse_ctx = torch.empty(rows, dtype=torch.int32, device=tk.device)
+    _dev(sparse_bt, "sparse_bt", torch.int32, 2)
+    _dev(sparse_ctx, "sparse_ctx", torch.int32)
+    st = lib().pbs_build_sparse_block_table_prefill(
+        _ptr(tk), tk.stride(0), rows, k, _ptr(pt), pt.stride(0), pt.shape[1], _ptr(cu), _ptr(sl), sl.shape[0],
+        int(block_page_stride), _ptr(sparse_bt), sparse_bt.stride(0), _ptr(sparse_ctx), _ptr(err_word),
+        _stream(stream, tk.device))
+    _check(st, "pbs_build_sparse_block_table_prefill")
+    return sparse_bt, sparse_ctx
+
+
+def _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out):
+    _dev(q, "q", torch.bfloat16, 3)
+    if q.stride(2) != 1:
+        raise ValueError("q must have a contiguous head_dim")
+    if kv_dtype not in KV_DTYPES:
+        raise ValueError(f"kv_dtype must be one of {sorted(KV_DTYPES)}")
+    num_pages, page_stride_bytes = _cache_geometry(kv_cache)
+    tk = _rows2d(topk, "topk")
+    pt = _table2d(page_table, "page_table")
+    if tk.shape[0] != q.shape[0]:
+        raise ValueError(f"topk has {tk.shape[0]} rows but q has {q.shape[0]}")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _dev(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape or out.stride(2) != 1:
+        raise ValueError("out must match q's shape with a contiguous head_dim")
+    return num_pages, page_stride_bytes, tk, pt, out
+
+
+def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
+                            decode_query_len: int, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                            block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None):
+    """Sparse decode attend (vLLM flashinfer msa_sparse_decode_attention / nvfp4 decode call).
+
+    q [rows, Hq, 128] bf16 with rows = batch * decode_query_len; kv_cache [num_pages, ...] in the
+    ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16."""
+    num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
+    sl = _dev(seq_lens, "seq_lens", torch.int32)
+    st = lib().pbs_sparse_decode_attention(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
+        int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
+        _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), float(softmax_scale),
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(err_word),
+        _stream(stream, q.device))
+    _check(st, "pbs_sparse_decode_attention")
+    return out
+
+
+def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
+                             seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                             block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None):
+    """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call)."""
+    num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
+    cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    sl = _dev(seq_lens, "seq_lens", torch.int32)
+    st = lib().pbs_sparse_prefill_attention(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
+        int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
+        _ptr(cu), _ptr(sl), sl.shape[0], q.shape[0], int(block_page_stride), float(softmax_scale), float(k_scale),
+        float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(err_word), _stream(stream, q.device))
+    _check(st, "pbs_sparse_prefill_attention")
+    return out
+
+
+def insert_index_cache(index_k, index_cache, index_slot_mapping, err_word=None, stream=None) -> None:
+    """Scatter index keys [N, D] into the key-only side cache [B, T, D] (vLLM sparse_pa
+    minimax_m3_insert_index_cache), with the page's argument checks."""
+    if index_k.numel() == 0 or index_cache.numel() == 0:
+        return
+    if index_k.dim() != 2 or index_cache.dim() != 3:
+        raise ValueError("index cache insert expects [N,D] and [B,T,D]")
+    if index_k.shape[1] != index_cache.shape[2]:
+        raise ValueError("index key dim must match index cache head dim")
+    if index_slot_mapping.dim() != 1 or index_slot_mapping.shape[0] != index_k.shape[0]:
+        raise ValueError("index slot mapping must be a length-N vector")
+    if index_cache.stride(2) != 1:
+        raise ValueError("index cache requires contiguous head dimension")
+    _dev(index_k, "index_k")
+    _dev(index_cache, "index_cache")
+    _dev(index_slot_mapping, "index_slot_mapping", torch.int64)
+    if index_k.dtype != index_cache.dtype:
+        raise TypeError("index_k and index_cache must share a dtype")
+    st = lib().pbs_insert_index_cache(
+        _ptr(index_k), index_k.stride(0), index_k.stride(1), index_k.shape[0], index_k.shape[1], _ptr(index_cache),
+        index_cache.stride(0), index_cache.stride(1), index_cache.shape[0], index_cache.shape[1],
+        _ptr(index_slot_mapping), index_slot_mapping.stride(0), index_k.element_size(), _ptr(err_word),
+        _stream(stream, index_k.device))
+    _check(st, "pbs_insert_index_cache")

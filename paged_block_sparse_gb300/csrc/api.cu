@@ -1,0 +1,338 @@
+// The C ABI of libpbs (include/pbs.h): argument validation, scale folding, tensor-map encoding,
+// launch-shape choice and dispatch to the kernels. Nothing here allocates device memory.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/pbs.h"
+#include "pbs_internal.h"
+
+namespace {
+
+using pbs::AttendArgs;
+using pbs::InsertArgs;
+using pbs::TableArgs;
+
+constexpr int kBlockPages = 8;
+constexpr int kPageRows = 16;
+constexpr int kHeadDim = 128;
+constexpr int kMaxTopk = 64;
+constexpr int kNvfp4SlotBytes = 1152;
+
+bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+int page_content_bytes(int kv_dtype, int num_kv_heads) {
+  switch (kv_dtype) {
+    case PBS_KV_BF16: return num_kv_heads * kPageRows * 2 * kHeadDim * 2;
+    case PBS_KV_FP8_E4M3: return num_kv_heads * kPageRows * 2 * kHeadDim;
+    case PBS_KV_NVFP4: return num_kv_heads * 2 * kNvfp4SlotBytes;
+    default: return -1;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Page rows of one kv head as a 4-D tensor {row elements, 16 rows, kv heads, pages}. A box is
+// 128 bytes of 16 consecutive rows of one (page, head), stored 128B-swizzled in shared memory.
+int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
+                     int64_t page_stride_bytes) {
+  std::memset(map, 0, sizeof(*map));
+  if (kv_dtype == PBS_KV_NVFP4) return PBS_OK;  // read with untiled bulk copies
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PBS_ERR_CUDA;
+  const int eb = kv_dtype == PBS_KV_BF16 ? 2 : 1;
+  const cuuint64_t row_elems = 2 * kHeadDim;
+  const cuuint64_t dims[4] = {row_elems, kPageRows, static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {row_elems * eb, row_elems * eb * kPageRows, static_cast<cuuint64_t>(page_stride_bytes)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), kPageRows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                         const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
+}
+
+// CTAs per (row, kv head): enough clusters to fill the GPU a few times over, but at least two
+// 128-key slots per CTA. PBS_ATTEND_SPLITS in {1, 2, 4, 8} overrides (tuning and tests).
+int choose_splits(int64_t units, int k) {
+  if (const char* env = std::getenv("PBS_ATTEND_SPLITS")) {
+    const int s = std::atoi(env);
+    if (s == 1 || s == 2 || s == 4 || s == 8) return s;
+  }
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t target = static_cast<int64_t>(sms) * 3 * 4;
+  int s = 1;
+  while (s < 8 && units * s < target && 4 * s <= k) s *= 2;
+  return s;
+}
+
+int check_common_table(const int32_t* topk, int64_t topk_row_stride, int32_t topk_k, const int32_t* page_table,
+                       int64_t pt_row_stride, int32_t max_blocks, int32_t block_page_stride) {
+  if (topk == nullptr || page_table == nullptr) return PBS_ERR_ARG;
+  if (topk_k <= 0 || max_blocks <= 0) return PBS_ERR_ARG;
+  if (topk_k > kMaxTopk) return PBS_ERR_UNSUPPORTED;
+  if (topk_row_stride < topk_k || pt_row_stride < max_blocks) return PBS_ERR_SHAPE;
+  if (block_page_stride < kBlockPages) return PBS_ERR_SHAPE;
+  return PBS_OK;
+}
+
+int check_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,
+                 int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype, int32_t num_heads,
+                 int32_t num_kv_heads, int32_t head_dim, float softmax_scale, float k_scale, float v_scale,
+                 const void* out, int64_t out_row_stride, int64_t out_head_stride) {
+  if (q == nullptr || kv_cache == nullptr || out == nullptr) return PBS_ERR_ARG;
+  if (kv_dtype != PBS_KV_BF16 && kv_dtype != PBS_KV_FP8_E4M3 && kv_dtype != PBS_KV_NVFP4) return PBS_ERR_ARG;
+  if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) return PBS_ERR_ARG;
+  if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return PBS_ERR_ARG;
+  if (num_heads % num_kv_heads != 0) return PBS_ERR_SHAPE;
+  if (head_dim != kHeadDim) return PBS_ERR_UNSUPPORTED;
+  const int G = num_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PBS_ERR_UNSUPPORTED;
+  if (num_kv_heads > 65535) return PBS_ERR_UNSUPPORTED;
+  if (q_row_stride < 0 || q_head_stride < 0 || out_row_stride < 0 || out_head_stride < 0) return PBS_ERR_SHAPE;
+  if (num_pages <= 0 || num_pages > 0x7fffffffLL) return PBS_ERR_SHAPE;
+  if (page_stride_bytes < page_content_bytes(kv_dtype, num_kv_heads)) return PBS_ERR_SHAPE;
+  if (!aligned(kv_cache, 16) || page_stride_bytes % 16 != 0) return PBS_ERR_ALIGN;
+  if (!aligned(q, 4) || q_row_stride % 2 != 0 || q_head_stride % 2 != 0) return PBS_ERR_ALIGN;
+  if (!aligned(out, 2)) return PBS_ERR_ALIGN;
+  return PBS_OK;
+}
+
+AttendArgs make_attend_args(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,
+                            int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype, int32_t num_heads,
+                            int32_t num_kv_heads, const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
+                            const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+                            const int32_t* seq_lens, int32_t block_page_stride, float softmax_scale,
+                            float k_scale, float v_scale, void* out, int64_t out_row_stride,
+                            int64_t out_head_stride, int32_t* err_word) {
+  AttendArgs a = {};
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_row_stride = q_row_stride;
+  a.q_head_stride = q_head_stride;
+  a.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  a.page_stride_bytes = page_stride_bytes;
+  a.num_pages = num_pages;
+  a.kv_dtype = kv_dtype;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_heads / num_kv_heads;
+  a.topk = topk;
+  a.topk_row_stride = topk_row_stride;
+  a.k = topk_k;
+  a.page_table = page_table;
+  a.pt_row_stride = pt_row_stride;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.block_page_stride = block_page_stride;
+  // k_scale folds into the logits, v_scale into the output (vLLM page
+  // vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer, forward); log2(e) moves the
+  // softmax to base 2.
+  a.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * k_scale * 1.4426950408889634);
+  a.v_scale = v_scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.out_row_stride = out_row_stride;
+  a.out_head_stride = out_head_stride;
+  a.err_word = err_word;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pbs_status_string(int status) {
+  switch (status) {
+    case PBS_OK: return "ok";
+    case PBS_ERR_ARG: return "invalid argument (null pointer, bad enum or non-positive size)";
+    case PBS_ERR_SHAPE: return "inconsistent shapes or strides";
+    case PBS_ERR_UNSUPPORTED: return "unsupported configuration (head_dim must be 128, GQA ratio 1/2/4/8, top-k <= 64)";
+    case PBS_ERR_ALIGN: return "misaligned pointer or stride (cache 16 B, q 4 B, out 2 B)";
+    case PBS_ERR_CUDA: return "CUDA error (launch, tensor-map encoding or driver entry point)";
+    default: return "unknown status";
+  }
+}
+
+int pbs_abi_version(void) { return 1; }
+
+int pbs_build_sparse_block_table_decode(const int32_t* topk, int64_t topk_row_stride, int32_t num_rows,
+                                        int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride,
+                                        int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                        int32_t decode_query_len, int32_t block_page_stride, int32_t* sparse_bt,
+                                        int64_t sbt_row_stride, int32_t* sparse_ctx, int32_t* err_word,
+                                        pbs_stream_t stream) {
+  if (num_rows < 0 || batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
+  if (static_cast<int64_t>(batch) * decode_query_len != num_rows) return PBS_ERR_SHAPE;
+  if (num_rows == 0) return PBS_OK;
+  int st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  if (st != PBS_OK) return st;
+  if (seq_lens == nullptr || sparse_bt == nullptr || sparse_ctx == nullptr) return PBS_ERR_ARG;
+  if (sbt_row_stride < static_cast<int64_t>(topk_k) * kBlockPages) return PBS_ERR_SHAPE;
+  TableArgs a = {};
+  a.topk = topk;
+  a.topk_row_stride = topk_row_stride;
+  a.num_rows = num_rows;
+  a.k = topk_k;
+  a.page_table = page_table;
+  a.pt_row_stride = pt_row_stride;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.decode_query_len = decode_query_len;
+  a.block_page_stride = block_page_stride;
+  a.sparse_bt = sparse_bt;
+  a.sbt_row_stride = sbt_row_stride;
+  a.sparse_ctx = sparse_ctx;
+  a.err_word = err_word;
+  return pbs::launch_build_table(a, false, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+                                                                                                  : PBS_ERR_CUDA;
+}
+
+int pbs_build_sparse_block_table_prefill(const int32_t* topk, int64_t topk_row_stride, int32_t total_q,
+                                         int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride,
+                                         int32_t max_blocks, const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                                         int32_t num_reqs, int32_t block_page_stride, int32_t* sparse_bt,
+                                         int64_t sbt_row_stride, int32_t* sparse_ctx, int32_t* err_word,
+                                         pbs_stream_t stream) {
+  if (total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
+  if (total_q == 0) return PBS_OK;
+  if (num_reqs == 0) return PBS_ERR_SHAPE;
+  int st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  if (st != PBS_OK) return st;
+  if (cu_seqlens_q == nullptr || seq_lens == nullptr || sparse_bt == nullptr || sparse_ctx == nullptr)
+    return PBS_ERR_ARG;
+  if (sbt_row_stride < static_cast<int64_t>(topk_k) * kBlockPages) return PBS_ERR_SHAPE;
+  TableArgs a = {};
+  a.topk = topk;
+  a.topk_row_stride = topk_row_stride;
+  a.num_rows = total_q;
+  a.k = topk_k;
+  a.page_table = page_table;
+  a.pt_row_stride = pt_row_stride;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.num_reqs = num_reqs;
+  a.block_page_stride = block_page_stride;
+  a.sparse_bt = sparse_bt;
+  a.sbt_row_stride = sbt_row_stride;
+  a.sparse_ctx = sparse_ctx;
+  a.err_word = err_word;
+  return pbs::launch_build_table(a, true, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+                                                                                                 : PBS_ERR_CUDA;
+}
+
+int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,
+                                int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, const int32_t* topk, int64_t topk_row_stride,
+                                int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+                                const int32_t* seq_lens, int32_t batch, int32_t decode_query_len,
+                                int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
+                                void* out, int64_t out_row_stride, int64_t out_head_stride, int32_t* err_word,
+                                pbs_stream_t stream) {
+  if (batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
+  const int64_t rows = static_cast<int64_t>(batch) * decode_query_len;
+  if (rows == 0) return PBS_OK;
+  if (rows > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
+  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
+                        out_head_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  if (st != PBS_OK) return st;
+  if (seq_lens == nullptr) return PBS_ERR_ARG;
+  AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
+                                  num_heads, num_kv_heads, topk, topk_row_stride, topk_k, page_table, pt_row_stride,
+                                  max_blocks, seq_lens, block_page_stride, softmax_scale, k_scale, v_scale, out,
+                                  out_row_stride, out_head_stride, err_word);
+  a.decode_query_len = decode_query_len;
+  a.num_rows = static_cast<int32_t>(rows);
+  a.splits = choose_splits(rows * num_kv_heads, topk_k);
+  CUtensorMap map;
+  st = encode_cache_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
+  if (st != PBS_OK) return st;
+  return pbs::launch_attend(a, false, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+                                                                                                  : PBS_ERR_CUDA;
+}
+
+int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,
+                                 int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype, int32_t num_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, const int32_t* topk, int64_t topk_row_stride,
+                                 int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+                                 const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs,
+                                 int32_t total_q, int32_t block_page_stride, float softmax_scale, float k_scale,
+                                 float v_scale, void* out, int64_t out_row_stride, int64_t out_head_stride,
+                                 int32_t* err_word, pbs_stream_t stream) {
+  if (total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
+  if (total_q == 0) return PBS_OK;
+  if (num_reqs == 0) return PBS_ERR_SHAPE;
+  if (total_q > 0x7fffffff / 8) return PBS_ERR_UNSUPPORTED;
+  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
+                        out_head_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  if (st != PBS_OK) return st;
+  if (cu_seqlens_q == nullptr || seq_lens == nullptr) return PBS_ERR_ARG;
+  AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
+                                  num_heads, num_kv_heads, topk, topk_row_stride, topk_k, page_table, pt_row_stride,
+                                  max_blocks, seq_lens, block_page_stride, softmax_scale, k_scale, v_scale, out,
+                                  out_row_stride, out_head_stride, err_word);
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.num_reqs = num_reqs;
+  a.num_rows = total_q;
+  a.splits = choose_splits(static_cast<int64_t>(total_q) * num_kv_heads, topk_k);
+  CUtensorMap map;
+  st = encode_cache_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
+  if (st != PBS_OK) return st;
+  return pbs::launch_attend(a, true, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+                                                                                                 : PBS_ERR_CUDA;
+}
+
+int pbs_insert_index_cache(const void* index_k, int64_t k_stride0, int64_t k_stride1, int32_t num_tokens, int32_t dim,
+                           void* index_cache, int64_t c_stride0, int64_t c_stride1, int32_t num_blocks,
+                           int32_t block_tokens, const int64_t* slot_mapping, int64_t slot_stride, int32_t elem_bytes,
+                           int32_t* err_word, pbs_stream_t stream) {
+  if (num_tokens < 0 || dim < 0 || num_blocks < 0 || block_tokens < 0) return PBS_ERR_ARG;
+  if (num_tokens == 0 || dim == 0 || num_blocks == 0 || block_tokens == 0) return PBS_OK;  // empty: nothing to do
+  if (index_k == nullptr || index_cache == nullptr || slot_mapping == nullptr) return PBS_ERR_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return PBS_ERR_ARG;
+  if (k_stride0 < 0 || k_stride1 < 0 || c_stride0 < 0 || c_stride1 < 0 || slot_stride < 0) return PBS_ERR_SHAPE;
+  if (!aligned(index_k, elem_bytes) || !aligned(index_cache, elem_bytes) || !aligned(slot_mapping, 8))
+    return PBS_ERR_ALIGN;
+  InsertArgs a = {};
+  a.index_k = static_cast<const uint8_t*>(index_k);
+  a.k_stride0 = k_stride0;
+  a.k_stride1 = k_stride1;
+  a.num_tokens = num_tokens;
+  a.dim = dim;
+  a.index_cache = static_cast<uint8_t*>(index_cache);
+  a.c_stride0 = c_stride0;
+  a.c_stride1 = c_stride1;
+  a.num_blocks = num_blocks;
+  a.block_tokens = block_tokens;
+  a.slot_mapping = slot_mapping;
+  a.slot_stride = slot_stride;
+  a.elem_bytes = elem_bytes;
+  a.err_word = err_word;
+  return pbs::launch_insert_index_cache(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+                                                                                                  : PBS_ERR_CUDA;
+}
+
+}  // extern "C"

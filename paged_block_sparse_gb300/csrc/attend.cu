@@ -1,0 +1,548 @@
+// Token-centric paged block-sparse attend (decode rows and prefill tokens).
+//
+// What it computes (vLLM pages vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer, forward,
+// and vllm.models.minimax_m3.amd.sparse_attention_nvfp4, forward): for each query row and kv head g,
+// out[h] = v_scale * softmax(softmax_scale * k_scale * q_h K^T) V over the keys of the row's
+// compacted sparse block table (built in-kernel by compact_row, the rule of
+// vllm.models.minimax_m3.amd.ops.sparse_pa, _write_sparse_block_table_row_from_values), for the G
+// query heads h of group g.
+//
+// GB300 design
+// ------------
+// * One cluster of S CTAs per (row, kv head); CTA s takes a contiguous range of the row's
+//   128-key slots. The S partial (max, sum, O) triples are merged through distributed shared
+//   memory after a cluster barrier, so no global scratch and no second launch are needed.
+// * Per CTA: 1 producer warp issues one page (16 rows x one kv head) per pipeline stage with TMA
+//   (cp.async.bulk.tensor, 128-byte swizzle, mbarrier completion); 4 consumer warps take pages
+//   round-robin. bf16/fp8 pages come through a 4-D tensor map; NVFP4 slots (K|V of the head,
+//   2304 contiguous bytes) through an untiled bulk copy.
+// * The contraction is tiny (8 heads x 16 keys x 128 dims per page), so it runs on mma.sync with
+//   keys as the M dimension (no padding of the 8 heads): S^T = K Q^T, then P^T is transposed in
+//   registers (movmatrix) into the B operand of O^T = V^T P^T. The kernel is HBM-bound; the
+//   tensor path only keeps the arithmetic off the critical path.
+// * bf16 K/V: bf16 MMAs, P split into bf16 hi + lo parts (keeps the attend within a 2e-3
+//   relative RMS of the fp64 result). fp8 / NVFP4 K/V: dequantised exactly to fp16 in
+//   registers, fp16 MMAs with fp16 P.
+// * Online softmax in the log2 domain, fp32 state; k_scale folds into the softmax scale and
+//   v_scale into the output (exact, since logits are linear in K and the output in V).
+#include <cooperative_groups.h>
+
+#include "pbs_device.cuh"
+#include "pbs_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace pbs {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 6;
+constexpr int kTileHeads = 8;  // the n8 tile of the MMA: up to 8 query heads per kv head
+
+template <int FMT>
+struct StageBytes;
+template <>
+struct StageBytes<PBS_KV_BF16> {  // [4 quarter rows][16 rows][128 B], 128B-swizzled
+  static constexpr int v = 8192;
+};
+template <>
+struct StageBytes<PBS_KV_FP8_E4M3> {  // [2 halves][16 rows][128 B], 128B-swizzled
+  static constexpr int v = 4096;
+};
+template <>
+struct StageBytes<PBS_KV_NVFP4> {  // K slot (1152 B) then V slot (1152 B), as stored
+  static constexpr int v = 2304;
+};
+constexpr int kNvfp4Slot = 1152;
+
+struct Merge {
+  float o[kConsumerWarps][kTileHeads][kHeadDim];
+  float m[kConsumerWarps][kTileHeads];
+  float l[kConsumerWarps][kTileHeads];
+  float cta_m[kTileHeads];
+  float cta_l[kTileHeads];
+};
+
+struct Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int32_t slot_base[kMaxTopk];
+  int32_t ctx;
+  int32_t abort;
+};
+
+template <int FMT>
+constexpr size_t smem_bytes() {
+  return 1024 + size_t(kStages) * StageBytes<FMT>::v + sizeof(Merge) + sizeof(Ctl);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128_zero(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Zero the V rows [nv, 16) of a stage, so that masked keys cannot inject NaN/Inf from
+// uninitialised cache rows into P*V (P is 0 there, but 0 * NaN is NaN).
+template <int FMT>
+__device__ __forceinline__ void zero_v_tail(uint32_t st, int nv, int lane) {
+  if (FMT == PBS_KV_BF16) {
+    // quarters 2 and 3, 8 chunks of 16 B per row each
+    for (int i = lane; i < (16 - nv) * 16; i += 32) {
+      const int r = nv + (i >> 4), q = 2 + ((i >> 3) & 1), c = i & 7;
+      sts128_zero(st + q * 2048 + r * 128 + c * 16);
+    }
+  } else if (FMT == PBS_KV_FP8_E4M3) {
+    for (int i = lane; i < (16 - nv) * 8; i += 32) {
+      const int r = nv + (i >> 3), c = i & 7;
+      sts128_zero(st + 2048 + r * 128 + c * 16);
+    }
+  } else {
+    // V codes: 4 chunks of 16 B per row; V scales: 8 B per row
+    for (int i = lane; i < (16 - nv) * 4; i += 32) {
+      const int r = nv + (i >> 2), c = i & 3;
+      sts128_zero(st + kNvfp4Slot + r * 64 + c * 16);
+    }
+    for (int r = nv + lane; r < 16; r += 32) {
+      asm volatile("st.shared.v2.b32 [%0], {%1, %1};" ::"r"(st + kNvfp4Slot + 1024 + r * 8), "r"(0) : "memory");
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
+template <int FMT, bool PREFILL>
+__global__ void __launch_bounds__(kThreads, 3) attend_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                             const AttendArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr int kStage = StageBytes<FMT>::v;
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+  uint8_t* stages = smem;
+  Merge* mg = reinterpret_cast<Merge*>(smem + kStages * kStage);
+  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(mg) + sizeof(Merge));
+
+  const int S = a.splits;
+  const int split = blockIdx.x % S;
+  const int row = blockIdx.x / S;
+  const int g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.group;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], 1);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+
+  int req, abs_pos;
+  if (PREFILL) prefill_position(row, a.cu_seqlens_q, a.num_reqs, a.seq_lens, req, abs_pos);
+  else decode_position(row, a.decode_query_len, a.seq_lens, req, abs_pos);
+
+  // ---- producer warp: the row's compaction; consumers: Q fragments --------------------------
+  uint32_t qf[8][2];
+  if (warp == kConsumerWarps) {
+    RowCompaction rc = compact_row(a.topk + static_cast<int64_t>(row) * a.topk_row_stride, a.k, abs_pos,
+                                   a.page_table + static_cast<int64_t>(req) * a.pt_row_stride, a.max_blocks,
+                                   a.block_page_stride, ctl->slot_base);
+    bool page_bad = false;
+    for (int s = lane; s < rc.n_written; s += 32) {
+      const int64_t base = ctl->slot_base[s];
+      page_bad |= base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages;
+    }
+    page_bad = __any_sync(0xffffffffu, page_bad);
+    if (lane == 0) {
+      if (rc.bad && split == 0 && g == 0) set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+      if (page_bad && split == 0 && g == 0) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+      ctl->ctx = page_bad ? 0 : rc.ctx;
+    }
+  } else {
+    const int hh = lane >> 2, c = lane & 3;
+    const bool live = hh < G;
+    const uint16_t* qh =
+        a.q + static_cast<int64_t>(row) * a.q_row_stride + static_cast<int64_t>(g * G + (live ? hh : 0)) * a.q_head_stride;
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int d0, d1;
+      if (FMT == PBS_KV_BF16) {
+        d0 = 16 * j + 2 * c;
+        d1 = d0 + 8;
+      } else if (FMT == PBS_KV_FP8_E4M3) {
+        d0 = 16 * j + 4 * c;
+        d1 = d0 + 2;
+      } else {
+        d0 = 32 * c + 4 * j;
+        d1 = d0 + 2;
+      }
+      uint32_t w0 = live ? __ldg(q32 + (d0 >> 1)) : 0u;
+      uint32_t w1 = live ? __ldg(q32 + (d1 >> 1)) : 0u;
+      if (FMT != PBS_KV_BF16) {
+        w0 = bf16x2_to_f16x2(w0);
+        w1 = bf16x2_to_f16x2(w1);
+      }
+      qf[j][0] = w0;
+      qf[j][1] = w1;
+    }
+  }
+  __syncthreads();
+
+  const int ctx = ctl->ctx;
+  const int n_slots = (ctx + kSparseBlock - 1) / kSparseBlock;
+  const int per = (n_slots + S - 1) / S;
+  const int slot0 = min(split * per, n_slots), slot1 = min(slot0 + per, n_slots);
+  const int key0 = slot0 * kSparseBlock;
+  const int key1 = min(slot1 * kSparseBlock, ctx);
+  const int npages = key1 > key0 ? (key1 - key0 + kPageRows - 1) / kPageRows : 0;
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int p = 0; p < npages; ++p) {
+        const int stage = p % kStages;
+        if (p >= kStages) {
+          if (!mbar_wait_bounded(&ctl->empty[stage], ((p / kStages) - 1) & 1)) {
+            set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+            atomicExch(&ctl->abort, 1);
+            break;
+          }
+        }
+        if (*reinterpret_cast<volatile int32_t*>(&ctl->abort)) break;
+        const int kp = (key0 >> 4) + p;
+        const int page = ctl->slot_base[kp >> 3] + (kp & 7);
+        uint8_t* dst = stages + stage * kStage;
+        mbar_arrive_expect_tx(&ctl->full[stage], kStage);
+        if (FMT == PBS_KV_BF16) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) tma_load_4d(dst + qq * 2048, &tmap, &ctl->full[stage], 64 * qq, 0, g, page);
+        } else if (FMT == PBS_KV_FP8_E4M3) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) tma_load_4d(dst + hh * 2048, &tmap, &ctl->full[stage], 128 * hh, 0, g, page);
+        } else {
+          const uint8_t* src = a.kv_cache + static_cast<int64_t>(page) * a.page_stride_bytes +
+                               static_cast<int64_t>(g) * (2 * kNvfp4Slot);
+          bulk_load(dst, src, kStage, &ctl->full[stage]);
+        }
+        issued = p + 1;
+      }
+      // every copy this CTA issued must land before its shared memory goes away
+      for (int p = max(0, issued - kStages); p < issued; ++p) {
+        if (!mbar_wait_bounded(&ctl->full[p % kStages], (p / kStages) & 1)) {
+          set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int hh = lane >> 2, c = lane & 3;
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const float sl2 = a.scale_log2;
+
+    for (int p = warp; p < npages; p += kConsumerWarps) {
+      const int stage = p % kStages;
+      if (!mbar_wait_bounded(&ctl->full[stage], (p / kStages) & 1)) {
+        set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+        atomicExch(&ctl->abort, 1);
+        break;
+      }
+      const uint32_t st = smem_u32(stages + stage * kStage);
+      const int nv = min(kPageRows, key1 - (key0 + p * kPageRows));
+      if (nv < kPageRows) zero_v_tail<FMT>(st, nv, lane);
+
+      // ---- S^T = K Q^T (16 keys x 8 heads)
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      if (FMT == PBS_KV_BF16) {
+        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int hi = lane >> 4;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int chunk = 2 * (j & 3) + hi;
+          uint32_t af[4];
+          ldsm_x4(st + (j >> 2) * 2048 + key * 128 + ((chunk ^ (key & 7)) << 4), af);
+          mma_bf16(s, af, qf[j][0], qf[j][1]);
+        }
+      } else if (FMT == PBS_KV_FP8_E4M3) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w0 = lds32(st + hh * 128 + ((j ^ hh) << 4) + 4 * c);
+          const uint32_t w1 = lds32(st + (hh + 8) * 128 + ((j ^ hh) << 4) + 4 * c);
+          uint32_t af[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
+                            e4m3x2_to_f16x2(w1 >> 16)};
+          mma_f16(s, af, qf[j][0], qf[j][1]);
+        }
+      } else {
+        const uint4 k0 = lds128(st + hh * 64 + 16 * c);
+        const uint4 k1 = lds128(st + (hh + 8) * 64 + 16 * c);
+        const uint32_t sc0 = e4m3x2_to_f16x2(lds16(st + 1024 + hh * 8 + 2 * c));
+        const uint32_t sc1 = e4m3x2_to_f16x2(lds16(st + 1024 + (hh + 8) * 8 + 2 * c));
+        const uint32_t s0lo = prmt(sc0, sc0, 0x1010), s0hi = prmt(sc0, sc0, 0x3232);
+        const uint32_t s1lo = prmt(sc1, sc1, 0x1010), s1hi = prmt(sc1, sc1, 0x3232);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w0 = word_of(k0, j >> 1) >> (16 * (j & 1));
+          const uint32_t w1 = word_of(k1, j >> 1) >> (16 * (j & 1));
+          const uint32_t sa = j < 4 ? s0lo : s0hi, sb = j < 4 ? s1lo : s1hi;
+          uint32_t af[4] = {hmul2(e2m1x2_to_f16x2(w0), sa), hmul2(e2m1x2_to_f16x2(w1), sb),
+                            hmul2(e2m1x2_to_f16x2(w0 >> 8), sa), hmul2(e2m1x2_to_f16x2(w1 >> 8), sb)};
+          mma_f16(s, af, qf[j][0], qf[j][1]);
+        }
+      }
+
+      // ---- online softmax (log2 domain); lane holds keys hh, hh+8 of heads 2c, 2c+1
+      const bool ok_lo = hh < nv, ok_hi = hh + 8 < nv;
+      const float t0 = ok_lo ? s[0] * sl2 : -INFINITY, t1 = ok_lo ? s[1] * sl2 : -INFINITY;
+      const float t2 = ok_hi ? s[2] * sl2 : -INFINITY, t3 = ok_hi ? s[3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+      const float p0 = ex2(t0 - mu0), p1 = ex2(t1 - mu1), p2 = ex2(t2 - mu0), p3 = ex2(t3 - mu1);
+      l0 = l0 * al0 + p0 + p2;
+      l1 = l1 * al1 + p1 + p3;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al1;
+        o[i][2] *= al0;
+        o[i][3] *= al1;
+      }
+
+      // ---- O^T += V^T P^T
+      if (FMT == PBS_KV_BF16) {
+        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+        const uint32_t l01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+        const uint32_t l23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        const int mi = lane >> 3;
+        const int key = (lane & 7) + 8 * (mi >> 1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int chunk = 2 * (i & 3) + (mi & 1);
+          uint32_t vf[4];
+          ldsm_x4_trans(st + (2 + (i >> 2)) * 2048 + key * 128 + ((chunk ^ (key & 7)) << 4), vf);
+          mma_bf16(o[i], vf, bh0, bh1);
+          mma_bf16(o[i], vf, bl0, bl1);
+        }
+      } else {
+        const uint32_t b0 = movmatrix_trans(pack_f16(p0, p1)), b1 = movmatrix_trans(pack_f16(p2, p3));
+        if (FMT == PBS_KV_FP8_E4M3) {
+          const uint32_t vb = st + 2048;
+          const uint4 va = lds128(vb + (2 * c) * 128 + ((hh ^ ((2 * c) & 7)) << 4));
+          const uint4 vbb = lds128(vb + (2 * c + 1) * 128 + ((hh ^ ((2 * c + 1) & 7)) << 4));
+          const uint4 vc = lds128(vb + (2 * c + 8) * 128 + ((hh ^ ((2 * c + 8) & 7)) << 4));
+          const uint4 vd = lds128(vb + (2 * c + 9) * 128 + ((hh ^ ((2 * c + 9) & 7)) << 4));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+            const uint32_t x = prmt(word_of(va, i >> 1), word_of(vbb, i >> 1), sel);
+            const uint32_t y = prmt(word_of(vc, i >> 1), word_of(vd, i >> 1), sel);
+            uint32_t af[4] = {e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y),
+                              e4m3x2_to_f16x2(y >> 16)};
+            mma_f16(o[i], af, b0, b1);
+          }
+        } else {
+          const uint32_t vc0 = st + kNvfp4Slot, vs0 = st + kNvfp4Slot + 1024;
+          const uint2 wa = lds64(vc0 + (2 * c) * 64 + 8 * hh);
+          const uint2 wb = lds64(vc0 + (2 * c + 1) * 64 + 8 * hh);
+          const uint2 wc = lds64(vc0 + (2 * c + 8) * 64 + 8 * hh);
+          const uint2 wd = lds64(vc0 + (2 * c + 9) * 64 + 8 * hh);
+          const uint32_t sab = e4m3x2_to_f16x2(lds8(vs0 + (2 * c) * 8 + hh) | (lds8(vs0 + (2 * c + 1) * 8 + hh) << 8));
+          const uint32_t scd = e4m3x2_to_f16x2(lds8(vs0 + (2 * c + 8) * 8 + hh) | (lds8(vs0 + (2 * c + 9) * 8 + hh) << 8));
+#pragma unroll
+          for (int wh = 0; wh < 2; ++wh) {
+            const uint32_t A = wh ? wa.y : wa.x, B = wh ? wb.y : wb.x;
+            const uint32_t C = wh ? wc.y : wc.x, D = wh ? wd.y : wd.x;
+            const uint32_t lo_ab = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
+            const uint32_t hi_ab = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
+            const uint32_t lo_cd = (C & 0x0F0F0F0Fu) | ((D & 0x0F0F0F0Fu) << 4);
+            const uint32_t hi_cd = ((C >> 4) & 0x0F0F0F0Fu) | (D & 0xF0F0F0F0u);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const int i = 4 * wh + b;
+              uint32_t af[4] = {hmul2(e2m1x2_to_f16x2(lo_ab >> (8 * b)), sab),
+                                hmul2(e2m1x2_to_f16x2(hi_ab >> (8 * b)), sab),
+                                hmul2(e2m1x2_to_f16x2(lo_cd >> (8 * b)), scd),
+                                hmul2(e2m1x2_to_f16x2(hi_cd >> (8 * b)), scd)};
+              mma_f16(o[i], af, b0, b1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->empty[stage]);
+    }
+
+    // ---- this warp's partial -> shared memory
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float(*ow)[kHeadDim] = mg->o[warp];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int d0, d1;
+      if (FMT == PBS_KV_BF16) {
+        d0 = 16 * i + hh;
+        d1 = d0 + 8;
+      } else {
+        d0 = 16 * hh + 2 * i;
+        d1 = d0 + 1;
+      }
+      ow[2 * c][d0] = o[i][0];
+      ow[2 * c + 1][d0] = o[i][1];
+      ow[2 * c][d1] = o[i][2];
+      ow[2 * c + 1][d1] = o[i][3];
+    }
+    if (hh == 0) {
+      mg->m[warp][2 * c] = m0;
+      mg->m[warp][2 * c + 1] = m1;
+      mg->l[warp][2 * c] = l0;
+      mg->l[warp][2 * c + 1] = l1;
+    }
+  }
+  __syncthreads();
+
+  // ---- merge the 4 warps (and write the output when the row has a single split)
+  const int E = G * kHeadDim;
+  uint16_t* out_row = a.out + static_cast<int64_t>(row) * a.out_row_stride;
+  if (threadIdx.x < kConsumerWarps * 32) {
+    for (int e = threadIdx.x; e < E; e += kConsumerWarps * 32) {
+      const int h = e >> 7, d = e & (kHeadDim - 1);
+      float M = mg->m[0][h];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, mg->m[w][h]);
+      float O = 0.f, L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = ex2(mg->m[w][h] - M);
+          O += f * mg->o[w][h][d];
+          L += f * mg->l[w][h];
+        }
+      }
+      if (S == 1) {
+        const float r = L > 0.f ? a.v_scale * O / L : 0.f;
+        out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(r);
+      } else {
+        mg->o[0][h][d] = O;
+        if (d == 0) {
+          mg->cta_m[h] = M;
+          mg->cta_l[h] = L;
+        }
+      }
+    }
+  }
+  if (S > 1) {
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int e0 = (E * rank) / S, e1 = (E * (rank + 1)) / S;
+    for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
+      const int h = e >> 7, d = e & (kHeadDim - 1);
+      float M = -INFINITY;
+      for (int r = 0; r < S; ++r) M = fmaxf(M, cluster.map_shared_rank(mg, r)->cta_m[h]);
+      float O = 0.f, L = 0.f;
+      if (M != -INFINITY) {
+        for (int r = 0; r < S; ++r) {
+          const Merge* rm = cluster.map_shared_rank(mg, r);
+          const float f = ex2(rm->cta_m[h] - M);
+          O += f * rm->o[0][h][d];
+          L += f * rm->cta_l[h];
+        }
+      }
+      const float res = L > 0.f ? a.v_scale * O / L : 0.f;
+      out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
+    }
+    cluster.sync();  // peers may still be reading this CTA's partial
+  }
+}
+
+template <int FMT, bool PREFILL>
+cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& tmap, cudaStream_t stream) {
+  constexpr size_t smem = smem_bytes<FMT>();
+  auto kern = attend_kernel<FMT, PREFILL>;
+  // dynamic shared memory above 48 KB must be opted into (per device; cheap to repeat)
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.num_rows) * static_cast<unsigned>(a.splits),
+                     static_cast<unsigned>(a.num_kv_heads), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, a);
+}
+
+}  // namespace
+
+cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream) {
+  switch (a.kv_dtype) {
+    case PBS_KV_BF16:
+      return prefill ? launch_one<PBS_KV_BF16, true>(a, tmap, stream) : launch_one<PBS_KV_BF16, false>(a, tmap, stream);
+    case PBS_KV_FP8_E4M3:
+      return prefill ? launch_one<PBS_KV_FP8_E4M3, true>(a, tmap, stream)
+                     : launch_one<PBS_KV_FP8_E4M3, false>(a, tmap, stream);
+    case PBS_KV_NVFP4:
+      return prefill ? launch_one<PBS_KV_NVFP4, true>(a, tmap, stream) : launch_one<PBS_KV_NVFP4, false>(a, tmap, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pbs

@@ -1,0 +1,85 @@
+// Host-side argument blocks and kernel launchers of libpbs (internal; not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pbs {
+
+struct TableArgs {
+  const int32_t* topk;
+  int64_t topk_row_stride;
+  int32_t num_rows;
+  int32_t k;
+  const int32_t* page_table;
+  int64_t pt_row_stride;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t decode_query_len;   // decode
+  const int32_t* cu_seqlens_q;  // prefill
+  int32_t num_reqs;             // prefill
+  int32_t block_page_stride;
+  int32_t* sparse_bt;
+  int64_t sbt_row_stride;
+  int32_t* sparse_ctx;
+  int32_t* err_word;
+};
+
+cudaError_t launch_build_table(const TableArgs& a, bool prefill, cudaStream_t stream);
+
+// Token-centric sparse attend (one query row per cluster of split CTAs, one kv head per cluster).
+struct AttendArgs {
+  const uint16_t* q;          // bf16 bits
+  int64_t q_row_stride;
+  int64_t q_head_stride;
+  const uint8_t* kv_cache;
+  int64_t page_stride_bytes;
+  int64_t num_pages;
+  int32_t kv_dtype;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t group;              // num_heads / num_kv_heads
+  const int32_t* topk;
+  int64_t topk_row_stride;
+  int32_t k;
+  const int32_t* page_table;
+  int64_t pt_row_stride;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t decode_query_len;   // decode mode
+  const int32_t* cu_seqlens_q;  // prefill mode
+  int32_t num_reqs;
+  int32_t num_rows;
+  int32_t block_page_stride;
+  float scale_log2;           // softmax_scale * k_scale * log2(e)
+  float v_scale;
+  uint16_t* out;              // bf16 bits
+  int64_t out_row_stride;
+  int64_t out_head_stride;
+  int32_t* err_word;
+  int32_t splits;             // CTAs per (row, kv head) = cluster size
+};
+
+// Launch the attend; `tmap` is a 4-D tensor map over the cache rows for the bf16/fp8 formats
+// (unused for NVFP4). Returns the launch status.
+cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream);
+
+// Index-cache insert.
+struct InsertArgs {
+  const uint8_t* index_k;
+  int64_t k_stride0, k_stride1;  // elements
+  int32_t num_tokens, dim;
+  uint8_t* index_cache;
+  int64_t c_stride0, c_stride1;  // elements
+  int32_t num_blocks, block_tokens;
+  const int64_t* slot_mapping;
+  int64_t slot_stride;
+  int32_t elem_bytes;
+  int32_t* err_word;
+};
+
+cudaError_t launch_insert_index_cache(const InsertArgs& a, cudaStream_t stream);
+
+}  // namespace pbs

@@ -1,0 +1,133 @@
+"""The C ABI library: it loads, exports every function include/pbs.h declares, and its host-side
+checks reject bad arguments before anything is launched (no GPU needed: every call below fails a
+check that runs before the first CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pbs.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_block_sparse_gb300 import _build
+    _build.build()
+    import paged_block_sparse_gb300 as pbs
+    return pbs.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"PBS_API\s+[\w\s\*]+?\b(pbs_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("pbs_build_sparse_block_table_decode", "pbs_build_sparse_block_table_prefill",
+                 "pbs_sparse_decode_attention", "pbs_sparse_prefill_attention", "pbs_insert_index_cache",
+                 "pbs_status_string", "pbs_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libpbs.so does not export {name}"
+
+
+def test_status_strings(L):
+    import paged_block_sparse_gb300 as pbs
+    assert pbs.abi_version() == 1
+    texts = {pbs.status_string(s) for s in range(6)}
+    assert len(texts) == 6 and "ok" in texts
+    assert pbs.status_string(99) == "unknown status"
+
+
+# Fake device addresses: never dereferenced, because each call below fails a host check first.
+A = ctypes.c_void_p(0x10000)
+N = ctypes.c_void_p(0)
+S = ctypes.c_void_p(0)
+
+
+def _decode_table(L, **kw):
+    args = dict(topk=A, trs=4, rows=2, k=4, pt=A, pts=8, mb=8, sl=A, batch=2, dql=1, bps=8, sbt=A, sbts=32,
+                ctx=A)
+    args.update(kw)
+    return L.pbs_build_sparse_block_table_decode(args["topk"], args["trs"], args["rows"], args["k"], args["pt"],
+                                                 args["pts"], args["mb"], args["sl"], args["batch"], args["dql"],
+                                                 args["bps"], args["sbt"], args["sbts"], args["ctx"], N, S)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
+def test_table_host_checks(L):
+    assert _decode_table(L, rows=3) == 2                  # rows != batch * dql (the page's assert)
+    assert _decode_table(L, topk=N) == 1
+    assert _decode_table(L, k=65, trs=65) == 3            # top-k wider than 64
+    assert _decode_table(L, k=0) == 1
+    assert _decode_table(L, trs=3) == 2                   # row stride < k
+    assert _decode_table(L, sbts=31) == 2                 # table row narrower than k*8
+    assert _decode_table(L, bps=4) == 2                   # a block spans at least 8 pages
+    assert _decode_table(L, rows=0, batch=0) == 0         # empty: nothing launched
+    assert _decode_table(L, dql=0) == 1
+    st = L.pbs_build_sparse_block_table_prefill(A, 4, 5, 4, A, 8, 8, A, A, 0, 8, A, 32, A, N, S)
+    assert st == 2                                        # tokens but no request
+
+
+def _decode_attend(L, **kw):
+    a = dict(q=A, qrs=1024, qhs=128, kv=A, psb=65536, npages=100, dt=0, hq=64, hkv=8, hd=128, topk=A, trs=16,
+             k=16, pt=A, pts=64, mb=64, sl=A, batch=4, dql=1, bps=8, sc=0.088, ks=1.0, vs=1.0, out=A, ors=8192,
+             ohs=128)
+    a.update(kw)
+    return L.pbs_sparse_decode_attention(a["q"], a["qrs"], a["qhs"], a["kv"], a["psb"], a["npages"], a["dt"],
+                                         a["hq"], a["hkv"], a["hd"], a["topk"], a["trs"], a["k"], a["pt"], a["pts"],
+                                         a["mb"], a["sl"], a["batch"], a["dql"], a["bps"], a["sc"], a["ks"], a["vs"],
+                                         a["out"], a["ors"], a["ohs"], N, S)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
+def test_attend_host_checks(L):
+    assert _decode_attend(L, hd=64) == 3                  # head_dim must be 128
+    assert _decode_attend(L, hq=48, hkv=8) == 3           # G = 6 unsupported
+    assert _decode_attend(L, hq=60, hkv=8) == 2           # heads not a multiple of kv heads
+    assert _decode_attend(L, dt=7) == 1
+    assert _decode_attend(L, q=N) == 1
+    assert _decode_attend(L, kv=ctypes.c_void_p(0x10008)) == 4   # cache not 16-byte aligned
+    assert _decode_attend(L, psb=65536 + 8) == 4                # page stride not a multiple of 16
+    assert _decode_attend(L, psb=4096) == 2                     # page stride below one page
+    assert _decode_attend(L, qhs=127) == 4
+    assert _decode_attend(L, sc=float("nan")) == 1
+    assert _decode_attend(L, batch=0) == 0
+    assert _decode_attend(L, npages=0) == 2
+    assert _decode_attend(L, k=80, trs=80) == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
+def test_insert_host_checks(L):
+    f = L.pbs_insert_index_cache
+    assert f(A, 128, 1, 0, 128, A, 2048, 128, 4, 16, A, 1, 2, N, S) == 0   # empty: early return
+    assert f(N, 128, 1, 4, 128, A, 2048, 128, 4, 16, A, 1, 2, N, S) == 1
+    assert f(A, 128, 1, 4, 128, A, 2048, 128, 4, 16, A, 1, 3, N, S) == 1   # bad element size
+    assert f(A, 128, 1, 4, 128, ctypes.c_void_p(0x10001), 2048, 128, 4, 16, A, 1, 2, N, S) == 4
+
+
+def test_binding_refuses_host_tensors():
+    import paged_block_sparse_gb300 as pbs
+    with pytest.raises(ValueError):
+        pbs.build_sparse_block_table_decode(torch.zeros(1, 2, 4, dtype=torch.int32),
+                                            torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32))
+
+
+def test_binding_insert_shape_checks():
+    """[sparse_pa] minimax_m3_insert_index_cache raises ValueError on rank/dim/length/stride."""
+    import paged_block_sparse_gb300 as pbs
+    k = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        pbs.insert_index_cache(k, torch.zeros(2, 4, 7), torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        pbs.insert_index_cache(k, torch.zeros(2, 4, 8), torch.zeros(3, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        pbs.insert_index_cache(k, torch.zeros(2, 8, 4).transpose(1, 2), torch.zeros(4, dtype=torch.int64))
+    pbs.insert_index_cache(torch.zeros(0, 8), torch.zeros(2, 4, 8), torch.zeros(0, dtype=torch.int64))

@@ -1,0 +1,275 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tables and context lengths must match bit for bit; attention outputs within max-abs 1e-2 /
+relative-RMS 2e-3 (bf16 KV) or 5e-2 / 1e-2 (fp8 / NVFP4 KV, against the oracle on the same
+dequantised values)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import TOL, assert_close, np_i32, oracle_decode, oracle_prefill
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pbs():
+    from paged_block_sparse_gb300 import _build
+    _build.build()
+    import paged_block_sparse_gb300 as m
+    return m
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def gpu_tables(pbs, b, part):
+    err = _err()
+    if part == "dec":
+        d = b.dec
+        sbt, ctx = pbs.build_sparse_block_table_decode(d.topk, d.page_table, d.seq_lens, d.decode_query_len,
+                                                       b.block_page_stride, err_word=err)
+    else:
+        p = b.pre
+        sbt, ctx = pbs.build_sparse_block_table_prefill(p.topk, p.page_table, p.cu_seqlens_q, p.seq_lens,
+                                                        b.block_page_stride, err_word=err)
+    torch.cuda.synchronize()
+    return np_i32(sbt), np_i32(ctx), int(err.item())
+
+
+def oracle_tables(b, part):
+    if part == "dec":
+        d = b.dec
+        return oracle.build_sparse_block_table_decode(np_i32(d.topk), np_i32(d.page_table), np_i32(d.seq_lens),
+                                                      d.decode_query_len, b.block_page_stride)
+    p = b.pre
+    return oracle.build_sparse_block_table_prefill(np_i32(p.topk), np_i32(p.page_table), np_i32(p.cu_seqlens_q),
+                                                   np_i32(p.seq_lens), b.block_page_stride)
+
+
+def gpu_attend(pbs, b, part, err=None):
+    if part == "dec":
+        d = b.dec
+        out = pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table,
+                                          d.seq_lens, d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale,
+                                          b.block_page_stride, err_word=err)
+    else:
+        p = b.pre
+        out = pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
+                                           p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
+                                           b.block_page_stride, err_word=err)
+    torch.cuda.synchronize()
+    return out.to(torch.float64).cpu().numpy()
+
+
+# ------------------------------------------------------------------------------------------
+# sparse block tables: bit-exact
+# ------------------------------------------------------------------------------------------
+
+def test_tables_tiny(pbs):
+    b = workloads.tiny(device=DEV)
+    for part in ("dec", "pre"):
+        sbt, ctx, err = gpu_tables(pbs, b, part)
+        o_sbt, o_ctx = oracle_tables(b, part)
+        assert err == 0
+        assert np.array_equal(sbt, o_sbt) and np.array_equal(ctx, o_ctx)
+
+
+@pytest.mark.parametrize("case", [
+    dict(dec_seq_lens=[0, 1, 127, 128, 129, 5000], topk=1),
+    dict(dec_seq_lens=[300, 4000, 9000], decode_query_len=3, topk=7),
+    dict(dec_seq_lens=[20000, 1500], topk=33),
+    dict(dec_seq_lens=[70000, 30, 2000], topk=64),
+    dict(pre_q_lens=[700, 0, 300, 1], pre_ctx_lens=[0, 5, 200, 4095], topk=16, future_prob=0.3),
+])
+def test_tables_small_variants(pbs, case):
+    b = workloads.small(device=DEV, seed=21, **case)
+    for part in ("dec", "pre"):
+        if (part == "dec" and b.dec is None) or (part == "pre" and b.pre is None):
+            continue
+        sbt, ctx, err = gpu_tables(pbs, b, part)
+        o_sbt, o_ctx = oracle_tables(b, part)
+        assert err == 0
+        assert np.array_equal(sbt, o_sbt), "sparse block table differs"
+        assert np.array_equal(ctx, o_ctx), "context lengths differ"
+
+
+def test_tables_duplicates_strides_and_side_packed(pbs):
+    """Duplicate ids follow the row writer literally; a strided top-k view and block stride 16."""
+    rng = np.random.default_rng(5)
+    rows, k = 300, 12
+    seq = rng.integers(1, 6000, size=rows).astype(np.int32)
+    pos = seq - 1
+    own = pos // 128
+    topk = np.full((rows, k + 5), -7, np.int32)             # wider buffer: row stride k+5
+    for r in range(rows):
+        ids = rng.integers(-1, own[r] + 3, size=k)
+        if r % 3 == 0:
+            ids[1] = ids[0]                                  # duplicate
+        if r % 5 == 0:
+            ids[2] = own[r]
+            ids[3] = own[r]                                  # duplicate own block
+        topk[r, :k] = ids
+    pt = rng.permutation(rows * 50).astype(np.int32).reshape(rows, 50)[:, :48]
+    t_topk = torch.from_numpy(topk).to(DEV)[:, :k]
+    t_pt = torch.from_numpy(np.ascontiguousarray(pt)).to(DEV)
+    for bps in (8, 16):
+        err = _err()
+        sbt, ctx = pbs.build_sparse_block_table_decode(t_topk, t_pt, torch.from_numpy(seq).to(DEV), 1, bps,
+                                                       err_word=err)
+        o_sbt, o_ctx = oracle.build_sparse_block_table_decode(topk[:, :k], pt, seq, 1, bps)
+        assert int(err.item()) == 0
+        assert np.array_equal(np_i32(sbt), o_sbt) and np.array_equal(np_i32(ctx), o_ctx)
+
+
+def test_table_block_past_page_table_sets_error(pbs):
+    topk = torch.tensor([[[0, 3, -1]]], dtype=torch.int32, device=DEV)   # block 3 is causal but past the table
+    pt = torch.tensor([[5, 6]], dtype=torch.int32, device=DEV)
+    err = _err()
+    sbt, ctx = pbs.build_sparse_block_table_decode(topk, pt, torch.tensor([500], dtype=torch.int32, device=DEV),
+                                                   err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pbs.DEVERR["block_oob"]
+    assert int(ctx.item()) == 0 and int(sbt.abs().sum().item()) == 0
+
+
+# ------------------------------------------------------------------------------------------
+# attention
+# ------------------------------------------------------------------------------------------
+
+def test_attend_tiny_bf16(pbs):
+    b = workloads.tiny(device=DEV)
+    got = gpu_attend(pbs, b, "dec")
+    want = oracle_decode(b)
+    assert_close({0: got[0]}, want, "bf16", "tiny decode")
+    got = gpu_attend(pbs, b, "pre")
+    want = oracle_prefill(b)
+    assert_close(dict(enumerate(got)), want, "bf16", "tiny prefill")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+@pytest.mark.parametrize("heads", [(64, 8), (16, 4), (8, 4), (4, 4)])
+def test_attend_small_decode(pbs, kv_dtype, heads):
+    hq, hkv = heads
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=hq, num_kv_heads=hkv, topk=9,
+                        dec_seq_lens=[1, 129, 2000, 5000, 1170], decode_query_len=2, seed=31)
+    got = gpu_attend(pbs, b, "dec")
+    want = oracle_decode(b)
+    assert_close(dict(enumerate(got)), want, kv_dtype, f"decode {kv_dtype} {heads}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+def test_attend_small_prefill(pbs, kv_dtype):
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8, topk=8,
+                        pre_q_lens=[300, 1, 260], pre_ctx_lens=[0, 700, 1000], future_prob=0.3, seed=32)
+    got = gpu_attend(pbs, b, "pre")
+    want = oracle_prefill(b)
+    assert_close(dict(enumerate(got)), want, kv_dtype, f"prefill {kv_dtype}")
+
+
+@pytest.mark.parametrize("splits", ["1", "2", "4", "8"])
+def test_attend_split_counts_agree(pbs, splits, monkeypatch):
+    """Every cluster size gives the oracle's answer (the DSMEM merge of the split partials)."""
+    monkeypatch.setenv("PBS_ATTEND_SPLITS", splits)
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, dec_seq_lens=[3000, 9000, 700],
+                        seed=33)
+    got = gpu_attend(pbs, b, "dec")
+    assert_close(dict(enumerate(got)), oracle_decode(b), "bf16", f"splits={splits}")
+
+
+def test_attend_empty_rows_are_zero(pbs):
+    b = workloads.small(device=DEV, num_heads=8, num_kv_heads=1, topk=4, dec_seq_lens=[0, 300, 0], seed=34)
+    got = gpu_attend(pbs, b, "dec")
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    assert_close({1: got[1]}, oracle_decode(b, rows=[1]), "bf16", "row 1")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+def test_attend_ignores_nan_past_the_context(pbs, kv_dtype):
+    """Cache rows past a query's position (unwritten in a live cache) may hold NaN; they are masked."""
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=8, num_kv_heads=2, topk=4,
+                        dec_seq_lens=[200, 1000, 77], seed=35)
+    d = b.dec
+    pt = np_i32(d.page_table)
+    for r, L in enumerate(np_i32(d.seq_lens)):
+        for x in range(L, ((L + 127) // 128) * 128):
+            page = int(pt[r, x // 128]) * 8 + (x % 128) // 16
+            row = x % 16
+            if kv_dtype == "nvfp4":
+                pg = b.cache[page].view(2 * b.num_kv_heads, 1152)
+                pg[:, row * 64:(row + 1) * 64] = 0xFF                # e2m1 -6 codes
+                pg[:, 1024 + row * 8:1024 + (row + 1) * 8] = 0x7F    # e4m3 NaN scales
+            else:
+                view = b.cache[page].view(b.num_kv_heads, 16, -1)
+                view[:, row, :] = 0xFF                               # NaN in bf16 and e4m3
+    got = gpu_attend(pbs, b, "dec")
+    assert_close(dict(enumerate(got)), oracle_decode(b), kv_dtype, "NaN past context")
+
+
+def test_attend_page_past_cache_sets_error(pbs):
+    b = workloads.small(device=DEV, num_heads=8, num_kv_heads=1, topk=4, dec_seq_lens=[300, 300], seed=36)
+    d = b.dec
+    pt = d.page_table.clone()
+    pt[0, 0] = b.num_pages // 8 + 10                                # block beyond the cache
+    err = _err()
+    out = pbs.sparse_decode_attention(d.q, b.cache, "bf16", 1, d.topk, pt, d.seq_lens, 1, b.softmax_scale,
+                                      err_word=err)
+    torch.cuda.synchronize()
+    tk = np_i32(d.topk)[0, 0]
+    if 0 in tk:
+        assert int(err.item()) & 2
+        assert float(out[0].abs().sum()) == 0.0
+    assert_close({1: out[1].double().cpu().numpy()}, oracle_decode(b, rows=[1]), "bf16", "row 1")
+
+
+def test_strided_q_and_out(pbs):
+    b = workloads.small(device=DEV, num_heads=16, num_kv_heads=2, topk=5, dec_seq_lens=[900, 1300], seed=37)
+    d = b.dec
+    big = torch.zeros(d.q.shape[0], 20, 128 + 64, dtype=torch.bfloat16, device=DEV)
+    big[:, 2:18, 32:160] = d.q
+    qv = big[:, 2:18, 32:160]
+    outbig = torch.full((d.q.shape[0], 24, 256), 7.0, dtype=torch.bfloat16, device=DEV)
+    ov = outbig[:, 4:20, 64:192]
+    pbs.sparse_decode_attention(qv, b.cache, "bf16", 2, d.topk, d.page_table, d.seq_lens, 1, b.softmax_scale,
+                                out=ov)
+    torch.cuda.synchronize()
+    assert_close(dict(enumerate(ov.double().cpu().numpy())), oracle_decode(b), "bf16", "strided")
+    assert float(outbig[:, :4].double().sub(7).abs().sum()) == 0.0       # nothing written outside the view
+
+
+# ------------------------------------------------------------------------------------------
+# index-cache insert
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_insert_index_cache(pbs, dtype):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    N, B, T, D = 4096, 300, 16, 128
+    k = torch.randn(N, D, generator=g, device=DEV).to(dtype)
+    cache = torch.randn(B, T, D, generator=g, device=DEV).to(dtype)
+    slots = torch.randperm(B * T, generator=g, device=DEV)[:N].to(torch.int64)
+    slots[::97] = -1
+    want = oracle.insert_index_cache(k.float().cpu().numpy(), cache.float().cpu().numpy(), slots.cpu().numpy())
+    err = _err()
+    pbs.insert_index_cache(k, cache, slots, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(cache.float().cpu().numpy(), want)
+
+
+def test_insert_index_cache_slot_past_cache(pbs):
+    k = torch.ones(2, 128, dtype=torch.bfloat16, device=DEV)
+    cache = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device=DEV)
+    err = _err()
+    pbs.insert_index_cache(k, cache, torch.tensor([1, 8], dtype=torch.int64, device=DEV), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 4
+    assert float(cache[0, 1].sum()) == 128.0 and float(cache.sum()) == 128.0
