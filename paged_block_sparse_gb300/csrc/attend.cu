@@ -37,7 +37,12 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 6;
+// Page p goes to stage p % kStages and to consumer warp p % kConsumerWarps. With kStages a
+// multiple of kConsumerWarps every stage is always consumed by the same warp, one phase after
+// the other, so a parity wait can never be answered by a phase two steps behind (with 6 stages
+// and 4 warps a warp would skip every other phase of a stage and could pass its wait early).
+constexpr int kStages = 8;
+static_assert(kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
 constexpr int kTileHeads = 8;  // the n8 tile of the MMA: up to 8 query heads per kv head
 
 template <int FMT>
@@ -144,7 +149,7 @@ __device__ __forceinline__ void zero_v_tail(uint32_t st, int nv, int lane) {
 }
 
 template <int FMT, bool PREFILL>
-__global__ void __launch_bounds__(kThreads, 3) attend_kernel(const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_constant__ CUtensorMap tmap,
                                                              const AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
   constexpr int kStage = StageBytes<FMT>::v;
@@ -247,6 +252,23 @@ __global__ void __launch_bounds__(kThreads, 3) attend_kernel(const __grid_consta
         const int kp = (key0 >> 4) + p;
         const int page = ctl->slot_base[kp >> 3] + (kp & 7);
         uint8_t* dst = stages + stage * kStage;
+#ifdef PBS_CHECKED
+        // checked build: every copy's source and destination are validated before issue
+        {
+          int bad = 0;
+          if ((kp >> 3) >= kMaxTopk || kp < 0) bad |= 1 << 16;
+          if (page < 0 || page >= a.num_pages) bad |= 1 << 17;
+          if (g < 0 || g >= a.num_kv_heads) bad |= 1 << 18;
+          if ((smem_u32(dst) & 1023u) != 0 || dst + kStage > reinterpret_cast<uint8_t*>(mg)) bad |= 1 << 19;
+          if ((reinterpret_cast<uintptr_t>(&tmap) & 63u) != 0) bad |= 1 << 20;
+          if (bad) {
+            set_err(a.err_word, bad);
+            mbar_arrive(&ctl->full[stage]);  // complete the phase without data
+            issued = p + 1;
+            continue;
+          }
+        }
+#endif
         mbar_arrive_expect_tx(&ctl->full[stage], kStage);
         if (FMT == PBS_KV_BF16) {
 #pragma unroll
