@@ -69,8 +69,13 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
-// CTAs per (row, kv head): enough clusters to fill the GPU a few times over, but at least two
-// 128-key slots per CTA. PBS_ATTEND_SPLITS in {1, 2, 4, 8} overrides (tuning and tests).
+// CTAs per (row, kv head). Splitting a row across a cluster costs a cluster barrier, a DSMEM
+// merge and one more CTA start-up (a chain of dependent loads: top-k, page table, first page)
+// per split; measured on the 64-request decode workload (512 row x head units, 2 CTAs per SM)
+// one CTA per unit streams at 75% of HBM peak against 61% / 57% / 43% for 2 / 4 / 8 splits.
+// So rows are split only while the units alone cannot fill every SM twice, and only while
+// each split keeps at least four 128-key slots. PBS_ATTEND_SPLITS in {1, 2, 4, 8} overrides
+// (tuning and tests).
 int choose_splits(int64_t units, int k) {
   if (const char* env = std::getenv("PBS_ATTEND_SPLITS")) {
     const int s = std::atoi(env);
@@ -78,9 +83,9 @@ int choose_splits(int64_t units, int k) {
   }
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t target = static_cast<int64_t>(sms) * 3 * 4;
+  const int64_t target = static_cast<int64_t>(sms) * 2;
   int s = 1;
-  while (s < 8 && units * s < target && 4 * s <= k) s *= 2;
+  while (s < 8 && units * s < target && 4 * (2 * s) <= k) s *= 2;
   return s;
 }
 

@@ -344,10 +344,10 @@ def tiny(device="cpu", seed: int = 1000, kv_dtype: str = "bf16") -> Batch:
     return b
 
 
-def decode(device="cuda", seed: int = 1001) -> Batch:
+def decode(device="cuda", seed: int = 1001, batch: int = 64) -> Batch:
     gen = torch.Generator()
     gen.manual_seed(seed + 3)
-    sl = torch.randint(16384, 32768 + 1, (64,), generator=gen).tolist()
+    sl = torch.randint(16384, 32768 + 1, (batch,), generator=gen).tolist()
     return make_batch("decode_b64_16k-32k_top16_bf16", kv_dtype="bf16", num_heads=64, num_kv_heads=8,
                       head_dim=128, topk=16, dec_seq_lens=sl, seed=seed, device=device)
 
