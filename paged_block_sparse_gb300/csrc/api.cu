@@ -69,6 +69,32 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
+// Queries as a 3-D tensor {head_dim, heads, tokens}; a box is 16 tokens x 8 heads x 64 dims, laid
+// out in shared memory as the 128-row K-major operand of the prefill MMA (row = token * 8 + head).
+int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int total_q, int64_t q_row_stride,
+                 int64_t q_head_stride) {
+  std::memset(map, 0, sizeof(*map));
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PBS_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(num_heads),
+                              static_cast<cuuint64_t>(total_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(q_head_stride) * 2, static_cast<cuuint64_t>(q_row_stride) * 2};
+  const cuuint32_t box[3] = {64, 8, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
+}
+
+// Which prefill kernel runs: the tcgen05 tile kernel where it applies, the token-centric
+// kernel otherwise. PBS_PREFILL_KERNEL=token forces the token-centric one (tests, tuning).
+bool use_prefill_tc(const AttendArgs& a) {
+  if (const char* env = std::getenv("PBS_PREFILL_KERNEL"))
+    if (std::strcmp(env, "token") == 0) return false;
+  return pbs::prefill_tc_supported(a);
+}
+
 // CTAs per (row, kv head). Splitting a row across a cluster costs a cluster barrier, a DSMEM
 // merge and one more CTA start-up (a chain of dependent loads: top-k, page table, first page)
 // per split; measured on the 64-request decode workload (512 row x head units, 2 CTAs per SM)
@@ -306,8 +332,16 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   CUtensorMap map;
   st = encode_cache_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
   if (st != PBS_OK) return st;
-  return pbs::launch_attend(a, true, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
-                                                                                                 : PBS_ERR_CUDA;
+  cudaError_t e;
+  if (use_prefill_tc(a)) {
+    CUtensorMap qmap;
+    st = encode_q_map(&qmap, q, num_heads, total_q, q_row_stride, q_head_stride);
+    if (st != PBS_OK) return st;
+    e = pbs::launch_prefill_tc(a, map, qmap, reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    e = pbs::launch_attend(a, true, map, reinterpret_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? PBS_OK : PBS_ERR_CUDA;
 }
 
 int pbs_insert_index_cache(const void* index_k, int64_t k_stride0, int64_t k_stride1, int32_t num_tokens, int32_t dim,

@@ -1,0 +1,508 @@
+// Prefill attend on the 5th-generation tensor cores (tcgen05 + TMEM), bf16 KV cache, GQA 8.
+//
+// What it computes (vLLM page vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer, forward:
+// the varlen msa_sparse_attention call; row rule of vllm.models.minimax_m3.amd.ops.sparse_pa,
+// _write_sparse_block_table_row_from_values): for every prefill token and query head h of kv
+// head g, out = v_scale * softmax(softmax_scale * k_scale * q_h K^T) V over the keys of the
+// 128-token blocks the token's top-k selects (block b valid iff 0 <= b <= pos/128; the own
+// block truncated at pos).
+//
+// GB300 design
+// ------------
+// * A CTA owns a tile of 16 consecutive tokens of one request and one kv head: 16 x 8 query
+//   heads = 128 rows, one MMA M-tile. The tile's selected blocks are merged into a sorted union;
+//   every union block is streamed once and each row is masked by its own token's selection.
+// * Warp 0: TMA producer (Q tile once via a 3-D tensor map; K and V of each union block page by
+//   page through the cache tensor map, 128B swizzle, 2-stage ring). Warp 1: one thread issues
+//   the tcgen05 MMAs. Warps 4-7: softmax and epilogue, thread i owning TMEM lane / row i.
+// * TMEM (512 columns): S double buffer (2 x 128) and the O accumulator (128), fp32.
+// * S = Q K^T: A = Q (K-major), B = K tile (K-major). O += P V: A = P (K-major, written by the
+//   softmax warps), B = V tile (MN-major). P is split into bf16 hi + lo halves, two MMAs, so the
+//   result stays within 2e-3 relative RMS of the fp64 attend.
+// * Online softmax in base 2 with lazy rescaling: the O row is rescaled only when the running
+//   maximum grows by more than 2^8, so most blocks never touch O from the CUDA cores.
+// * Duplicate ids in a token's list count once (set semantics of the attend); the decode path and
+//   the table builders follow the row writer literally. With distinct ids the two agree.
+#include "pbs_device.cuh"
+#include "pbs_internal.h"
+#include "tc_device.cuh"
+
+namespace pbs {
+namespace {
+
+constexpr int kTok = 16;          // tokens per tile
+constexpr int kG = 8;             // query heads per kv head on this path
+constexpr int kRows = kTok * kG;  // 128 = MMA M
+constexpr int kThreadsTc = 256;
+constexpr int kQBytes = kRows * kHeadDim * 2;          // 32 KiB
+constexpr int kHalf = 128 * 128;                       // one 64-dim half of a 128 x 128 bf16 tile
+constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB
+constexpr int kKVBytes = 2 * kTileBytes;               // K then V
+constexpr int kPBytes = 2 * kTileBytes;                // P hi then P lo
+constexpr int kBigBytes = kQBytes + 2 * kKVBytes + kPBytes;  // 224 KiB
+constexpr int kMaxUnion = 256;
+constexpr int kTcMaxTopk = 16;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
+
+struct TcCtl {
+  uint64_t q_full;
+  uint64_t kv_full[2];
+  uint64_t kv_empty[2];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint32_t tmem_base;
+  int32_t n_union;
+  int32_t req, t0, n_tok;
+  int32_t bad_mask;   // tokens whose row hit an out-of-range block id
+  int32_t abort;
+  int32_t own[kTok];  // own block of each token (-1: none)
+  int32_t lim[kTok];  // keys of the own block the token sees
+  int32_t cnt[kTok];  // distinct valid blocks per token
+  uint16_t union_blk[kMaxUnion];
+  uint16_t tok_blk[kTok][kTcMaxTopk];
+};
+
+constexpr size_t kTcSmem = 232448;  // the per-block opt-in maximum of sm_100-family GPUs
+static_assert(sizeof(TcCtl) + 1023 + kBigBytes <= kTcSmem, "shared memory layout exceeds 227 KiB");
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Waits in this kernel last microseconds; give up after 100 ms.
+constexpr unsigned long long kTcWaitNs = 100000000ull;
+
+// Bounded wait that records a timeout and raises the CTA's abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, TcCtl* ctl, int32_t* err) {
+  if (mbar_wait_bounded(bar, parity, kTcWaitNs)) return true;
+  set_err(err, PBS_DEVERR_TIMEOUT);
+  atomicExch(&ctl->abort, 1);
+  return false;
+}
+
+// Same, for a whole warp that must stay converged (the softmax warps issue warp-collective
+// tcgen05.ld / st): every lane waits, and the warp agrees on the result.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, TcCtl* ctl, int32_t* err) {
+  const bool ok = wait_or_abort(bar, parity, ctl, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool aborted(TcCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                      const AttendArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  TcCtl* ctl = reinterpret_cast<TcCtl*>(smem_raw);
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t big_off = ((raw + sizeof(TcCtl) + 1023u) & ~1023u) - raw;
+  uint8_t* big = smem_raw + big_off;
+  uint8_t* q_s = big;
+  uint8_t* kv_s = big + kQBytes;  // stage st at kv_s + st * kKVBytes: K halves, then V halves
+  uint8_t* p_s = big + kQBytes + 2 * kKVBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.y;
+
+  // ---- tile -> (request, first token): tiles are numbered request by request ----------------
+  if (warp == 0) {
+    int r = -1, t0 = 0, n = 0;
+    int base_tiles = 0;
+    for (int r0 = 0; r0 < a.num_reqs && r < 0; r0 += 32) {
+      const int rr = r0 + lane;
+      int q_len = 0;
+      if (rr < a.num_reqs) q_len = __ldg(a.cu_seqlens_q + rr + 1) - __ldg(a.cu_seqlens_q + rr);
+      const int tiles = (q_len + kTok - 1) / kTok;
+      int incl = tiles;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const int excl = incl - tiles + base_tiles;
+      const bool mine = static_cast<int>(blockIdx.x) >= excl && static_cast<int>(blockIdx.x) < excl + tiles;
+      const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        r = r0 + src;
+        const int ex = __shfl_sync(0xffffffffu, excl, src);
+        const int ql = __shfl_sync(0xffffffffu, q_len, src);
+        const int tile = static_cast<int>(blockIdx.x) - ex;
+        t0 = __ldg(a.cu_seqlens_q + r) + tile * kTok;
+        n = min(kTok, ql - tile * kTok);
+      }
+      base_tiles += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      // once any CTA has given up on a wait, the rest of the grid does no work
+      const bool gave_up = a.err_word != nullptr &&
+                           (*reinterpret_cast<volatile int32_t*>(a.err_word) & PBS_DEVERR_TIMEOUT) != 0;
+      ctl->req = r;
+      ctl->t0 = t0;
+      ctl->n_tok = (r < 0 || gave_up) ? 0 : n;
+      ctl->bad_mask = 0;
+      ctl->abort = 0;
+      mbar_init(&ctl->q_full, 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&ctl->kv_full[i], 1);
+        mbar_init(&ctl->kv_empty[i], 1);
+        mbar_init(&ctl->s_full[i], 1);
+        mbar_init(&ctl->s_free[i], 4);
+      }
+      mbar_init(&ctl->p_full, 4);
+      mbar_init(&ctl->pv_done, 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  const int req = ctl->req, t0 = ctl->t0, n_tok = ctl->n_tok;
+  if (n_tok <= 0) return;  // surplus tile, or the grid already gave up; uniform across the CTA
+
+  // ---- each token's distinct valid blocks, sorted, plus the union bitmap ---------------------
+  // The union is built as a bitmap over the block ids in the P region (free until the loop).
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(p_s);
+  const int pos_last = __ldg(a.seq_lens + req) - 1;  // position of the request's last token
+  // valid block ids are <= pos_last / 128 and < max_blocks (<= 65536): at most 2048 words
+  const int nwords = min(max(pos_last, 0) / kSparseBlock / 32 + 1, (a.max_blocks + 31) / 32);
+  for (int w = threadIdx.x; w < nwords; w += kThreadsTc) bitmap[w] = 0u;
+  __syncthreads();
+  if (warp < 4) {
+    for (int tt = warp; tt < kTok; tt += 4) {
+      if (tt >= n_tok) {
+        if (lane == 0) {
+          ctl->cnt[tt] = 0;
+          ctl->own[tt] = -1;
+          ctl->lim[tt] = 0;
+        }
+        continue;
+      }
+      const int t = t0 + tt;
+      const int c0 = __ldg(a.cu_seqlens_q + req), c1 = __ldg(a.cu_seqlens_q + req + 1);
+      const int pos = __ldg(a.seq_lens + req) - (c1 - c0) + (t - c0);
+      const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
+      const int own = causal_len > 0 ? pos / kSparseBlock : -1;
+      const int b = lane < a.k ? __ldg(a.topk + static_cast<int64_t>(t) * a.topk_row_stride + lane) : -1;
+      bool valid = lane < a.k && causal_len > 0 && b >= 0 && b <= own;
+      const bool oob = valid && b >= a.max_blocks;
+      if (__any_sync(0xffffffffu, oob)) {
+        if (lane == 0) {
+          atomicOr(&ctl->bad_mask, 1 << tt);
+          set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+        }
+        valid = false;
+      }
+      // drop repeated ids: keep the lowest lane of each value
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      const uint32_t same = __match_any_sync(0xffffffffu, valid ? b : -1 - lane);
+      const bool keep = valid && (__ffs(same & vmask) - 1) == lane;
+      const uint32_t kmask = __ballot_sync(0xffffffffu, keep);
+      int rank = 0;
+      for (int j = 0; j < 32; ++j) {
+        const int bj = __shfl_sync(0xffffffffu, b, j);
+        if (((kmask >> j) & 1u) && bj < b) ++rank;
+      }
+      if (keep) {
+        ctl->tok_blk[tt][rank] = static_cast<uint16_t>(b);
+        atomicOr(&bitmap[b >> 5], 1u << (b & 31));
+      }
+      if (lane == 0) {
+        ctl->cnt[tt] = __popc(kmask);
+        ctl->own[tt] = own;
+        ctl->lim[tt] = causal_len - own * kSparseBlock;
+      }
+    }
+  }
+  if (warp == 2) tc::alloc(&ctl->tmem_base, 512);
+  __syncthreads();
+  // union = set bits in increasing order (one warp; a handful of words per tile)
+  if (warp == 0) {
+    int at = 0;
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+      const uint32_t word = w0 + lane < nwords ? bitmap[w0 + lane] : 0u;
+      const int c = __popc(word);
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int o = at + incl - c;
+      uint32_t bits = word;
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (o < kMaxUnion) ctl->union_blk[o] = static_cast<uint16_t>(((w0 + lane) << 5) + bit);
+        ++o;
+      }
+      at += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) ctl->n_union = at < kMaxUnion ? at : kMaxUnion;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const int nU = ctl->n_union;
+  const uint32_t tmem = ctl->tmem_base;
+  const uint32_t tm_s0 = tmem, tm_o = tmem + 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+      tma_load_3d(q_s, &q_map, &ctl->q_full, 0, g * kG, t0);
+      tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, g * kG, t0);
+      const int32_t* bt_row = a.page_table + static_cast<int64_t>(req) * a.pt_row_stride;
+      int next_phys = nU > 0 ? __ldg(bt_row + ctl->union_blk[0]) : 0;
+      int issued = 0;
+      for (int i = 0; i < nU; ++i) {
+        const int st = i & 1;
+        const int phys = next_phys;
+        if (i + 1 < nU) next_phys = __ldg(bt_row + ctl->union_blk[i + 1]);
+        if (i >= 2 && !wait_or_abort(&ctl->kv_empty[st], ((i >> 1) - 1) & 1, ctl, a.err_word)) break;
+        if (aborted(ctl)) break;
+        const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
+        if (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+        uint8_t* dst = kv_s + st * kKVBytes;
+        mbar_arrive_expect_tx(&ctl->kv_full[st], kKVBytes);
+        for (int j = 0; j < kPagesPerBlock; ++j) {
+          const int page = static_cast<int>(base) + j;  // out-of-range pages read as zeros (TMA bounds)
+#pragma unroll
+          for (int part = 0; part < 4; ++part)  // K dims 0-63, K 64-127, V 0-63, V 64-127
+            tma_load_4d(dst + part * kHalf + j * 2048, &kv_map, &ctl->kv_full[st], 64 * part, 0, g, page);
+        }
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - 2); i < issued; ++i)
+        if (!mbar_wait_bounded(&ctl->kv_full[i & 1], (i >> 1) & 1, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+      if (!mbar_wait_bounded(&ctl->q_full, 0, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
+      constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
+      const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
+      bool ok = nU == 0 || wait_or_abort(&ctl->q_full, 0, ctl, a.err_word);
+      int last_commit = -1;  // 0: s_full, 1: pv_done
+      for (int i = 0; ok && i <= nU; ++i) {
+        if (i < nU) {
+          const int st = i & 1;
+          if (!wait_or_abort(&ctl->kv_full[st], (i >> 1) & 1, ctl, a.err_word)) break;
+          if (i >= 2 && !wait_or_abort(&ctl->s_free[st], ((i >> 1) - 1) & 1, ctl, a.err_word)) break;
+          tc::fence_after_sync();
+          const uint32_t k_addr = smem_u32(kv_s + st * kKVBytes);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+            tc::mma_ss(tm_s0 + st * 128, tc::smem_desc_sw128(q_addr + off, 16, 1024),
+                       tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS, ks > 0);
+          }
+          tc::commit(&ctl->s_full[st]);
+          last_commit = 0;
+        }
+        if (i >= 1) {
+          const int j = i - 1, st = j & 1;
+          if (!wait_or_abort(&ctl->p_full, j & 1, ctl, a.err_word)) break;
+          tc::fence_after_sync();
+          const uint32_t v_addr = smem_u32(kv_s + st * kKVBytes + kTileBytes);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {  // P hi, then P lo
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t aoff = part * kTileBytes + (ks >> 2) * kHalf + (ks & 3) * 32;
+              tc::mma_ss(tm_o, tc::smem_desc_sw128(p_addr + aoff, 16, 1024),
+                         tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
+                         !(j == 0 && part == 0 && ks == 0));
+            }
+          }
+          tc::commit(&ctl->pv_done);
+          tc::commit(&ctl->kv_empty[st]);
+          last_commit = 1;
+        }
+      }
+      // all MMAs issued must complete before TMEM is released
+      if (last_commit >= 0) {
+        // the last commit of each kind arrived or will arrive; the waits below are bounded
+        if (nU > 0) mbar_wait_bounded(&ctl->pv_done, (nU - 1) & 1, kTcWaitNs);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int row = (warp - 4) * 32 + lane;  // = TMEM lane
+    const int tt = row >> 3, h = row & 7;
+    const bool live = tt < n_tok && !((ctl->bad_mask >> tt) & 1);
+    const int cnt_t = live ? ctl->cnt[tt] : 0;
+    const int own_t = ctl->own[tt], lim_t = ctl->lim[tt];
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const int last_blk = pos_last / kSparseBlock;
+    const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
+    float m_ref = -INFINITY, l = 0.f;
+    int ptr = 0;
+    // P rows: K-major, 128B swizzle; row at (row/8)*1024 + (row%8)*128 within each 64-key half
+    const uint32_t p_row = smem_u32(p_s) + (row >> 3) * 1024 + (row & 7) * 128;
+    bool ok = true;
+    for (int i = 0; i < nU && ok; ++i) {
+      const int sb = i & 1;
+      const int b = ctl->union_blk[i];
+      while (ptr < cnt_t && ctl->tok_blk[tt][ptr] < b) ++ptr;
+      const bool active = ptr < cnt_t && ctl->tok_blk[tt][ptr] == b;
+      const int lim = b == own_t ? lim_t : kSparseBlock;
+      if (!warp_wait_or_abort(&ctl->s_full[sb], (i >> 1) & 1, ctl, a.err_word)) { ok = false; break; }
+      // the P buffer and O are free once the previous block's PV has completed
+      if (i > 0 && !warp_wait_or_abort(&ctl->pv_done, (i - 1) & 1, ctl, a.err_word)) { ok = false; break; }
+      tc::fence_after_sync();
+      // rows past the request's last token in its last block may hold anything: zero that V
+      if (b == last_blk && last_rows < kSparseBlock) {
+        if (!warp_wait_or_abort(&ctl->kv_full[sb], (i >> 1) & 1, ctl, a.err_word)) { ok = false; break; }
+        const uint32_t v_base = smem_u32(kv_s + sb * kKVBytes + kTileBytes);
+        for (int e = row; e < (kSparseBlock - last_rows) * 16; e += kRows) {
+          const int key = last_rows + (e >> 4), part = (e >> 3) & 1, chunk = e & 7;
+          sts128(v_base + part * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
+        }
+      }
+      const uint32_t ts = tm_s0 + sb * 128 + lane_off;
+      // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
+      // take part in this block are masked arithmetically (their P row becomes zero).
+      if (__any_sync(0xffffffffu, active)) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tc::ld32(ts + 32 * c, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (active && 32 * c + j < lim) mx = fmaxf(mx, __uint_as_float(v[j]));
+        }
+        mx *= sl2;
+        const bool grow = active && (m_ref == -INFINITY || mx > m_ref + kRescaleLog2);
+        const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
+        const bool resc = grow && l > 0.f;
+        const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tc::ld32(tm_o + lane_off + 32 * c, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            tc::st32(tm_o + lane_off + 32 * c, v);
+          }
+          tc::wait_st();
+        }
+        l *= alpha;
+        m_ref = m_new;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tc::ld32(ts + 32 * c, v);
+          tc::wait_ld();
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float p0 = (active && 32 * c + j < lim) ? ex2(__uint_as_float(v[j]) * sl2 - m_ref) : 0.f;
+            const float p1 = (active && 32 * c + j + 1 < lim) ? ex2(__uint_as_float(v[j + 1]) * sl2 - m_ref) : 0.f;
+            l += p0 + p1;
+            const uint32_t hh = pack_bf16(p0, p1);
+            hi[j >> 1] = hh;
+            lo[j >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
+          }
+          // keys 32c..32c+31: half c/2, logical 16-byte chunks 4(c%2)..4(c%2)+3
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = 4 * (c & 1) + q4;
+            const uint32_t addr = p_row + (c >> 1) * kHalf + ((chunk ^ (row & 7)) << 4);
+            sts128(addr, hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
+            sts128(addr + kTileBytes, lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int chunk = 0; chunk < 8; ++chunk) {
+            sts128(p_row + half * kHalf + (chunk << 4), 0, 0, 0, 0);
+            sts128(p_row + half * kHalf + (chunk << 4) + kTileBytes, 0, 0, 0, 0);
+          }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->s_free[sb]);
+        mbar_arrive(&ctl->p_full);
+      }
+    }
+    // ---- epilogue: O / l -> bf16
+    if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done, (nU - 1) & 1, ctl, a.err_word)) ok = false;
+    tc::fence_after_sync();
+    {
+      // warp-collective TMEM reads for every lane; only rows of real tokens are stored
+      uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
+                      static_cast<int64_t>(g * kG + h) * a.out_head_stride;
+      const float inv = (live && l > 0.f && ok) ? a.v_scale / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (nU > 0) {
+          tc::ld32(tm_o + lane_off + 32 * c, v);
+          tc::wait_ld();
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float o0 = nU > 0 ? __uint_as_float(v[j]) * inv : 0.f;
+          const float o1 = nU > 0 ? __uint_as_float(v[j + 1]) * inv : 0.f;
+          w[j >> 1] = pack_bf16(o0, o1);
+        }
+        if (tt < n_tok) {
+          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc::fence_after_sync();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const AttendArgs& a) {
+  return a.kv_dtype == PBS_KV_BF16 && a.group == kG && a.k <= kTcMaxTopk && a.max_blocks <= 65536 &&
+         a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
+         reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 &&
+         reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
+}
+
+cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                              cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kTcSmem));
+  if (e != cudaSuccess) return e;
+  // tiles are numbered request by request; the grid is an upper bound and surplus CTAs exit
+  const unsigned tiles = static_cast<unsigned>(a.num_rows / kTok + a.num_reqs + 1);
+  prefill_tc_kernel<<<dim3(tiles, static_cast<unsigned>(a.num_kv_heads)), kThreadsTc, kTcSmem, stream>>>(kv_map,
+                                                                                                        q_map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace pbs

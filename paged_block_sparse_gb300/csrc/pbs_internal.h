@@ -66,6 +66,12 @@ struct AttendArgs {
 // (unused for NVFP4). Returns the launch status.
 cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream);
 
+// Prefill attend on tcgen05 tensor cores (bf16 cache, GQA 8, top-k <= 16, 16-byte aligned q/out
+// rows). `q_map` is a 3-D tensor map {head_dim, heads, tokens} with a {64, 8, 16} box.
+bool prefill_tc_supported(const AttendArgs& a);
+cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                              cudaStream_t stream);
+
 // Index-cache insert.
 struct InsertArgs {
   const uint8_t* index_k;

@@ -273,3 +273,55 @@ def test_insert_index_cache_slot_past_cache(pbs):
     torch.cuda.synchronize()
     assert int(err.item()) & 4
     assert float(cache[0, 1].sum()) == 128.0 and float(cache.sum()) == 128.0
+
+
+# ------------------------------------------------------------------------------------------
+# prefill: tcgen05 tile kernel and token-centric kernel
+# ------------------------------------------------------------------------------------------
+
+PREFILL_CASES = [
+    dict(pre_q_lens=[37, 16, 1, 200], pre_ctx_lens=[0, 100, 5, 3000], topk=16),
+    dict(pre_q_lens=[3] * 40, pre_ctx_lens=[i * 50 for i in range(40)], topk=8),   # > 32 requests
+    dict(pre_q_lens=[500], pre_ctx_lens=[7], topk=12, future_prob=0.5),
+    dict(pre_q_lens=[130, 260], pre_ctx_lens=[0, 0], topk=2),
+]
+
+
+@pytest.mark.parametrize("kernel", ["tc", "token"])
+@pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
+def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, monkeypatch):
+    if kernel == "token":
+        monkeypatch.setenv("PBS_PREFILL_KERNEL", "token")
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, seed=41 + ci, **PREFILL_CASES[ci])
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err)
+    assert int(err.item()) == 0
+    assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", f"prefill {kernel} case {ci}")
+
+
+def test_prefill_tc_duplicate_ids_count_once(pbs):
+    """The tile kernel reads each selected block once per token, the attend's set reading."""
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=6, pre_q_lens=[300], pre_ctx_lens=[400],
+                        seed=45)
+    tk = b.pre.topk.clone()
+    tk[0, :, 1] = tk[0, :, 0]                                       # duplicate the first slot
+    b.pre.topk = tk
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err)
+    assert int(err.item()) == 0
+    assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill duplicates")
+
+
+def test_prefill_tc_ignores_nan_past_last_token(pbs):
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, pre_q_lens=[77, 200], pre_ctx_lens=[0, 50],
+                        seed=46)
+    p = b.pre
+    pt = np_i32(p.page_table)
+    for r, L in enumerate(np_i32(p.seq_lens)):
+        for x in range(L, ((L + 127) // 128) * 128):
+            page = int(pt[r, x // 128]) * 8 + (x % 128) // 16
+            b.cache[page].view(b.num_kv_heads, 16, -1)[:, x % 16, :] = 0xFF
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err)
+    assert int(err.item()) == 0
+    assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill NaN past the end")
