@@ -372,6 +372,45 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, peak_src):
+    """One JSON line for a non-headline workload (prefill TFLOP/s, or decode GB/s for fp8/NVFP4)."""
+    make = {"prefill": workloads.prefill, "mtp_fp8": workloads.mtp_fp8, "mixed_nvfp4": workloads.mixed_nvfp4}
+    b = make[args.workload](device="cuda", seed={"prefill": 1002, "mtp_fp8": 1003, "mixed_nvfp4": 1004}[
+        args.workload] + 17 * rank)
+    if pg:
+        pg.barrier()
+    with ClockSampler(local) as clk:
+        if args.workload == "prefill" or (args.workload == "mixed_nvfp4" and args.part == "prefill"):
+            work = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
+            times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream)
+            unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
+        else:
+            work = decode_bytes(b, decode_ctx(pbs, b))
+            times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
+            unit, bound, peak, metric = "GB/s", "hbm", hbm, "decode HBM GB/s"
+    ms = statistics.mean(times)
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    achieved = work / (statistics.mean(times) * 1e-3) / scale
+    if rank == 0:
+        print(json.dumps({
+            "metric": metric, "value": world * work / (ms * 1e-3) / scale, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
+            "data": "synthetic", "config": {"workload": b.name, "part": args.part,
+                                            "l2": "flushed (256 MiB write) before every step"},
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                         "traffic": None, "peak_source": f"{peak_src} (burst, kernel timed alone)",
+                         "algorithmic_work_per_launch": work},
+            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
 # --------------------------------------------------------------------------------------------
 # main
 # --------------------------------------------------------------------------------------------
@@ -387,6 +426,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=64,
                     help="decode requests (64 is the headline workload; smaller only for profiling)")
+    ap.add_argument("--part", choices=["decode", "prefill"], default="decode",
+                    help="which half of the mixed NVFP4 batch --workload mixed_nvfp4 times")
+    ap.add_argument("--workload", choices=["decode", "prefill", "mtp_fp8", "mixed_nvfp4"], default="decode",
+                    help="timed workload (the headline line is decode; the others for profiling and tuning)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -410,6 +453,8 @@ def main():
 
     stream = torch.cuda.Stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    if args.workload != "decode":
+        return secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, peak_src)
     b = workloads.decode(device="cuda", seed=1001 + 17 * rank, batch=args.batch)
     ctx = decode_ctx(pbs, b)
     by = decode_bytes(b, ctx)

@@ -13,12 +13,17 @@
 //   heads = 128 rows, one MMA M-tile. The tile's selected blocks are merged into a sorted union;
 //   every union block is streamed once and each row is masked by its own token's selection.
 // * Warp 0: TMA producer (Q tile once via a 3-D tensor map; K and V of each union block page by
-//   page through the cache tensor map, 128B swizzle, 2-stage ring). Warp 1: one thread issues
+//   page through the cache tensor map, 128B swizzle, 3-stage ring). Warp 1: one thread issues
 //   the tcgen05 MMAs. Warps 4-7: softmax and epilogue, thread i owning TMEM lane / row i.
-// * TMEM (512 columns): S double buffer (2 x 128) and the O accumulator (128), fp32.
-// * S = Q K^T: A = Q (K-major), B = K tile (K-major). O += P V: A = P (K-major, written by the
-//   softmax warps), B = V tile (MN-major). P is split into bf16 hi + lo halves, two MMAs, so the
-//   result stays within 2e-3 relative RMS of the fp64 attend.
+// * TMEM (512 columns): S double buffer (2 x 128, fp32), the O accumulator (128, fp32) and two
+//   64-column buffers for the low half of P. The high half of P (bf16, two keys per column)
+//   overwrites the first 64 columns of its own S buffer.
+// * S = Q K^T: A = Q (K-major smem), B = K tile (K-major smem). O += P V: A = P read from TMEM,
+//   B = V tile (MN-major smem). P is split into bf16 hi + lo halves, two MMAs, so the result
+//   stays within 2e-3 relative RMS of the fp64 attend.
+// * The MMAs of one thread execute in issue order, so S(i) may reuse the buffer whose P(i-2)
+//   was read by PV(i-2), issued before it; the softmax of block i waits only for S(i), and for
+//   PV(i-1) when it has to rescale O.
 // * Online softmax in base 2 with lazy rescaling: the O row is rescaled only when the running
 //   maximum grows by more than 2^8, so most blocks never touch O from the CUDA cores.
 // * Duplicate ids in a token's list count once (set semantics of the attend); the decode path and
@@ -38,20 +43,21 @@ constexpr int kQBytes = kRows * kHeadDim * 2;          // 32 KiB
 constexpr int kHalf = 128 * 128;                       // one 64-dim half of a 128 x 128 bf16 tile
 constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB
 constexpr int kKVBytes = 2 * kTileBytes;               // K then V
-constexpr int kPBytes = 2 * kTileBytes;                // P hi then P lo
-constexpr int kBigBytes = kQBytes + 2 * kKVBytes + kPBytes;  // 224 KiB
+constexpr int kStagesTc = 3;
+constexpr int kBigBytes = kQBytes + kStagesTc * kKVBytes;  // 224 KiB
 constexpr int kMaxUnion = 256;
 constexpr int kTcMaxTopk = 16;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
 struct TcCtl {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
+  uint64_t kv_full[kStagesTc];
+  uint64_t kv_empty[kStagesTc];
   uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  // P of even / odd blocks: the softmax may finish block j+1 before the MMA thread has waited for
+  // block j (it only waits for PV when it rescales), but never block j+2 (S(j+2) follows PV(j)).
+  uint64_t p_full[2];
+  uint64_t pv_done[2];  // PV of even / odd blocks
   uint32_t tmem_base;
   int32_t n_union;
   int32_t req, t0, n_tok;
@@ -109,7 +115,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint8_t* big = smem_raw + big_off;
   uint8_t* q_s = big;
   uint8_t* kv_s = big + kQBytes;  // stage st at kv_s + st * kKVBytes: K halves, then V halves
-  uint8_t* p_s = big + kQBytes + 2 * kKVBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
@@ -153,14 +158,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       ctl->bad_mask = 0;
       ctl->abort = 0;
       mbar_init(&ctl->q_full, 1);
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kStagesTc; ++i) {
         mbar_init(&ctl->kv_full[i], 1);
         mbar_init(&ctl->kv_empty[i], 1);
-        mbar_init(&ctl->s_full[i], 1);
-        mbar_init(&ctl->s_free[i], 4);
       }
-      mbar_init(&ctl->p_full, 4);
-      mbar_init(&ctl->pv_done, 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&ctl->s_full[i], 1);
+        mbar_init(&ctl->p_full[i], 4);
+        mbar_init(&ctl->pv_done[i], 1);
+      }
       fence_mbar_init();
     }
   }
@@ -169,8 +175,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (n_tok <= 0) return;  // surplus tile, or the grid already gave up; uniform across the CTA
 
   // ---- each token's distinct valid blocks, sorted, plus the union bitmap ---------------------
-  // The union is built as a bitmap over the block ids in the P region (free until the loop).
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(p_s);
+  // The union is built as a bitmap over the block ids in the last K/V stage (free until the loop).
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(kv_s + (kStagesTc - 1) * kKVBytes);
   const int pos_last = __ldg(a.seq_lens + req) - 1;  // position of the request's last token
   // valid block ids are <= pos_last / 128 and < max_blocks (<= 65536): at most 2048 words
   const int nwords = min(max(pos_last, 0) / kSparseBlock / 32 + 1, (a.max_blocks + 31) / 32);
@@ -248,12 +254,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     if (lane == 0) ctl->n_union = at < kMaxUnion ? at : kMaxUnion;
   }
+  // the bitmap's generic writes precede the copy engine's writes into the same stage
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const int nU = ctl->n_union;
   const uint32_t tmem = ctl->tmem_base;
-  const uint32_t tm_s0 = tmem, tm_o = tmem + 256;
+  const uint32_t tm_s0 = tmem, tm_o = tmem + 256, tm_plo = tmem + 384;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -265,10 +273,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       int next_phys = nU > 0 ? __ldg(bt_row + ctl->union_blk[0]) : 0;
       int issued = 0;
       for (int i = 0; i < nU; ++i) {
-        const int st = i & 1;
+        const int st = i % kStagesTc;
         const int phys = next_phys;
         if (i + 1 < nU) next_phys = __ldg(bt_row + ctl->union_blk[i + 1]);
-        if (i >= 2 && !wait_or_abort(&ctl->kv_empty[st], ((i >> 1) - 1) & 1, ctl, a.err_word)) break;
+        if (i >= kStagesTc && !wait_or_abort(&ctl->kv_empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word)) break;
         if (aborted(ctl)) break;
         const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
         if (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
@@ -282,8 +290,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         issued = i + 1;
       }
-      for (int i = max(0, issued - 2); i < issued; ++i)
-        if (!mbar_wait_bounded(&ctl->kv_full[i & 1], (i >> 1) & 1, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+      for (int i = max(0, issued - kStagesTc); i < issued; ++i)
+        if (!mbar_wait_bounded(&ctl->kv_full[i % kStagesTc], (i / kStagesTc) & 1, kTcWaitNs))
+          set_err(a.err_word, PBS_DEVERR_TIMEOUT);
       if (!mbar_wait_bounded(&ctl->q_full, 0, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
@@ -291,50 +300,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
       constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
-      const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
+      const uint32_t q_addr = smem_u32(q_s);
       bool ok = nU == 0 || wait_or_abort(&ctl->q_full, 0, ctl, a.err_word);
-      int last_commit = -1;  // 0: s_full, 1: pv_done
+      int issued_pv = 0;
       for (int i = 0; ok && i <= nU; ++i) {
         if (i < nU) {
-          const int st = i & 1;
-          if (!wait_or_abort(&ctl->kv_full[st], (i >> 1) & 1, ctl, a.err_word)) break;
-          if (i >= 2 && !wait_or_abort(&ctl->s_free[st], ((i >> 1) - 1) & 1, ctl, a.err_word)) break;
+          // S(i) -> TMEM buffer i&1 (its previous P was read by PV(i-2), issued earlier)
+          const int st = i % kStagesTc;
+          if (!wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
           const uint32_t k_addr = smem_u32(kv_s + st * kKVBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-            tc::mma_ss(tm_s0 + st * 128, tc::smem_desc_sw128(q_addr + off, 16, 1024),
+            tc::mma_ss(tm_s0 + (i & 1) * 128, tc::smem_desc_sw128(q_addr + off, 16, 1024),
                        tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS, ks > 0);
           }
-          tc::commit(&ctl->s_full[st]);
-          last_commit = 0;
+          tc::commit(&ctl->s_full[i & 1]);
         }
         if (i >= 1) {
-          const int j = i - 1, st = j & 1;
-          if (!wait_or_abort(&ctl->p_full, j & 1, ctl, a.err_word)) break;
+          // O += P(j) V(j): P hi in the first 64 columns of S buffer j&1, P lo in its own buffer
+          const int j = i - 1, st = j % kStagesTc;
+          if (!wait_or_abort(&ctl->p_full[j & 1], (j >> 1) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
           const uint32_t v_addr = smem_u32(kv_s + st * kKVBytes + kTileBytes);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {  // P hi, then P lo
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t pa = part == 0 ? tm_s0 + (j & 1) * 128 : tm_plo + (j & 1) * 64;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t aoff = part * kTileBytes + (ks >> 2) * kHalf + (ks & 3) * 32;
-              tc::mma_ss(tm_o, tc::smem_desc_sw128(p_addr + aoff, 16, 1024),
-                         tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
+            for (int ks = 0; ks < 8; ++ks)
+              tc::mma_ts(tm_o, pa + 8 * ks, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
                          !(j == 0 && part == 0 && ks == 0));
-            }
           }
-          tc::commit(&ctl->pv_done);
+          tc::commit(&ctl->pv_done[j & 1]);
           tc::commit(&ctl->kv_empty[st]);
-          last_commit = 1;
+          issued_pv = j + 1;
         }
       }
-      // all MMAs issued must complete before TMEM is released
-      if (last_commit >= 0) {
-        // the last commit of each kind arrived or will arrive; the waits below are bounded
-        if (nU > 0) mbar_wait_bounded(&ctl->pv_done, (nU - 1) & 1, kTcWaitNs);
-      }
+      // every MMA issued must complete before TMEM is released
+      if (issued_pv > 0)
+        mbar_wait_bounded(&ctl->pv_done[(issued_pv - 1) & 1], ((issued_pv - 1) >> 1) & 1, kTcWaitNs);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
@@ -349,29 +354,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
     float m_ref = -INFINITY, l = 0.f;
     int ptr = 0;
-    // P rows: K-major, 128B swizzle; row at (row/8)*1024 + (row%8)*128 within each 64-key half
-    const uint32_t p_row = smem_u32(p_s) + (row >> 3) * 1024 + (row & 7) * 128;
     bool ok = true;
     for (int i = 0; i < nU && ok; ++i) {
-      const int sb = i & 1;
+      const int sb = i & 1, st = i % kStagesTc;
       const int b = ctl->union_blk[i];
       while (ptr < cnt_t && ctl->tok_blk[tt][ptr] < b) ++ptr;
       const bool active = ptr < cnt_t && ctl->tok_blk[tt][ptr] == b;
       const int lim = b == own_t ? lim_t : kSparseBlock;
       if (!warp_wait_or_abort(&ctl->s_full[sb], (i >> 1) & 1, ctl, a.err_word)) { ok = false; break; }
-      // the P buffer and O are free once the previous block's PV has completed
-      if (i > 0 && !warp_wait_or_abort(&ctl->pv_done, (i - 1) & 1, ctl, a.err_word)) { ok = false; break; }
       tc::fence_after_sync();
       // rows past the request's last token in its last block may hold anything: zero that V
       if (b == last_blk && last_rows < kSparseBlock) {
-        if (!warp_wait_or_abort(&ctl->kv_full[sb], (i >> 1) & 1, ctl, a.err_word)) { ok = false; break; }
-        const uint32_t v_base = smem_u32(kv_s + sb * kKVBytes + kTileBytes);
+        if (!warp_wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) { ok = false; break; }
+        const uint32_t v_base = smem_u32(kv_s + st * kKVBytes + kTileBytes);
         for (int e = row; e < (kSparseBlock - last_rows) * 16; e += kRows) {
           const int key = last_rows + (e >> 4), part = (e >> 3) & 1, chunk = e & 7;
           sts128(v_base + part * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       const uint32_t ts = tm_s0 + sb * 128 + lane_off;
+      const uint32_t tplo = tm_plo + sb * 64 + lane_off;
       // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
       // take part in this block are masked arithmetically (their P row becomes zero).
       if (__any_sync(0xffffffffu, active)) {
@@ -391,6 +394,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const bool resc = grow && l > 0.f;
         const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
         if (__any_sync(0xffffffffu, resc)) {
+          // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
+          if (i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl, a.err_word)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
@@ -400,7 +409,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
             tc::st32(tm_o + lane_off + 32 * c, v);
           }
-          tc::wait_st();
         }
         l *= alpha;
         m_ref = m_new;
@@ -419,34 +427,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             hi[j >> 1] = hh;
             lo[j >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
           }
-          // keys 32c..32c+31: half c/2, logical 16-byte chunks 4(c%2)..4(c%2)+3
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = 4 * (c & 1) + q4;
-            const uint32_t addr = p_row + (c >> 1) * kHalf + ((chunk ^ (row & 7)) << 4);
-            sts128(addr, hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
-            sts128(addr + kTileBytes, lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]);
-          }
+          // keys 32c..32c+31 -> packed columns 16c..16c+15 (S columns already consumed)
+          tc::st16(ts + 16 * c, hi);
+          tc::st16(tplo + 16 * c, lo);
         }
       } else {
+        uint32_t z[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
+        for (int j = 0; j < 16; ++j) z[j] = 0u;
 #pragma unroll
-          for (int chunk = 0; chunk < 8; ++chunk) {
-            sts128(p_row + half * kHalf + (chunk << 4), 0, 0, 0, 0);
-            sts128(p_row + half * kHalf + (chunk << 4) + kTileBytes, 0, 0, 0, 0);
-          }
+        for (int c = 0; c < 4; ++c) {
+          tc::st16(ts + 16 * c, z);
+          tc::st16(tplo + 16 * c, z);
+        }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&ctl->s_free[sb]);
-        mbar_arrive(&ctl->p_full);
-      }
+      if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
     }
     // ---- epilogue: O / l -> bf16
-    if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done, (nU - 1) & 1, ctl, a.err_word)) ok = false;
+    if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(nU - 1) & 1], ((nU - 1) >> 1) & 1, ctl, a.err_word))
+      ok = false;
     tc::fence_after_sync();
     {
       // warp-collective TMEM reads for every lane; only rows of real tokens are stored
