@@ -38,7 +38,10 @@ namespace {
 constexpr int kTok = 16;          // tokens per tile
 constexpr int kG = 8;             // query heads per kv head on this path
 constexpr int kRows = kTok * kG;  // 128 = MMA M
-constexpr int kThreadsTc = 256;
+constexpr int kSplit = 2;                        // softmax warps per TMEM lane quadrant
+constexpr int kW = 128 / kSplit;                 // S columns (keys) per softmax thread
+constexpr int kSoftWarps = 4 * kSplit;
+constexpr int kThreadsTc = 32 * (4 + kSoftWarps);
 constexpr int kQBytes = kRows * kHeadDim * 2;          // 32 KiB
 constexpr int kHalf = 128 * 128;                       // one 64-dim half of a 128 x 128 bf16 tile
 constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB
@@ -68,10 +71,17 @@ struct TcCtl {
   int32_t cnt[kTok];  // distinct valid blocks per token
   uint16_t union_blk[kMaxUnion];
   uint16_t tok_blk[kTok][kTcMaxTopk];
+  float xchg[kSplit][kRows];  // per-row partial maxima / sums exchanged within a lane quadrant
 };
 
 constexpr size_t kTcSmem = 232448;  // the per-block opt-in maximum of sm_100-family GPUs
-static_assert(sizeof(TcCtl) + 1023 + kBigBytes <= kTcSmem, "shared memory layout exceeds 227 KiB");
+// The big buffers start at the (1024-aligned) dynamic shared memory base; the control block
+// follows them.
+static_assert(kBigBytes + sizeof(TcCtl) <= kTcSmem, "shared memory layout exceeds 227 KiB");
+
+__device__ __forceinline__ void quad_bar(int quad) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + quad), "r"(32 * kSplit) : "memory");
+}
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
@@ -108,11 +118,14 @@ __device__ __forceinline__ bool aborted(TcCtl* ctl) { return *reinterpret_cast<v
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const AttendArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  TcCtl* ctl = reinterpret_cast<TcCtl*>(smem_raw);
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t big_off = ((raw + sizeof(TcCtl) + 1023u) & ~1023u) - raw;
-  uint8_t* big = smem_raw + big_off;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* big = smem_raw;
+  TcCtl* ctl = reinterpret_cast<TcCtl*>(smem_raw + kBigBytes);
+  // the 128B-swizzled operands need 1024-byte alignment; the dynamic base provides it
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+    return;
+  }
   uint8_t* q_s = big;
   uint8_t* kv_s = big + kQBytes;  // stage st at kv_s + st * kKVBytes: K halves, then V halves
 
@@ -164,7 +177,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&ctl->s_full[i], 1);
-        mbar_init(&ctl->p_full[i], 4);
+        mbar_init(&ctl->p_full[i], kSoftWarps);
         mbar_init(&ctl->pv_done[i], 1);
       }
       fence_mbar_init();
@@ -326,11 +339,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const uint32_t v_addr = smem_u32(kv_s + st * kKVBytes + kTileBytes);
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
-            const uint32_t pa = part == 0 ? tm_s0 + (j & 1) * 128 : tm_plo + (j & 1) * 64;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              tc::mma_ts(tm_o, pa + 8 * ks, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
+            for (int ks = 0; ks < 8; ++ks) {
+              // keys 16ks..16ks+15: P hi lives in the first half of the S columns of the softmax
+              // part that owns those keys; P lo is packed contiguously
+              const int owner = (16 * ks) / kW;
+              const uint32_t pa = part == 0 ? tm_s0 + (j & 1) * 128 + owner * kW + (16 * ks - owner * kW) / 2
+                                            : tm_plo + (j & 1) * 64 + 8 * ks;
+              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
                          !(j == 0 && part == 0 && ks == 0));
+            }
           }
           tc::commit(&ctl->pv_done[j & 1]);
           tc::commit(&ctl->kv_empty[st]);
@@ -343,51 +361,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
-    const int row = (warp - 4) * 32 + lane;  // = TMEM lane
+    // kSplit warps share each 32-lane quadrant of TMEM; warp part p owns S / O columns
+    // [p*kW, p*kW + kW) of its 32 rows. Row maxima and sums are combined through shared memory.
+    const int sw = warp - 4, quad = sw & 3, part = sw >> 2;
+    const int row = quad * 32 + lane;  // = TMEM lane
+    const int col0 = part * kW;
     const int tt = row >> 3, h = row & 7;
     const bool live = tt < n_tok && !((ctl->bad_mask >> tt) & 1);
     const int cnt_t = live ? ctl->cnt[tt] : 0;
     const int own_t = ctl->own[tt], lim_t = ctl->lim[tt];
-    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = a.scale_log2;
     const int last_blk = pos_last / kSparseBlock;
     const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
     int ptr = 0;
     bool ok = true;
-    for (int i = 0; i < nU && ok; ++i) {
+    // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
+    // the blocks, so the two warps of a quadrant always meet at the same named barriers.
+    for (int i = 0; i < nU; ++i) {
       const int sb = i & 1, st = i % kStagesTc;
       const int b = ctl->union_blk[i];
       while (ptr < cnt_t && ctl->tok_blk[tt][ptr] < b) ++ptr;
       const bool active = ptr < cnt_t && ctl->tok_blk[tt][ptr] == b;
       const int lim = b == own_t ? lim_t : kSparseBlock;
-      if (!warp_wait_or_abort(&ctl->s_full[sb], (i >> 1) & 1, ctl, a.err_word)) { ok = false; break; }
+      if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (i >> 1) & 1, ctl, a.err_word)) ok = false;
       tc::fence_after_sync();
       // rows past the request's last token in its last block may hold anything: zero that V
       if (b == last_blk && last_rows < kSparseBlock) {
-        if (!warp_wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) { ok = false; break; }
+        if (ok && !warp_wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) ok = false;
         const uint32_t v_base = smem_u32(kv_s + st * kKVBytes + kTileBytes);
-        for (int e = row; e < (kSparseBlock - last_rows) * 16; e += kRows) {
-          const int key = last_rows + (e >> 4), part = (e >> 3) & 1, chunk = e & 7;
-          sts128(v_base + part * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
+        for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
+          const int key = last_rows + (e >> 4), vp = (e >> 3) & 1, chunk = e & 7;
+          sts128(v_base + vp * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       const uint32_t ts = tm_s0 + sb * 128 + lane_off;
       const uint32_t tplo = tm_plo + sb * 64 + lane_off;
       // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
-      // take part in this block are masked arithmetically (their P row becomes zero).
+      // take part in this block are masked arithmetically (their P row becomes zero). Activity
+      // depends only on the row, so the kSplit warps of a quadrant always agree.
       if (__any_sync(0xffffffffu, active)) {
-        float mx = -INFINITY;
+        uint32_t v[kW];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tc::ld32(ts + 32 * c, v);
-          tc::wait_ld();
+        for (int c = 0; c < kW / 32; ++c) tc::ld32(ts + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+        tc::wait_ld();
+        float pm = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (active && 32 * c + j < lim) mx = fmaxf(mx, __uint_as_float(v[j]));
-        }
+        for (int j = 0; j < kW; ++j)
+          if (active && col0 + j < lim) pm = fmaxf(pm, __uint_as_float(v[j]));
+        ctl->xchg[part][row] = pm;
+        quad_bar(quad);
+        float mx = pm;
+#pragma unroll
+        for (int q = 0; q < kSplit; ++q) mx = fmaxf(mx, ctl->xchg[q][row]);
+        quad_bar(quad);  // every part has read before the next block overwrites
         mx *= sl2;
         const bool grow = active && (m_ref == -INFINITY || mx > m_ref + kRescaleLog2);
         const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
@@ -395,50 +424,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
         if (__any_sync(0xffffffffu, resc)) {
           // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
-          if (i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl, a.err_word)) {
+          if (ok && i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl, a.err_word))
             ok = false;
-            break;
-          }
           tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tc::ld32(tm_o + lane_off + 32 * c, v);
+          for (int c = 0; c < kW / 32; ++c) {
+            uint32_t o[32];
+            tc::ld32(tm_o + lane_off + col0 + 32 * c, o);
             tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            tc::st32(tm_o + lane_off + 32 * c, v);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tc::st32(tm_o + lane_off + col0 + 32 * c, o);
           }
         }
         l *= alpha;
         m_ref = m_new;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tc::ld32(ts + 32 * c, v);
-          tc::wait_ld();
+        for (int c = 0; c < kW / 32; ++c) {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float p0 = (active && 32 * c + j < lim) ? ex2(__uint_as_float(v[j]) * sl2 - m_ref) : 0.f;
-            const float p1 = (active && 32 * c + j + 1 < lim) ? ex2(__uint_as_float(v[j + 1]) * sl2 - m_ref) : 0.f;
+            const int key = col0 + 32 * c + j;
+            const float p0 = (active && key < lim) ? ex2(__uint_as_float(v[32 * c + j]) * sl2 - m_ref) : 0.f;
+            const float p1 = (active && key + 1 < lim) ? ex2(__uint_as_float(v[32 * c + j + 1]) * sl2 - m_ref) : 0.f;
             l += p0 + p1;
             const uint32_t hh = pack_bf16(p0, p1);
             hi[j >> 1] = hh;
             lo[j >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
           }
-          // keys 32c..32c+31 -> packed columns 16c..16c+15 (S columns already consumed)
-          tc::st16(ts + 16 * c, hi);
-          tc::st16(tplo + 16 * c, lo);
+          // P hi over the first half of this part's own S columns (all already in registers)
+          tc::st16(ts + col0 + 16 * c, hi);
+          tc::st16(tplo + col0 / 2 + 16 * c, lo);
         }
       } else {
         uint32_t z[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) z[j] = 0u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tc::st16(ts + 16 * c, z);
-          tc::st16(tplo + 16 * c, z);
+        for (int c = 0; c < kW / 32; ++c) {
+          tc::st16(ts + col0 + 16 * c, z);
+          tc::st16(tplo + col0 / 2 + 16 * c, z);
         }
       }
       tc::wait_st();
@@ -446,20 +471,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
     }
-    // ---- epilogue: O / l -> bf16
+    // ---- epilogue: O / l -> bf16 (row sum combined over the parts of the quadrant)
     if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(nU - 1) & 1], ((nU - 1) >> 1) & 1, ctl, a.err_word))
       ok = false;
     tc::fence_after_sync();
+    ctl->xchg[part][row] = l;
+    quad_bar(quad);
+    float lsum = 0.f;
+#pragma unroll
+    for (int q = 0; q < kSplit; ++q) lsum += ctl->xchg[q][row];
     {
       // warp-collective TMEM reads for every lane; only rows of real tokens are stored
       uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
-                      static_cast<int64_t>(g * kG + h) * a.out_head_stride;
-      const float inv = (live && l > 0.f && ok) ? a.v_scale / l : 0.f;
+                      static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
+      const float inv = (live && lsum > 0.f && ok) ? a.v_scale / lsum : 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kW / 32; ++c) {
         uint32_t v[32];
         if (nU > 0) {
-          tc::ld32(tm_o + lane_off + 32 * c, v);
+          tc::ld32(tm_o + lane_off + col0 + 32 * c, v);
           tc::wait_ld();
         }
         uint32_t w[16];
