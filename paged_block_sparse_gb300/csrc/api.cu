@@ -69,6 +69,25 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
+// The packed bf16 cache as seen by the prefill tile kernel: one (page, kv head) chunk of
+// 16 rows x 512 B as a 5-D box {64 elements, 8 rows, 4 quarters (K lo, K hi, V lo, V hi),
+// 2 row halves, page * Hkv + head}; the box lands as [half][quarter][8 rows][128 B], i.e.
+// 128B-swizzle atoms of 8 rows per quarter. Every address stays inside its own 8 KiB chunk.
+// Needs page_stride_bytes == Hkv * 8192 (pages packed back to back).
+int encode_cache_map_tc(CUtensorMap* map, const void* cache, int num_kv_heads, int64_t num_pages) {
+  std::memset(map, 0, sizeof(*map));
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PBS_ERR_CUDA;
+  const cuuint64_t dims[5] = {64, 8, 4, 2, static_cast<cuuint64_t>(num_pages) * num_kv_heads};
+  const cuuint64_t strides[4] = {512, 128, 4096, 8192};
+  const cuuint32_t box[5] = {64, 8, 4, 2, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
+}
+
 // Queries as a 3-D tensor {head_dim, heads, tokens}; a box is 16 tokens x 8 heads x 64 dims, laid
 // out in shared memory as the 128-row K-major operand of the prefill MMA (row = token * 8 + head).
 int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int total_q, int64_t q_row_stride,
@@ -88,11 +107,14 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int total_q, in
 }
 
 // Which prefill kernel runs: the tcgen05 tile kernel where it applies, the token-centric
-// kernel otherwise. PBS_PREFILL_KERNEL=token forces the token-centric one (tests, tuning).
-bool use_prefill_tc(const AttendArgs& a) {
-  if (const char* env = std::getenv("PBS_PREFILL_KERNEL"))
-    if (std::strcmp(env, "token") == 0) return false;
-  return pbs::prefill_tc_supported(a);
+// kernel otherwise. PBS_PREFILL_KERNEL=token forces the token-centric one, =tc requires the
+// tile kernel (tests, tuning).
+int prefill_kernel_override() {
+  if (const char* env = std::getenv("PBS_PREFILL_KERNEL")) {
+    if (std::strcmp(env, "token") == 0) return 1;
+    if (std::strcmp(env, "tc") == 0) return 2;
+  }
+  return 0;
 }
 
 // CTAs per (row, kv head). Splitting a row across a cluster costs a cluster barrier, a DSMEM
@@ -333,11 +355,16 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   st = encode_cache_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
   if (st != PBS_OK) return st;
   cudaError_t e;
-  if (use_prefill_tc(a)) {
+  CUtensorMap tcmap;
+  const int force = prefill_kernel_override();
+  const bool tc_ok = force != 1 && pbs::prefill_tc_supported(a) &&
+                     encode_cache_map_tc(&tcmap, kv_cache, num_kv_heads, num_pages) == PBS_OK;
+  if (force == 2 && !tc_ok) return PBS_ERR_UNSUPPORTED;
+  if (tc_ok) {
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
-    e = pbs::launch_prefill_tc(a, map, qmap, reinterpret_cast<cudaStream_t>(stream));
+    e = pbs::launch_prefill_tc(a, tcmap, qmap, reinterpret_cast<cudaStream_t>(stream));
   } else {
     e = pbs::launch_attend(a, true, map, reinterpret_cast<cudaStream_t>(stream));
   }

@@ -12,8 +12,10 @@
 // * A CTA owns a tile of 16 consecutive tokens of one request and one kv head: 16 x 8 query
 //   heads = 128 rows, one MMA M-tile. The tile's selected blocks are merged into a sorted union;
 //   every union block is streamed once and each row is masked by its own token's selection.
-// * Warp 0: TMA producer (Q tile once via a 3-D tensor map; K and V of each union block page by
-//   page through the cache tensor map, 128B swizzle, 3-stage ring). Warp 1: one thread issues
+// * Warp 0: TMA producer (Q tile once via a 3-D tensor map; K and V of each union block with one
+//   8 KiB copy per page through a 5-D tensor map over the packed cache, 128B swizzle, 3-stage
+//   ring). A stage is [page][row half][quarter: K lo, K hi, V lo, V hi][8 rows][128 B], so every
+//   8-key group of K and of V sits 4 KiB after the previous one. Warp 1: one thread issues
 //   the tcgen05 MMAs. Warps 4-7: softmax and epilogue, thread i owning TMEM lane / row i.
 // * TMEM (512 columns): S double buffer (2 x 128, fp32), the O accumulator (128, fp32) and two
 //   64-column buffers for the low half of P. The high half of P (bf16, two keys per column)
@@ -46,7 +48,7 @@ constexpr int kQBytes = kRows * kHeadDim * 2;          // 32 KiB
 constexpr int kHalf = 128 * 128;                       // one 64-dim half of a 128 x 128 bf16 tile
 constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB
 constexpr int kKVBytes = 2 * kTileBytes;               // K then V
-constexpr int kStagesTc = 3;
+constexpr int kStagesTc = kSplit >= 4 ? 2 : 3;
 constexpr int kBigBytes = kQBytes + kStagesTc * kKVBytes;  // 224 KiB
 constexpr int kMaxUnion = 256;
 constexpr int kTcMaxTopk = 16;
@@ -79,6 +81,50 @@ constexpr size_t kTcSmem = 232448;  // the per-block opt-in maximum of sm_100-fa
 // follows them.
 static_assert(kBigBytes + sizeof(TcCtl) <= kTcSmem, "shared memory layout exceeds 227 KiB");
 
+#ifdef PBS_TRACE
+// Trace build only: one CTA records SM-clock timestamps of its pipeline events.
+constexpr int kTraceBlocks = 64;
+enum TraceEv { kEvStart, kEvSetup, kEvEpi, kEvEnd, kEvProdIssue0, kEvProdIssue1 = kEvProdIssue0 + kTraceBlocks,
+               kEvS = kEvProdIssue1 + kTraceBlocks, kEvPV = kEvS + kTraceBlocks,
+               kEvSoftIn = kEvPV + kTraceBlocks, kEvSoftMax = kEvSoftIn + kTraceBlocks,
+               kEvSoftOut = kEvSoftMax + kTraceBlocks, kEvCount = kEvSoftOut + kTraceBlocks };
+__device__ long long g_trace[kEvCount + 4];
+__device__ int g_trace_cta;
+#define TRACE(ev) do { if (blockIdx.x == static_cast<unsigned>(g_trace_cta) && blockIdx.y == 0 && (ev) < kEvCount) \
+                         g_trace[(ev)] = clock64(); } while (0)
+#else
+#define TRACE(ev) do { } while (0)
+#endif
+
+// p = 2^(s * sl2 - m) for the first `nval` of this thread's kW key columns (0 beyond), written
+// to TMEM as bf16 hi (over the thread's own S columns) and lo; returns the sum of p and the
+// maximum of the valid s.
+__device__ __forceinline__ float write_p(const uint32_t (&v)[kW], int nval, float sl2, float m, uint32_t t_hi,
+                                         uint32_t t_lo, float& smax) {
+  float psum = 0.f, mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < kW / 32; ++c) {
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const int k = 32 * c + j;
+      const float s0 = __uint_as_float(v[k]), s1 = __uint_as_float(v[k + 1]);
+      mx = fmaxf(mx, k < nval ? s0 : -INFINITY);
+      mx = fmaxf(mx, k + 1 < nval ? s1 : -INFINITY);
+      const float p0 = k < nval ? ex2(s0 * sl2 - m) : 0.f;
+      const float p1 = k + 1 < nval ? ex2(s1 * sl2 - m) : 0.f;
+      psum += p0 + p1;
+      const uint32_t hh = pack_bf16(p0, p1);
+      hi[j >> 1] = hh;
+      lo[j >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
+    }
+    tc::st16(t_hi + 16 * c, hi);
+    tc::st16(t_lo + 16 * c, lo);
+  }
+  smax = mx;
+  return psum;
+}
+
 __device__ __forceinline__ void quad_bar(int quad) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + quad), "r"(32 * kSplit) : "memory");
 }
@@ -88,6 +134,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2, int c3,
+                                            int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
 
@@ -131,6 +186,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
+  if (threadIdx.x == 0) TRACE(kEvStart);
 
   // ---- tile -> (request, first token): tiles are numbered request by request ----------------
   if (warp == 0) {
@@ -273,36 +329,47 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc::fence_after_sync();
   const int nU = ctl->n_union;
+  if (threadIdx.x == 0) TRACE(kEvSetup);
   const uint32_t tmem = ctl->tmem_base;
   const uint32_t tm_s0 = tmem, tm_o = tmem + 256, tm_plo = tmem + 384;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // One 8 KiB copy per page (K and V of this kv head); lanes 0..7 issue the 8 pages of a block.
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
       mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
       tma_load_3d(q_s, &q_map, &ctl->q_full, 0, g * kG, t0);
       tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, g * kG, t0);
-      const int32_t* bt_row = a.page_table + static_cast<int64_t>(req) * a.pt_row_stride;
-      int next_phys = nU > 0 ? __ldg(bt_row + ctl->union_blk[0]) : 0;
-      int issued = 0;
-      for (int i = 0; i < nU; ++i) {
-        const int st = i % kStagesTc;
-        const int phys = next_phys;
-        if (i + 1 < nU) next_phys = __ldg(bt_row + ctl->union_blk[i + 1]);
-        if (i >= kStagesTc && !wait_or_abort(&ctl->kv_empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word)) break;
-        if (aborted(ctl)) break;
-        const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
-        if (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-        uint8_t* dst = kv_s + st * kKVBytes;
-        mbar_arrive_expect_tx(&ctl->kv_full[st], kKVBytes);
-        for (int j = 0; j < kPagesPerBlock; ++j) {
-          const int page = static_cast<int>(base) + j;  // out-of-range pages read as zeros (TMA bounds)
-#pragma unroll
-          for (int part = 0; part < 4; ++part)  // K dims 0-63, K 64-127, V 0-63, V 64-127
-            tma_load_4d(dst + part * kHalf + j * 2048, &kv_map, &ctl->kv_full[st], 64 * part, 0, g, page);
-        }
-        issued = i + 1;
-      }
+    }
+    const int32_t* bt_row = a.page_table + static_cast<int64_t>(req) * a.pt_row_stride;
+    int next_phys = nU > 0 ? __ldg(bt_row + ctl->union_blk[0]) : 0;
+    int issued = 0;
+    for (int i = 0; i < nU; ++i) {
+      const int st = i % kStagesTc;
+      const int phys = next_phys;
+      if (i + 1 < nU) next_phys = __ldg(bt_row + ctl->union_blk[i + 1]);
+      bool go = true;
+      if (lane == 0 && i >= kStagesTc)
+        go = wait_or_abort(&ctl->kv_empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word);
+      if (lane == 0) go = go && !aborted(ctl);
+      go = __shfl_sync(0xffffffffu, go, 0);
+      if (!go) break;
+      const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
+      if (lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages)) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+      uint8_t* dst = kv_s + st * kKVBytes;
+      TRACE(kEvProdIssue0 + i);
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[st], kKVBytes);
+      __syncwarp();
+      // out-of-range pages read as zeros (TMA bounds)
+      if (lane < kPagesPerBlock)
+        tma_load_5d(dst + lane * 8192, &kv_map, &ctl->kv_full[st], 0, 0, 0, 0,
+                    static_cast<int>((base + lane) * a.num_kv_heads + g));
+      TRACE(kEvProdIssue1 + i);
+      issued = i + 1;
+    }
+    if (lane == 0) {
       for (int i = max(0, issued - kStagesTc); i < issued; ++i)
         if (!mbar_wait_bounded(&ctl->kv_full[i % kStagesTc], (i / kStagesTc) & 1, kTcWaitNs))
           set_err(a.err_word, PBS_DEVERR_TIMEOUT);
@@ -325,18 +392,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const uint32_t k_addr = smem_u32(kv_s + st * kKVBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-            tc::mma_ss(tm_s0 + (i & 1) * 128, tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                       tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS, ks > 0);
+            // dims 16ks..: Q half ks/4 (16 KiB apart, 8-row groups 1 KiB apart); K quarter ks/4
+            // (1 KiB apart, 8-key groups 4 KiB apart)
+            tc::mma_ss(tm_s0 + (i & 1) * 128,
+                       tc::smem_desc_sw128(q_addr + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024),
+                       tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 4096), kIdescS,
+                       ks > 0);
           }
           tc::commit(&ctl->s_full[i & 1]);
+          TRACE(kEvS + i);
         }
         if (i >= 1) {
           // O += P(j) V(j): P hi in the first 64 columns of S buffer j&1, P lo in its own buffer
           const int j = i - 1, st = j % kStagesTc;
           if (!wait_or_abort(&ctl->p_full[j & 1], (j >> 1) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
-          const uint32_t v_addr = smem_u32(kv_s + st * kKVBytes + kTileBytes);
+          const uint32_t v_addr = smem_u32(kv_s + st * kKVBytes) + 2 * 1024;  // quarters 2, 3 = V
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -346,11 +417,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               const int owner = (16 * ks) / kW;
               const uint32_t pa = part == 0 ? tm_s0 + (j & 1) * 128 + owner * kW + (16 * ks - owner * kW) / 2
                                             : tm_plo + (j & 1) * 64 + 8 * ks;
-              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
+              // keys 16ks..16ks+15 = two 8-key groups (4 KiB apart) from key group 2ks; dims in
+              // two 64-wide MN atoms 1 KiB apart
+              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 8192, 1024, 4096), kIdescPV,
                          !(j == 0 && part == 0 && ks == 0));
             }
           }
           tc::commit(&ctl->pv_done[j & 1]);
+          TRACE(kEvPV + j);
           tc::commit(&ctl->kv_empty[st]);
           issued_pv = j + 1;
         }
@@ -387,13 +461,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int lim = b == own_t ? lim_t : kSparseBlock;
       if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (i >> 1) & 1, ctl, a.err_word)) ok = false;
       tc::fence_after_sync();
+      if (sw == 0 && lane == 0) TRACE(kEvSoftIn + i);
       // rows past the request's last token in its last block may hold anything: zero that V
       if (b == last_blk && last_rows < kSparseBlock) {
         if (ok && !warp_wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) ok = false;
-        const uint32_t v_base = smem_u32(kv_s + st * kKVBytes + kTileBytes);
+        const uint32_t v_base = smem_u32(kv_s + st * kKVBytes);
         for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
-          const int key = last_rows + (e >> 4), vp = (e >> 3) & 1, chunk = e & 7;
-          sts128(v_base + vp * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
+          const int key = last_rows + (e >> 4), vq = 2 + ((e >> 3) & 1), chunk = e & 7;
+          // key = 16 page + 8 half + row
+          sts128(v_base + (key >> 3) * 4096 + vq * 1024 + (key & 7) * 128 + chunk * 16, 0, 0, 0, 0);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
@@ -407,55 +483,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int c = 0; c < kW / 32; ++c) tc::ld32(ts + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
         tc::wait_ld();
+        const int nval = active ? min(max(lim - col0, 0), kW) : 0;  // valid keys among my columns
+        // P with the running reference (the common case), and this part's maximum
         float pm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kW; ++j)
-          if (active && col0 + j < lim) pm = fmaxf(pm, __uint_as_float(v[j]));
+        float psum = write_p(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, pm);
         ctl->xchg[part][row] = pm;
         quad_bar(quad);
         float mx = pm;
 #pragma unroll
         for (int q = 0; q < kSplit; ++q) mx = fmaxf(mx, ctl->xchg[q][row]);
         quad_bar(quad);  // every part has read before the next block overwrites
+        if (sw == 0 && lane == 0) TRACE(kEvSoftMax + i);
         mx *= sl2;
+        // the reference moves only when the row maximum passes it by 2^8 (or on the row's first
+        // block); then O is rescaled and this block's P recomputed
         const bool grow = active && (m_ref == -INFINITY || mx > m_ref + kRescaleLog2);
-        const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
-        const bool resc = grow && l > 0.f;
-        const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
-        if (__any_sync(0xffffffffu, resc)) {
-          // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
-          if (ok && i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl, a.err_word))
-            ok = false;
-          tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
+          const bool resc = grow && l > 0.f;
+          const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+          if (__any_sync(0xffffffffu, resc)) {
+            // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
+            if (ok && i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl, a.err_word))
+              ok = false;
+            tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < kW / 32; ++c) {
-            uint32_t o[32];
-            tc::ld32(tm_o + lane_off + col0 + 32 * c, o);
-            tc::wait_ld();
+            for (int c = 0; c < kW / 32; ++c) {
+              uint32_t o[32];
+              tc::ld32(tm_o + lane_off + col0 + 32 * c, o);
+              tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tc::st32(tm_o + lane_off + col0 + 32 * c, o);
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tc::st32(tm_o + lane_off + col0 + 32 * c, o);
+            }
           }
+          l *= alpha;
+          m_ref = m_new;
+          float unused;
+          psum = write_p(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, unused);
         }
-        l *= alpha;
-        m_ref = m_new;
-#pragma unroll
-        for (int c = 0; c < kW / 32; ++c) {
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int key = col0 + 32 * c + j;
-            const float p0 = (active && key < lim) ? ex2(__uint_as_float(v[32 * c + j]) * sl2 - m_ref) : 0.f;
-            const float p1 = (active && key + 1 < lim) ? ex2(__uint_as_float(v[32 * c + j + 1]) * sl2 - m_ref) : 0.f;
-            l += p0 + p1;
-            const uint32_t hh = pack_bf16(p0, p1);
-            hi[j >> 1] = hh;
-            lo[j >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
-          }
-          // P hi over the first half of this part's own S columns (all already in registers)
-          tc::st16(ts + col0 + 16 * c, hi);
-          tc::st16(tplo + col0 / 2 + 16 * c, lo);
-        }
+        l += psum;
       } else {
         uint32_t z[16];
 #pragma unroll
@@ -470,7 +537,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
+      if (sw == 0 && lane == 0) TRACE(kEvSoftOut + i);
     }
+    if (sw == 0 && lane == 0) TRACE(kEvEpi);
     // ---- epilogue: O / l -> bf16 (row sum combined over the parts of the quadrant)
     if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(nU - 1) & 1], ((nU - 1) >> 1) & 1, ctl, a.err_word))
       ok = false;
@@ -514,12 +583,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc::fence_after_sync();
     tc::dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) TRACE(kEvEnd);
 }
 
 }  // namespace
 
+#ifdef PBS_TRACE
+}  // namespace pbs
+// Trace build only: choose the traced CTA, and copy the timestamps out (host buffer of
+// kEvCount int64). Not part of the C ABI.
+extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_set(int cta) {
+  return cudaMemcpyToSymbol(pbs::g_trace_cta, &cta, sizeof(int)) == cudaSuccess ? 0 : 5;
+}
+extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_get(long long* host, int n) {
+  if (n > pbs::kEvCount) n = pbs::kEvCount;
+  return cudaMemcpyFromSymbol(host, pbs::g_trace, sizeof(long long) * n) == cudaSuccess ? 0 : 5;
+}
+namespace pbs {
+#endif
+
 bool prefill_tc_supported(const AttendArgs& a) {
   return a.kv_dtype == PBS_KV_BF16 && a.group == kG && a.k <= kTcMaxTopk && a.max_blocks <= 65536 &&
+         a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
+         a.num_pages * a.num_kv_heads <= 0x7fffffffLL &&
          a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
          reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 &&
          reinterpret_cast<uintptr_t>(a.q) % 16 == 0;

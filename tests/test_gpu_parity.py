@@ -290,8 +290,7 @@ PREFILL_CASES = [
 @pytest.mark.parametrize("kernel", ["tc", "token"])
 @pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
 def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, monkeypatch):
-    if kernel == "token":
-        monkeypatch.setenv("PBS_PREFILL_KERNEL", "token")
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, seed=41 + ci, **PREFILL_CASES[ci])
     err = _err()
     got = gpu_attend(pbs, b, "pre", err)
@@ -299,8 +298,9 @@ def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, monkeypatch):
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", f"prefill {kernel} case {ci}")
 
 
-def test_prefill_tc_duplicate_ids_count_once(pbs):
+def test_prefill_tc_duplicate_ids_count_once(pbs, monkeypatch):
     """The tile kernel reads each selected block once per token, the attend's set reading."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=6, pre_q_lens=[300], pre_ctx_lens=[400],
                         seed=45)
     tk = b.pre.topk.clone()
@@ -312,7 +312,8 @@ def test_prefill_tc_duplicate_ids_count_once(pbs):
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill duplicates")
 
 
-def test_prefill_tc_ignores_nan_past_last_token(pbs):
+def test_prefill_tc_ignores_nan_past_last_token(pbs, monkeypatch):
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, pre_q_lens=[77, 200], pre_ctx_lens=[0, 50],
                         seed=46)
     p = b.pre
