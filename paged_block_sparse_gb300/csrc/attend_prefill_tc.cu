@@ -98,22 +98,37 @@ __device__ int g_trace_cta;
 
 // p = 2^(s * sl2 - m) for the first `nval` of this thread's kW key columns (0 beyond), written
 // to TMEM as bf16 hi (over the thread's own S columns) and lo; returns the sum of p and the
-// maximum of the valid s.
+// maximum of the valid s. `prefix` = some lane of the warp has a partly valid range (the own
+// block), so keys are masked one by one; otherwise every lane has all or none of its keys
+// valid, and a lane with none gets m = +inf (p = 0) and maximum -inf. The caller skips warps in
+// which no lane has a valid key, so on the unmasked path every column holds a written key row.
+template <bool kPrefix>
 __device__ __forceinline__ float write_p(const uint32_t (&v)[kW], int nval, float sl2, float m, uint32_t t_hi,
                                          uint32_t t_lo, float& smax) {
-  float psum = 0.f, mx = -INFINITY;
+  float psum0 = 0.f, psum1 = 0.f, mx = -INFINITY;
+  const float mu = (!kPrefix && nval == 0) ? INFINITY : m;
 #pragma unroll
   for (int c = 0; c < kW / 32; ++c) {
     uint32_t hi[16], lo[16];
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
       const int k = 32 * c + j;
-      const float s0 = __uint_as_float(v[k]), s1 = __uint_as_float(v[k + 1]);
-      mx = fmaxf(mx, k < nval ? s0 : -INFINITY);
-      mx = fmaxf(mx, k + 1 < nval ? s1 : -INFINITY);
-      const float p0 = k < nval ? ex2(s0 * sl2 - m) : 0.f;
-      const float p1 = k + 1 < nval ? ex2(s1 * sl2 - m) : 0.f;
-      psum += p0 + p1;
+      float s0 = __uint_as_float(v[k]), s1 = __uint_as_float(v[k + 1]);
+      float p0, p1;
+      if (kPrefix) {
+        // columns past the valid range may hold anything (rows beyond the last token): select
+        // on the results, never compute with them
+        s0 = k < nval ? s0 : -INFINITY;
+        s1 = k + 1 < nval ? s1 : -INFINITY;
+        p0 = k < nval ? ex2(fmaf(s0, sl2, -mu)) : 0.f;
+        p1 = k + 1 < nval ? ex2(fmaf(s1, sl2, -mu)) : 0.f;
+      } else {
+        p0 = ex2(fmaf(s0, sl2, -mu));
+        p1 = ex2(fmaf(s1, sl2, -mu));
+      }
+      mx = fmaxf(mx, fmaxf(s0, s1));
+      psum0 += p0;
+      psum1 += p1;
       const uint32_t hh = pack_bf16(p0, p1);
       hi[j >> 1] = hh;
       lo[j >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
@@ -121,8 +136,19 @@ __device__ __forceinline__ float write_p(const uint32_t (&v)[kW], int nval, floa
     tc::st16(t_hi + 16 * c, hi);
     tc::st16(t_lo + 16 * c, lo);
   }
-  smax = mx;
-  return psum;
+  smax = (!kPrefix && nval == 0) ? -INFINITY : mx;
+  return psum0 + psum1;
+}
+
+__device__ __forceinline__ void zero_p(uint32_t t_hi, uint32_t t_lo) {
+  uint32_t z[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) z[j] = 0u;
+#pragma unroll
+  for (int c = 0; c < kW / 32; ++c) {
+    tc::st16(t_hi + 16 * c, z);
+    tc::st16(t_lo + 16 * c, z);
+  }
 }
 
 __device__ __forceinline__ void quad_bar(int quad) {
@@ -449,6 +475,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int last_blk = pos_last / kSparseBlock;
     const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
     float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
+    bool started = false;              // the row has had an active block (same in every part)
     int ptr = 0;
     bool ok = true;
     // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
@@ -478,15 +505,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
       // take part in this block are masked arithmetically (their P row becomes zero). Activity
       // depends only on the row, so the kSplit warps of a quadrant always agree.
+      // Activity depends only on the row, so both warps of a quadrant take the same branches
+      // around the named barriers below.
       if (__any_sync(0xffffffffu, active)) {
-        uint32_t v[kW];
-#pragma unroll
-        for (int c = 0; c < kW / 32; ++c) tc::ld32(ts + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-        tc::wait_ld();
         const int nval = active ? min(max(lim - col0, 0), kW) : 0;  // valid keys among my columns
-        // P with the running reference (the common case), and this part's maximum
-        float pm = -INFINITY;
-        float psum = write_p(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, pm);
+        // a part whose columns hold no valid key (they may lie past the last token) writes zeros
+        const bool any_valid = __any_sync(0xffffffffu, nval > 0);
+        uint32_t v[kW];
+        bool prefix = false;
+        float pm = -INFINITY, psum = 0.f;
+        if (any_valid) {
+#pragma unroll
+          for (int c = 0; c < kW / 32; ++c) tc::ld32(ts + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+          tc::wait_ld();
+          prefix = __any_sync(0xffffffffu, nval != 0 && nval != kW);
+          // P with the running reference (the common case), and this part's maximum
+          psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, pm)
+                        : write_p<false>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, pm);
+        } else {
+          zero_p(ts + col0, tplo + col0 / 2);
+        }
         ctl->xchg[part][row] = pm;
         quad_bar(quad);
         float mx = pm;
@@ -500,7 +538,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const bool grow = active && (m_ref == -INFINITY || mx > m_ref + kRescaleLog2);
         if (__any_sync(0xffffffffu, grow)) {
           const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
-          const bool resc = grow && l > 0.f;
+          // O's dim columns hold contributions of every key part once the row has started
+          const bool resc = grow && started;
           const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
           if (__any_sync(0xffffffffu, resc)) {
             // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
@@ -519,19 +558,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           }
           l *= alpha;
           m_ref = m_new;
-          float unused;
-          psum = write_p(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, unused);
+          if (any_valid) {
+            float unused;
+            psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, unused)
+                          : write_p<false>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, unused);
+          }
         }
         l += psum;
+        started = started || active;
       } else {
-        uint32_t z[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] = 0u;
-#pragma unroll
-        for (int c = 0; c < kW / 32; ++c) {
-          tc::st16(ts + col0 + 16 * c, z);
-          tc::st16(tplo + col0 / 2 + 16 * c, z);
-        }
+        zero_p(ts + col0, tplo + col0 / 2);
       }
       tc::wait_st();
       tc::fence_before_sync();
