@@ -25,7 +25,8 @@
  * Conventions for every entry point
  * ---------------------------------
  * - All pointers are DEVICE pointers owned by the caller, unless stated otherwise.
- *   The library allocates no memory and keeps no state between calls.
+ *   The library allocates no memory and keeps no state between calls (an optional caller-owned
+ *   workspace carries split partials within a call).
  * - Work is enqueued on `stream` (NULL = legacy default stream) and is
  *   asynchronous; the return value only reports what the host could check
  *   plus launch errors. Faults found by the kernels themselves are OR-ed into
@@ -92,6 +93,20 @@ PBS_API const char* pbs_status_string(int status);
 PBS_API int pbs_abi_version(void);
 
 /*
+ * Bytes of the optional workspace of pbs_sparse_decode_attention / pbs_sparse_prefill_attention
+ * for `num_rows` query rows (decode rows or prefill tokens) and `num_kv_heads` kv heads.
+ * No counterpart on the pages: with a workspace, a row x kv-head split into chunks merges
+ * through it (the last chunk to finish merges the others' partials) instead of through a
+ * thread-block cluster, which keeps the block scheduler free to balance the tail. The caller
+ * owns it (16-byte aligned) and zeroes it once before first use. Partials are written from its
+ * front, one int32 arrival ticket per (row, kv head) sits in its last bytes; every completed call
+ * leaves its tickets zero again, so the buffer serves any later call that fits it without
+ * re-zeroing (after a PBS_DEVERR_TIMEOUT, zero it again). Calls that share one workspace must
+ * not run concurrently.
+ */
+PBS_API size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_kv_heads);
+
+/*
  * Sparse block table, decode ([sparse_pa] minimax_m3_build_sparse_block_table_decode and
  * _write_sparse_block_table_row_from_values; positions right-aligned per [flashinfer] forward).
  *
@@ -150,6 +165,7 @@ PBS_API int pbs_build_sparse_block_table_prefill(
  *               kernel folds k_scale into the softmax scale and v_scale into the output.
  *   out         [num_rows, num_heads, head_dim] bf16, strides out_row_stride / out_head_stride.
  *               A row that attends no key gets zeros.
+ *   workspace   optional (NULL, 0): see pbs_attend_workspace_bytes; too small -> PBS_ERR_SHAPE.
  */
 PBS_API int pbs_sparse_decode_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -160,12 +176,15 @@ PBS_API int pbs_sparse_decode_attention(
     const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
     float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
+    void* workspace, size_t workspace_bytes,
     int32_t* err_word, pbs_stream_t stream);
 
 /*
  * Sparse prefill attention, varlen ([flashinfer] msa_sparse_attention call with cu_seqlens_q;
  * [nvfp4] minimax_m3_nvfp4_sparse_prefill call). Token positions as in
  * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention.
+ * Shapes the tcgen05 tile kernel takes (bf16 packed cache, GQA 8, top-k <= 16, 16-byte aligned q
+ * and out rows) ignore the workspace.
  */
 PBS_API int pbs_sparse_prefill_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -176,6 +195,7 @@ PBS_API int pbs_sparse_prefill_attention(
     const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs, int32_t total_q,
     int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
+    void* workspace, size_t workspace_bytes,
     int32_t* err_word, pbs_stream_t stream);
 
 /*

@@ -20,6 +20,7 @@ __all__ = [
     "PbsError", "KV_DTYPES", "SPARSE_BLOCK_SIZE", "PAGES_PER_BLOCK", "PAGE_ROWS", "library_path", "lib",
     "abi_version", "status_string", "build_sparse_block_table_decode", "build_sparse_block_table_prefill",
     "sparse_decode_attention", "sparse_prefill_attention", "insert_index_cache", "DEVERR",
+    "attend_workspace_bytes", "attend_workspace",
 ]
 
 SPARSE_BLOCK_SIZE = 128
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
     L.pbs_status_string.argtypes = [ctypes.c_int]
     L.pbs_abi_version.restype = ctypes.c_int
     L.pbs_abi_version.argtypes = []
+    L.pbs_attend_workspace_bytes.restype = ctypes.c_size_t
+    L.pbs_attend_workspace_bytes.argtypes = [i64, i32]
     table_common = [vp, i64, i32, i32, vp, i64, i32]
     L.pbs_build_sparse_block_table_decode.restype = ctypes.c_int
     L.pbs_build_sparse_block_table_decode.argtypes = table_common + [vp, i32, i32, i32, vp, i64, vp, vp, vp]
@@ -64,10 +67,11 @@ def lib() -> ctypes.CDLL:
     L.pbs_build_sparse_block_table_prefill.argtypes = table_common + [vp, vp, i32, i32, vp, i64, vp, vp, vp]
     attend_head = [vp, i64, i64, vp, i64, i64, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32]
     L.pbs_sparse_decode_attention.restype = ctypes.c_int
-    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp, vp]
+    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp,
+                                                            ctypes.c_size_t, vp, vp]
     L.pbs_sparse_prefill_attention.restype = ctypes.c_int
     L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
-                                                             vp, vp]
+                                                             vp, ctypes.c_size_t, vp, vp]
     L.pbs_insert_index_cache.restype = ctypes.c_int
     L.pbs_insert_index_cache.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32, vp, i64, i32, vp, vp]
     del sz
@@ -209,20 +213,63 @@ def _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     return num_pages, page_stride_bytes, tk, pt, out
 
 
+def attend_workspace_bytes(num_rows: int, num_kv_heads: int) -> int:
+    """Bytes of the optional split-merge workspace for ``num_rows`` query rows."""
+    return int(lib().pbs_attend_workspace_bytes(int(num_rows), int(num_kv_heads)))
+
+
+_workspaces: dict = {}
+
+
+def attend_workspace(num_rows: int, num_kv_heads: int, device, stream=None) -> torch.Tensor:
+    """A zeroed workspace for the attends, cached per (device, stream) and grown on demand.
+
+    Calls that share one workspace must not overlap, so the cache is keyed by stream: calls on
+    one stream run in order. Every completed call leaves the workspace's ticket words zero."""
+    device = torch.device(device)
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device.index, s.cuda_stream)
+    need = attend_workspace_bytes(num_rows, num_kv_heads)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _workspace_args(workspace, rows, num_kv_heads, device, stream):
+    """(pointer, bytes) for the C call: "auto" takes the cached workspace, None passes none."""
+    if workspace is None:
+        return None, 0
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
+        workspace = attend_workspace(rows, num_kv_heads, device, stream)
+    _dev(workspace, "workspace", torch.uint8)
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    return _ptr(workspace), workspace.numel()
+
+
 def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
                             decode_query_len: int, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
-                            block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None):
+                            block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
+                            workspace="auto"):
     """Sparse decode attend (vLLM flashinfer msa_sparse_decode_attention / nvfp4 decode call).
 
     q [rows, Hq, 128] bf16 with rows = batch * decode_query_len; kv_cache [num_pages, ...] in the
-    ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16."""
+    ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16. ``workspace``: "auto" (a cached
+    per-stream buffer), None (splits merge inside a thread-block cluster) or a zeroed uint8
+    tensor of at least ``attend_workspace_bytes(rows, num_kv_heads)`` bytes."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
+    wp, wb = _workspace_args(workspace, q.shape[0], num_kv_heads, q.device, stream)
     st = lib().pbs_sparse_decode_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
         _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), float(softmax_scale),
-        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(err_word),
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), wp, wb, _ptr(err_word),
         _stream(stream, q.device))
     _check(st, "pbs_sparse_decode_attention")
     return out
@@ -230,16 +277,19 @@ def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk,
 
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
-                             block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None):
-    """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call)."""
+                             block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
+                             workspace="auto"):
+    """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
+    ``workspace`` as in :func:`sparse_decode_attention`."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
+    wp, wb = _workspace_args(workspace, q.shape[0], num_kv_heads, q.device, stream)
     st = lib().pbs_sparse_prefill_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
         _ptr(cu), _ptr(sl), sl.shape[0], q.shape[0], int(block_page_stride), float(softmax_scale), float(k_scale),
-        float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(err_word), _stream(stream, q.device))
+        float(v_scale), _ptr(out), out.stride(0), out.stride(1), wp, wb, _ptr(err_word), _stream(stream, q.device))
     _check(st, "pbs_sparse_prefill_attention")
     return out
 

@@ -69,23 +69,44 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
-// The packed bf16 cache as seen by the prefill tile kernel: one (page, kv head) chunk of
-// 16 rows x 512 B as a 5-D box {64 elements, 8 rows, 4 quarters (K lo, K hi, V lo, V hi),
-// 2 row halves, page * Hkv + head}; the box lands as [half][quarter][8 rows][128 B], i.e.
-// 128B-swizzle atoms of 8 rows per quarter. Every address stays inside its own 8 KiB chunk.
-// Needs page_stride_bytes == Hkv * 8192 (pages packed back to back).
-int encode_cache_map_tc(CUtensorMap* map, const void* cache, int num_kv_heads, int64_t num_pages) {
+// A packed cache (pages back to back: page stride = Hkv * 16 rows * row bytes) as one box per
+// (page, kv head): a 5-D map {row bytes' first 128 B, 8 rows, q, 2 row halves, page * Hkv + head}
+// whose box lands as [row half][q][8 rows][128 B], q = the four 64-element quarters of a bf16 row
+// (K lo, K hi, V lo, V hi) or the two halves of an fp8 row (K, V): 128B-swizzle atoms of 8 rows.
+// Every address stays inside its own (page, head) chunk. PBS_CACHE_MAP=4d disables it (tests).
+int encode_cache_map_packed(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
+                            int64_t page_stride_bytes) {
   std::memset(map, 0, sizeof(*map));
+  if (kv_dtype != PBS_KV_BF16 && kv_dtype != PBS_KV_FP8_E4M3) return PBS_ERR_UNSUPPORTED;
+  if (page_stride_bytes != page_content_bytes(kv_dtype, num_kv_heads)) return PBS_ERR_UNSUPPORTED;
+  if (num_pages * num_kv_heads > 0x7fffffffLL) return PBS_ERR_UNSUPPORTED;
+  if (const char* env = std::getenv("PBS_CACHE_MAP"))
+    if (std::strcmp(env, "4d") == 0) return PBS_ERR_UNSUPPORTED;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return PBS_ERR_CUDA;
-  const cuuint64_t dims[5] = {64, 8, 4, 2, static_cast<cuuint64_t>(num_pages) * num_kv_heads};
-  const cuuint64_t strides[4] = {512, 128, 4096, 8192};
-  const cuuint32_t box[5] = {64, 8, 4, 2, 1};
+  const bool bf = kv_dtype == PBS_KV_BF16;
+  const cuuint64_t row = bf ? 512 : 256;  // bytes per page row of one head
+  const cuuint64_t nq = bf ? 4 : 2;
+  const cuuint64_t dims[5] = {bf ? 64u : 128u, 8, nq, 2, static_cast<cuuint64_t>(num_pages) * num_kv_heads};
+  const cuuint64_t strides[4] = {row, 128, 8 * row, 16 * row};
+  const cuuint32_t box[5] = {bf ? 64u : 128u, 8, static_cast<cuuint32_t>(nq), 2, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = enc(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                         const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
+}
+
+// The tensor map the token-centric kernel reads: the packed one when the cache allows it.
+int encode_attend_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
+                      int64_t page_stride_bytes, int32_t* packed) {
+  *packed = 0;
+  if (encode_cache_map_packed(map, cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes) == PBS_OK) {
+    *packed = 1;
+    return PBS_OK;
+  }
+  return encode_cache_map(map, cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
 }
 
 // Queries as a 3-D tensor {head_dim, heads, tokens}; a box is 16 tokens x 8 heads x 64 dims, laid
@@ -124,17 +145,46 @@ int prefill_kernel_override() {
 // So rows are split only while the units alone cannot fill every SM twice, and only while
 // each split keeps at least four 128-key slots. PBS_ATTEND_SPLITS in {1, 2, 4, 8} overrides
 // (tuning and tests).
-int choose_splits(int64_t units, int k) {
+//
+// With a workspace the splits merge through it instead (no cluster, no waiting: the last chunk
+// of a row merges), so any split count up to 8 schedules freely; a row is cut into chunks while
+// the chunks still fit one wave of resident CTAs (4 per SM), keeping at least two 128-key slots
+// per chunk. More than one wave loses more to per-CTA start-up than it gains in balance.
+int num_sms() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+int choose_splits(int64_t units, int k, bool workspace) {
   if (const char* env = std::getenv("PBS_ATTEND_SPLITS")) {
     const int s = std::atoi(env);
     if (s == 1 || s == 2 || s == 4 || s == 8) return s;
   }
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t target = static_cast<int64_t>(sms) * 2;
+  const int64_t sms = num_sms();
   int s = 1;
-  while (s < 8 && units * s < target && 4 * (2 * s) <= k) s *= 2;
+  if (workspace) {
+    while (s < pbs::kMaxSplits && units * (2 * s) <= 4 * sms && 2 * (2 * s) <= k) s *= 2;
+  } else {
+    while (s < 8 && units * s < 2 * sms && 4 * (2 * s) <= k) s *= 2;
+  }
   return s;
+}
+
+// A workspace (optional) lets splits merge through global memory. It must hold
+// attend_workspace_bytes(units) bytes, 16-byte aligned. Partials fill it from the front, the
+// per-unit tickets sit at its very end: a call of any size that fits the buffer writes partials
+// only below the ticket words of every other call that fits it, so one zeroing of the buffer
+// serves calls of all sizes (each completed call leaves its tickets zero).
+int attach_workspace(AttendArgs* a, int64_t units, void* workspace, size_t workspace_bytes) {
+  a->split_ws = nullptr;
+  a->split_tickets = nullptr;
+  if (workspace == nullptr) return workspace_bytes == 0 ? PBS_OK : PBS_ERR_ARG;
+  if (!aligned(workspace, 16)) return PBS_ERR_ALIGN;
+  if (workspace_bytes < pbs::attend_workspace_bytes(units)) return PBS_ERR_SHAPE;
+  a->split_ws = static_cast<float*>(workspace);
+  a->split_tickets = static_cast<int32_t*>(workspace) + (workspace_bytes / sizeof(int32_t) - static_cast<size_t>(units));
+  return PBS_OK;
 }
 
 int check_common_table(const int32_t* topk, int64_t topk_row_stride, int32_t topk_k, const int32_t* page_table,
@@ -223,7 +273,12 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 1; }
+int pbs_abi_version(void) { return 2; }
+
+size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_kv_heads) {
+  if (num_rows <= 0 || num_kv_heads <= 0) return 0;
+  return pbs::attend_workspace_bytes(num_rows * num_kv_heads);
+}
 
 int pbs_build_sparse_block_table_decode(const int32_t* topk, int64_t topk_row_stride, int32_t num_rows,
                                         int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride,
@@ -297,8 +352,8 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                 int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
                                 const int32_t* seq_lens, int32_t batch, int32_t decode_query_len,
                                 int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
-                                void* out, int64_t out_row_stride, int64_t out_head_stride, int32_t* err_word,
-                                pbs_stream_t stream) {
+                                void* out, int64_t out_row_stride, int64_t out_head_stride, void* workspace,
+                                size_t workspace_bytes, int32_t* err_word, pbs_stream_t stream) {
   if (batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
   const int64_t rows = static_cast<int64_t>(batch) * decode_query_len;
   if (rows == 0) return PBS_OK;
@@ -316,9 +371,11 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                   out_row_stride, out_head_stride, err_word);
   a.decode_query_len = decode_query_len;
   a.num_rows = static_cast<int32_t>(rows);
-  a.splits = choose_splits(rows * num_kv_heads, topk_k);
+  st = attach_workspace(&a, rows * num_kv_heads, workspace, workspace_bytes);
+  if (st != PBS_OK) return st;
+  a.splits = choose_splits(rows * num_kv_heads, topk_k, a.split_ws != nullptr);
   CUtensorMap map;
-  st = encode_cache_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
   return pbs::launch_attend(a, false, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
                                                                                                   : PBS_ERR_CUDA;
@@ -331,7 +388,7 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
                                  const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs,
                                  int32_t total_q, int32_t block_page_stride, float softmax_scale, float k_scale,
                                  float v_scale, void* out, int64_t out_row_stride, int64_t out_head_stride,
-                                 int32_t* err_word, pbs_stream_t stream) {
+                                 void* workspace, size_t workspace_bytes, int32_t* err_word, pbs_stream_t stream) {
   if (total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
   if (total_q == 0) return PBS_OK;
   if (num_reqs == 0) return PBS_ERR_SHAPE;
@@ -350,21 +407,22 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   a.cu_seqlens_q = cu_seqlens_q;
   a.num_reqs = num_reqs;
   a.num_rows = total_q;
-  a.splits = choose_splits(static_cast<int64_t>(total_q) * num_kv_heads, topk_k);
+  st = attach_workspace(&a, static_cast<int64_t>(total_q) * num_kv_heads, workspace, workspace_bytes);
+  if (st != PBS_OK) return st;
+  a.splits = choose_splits(static_cast<int64_t>(total_q) * num_kv_heads, topk_k, a.split_ws != nullptr);
   CUtensorMap map;
-  st = encode_cache_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
   cudaError_t e;
-  CUtensorMap tcmap;
   const int force = prefill_kernel_override();
-  const bool tc_ok = force != 1 && pbs::prefill_tc_supported(a) &&
-                     encode_cache_map_tc(&tcmap, kv_cache, num_kv_heads, num_pages) == PBS_OK;
+  // the tile kernel reads the packed bf16 cache through the 5-D map
+  const bool tc_ok = force != 1 && a.packed_map != 0 && pbs::prefill_tc_supported(a);
   if (force == 2 && !tc_ok) return PBS_ERR_UNSUPPORTED;
   if (tc_ok) {
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
-    e = pbs::launch_prefill_tc(a, tcmap, qmap, reinterpret_cast<cudaStream_t>(stream));
+    e = pbs::launch_prefill_tc(a, map, qmap, reinterpret_cast<cudaStream_t>(stream));
   } else {
     e = pbs::launch_attend(a, true, map, reinterpret_cast<cudaStream_t>(stream));
   }

@@ -35,13 +35,16 @@ namespace cg = cooperative_groups;
 namespace pbs {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+// 3 consumer warps + 1 producer (128 threads, <= 128 registers) and the merge buffer aliased
+// onto the drained stages keep a CTA near 50 KB, so 4 CTAs fit on an SM and a 64-request batch
+// (512 row x kv-head CTAs) runs in a single wave.
+constexpr int kConsumerWarps = 3;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // Page p goes to stage p % kStages and to consumer warp p % kConsumerWarps. With kStages a
 // multiple of kConsumerWarps every stage is always consumed by the same warp, one phase after
 // the other, so a parity wait can never be answered by a phase two steps behind (with 6 stages
 // and 4 warps a warp would skip every other phase of a stage and could pass its wait early).
-constexpr int kStages = 8;
+constexpr int kStages = 6;
 static_assert(kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
 constexpr int kTileHeads = 8;  // the n8 tile of the MMA: up to 8 query heads per kv head
 
@@ -60,6 +63,20 @@ struct StageBytes<PBS_KV_NVFP4> {  // K slot (1152 B) then V slot (1152 B), as s
   static constexpr int v = 2304;
 };
 constexpr int kNvfp4Slot = 1152;
+// Workspace partial of one chunk: O [8 heads][128] then m[8], l[8] (floats).
+constexpr int kWsPartial = 8 * 128 + 16;
+
+// Byte offset of the 128-byte line holding page row r (0..15), quarter q of a bf16 row (K lo,
+// K hi, V lo, V hi) or half q of an fp8 row (K, V), inside a stage. Unpacked caches arrive as
+// one box per quarter ([q][16 rows][128 B]); packed caches (page stride = Hkv * rows * row bytes)
+// as one box per (page, head) from a 5-D map ([row half][q][8 rows][128 B]). The 128B swizzle
+// XORs the 16-byte chunk index with r % 8 in both.
+template <int FMT, bool PACKED>
+__device__ __forceinline__ uint32_t line_off(int r, int q) {
+  if (!PACKED) return q * 2048 + r * 128;
+  if (FMT == PBS_KV_BF16) return (r >> 3) * 4096 + q * 1024 + (r & 7) * 128;
+  return (r >> 3) * 2048 + q * 1024 + (r & 7) * 128;
+}
 
 struct Merge {
   float o[kConsumerWarps][kTileHeads][kHeadDim];
@@ -75,11 +92,27 @@ struct Ctl {
   int32_t slot_base[kMaxTopk];
   int32_t ctx;
   int32_t abort;
+  int32_t last;  // this chunk arrived last for its (row, kv head)
 };
 
+// The merge buffer reuses the stage ring once every page has been consumed.
+template <int FMT>
+constexpr size_t ring_bytes() {
+  return size_t(kStages) * StageBytes<FMT>::v > sizeof(Merge) ? size_t(kStages) * StageBytes<FMT>::v
+                                                               : ((sizeof(Merge) + 1023) / 1024) * 1024;
+}
 template <int FMT>
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(kStages) * StageBytes<FMT>::v + sizeof(Merge) + sizeof(Ctl);
+  return 1024 + ring_bytes<FMT>() + sizeof(Ctl);
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2, int c3,
+                                            int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -121,18 +154,18 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 
 // Zero the V rows [nv, 16) of a stage, so that masked keys cannot inject NaN/Inf from
 // uninitialised cache rows into P*V (P is 0 there, but 0 * NaN is NaN).
-template <int FMT>
+template <int FMT, bool PACKED>
 __device__ __forceinline__ void zero_v_tail(uint32_t st, int nv, int lane) {
   if (FMT == PBS_KV_BF16) {
     // quarters 2 and 3, 8 chunks of 16 B per row each
     for (int i = lane; i < (16 - nv) * 16; i += 32) {
       const int r = nv + (i >> 4), q = 2 + ((i >> 3) & 1), c = i & 7;
-      sts128_zero(st + q * 2048 + r * 128 + c * 16);
+      sts128_zero(st + line_off<FMT, PACKED>(r, q) + c * 16);
     }
   } else if (FMT == PBS_KV_FP8_E4M3) {
     for (int i = lane; i < (16 - nv) * 8; i += 32) {
       const int r = nv + (i >> 3), c = i & 7;
-      sts128_zero(st + 2048 + r * 128 + c * 16);
+      sts128_zero(st + line_off<FMT, PACKED>(r, 1) + c * 16);
     }
   } else {
     // V codes: 4 chunks of 16 B per row; V scales: 8 B per row
@@ -148,16 +181,26 @@ __device__ __forceinline__ void zero_v_tail(uint32_t st, int nv, int lane) {
   __syncwarp();
 }
 
-template <int FMT, bool PREFILL>
-__global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_constant__ CUtensorMap tmap,
+#ifdef PBS_TRACE
+// Trace build only: per CTA {SM id, start, first page landed, end} in global-timer ns.
+constexpr int kDTraceCtas = 8192;
+__device__ unsigned long long g_dtrace[kDTraceCtas][4];
+#define DTRACE(k, v) do { const unsigned _c = blockIdx.y * gridDim.x + blockIdx.x; \
+                          if (_c < kDTraceCtas) g_dtrace[_c][(k)] = (v); } while (0)
+#else
+#define DTRACE(k, v) do { } while (0)
+#endif
+
+template <int FMT, bool PREFILL, bool PACKED>
+__global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_constant__ CUtensorMap tmap,
                                                              const AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
   constexpr int kStage = StageBytes<FMT>::v;
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
   uint8_t* stages = smem;
-  Merge* mg = reinterpret_cast<Merge*>(smem + kStages * kStage);
-  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(mg) + sizeof(Merge));
+  Merge* mg = reinterpret_cast<Merge*>(smem);  // valid only after the pipeline has drained
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + ring_bytes<FMT>());
 
   const int S = a.splits;
   const int split = blockIdx.x % S;
@@ -167,6 +210,10 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
   const int G = a.group;
 
   if (threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    DTRACE(0, smid);
+    DTRACE(1, global_timer_ns());
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], 1);
@@ -235,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
   const int key1 = min(slot1 * kSparseBlock, ctx);
   const int npages = key1 > key0 ? (key1 - key0 + kPageRows - 1) / kPageRows : 0;
 
+  // a consumer warp's partial (max, sum, O) waits in registers until the ring has drained
+  float part_m[2] = {-INFINITY, -INFINITY}, part_l[2] = {0.f, 0.f}, part_o[8][4] = {};
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
@@ -270,7 +319,10 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
         }
 #endif
         mbar_arrive_expect_tx(&ctl->full[stage], kStage);
-        if (FMT == PBS_KV_BF16) {
+        if (FMT != PBS_KV_NVFP4 && PACKED) {
+          // one box per (page, head): coordinate page * Hkv + head on the 5-D map
+          tma_load_5d(dst, &tmap, &ctl->full[stage], 0, 0, 0, 0, page * a.num_kv_heads + g);
+        } else if (FMT == PBS_KV_BF16) {
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) tma_load_4d(dst + qq * 2048, &tmap, &ctl->full[stage], 64 * qq, 0, g, page);
         } else if (FMT == PBS_KV_FP8_E4M3) {
@@ -308,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
         break;
       }
       const uint32_t st = smem_u32(stages + stage * kStage);
+      if (p == 0 && lane == 0) DTRACE(2, global_timer_ns());
       const int nv = min(kPageRows, key1 - (key0 + p * kPageRows));
-      if (nv < kPageRows) zero_v_tail<FMT>(st, nv, lane);
+      if (nv < kPageRows) zero_v_tail<FMT, PACKED>(st, nv, lane);
 
       // ---- S^T = K Q^T (16 keys x 8 heads)
       float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -320,14 +373,14 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
         for (int j = 0; j < 8; ++j) {
           const int chunk = 2 * (j & 3) + hi;
           uint32_t af[4];
-          ldsm_x4(st + (j >> 2) * 2048 + key * 128 + ((chunk ^ (key & 7)) << 4), af);
+          ldsm_x4(st + line_off<FMT, PACKED>(key, j >> 2) + ((chunk ^ (key & 7)) << 4), af);
           mma_bf16(s, af, qf[j][0], qf[j][1]);
         }
       } else if (FMT == PBS_KV_FP8_E4M3) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint32_t w0 = lds32(st + hh * 128 + ((j ^ hh) << 4) + 4 * c);
-          const uint32_t w1 = lds32(st + (hh + 8) * 128 + ((j ^ hh) << 4) + 4 * c);
+          const uint32_t w0 = lds32(st + line_off<FMT, PACKED>(hh, 0) + ((j ^ hh) << 4) + 4 * c);
+          const uint32_t w1 = lds32(st + line_off<FMT, PACKED>(hh + 8, 0) + ((j ^ hh) << 4) + 4 * c);
           uint32_t af[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
                             e4m3x2_to_f16x2(w1 >> 16)};
           mma_f16(s, af, qf[j][0], qf[j][1]);
@@ -389,18 +442,17 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
         for (int i = 0; i < 8; ++i) {
           const int chunk = 2 * (i & 3) + (mi & 1);
           uint32_t vf[4];
-          ldsm_x4_trans(st + (2 + (i >> 2)) * 2048 + key * 128 + ((chunk ^ (key & 7)) << 4), vf);
+          ldsm_x4_trans(st + line_off<FMT, PACKED>(key, 2 + (i >> 2)) + ((chunk ^ (key & 7)) << 4), vf);
           mma_bf16(o[i], vf, bh0, bh1);
           mma_bf16(o[i], vf, bl0, bl1);
         }
       } else {
         const uint32_t b0 = movmatrix_trans(pack_f16(p0, p1)), b1 = movmatrix_trans(pack_f16(p2, p3));
         if (FMT == PBS_KV_FP8_E4M3) {
-          const uint32_t vb = st + 2048;
-          const uint4 va = lds128(vb + (2 * c) * 128 + ((hh ^ ((2 * c) & 7)) << 4));
-          const uint4 vbb = lds128(vb + (2 * c + 1) * 128 + ((hh ^ ((2 * c + 1) & 7)) << 4));
-          const uint4 vc = lds128(vb + (2 * c + 8) * 128 + ((hh ^ ((2 * c + 8) & 7)) << 4));
-          const uint4 vd = lds128(vb + (2 * c + 9) * 128 + ((hh ^ ((2 * c + 9) & 7)) << 4));
+          const uint4 va = lds128(st + line_off<FMT, PACKED>(2 * c, 1) + ((hh ^ ((2 * c) & 7)) << 4));
+          const uint4 vbb = lds128(st + line_off<FMT, PACKED>(2 * c + 1, 1) + ((hh ^ ((2 * c + 1) & 7)) << 4));
+          const uint4 vc = lds128(st + line_off<FMT, PACKED>(2 * c + 8, 1) + ((hh ^ ((2 * c + 8) & 7)) << 4));
+          const uint4 vd = lds128(st + line_off<FMT, PACKED>(2 * c + 9, 1) + ((hh ^ ((2 * c + 9) & 7)) << 4));
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
@@ -442,12 +494,27 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&ctl->empty[stage]);
     }
 
-    // ---- this warp's partial -> shared memory
+    // ---- this warp's row sums; the partials go to shared memory once the ring is drained
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+    part_m[0] = m0;
+    part_m[1] = m1;
+    part_l[0] = l0;
+    part_l[1] = l1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) part_o[i][j] = o[i][j];
+  }
+  // every warp has finished with the stage ring (and the producer has drained its copies)
+  __syncthreads();
+  if (warp < kConsumerWarps) {
+    const int hh = lane >> 2, c = lane & 3;
+    const float m0 = part_m[0], m1 = part_m[1], l0 = part_l[0], l1 = part_l[1];
+    const float(&o)[8][4] = part_o;
     float(*ow)[kHeadDim] = mg->o[warp];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -473,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
   }
   __syncthreads();
 
-  // ---- merge the 4 warps (and write the output when the row has a single split)
+  // ---- merge the consumer warps (and write the output when the row has a single split)
   const int E = G * kHeadDim;
   uint16_t* out_row = a.out + static_cast<int64_t>(row) * a.out_row_stride;
   if (threadIdx.x < kConsumerWarps * 32) {
@@ -494,6 +561,13 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
       if (S == 1) {
         const float r = L > 0.f ? a.v_scale * O / L : 0.f;
         out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(r);
+      } else if (a.split_ws != nullptr) {
+        const int64_t pi = (static_cast<int64_t>(row) * a.num_kv_heads + g) * S + split;
+        a.split_ws[pi * kWsPartial + h * kHeadDim + d] = O;
+        if (d == 0) {
+          a.split_ws[pi * kWsPartial + kTileHeads * kHeadDim + h] = M;
+          a.split_ws[pi * kWsPartial + kTileHeads * kHeadDim + kTileHeads + h] = L;
+        }
       } else {
         mg->o[0][h][d] = O;
         if (d == 0) {
@@ -503,7 +577,36 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
       }
     }
   }
-  if (S > 1) {
+  if (S > 1 && a.split_ws != nullptr) {
+    // Split through the workspace: publish this chunk's partial, take a ticket; the last chunk
+    // of the (row, kv head) merges all partials and clears the ticket for the next call.
+    // No chunk waits for another, so early finishers free their SM slot at once.
+    const int64_t unit = static_cast<int64_t>(row) * a.num_kv_heads + g;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) ctl->last = atomicAdd(a.split_tickets + unit, 1) == S - 1;
+    __syncthreads();
+    if (ctl->last) {
+      __threadfence();
+      const float* base = a.split_ws + unit * S * kWsPartial;
+      for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int h = e >> 7, d = e & (kHeadDim - 1);
+        float M = -INFINITY;
+        for (int r = 0; r < S; ++r) M = fmaxf(M, __ldcg(base + r * kWsPartial + kTileHeads * kHeadDim + h));
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+          for (int r = 0; r < S; ++r) {
+            const float f = ex2(__ldcg(base + r * kWsPartial + kTileHeads * kHeadDim + h) - M);
+            O += f * __ldcg(base + r * kWsPartial + h * kHeadDim + d);
+            L += f * __ldcg(base + r * kWsPartial + kTileHeads * kHeadDim + kTileHeads + h);
+          }
+        }
+        const float res = L > 0.f ? a.v_scale * O / L : 0.f;
+        out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
+      }
+      if (threadIdx.x == 0) a.split_tickets[unit] = 0;
+    }
+  } else if (S > 1) {
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -526,12 +629,13 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const __grid_consta
     }
     cluster.sync();  // peers may still be reading this CTA's partial
   }
+  if (threadIdx.x == 0) DTRACE(3, global_timer_ns());
 }
 
-template <int FMT, bool PREFILL>
+template <int FMT, bool PREFILL, bool PACKED>
 cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& tmap, cudaStream_t stream) {
   constexpr size_t smem = smem_bytes<FMT>();
-  auto kern = attend_kernel<FMT, PREFILL>;
+  auto kern = attend_kernel<FMT, PREFILL, PACKED>;
   // dynamic shared memory above 48 KB must be opted into (per device; cheap to repeat)
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -543,7 +647,7 @@ cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& tmap, cudaStream_
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[0].val.clusterDim.x = a.split_ws != nullptr ? 1u : static_cast<unsigned>(a.splits);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -553,15 +657,34 @@ cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& tmap, cudaStream_
 
 }  // namespace
 
+#ifdef PBS_TRACE
+}  // namespace pbs
+// Trace build only: copy the per-CTA decode timeline out (host buffer of n x 4 uint64).
+extern "C" __attribute__((visibility("default"))) int pbs_debug_dtrace_get(unsigned long long* host, int n) {
+  if (n > pbs::kDTraceCtas) n = pbs::kDTraceCtas;
+  return cudaMemcpyFromSymbol(host, pbs::g_dtrace, sizeof(unsigned long long) * 4 * n) == cudaSuccess ? 0 : 5;
+}
+namespace pbs {
+#endif
+
 cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream) {
+  const bool packed = a.packed_map != 0;
   switch (a.kv_dtype) {
     case PBS_KV_BF16:
-      return prefill ? launch_one<PBS_KV_BF16, true>(a, tmap, stream) : launch_one<PBS_KV_BF16, false>(a, tmap, stream);
+      if (packed)
+        return prefill ? launch_one<PBS_KV_BF16, true, true>(a, tmap, stream)
+                       : launch_one<PBS_KV_BF16, false, true>(a, tmap, stream);
+      return prefill ? launch_one<PBS_KV_BF16, true, false>(a, tmap, stream)
+                     : launch_one<PBS_KV_BF16, false, false>(a, tmap, stream);
     case PBS_KV_FP8_E4M3:
-      return prefill ? launch_one<PBS_KV_FP8_E4M3, true>(a, tmap, stream)
-                     : launch_one<PBS_KV_FP8_E4M3, false>(a, tmap, stream);
+      if (packed)
+        return prefill ? launch_one<PBS_KV_FP8_E4M3, true, true>(a, tmap, stream)
+                       : launch_one<PBS_KV_FP8_E4M3, false, true>(a, tmap, stream);
+      return prefill ? launch_one<PBS_KV_FP8_E4M3, true, false>(a, tmap, stream)
+                     : launch_one<PBS_KV_FP8_E4M3, false, false>(a, tmap, stream);
     case PBS_KV_NVFP4:
-      return prefill ? launch_one<PBS_KV_NVFP4, true>(a, tmap, stream) : launch_one<PBS_KV_NVFP4, false>(a, tmap, stream);
+      return prefill ? launch_one<PBS_KV_NVFP4, true, false>(a, tmap, stream)
+                     : launch_one<PBS_KV_NVFP4, false, false>(a, tmap, stream);
     default:
       return cudaErrorInvalidValue;
   }

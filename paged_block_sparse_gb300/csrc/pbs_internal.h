@@ -60,10 +60,23 @@ struct AttendArgs {
   int64_t out_head_stride;
   int32_t* err_word;
   int32_t splits;             // CTAs per (row, kv head) = cluster size
+  int32_t packed_map;         // tmap is the 5-D one-box-per-(page, head) map of a packed cache
+  float* split_ws;            // non-null: splits merge through this workspace, not a cluster
+  int32_t* split_tickets;     // one arrival counter per (row, kv head), zero between calls
 };
 
-// Launch the attend; `tmap` is a 4-D tensor map over the cache rows for the bf16/fp8 formats
-// (unused for NVFP4). Returns the launch status.
+// Workspace of the split decode / token-centric prefill: per (row, kv head, chunk) a partial
+// (1040 floats) from the front, one int32 ticket per (row, kv head) at the end of the caller's
+// buffer. Sized for up to kMaxSplits chunks.
+constexpr int kMaxSplits = 8;
+constexpr size_t kWsPartialBytes = (8 * 128 + 16) * sizeof(float);
+inline size_t attend_workspace_bytes(int64_t units) {
+  return static_cast<size_t>(units) * kMaxSplits * kWsPartialBytes + static_cast<size_t>(units) * sizeof(int32_t);
+}
+
+// Launch the attend; `tmap` is a tensor map over the cache rows for the bf16/fp8 formats
+// (unused for NVFP4): 4-D (one box per quarter / half row) or, with a.packed_map, 5-D (one box
+// per page and head). Returns the launch status.
 cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream);
 
 // Prefill attend on tcgen05 tensor cores (bf16 cache, GQA 8, top-k <= 16, 16-byte aligned q/out

@@ -54,17 +54,17 @@ def oracle_tables(b, part):
                                                    np_i32(p.seq_lens), b.block_page_stride)
 
 
-def gpu_attend(pbs, b, part, err=None):
+def gpu_attend(pbs, b, part, err=None, workspace="auto"):
     if part == "dec":
         d = b.dec
         out = pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table,
                                           d.seq_lens, d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale,
-                                          b.block_page_stride, err_word=err)
+                                          b.block_page_stride, err_word=err, workspace=workspace)
     else:
         p = b.pre
         out = pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
                                            p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
-                                           b.block_page_stride, err_word=err)
+                                           b.block_page_stride, err_word=err, workspace=workspace)
     torch.cuda.synchronize()
     return out.to(torch.float64).cpu().numpy()
 
@@ -174,14 +174,51 @@ def test_attend_small_prefill(pbs, kv_dtype):
     assert_close(dict(enumerate(got)), want, kv_dtype, f"prefill {kv_dtype}")
 
 
+@pytest.mark.parametrize("workspace", [None, "auto"])
 @pytest.mark.parametrize("splits", ["1", "2", "4", "8"])
-def test_attend_split_counts_agree(pbs, splits, monkeypatch):
-    """Every cluster size gives the oracle's answer (the DSMEM merge of the split partials)."""
+def test_attend_split_counts_agree(pbs, splits, workspace, monkeypatch):
+    """Every split count gives the oracle's answer, merged through a cluster's shared memory
+    (no workspace) or through the workspace by the last chunk to finish."""
     monkeypatch.setenv("PBS_ATTEND_SPLITS", splits)
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, dec_seq_lens=[3000, 9000, 700],
                         seed=33)
-    got = gpu_attend(pbs, b, "dec")
-    assert_close(dict(enumerate(got)), oracle_decode(b), "bf16", f"splits={splits}")
+    got = gpu_attend(pbs, b, "dec", workspace=workspace)
+    assert_close(dict(enumerate(got)), oracle_decode(b), "bf16", f"splits={splits} workspace={workspace}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+def test_attend_workspace_leaves_tickets_zero(pbs, kv_dtype, monkeypatch):
+    """Two calls in a row on one caller workspace: both match the oracle, and each leaves the
+    per-(row, kv head) arrival counters at zero for the next call."""
+    monkeypatch.setenv("PBS_ATTEND_SPLITS", "8")
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=4, topk=16,
+                        dec_seq_lens=[1, 2100, 7000, 0, 4000], decode_query_len=2, seed=38)
+    rows, hkv = b.dec.q.shape[0], b.num_kv_heads
+    nbytes = pbs.attend_workspace_bytes(rows, hkv)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    want = oracle_decode(b)
+    for call in range(2):
+        got = gpu_attend(pbs, b, "dec", workspace=ws)
+        assert_close(dict(enumerate(got)), want, kv_dtype, f"workspace call {call}")
+        assert int(ws[nbytes - rows * hkv * 4:].view(torch.int32).abs().sum()) == 0
+    # a smaller call on the same buffer (its tickets sit in the same tail) still matches
+    sub = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=4, topk=16,
+                          dec_seq_lens=[5000], decode_query_len=1, seed=40)
+    got = gpu_attend(pbs, sub, "dec", workspace=ws)
+    assert_close(dict(enumerate(got)), oracle_decode(sub), kv_dtype, "smaller call after")
+    assert int(ws[nbytes - rows * hkv * 4:].view(torch.int32).abs().sum()) == 0
+    got = gpu_attend(pbs, b, "dec", workspace=ws)
+    assert_close(dict(enumerate(got)), want, kv_dtype, "larger call again")
+
+
+def test_prefill_token_kernel_workspace_splits(pbs, monkeypatch):
+    """The token-centric prefill kernel with its splits merged through the workspace."""
+    monkeypatch.setenv("PBS_ATTEND_SPLITS", "4")
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "token")
+    b = workloads.small(device=DEV, kv_dtype="fp8_e4m3", num_heads=64, num_kv_heads=8, topk=16,
+                        pre_q_lens=[200, 1, 90], pre_ctx_lens=[3000, 700, 5000], future_prob=0.3, seed=39)
+    got = gpu_attend(pbs, b, "pre")
+    assert_close(dict(enumerate(got)), oracle_prefill(b), "fp8_e4m3", "prefill workspace splits")
 
 
 def test_attend_empty_rows_are_zero(pbs):
@@ -326,3 +363,24 @@ def test_prefill_tc_ignores_nan_past_last_token(pbs, monkeypatch):
     got = gpu_attend(pbs, b, "pre", err)
     assert int(err.item()) == 0
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill NaN past the end")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_attend_per_quarter_map(pbs, kv_dtype, monkeypatch):
+    """The token-centric kernel on the per-quarter (4-D) cache map as well as the packed one."""
+    monkeypatch.setenv("PBS_CACHE_MAP", "4d")
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8, topk=9,
+                        dec_seq_lens=[129, 2000, 5000], decode_query_len=2, seed=51)
+    assert_close(dict(enumerate(gpu_attend(pbs, b, "dec"))), oracle_decode(b), kv_dtype, "decode 4-D map")
+
+
+def test_attend_strided_pages(pbs):
+    """A cache whose pages are not back to back (page stride > content) uses the 4-D map."""
+    b = workloads.small(device=DEV, num_heads=16, num_kv_heads=2, topk=6, dec_seq_lens=[700, 1500], seed=52)
+    wide = torch.zeros(b.num_pages, b.page_bytes + 4096, dtype=torch.uint8, device=DEV)
+    wide[:, :b.page_bytes] = b.cache
+    view = wide[:, :b.page_bytes]
+    d = b.dec
+    out = pbs.sparse_decode_attention(d.q, view, "bf16", 2, d.topk, d.page_table, d.seq_lens, 1, b.softmax_scale)
+    torch.cuda.synchronize()
+    assert_close(dict(enumerate(out.double().cpu().numpy())), oracle_decode(b), "bf16", "strided pages")
