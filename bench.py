@@ -153,16 +153,35 @@ def recorded_traffic(profile_name: str, src_hash: str):
 # timing helpers
 # --------------------------------------------------------------------------------------------
 
-def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor, stream: torch.cuda.Stream):
+class L2Flush:
+    """Before every timed step: write a buffer larger than L2, then read a second one. The write
+    evicts whatever the last step left in L2; the read makes those now-dirty flush lines get
+    written back here, outside the timed region, so the step starts with a cold and clean L2
+    instead of paying for the flush's own write-backs."""
+
+    def __init__(self, nbytes: int = L2_FLUSH_BYTES):
+        self.w = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.ones(nbytes // 4, dtype=torch.float32, device="cuda")
+        self.s = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.add_(1)
+        torch.sum(self.r, dim=0, out=self.s)
+
+
+L2_NOTE = "flushed before every step (256 MiB write, then 256 MiB read: cold, clean L2)"
+
+
+def time_steps(fn, steps: int, warmup: int, flush: L2Flush, stream: torch.cuda.Stream):
     """Per-step CUDA-event times (ms) on `stream`, L2 flushed before every step."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            flush.add_(1)
+            flush()
             fn()
         stream.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for s, e in evs:
-            flush.add_(1)
+            flush()
             s.record(stream)
             fn()
             e.record(stream)
@@ -401,7 +420,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
             "data": "synthetic", "config": {"workload": b.name, "part": args.part,
-                                            "l2": "flushed (256 MiB write) before every step"},
+                                            "l2": L2_NOTE},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                          "traffic": None, "peak_source": f"{peak_src} (burst, kernel timed alone)",
                          "algorithmic_work_per_launch": work},
@@ -452,7 +471,7 @@ def main():
     hbm, bf16, bf16_sus, peak_src = peaks()
 
     stream = torch.cuda.Stream()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     if args.workload != "decode":
         return secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, peak_src)
     b = workloads.decode(device="cuda", seed=1001 + 17 * rank, batch=args.batch)
@@ -507,7 +526,7 @@ def main():
             "config": {"workload": b_name, "batch": rows, "decode_query_len": 1,
                        "seq_lens": "U[16384, 32768]", "heads": "64/8", "head_dim": 128, "topk_blocks": 16,
                        "kv": "bf16 paged LBHNC, page 16, K|V per row", "parallelism": f"replicas x{world}",
-                       "l2": "flushed (256 MiB write) before every step"},
+                       "l2": L2_NOTE},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
                          "algorithmic_bytes_per_launch": by},

@@ -255,13 +255,14 @@ def _workspace_args(workspace, rows, num_kv_heads, device, stream):
 def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
                             decode_query_len: int, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                             block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                            workspace="auto"):
+                            workspace=None):
     """Sparse decode attend (vLLM flashinfer msa_sparse_decode_attention / nvfp4 decode call).
 
     q [rows, Hq, 128] bf16 with rows = batch * decode_query_len; kv_cache [num_pages, ...] in the
-    ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16. ``workspace``: "auto" (a cached
-    per-stream buffer), None (splits merge inside a thread-block cluster) or a zeroed uint8
-    tensor of at least ``attend_workspace_bytes(rows, num_kv_heads)`` bytes."""
+    ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16. ``workspace``: None (the default:
+    splits merge inside a thread-block cluster, the faster path on GB300), "auto" (a cached
+    per-stream buffer) or a zeroed uint8 tensor of at least
+    ``attend_workspace_bytes(rows, num_kv_heads)`` bytes; with one, splits merge through it."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     wp, wb = _workspace_args(workspace, q.shape[0], num_kv_heads, q.device, stream)
@@ -278,7 +279,7 @@ def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk,
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                              block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                             workspace="auto"):
+                             workspace=None):
     """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
     ``workspace`` as in :func:`sparse_decode_attention`."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)

@@ -54,7 +54,7 @@ def oracle_tables(b, part):
                                                    np_i32(p.seq_lens), b.block_page_stride)
 
 
-def gpu_attend(pbs, b, part, err=None, workspace="auto"):
+def gpu_attend(pbs, b, part, err=None, workspace=None):
     if part == "dec":
         d = b.dec
         out = pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table,
@@ -154,13 +154,14 @@ def test_attend_tiny_bf16(pbs):
     assert_close(dict(enumerate(got)), want, "bf16", "tiny prefill")
 
 
+@pytest.mark.parametrize("workspace", [None, "auto"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
 @pytest.mark.parametrize("heads", [(64, 8), (16, 4), (8, 4), (4, 4)])
-def test_attend_small_decode(pbs, kv_dtype, heads):
+def test_attend_small_decode(pbs, kv_dtype, heads, workspace):
     hq, hkv = heads
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=hq, num_kv_heads=hkv, topk=9,
                         dec_seq_lens=[1, 129, 2000, 5000, 1170], decode_query_len=2, seed=31)
-    got = gpu_attend(pbs, b, "dec")
+    got = gpu_attend(pbs, b, "dec", workspace=workspace)
     want = oracle_decode(b)
     assert_close(dict(enumerate(got)), want, kv_dtype, f"decode {kv_dtype} {heads}")
 
