@@ -26,7 +26,8 @@
  * ---------------------------------
  * - All pointers are DEVICE pointers owned by the caller, unless stated otherwise.
  *   The library allocates no memory and keeps no state between calls (an optional caller-owned
- *   workspace carries split partials within a call).
+ *   workspace carries split partials within a call), except the fixed device scratch of
+ *   pbs_sparse_decode_attention_noalloc, whose tickets are zero between calls.
  * - Work is enqueued on `stream` (NULL = legacy default stream) and is
  *   asynchronous; the return value only reports what the host could check
  *   plus launch errors. Faults found by the kernels themselves are OR-ed into
@@ -69,6 +70,7 @@ typedef struct CUstream_st* pbs_stream_t;
 #define PBS_ERR_UNSUPPORTED 3   /* valid but not implemented here (head_dim != 128, GQA ratio, top-k > 64) */
 #define PBS_ERR_ALIGN       4   /* a pointer or stride breaks the 16-byte alignment the copy engine needs */
 #define PBS_ERR_CUDA        5   /* a CUDA runtime/driver call or a launch failed */
+#define PBS_ERR_SCRATCH     6   /* pbs_sparse_decode_attention_noalloc: request beyond its fixed scratch */
 
 /* ---- device error bits (OR-ed into *err_word by the kernels) ----------------------------- */
 #define PBS_DEVERR_BLOCK_OOB  1  /* a selected, causally valid block id >= max_blocks (row written as empty) */
@@ -177,6 +179,37 @@ PBS_API int pbs_sparse_decode_attention(
     float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
     void* workspace, size_t workspace_bytes,
+    int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Sparse decode attention without caller memory: pbs_sparse_decode_attention with the split
+ * partials and arrival tickets in a fixed 4 MiB device array inside this library instead of a
+ * workspace. No counterpart on the pages; it exists for callers that may not allocate device
+ * memory once serving has started (a fixed memory plan, or an allocator owned by another
+ * framework) and still want split rows merged without a thread-block cluster. The call itself
+ * never allocates (no cudaMalloc, no allocating library routine).
+ *
+ * Limits: when the call splits rows (it does so only while the chunks fit one wave of CTAs),
+ * rows x kv heads must be <= 4096 and rows x kv heads x splits <= 1004, else PBS_ERR_SCRATCH
+ * and nothing is launched. Unsplit calls have no limit.
+ * Setup: the first call on each device looks up the array's device address with the device
+ * current (a CUDA runtime call that may load the library's device module); make that first
+ * call before any stream capture begins. A failed lookup returns PBS_ERR_CUDA.
+ * State: the tickets start at zero (static device memory is zero at module load) and every
+ * completed call leaves them zero. All calls on one device share the array: calls whose
+ * kernels could run at the same time (other streams, unordered host threads) race on it and
+ * must be serialised by the caller, e.g. by issuing them on one stream.
+ * Arguments, layouts and error behaviour otherwise as in pbs_sparse_decode_attention.
+ */
+PBS_API int pbs_sparse_decode_attention_noalloc(
+    const void* q, int64_t q_row_stride, int64_t q_head_stride,
+    const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
+    const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+    const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
+    float softmax_scale, float k_scale, float v_scale,
+    void* out, int64_t out_row_stride, int64_t out_head_stride,
     int32_t* err_word, pbs_stream_t stream);
 
 /*

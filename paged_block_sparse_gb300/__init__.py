@@ -20,7 +20,7 @@ __all__ = [
     "PbsError", "KV_DTYPES", "SPARSE_BLOCK_SIZE", "PAGES_PER_BLOCK", "PAGE_ROWS", "library_path", "lib",
     "abi_version", "status_string", "build_sparse_block_table_decode", "build_sparse_block_table_prefill",
     "sparse_decode_attention", "sparse_prefill_attention", "insert_index_cache", "DEVERR",
-    "attend_workspace_bytes", "attend_workspace",
+    "attend_workspace_bytes", "attend_workspace", "sparse_decode_attention_noalloc",
 ]
 
 SPARSE_BLOCK_SIZE = 128
@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
     L.pbs_sparse_decode_attention.restype = ctypes.c_int
     L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp,
                                                             ctypes.c_size_t, vp, vp]
+    L.pbs_sparse_decode_attention_noalloc.restype = ctypes.c_int
+    L.pbs_sparse_decode_attention_noalloc.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
+                                                                    vp, vp]
     L.pbs_sparse_prefill_attention.restype = ctypes.c_int
     L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
                                                              vp, ctypes.c_size_t, vp, vp]
@@ -273,6 +276,29 @@ def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk,
         float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), wp, wb, _ptr(err_word),
         _stream(stream, q.device))
     _check(st, "pbs_sparse_decode_attention")
+    return out
+
+
+def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
+                                    decode_query_len: int, softmax_scale: float, out, k_scale: float = 1.0,
+                                    v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK, err_word=None,
+                                    stream=None):
+    """:func:`sparse_decode_attention` for callers that may not allocate device memory: split
+    partials go to a fixed 4 MiB scratch inside the library, and ``out`` must be given (this
+    wrapper allocates nothing either). Calls that could overlap on one device (other streams,
+    unordered threads) race on the scratch; the first call on a device does a one-time address
+    lookup and should come before any stream capture."""
+    if out is None:
+        raise ValueError("out is required: the no-allocation entry allocates nothing")
+    num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
+    sl = _dev(seq_lens, "seq_lens", torch.int32)
+    st = lib().pbs_sparse_decode_attention_noalloc(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
+        int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
+        _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), float(softmax_scale),
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(err_word),
+        _stream(stream, q.device))
+    _check(st, "pbs_sparse_decode_attention_noalloc")
     return out
 
 

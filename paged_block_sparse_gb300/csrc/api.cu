@@ -259,6 +259,49 @@ AttendArgs make_attend_args(const void* q, int64_t q_row_stride, int64_t q_head_
 
 }  // namespace
 
+// ---- fixed scratch of pbs_sparse_decode_attention_noalloc ------------------------------------
+// Some callers cannot allocate device memory while serving a step: an engine that fixes its
+// memory plan at start-up and treats any later allocation as an error, or one sharing the GPU
+// with a framework that owns the allocator. For them the split partials and arrival tickets
+// live in this file-scope device array instead of a caller workspace. Layout: partials from
+// the front (kWsPartialBytes each, at most kNoAllocMaxPartials), tickets in the last
+// kNoAllocTicketBytes. The tickets must start at zero: a static device array is zero when the
+// module loads, and every completed call leaves the tickets it used at zero. The partials need
+// no initial value. All calls on one device share the array, so two calls whose kernels could
+// overlap (different streams, or host threads without ordering) race on it.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+constexpr size_t kNoAllocTicketBytes = size_t(16) << 10;
+constexpr int64_t kNoAllocMaxUnits = static_cast<int64_t>(kNoAllocTicketBytes / sizeof(int32_t));
+constexpr int64_t kNoAllocMaxPartials =
+    static_cast<int64_t>((kNoAllocScratchBytes - kNoAllocTicketBytes) / pbs::kWsPartialBytes);
+static_assert(kNoAllocMaxPartials == 1004, "the status text states this limit");
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per device (the lookup
+// may load this library's device module, which is why the first call should come before any
+// stream capture begins).
+int noalloc_scratch(void** addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return PBS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PBS_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return PBS_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* pbs_status_string(int status) {
@@ -269,6 +312,9 @@ const char* pbs_status_string(int status) {
     case PBS_ERR_UNSUPPORTED: return "unsupported configuration (head_dim must be 128, GQA ratio 1/2/4/8, top-k <= 64)";
     case PBS_ERR_ALIGN: return "misaligned pointer or stride (cache 16 B, q 4 B, out 2 B)";
     case PBS_ERR_CUDA: return "CUDA error (launch, tensor-map encoding or driver entry point)";
+    case PBS_ERR_SCRATCH:
+      return "request needs more than the fixed no-allocation scratch (4 MiB: at most 1004 split partials "
+             "= rows x kv heads x splits, and 4096 rows x kv heads when split)";
     default: return "unknown status";
   }
 }
@@ -374,6 +420,54 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
   st = attach_workspace(&a, rows * num_kv_heads, workspace, workspace_bytes);
   if (st != PBS_OK) return st;
   a.splits = choose_splits(rows * num_kv_heads, topk_k, a.split_ws != nullptr);
+  CUtensorMap map;
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
+  if (st != PBS_OK) return st;
+  return pbs::launch_attend(a, false, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+                                                                                                  : PBS_ERR_CUDA;
+}
+
+int pbs_sparse_decode_attention_noalloc(const void* q, int64_t q_row_stride, int64_t q_head_stride,
+                                        const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages,
+                                        int32_t kv_dtype, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
+                                        const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
+                                        const int32_t* seq_lens, int32_t batch, int32_t decode_query_len,
+                                        int32_t block_page_stride, float softmax_scale, float k_scale,
+                                        float v_scale, void* out, int64_t out_row_stride, int64_t out_head_stride,
+                                        int32_t* err_word, pbs_stream_t stream) {
+  if (batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
+  const int64_t rows = static_cast<int64_t>(batch) * decode_query_len;
+  if (rows == 0) return PBS_OK;
+  if (rows > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
+  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
+                        out_head_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  if (st != PBS_OK) return st;
+  if (seq_lens == nullptr) return PBS_ERR_ARG;
+  AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
+                                  num_heads, num_kv_heads, topk, topk_row_stride, topk_k, page_table, pt_row_stride,
+                                  max_blocks, seq_lens, block_page_stride, softmax_scale, k_scale, v_scale, out,
+                                  out_row_stride, out_head_stride, err_word);
+  a.decode_query_len = decode_query_len;
+  a.num_rows = static_cast<int32_t>(rows);
+  // resolved on every call (cached after the first one on a device), split or not, so the
+  // one-time lookup always happens on a device's first call
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != PBS_OK) return st;
+  const int64_t units = rows * num_kv_heads;
+  a.splits = choose_splits(units, topk_k, true);
+  a.split_ws = nullptr;
+  a.split_tickets = nullptr;
+  if (a.splits > 1) {
+    // split rows merge through the fixed scratch: refuse what it cannot hold
+    if (units > kNoAllocMaxUnits || units * a.splits > kNoAllocMaxPartials) return PBS_ERR_SCRATCH;
+    a.split_ws = static_cast<float*>(scratch);
+    a.split_tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kNoAllocScratchBytes) - units;
+  }
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
