@@ -96,17 +96,18 @@ PBS_API int pbs_abi_version(void);
 
 /*
  * Bytes of the optional workspace of pbs_sparse_decode_attention / pbs_sparse_prefill_attention
- * for `num_rows` query rows (decode rows or prefill tokens) and `num_kv_heads` kv heads.
+ * for `num_rows` query rows (decode rows or prefill tokens), `num_heads` query heads and
+ * `num_kv_heads` kv heads (0 for an invalid combination).
  * No counterpart on the pages: with a workspace, a row x kv-head split into chunks merges
  * through it (the last chunk to finish merges the others' partials) instead of through a
- * thread-block cluster, which keeps the block scheduler free to balance the tail. The caller
+ * thread-block cluster, with no co-scheduling needed between the chunks. The caller
  * owns it (16-byte aligned) and zeroes it once before first use. Partials are written from its
  * front, one int32 arrival ticket per (row, kv head) sits in its last bytes; every completed call
  * leaves its tickets zero again, so the buffer serves any later call that fits it without
  * re-zeroing (after a PBS_DEVERR_TIMEOUT, zero it again). Calls that share one workspace must
  * not run concurrently.
  */
-PBS_API size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_kv_heads);
+PBS_API size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads);
 
 /*
  * Sparse block table, decode ([sparse_pa] minimax_m3_build_sparse_block_table_decode and
@@ -161,7 +162,7 @@ PBS_API int pbs_build_sparse_block_table_prefill(
  *               kv_cache + p*page_stride_bytes (16-byte aligned, as is the base)
  *   num_pages   pages addressable from kv_cache (page ids >= num_pages set PBS_DEVERR_PAGE_OOB)
  *   num_heads / num_kv_heads: GQA ratio G = num_heads / num_kv_heads; query head h reads kv head h / G.
- *               Supported: head_dim 128, G in {1, 2, 4, 8}.
+ *               Supported: head_dim 128, G in {1, 2, 4, 8, 16}.
  *   softmax_scale, k_scale, v_scale: fp32. The stored K is multiplied by k_scale and V by v_scale
  *               (for NVFP4 these are the per-tensor global scales). As on [flashinfer] forward the
  *               kernel folds k_scale into the softmax scale and v_scale into the output.
@@ -190,7 +191,8 @@ PBS_API int pbs_sparse_decode_attention(
  * never allocates (no cudaMalloc, no allocating library routine).
  *
  * Limits: when the call splits rows (it does so only while the chunks fit one wave of CTAs),
- * rows x kv heads must be <= 4096 and rows x kv heads x splits <= 1004, else PBS_ERR_SCRATCH
+ * rows x head groups must be <= 4096 and rows x head groups x splits <= 1004 (a head group is a
+ * kv head's query heads, or 8 of them when it serves 16), else PBS_ERR_SCRATCH
  * and nothing is launched. Unsplit calls have no limit.
  * Setup: the first call on each device looks up the array's device address with the device
  * current (a CUDA runtime call that may load the library's device module); make that first
@@ -216,7 +218,7 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
  * Sparse prefill attention, varlen ([flashinfer] msa_sparse_attention call with cu_seqlens_q;
  * [nvfp4] minimax_m3_nvfp4_sparse_prefill call). Token positions as in
  * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention.
- * Shapes the tcgen05 tile kernel takes (bf16 packed cache, GQA 8, top-k <= 16, 16-byte aligned q
+ * Shapes the tcgen05 tile kernel takes (bf16 packed cache, GQA 8 or 16, top-k <= 16, 16-byte aligned q
  * and out rows) ignore the workspace.
  */
 PBS_API int pbs_sparse_prefill_attention(

@@ -59,7 +59,7 @@ def lib() -> ctypes.CDLL:
     L.pbs_abi_version.restype = ctypes.c_int
     L.pbs_abi_version.argtypes = []
     L.pbs_attend_workspace_bytes.restype = ctypes.c_size_t
-    L.pbs_attend_workspace_bytes.argtypes = [i64, i32]
+    L.pbs_attend_workspace_bytes.argtypes = [i64, i32, i32]
     table_common = [vp, i64, i32, i32, vp, i64, i32]
     L.pbs_build_sparse_block_table_decode.restype = ctypes.c_int
     L.pbs_build_sparse_block_table_decode.argtypes = table_common + [vp, i32, i32, i32, vp, i64, vp, vp, vp]
@@ -216,15 +216,15 @@ def _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     return num_pages, page_stride_bytes, tk, pt, out
 
 
-def attend_workspace_bytes(num_rows: int, num_kv_heads: int) -> int:
+def attend_workspace_bytes(num_rows: int, num_heads: int, num_kv_heads: int) -> int:
     """Bytes of the optional split-merge workspace for ``num_rows`` query rows."""
-    return int(lib().pbs_attend_workspace_bytes(int(num_rows), int(num_kv_heads)))
+    return int(lib().pbs_attend_workspace_bytes(int(num_rows), int(num_heads), int(num_kv_heads)))
 
 
 _workspaces: dict = {}
 
 
-def attend_workspace(num_rows: int, num_kv_heads: int, device, stream=None) -> torch.Tensor:
+def attend_workspace(num_rows: int, num_heads: int, num_kv_heads: int, device, stream=None) -> torch.Tensor:
     """A zeroed workspace for the attends, cached per (device, stream) and grown on demand.
 
     Calls that share one workspace must not overlap, so the cache is keyed by stream: calls on
@@ -232,7 +232,7 @@ def attend_workspace(num_rows: int, num_kv_heads: int, device, stream=None) -> t
     device = torch.device(device)
     s = stream if stream is not None else torch.cuda.current_stream(device)
     key = (device.index, s.cuda_stream)
-    need = attend_workspace_bytes(num_rows, num_kv_heads)
+    need = attend_workspace_bytes(num_rows, num_heads, num_kv_heads)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
         with torch.cuda.stream(s):
@@ -241,14 +241,14 @@ def attend_workspace(num_rows: int, num_kv_heads: int, device, stream=None) -> t
     return ws
 
 
-def _workspace_args(workspace, rows, num_kv_heads, device, stream):
+def _workspace_args(workspace, rows, num_heads, num_kv_heads, device, stream):
     """(pointer, bytes) for the C call: "auto" takes the cached workspace, None passes none."""
     if workspace is None:
         return None, 0
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
-        workspace = attend_workspace(rows, num_kv_heads, device, stream)
+        workspace = attend_workspace(rows, num_heads, num_kv_heads, device, stream)
     _dev(workspace, "workspace", torch.uint8)
     if not workspace.is_contiguous():
         raise ValueError("workspace must be contiguous")
@@ -265,10 +265,10 @@ def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk,
     ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16. ``workspace``: None (the default:
     splits merge inside a thread-block cluster, the faster path on GB300), "auto" (a cached
     per-stream buffer) or a zeroed uint8 tensor of at least
-    ``attend_workspace_bytes(rows, num_kv_heads)`` bytes; with one, splits merge through it."""
+    ``attend_workspace_bytes(rows, Hq, num_kv_heads)`` bytes; with one, splits merge through it."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
-    wp, wb = _workspace_args(workspace, q.shape[0], num_kv_heads, q.device, stream)
+    wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     st = lib().pbs_sparse_decode_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
@@ -311,7 +311,7 @@ def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
-    wp, wb = _workspace_args(workspace, q.shape[0], num_kv_heads, q.device, stream)
+    wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     st = lib().pbs_sparse_prefill_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],

@@ -109,9 +109,10 @@ int encode_attend_map(CUtensorMap* map, const void* cache, int kv_dtype, int num
   return encode_cache_map(map, cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes);
 }
 
-// Queries as a 3-D tensor {head_dim, heads, tokens}; a box is 16 tokens x 8 heads x 64 dims, laid
-// out in shared memory as the 128-row K-major operand of the prefill MMA (row = token * 8 + head).
-int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int total_q, int64_t q_row_stride,
+// Queries as a 3-D tensor {head_dim, heads, tokens}; a box is (128 / G) tokens x G heads x 64
+// dims (G = 8 or 16 query heads per kv head), laid out in shared memory as the 128-row K-major
+// operand of the prefill MMA (row = token * G + head).
+int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int total_q, int64_t q_row_stride,
                  int64_t q_head_stride) {
   std::memset(map, 0, sizeof(*map));
   auto enc = tensor_map_encoder();
@@ -119,7 +120,7 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int total_q, in
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(num_heads),
                               static_cast<cuuint64_t>(total_q)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(q_head_stride) * 2, static_cast<cuuint64_t>(q_row_stride) * 2};
-  const cuuint32_t box[3] = {64, 8, 16};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -208,7 +209,7 @@ int check_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride, con
   if (num_heads % num_kv_heads != 0) return PBS_ERR_SHAPE;
   if (head_dim != kHeadDim) return PBS_ERR_UNSUPPORTED;
   const int G = num_heads / num_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return PBS_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PBS_ERR_UNSUPPORTED;
   if (num_kv_heads > 65535) return PBS_ERR_UNSUPPORTED;
   if (q_row_stride < 0 || q_head_stride < 0 || out_row_stride < 0 || out_head_stride < 0) return PBS_ERR_SHAPE;
   if (num_pages <= 0 || num_pages > 0x7fffffffLL) return PBS_ERR_SHAPE;
@@ -237,6 +238,7 @@ AttendArgs make_attend_args(const void* q, int64_t q_row_stride, int64_t q_head_
   a.num_heads = num_heads;
   a.num_kv_heads = num_kv_heads;
   a.group = num_heads / num_kv_heads;
+  a.sub_groups = a.group > 8 ? a.group / 8 : 1;
   a.topk = topk;
   a.topk_row_stride = topk_row_stride;
   a.k = topk_k;
@@ -309,21 +311,21 @@ const char* pbs_status_string(int status) {
     case PBS_OK: return "ok";
     case PBS_ERR_ARG: return "invalid argument (null pointer, bad enum or non-positive size)";
     case PBS_ERR_SHAPE: return "inconsistent shapes or strides";
-    case PBS_ERR_UNSUPPORTED: return "unsupported configuration (head_dim must be 128, GQA ratio 1/2/4/8, top-k <= 64)";
+    case PBS_ERR_UNSUPPORTED: return "unsupported configuration (head_dim must be 128, GQA ratio 1/2/4/8/16, top-k <= 64)";
     case PBS_ERR_ALIGN: return "misaligned pointer or stride (cache 16 B, q 4 B, out 2 B)";
     case PBS_ERR_CUDA: return "CUDA error (launch, tensor-map encoding or driver entry point)";
     case PBS_ERR_SCRATCH:
       return "request needs more than the fixed no-allocation scratch (4 MiB: at most 1004 split partials "
-             "= rows x kv heads x splits, and 4096 rows x kv heads when split)";
+             "= rows x head groups x splits, and 4096 rows x head groups when split)";
     default: return "unknown status";
   }
 }
 
-int pbs_abi_version(void) { return 2; }
+int pbs_abi_version(void) { return 3; }
 
-size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_kv_heads) {
-  if (num_rows <= 0 || num_kv_heads <= 0) return 0;
-  return pbs::attend_workspace_bytes(num_rows * num_kv_heads);
+size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
+  if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
+  return pbs::attend_workspace_bytes(pbs::attend_units(num_rows, num_kv_heads, num_heads / num_kv_heads));
 }
 
 int pbs_build_sparse_block_table_decode(const int32_t* topk, int64_t topk_row_stride, int32_t num_rows,
@@ -417,9 +419,10 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                   out_row_stride, out_head_stride, err_word);
   a.decode_query_len = decode_query_len;
   a.num_rows = static_cast<int32_t>(rows);
-  st = attach_workspace(&a, rows * num_kv_heads, workspace, workspace_bytes);
+  const int64_t units = pbs::attend_units(rows, num_kv_heads, a.group);
+  st = attach_workspace(&a, units, workspace, workspace_bytes);
   if (st != PBS_OK) return st;
-  a.splits = choose_splits(rows * num_kv_heads, topk_k, a.split_ws != nullptr);
+  a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
@@ -458,7 +461,7 @@ int pbs_sparse_decode_attention_noalloc(const void* q, int64_t q_row_stride, int
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != PBS_OK) return st;
-  const int64_t units = rows * num_kv_heads;
+  const int64_t units = pbs::attend_units(rows, num_kv_heads, a.group);
   a.splits = choose_splits(units, topk_k, true);
   a.split_ws = nullptr;
   a.split_tickets = nullptr;
@@ -501,9 +504,10 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   a.cu_seqlens_q = cu_seqlens_q;
   a.num_reqs = num_reqs;
   a.num_rows = total_q;
-  st = attach_workspace(&a, static_cast<int64_t>(total_q) * num_kv_heads, workspace, workspace_bytes);
+  const int64_t units = pbs::attend_units(total_q, num_kv_heads, a.group);
+  st = attach_workspace(&a, units, workspace, workspace_bytes);
   if (st != PBS_OK) return st;
-  a.splits = choose_splits(static_cast<int64_t>(total_q) * num_kv_heads, topk_k, a.split_ws != nullptr);
+  a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
@@ -514,7 +518,7 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   if (force == 2 && !tc_ok) return PBS_ERR_UNSUPPORTED;
   if (tc_ok) {
     CUtensorMap qmap;
-    st = encode_q_map(&qmap, q, num_heads, total_q, q_row_stride, q_head_stride);
+    st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
     e = pbs::launch_prefill_tc(a, map, qmap, reinterpret_cast<cudaStream_t>(stream));
   } else {

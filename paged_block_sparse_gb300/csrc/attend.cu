@@ -205,9 +205,11 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
   const int S = a.splits;
   const int split = blockIdx.x % S;
   const int row = blockIdx.x / S;
-  const int g = blockIdx.y;
+  // head group gv = kv head g's query heads gv * G .. gv * G + G - 1 (G <= 8 heads per CTA)
+  const int gv = blockIdx.y;
+  const int g = gv / a.sub_groups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = a.group;
+  const int G = a.group / a.sub_groups;
 
   if (threadIdx.x == 0) {
     unsigned smid;
@@ -239,15 +241,15 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     }
     page_bad = __any_sync(0xffffffffu, page_bad);
     if (lane == 0) {
-      if (rc.bad && split == 0 && g == 0) set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
-      if (page_bad && split == 0 && g == 0) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+      if (rc.bad && split == 0 && gv == 0) set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+      if (page_bad && split == 0 && gv == 0) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
       ctl->ctx = page_bad ? 0 : rc.ctx;
     }
   } else {
     const int hh = lane >> 2, c = lane & 3;
     const bool live = hh < G;
     const uint16_t* qh =
-        a.q + static_cast<int64_t>(row) * a.q_row_stride + static_cast<int64_t>(g * G + (live ? hh : 0)) * a.q_head_stride;
+        a.q + static_cast<int64_t>(row) * a.q_row_stride + static_cast<int64_t>(gv * G + (live ? hh : 0)) * a.q_head_stride;
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -560,9 +562,9 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
       }
       if (S == 1) {
         const float r = L > 0.f ? a.v_scale * O / L : 0.f;
-        out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(r);
+        out_row[static_cast<int64_t>(gv * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(r);
       } else if (a.split_ws != nullptr) {
-        const int64_t pi = (static_cast<int64_t>(row) * a.num_kv_heads + g) * S + split;
+        const int64_t pi = (static_cast<int64_t>(row) * gridDim.y + gv) * S + split;
         a.split_ws[pi * kWsPartial + h * kHeadDim + d] = O;
         if (d == 0) {
           a.split_ws[pi * kWsPartial + kTileHeads * kHeadDim + h] = M;
@@ -581,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     // Split through the workspace: publish this chunk's partial, take a ticket; the last chunk
     // of the (row, kv head) merges all partials and clears the ticket for the next call.
     // No chunk waits for another, so early finishers free their SM slot at once.
-    const int64_t unit = static_cast<int64_t>(row) * a.num_kv_heads + g;
+    const int64_t unit = static_cast<int64_t>(row) * gridDim.y + gv;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) ctl->last = atomicAdd(a.split_tickets + unit, 1) == S - 1;
@@ -602,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
           }
         }
         const float res = L > 0.f ? a.v_scale * O / L : 0.f;
-        out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
+        out_row[static_cast<int64_t>(gv * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
       }
       if (threadIdx.x == 0) a.split_tickets[unit] = 0;
     }
@@ -625,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
         }
       }
       const float res = L > 0.f ? a.v_scale * O / L : 0.f;
-      out_row[static_cast<int64_t>(g * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
+      out_row[static_cast<int64_t>(gv * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
     }
     cluster.sync();  // peers may still be reading this CTA's partial
   }
@@ -641,7 +643,7 @@ cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& tmap, cudaStream_
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.num_rows) * static_cast<unsigned>(a.splits),
-                     static_cast<unsigned>(a.num_kv_heads), 1);
+                     static_cast<unsigned>(a.num_kv_heads * a.sub_groups), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

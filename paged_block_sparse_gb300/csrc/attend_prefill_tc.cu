@@ -1,4 +1,4 @@
-// Prefill attend on the 5th-generation tensor cores (tcgen05 + TMEM), bf16 KV cache, GQA 8.
+// Prefill attend on the 5th-generation tensor cores (tcgen05 + TMEM), bf16 KV cache, GQA 8 or 16.
 //
 // What it computes (vLLM page vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer, forward:
 // the varlen msa_sparse_attention call; row rule of vllm.models.minimax_m3.amd.ops.sparse_pa,
@@ -9,9 +9,10 @@
 //
 // GB300 design
 // ------------
-// * A CTA owns a tile of 16 consecutive tokens of one request and one kv head: 16 x 8 query
-//   heads = 128 rows, one MMA M-tile. The tile's selected blocks are merged into a sorted union;
-//   every union block is streamed once and each row is masked by its own token's selection.
+// * A CTA owns a tile of consecutive tokens of one request and one kv head: 16 tokens x 8 query
+//   heads, or 8 tokens x 16 heads, = 128 rows, one MMA M-tile. The tile's selected blocks are
+//   merged into a sorted union; every union block is streamed once and each row is masked by its
+//   own token's selection.
 // * Warp 0: TMA producer (Q tile once via a 3-D tensor map; K and V of each union block with one
 //   8 KiB copy per page through a 5-D tensor map over the packed cache, 128B swizzle, 3-stage
 //   ring). A stage is [page][row half][quarter: K lo, K hi, V lo, V hi][8 rows][128 B], so every
@@ -37,9 +38,10 @@
 namespace pbs {
 namespace {
 
-constexpr int kTok = 16;          // tokens per tile
-constexpr int kG = 8;             // query heads per kv head on this path
-constexpr int kRows = kTok * kG;  // 128 = MMA M
+// A tile is 128 rows = the MMA M: kTok tokens x kG query heads of one kv head, kG = 8 (16
+// tokens) or 16 (8 tokens). Rows are token-major: row = token * kG + head.
+constexpr int kRows = 128;
+constexpr int kTokMax = 16;
 constexpr int kSplit = 2;                        // softmax warps per TMEM lane quadrant
 constexpr int kW = 128 / kSplit;                 // S columns (keys) per softmax thread
 constexpr int kSoftWarps = 4 * kSplit;
@@ -68,11 +70,11 @@ struct TcCtl {
   int32_t req, t0, n_tok;
   int32_t bad_mask;   // tokens whose row hit an out-of-range block id
   int32_t abort;
-  int32_t own[kTok];  // own block of each token (-1: none)
-  int32_t lim[kTok];  // keys of the own block the token sees
-  int32_t cnt[kTok];  // distinct valid blocks per token
+  int32_t own[kTokMax];  // own block of each token (-1: none)
+  int32_t lim[kTokMax];  // keys of the own block the token sees
+  int32_t cnt[kTokMax];  // distinct valid blocks per token
   uint16_t union_blk[kMaxUnion];
-  uint16_t tok_blk[kTok][kTcMaxTopk];
+  uint16_t tok_blk[kTokMax][kTcMaxTopk];
   float xchg[kSplit][kRows];  // per-row partial maxima / sums exchanged within a lane quadrant
 };
 
@@ -196,9 +198,11 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
 
 __device__ __forceinline__ bool aborted(TcCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
 
+template <int kG>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const AttendArgs a) {
+  constexpr int kTok = kRows / kG;  // tokens per tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* big = smem_raw;
   TcCtl* ctl = reinterpret_cast<TcCtl*>(smem_raw + kBigBytes);
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int sw = warp - 4, quad = sw & 3, part = sw >> 2;
     const int row = quad * 32 + lane;  // = TMEM lane
     const int col0 = part * kW;
-    const int tt = row >> 3, h = row & 7;
+    const int tt = row / kG, h = row % kG;
     const bool live = tt < n_tok && !((ctl->bad_mask >> tt) & 1);
     const int cnt_t = live ? ctl->cnt[tt] : 0;
     const int own_t = ctl->own[tt], lim_t = ctl->lim[tt];
@@ -639,7 +643,7 @@ namespace pbs {
 #endif
 
 bool prefill_tc_supported(const AttendArgs& a) {
-  return a.kv_dtype == PBS_KV_BF16 && a.group == kG && a.k <= kTcMaxTopk && a.max_blocks <= 65536 &&
+  return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.k <= kTcMaxTopk && a.max_blocks <= 65536 &&
          a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
          a.num_pages * a.num_kv_heads <= 0x7fffffffLL &&
          a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
@@ -647,16 +651,21 @@ bool prefill_tc_supported(const AttendArgs& a) {
          reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
 }
 
-cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
-                              cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int kG>
+cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kTcSmem));
   if (e != cudaSuccess) return e;
   // tiles are numbered request by request; the grid is an upper bound and surplus CTAs exit
-  const unsigned tiles = static_cast<unsigned>(a.num_rows / kTok + a.num_reqs + 1);
-  prefill_tc_kernel<<<dim3(tiles, static_cast<unsigned>(a.num_kv_heads)), kThreadsTc, kTcSmem, stream>>>(kv_map,
-                                                                                                        q_map, a);
+  const unsigned tiles = static_cast<unsigned>(a.num_rows / (kRows / kG) + a.num_reqs + 1);
+  prefill_tc_kernel<kG><<<dim3(tiles, static_cast<unsigned>(a.num_kv_heads)), kThreadsTc, kTcSmem, stream>>>(
+      kv_map, q_map, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                              cudaStream_t stream) {
+  return a.group == 16 ? launch_tc<16>(a, kv_map, q_map, stream) : launch_tc<8>(a, kv_map, q_map, stream);
 }
 
 }  // namespace pbs

@@ -40,7 +40,8 @@ struct AttendArgs {
   int32_t kv_dtype;
   int32_t num_heads;
   int32_t num_kv_heads;
-  int32_t group;              // num_heads / num_kv_heads
+  int32_t group;              // num_heads / num_kv_heads (1, 2, 4, 8 or 16)
+  int32_t sub_groups;         // query-head groups of at most 8 per kv head (2 when group is 16)
   const int32_t* topk;
   int64_t topk_row_stride;
   int32_t k;
@@ -59,15 +60,21 @@ struct AttendArgs {
   int64_t out_row_stride;
   int64_t out_head_stride;
   int32_t* err_word;
-  int32_t splits;             // CTAs per (row, kv head) = cluster size
+  int32_t splits;             // CTAs per (row, head group) = cluster size
   int32_t packed_map;         // tmap is the 5-D one-box-per-(page, head) map of a packed cache
   float* split_ws;            // non-null: splits merge through this workspace, not a cluster
-  int32_t* split_tickets;     // one arrival counter per (row, kv head), zero between calls
+  int32_t* split_tickets;     // one arrival counter per (row, head group), zero between calls
 };
 
-// Workspace of the split decode / token-centric prefill: per (row, kv head, chunk) a partial
-// (1040 floats) from the front, one int32 ticket per (row, kv head) at the end of the caller's
-// buffer. Sized for up to kMaxSplits chunks.
+// Work units of the token-centric attend: (row, head group) pairs, a head group being the query
+// heads of one kv head (two groups of 8 when a kv head serves 16).
+inline int64_t attend_units(int64_t rows, int num_kv_heads, int group) {
+  return rows * num_kv_heads * (group > 8 ? group / 8 : 1);
+}
+
+// Workspace of the split decode / token-centric prefill: per (unit, chunk) a partial (1040
+// floats) from the front, one int32 ticket per unit at the end of the caller's buffer. Sized for
+// up to kMaxSplits chunks.
 constexpr int kMaxSplits = 8;
 constexpr size_t kWsPartialBytes = (8 * 128 + 16) * sizeof(float);
 inline size_t attend_workspace_bytes(int64_t units) {

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 2
+    assert pbs.abi_version() == 3
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"
@@ -91,6 +91,7 @@ def _decode_attend(L, **kw):
 def test_attend_host_checks(L):
     assert _decode_attend(L, hd=64) == 3                  # head_dim must be 128
     assert _decode_attend(L, hq=48, hkv=8) == 3           # G = 6 unsupported
+    assert _decode_attend(L, hq=256, hkv=8) == 3          # G = 32 unsupported
     assert _decode_attend(L, hq=60, hkv=8) == 2           # heads not a multiple of kv heads
     assert _decode_attend(L, dt=7) == 1
     assert _decode_attend(L, q=N) == 1
@@ -102,9 +103,11 @@ def test_attend_host_checks(L):
     assert _decode_attend(L, batch=0) == 0
     assert _decode_attend(L, npages=0) == 2
     assert _decode_attend(L, k=80, trs=80) == 3
-    need = L.pbs_attend_workspace_bytes(4, 8)
+    need = L.pbs_attend_workspace_bytes(4, 64, 8)
     assert need == 4 * 8 * (8 * 1040 * 4 + 4)              # 8 split partials + 1 ticket per (row, kv head)
-    assert L.pbs_attend_workspace_bytes(0, 8) == 0
+    assert L.pbs_attend_workspace_bytes(4, 128, 8) == 2 * need   # GQA 16: two head groups per kv head
+    assert L.pbs_attend_workspace_bytes(0, 64, 8) == 0
+    assert L.pbs_attend_workspace_bytes(4, 60, 8) == 0
     assert _decode_attend(L, ws=N, wsb=16) == 1            # bytes without a pointer
     assert _decode_attend(L, ws=ctypes.c_void_p(0x10008), wsb=need) == 4
     assert _decode_attend(L, ws=A, wsb=need - 1) == 2      # too small for the rows

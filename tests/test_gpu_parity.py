@@ -156,7 +156,7 @@ def test_attend_tiny_bf16(pbs):
 
 @pytest.mark.parametrize("workspace", [None, "auto"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
-@pytest.mark.parametrize("heads", [(64, 8), (16, 4), (8, 4), (4, 4)])
+@pytest.mark.parametrize("heads", [(64, 8), (32, 2), (16, 4), (8, 4), (4, 4)])
 def test_attend_small_decode(pbs, kv_dtype, heads, workspace):
     hq, hkv = heads
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=hq, num_kv_heads=hkv, topk=9,
@@ -195,7 +195,7 @@ def test_attend_workspace_leaves_tickets_zero(pbs, kv_dtype, monkeypatch):
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=4, topk=16,
                         dec_seq_lens=[1, 2100, 7000, 0, 4000], decode_query_len=2, seed=38)
     rows, hkv = b.dec.q.shape[0], b.num_kv_heads
-    nbytes = pbs.attend_workspace_bytes(rows, hkv)
+    nbytes = pbs.attend_workspace_bytes(rows, b.num_heads, hkv)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     want = oracle_decode(b)
     for call in range(2):
@@ -325,11 +325,13 @@ PREFILL_CASES = [
 ]
 
 
+@pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
 @pytest.mark.parametrize("kernel", ["tc", "token"])
 @pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
-def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, monkeypatch):
+def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, heads, monkeypatch):
+    """Both prefill kernels, GQA 8 (tile = 16 tokens x 8 heads) and GQA 16 (8 tokens x 16 heads)."""
     monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
-    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, seed=41 + ci, **PREFILL_CASES[ci])
+    b = workloads.small(device=DEV, num_heads=heads[0], num_kv_heads=heads[1], seed=41 + ci, **PREFILL_CASES[ci])
     err = _err()
     got = gpu_attend(pbs, b, "pre", err)
     assert int(err.item()) == 0

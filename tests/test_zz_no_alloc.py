@@ -39,7 +39,8 @@ def test_noalloc_matches_workspace_entry_twice(pbs, kv_dtype):
     d = b.dec
     args = (d.q, b.cache, kv_dtype, b.num_kv_heads, d.topk, d.page_table, d.seq_lens, d.decode_query_len,
             b.softmax_scale)
-    ws = torch.zeros(pbs.attend_workspace_bytes(d.q.shape[0], b.num_kv_heads), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(pbs.attend_workspace_bytes(d.q.shape[0], b.num_heads, b.num_kv_heads), dtype=torch.uint8,
+                     device=DEV)
     want = pbs.sparse_decode_attention(*args, b.k_scale, b.v_scale, workspace=ws)
     torch.cuda.synchronize()
     want = want.double().cpu().numpy()
