@@ -5,7 +5,7 @@ the cpu_baseline leg of ``bench.py``; never by the product path. It shares no
 code with the CUDA kernels.
 """
 from .sparse_attend import (  # noqa: F401
-    PAGES_PER_BLOCK, PAGE_ROWS, SPARSE_BLOCK_SIZE, attend, attended_positions,
+    PAGES_PER_BLOCK, PAGE_ROWS, SPARSE_BLOCK_SIZE, attend, attend_lse, attended_positions,
     build_sparse_block_table_decode, build_sparse_block_table_prefill, decode_query_positions,
     gather_kv, insert_index_cache, prefill_query_positions, sparse_block_table_row,
     sparse_decode_attention, sparse_prefill_attention)

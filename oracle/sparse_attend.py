@@ -43,6 +43,10 @@ Sources are three vLLM API pages:
    in K and the output in V); the oracle applies them to the values instead.
 4. Index-cache insert ([sparse_pa] insert): cache[slot // T, slot % T, :] =
    index_k[n, :].
+5. Log-sum-exp of a row's logits (not on the pages; an optional output of the
+   attends so that partial attends over disjoint key sets can be merged):
+   lse_h = ln sum_n exp(scale * q_h . k_n) over the same keys as step 3, with
+   the same scales; -inf for a row with no attended key.
 
 Readings where the pages are silent (each listed in the design notes too):
 SPARSE_BLOCK_SIZE = 128, page rows = 16, PAGES_PER_BLOCK = 8; a page-table
@@ -241,37 +245,59 @@ def attend(q_heads, K, V, softmax_scale: float, k_scale: float = 1.0, v_scale: f
     return out
 
 
+def attend_lse(q_heads, K, softmax_scale: float, k_scale: float = 1.0):
+    """Natural-log log-sum-exp of each head's logits (step 5): [Hq], -inf when n == 0."""
+    q = np.asarray(q_heads, dtype=np.float64)
+    Hq, _ = q.shape
+    Hkv, n, _ = K.shape
+    G = Hq // Hkv
+    lse = np.full(Hq, -np.inf)
+    if n == 0:
+        return lse
+    Kd = K * k_scale
+    for h in range(Hq):
+        logits = softmax_scale * (Kd[h // G] @ q[h])
+        m = logits.max()
+        lse[h] = m + np.log(np.exp(logits - m).sum())
+    return lse
+
+
 def _attend_rows(q, cache, kv_dtype, num_kv_heads, topk, page_table, req, pos, softmax_scale,
-                 k_scale, v_scale, block_page_stride, rows):
+                 k_scale, v_scale, block_page_stride, rows, return_lse=False):
     qa = np.asarray(q, dtype=np.float64)
     tk = np.asarray(topk).reshape(-1, np.asarray(topk).shape[-1])
     pt = np.asarray(page_table)
     n, Hq, D = qa.shape
     rows = range(n) if rows is None else rows
-    out = {}
+    out, lse = {}, {}
     for r in rows:
         keys = attended_positions(tk[r], int(pos[r]))
         K, V = gather_kv(cache, kv_dtype, num_kv_heads, D, pt[req[r]], keys, block_page_stride)
         out[r] = attend(qa[r], K, V, softmax_scale, k_scale, v_scale)
-    return out
+        if return_lse:
+            lse[r] = attend_lse(qa[r], K, softmax_scale, k_scale)
+    return (out, lse) if return_lse else out
 
 
 def sparse_decode_attention(q, cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
                             decode_query_len: int, softmax_scale: float, k_scale: float = 1.0,
-                            v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK, rows=None):
-    """Decode attend; returns {row: out[Hq, D]} for the requested rows (all by default)."""
+                            v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK, rows=None,
+                            return_lse: bool = False):
+    """Decode attend; returns {row: out[Hq, D]} for the requested rows (all by default), and
+    {row: lse[Hq]} as well with ``return_lse``."""
     req, pos = decode_query_positions(seq_lens, decode_query_len)
     return _attend_rows(q, cache, kv_dtype, num_kv_heads, topk, page_table, req, pos, softmax_scale,
-                        k_scale, v_scale, block_page_stride, rows)
+                        k_scale, v_scale, block_page_stride, rows, return_lse)
 
 
 def sparse_prefill_attention(q, cache, kv_dtype: str, num_kv_heads: int, topk, page_table,
                              cu_seqlens_q, seq_lens, softmax_scale: float, k_scale: float = 1.0,
-                             v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK, rows=None):
-    """Prefill attend (varlen); returns {token: out[Hq, D]}."""
+                             v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK, rows=None,
+                             return_lse: bool = False):
+    """Prefill attend (varlen); returns {token: out[Hq, D]} (and {token: lse[Hq]})."""
     req, pos = prefill_query_positions(cu_seqlens_q, seq_lens)
     return _attend_rows(q, cache, kv_dtype, num_kv_heads, topk, page_table, req, pos, softmax_scale,
-                        k_scale, v_scale, block_page_stride, rows)
+                        k_scale, v_scale, block_page_stride, rows, return_lse)
 
 
 # ------------------------------------------------------------------------------------------

@@ -244,6 +244,54 @@ def test_dense_topk_equals_causal_attention(kv_dtype, Hq, Hkv):
     np.testing.assert_allclose(ours, ref, rtol=0, atol=1e-12)
 
 
+def test_dense_lse_equals_torch_logsumexp():
+    """Log-sum-exp output, dense top-k: equals torch.logsumexp of the causal logits computed on
+    the unpaged sequence (a library routine on an independent path from the paged gather)."""
+    rng = np.random.default_rng(14)
+    Hq, Hkv, L, D = 8, 2, 300, 128
+    Kb = torch.randn(Hkv, L, D).to(torch.bfloat16)
+    Vb = torch.randn(Hkv, L, D).to(torch.bfloat16)
+    Kst, Vst = (t.view(torch.int16).numpy().view(np.uint16) for t in (Kb, Vb))
+    cache, bt = _paged_cache_from_logical(Kst, Vst, "bf16", rng)
+    positions = np.array([0, 1, 127, 128, 200, 299])
+    topk = np.full((1, len(positions), 4), -1, np.int32)
+    for i, p in enumerate(positions):
+        topk[0, i, :p // 128 + 1] = rng.permutation(p // 128 + 1)
+    q = torch.randn(len(positions), Hq, D).to(torch.bfloat16).double()
+    scale, ks = 0.07, 1.25
+    logits = torch.einsum("nhd,hld->nhl", q, Kb.double().repeat_interleave(Hq // Hkv, 0) * ks) * scale
+    mask = torch.from_numpy(np.arange(L)[None, :] <= positions[:, None])[:, None, :]
+    ref = torch.logsumexp(logits.masked_fill(~mask, -math.inf), dim=-1).numpy()
+    for i, p in enumerate(positions):
+        _, lse = oracle.sparse_prefill_attention(q[i:i + 1].numpy(), cache, "bf16", Hkv, topk[:, i:i + 1], bt[None],
+                                                 [0, 1], [p + 1], scale, ks, 1.0, return_lse=True)
+        np.testing.assert_allclose(lse[0], ref[i], rtol=0, atol=1e-11)
+
+
+def test_lse_with_equal_keys_is_logit_plus_log_ctx():
+    """Closed form: when every cached key is the same vector k, every logit is scale*q.k, so
+    lse = scale*q.k + ln(ctx) with ctx the row's attended-key count from the table's closed form
+    (random top-k with padding and future ids); an empty row gives -inf."""
+    rng = np.random.default_rng(15)
+    Hq, Hkv, L, D = 4, 1, 1000, 128
+    k = torch.randn(D).to(torch.bfloat16)
+    Kst = k.view(torch.int16).numpy().view(np.uint16)[None, None, :].repeat(L, 1)
+    Vst = torch.randn(Hkv, L, D).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    cache, bt = _paged_cache_from_logical(Kst, Vst, "bf16", rng)
+    q = torch.randn(1, Hq, D).to(torch.bfloat16).double().numpy()
+    scale = 0.09
+    for p in [-1, 0, 130, 511, 999]:
+        row = rng.permutation(np.arange(-1, 9))[:6].astype(np.int32)
+        _, ctx = oracle.sparse_block_table_row(row, bt, p)
+        _, lse = oracle.sparse_prefill_attention(q, cache, "bf16", Hkv, row[None, None, :], bt[None], [0, 1], [p + 1],
+                                                 scale, return_lse=True)
+        if ctx == 0:
+            assert np.all(np.isneginf(lse[0]))
+        else:
+            want = scale * (q[0] @ k.double().numpy()) + math.log(ctx)
+            np.testing.assert_allclose(lse[0], want, rtol=0, atol=1e-11)
+
+
 def test_dense_ctx_is_position_plus_one():
     rng = np.random.default_rng(5)
     bt = rng.permutation(10)

@@ -21,6 +21,7 @@ with -1):
                 top-k 32, fp8-e4m3 cache with per-tensor scales in [0.5, 2].
 * ``mixed_nvfp4`` 32 decode requests (8k..64k) plus 2 prefill chunks of 4096
                 at contexts 16k and 32k, NVFP4 cache, top-k 16.
+* ``prefill_g16`` the prefill prompts with GQA 16 (64 q heads on 4 kv heads).
 * ``small``     parameterised small cases for parity tests.
 """
 from __future__ import annotations
@@ -358,6 +359,13 @@ def prefill(device="cuda", seed: int = 1002) -> Batch:
                       future_prob=0.3, seed=seed, device=device)
 
 
+def prefill_g16(device="cuda", seed: int = 1005) -> Batch:
+    """The prefill workload's prompts with GQA 16 (64 query heads on 4 kv heads)."""
+    return make_batch("prefill_varlen_2k4k8k8k_top16_gqa16_bf16", kv_dtype="bf16", num_heads=64,
+                      num_kv_heads=4, head_dim=128, topk=16, pre_q_lens=[2048, 4096, 8192, 8192],
+                      future_prob=0.3, seed=seed, device=device)
+
+
 def mtp_fp8(device="cuda", seed: int = 1003) -> Batch:
     gen = torch.Generator()
     gen.manual_seed(seed + 3)
@@ -387,4 +395,4 @@ def small(*, kv_dtype: str = "bf16", num_heads: int = 16, num_kv_heads: int = 2,
 
 
 CONFIGS = {"tiny": tiny, "decode": decode, "prefill": prefill, "mtp_fp8": mtp_fp8,
-           "mixed_nvfp4": mixed_nvfp4}
+           "mixed_nvfp4": mixed_nvfp4, "prefill_g16": prefill_g16}
