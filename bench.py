@@ -304,6 +304,15 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
                                   "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16, "algorithmic_tflop": fl / 1e12}
     del b, p, sbt, ctxb
     torch.cuda.empty_cache()
+    # the same prompts with GQA 16 (tile = 8 tokens x 16 heads)
+    b = workloads.prefill_g16(device="cuda")
+    fl = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
+    t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream))
+    res["prefill_varlen_gqa16_bf16"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
+                                        "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
+                                        "algorithmic_tflop": fl / 1e12}
+    del b
+    torch.cuda.empty_cache()
     # fp8 MTP decode
     b = workloads.mtp_fp8(device="cuda")
     ctx = decode_ctx(pbs, b)
@@ -393,13 +402,14 @@ def reference_arm(args, world, rank):
 
 def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, peak_src):
     """One JSON line for a non-headline workload (prefill TFLOP/s, or decode GB/s for fp8/NVFP4)."""
-    make = {"prefill": workloads.prefill, "mtp_fp8": workloads.mtp_fp8, "mixed_nvfp4": workloads.mixed_nvfp4}
-    b = make[args.workload](device="cuda", seed={"prefill": 1002, "mtp_fp8": 1003, "mixed_nvfp4": 1004}[
-        args.workload] + 17 * rank)
+    make = {"prefill": workloads.prefill, "mtp_fp8": workloads.mtp_fp8, "mixed_nvfp4": workloads.mixed_nvfp4,
+            "prefill_g16": workloads.prefill_g16}
+    b = make[args.workload](device="cuda", seed={"prefill": 1002, "mtp_fp8": 1003, "mixed_nvfp4": 1004,
+                                                 "prefill_g16": 1005}[args.workload] + 17 * rank)
     if pg:
         pg.barrier()
     with ClockSampler(local) as clk:
-        if args.workload == "prefill" or (args.workload == "mixed_nvfp4" and args.part == "prefill"):
+        if args.workload in ("prefill", "prefill_g16") or (args.workload == "mixed_nvfp4" and args.part == "prefill"):
             work = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
             times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream)
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
@@ -447,7 +457,8 @@ def main():
                     help="decode requests (64 is the headline workload; smaller only for profiling)")
     ap.add_argument("--part", choices=["decode", "prefill"], default="decode",
                     help="which half of the mixed NVFP4 batch --workload mixed_nvfp4 times")
-    ap.add_argument("--workload", choices=["decode", "prefill", "mtp_fp8", "mixed_nvfp4"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "prefill", "prefill_g16", "mtp_fp8", "mixed_nvfp4"],
+                    default="decode",
                     help="timed workload (the headline line is decode; the others for profiling and tuning)")
     args = ap.parse_args()
     if args.warmup < 3:

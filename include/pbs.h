@@ -168,6 +168,11 @@ PBS_API int pbs_build_sparse_block_table_prefill(
  *               kernel folds k_scale into the softmax scale and v_scale into the output.
  *   out         [num_rows, num_heads, head_dim] bf16, strides out_row_stride / out_head_stride.
  *               A row that attends no key gets zeros.
+ *   lse         optional (NULL: not written) [num_rows, num_heads] fp32, row stride lse_row_stride
+ *               (>= num_heads, else PBS_ERR_SHAPE), head stride 1: the natural-log log-sum-exp of
+ *               each head's scaled logits, ln sum_n exp(softmax_scale * k_scale * q_h . k_n), over
+ *               the row's attended keys; -inf for a row with none. Not on the pages: it lets a
+ *               caller merge this attend with another over disjoint keys.
  *   workspace   optional (NULL, 0): see pbs_attend_workspace_bytes; too small -> PBS_ERR_SHAPE.
  */
 PBS_API int pbs_sparse_decode_attention(
@@ -179,6 +184,7 @@ PBS_API int pbs_sparse_decode_attention(
     const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
     float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
+    float* lse, int64_t lse_row_stride,
     void* workspace, size_t workspace_bytes,
     int32_t* err_word, pbs_stream_t stream);
 
@@ -230,6 +236,7 @@ PBS_API int pbs_sparse_prefill_attention(
     const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs, int32_t total_q,
     int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
+    float* lse, int64_t lse_row_stride,
     void* workspace, size_t workspace_bytes,
     int32_t* err_word, pbs_stream_t stream);
 

@@ -67,14 +67,14 @@ def lib() -> ctypes.CDLL:
     L.pbs_build_sparse_block_table_prefill.argtypes = table_common + [vp, vp, i32, i32, vp, i64, vp, vp, vp]
     attend_head = [vp, i64, i64, vp, i64, i64, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32]
     L.pbs_sparse_decode_attention.restype = ctypes.c_int
-    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp,
-                                                            ctypes.c_size_t, vp, vp]
+    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp, i64,
+                                                            vp, ctypes.c_size_t, vp, vp]
     L.pbs_sparse_decode_attention_noalloc.restype = ctypes.c_int
     L.pbs_sparse_decode_attention_noalloc.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
                                                                     vp, vp]
     L.pbs_sparse_prefill_attention.restype = ctypes.c_int
     L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
-                                                             vp, ctypes.c_size_t, vp, vp]
+                                                             vp, i64, vp, ctypes.c_size_t, vp, vp]
     L.pbs_insert_index_cache.restype = ctypes.c_int
     L.pbs_insert_index_cache.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32, vp, i64, i32, vp, vp]
     del sz
@@ -255,28 +255,43 @@ def _workspace_args(workspace, rows, num_heads, num_kv_heads, device, stream):
     return _ptr(workspace), workspace.numel()
 
 
+def _lse_arg(lse, return_lse, q):
+    """(tensor or None) for the optional log-sum-exp output [rows, Hq] fp32."""
+    if lse is None and not return_lse:
+        return None
+    if lse is None:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    _dev(lse, "lse", torch.float32, 2)
+    if lse.shape[0] != q.shape[0] or lse.shape[1] != q.shape[1] or lse.stride(1) != 1:
+        raise ValueError("lse must be [rows, Hq] float32 with a contiguous last dimension")
+    return lse
+
+
 def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
                             decode_query_len: int, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                             block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                            workspace=None):
+                            workspace=None, lse=None, return_lse: bool = False):
     """Sparse decode attend (vLLM flashinfer msa_sparse_decode_attention / nvfp4 decode call).
 
     q [rows, Hq, 128] bf16 with rows = batch * decode_query_len; kv_cache [num_pages, ...] in the
     ``kv_dtype`` page layout; returns out [rows, Hq, 128] bf16. ``workspace``: None (the default:
     splits merge inside a thread-block cluster, the faster path on GB300), "auto" (a cached
     per-stream buffer) or a zeroed uint8 tensor of at least
-    ``attend_workspace_bytes(rows, Hq, num_kv_heads)`` bytes; with one, splits merge through it."""
+    ``attend_workspace_bytes(rows, Hq, num_kv_heads)`` bytes; with one, splits merge through it.
+    With ``return_lse`` (or an ``lse`` tensor [rows, Hq] fp32) the natural-log log-sum-exp of each
+    head's scaled logits is written too and ``(out, lse)`` is returned."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
+    lse = _lse_arg(lse, return_lse, q)
     st = lib().pbs_sparse_decode_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
         _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), float(softmax_scale),
-        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), wp, wb, _ptr(err_word),
-        _stream(stream, q.device))
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
+        lse.stride(0) if lse is not None else 0, wp, wb, _ptr(err_word), _stream(stream, q.device))
     _check(st, "pbs_sparse_decode_attention")
-    return out
+    return (out, lse) if lse is not None else out
 
 
 def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
@@ -305,20 +320,22 @@ def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: in
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                              block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                             workspace=None):
+                             workspace=None, lse=None, return_lse: bool = False):
     """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
-    ``workspace`` as in :func:`sparse_decode_attention`."""
+    ``workspace``, ``lse`` and ``return_lse`` as in :func:`sparse_decode_attention`."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
+    lse = _lse_arg(lse, return_lse, q)
     st = lib().pbs_sparse_prefill_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
         _ptr(cu), _ptr(sl), sl.shape[0], q.shape[0], int(block_page_stride), float(softmax_scale), float(k_scale),
-        float(v_scale), _ptr(out), out.stride(0), out.stride(1), wp, wb, _ptr(err_word), _stream(stream, q.device))
+        float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0) if lse is not None else 0,
+        wp, wb, _ptr(err_word), _stream(stream, q.device))
     _check(st, "pbs_sparse_prefill_attention")
-    return out
+    return (out, lse) if lse is not None else out
 
 
 def insert_index_cache(index_k, index_cache, index_slot_mapping, err_word=None, stream=None) -> None:

@@ -172,6 +172,16 @@ int choose_splits(int64_t units, int k, bool workspace) {
   return s;
 }
 
+// Optional log-sum-exp output: [rows, num_heads] fp32 with a unit head stride.
+int attach_lse(AttendArgs* a, float* lse, int64_t lse_row_stride) {
+  a->lse = lse;
+  a->lse_row_stride = lse_row_stride;
+  if (lse == nullptr) return PBS_OK;
+  if (!aligned(lse, 4)) return PBS_ERR_ALIGN;
+  if (lse_row_stride < a->num_heads) return PBS_ERR_SHAPE;
+  return PBS_OK;
+}
+
 // A workspace (optional) lets splits merge through global memory. It must hold
 // attend_workspace_bytes(units) bytes, 16-byte aligned. Partials fill it from the front, the
 // per-unit tickets sit at its very end: a call of any size that fits the buffer writes partials
@@ -321,7 +331,7 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 3; }
+int pbs_abi_version(void) { return 4; }
 
 size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
   if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
@@ -400,8 +410,9 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                 int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
                                 const int32_t* seq_lens, int32_t batch, int32_t decode_query_len,
                                 int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
-                                void* out, int64_t out_row_stride, int64_t out_head_stride, void* workspace,
-                                size_t workspace_bytes, int32_t* err_word, pbs_stream_t stream) {
+                                void* out, int64_t out_row_stride, int64_t out_head_stride, float* lse,
+                                int64_t lse_row_stride, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                pbs_stream_t stream) {
   if (batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
   const int64_t rows = static_cast<int64_t>(batch) * decode_query_len;
   if (rows == 0) return PBS_OK;
@@ -419,6 +430,8 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                   out_row_stride, out_head_stride, err_word);
   a.decode_query_len = decode_query_len;
   a.num_rows = static_cast<int32_t>(rows);
+  st = attach_lse(&a, lse, lse_row_stride);
+  if (st != PBS_OK) return st;
   const int64_t units = pbs::attend_units(rows, num_kv_heads, a.group);
   st = attach_workspace(&a, units, workspace, workspace_bytes);
   if (st != PBS_OK) return st;
@@ -485,7 +498,8 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
                                  const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs,
                                  int32_t total_q, int32_t block_page_stride, float softmax_scale, float k_scale,
                                  float v_scale, void* out, int64_t out_row_stride, int64_t out_head_stride,
-                                 void* workspace, size_t workspace_bytes, int32_t* err_word, pbs_stream_t stream) {
+                                 float* lse, int64_t lse_row_stride, void* workspace, size_t workspace_bytes,
+                                 int32_t* err_word, pbs_stream_t stream) {
   if (total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
   if (total_q == 0) return PBS_OK;
   if (num_reqs == 0) return PBS_ERR_SHAPE;
@@ -504,6 +518,8 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   a.cu_seqlens_q = cu_seqlens_q;
   a.num_reqs = num_reqs;
   a.num_rows = total_q;
+  st = attach_lse(&a, lse, lse_row_stride);
+  if (st != PBS_OK) return st;
   const int64_t units = pbs::attend_units(total_q, num_kv_heads, a.group);
   st = attach_workspace(&a, units, workspace, workspace_bytes);
   if (st != PBS_OK) return st;

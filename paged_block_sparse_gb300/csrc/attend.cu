@@ -563,6 +563,8 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
       if (S == 1) {
         const float r = L > 0.f ? a.v_scale * O / L : 0.f;
         out_row[static_cast<int64_t>(gv * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(r);
+        if (a.lse != nullptr && d == 0)
+          a.lse[static_cast<int64_t>(row) * a.lse_row_stride + gv * G + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       } else if (a.split_ws != nullptr) {
         const int64_t pi = (static_cast<int64_t>(row) * gridDim.y + gv) * S + split;
         a.split_ws[pi * kWsPartial + h * kHeadDim + d] = O;
@@ -605,6 +607,8 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
         }
         const float res = L > 0.f ? a.v_scale * O / L : 0.f;
         out_row[static_cast<int64_t>(gv * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
+        if (a.lse != nullptr && d == 0)
+          a.lse[static_cast<int64_t>(row) * a.lse_row_stride + gv * G + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       }
       if (threadIdx.x == 0) a.split_tickets[unit] = 0;
     }
@@ -628,6 +632,8 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
       }
       const float res = L > 0.f ? a.v_scale * O / L : 0.f;
       out_row[static_cast<int64_t>(gv * G + h) * a.out_head_stride + d] = f32_to_bf16_bits(res);
+      if (a.lse != nullptr && d == 0)
+        a.lse[static_cast<int64_t>(row) * a.lse_row_stride + gv * G + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
     cluster.sync();  // peers may still be reading this CTA's partial
   }

@@ -594,6 +594,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
                       static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
       const float inv = (live && lsum > 0.f && ok) ? a.v_scale / lsum : 0.f;
+      // p = 2^(t - m_ref), so the row's base-2 log-sum-exp is m_ref + log2(sum p)
+      if (a.lse != nullptr && part == 0 && tt < n_tok)
+        a.lse[static_cast<int64_t>(t0 + tt) * a.lse_row_stride + g * kG + h] =
+            (live && lsum > 0.f && ok) ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int c = 0; c < kW / 32; ++c) {
         uint32_t v[32];

@@ -59,12 +59,17 @@ struct AttendArgs {
   uint16_t* out;              // bf16 bits
   int64_t out_row_stride;
   int64_t out_head_stride;
+  float* lse;                 // optional [rows, num_heads] natural-log log-sum-exp of the logits
+  int64_t lse_row_stride;
   int32_t* err_word;
   int32_t splits;             // CTAs per (row, head group) = cluster size
   int32_t packed_map;         // tmap is the 5-D one-box-per-(page, head) map of a packed cache
   float* split_ws;            // non-null: splits merge through this workspace, not a cluster
   int32_t* split_tickets;     // one arrival counter per (row, head group), zero between calls
 };
+
+// ln 2: a base-2 log-sum-exp (what the kernels track) times this is the natural-log one.
+constexpr float kLn2 = 0.693147180559945309f;
 
 // Work units of the token-centric attend: (row, head group) pairs, a head group being the query
 // heads of one kv head (two groups of 8 when a kv head serves 16).

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 3
+    assert pbs.abi_version() == 4
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"
@@ -79,12 +79,12 @@ def test_table_host_checks(L):
 def _decode_attend(L, **kw):
     a = dict(q=A, qrs=1024, qhs=128, kv=A, psb=65536, npages=100, dt=0, hq=64, hkv=8, hd=128, topk=A, trs=16,
              k=16, pt=A, pts=64, mb=64, sl=A, batch=4, dql=1, bps=8, sc=0.088, ks=1.0, vs=1.0, out=A, ors=8192,
-             ohs=128, ws=N, wsb=0)
+             ohs=128, lse=N, lses=0, ws=N, wsb=0)
     a.update(kw)
     return L.pbs_sparse_decode_attention(a["q"], a["qrs"], a["qhs"], a["kv"], a["psb"], a["npages"], a["dt"],
                                          a["hq"], a["hkv"], a["hd"], a["topk"], a["trs"], a["k"], a["pt"], a["pts"],
                                          a["mb"], a["sl"], a["batch"], a["dql"], a["bps"], a["sc"], a["ks"], a["vs"],
-                                         a["out"], a["ors"], a["ohs"], a["ws"], a["wsb"], N, S)
+                                         a["out"], a["ors"], a["ohs"], a["lse"], a["lses"], a["ws"], a["wsb"], N, S)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
@@ -103,6 +103,8 @@ def test_attend_host_checks(L):
     assert _decode_attend(L, batch=0) == 0
     assert _decode_attend(L, npages=0) == 2
     assert _decode_attend(L, k=80, trs=80) == 3
+    assert _decode_attend(L, lse=ctypes.c_void_p(0x10002), lses=64) == 4   # lse not 4-byte aligned
+    assert _decode_attend(L, lse=A, lses=63) == 2                         # lse row narrower than Hq
     need = L.pbs_attend_workspace_bytes(4, 64, 8)
     assert need == 4 * 8 * (8 * 1040 * 4 + 4)              # 8 split partials + 1 ticket per (row, kv head)
     assert L.pbs_attend_workspace_bytes(4, 128, 8) == 2 * need   # GQA 16: two head groups per kv head

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads
-from helpers import TOL, assert_close, np_i32, oracle_decode, oracle_prefill
+from helpers import TOL, assert_close, cache_source, np_i32, oracle_decode, oracle_prefill, q64
 
 pytestmark = pytest.mark.gpu
 
@@ -220,6 +220,66 @@ def test_prefill_token_kernel_workspace_splits(pbs, monkeypatch):
                         pre_q_lens=[200, 1, 90], pre_ctx_lens=[3000, 700, 5000], future_prob=0.3, seed=39)
     got = gpu_attend(pbs, b, "pre")
     assert_close(dict(enumerate(got)), oracle_prefill(b), "fp8_e4m3", "prefill workspace splits")
+
+
+# log-sum-exp output: |lse - oracle| within this bound (logits are fp32 dot products of the
+# stored values; ex2 / log2 round-off is far below it)
+LSE_TOL = 2e-3
+
+
+def _oracle_lse(b, part):
+    if part == "dec":
+        d = b.dec
+        return oracle.sparse_decode_attention(q64(d.q), cache_source(b), b.kv_dtype, b.num_kv_heads, np_i32(d.topk),
+                                              np_i32(d.page_table), np_i32(d.seq_lens), d.decode_query_len,
+                                              b.softmax_scale, b.k_scale, b.v_scale, b.block_page_stride,
+                                              return_lse=True)[1]
+    p = b.pre
+    return oracle.sparse_prefill_attention(q64(p.q), cache_source(b), b.kv_dtype, b.num_kv_heads, np_i32(p.topk),
+                                           np_i32(p.page_table), np_i32(p.cu_seqlens_q), np_i32(p.seq_lens),
+                                           b.softmax_scale, b.k_scale, b.v_scale, b.block_page_stride,
+                                           return_lse=True)[1]
+
+
+def _check_lse(got, want, what):
+    got = got.double().cpu().numpy()
+    for r, w in want.items():
+        fin = np.isfinite(w)
+        assert np.array_equal(np.isfinite(got[r]), fin), f"{what}: row {r} empty-row pattern"
+        assert np.all(np.isneginf(got[r][~fin])), f"{what}: row {r} empty heads not -inf"
+        if fin.any():
+            err = float(np.abs(got[r][fin] - w[fin]).max())
+            assert err <= LSE_TOL, f"{what}: row {r} lse error {err:.3g}"
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+@pytest.mark.parametrize("split", ["1", "4", "4ws"])
+@pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
+def test_attend_lse_decode(pbs, kv_dtype, split, heads, monkeypatch):
+    """The optional log-sum-exp of every row and head, through each merge path."""
+    monkeypatch.setenv("PBS_ATTEND_SPLITS", split[0])
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=heads[0], num_kv_heads=heads[1], topk=16,
+                        dec_seq_lens=[0, 129, 2000, 9000, 1170], decode_query_len=2, seed=60)
+    d = b.dec
+    out, lse = pbs.sparse_decode_attention(d.q, b.cache, kv_dtype, b.num_kv_heads, d.topk, d.page_table, d.seq_lens,
+                                           d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale,
+                                           workspace="auto" if split.endswith("ws") else None, return_lse=True)
+    torch.cuda.synchronize()
+    _check_lse(lse, _oracle_lse(b, "dec"), f"decode lse {kv_dtype} S={split} {heads}")
+    assert_close(dict(enumerate(out.double().cpu().numpy())), oracle_decode(b), kv_dtype, "decode out with lse")
+
+
+@pytest.mark.parametrize("kernel", ["tc", "token"])
+@pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
+def test_attend_lse_prefill(pbs, kernel, heads, monkeypatch):
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
+    b = workloads.small(device=DEV, num_heads=heads[0], num_kv_heads=heads[1], topk=8, pre_q_lens=[37, 200, 1],
+                        pre_ctx_lens=[0, 700, 3000], future_prob=0.3, seed=61)
+    p = b.pre
+    out, lse = pbs.sparse_prefill_attention(p.q, b.cache, "bf16", b.num_kv_heads, p.topk, p.page_table,
+                                            p.cu_seqlens_q, p.seq_lens, b.softmax_scale, return_lse=True)
+    torch.cuda.synchronize()
+    _check_lse(lse, _oracle_lse(b, "pre"), f"prefill lse {kernel} {heads}")
 
 
 def test_attend_empty_rows_are_zero(pbs):
