@@ -424,6 +424,10 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
         ms = float(t.item())
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     achieved = work / (statistics.mean(times) * 1e-3) / scale
+    traffic = None
+    if args.workload == "prefill":
+        traffic = recorded_traffic("prefill_tc_prefill_varlen_bf16.md",
+                                   kernel_source_hash("attend_prefill_tc.cu", "tc_device.cuh", "pbs_device.cuh"))
     if rank == 0:
         print(json.dumps({
             "metric": metric, "value": world * work / (ms * 1e-3) / scale, "unit": unit, "n_gpus": world,
@@ -432,7 +436,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             "data": "synthetic", "config": {"workload": b.name, "part": args.part,
                                             "l2": L2_NOTE},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                         "traffic": None, "peak_source": f"{peak_src} (burst, kernel timed alone)",
+                         "traffic": traffic, "peak_source": f"{peak_src} (burst, kernel timed alone)",
                          "algorithmic_work_per_launch": work},
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
     if pg:

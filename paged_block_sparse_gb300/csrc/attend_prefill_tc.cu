@@ -374,12 +374,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, g * kG, t0);
     }
     const int32_t* bt_row = a.page_table + static_cast<int64_t>(req) * a.pt_row_stride;
-    int next_phys = nU > 0 ? __ldg(bt_row + ctl->union_blk[0]) : 0;
+    int phys_lane = 0;
     int issued = 0;
     for (int i = 0; i < nU; ++i) {
       const int st = i % kStagesTc;
-      const int phys = next_phys;
-      if (i + 1 < nU) next_phys = __ldg(bt_row + ctl->union_blk[i + 1]);
+      if ((i & 31) == 0) phys_lane = i + lane < nU ? __ldg(bt_row + ctl->union_blk[i + lane]) : 0;
+      const int phys = __shfl_sync(0xffffffffu, phys_lane, i & 31);
       bool go = true;
       if (lane == 0 && i >= kStagesTc)
         go = wait_or_abort(&ctl->kv_empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word);
