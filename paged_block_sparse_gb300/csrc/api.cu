@@ -131,6 +131,15 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
 // Which prefill kernel runs: the tcgen05 tile kernel where it applies, the token-centric
 // kernel otherwise. PBS_PREFILL_KERNEL=token forces the token-centric one, =tc requires the
 // tile kernel (tests, tuning).
+//
+// The tile kernel streams the union of its 16 tokens' selections to all of them, so its waste
+// grows with the context a token chooses from: a token at block s selects k of s + 1 blocks,
+// and the union nears min(s + 1, 16 k). The page table's width bounds every context, and only
+// the host sees it without a device read, so the tile kernel is taken while
+// max_blocks <= kTileMaxBlocksPerTopk * k. Measured (bf16, 64/8 heads, top-k 16, 2 x 4096
+// tokens): contexts 0 / 2k-4k / 16k-32k give 462 / 312 / 114 TFLOP/s on the tile kernel and
+// 133 / 139 / 139 on the token-centric one.
+constexpr int kTileMaxBlocksPerTopk = 8;
 int prefill_kernel_override() {
   if (const char* env = std::getenv("PBS_PREFILL_KERNEL")) {
     if (std::strcmp(env, "token") == 0) return 1;
@@ -530,8 +539,9 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   cudaError_t e;
   const int force = prefill_kernel_override();
   // the tile kernel reads the packed bf16 cache through the 5-D map
-  const bool tc_ok = force != 1 && a.packed_map != 0 && pbs::prefill_tc_supported(a);
-  if (force == 2 && !tc_ok) return PBS_ERR_UNSUPPORTED;
+  const bool tc_fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
+  if (force == 2 && !tc_fits) return PBS_ERR_UNSUPPORTED;
+  const bool tc_ok = force == 2 || (force == 0 && tc_fits && max_blocks <= kTileMaxBlocksPerTopk * topk_k);
   if (tc_ok) {
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
