@@ -329,8 +329,21 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     td = statistics.median(run_decode(pbs, b, steps, warmup, flush, stream))
     fl = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
     tp = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream))
+    # the same batch through the one-call mixed entry (decode rows then prefill tokens)
+    d, p = b.dec, b.pre
+    qm = torch.cat([d.q, p.q])
+    tkm = torch.cat([d.topk[0], p.topk[0]])
+    om = torch.empty_like(qm)
+
+    def mstep():
+        pbs.sparse_mixed_attention(qm, b.cache, b.kv_dtype, b.num_kv_heads, tkm, d.page_table, d.seq_lens,
+                                   d.decode_query_len, p.page_table, p.cu_seqlens_q, p.seq_lens, b.softmax_scale,
+                                   b.k_scale, b.v_scale, b.block_page_stride, out=om, stream=stream)
+    tm = statistics.median(time_steps(mstep, max(2, steps // 4), min(warmup, 3), flush, stream))
     res["mixed_nvfp4"] = {"decode_ms": td, "decode_GB/s": by / (td * 1e-3) / 1e9,
-                          "prefill_ms": tp, "prefill_TFLOP/s": fl / (tp * 1e-3) / 1e12, "total_ms": td + tp}
+                          "prefill_ms": tp, "prefill_TFLOP/s": fl / (tp * 1e-3) / 1e12, "total_ms": td + tp,
+                          "one_call_ms": tm}
+    del qm, tkm, om
     del b
     torch.cuda.empty_cache()
     return res

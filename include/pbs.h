@@ -241,6 +241,32 @@ PBS_API int pbs_sparse_prefill_attention(
     int32_t* err_word, pbs_stream_t stream);
 
 /*
+ * Mixed batch in one call ([flashinfer] forward with both parts: decode rows q[:nd], prefill
+ * tokens q[nd:], one token-major top-k buffer for all of them). Rows [0, nd), nd = batch *
+ * decode_query_len, are decode rows read with dec_page_table / dec_seq_lens / decode_query_len
+ * as in pbs_sparse_decode_attention; rows [nd, nd + total_q) are prefill tokens read with
+ * pre_page_table / cu_seqlens_q / pre_seq_lens as in pbs_sparse_prefill_attention. q, topk,
+ * out and lse are indexed by that row over both parts. Where the prefill part takes the tcgen05
+ * tile kernel this issues the two calls on `stream`, decode first (what the page's forward
+ * does); otherwise it is one launch of the token-centric kernel, whose CTAs take their part by
+ * row, so the decode rows run beside the prefill tokens. No workspace. Errors as in the two
+ * calls; with no rows in one part it is that part's call.
+ */
+PBS_API int pbs_sparse_mixed_attention(
+    const void* q, int64_t q_row_stride, int64_t q_head_stride,
+    const void* kv_cache, int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
+    const int32_t* dec_page_table, int64_t dec_pt_row_stride, int32_t dec_max_blocks,
+    const int32_t* dec_seq_lens, int32_t batch, int32_t decode_query_len,
+    const int32_t* pre_page_table, int64_t pre_pt_row_stride, int32_t pre_max_blocks,
+    const int32_t* cu_seqlens_q, const int32_t* pre_seq_lens, int32_t num_reqs, int32_t total_q,
+    int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
+    void* out, int64_t out_row_stride, int64_t out_head_stride,
+    float* lse, int64_t lse_row_stride,
+    int32_t* err_word, pbs_stream_t stream);
+
+/*
  * Index-cache insert ([sparse_pa] minimax_m3_insert_index_cache): for n < num_tokens,
  * index_cache[slot / block_tokens, slot % block_tokens, :] = index_k[n, :] with
  * slot = slot_mapping[n * slot_stride]. A negative slot is padding and is skipped; a slot

@@ -20,7 +20,7 @@ __all__ = [
     "PbsError", "KV_DTYPES", "SPARSE_BLOCK_SIZE", "PAGES_PER_BLOCK", "PAGE_ROWS", "library_path", "lib",
     "abi_version", "status_string", "build_sparse_block_table_decode", "build_sparse_block_table_prefill",
     "sparse_decode_attention", "sparse_prefill_attention", "insert_index_cache", "DEVERR",
-    "attend_workspace_bytes", "attend_workspace", "sparse_decode_attention_noalloc",
+    "attend_workspace_bytes", "attend_workspace", "sparse_decode_attention_noalloc", "sparse_mixed_attention",
 ]
 
 SPARSE_BLOCK_SIZE = 128
@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
     L.pbs_sparse_prefill_attention.restype = ctypes.c_int
     L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
                                                              vp, i64, vp, ctypes.c_size_t, vp, vp]
+    L.pbs_sparse_mixed_attention.restype = ctypes.c_int
+    L.pbs_sparse_mixed_attention.argtypes = attend_head[:13] + [vp, i64, i32, vp, i32, i32, vp, i64, i32, vp, vp, i32,
+                                                                i32, i32, f32, f32, f32, vp, i64, i64, vp, i64, vp, vp]
     L.pbs_insert_index_cache.restype = ctypes.c_int
     L.pbs_insert_index_cache.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32, vp, i64, i32, vp, vp]
     del sz
@@ -335,6 +338,34 @@ def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk
         float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0) if lse is not None else 0,
         wp, wb, _ptr(err_word), _stream(stream, q.device))
     _check(st, "pbs_sparse_prefill_attention")
+    return (out, lse) if lse is not None else out
+
+
+def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, dec_page_table, dec_seq_lens,
+                           decode_query_len: int, pre_page_table, cu_seqlens_q, pre_seq_lens, softmax_scale: float,
+                           k_scale: float = 1.0, v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK,
+                           out=None, err_word=None, stream=None, lse=None, return_lse: bool = False):
+    """Decode rows then prefill tokens in one call (vLLM flashinfer forward with both parts):
+    q [nd + total_q, Hq, 128] with nd = len(dec_seq_lens) * decode_query_len; topk one row per
+    q row. Returns out (and lse)."""
+    num_pages, psb, tk, pt_d, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, dec_page_table, out)
+    pt_p = _table2d(pre_page_table, "pre_page_table")
+    sl_d = _dev(dec_seq_lens, "dec_seq_lens", torch.int32)
+    cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    sl_p = _dev(pre_seq_lens, "pre_seq_lens", torch.int32)
+    nd = sl_d.shape[0] * int(decode_query_len)
+    total_q = q.shape[0] - nd
+    if total_q < 0:
+        raise ValueError(f"q has {q.shape[0]} rows, fewer than the {nd} decode rows")
+    lse = _lse_arg(lse, return_lse, q)
+    st = lib().pbs_sparse_mixed_attention(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
+        int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt_d), pt_d.stride(0),
+        pt_d.shape[1], _ptr(sl_d), sl_d.shape[0], int(decode_query_len), _ptr(pt_p), pt_p.stride(0), pt_p.shape[1],
+        _ptr(cu), _ptr(sl_p), sl_p.shape[0], total_q, int(block_page_stride), float(softmax_scale), float(k_scale),
+        float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0) if lse is not None else 0,
+        _ptr(err_word), _stream(stream, q.device))
+    _check(st, "pbs_sparse_mixed_attention")
     return (out, lse) if lse is not None else out
 
 

@@ -140,12 +140,24 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
 // tokens): contexts 0 / 2k-4k / 16k-32k give 462 / 312 / 114 TFLOP/s on the tile kernel and
 // 133 / 139 / 139 on the token-centric one.
 constexpr int kTileMaxBlocksPerTopk = 8;
+
 int prefill_kernel_override() {
   if (const char* env = std::getenv("PBS_PREFILL_KERNEL")) {
     if (std::strcmp(env, "token") == 0) return 1;
     if (std::strcmp(env, "tc") == 0) return 2;
   }
   return 0;
+}
+
+// Sets *use_tile for a prefill call whose AttendArgs (map already encoded) are `a`;
+// PBS_ERR_UNSUPPORTED when PBS_PREFILL_KERNEL=tc asks for a tile kernel that cannot run.
+int choose_prefill_kernel(const AttendArgs& a, bool* use_tile) {
+  const int force = prefill_kernel_override();
+  // the tile kernel reads the packed bf16 cache through the 5-D map
+  const bool fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
+  if (force == 2 && !fits) return PBS_ERR_UNSUPPORTED;
+  *use_tile = force == 2 || (force == 0 && fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k);
+  return PBS_OK;
 }
 
 // CTAs per (row, kv head). Splitting a row across a cluster costs a cluster barrier, a DSMEM
@@ -340,7 +352,7 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 4; }
+int pbs_abi_version(void) { return 5; }
 
 size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
   if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
@@ -448,7 +460,7 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
-  return pbs::launch_attend(a, false, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+  return pbs::launch_attend(a, pbs::kModeDecode, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
                                                                                                   : PBS_ERR_CUDA;
 }
 
@@ -496,7 +508,7 @@ int pbs_sparse_decode_attention_noalloc(const void* q, int64_t q_row_stride, int
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
-  return pbs::launch_attend(a, false, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
+  return pbs::launch_attend(a, pbs::kModeDecode, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
                                                                                                   : PBS_ERR_CUDA;
 }
 
@@ -537,20 +549,115 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
   cudaError_t e;
-  const int force = prefill_kernel_override();
-  // the tile kernel reads the packed bf16 cache through the 5-D map
-  const bool tc_fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
-  if (force == 2 && !tc_fits) return PBS_ERR_UNSUPPORTED;
-  const bool tc_ok = force == 2 || (force == 0 && tc_fits && max_blocks <= kTileMaxBlocksPerTopk * topk_k);
+  bool tc_ok = false;
+  st = choose_prefill_kernel(a, &tc_ok);
+  if (st != PBS_OK) return st;
   if (tc_ok) {
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
     e = pbs::launch_prefill_tc(a, map, qmap, reinterpret_cast<cudaStream_t>(stream));
   } else {
-    e = pbs::launch_attend(a, true, map, reinterpret_cast<cudaStream_t>(stream));
+    e = pbs::launch_attend(a, pbs::kModePrefill, map, reinterpret_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PBS_OK : PBS_ERR_CUDA;
+}
+
+int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,
+                               int64_t page_stride_bytes, int64_t num_pages, int32_t kv_dtype, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, const int32_t* topk, int64_t topk_row_stride,
+                               int32_t topk_k, const int32_t* dec_page_table, int64_t dec_pt_row_stride,
+                               int32_t dec_max_blocks, const int32_t* dec_seq_lens, int32_t batch,
+                               int32_t decode_query_len, const int32_t* pre_page_table, int64_t pre_pt_row_stride,
+                               int32_t pre_max_blocks, const int32_t* cu_seqlens_q, const int32_t* pre_seq_lens,
+                               int32_t num_reqs, int32_t total_q, int32_t block_page_stride, float softmax_scale,
+                               float k_scale, float v_scale, void* out, int64_t out_row_stride,
+                               int64_t out_head_stride, float* lse, int64_t lse_row_stride, int32_t* err_word,
+                               pbs_stream_t stream) {
+  if (batch < 0 || decode_query_len <= 0 || total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
+  const int64_t nd = static_cast<int64_t>(batch) * decode_query_len;
+  // one part only: the plain entry points
+  if (total_q == 0)
+    return pbs_sparse_decode_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
+                                       kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,
+                                       dec_page_table, dec_pt_row_stride, dec_max_blocks, dec_seq_lens, batch,
+                                       decode_query_len, block_page_stride, softmax_scale, k_scale, v_scale, out,
+                                       out_row_stride, out_head_stride, lse, lse_row_stride, nullptr, 0, err_word,
+                                       stream);
+  if (nd == 0)
+    return pbs_sparse_prefill_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
+                                        kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,
+                                        pre_page_table, pre_pt_row_stride, pre_max_blocks, cu_seqlens_q, pre_seq_lens,
+                                        num_reqs, total_q, block_page_stride, softmax_scale, k_scale, v_scale, out,
+                                        out_row_stride, out_head_stride, lse, lse_row_stride, nullptr, 0, err_word,
+                                        stream);
+  if (num_reqs == 0) return PBS_ERR_SHAPE;
+  if (nd + total_q > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
+  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
+                        out_head_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, dec_page_table, dec_pt_row_stride, dec_max_blocks,
+                          block_page_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, pre_page_table, pre_pt_row_stride, pre_max_blocks,
+                          block_page_stride);
+  if (st != PBS_OK) return st;
+  if (dec_seq_lens == nullptr || cu_seqlens_q == nullptr || pre_seq_lens == nullptr) return PBS_ERR_ARG;
+
+  // the prefill part as its own call would see: rows from nd on
+  const void* q_pre = static_cast<const uint8_t*>(q) + nd * q_row_stride * 2;
+  const int32_t* topk_pre = topk + nd * topk_row_stride;
+  void* out_pre = static_cast<uint8_t*>(out) + nd * out_row_stride * 2;
+  float* lse_pre = lse != nullptr ? lse + nd * lse_row_stride : nullptr;
+  AttendArgs p = make_attend_args(q_pre, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
+                                  kv_dtype, num_heads, num_kv_heads, topk_pre, topk_row_stride, topk_k,
+                                  pre_page_table, pre_pt_row_stride, pre_max_blocks, pre_seq_lens,
+                                  block_page_stride, softmax_scale, k_scale, v_scale, out_pre, out_row_stride,
+                                  out_head_stride, err_word);
+  CUtensorMap map;
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &p.packed_map);
+  if (st != PBS_OK) return st;
+  bool tile = false;
+  st = choose_prefill_kernel(p, &tile);
+  if (st != PBS_OK) return st;
+  if (tile) {
+    // the prefill part runs on the tcgen05 tile kernel: two launches, decode first
+    st = pbs_sparse_decode_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
+                                     kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,
+                                     dec_page_table, dec_pt_row_stride, dec_max_blocks, dec_seq_lens, batch,
+                                     decode_query_len, block_page_stride, softmax_scale, k_scale, v_scale, out,
+                                     out_row_stride, out_head_stride, lse, lse_row_stride, nullptr, 0, err_word,
+                                     stream);
+    if (st != PBS_OK) return st;
+    return pbs_sparse_prefill_attention(q_pre, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
+                                        kv_dtype, num_heads, num_kv_heads, head_dim, topk_pre, topk_row_stride,
+                                        topk_k, pre_page_table, pre_pt_row_stride, pre_max_blocks, cu_seqlens_q,
+                                        pre_seq_lens, num_reqs, total_q, block_page_stride, softmax_scale, k_scale,
+                                        v_scale, out_pre, out_row_stride, out_head_stride, lse_pre, lse_row_stride,
+                                        nullptr, 0, err_word, stream);
+  }
+  // both parts on the token-centric kernel: one launch, each CTA picks its part by row
+  AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
+                                  num_heads, num_kv_heads, topk, topk_row_stride, topk_k, dec_page_table,
+                                  dec_pt_row_stride, dec_max_blocks, dec_seq_lens, block_page_stride, softmax_scale,
+                                  k_scale, v_scale, out, out_row_stride, out_head_stride, err_word);
+  a.decode_query_len = decode_query_len;
+  a.num_dec_rows = static_cast<int32_t>(nd);
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.num_reqs = num_reqs;
+  a.pre_page_table = pre_page_table;
+  a.pre_pt_row_stride = pre_pt_row_stride;
+  a.pre_max_blocks = pre_max_blocks;
+  a.pre_seq_lens = pre_seq_lens;
+  a.num_rows = static_cast<int32_t>(nd + total_q);
+  a.packed_map = p.packed_map;
+  st = attach_lse(&a, lse, lse_row_stride);
+  if (st != PBS_OK) return st;
+  a.splits = choose_splits(pbs::attend_units(nd + total_q, num_kv_heads, a.group), topk_k, false);
+  return pbs::launch_attend(a, pbs::kModeMixed, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PBS_OK
+             : PBS_ERR_CUDA;
 }
 
 int pbs_insert_index_cache(const void* index_k, int64_t k_stride0, int64_t k_stride1, int32_t num_tokens, int32_t dim,

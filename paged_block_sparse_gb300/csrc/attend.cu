@@ -191,7 +191,7 @@ __device__ unsigned long long g_dtrace[kDTraceCtas][4];
 #define DTRACE(k, v) do { } while (0)
 #endif
 
-template <int FMT, bool PREFILL, bool PACKED>
+template <int FMT, int MODE, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_constant__ CUtensorMap tmap,
                                                              const AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -224,15 +224,27 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     fence_mbar_init();
   }
 
+  // the row's position, and the page table its request reads
   int req, abs_pos;
-  if (PREFILL) prefill_position(row, a.cu_seqlens_q, a.num_reqs, a.seq_lens, req, abs_pos);
-  else decode_position(row, a.decode_query_len, a.seq_lens, req, abs_pos);
+  const int32_t* pt = a.page_table;
+  int64_t pt_stride = a.pt_row_stride;
+  int max_blocks = a.max_blocks;
+  if (MODE == kModePrefill) {
+    prefill_position(row, a.cu_seqlens_q, a.num_reqs, a.seq_lens, req, abs_pos);
+  } else if (MODE == kModeDecode || row < a.num_dec_rows) {
+    decode_position(row, a.decode_query_len, a.seq_lens, req, abs_pos);
+  } else {
+    prefill_position(row - a.num_dec_rows, a.cu_seqlens_q, a.num_reqs, a.pre_seq_lens, req, abs_pos);
+    pt = a.pre_page_table;
+    pt_stride = a.pre_pt_row_stride;
+    max_blocks = a.pre_max_blocks;
+  }
 
   // ---- producer warp: the row's compaction; consumers: Q fragments --------------------------
   uint32_t qf[8][2];
   if (warp == kConsumerWarps) {
     RowCompaction rc = compact_row(a.topk + static_cast<int64_t>(row) * a.topk_row_stride, a.k, abs_pos,
-                                   a.page_table + static_cast<int64_t>(req) * a.pt_row_stride, a.max_blocks,
+                                   pt + static_cast<int64_t>(req) * pt_stride, max_blocks,
                                    a.block_page_stride, ctl->slot_base);
     bool page_bad = false;
     for (int s = lane; s < rc.n_written; s += 32) {
@@ -640,10 +652,10 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
   if (threadIdx.x == 0) DTRACE(3, global_timer_ns());
 }
 
-template <int FMT, bool PREFILL, bool PACKED>
+template <int FMT, int MODE, bool PACKED>
 cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& tmap, cudaStream_t stream) {
   constexpr size_t smem = smem_bytes<FMT>();
-  auto kern = attend_kernel<FMT, PREFILL, PACKED>;
+  auto kern = attend_kernel<FMT, MODE, PACKED>;
   // dynamic shared memory above 48 KB must be opted into (per device; cheap to repeat)
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -675,24 +687,27 @@ extern "C" __attribute__((visibility("default"))) int pbs_debug_dtrace_get(unsig
 namespace pbs {
 #endif
 
-cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream) {
+template <int FMT, bool PACKED>
+cudaError_t launch_mode(const AttendArgs& a, int mode, const CUtensorMap& tmap, cudaStream_t stream) {
+  switch (mode) {
+    case kModeDecode: return launch_one<FMT, kModeDecode, PACKED>(a, tmap, stream);
+    case kModePrefill: return launch_one<FMT, kModePrefill, PACKED>(a, tmap, stream);
+    case kModeMixed: return launch_one<FMT, kModeMixed, PACKED>(a, tmap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_attend(const AttendArgs& a, int mode, const CUtensorMap& tmap, cudaStream_t stream) {
   const bool packed = a.packed_map != 0;
   switch (a.kv_dtype) {
     case PBS_KV_BF16:
-      if (packed)
-        return prefill ? launch_one<PBS_KV_BF16, true, true>(a, tmap, stream)
-                       : launch_one<PBS_KV_BF16, false, true>(a, tmap, stream);
-      return prefill ? launch_one<PBS_KV_BF16, true, false>(a, tmap, stream)
-                     : launch_one<PBS_KV_BF16, false, false>(a, tmap, stream);
+      return packed ? launch_mode<PBS_KV_BF16, true>(a, mode, tmap, stream)
+                    : launch_mode<PBS_KV_BF16, false>(a, mode, tmap, stream);
     case PBS_KV_FP8_E4M3:
-      if (packed)
-        return prefill ? launch_one<PBS_KV_FP8_E4M3, true, true>(a, tmap, stream)
-                       : launch_one<PBS_KV_FP8_E4M3, false, true>(a, tmap, stream);
-      return prefill ? launch_one<PBS_KV_FP8_E4M3, true, false>(a, tmap, stream)
-                     : launch_one<PBS_KV_FP8_E4M3, false, false>(a, tmap, stream);
+      return packed ? launch_mode<PBS_KV_FP8_E4M3, true>(a, mode, tmap, stream)
+                    : launch_mode<PBS_KV_FP8_E4M3, false>(a, mode, tmap, stream);
     case PBS_KV_NVFP4:
-      return prefill ? launch_one<PBS_KV_NVFP4, true, false>(a, tmap, stream)
-                     : launch_one<PBS_KV_NVFP4, false, false>(a, tmap, stream);
+      return launch_mode<PBS_KV_NVFP4, false>(a, mode, tmap, stream);
     default:
       return cudaErrorInvalidValue;
   }

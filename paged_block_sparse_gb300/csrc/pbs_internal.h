@@ -52,6 +52,13 @@ struct AttendArgs {
   int32_t decode_query_len;   // decode mode
   const int32_t* cu_seqlens_q;  // prefill mode
   int32_t num_reqs;
+  // mixed mode: rows [0, num_dec_rows) are decode rows (page_table, seq_lens, decode_query_len
+  // above), the rest prefill tokens with their own page table and sequence lengths
+  int32_t num_dec_rows;
+  const int32_t* pre_page_table;
+  int64_t pre_pt_row_stride;
+  int32_t pre_max_blocks;
+  const int32_t* pre_seq_lens;
   int32_t num_rows;
   int32_t block_page_stride;
   float scale_log2;           // softmax_scale * k_scale * log2(e)
@@ -88,8 +95,12 @@ inline size_t attend_workspace_bytes(int64_t units) {
 
 // Launch the attend; `tmap` is a tensor map over the cache rows for the bf16/fp8 formats
 // (unused for NVFP4): 4-D (one box per quarter / half row) or, with a.packed_map, 5-D (one box
-// per page and head). Returns the launch status.
-cudaError_t launch_attend(const AttendArgs& a, bool prefill, const CUtensorMap& tmap, cudaStream_t stream);
+// per page and head). `mode`: kModeDecode, kModePrefill or kModeMixed (decode rows then prefill
+// tokens in one launch). Returns the launch status.
+constexpr int kModeDecode = 0;
+constexpr int kModePrefill = 1;
+constexpr int kModeMixed = 2;
+cudaError_t launch_attend(const AttendArgs& a, int mode, const CUtensorMap& tmap, cudaStream_t stream);
 
 // Prefill attend on tcgen05 tensor cores (bf16 cache, GQA 8, top-k <= 16, 16-byte aligned q/out
 // rows). `q_map` is a 3-D tensor map {head_dim, heads, tokens} with a {64, 8, 16} box.

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 4
+    assert pbs.abi_version() == 5
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"

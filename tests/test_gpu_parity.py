@@ -437,6 +437,53 @@ def test_attend_per_quarter_map(pbs, kv_dtype, monkeypatch):
     assert_close(dict(enumerate(gpu_attend(pbs, b, "dec"))), oracle_decode(b), kv_dtype, "decode 4-D map")
 
 
+@pytest.mark.parametrize("kv_dtype,prefill_kernel", [("bf16", "tc"), ("bf16", "token"), ("fp8_e4m3", None),
+                                                     ("nvfp4", None)])
+def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel, monkeypatch):
+    """Decode rows then prefill tokens through pbs_sparse_mixed_attention: one fused launch of the
+    token-centric kernel, or decode + tile kernel when the prefill part takes the tile kernel;
+    outputs and log-sum-exp against the oracle's decode and prefill attends."""
+    if prefill_kernel:
+        monkeypatch.setenv("PBS_PREFILL_KERNEL", prefill_kernel)
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8, topk=12,
+                        dec_seq_lens=[2500, 0, 9000], decode_query_len=2, pre_q_lens=[150, 1, 60],
+                        pre_ctx_lens=[0, 900, 2000], future_prob=0.3, seed=54)
+    d, p = b.dec, b.pre
+    nd = d.q.shape[0]
+    q = torch.cat([d.q, p.q])
+    topk = torch.cat([d.topk[0], p.topk[0]])
+    out, lse = pbs.sparse_mixed_attention(q, b.cache, kv_dtype, b.num_kv_heads, topk, d.page_table, d.seq_lens,
+                                          d.decode_query_len, p.page_table, p.cu_seqlens_q, p.seq_lens,
+                                          b.softmax_scale, b.k_scale, b.v_scale, return_lse=True)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert_close(dict(enumerate(got[:nd])), oracle_decode(b), kv_dtype, "mixed: decode rows")
+    assert_close(dict(enumerate(got[nd:])), oracle_prefill(b), kv_dtype, "mixed: prefill rows")
+    _check_lse(lse[:nd], _oracle_lse(b, "dec"), "mixed lse decode")
+    _check_lse(lse[nd:], _oracle_lse(b, "pre"), "mixed lse prefill")
+
+
+@pytest.mark.parametrize("part", ["dec", "tc", "token"])
+def test_attend_side_packed_blocks(pbs, part, monkeypatch):
+    """block_page_stride 16 ([sparse_pa] minimax_m3_sparse_block_page_stride with packed sides):
+    block b's pages are 16 b + j, j < 8; the other 8 pages of each block hold NaN and must not be
+    read."""
+    if part != "dec":
+        monkeypatch.setenv("PBS_PREFILL_KERNEL", part)
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, dec_seq_lens=[3000, 700],
+                        pre_q_lens=[200, 40], pre_ctx_lens=[900, 0], future_prob=0.3, seed=53)
+    nblk = b.num_pages // 8
+    wide = torch.full((nblk * 16, b.page_bytes), 0xFF, dtype=torch.uint8, device=DEV)
+    wide.view(nblk, 16, -1)[:, :8] = b.cache.view(nblk, 8, -1)
+    b.cache = wide
+    b.block_page_stride = 16
+    err = _err()
+    got = gpu_attend(pbs, b, "dec" if part == "dec" else "pre", err)
+    assert int(err.item()) == 0
+    want = oracle_decode(b) if part == "dec" else oracle_prefill(b)
+    assert_close(dict(enumerate(got)), want, "bf16", f"side-packed {part}")
+
+
 def test_attend_strided_pages(pbs):
     """A cache whose pages are not back to back (page stride > content) uses the 4-D map."""
     b = workloads.small(device=DEV, num_heads=16, num_kv_heads=2, topk=6, dec_seq_lens=[700, 1500], seed=52)
