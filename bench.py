@@ -54,6 +54,20 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, pg, device) -> float:
+    """The slowest rank's step time (every rank gets it): the job is as fast as its slowest replica."""
+    if pg is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank units in (at most) ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -430,11 +444,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             work = decode_bytes(b, decode_ctx(pbs, b))
             times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
             unit, bound, peak, metric = "GB/s", "hbm", hbm, "decode HBM GB/s"
-    ms = statistics.mean(times)
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times), pg, "cuda")
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     achieved = work / (statistics.mean(times) * 1e-3) / scale
     traffic = None
@@ -443,7 +453,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                                    kernel_source_hash("attend_prefill_tc.cu", "tc_device.cuh", "pbs_device.cuh"))
     if rank == 0:
         print(json.dumps({
-            "metric": metric, "value": world * work / (ms * 1e-3) / scale, "unit": unit, "n_gpus": world,
+            "metric": metric, "value": job_rate(world, work, ms) / scale, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
             "data": "synthetic", "config": {"workload": b.name, "part": args.part,
@@ -514,19 +524,17 @@ def main():
     with ClockSampler(local) as clk:
         times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
-    ms = statistics.mean(times)
+    ms = max_over_ranks(statistics.mean(times), pg, "cuda")
     if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
         pg.barrier()
-    value = world * rows / (ms * 1e-3)
+    value = job_rate(world, rows, ms)
     achieved = by / (statistics.mean(times) * 1e-3) / 1e9
     src_hash = kernel_source_hash("attend.cu", "pbs_device.cuh")
     traffic = recorded_traffic("attend_decode_b64_bf16.md", src_hash)
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if args.no_e2e else e2e_decode(pbs, b, max(3, args.steps // 2), 3,
                                                                              stream)
+    e2e_ms = max_over_ranks(e2e_ms, pg, "cuda")
     extra = {}
     if not args.no_extra and rank == 0:
         del b
@@ -558,7 +566,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
                          "algorithmic_bytes_per_launch": by},
-            "e2e": {"value": world * rows / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(world, rows, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
