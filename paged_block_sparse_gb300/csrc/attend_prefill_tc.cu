@@ -68,6 +68,7 @@ struct TcCtl {
   uint32_t tmem_base;
   int32_t n_union;
   int32_t req, t0, n_tok;
+  int32_t c0, ctx0, pos_last;  // request's first token row, context length, last position
   int32_t bad_mask;   // tokens whose row hit an out-of-range block id
   int32_t abort;
   int32_t own[kTokMax];  // own block of each token (-1: none)
@@ -220,12 +221,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   // ---- tile -> (request, first token): tiles are numbered request by request ----------------
   if (warp == 0) {
-    int r = -1, t0 = 0, n = 0;
+    int r = -1, t0 = 0, n = 0, c0 = 0, ctx0 = 0, seq_len = 0;
     int base_tiles = 0;
     for (int r0 = 0; r0 < a.num_reqs && r < 0; r0 += 32) {
       const int rr = r0 + lane;
-      int q_len = 0;
-      if (rr < a.num_reqs) q_len = __ldg(a.cu_seqlens_q + rr + 1) - __ldg(a.cu_seqlens_q + rr);
+      // every lane loads its request's bounds and length at once (one round trip)
+      int q_len = 0, cb = 0, sl = 0;
+      if (rr < a.num_reqs) {
+        cb = __ldg(a.cu_seqlens_q + rr);
+        q_len = __ldg(a.cu_seqlens_q + rr + 1) - cb;
+        sl = __ldg(a.seq_lens + rr);
+      }
       const int tiles = (q_len + kTok - 1) / kTok;
       int incl = tiles;
 #pragma unroll
@@ -242,7 +248,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int ex = __shfl_sync(0xffffffffu, excl, src);
         const int ql = __shfl_sync(0xffffffffu, q_len, src);
         const int tile = static_cast<int>(blockIdx.x) - ex;
-        t0 = __ldg(a.cu_seqlens_q + r) + tile * kTok;
+        c0 = __shfl_sync(0xffffffffu, cb, src);
+        seq_len = __shfl_sync(0xffffffffu, sl, src);
+        ctx0 = seq_len - ql;
+        t0 = c0 + tile * kTok;
         n = min(kTok, ql - tile * kTok);
       }
       base_tiles += __shfl_sync(0xffffffffu, incl, 31);
@@ -253,6 +262,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                            (*reinterpret_cast<volatile int32_t*>(a.err_word) & PBS_DEVERR_TIMEOUT) != 0;
       ctl->req = r;
       ctl->t0 = t0;
+      ctl->c0 = c0;
+      ctl->ctx0 = ctx0;
+      ctl->pos_last = seq_len - 1;
       ctl->n_tok = (r < 0 || gave_up) ? 0 : n;
       ctl->bad_mask = 0;
       ctl->abort = 0;
@@ -276,13 +288,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // ---- each token's distinct valid blocks, sorted, plus the union bitmap ---------------------
   // The union is built as a bitmap over the block ids in the last K/V stage (free until the loop).
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(kv_s + (kStagesTc - 1) * kKVBytes);
-  const int pos_last = __ldg(a.seq_lens + req) - 1;  // position of the request's last token
+  const int pos_last = ctl->pos_last;  // position of the request's last token
   // valid block ids are <= pos_last / 128 and < max_blocks (<= 65536): at most 2048 words
   const int nwords = min(max(pos_last, 0) / kSparseBlock / 32 + 1, (a.max_blocks + 31) / 32);
   for (int w = threadIdx.x; w < nwords; w += kThreadsTc) bitmap[w] = 0u;
   __syncthreads();
-  if (warp < 4) {
-    for (int tt = warp; tt < kTok; tt += 4) {
+  {
+    // every warp takes tokens warp and warp + 12 and loads both top-k rows before working on them
+    constexpr int kWarps = kThreadsTc / 32;
+    const int c0 = ctl->c0, ctx0 = ctl->ctx0;
+    const int tt0 = warp, tt1 = warp + kWarps;
+    const int b0 = (tt0 < n_tok && lane < a.k) ? __ldg(a.topk + static_cast<int64_t>(t0 + tt0) * a.topk_row_stride + lane)
+                                               : -1;
+    const int b1 = (tt1 < n_tok && lane < a.k) ? __ldg(a.topk + static_cast<int64_t>(t0 + tt1) * a.topk_row_stride + lane)
+                                               : -1;
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      const int tt = u == 0 ? tt0 : tt1;
+      if (tt >= kTok) continue;
       if (tt >= n_tok) {
         if (lane == 0) {
           ctl->cnt[tt] = 0;
@@ -292,11 +315,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         continue;
       }
       const int t = t0 + tt;
-      const int c0 = __ldg(a.cu_seqlens_q + req), c1 = __ldg(a.cu_seqlens_q + req + 1);
-      const int pos = __ldg(a.seq_lens + req) - (c1 - c0) + (t - c0);
+      const int pos = ctx0 + (t - c0);
       const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
       const int own = causal_len > 0 ? pos / kSparseBlock : -1;
-      const int b = lane < a.k ? __ldg(a.topk + static_cast<int64_t>(t) * a.topk_row_stride + lane) : -1;
+      const int b = u == 0 ? b0 : b1;
       bool valid = lane < a.k && causal_len > 0 && b >= 0 && b <= own;
       const bool oob = valid && b >= a.max_blocks;
       if (__any_sync(0xffffffffu, oob)) {
@@ -331,25 +353,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   // union = set bits in increasing order (one warp; a handful of words per tile)
   if (warp == 0) {
+    // 32 words per step; each non-empty word is expanded by the whole warp, lane = bit
     int at = 0;
     for (int w0 = 0; w0 < nwords; w0 += 32) {
-      const uint32_t word = w0 + lane < nwords ? bitmap[w0 + lane] : 0u;
-      const int c = __popc(word);
-      int incl = c;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
+      const uint32_t mine = w0 + lane < nwords ? bitmap[w0 + lane] : 0u;
+      uint32_t nz = __ballot_sync(0xffffffffu, mine != 0u);
+      while (nz) {
+        const int src = __ffs(nz) - 1;
+        nz &= nz - 1;
+        const uint32_t word = __shfl_sync(0xffffffffu, mine, src);
+        const int o = at + __popc(word & ((1u << lane) - 1u));
+        if (((word >> lane) & 1u) && o < kMaxUnion)
+          ctl->union_blk[o] = static_cast<uint16_t>(((w0 + src) << 5) + lane);
+        at += __popc(word);
       }
-      int o = at + incl - c;
-      uint32_t bits = word;
-      while (bits) {
-        const int bit = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (o < kMaxUnion) ctl->union_blk[o] = static_cast<uint16_t>(((w0 + lane) << 5) + bit);
-        ++o;
-      }
-      at += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) ctl->n_union = at < kMaxUnion ? at : kMaxUnion;
   }
