@@ -74,8 +74,10 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_
 // whose box lands as [row half][q][8 rows][128 B], q = the four 64-element quarters of a bf16 row
 // (K lo, K hi, V lo, V hi) or the two halves of an fp8 row (K, V): 128B-swizzle atoms of 8 rows.
 // Every address stays inside its own (page, head) chunk. PBS_CACHE_MAP=4d disables it (tests).
+// With quarters_per_box = 2 (bf16 only) a box holds either the K or the V half of every row
+// (quarter coordinate 0 or 2), landing as [row half][2][8 rows][128 B].
 int encode_cache_map_packed(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
-                            int64_t page_stride_bytes) {
+                            int64_t page_stride_bytes, int quarters_per_box = 0) {
   std::memset(map, 0, sizeof(*map));
   if (kv_dtype != PBS_KV_BF16 && kv_dtype != PBS_KV_FP8_E4M3) return PBS_ERR_UNSUPPORTED;
   if (page_stride_bytes != page_content_bytes(kv_dtype, num_kv_heads)) return PBS_ERR_UNSUPPORTED;
@@ -89,7 +91,9 @@ int encode_cache_map_packed(CUtensorMap* map, const void* cache, int kv_dtype, i
   const cuuint64_t nq = bf ? 4 : 2;
   const cuuint64_t dims[5] = {bf ? 64u : 128u, 8, nq, 2, static_cast<cuuint64_t>(num_pages) * num_kv_heads};
   const cuuint64_t strides[4] = {row, 128, 8 * row, 16 * row};
-  const cuuint32_t box[5] = {bf ? 64u : 128u, 8, static_cast<cuuint32_t>(nq), 2, 1};
+  if (quarters_per_box != 0 && (!bf || quarters_per_box != 2)) return PBS_ERR_UNSUPPORTED;
+  const cuuint32_t qbox = quarters_per_box != 0 ? static_cast<cuuint32_t>(quarters_per_box) : static_cast<cuuint32_t>(nq);
+  const cuuint32_t box[5] = {bf ? 64u : 128u, 8, qbox, 2, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = enc(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
                          const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -556,7 +560,11 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
-    e = pbs::launch_prefill_tc(a, map, qmap, reinterpret_cast<cudaStream_t>(stream));
+    // the tile kernel streams K and V separately: one box per (page, head) half row
+    CUtensorMap half_map;
+    st = encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2);
+    if (st != PBS_OK) return st;
+    e = pbs::launch_prefill_tc(a, half_map, qmap, reinterpret_cast<cudaStream_t>(stream));
   } else {
     e = pbs::launch_attend(a, pbs::kModePrefill, map, reinterpret_cast<cudaStream_t>(stream));
   }

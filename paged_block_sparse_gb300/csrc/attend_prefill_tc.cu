@@ -13,20 +13,22 @@
 //   heads, or 8 tokens x 16 heads, = 128 rows, one MMA M-tile. The tile's selected blocks are
 //   merged into a sorted union; every union block is streamed once and each row is masked by its
 //   own token's selection.
-// * Warp 0: TMA producer (Q tile once via a 3-D tensor map; K and V of each union block with one
-//   8 KiB copy per page through a 5-D tensor map over the packed cache, 128B swizzle, 3-stage
-//   ring). A stage is [page][row half][quarter: K lo, K hi, V lo, V hi][8 rows][128 B], so every
-//   8-key group of K and of V sits 4 KiB after the previous one. Warp 1: one thread issues
-//   the tcgen05 MMAs. Warps 4-7: softmax and epilogue, thread i owning TMEM lane / row i.
-// * TMEM (512 columns): S double buffer (2 x 128, fp32), the O accumulator (128, fp32) and two
-//   64-column buffers for the low half of P. The high half of P (bf16, two keys per column)
-//   overwrites the first 64 columns of its own S buffer.
+// * Warps 0 and 3: TMA producers. Warp 0 loads the Q tile once (3-D tensor map) and streams the
+//   K of each union block, warp 3 its V, each through its own 3-stage ring, one 4 KiB copy per
+//   page (the K or the V half of the page's 16 rows of this kv head) through a 5-D tensor map
+//   over the packed cache, 128B swizzle. A stage is [page][row half][64-dim quarter][8 rows]
+//   [128 B], so 8-key groups sit 2 KiB apart. Warp 1: one thread issues the tcgen05 MMAs, S two
+//   blocks ahead of PV. Warps 4-11: softmax and epilogue, two warps per TMEM lane quadrant.
+// * TMEM (512 columns): S triple buffer (3 x 128, fp32) and the O accumulator (128, fp32). Each
+//   softmax part rewrites its own 64 S columns with P: hi (bf16, two keys per column) in the
+//   first 32, lo in the last 32, once all 64 S values are in its registers.
 // * S = Q K^T: A = Q (K-major smem), B = K tile (K-major smem). O += P V: A = P read from TMEM,
 //   B = V tile (MN-major smem). P is split into bf16 hi + lo halves, two MMAs, so the result
 //   stays within 2e-3 relative RMS of the fp64 attend.
-// * The MMAs of one thread execute in issue order, so S(i) may reuse the buffer whose P(i-2)
-//   was read by PV(i-2), issued before it; the softmax of block i waits only for S(i), and for
-//   PV(i-1) when it has to rescale O.
+// * The MMAs of one thread execute in issue order, so S(i) may reuse the buffer whose P(i-3)
+//   was read by PV(i-3), issued before it; the softmax of block i waits only for S(i), and for
+//   PV(i-1) when it has to rescale O. K stages are released when S has read them, V stages when
+//   PV has, so K is fetched up to three blocks ahead of S.
 // * Online softmax in base 2 with lazy rescaling: the O row is rescaled only when the running
 //   maximum grows by more than 2^8, so most blocks never touch O from the CUDA cores.
 // * Duplicate ids in a token's list count once (set semantics of the attend); the decode path and
@@ -48,23 +50,27 @@ constexpr int kSoftWarps = 4 * kSplit;
 constexpr int kThreadsTc = 32 * (4 + kSoftWarps);
 constexpr int kQBytes = kRows * kHeadDim * 2;          // 32 KiB
 constexpr int kHalf = 128 * 128;                       // one 64-dim half of a 128 x 128 bf16 tile
-constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB
-constexpr int kKVBytes = 2 * kTileBytes;               // K then V
-constexpr int kStagesTc = kSplit >= 4 ? 2 : 3;
-constexpr int kBigBytes = kQBytes + kStagesTc * kKVBytes;  // 224 KiB
+constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB: a block's K, or its V
+constexpr int kStagesTc = 3;                           // stages of the K ring and of the V ring
+constexpr int kSBuf = 3;                               // S buffers in TMEM (S runs 2 blocks ahead of PV)
+constexpr int kBigBytes = kQBytes + 2 * kStagesTc * kTileBytes;  // 224 KiB
 constexpr int kMaxUnion = 256;
 constexpr int kTcMaxTopk = 16;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
 struct TcCtl {
   uint64_t q_full;
-  uint64_t kv_full[kStagesTc];
-  uint64_t kv_empty[kStagesTc];
-  uint64_t s_full[2];
-  // P of even / odd blocks: the softmax may finish block j+1 before the MMA thread has waited for
-  // block j (it only waits for PV when it rescales), but never block j+2 (S(j+2) follows PV(j)).
-  uint64_t p_full[2];
-  uint64_t pv_done[2];  // PV of even / odd blocks
+  // K and V stream through separate rings: a K stage is free once S has read it, a V stage once
+  // PV has, so K can be loaded three blocks ahead of S while S runs two blocks ahead of PV
+  uint64_t k_full[kStagesTc];
+  uint64_t k_empty[kStagesTc];
+  uint64_t v_full[kStagesTc];
+  uint64_t v_empty[kStagesTc];
+  uint64_t s_full[kSBuf];
+  // per S buffer (block i uses buffer i % 3): P(i) written, PV(i) done. A barrier cannot be lapped:
+  // block i + 3 needs S(i + 3), which the MMA thread issues only after PV(i).
+  uint64_t p_full[kSBuf];
+  uint64_t pv_done[kSBuf];
   uint32_t tmem_base;
   int32_t n_union;
   int32_t req, t0, n_tok;
@@ -213,7 +219,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     return;
   }
   uint8_t* q_s = big;
-  uint8_t* kv_s = big + kQBytes;  // stage st at kv_s + st * kKVBytes: K halves, then V halves
+  // stage st of each ring at + st * kTileBytes; a stage is [page][row half][64-dim quarter][8 rows]
+  // [128 B], so 8-key groups are 2 KiB apart and the two quarters of a row 1 KiB apart
+  uint8_t* k_s = big + kQBytes;
+  uint8_t* v_s = k_s + kStagesTc * kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
@@ -270,10 +279,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       ctl->abort = 0;
       mbar_init(&ctl->q_full, 1);
       for (int i = 0; i < kStagesTc; ++i) {
-        mbar_init(&ctl->kv_full[i], 1);
-        mbar_init(&ctl->kv_empty[i], 1);
+        mbar_init(&ctl->k_full[i], 1);
+        mbar_init(&ctl->k_empty[i], 1);
+        mbar_init(&ctl->v_full[i], 1);
+        mbar_init(&ctl->v_empty[i], 1);
       }
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kSBuf; ++i) {
         mbar_init(&ctl->s_full[i], 1);
         mbar_init(&ctl->p_full[i], kSoftWarps);
         mbar_init(&ctl->pv_done[i], 1);
@@ -286,8 +297,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (n_tok <= 0) return;  // surplus tile, or the grid already gave up; uniform across the CTA
 
   // ---- each token's distinct valid blocks, sorted, plus the union bitmap ---------------------
-  // The union is built as a bitmap over the block ids in the last K/V stage (free until the loop).
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(kv_s + (kStagesTc - 1) * kKVBytes);
+  // The union is built as a bitmap over the block ids in the last V stage (free until the loop).
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(v_s + (kStagesTc - 1) * kTileBytes);
   const int pos_last = ctl->pos_last;  // position of the request's last token
   // valid block ids are <= pos_last / 128 and < max_blocks (<= 65536): at most 2048 words
   const int nwords = min(max(pos_last, 0) / kSparseBlock / 32 + 1, (a.max_blocks + 31) / 32);
@@ -378,18 +389,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int nU = ctl->n_union;
   if (threadIdx.x == 0) TRACE(kEvSetup);
   const uint32_t tmem = ctl->tmem_base;
-  const uint32_t tm_s0 = tmem, tm_o = tmem + 256, tm_plo = tmem + 384;
+  const uint32_t tm_s0 = tmem, tm_o = tmem + kSBuf * 128;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    // One 8 KiB copy per page (K and V of this kv head); lanes 0..7 issue the 8 pages of a block.
-    if (lane == 0) {
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 0 loads the Q tile and streams the K of each union block, warp 3 its V: one 4 KiB
+    // copy per page (the K or V half of its 16 rows of this kv head: quarter coordinate 0 or 2 of
+    // the half-row map); lanes 0..7 issue the 8 pages of a block.
+    const bool is_k = warp == 0;
+    if (is_k && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
       mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
       tma_load_3d(q_s, &q_map, &ctl->q_full, 0, g * kG, t0);
       tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, g * kG, t0);
     }
+    uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
+    uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
+    uint8_t* ring = is_k ? k_s : v_s;
+    const int quarter = is_k ? 0 : 2;
     const int32_t* bt_row = a.page_table + static_cast<int64_t>(req) * a.pt_row_stride;
     int phys_lane = 0;
     int issued = 0;
@@ -398,29 +416,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if ((i & 31) == 0) phys_lane = i + lane < nU ? __ldg(bt_row + ctl->union_blk[i + lane]) : 0;
       const int phys = __shfl_sync(0xffffffffu, phys_lane, i & 31);
       bool go = true;
-      if (lane == 0 && i >= kStagesTc)
-        go = wait_or_abort(&ctl->kv_empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word);
+      if (lane == 0 && i >= kStagesTc) go = wait_or_abort(&empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word);
       if (lane == 0) go = go && !aborted(ctl);
       go = __shfl_sync(0xffffffffu, go, 0);
       if (!go) break;
       const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
-      if (lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages)) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-      uint8_t* dst = kv_s + st * kKVBytes;
-      TRACE(kEvProdIssue0 + i);
-      if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[st], kKVBytes);
+      if (is_k && lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages))
+        set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+      uint8_t* dst = ring + st * kTileBytes;
+      if (is_k) TRACE(kEvProdIssue0 + i);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
       __syncwarp();
       // out-of-range pages read as zeros (TMA bounds)
       if (lane < kPagesPerBlock)
-        tma_load_5d(dst + lane * 8192, &kv_map, &ctl->kv_full[st], 0, 0, 0, 0,
+        tma_load_5d(dst + lane * 4096, &kv_map, &full[st], 0, 0, quarter, 0,
                     static_cast<int>((base + lane) * a.num_kv_heads + g));
-      TRACE(kEvProdIssue1 + i);
+      if (is_k) TRACE(kEvProdIssue1 + i);
       issued = i + 1;
     }
     if (lane == 0) {
       for (int i = max(0, issued - kStagesTc); i < issued; ++i)
-        if (!mbar_wait_bounded(&ctl->kv_full[i % kStagesTc], (i / kStagesTc) & 1, kTcWaitNs))
+        if (!mbar_wait_bounded(&full[i % kStagesTc], (i / kStagesTc) & 1, kTcWaitNs))
           set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-      if (!mbar_wait_bounded(&ctl->q_full, 0, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+      if (is_k && !mbar_wait_bounded(&ctl->q_full, 0, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -430,55 +448,59 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t q_addr = smem_u32(q_s);
       bool ok = nU == 0 || wait_or_abort(&ctl->q_full, 0, ctl, a.err_word);
       int issued_pv = 0;
-      for (int i = 0; ok && i <= nU; ++i) {
+      // issue order S(0), S(1), S(2), PV(0), S(3), PV(1), ...: S runs two blocks ahead of PV, so
+      // the softmax of block i + 1 finds S(i + 1) done while PV(i - 1) is still queued. S(i) reuses
+      // buffer i % 3, whose last reader PV(i - 3) was issued before it.
+      for (int i = 0; ok && i < nU + 2; ++i) {
         if (i < nU) {
-          // S(i) -> TMEM buffer i&1 (its previous P was read by PV(i-2), issued earlier)
-          const int st = i % kStagesTc;
-          if (!wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) break;
+          const int st = i % kStagesTc, sb = i % kSBuf;
+          if (!wait_or_abort(&ctl->k_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
-          const uint32_t k_addr = smem_u32(kv_s + st * kKVBytes);
+          const uint32_t k_addr = smem_u32(k_s + st * kTileBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             // dims 16ks..: Q half ks/4 (16 KiB apart, 8-row groups 1 KiB apart); K quarter ks/4
-            // (1 KiB apart, 8-key groups 4 KiB apart)
-            tc::mma_ss(tm_s0 + (i & 1) * 128,
+            // (1 KiB apart, 8-key groups 2 KiB apart)
+            tc::mma_ss(tm_s0 + sb * 128,
                        tc::smem_desc_sw128(q_addr + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024),
-                       tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 4096), kIdescS,
+                       tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048), kIdescS,
                        ks > 0);
           }
-          tc::commit(&ctl->s_full[i & 1]);
+          tc::commit(&ctl->s_full[sb]);
+          tc::commit(&ctl->k_empty[st]);  // the K stage is free once S(i) has read it
           TRACE(kEvS + i);
         }
-        if (i >= 1) {
-          // O += P(j) V(j): P hi in the first 64 columns of S buffer j&1, P lo in its own buffer
-          const int j = i - 1, st = j % kStagesTc;
-          if (!wait_or_abort(&ctl->p_full[j & 1], (j >> 1) & 1, ctl, a.err_word)) break;
+        const int j = i - 2;
+        if (j >= 0) {
+          // O += P(j) V(j): in S buffer j % 3 each softmax part's 64 columns hold P hi (bf16, two
+          // keys per column) in their first 32 and P lo in their last 32
+          const int st = j % kStagesTc, sb = j % kSBuf;
+          if (!wait_or_abort(&ctl->p_full[sb], (j / kSBuf) & 1, ctl, a.err_word)) break;
+          if (!wait_or_abort(&ctl->v_full[st], (j / kStagesTc) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
-          const uint32_t v_addr = smem_u32(kv_s + st * kKVBytes) + 2 * 1024;  // quarters 2, 3 = V
+          const uint32_t v_addr = smem_u32(v_s + st * kTileBytes);
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              // keys 16ks..16ks+15: P hi lives in the first half of the S columns of the softmax
-              // part that owns those keys; P lo is packed contiguously
+              // keys 16ks..16ks+15 belong to softmax part `owner`
               const int owner = (16 * ks) / kW;
-              const uint32_t pa = part == 0 ? tm_s0 + (j & 1) * 128 + owner * kW + (16 * ks - owner * kW) / 2
-                                            : tm_plo + (j & 1) * 64 + 8 * ks;
-              // keys 16ks..16ks+15 = two 8-key groups (4 KiB apart) from key group 2ks; dims in
+              const uint32_t pa = tm_s0 + sb * 128 + owner * kW + part * (kW / 2) + (16 * ks - owner * kW) / 2;
+              // keys 16ks..16ks+15 = two 8-key groups (2 KiB apart) from key group 2ks; dims in
               // two 64-wide MN atoms 1 KiB apart
-              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 8192, 1024, 4096), kIdescPV,
+              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), kIdescPV,
                          !(j == 0 && part == 0 && ks == 0));
             }
           }
-          tc::commit(&ctl->pv_done[j & 1]);
+          tc::commit(&ctl->pv_done[sb]);
           TRACE(kEvPV + j);
-          tc::commit(&ctl->kv_empty[st]);
+          tc::commit(&ctl->v_empty[st]);
           issued_pv = j + 1;
         }
       }
       // every MMA issued must complete before TMEM is released
       if (issued_pv > 0)
-        mbar_wait_bounded(&ctl->pv_done[(issued_pv - 1) & 1], ((issued_pv - 1) >> 1) & 1, kTcWaitNs);
+        mbar_wait_bounded(&ctl->pv_done[(issued_pv - 1) % kSBuf], ((issued_pv - 1) / kSBuf) & 1, kTcWaitNs);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
@@ -502,27 +524,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
     // the blocks, so the two warps of a quadrant always meet at the same named barriers.
     for (int i = 0; i < nU; ++i) {
-      const int sb = i & 1, st = i % kStagesTc;
+      const int sb = i % kSBuf, st = i % kStagesTc;
       const int b = ctl->union_blk[i];
       while (ptr < cnt_t && ctl->tok_blk[tt][ptr] < b) ++ptr;
       const bool active = ptr < cnt_t && ctl->tok_blk[tt][ptr] == b;
       const int lim = b == own_t ? lim_t : kSparseBlock;
-      if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (i >> 1) & 1, ctl, a.err_word)) ok = false;
+      if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (i / kSBuf) & 1, ctl, a.err_word)) ok = false;
       tc::fence_after_sync();
       if (sw == 0 && lane == 0) TRACE(kEvSoftIn + i);
       // rows past the request's last token in its last block may hold anything: zero that V
       if (b == last_blk && last_rows < kSparseBlock) {
-        if (ok && !warp_wait_or_abort(&ctl->kv_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) ok = false;
-        const uint32_t v_base = smem_u32(kv_s + st * kKVBytes);
+        if (ok && !warp_wait_or_abort(&ctl->v_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) ok = false;
+        const uint32_t v_base = smem_u32(v_s + st * kTileBytes);
         for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
-          const int key = last_rows + (e >> 4), vq = 2 + ((e >> 3) & 1), chunk = e & 7;
-          // key = 16 page + 8 half + row
-          sts128(v_base + (key >> 3) * 4096 + vq * 1024 + (key & 7) * 128 + chunk * 16, 0, 0, 0, 0);
+          const int key = last_rows + (e >> 4), vq = (e >> 3) & 1, chunk = e & 7;
+          // key = 16 page + 8 half + row; 8-key groups 2 KiB apart
+          sts128(v_base + (key >> 3) * 2048 + vq * 1024 + (key & 7) * 128 + chunk * 16, 0, 0, 0, 0);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       const uint32_t ts = tm_s0 + sb * 128 + lane_off;
-      const uint32_t tplo = tm_plo + sb * 64 + lane_off;
       // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
       // take part in this block are masked arithmetically (their P row becomes zero). Activity
       // depends only on the row, so the kSplit warps of a quadrant always agree.
@@ -541,10 +562,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc::wait_ld();
           prefix = __any_sync(0xffffffffu, nval != 0 && nval != kW);
           // P with the running reference (the common case), and this part's maximum
-          psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, pm)
-                        : write_p<false>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, pm);
+          psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm)
+                        : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm);
         } else {
-          zero_p(ts + col0, tplo + col0 / 2);
+          zero_p(ts + col0, ts + col0 + kW / 2);
         }
         ctl->xchg[part][row] = pm;
         quad_bar(quad);
@@ -564,7 +585,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
           if (__any_sync(0xffffffffu, resc)) {
             // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
-            if (ok && i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, ctl, a.err_word))
+            if (ok && i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) % kSBuf], ((i - 1) / kSBuf) & 1, ctl, a.err_word))
               ok = false;
             tc::fence_after_sync();
 #pragma unroll
@@ -581,14 +602,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           m_ref = m_new;
           if (any_valid) {
             float unused;
-            psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, unused)
-                          : write_p<false>(v, nval, sl2, m_ref, ts + col0, tplo + col0 / 2, unused);
+            psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused)
+                          : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused);
           }
         }
         l += psum;
         started = started || active;
       } else {
-        zero_p(ts + col0, tplo + col0 / 2);
+        zero_p(ts + col0, ts + col0 + kW / 2);
       }
       tc::wait_st();
       tc::fence_before_sync();
@@ -598,7 +619,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     if (sw == 0 && lane == 0) TRACE(kEvEpi);
     // ---- epilogue: O / l -> bf16 (row sum combined over the parts of the quadrant)
-    if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(nU - 1) & 1], ((nU - 1) >> 1) & 1, ctl, a.err_word))
+    if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(nU - 1) % kSBuf], ((nU - 1) / kSBuf) & 1, ctl, a.err_word))
       ok = false;
     tc::fence_after_sync();
     ctl->xchg[part][row] = l;
