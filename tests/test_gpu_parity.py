@@ -463,6 +463,23 @@ def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel, monkeypatch):
     _check_lse(lse[nd:], _oracle_lse(b, "pre"), "mixed lse prefill")
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+def test_attend_topk_64_and_padded_topk_rows(pbs, kv_dtype, monkeypatch):
+    """The largest top-k the boundary accepts (64), four query rows per decode request, and top-k
+    rows read through a padded row stride (a [rows, 80] buffer viewed as [rows, 64])."""
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=2, topk=64,
+                        dec_seq_lens=[9000, 300, 20000], decode_query_len=4, pre_q_lens=[100, 30],
+                        pre_ctx_lens=[12000, 0], future_prob=0.3, seed=55)
+    for part in ("dec", "pre"):
+        src = b.dec if part == "dec" else b.pre
+        padded = torch.full((src.topk.shape[1], 80), -1, dtype=torch.int32, device=DEV)
+        padded[:, :64] = src.topk[0]
+        src.topk = padded[:, :64]
+        got = gpu_attend(pbs, b, part)
+        want = oracle_decode(b) if part == "dec" else oracle_prefill(b)
+        assert_close(dict(enumerate(got)), want, kv_dtype, f"top-k 64 {part}")
+
+
 @pytest.mark.parametrize("part", ["dec", "tc", "token"])
 def test_attend_side_packed_blocks(pbs, part, monkeypatch):
     """block_page_stride 16 ([sparse_pa] minimax_m3_sparse_block_page_stride with packed sides):
