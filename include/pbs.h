@@ -223,9 +223,20 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
 /*
  * Sparse prefill attention, varlen ([flashinfer] msa_sparse_attention call with cu_seqlens_q;
  * [nvfp4] minimax_m3_nvfp4_sparse_prefill call). Token positions as in
- * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention.
- * Shapes the tcgen05 tile kernel takes (bf16 packed cache, GQA 8 or 16, top-k <= 16, 16-byte aligned q
- * and out rows) ignore the workspace.
+ * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention,
+ * except the workspace:
+ *   workspace   optional (NULL, 0), caller-owned device memory, contents need no initial value.
+ *               With a 256-byte aligned workspace of at least
+ *               pbs_prefill_workspace_bytes(256, num_reqs, num_heads, num_kv_heads, topk_k,
+ *               max_blocks) bytes, calls the gathered-row kernel takes (bf16 cache packed as
+ *               [pages][Hkv][16 rows][K | V], GQA 8 or 16, max_blocks <= 8192, 16-byte aligned q
+ *               and out rows) run on it: per-block partial outputs and the per-window token buckets
+ *               live in the workspace, and the call is processed in as many token segments as its
+ *               size requires (pbs_prefill_workspace_bytes(total_q, ...) bytes: one segment).
+ *               Otherwise the tcgen05 tile kernel or the token-centric kernel runs; the latter
+ *               merges split rows through the workspace when it holds pbs_attend_workspace_bytes
+ *               (zeroed before first use, as described there) and ignores a smaller one.
+ *               Calls that share one workspace must not run concurrently.
  */
 PBS_API int pbs_sparse_prefill_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -239,6 +250,17 @@ PBS_API int pbs_sparse_prefill_attention(
     float* lse, int64_t lse_row_stride,
     void* workspace, size_t workspace_bytes,
     int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Bytes of the workspace with which pbs_sparse_prefill_attention runs a call of `total_q`
+ * tokens (at most 2^20 per segment) over `num_reqs` requests on its gathered-row kernel in one
+ * segment; 0 for invalid arguments. No counterpart on the pages. With total_q = 256 it is the
+ * smallest workspace that kernel accepts. For Hq query heads and top-k k the size is about
+ * total_q * Hq * k * 264 bytes (fp16 partial outputs and their log-sum-exp pairs) plus the
+ * buckets.
+ */
+PBS_API size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads,
+                                           int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks);
 
 /*
  * Mixed batch in one call ([flashinfer] forward with both parts: decode rows q[:nd], prefill

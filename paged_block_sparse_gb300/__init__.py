@@ -21,6 +21,7 @@ __all__ = [
     "abi_version", "status_string", "build_sparse_block_table_decode", "build_sparse_block_table_prefill",
     "sparse_decode_attention", "sparse_prefill_attention", "insert_index_cache", "DEVERR",
     "attend_workspace_bytes", "attend_workspace", "sparse_decode_attention_noalloc", "sparse_mixed_attention",
+    "prefill_workspace_bytes", "prefill_workspace",
 ]
 
 SPARSE_BLOCK_SIZE = 128
@@ -60,6 +61,8 @@ def lib() -> ctypes.CDLL:
     L.pbs_abi_version.argtypes = []
     L.pbs_attend_workspace_bytes.restype = ctypes.c_size_t
     L.pbs_attend_workspace_bytes.argtypes = [i64, i32, i32]
+    L.pbs_prefill_workspace_bytes.restype = ctypes.c_size_t
+    L.pbs_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     table_common = [vp, i64, i32, i32, vp, i64, i32]
     L.pbs_build_sparse_block_table_decode.restype = ctypes.c_int
     L.pbs_build_sparse_block_table_decode.argtypes = table_common + [vp, i32, i32, i32, vp, i64, vp, vp, vp]
@@ -258,6 +261,39 @@ def _workspace_args(workspace, rows, num_heads, num_kv_heads, device, stream):
     return _ptr(workspace), workspace.numel()
 
 
+def prefill_workspace_bytes(total_q: int, num_reqs: int, num_heads: int, num_kv_heads: int, topk: int,
+                            max_blocks: int) -> int:
+    """Bytes with which the prefill attend runs ``total_q`` tokens on its gathered-row kernel in
+    one segment (``total_q = 256``: the smallest workspace that kernel takes)."""
+    return int(lib().pbs_prefill_workspace_bytes(int(total_q), int(num_reqs), int(num_heads), int(num_kv_heads),
+                                                 int(topk), int(max_blocks)))
+
+
+# the default prefill workspace is capped; larger calls run in several token segments
+PREFILL_WORKSPACE_CAP = 2 << 30
+_prefill_workspaces: dict = {}
+
+
+def prefill_workspace(total_q: int, num_reqs: int, num_heads: int, num_kv_heads: int, topk: int, max_blocks: int,
+                      device, stream=None) -> torch.Tensor:
+    """A workspace for the prefill attend's gathered-row kernel, cached per (device, stream) and
+    grown on demand: one segment for the whole call when that fits ``PREFILL_WORKSPACE_CAP``,
+    else the cap (the call then runs in segments). Needs no initial value."""
+    device = torch.device(device)
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device.index, s.cuda_stream)
+    full = prefill_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, topk, max_blocks)
+    least = prefill_workspace_bytes(min(total_q, 256), num_reqs, num_heads, num_kv_heads, topk, max_blocks)
+    need = max(min(full, PREFILL_WORKSPACE_CAP), least)
+    ws = _prefill_workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        _prefill_workspaces.pop(key, None)
+        with torch.cuda.stream(s):
+            ws = torch.empty(need, dtype=torch.uint8, device=device)
+        _prefill_workspaces[key] = ws
+    return ws
+
+
 def _lse_arg(lse, return_lse, q):
     """(tensor or None) for the optional log-sum-exp output [rows, Hq] fp32."""
     if lse is None and not return_lse:
@@ -323,12 +359,20 @@ def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: in
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                              block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                             workspace=None, lse=None, return_lse: bool = False):
+                             workspace="auto", lse=None, return_lse: bool = False):
     """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
-    ``workspace``, ``lse`` and ``return_lse`` as in :func:`sparse_decode_attention`."""
+
+    ``workspace``: "auto" (the default: a cached per-stream buffer from :func:`prefill_workspace`,
+    with which bf16 caches run on the gathered-row kernel), None (no workspace: the tcgen05 tile
+    kernel or the token-centric kernel) or a uint8 CUDA tensor (see ``pbs_sparse_prefill_attention``
+    in include/pbs.h for how each kernel uses it). ``lse`` and ``return_lse`` as in
+    :func:`sparse_decode_attention`."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1], pt.shape[1],
+                                      q.device, stream)
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
     st = lib().pbs_sparse_prefill_attention(

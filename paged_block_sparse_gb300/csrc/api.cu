@@ -1,5 +1,6 @@
 // The C ABI of libpbs (include/pbs.h): argument validation, scale folding, tensor-map encoding,
 // launch-shape choice and dispatch to the kernels. Nothing here allocates device memory.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -117,14 +118,15 @@ int encode_attend_map(CUtensorMap* map, const void* cache, int kv_dtype, int num
 // dims (G = 8 or 16 query heads per kv head), laid out in shared memory as the 128-row K-major
 // operand of the prefill MMA (row = token * G + head).
 int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int total_q, int64_t q_row_stride,
-                 int64_t q_head_stride) {
+                 int64_t q_head_stride, int box_tokens = 0) {
   std::memset(map, 0, sizeof(*map));
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return PBS_ERR_CUDA;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(num_heads),
                               static_cast<cuuint64_t>(total_q)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(q_head_stride) * 2, static_cast<cuuint64_t>(q_row_stride) * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(box_tokens > 0 ? box_tokens : 128 / group)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -132,9 +134,12 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
-// Which prefill kernel runs: the tcgen05 tile kernel where it applies, the token-centric
-// kernel otherwise. PBS_PREFILL_KERNEL=token forces the token-centric one, =tc requires the
-// tile kernel (tests, tuning).
+// Which prefill kernel runs. With a workspace that holds at least one 256-token segment, shapes
+// the gathered-row kernel takes (bf16 packed cache, GQA 8 or 16, page table <= 8192 blocks) run
+// on it: its MMA rows are the tokens that selected a block, so its work does not grow with the
+// context the selections are spread over. Otherwise the tcgen05 tile kernel where it applies,
+// the token-centric kernel elsewhere. PBS_PREFILL_KERNEL=gather|tc|token requires that kernel
+// (tests, tuning).
 //
 // The tile kernel streams the union of its 16 tokens' selections to all of them, so its waste
 // grows with the context a token chooses from: a token at block s selects k of s + 1 blocks,
@@ -144,23 +149,33 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
 // tokens): contexts 0 / 2k-4k / 16k-32k give 462 / 312 / 114 TFLOP/s on the tile kernel and
 // 133 / 139 / 139 on the token-centric one.
 constexpr int kTileMaxBlocksPerTopk = 8;
+enum PrefillKernel { kPrefillToken = 0, kPrefillTile = 1, kPrefillGather = 2 };
 
 int prefill_kernel_override() {
   if (const char* env = std::getenv("PBS_PREFILL_KERNEL")) {
     if (std::strcmp(env, "token") == 0) return 1;
     if (std::strcmp(env, "tc") == 0) return 2;
+    if (std::strcmp(env, "gather") == 0) return 3;
   }
   return 0;
 }
 
-// Sets *use_tile for a prefill call whose AttendArgs (map already encoded) are `a`;
-// PBS_ERR_UNSUPPORTED when PBS_PREFILL_KERNEL=tc asks for a tile kernel that cannot run.
-int choose_prefill_kernel(const AttendArgs& a, bool* use_tile) {
+// Sets *kernel for a prefill call whose AttendArgs (map already encoded) are `a`, given the
+// caller's workspace size; PBS_ERR_UNSUPPORTED when PBS_PREFILL_KERNEL asks for a kernel that
+// cannot run the call.
+int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, PrefillKernel* kernel) {
   const int force = prefill_kernel_override();
-  // the tile kernel reads the packed bf16 cache through the 5-D map
-  const bool fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
-  if (force == 2 && !fits) return PBS_ERR_UNSUPPORTED;
-  *use_tile = force == 2 || (force == 0 && fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k);
+  // the tcgen05 kernels read the packed bf16 cache through the 5-D map
+  const bool tile_fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
+  const bool gather_fits = a.packed_map != 0 && pbs::prefill_gather_supported(a) && a.num_rows < (1 << 25) &&
+                           pbs::gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k,
+                                                      a.max_blocks, workspace_bytes) > 0;
+  if ((force == 2 && !tile_fits) || (force == 3 && !gather_fits)) return PBS_ERR_UNSUPPORTED;
+  if (force == 1) *kernel = kPrefillToken;
+  else if (force == 2) *kernel = kPrefillTile;
+  else if (force == 3 || gather_fits) *kernel = kPrefillGather;
+  else if (tile_fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k) *kernel = kPrefillTile;
+  else *kernel = kPrefillToken;
   return PBS_OK;
 }
 
@@ -356,7 +371,7 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 5; }
+int pbs_abi_version(void) { return 6; }
 
 size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
   if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
@@ -545,30 +560,47 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   a.num_rows = total_q;
   st = attach_lse(&a, lse, lse_row_stride);
   if (st != PBS_OK) return st;
-  const int64_t units = pbs::attend_units(total_q, num_kv_heads, a.group);
-  st = attach_workspace(&a, units, workspace, workspace_bytes);
-  if (st != PBS_OK) return st;
-  a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
+  if (workspace == nullptr && workspace_bytes != 0) return PBS_ERR_ARG;
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
   if (st != PBS_OK) return st;
-  cudaError_t e;
-  bool tc_ok = false;
-  st = choose_prefill_kernel(a, &tc_ok);
+  // the gathered-row kernel lays its arrays out from a 256-byte aligned workspace base
+  PrefillKernel kernel = kPrefillToken;
+  st = choose_prefill_kernel(a, workspace != nullptr && aligned(workspace, 256) ? workspace_bytes : 0, &kernel);
   if (st != PBS_OK) return st;
-  if (tc_ok) {
-    CUtensorMap qmap;
-    st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
-    if (st != PBS_OK) return st;
-    // the tile kernel streams K and V separately: one box per (page, head) half row
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (kernel == kPrefillToken) {
+    // the workspace, when it holds the split partials, merges split rows
+    const int64_t units = pbs::attend_units(total_q, num_kv_heads, a.group);
+    if (workspace != nullptr && workspace_bytes >= pbs::attend_workspace_bytes(units)) {
+      st = attach_workspace(&a, units, workspace, workspace_bytes);
+      if (st != PBS_OK) return st;
+    }
+    a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
+    e = pbs::launch_attend(a, pbs::kModePrefill, map, cs);
+  } else {
+    // both tcgen05 kernels stream K and V separately: one box per (page, head) half row
     CUtensorMap half_map;
     st = encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2);
     if (st != PBS_OK) return st;
-    e = pbs::launch_prefill_tc(a, half_map, qmap, reinterpret_cast<cudaStream_t>(stream));
-  } else {
-    e = pbs::launch_attend(a, pbs::kModePrefill, map, reinterpret_cast<cudaStream_t>(stream));
+    CUtensorMap qmap;
+    st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride,
+                      kernel == kPrefillGather ? 1 : 0);
+    if (st != PBS_OK) return st;
+    e = kernel == kPrefillGather ? pbs::launch_prefill_gather(a, half_map, qmap, workspace, workspace_bytes, cs)
+                                 : pbs::launch_prefill_tc(a, half_map, qmap, cs);
   }
   return e == cudaSuccess ? PBS_OK : PBS_ERR_CUDA;
+}
+
+size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t topk_k, int32_t max_blocks) {
+  if (total_q <= 0 || num_reqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      topk_k <= 0 || topk_k > kMaxTopk || max_blocks <= 0)
+    return 0;
+  const int64_t seg = std::min<int64_t>(total_q, pbs::kGatherMaxSegment);
+  return pbs::gather_workspace_bytes(seg, num_reqs, num_heads, num_kv_heads, topk_k, max_blocks);
 }
 
 int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,
@@ -626,10 +658,10 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
   CUtensorMap map;
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &p.packed_map);
   if (st != PBS_OK) return st;
-  bool tile = false;
-  st = choose_prefill_kernel(p, &tile);
+  PrefillKernel kernel = kPrefillToken;
+  st = choose_prefill_kernel(p, 0, &kernel);
   if (st != PBS_OK) return st;
-  if (tile) {
+  if (kernel != kPrefillToken) {
     // the prefill part runs on the tcgen05 tile kernel: two launches, decode first
     st = pbs_sparse_decode_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
                                      kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,

@@ -1,0 +1,951 @@
+// Prefill attend by key block ("gathered rows") on the 5th-generation tensor cores (tcgen05 +
+// TMEM), bf16 KV cache, GQA 8 or 16.
+//
+// What it computes (vLLM page vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer, forward:
+// the varlen msa_sparse_attention call; row rule of vllm.models.minimax_m3.amd.ops.sparse_pa,
+// _write_sparse_block_table_row_from_values): for every prefill token and query head h of kv
+// head g, out = v_scale * softmax(softmax_scale * k_scale * q_h K^T) V over the keys of the
+// 128-token blocks the token's top-k selects (block b valid iff 0 <= b <= pos/128; the own
+// block truncated at pos). Duplicate ids in a token's list count once.
+//
+// GB300 design
+// ------------
+// A tile of consecutive tokens shares few of its selected blocks when the selections are
+// spread over a long context, so a tile that streams the union of its tokens' blocks wastes
+// most of its MMA rows. Here the work is inverted: a work item is one (key block b, kv head g)
+// of a window of 256 consecutive tokens of one request, and its MMA rows are the window's
+// tokens that selected b, gathered 16 at a time (x 8 query heads = the 128-row M tile; 8 tokens
+// x 16 heads at GQA 16). Every row of every tile does useful work except in a bucket's last
+// chunk.
+//
+// * Index kernel (one CTA per window): each token's distinct valid blocks, sorted, give the
+//   token's partial slots; tokens are bucketed by block (shared-memory histogram, block scan,
+//   scatter). Tokens with no valid block get zero output here.
+// * Attend kernel (persistent, one CTA per SM): windows are taken in order and the items of a
+//   window from a per-window counter, so the partial results of a window are written and
+//   merged while they sit in L2. Per item, warp 0 loads K_b and V_b of head g (one 4 KiB tensor
+//   copy per page and half row, 128B swizzle) into one of two K/V buffers, then per chunk writes
+//   a descriptor (tokens, partial slots, own-block key limits) into a 4-deep ring and gathers
+//   the chunk's Q rows (one {64 dims, G heads, 1 token} tensor copy per token and half). Warp 1
+//   (one thread) issues S(c) = Q K^T into TMEM buffer c % 2, then PV(c-1), so the softmax of
+//   chunk c overlaps PV(c-1) and S(c+1). Warps 4-7 and 8-11 are two softmax warpgroups taking
+//   chunks alternately; a thread owns one row (TMEM lane).
+// * Softmax of one chunk (one key block): the row maximum over the block's valid keys (first
+//   pass over the S row in TMEM), then P = 2^(s * scale * log2 e - m) written back over S as bf16
+//   hi + lo (32 keys at a time into the same 32 columns), so the PV product (two MMAs, A = P from
+//   TMEM) keeps the output within 2e-3 relative RMS of the fp64 attend.
+// * Epilogue: the row's partial output O / l, scaled by a power of two so that its largest
+//   element lies in [2^14, 2^15), is stored as fp16 together with (log2-sum-exp, exponent).
+//   Each (token, kv head) counts its finished partials with an atomic ticket; the chunk that
+//   completes a token merges its partials (fp32, log-sum-exp weights), writes the bf16 output
+//   and the log-sum-exp, and drops the merged partial lines from L2 without writing them back.
+// * TMEM (512 columns): S / P double buffer (2 x 128) and O double buffer (2 x 128).
+#include <algorithm>
+
+#include <cuda_fp16.h>
+
+#include "pbs_device.cuh"
+#include "pbs_internal.h"
+#include "tc_device.cuh"
+
+namespace pbs {
+namespace {
+
+constexpr int kGRows = 128;                     // MMA M: tokens x query heads of a chunk
+constexpr int kGThreads = 384;                  // 12 warps
+constexpr int kDescRing = 4;                    // chunk descriptors in flight
+constexpr int kGQBytes = kGRows * kHeadDim * 2;  // 32 KiB Q tile
+constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of the Q tile
+constexpr int kGTile = 32768;                   // a block's K (or V) for one kv head
+constexpr int kGSmemBig = 2 * kGQBytes + 4 * kGTile;  // Q x 2, K x 2, V x 2 = 192 KiB
+constexpr unsigned long long kGWaitNs = 100000000ull;  // waits here last microseconds: 100 ms cap
+constexpr int kIdxThreads = 256;
+
+struct ChunkDesc {
+  int32_t end;    // 1: no more work for this CTA
+  int32_t b;      // key block
+  int32_t g;      // kv head
+  int32_t ybuf;   // K/V buffer of the item
+  int32_t last;   // last chunk of the item
+  int32_t n_tok;  // tokens in this chunk
+  int32_t item;   // the CTA's item number (phase of the K/V buffer barriers)
+  int32_t pad;
+  int32_t tr[16];    // segment-relative token index
+  int32_t slot[16];  // the token's partial slot for block b
+  int32_t lim[16];   // keys of block b the token sees (128, or pos - 128 b + 1 for its own block)
+  int32_t nsel[16];  // the token's number of partials
+};
+
+struct GCtl {
+  uint64_t desc_full[kDescRing];
+  uint64_t desc_empty[kDescRing];  // 1 (MMA thread) + 4 (softmax warps) arrivals
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[2], v_full[2], v_land[2], kv_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t mma_fin;
+  uint32_t tmem_base;
+  int32_t abort;
+  ChunkDesc desc[kDescRing];
+};
+
+constexpr size_t kGSmem = kGSmemBig + sizeof(GCtl) + 1024;
+static_assert(kGSmem <= 232448, "shared memory layout exceeds 227 KiB");
+
+__device__ __forceinline__ bool g_aborted(GCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
+
+__device__ __forceinline__ bool g_wait(uint64_t* bar, uint32_t parity, GCtl* ctl, int32_t* err) {
+  if (mbar_wait_bounded(bar, parity, kGWaitNs)) return true;
+  set_err(err, PBS_DEVERR_TIMEOUT);
+  atomicExch(&ctl->abort, 1);
+  return false;
+}
+
+__device__ __forceinline__ bool g_warp_wait(uint64_t* bar, uint32_t parity, GCtl* ctl, int32_t* err) {
+  const bool ok = g_wait(bar, parity, ctl, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void g_tma_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void g_tma_5d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2, int c3,
+                                         int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
+__device__ __forceinline__ void g_sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Drop a 128-byte line from L2 without writing it back (its contents become undefined).
+__device__ __forceinline__ void discard_l2(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+__device__ __forceinline__ uint4 ldcg16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float2 ldcg_f2(const void* p) {
+  float2 r;
+  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(r.x), "=f"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t x) { return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu))); }
+__device__ __forceinline__ float f16_hi(uint32_t x) { return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16))); }
+
+// Window of the segment [T0, T1) with index `wi`: windows are numbered request by request, each
+// request's tokens cut at multiples of kGatherWinTok from its first token. Warp-collective.
+// Returns false when wi is past the last window.
+struct WinInfo {
+  int r, ta, tb, c0, ctx0, seq_len;
+};
+__device__ __forceinline__ bool find_window(const AttendArgs& a, const GatherWs& w, int wi, WinInfo& out) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  bool found = false;
+  for (int r0 = 0; r0 < a.num_reqs && !found; r0 += 32) {
+    const int rr = r0 + lane;
+    int c0 = 0, c1 = 0, sl = 0;
+    if (rr < a.num_reqs) {
+      c0 = __ldg(a.cu_seqlens_q + rr);
+      c1 = __ldg(a.cu_seqlens_q + rr + 1);
+      sl = __ldg(a.seq_lens + rr);
+    }
+    const int lo = max(c0, w.T0), hi = min(c1, w.T1);
+    const int nw = lo < hi ? (hi - 1 - c0) / kGatherWinTok - (lo - c0) / kGatherWinTok + 1 : 0;
+    int incl = nw;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - nw + base;
+    const uint32_t hit = __ballot_sync(0xffffffffu, wi >= excl && wi < excl + nw);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const int ex = __shfl_sync(0xffffffffu, excl, src);
+      const int sc0 = __shfl_sync(0xffffffffu, c0, src);
+      const int sc1 = __shfl_sync(0xffffffffu, c1, src);
+      const int ssl = __shfl_sync(0xffffffffu, sl, src);
+      const int slo = max(sc0, w.T0), shi = min(sc1, w.T1);
+      const int wrel = (slo - sc0) / kGatherWinTok + (wi - ex);
+      out.r = r0 + src;
+      out.c0 = sc0;
+      out.ctx0 = ssl - (sc1 - sc0);
+      out.seq_len = ssl;
+      out.ta = max(sc0 + wrel * kGatherWinTok, slo);
+      out.tb = min(sc0 + (wrel + 1) * kGatherWinTok, shi);
+      found = true;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return found;
+}
+
+// ------------------------------------------------------------------------------------------
+// index kernel: one CTA per window
+// ------------------------------------------------------------------------------------------
+// Dynamic shared memory: cnt[max_blocks], cur[max_blocks], pairs_s[kGatherWinTok * k].
+__global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendArgs a, const GatherWs w) {
+  extern __shared__ int32_t ish[];
+  int32_t* cnt = ish;
+  int32_t* cur = ish + a.max_blocks;
+  int32_t* pairs_s = cur + a.max_blocks;
+  __shared__ int s_win[6];
+  __shared__ int s_found, s_np, s_nblk;
+  __shared__ int s_wsum[kIdxThreads / 32], s_wnz[kIdxThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wi = blockIdx.x;
+  int32_t* wrec = w.wins + static_cast<int64_t>(wi) * 8;
+  if (warp == 0) {
+    WinInfo info;
+    const bool f = find_window(a, w, wi, info);
+    if (lane == 0) {
+      s_found = f ? 1 : 0;
+      s_np = 0;
+      if (f) {
+        s_win[0] = info.r;
+        s_win[1] = info.ta;
+        s_win[2] = info.tb;
+        s_win[3] = info.c0;
+        s_win[4] = info.ctx0;
+        s_win[5] = info.seq_len;
+        // blocks any token of the window may select: up to the last token's own block
+        const int pos_last = info.ctx0 + (info.tb - 1 - info.c0);
+        s_nblk = pos_last >= 0 ? min(pos_last / kSparseBlock + 1, a.max_blocks) : 0;
+      } else {
+        s_nblk = 0;
+      }
+    }
+  }
+  __syncthreads();
+  if (!s_found) {
+    if (threadIdx.x == 0) {
+      wrec[0] = -1;
+      wrec[4] = 0;
+      wrec[5] = 0;
+      w.win_ctr[wi] = 0;
+    }
+    return;
+  }
+  const int r = s_win[0], ta = s_win[1], tb = s_win[2], c0 = s_win[3], ctx0 = s_win[4];
+  const int nblk = s_nblk;
+  for (int i = threadIdx.x; i < nblk; i += kIdxThreads) cnt[i] = 0;
+  __syncthreads();
+
+  // ---- each token's distinct valid blocks, sorted; count per block -------------------------
+  const int n = tb - ta;
+  for (int tt = warp; tt < n; tt += kIdxThreads / 32) {
+    const int t = ta + tt;
+    const int tr = t - w.T0;
+    const int pos = ctx0 + (t - c0);
+    const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
+    const int own = causal_len > 0 ? pos / kSparseBlock : -1;
+    const int32_t* row = a.topk + static_cast<int64_t>(t) * a.topk_row_stride;
+    const int b0 = lane < a.k ? __ldg(row + lane) : -1;
+    const int b1 = lane + 32 < a.k ? __ldg(row + lane + 32) : -1;
+    bool v0 = lane < a.k && causal_len > 0 && b0 >= 0 && b0 <= own;
+    bool v1 = lane + 32 < a.k && causal_len > 0 && b1 >= 0 && b1 <= own;
+    const bool oob = (v0 && b0 >= a.max_blocks) || (v1 && b1 >= a.max_blocks);
+    const bool bad = __any_sync(0xffffffffu, oob);
+    int n_t = 0;
+    if (bad) {
+      if (lane == 0) set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+    } else {
+      // keep the first occurrence of every value (entries j = lane and j = lane + 32)
+      const uint32_t vm0 = __ballot_sync(0xffffffffu, v0), vm1 = __ballot_sync(0xffffffffu, v1);
+      bool k0 = v0, k1 = v1;
+      const int kk = a.k;
+      for (int j = 0; j < kk; ++j) {
+        const int bj = j < 32 ? __shfl_sync(0xffffffffu, b0, j) : __shfl_sync(0xffffffffu, b1, j - 32);
+        const bool vj = ((j < 32 ? vm0 >> j : vm1 >> (j - 32)) & 1u) != 0;
+        if (vj) {
+          if (j < lane && bj == b0) k0 = false;
+          if (j < lane + 32 && bj == b1) k1 = false;
+        }
+      }
+      const uint32_t km0 = __ballot_sync(0xffffffffu, k0), km1 = __ballot_sync(0xffffffffu, k1);
+      n_t = __popc(km0) + __popc(km1);
+      // slot = rank of the value among the kept ones (sorted order)
+      int r0 = 0, r1 = 0;
+      for (int j = 0; j < kk; ++j) {
+        const int bj = j < 32 ? __shfl_sync(0xffffffffu, b0, j) : __shfl_sync(0xffffffffu, b1, j - 32);
+        const bool kj = ((j < 32 ? km0 >> j : km1 >> (j - 32)) & 1u) != 0;
+        if (kj) {
+          r0 += bj < b0 ? 1 : 0;
+          r1 += bj < b1 ? 1 : 0;
+        }
+      }
+      if (k0) {
+        atomicAdd(&cnt[b0], 1);
+        const int at = atomicAdd(&s_np, 1);
+        pairs_s[at] = (b0 << 14) | (tt << 6) | r0;
+      }
+      if (k1) {
+        atomicAdd(&cnt[b1], 1);
+        const int at = atomicAdd(&s_np, 1);
+        pairs_s[at] = (b1 << 14) | (tt << 6) | r1;
+      }
+    }
+    if (lane == 0) w.tok_n[tr] = n_t;
+    for (int g = lane; g < a.num_kv_heads; g += 32) w.tickets[static_cast<int64_t>(tr) * a.num_kv_heads + g] = 0;
+    if (n_t == 0) {
+      // nothing to attend (no valid block, or a block past the page table): zero output
+      uint16_t* orow = a.out + static_cast<int64_t>(t) * a.out_row_stride;
+      for (int h = 0; h < a.num_heads; ++h) {
+        if (lane < 16)
+          *reinterpret_cast<uint4*>(orow + static_cast<int64_t>(h) * a.out_head_stride + lane * 8) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (a.lse != nullptr)
+        for (int h = lane; h < a.num_heads; h += 32)
+          a.lse[static_cast<int64_t>(t) * a.lse_row_stride + h] = -INFINITY;
+    }
+  }
+  __syncthreads();
+
+  // ---- exclusive scan of the counts; buckets numbered by decreasing block id ----------------
+  const int per = (nblk + kIdxThreads - 1) / kIdxThreads;
+  const int lo = min(static_cast<int>(threadIdx.x) * per, nblk), hi = min(lo + per, nblk);
+  int s = 0, z = 0;
+  for (int i = lo; i < hi; ++i) {
+    s += cnt[i];
+    z += cnt[i] > 0 ? 1 : 0;
+  }
+  int is = s, iz = z;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int vs = __shfl_up_sync(0xffffffffu, is, off), vz = __shfl_up_sync(0xffffffffu, iz, off);
+    if (lane >= off) {
+      is += vs;
+      iz += vz;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[warp] = is;
+    s_wnz[warp] = iz;
+  }
+  __syncthreads();
+  int ws = 0, wz = 0, tz = 0;
+  for (int i = 0; i < kIdxThreads / 32; ++i) {
+    if (i < warp) {
+      ws += s_wsum[i];
+      wz += s_wnz[i];
+    }
+    tz += s_wnz[i];
+  }
+  int off_s = ws + is - s, off_z = wz + iz - z;  // exclusive prefixes at this thread's first block
+  const int64_t pair_base = static_cast<int64_t>(wi) * kGatherWinTok * a.k;
+  int4* brow = w.buckets + static_cast<int64_t>(wi) * w.bcap;
+  for (int i = lo; i < hi; ++i) {
+    const int c = cnt[i];
+    cur[i] = off_s;
+    if (c > 0) {
+      brow[tz - 1 - off_z] = make_int4(i, static_cast<int>(pair_base + off_s), c, 0);
+      ++off_z;
+    }
+    off_s += c;
+  }
+  __syncthreads();
+
+  // ---- scatter the pairs into their buckets ---------------------------------------------------
+  const int np = s_np;
+  for (int p = threadIdx.x; p < np; p += kIdxThreads) {
+    const int v = pairs_s[p];
+    const int b = v >> 14, tt = (v >> 6) & 255, rank = v & 63;
+    const int at = atomicAdd(&cur[b], 1);
+    w.pairs[pair_base + at] = ((ta + tt - w.T0) << 6) | rank;
+  }
+  if (threadIdx.x == 0) {
+    wrec[0] = r;
+    wrec[1] = c0;
+    wrec[2] = ctx0;
+    wrec[3] = s_win[5];
+    wrec[4] = tz;                     // buckets
+    wrec[5] = tz * a.num_kv_heads;    // work items
+    w.win_ctr[wi] = 0;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// attend kernel: persistent, one CTA per SM
+// ------------------------------------------------------------------------------------------
+
+// Merge the partials of (segment token tr, kv head g) and write its output rows (warp-wide).
+template <int kG>
+__device__ __forceinline__ void merge_token(const AttendArgs& a, const GatherWs& w, int tr, int g, int nsel) {
+  constexpr int kLanesPerHead = 32 / kG;        // 4 (G = 8) or 2 (G = 16)
+  constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
+  const int lane = threadIdx.x & 31;
+  const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
+  const int64_t base = (static_cast<int64_t>(tr) * a.num_kv_heads + g) * a.k;  // slot 0 of (tr, g)
+  float L = -INFINITY;
+  for (int j = 0; j < nsel; ++j) L = fmaxf(L, ldcg_f2(w.ml + (base + j) * kG + h).x);
+  float acc[kE];
+#pragma unroll
+  for (int i = 0; i < kE; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  for (int j = 0; j < nsel; ++j) {
+    const float2 me = ldcg_f2(w.ml + (base + j) * kG + h);
+    den += ex2(me.x - L);
+    const float f = ex2(me.x - L + me.y);
+    const uint16_t* src = w.part + ((base + j) * kG + h) * kHeadDim + d0;
+#pragma unroll
+    for (int q = 0; q < kE / 8; ++q) {
+      const uint4 v = ldcg16(src + 8 * q);
+      acc[8 * q + 0] = fmaf(f, f16_lo(v.x), acc[8 * q + 0]);
+      acc[8 * q + 1] = fmaf(f, f16_hi(v.x), acc[8 * q + 1]);
+      acc[8 * q + 2] = fmaf(f, f16_lo(v.y), acc[8 * q + 2]);
+      acc[8 * q + 3] = fmaf(f, f16_hi(v.y), acc[8 * q + 3]);
+      acc[8 * q + 4] = fmaf(f, f16_lo(v.z), acc[8 * q + 4]);
+      acc[8 * q + 5] = fmaf(f, f16_hi(v.z), acc[8 * q + 5]);
+      acc[8 * q + 6] = fmaf(f, f16_lo(v.w), acc[8 * q + 6]);
+      acc[8 * q + 7] = fmaf(f, f16_hi(v.w), acc[8 * q + 7]);
+    }
+  }
+  const int t = w.T0 + tr;
+  const float inv = a.v_scale / den;
+  uint16_t* dst = a.out + static_cast<int64_t>(t) * a.out_row_stride +
+                  static_cast<int64_t>(g * kG + h) * a.out_head_stride + d0;
+#pragma unroll
+  for (int q = 0; q < kE / 8; ++q)
+    *reinterpret_cast<uint4*>(dst + 8 * q) =
+        make_uint4(pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                   pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+  if (a.lse != nullptr && (lane % kLanesPerHead) == 0)
+    a.lse[static_cast<int64_t>(t) * a.lse_row_stride + g * kG + h] = (L + log2f(den)) * kLn2;
+  // the merged partials are not read again: drop their lines (128 B = 64 dims) from L2
+  __syncwarp();
+  if ((d0 & 63) == 0)
+    for (int j = 0; j < nsel; ++j) discard_l2(w.part + ((base + j) * kG + h) * kHeadDim + d0);
+}
+
+template <int kG>
+__global__ void __launch_bounds__(kGThreads, 1)
+    gather_attend_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                         const AttendArgs a, const GatherWs w) {
+  constexpr int kTok = kGRows / kG;  // tokens per chunk
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the 128B-swizzled operands need 1024-byte alignment
+  uint8_t* big = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = big;                   // 2 x 32 KiB: [half][rows][128 B]
+  uint8_t* k_s = big + 2 * kGQBytes;    // 2 x 32 KiB: [page][row half][quarter][8 rows][128 B]
+  uint8_t* v_s = k_s + 2 * kGTile;      // 2 x 32 KiB
+  GCtl* ctl = reinterpret_cast<GCtl*>(v_s + 2 * kGTile);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDescRing; ++i) {
+      mbar_init(&ctl->desc_full[i], 1);
+      mbar_init(&ctl->desc_empty[i], 5);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->q_full[i], 1);
+      mbar_init(&ctl->q_empty[i], 1);
+      mbar_init(&ctl->k_full[i], 1);
+      mbar_init(&ctl->v_full[i], 1);
+      mbar_init(&ctl->v_land[i], 1);
+      mbar_init(&ctl->kv_empty[i], 1);
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->p_full[i], 4);
+      mbar_init(&ctl->pv_done[i], 1);
+    }
+    mbar_init(&ctl->mma_fin, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) tc::alloc(&ctl->tmem_base, 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer / scheduler
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
+    }
+    int cur_w = 0, n_item = 0, c = 0;
+    int q_n[2] = {0, 0}, k_n[2] = {0, 0}, v_n[2] = {0, 0}, land_n[2] = {0, 0};
+    bool ok = true;
+    while (ok) {
+      // ---- next item: windows in order, items of a window from its counter
+      int item = -1;
+      if (lane == 0) {
+        while (cur_w < w.num_win) {
+          const int n_items = __ldg(w.wins + static_cast<int64_t>(cur_w) * 8 + 5);
+          if (n_items > 0) {
+            const int i = atomicAdd(w.win_ctr + cur_w, 1);
+            if (i < n_items) {
+              item = i;
+              break;
+            }
+          }
+          ++cur_w;
+        }
+      }
+      item = __shfl_sync(0xffffffffu, item, 0);
+      cur_w = __shfl_sync(0xffffffffu, cur_w, 0);
+      if (item < 0) break;
+      if (g_aborted(ctl)) {
+        ok = false;
+        break;
+      }
+      const int32_t* wrec = w.wins + static_cast<int64_t>(cur_w) * 8;
+      const int r = __ldg(wrec + 0), c0 = __ldg(wrec + 1), ctx0 = __ldg(wrec + 2), seq_len = __ldg(wrec + 3);
+      const int g = item % a.num_kv_heads;
+      const int4 bk = __ldg(w.buckets + static_cast<int64_t>(cur_w) * w.bcap + item / a.num_kv_heads);
+      const int b = bk.x, poff = bk.y, pcnt = bk.z;
+      const int Y = n_item & 1;
+      // ---- K and V of block b, head g
+      if (n_item >= 2) {
+        bool go = true;
+        if (lane == 0) go = g_wait(&ctl->kv_empty[Y], ((n_item >> 1) - 1) & 1, ctl, a.err_word);
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      const int phys = __ldg(a.page_table + static_cast<int64_t>(r) * a.pt_row_stride + b);
+      const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
+      if (lane == 0 && (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages)) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+      const int pos_last = seq_len - 1;
+      const int last_rows = pos_last - b * kSparseBlock + 1;  // rows of block b holding written tokens
+      const bool tail = last_rows < kSparseBlock;
+      uint64_t* vbar = tail ? &ctl->v_land[Y] : &ctl->v_full[Y];
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ctl->k_full[Y], kGTile);
+        mbar_arrive_expect_tx(vbar, kGTile);
+      }
+      __syncwarp();
+      // out-of-range pages read as zeros (tensor-map bounds)
+      if (lane < 2 * kPagesPerBlock) {
+        const int pg = lane & 7;
+        const bool isv = lane >= kPagesPerBlock;
+        g_tma_5d((isv ? v_s : k_s) + Y * kGTile + pg * 4096, &kv_map, isv ? vbar : &ctl->k_full[Y], 0, 0, isv ? 2 : 0, 0,
+                 static_cast<int>((pbase + pg) * a.num_kv_heads + g));
+      }
+      ++k_n[Y];
+      if (tail) {
+        // rows past the request's last token may hold anything (unwritten cache rows): zero
+        // them in V before any PV reads the buffer
+        ++land_n[Y];
+        bool go = true;
+        if (lane == 0) go = g_wait(&ctl->v_land[Y], (land_n[Y] - 1) & 1, ctl, a.err_word);
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t vb = smem_u32(v_s + Y * kGTile);
+        const int first = max(last_rows, 0);
+        for (int e = lane; e < (kSparseBlock - first) * 16; e += 32) {
+          const int key = first + (e >> 4), vq = (e >> 3) & 1, ch = e & 7;
+          g_sts128(vb + (key >> 3) * 2048 + vq * 1024 + (key & 7) * 128 + ch * 16, 0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->v_full[Y]);
+      }
+      ++v_n[Y];
+      // ---- the item's chunks
+      const int nch = (pcnt + kTok - 1) / kTok;
+      for (int ch = 0; ch < nch && ok; ++ch, ++c) {
+        const int ds = c % kDescRing;
+        if (c >= kDescRing) {
+          bool go = true;
+          if (lane == 0) go = g_wait(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1, ctl, a.err_word);
+          if (!__shfl_sync(0xffffffffu, go, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        ChunkDesc* d = &ctl->desc[ds];
+        const int n_tok = min(kTok, pcnt - ch * kTok);
+        int t_lane = 0;
+        if (lane < n_tok) {
+          const int pr = __ldg(w.pairs + poff + ch * kTok + lane);
+          const int tr = pr >> 6;
+          const int t = w.T0 + tr;
+          const int pos = ctx0 + (t - c0);
+          d->tr[lane] = tr;
+          d->slot[lane] = pr & 63;
+          d->lim[lane] = pos / kSparseBlock == b ? pos - b * kSparseBlock + 1 : kSparseBlock;
+          d->nsel[lane] = __ldg(w.tok_n + tr);
+          t_lane = t;
+        }
+        if (lane == 0) {
+          d->end = 0;
+          d->b = b;
+          d->g = g;
+          d->ybuf = Y;
+          d->last = ch == nch - 1 ? 1 : 0;
+          d->n_tok = n_tok;
+          d->item = n_item;
+        }
+        // ---- gather the chunk's Q rows: token j, half hf -> rows j*G.., dims 64 hf..
+        const int qb = c & 1;
+        if (c >= 2) {
+          bool go = true;
+          if (lane == 0) go = g_wait(&ctl->q_empty[qb], ((c >> 1) - 1) & 1, ctl, a.err_word);
+          if (!__shfl_sync(0xffffffffu, go, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&ctl->q_full[qb], n_tok * 2 * kG * 128);
+        __syncwarp();
+        {
+          const int j = lane % kTok, hf = lane / kTok;
+          const int tj = __shfl_sync(0xffffffffu, t_lane, j);
+          if (lane < 2 * kTok && j < n_tok)
+            g_tma_3d(q_s + qb * kGQBytes + hf * kGHalf + j * kG * 128, &q_map, &ctl->q_full[qb], hf * 64, g * kG, tj);
+        }
+        ++q_n[qb];
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->desc_full[ds]);
+      }
+      ++n_item;
+    }
+    // ---- end marks: one for each softmax warpgroup (chunks c and c + 1)
+    for (int e = 0; e < 2 && ok; ++e, ++c) {
+      const int ds = c % kDescRing;
+      if (c >= kDescRing) {
+        bool go = true;
+        if (lane == 0) go = g_wait(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1, ctl, a.err_word);
+        if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      }
+      if (lane == 0) {
+        ctl->desc[ds].end = 1;
+        __threadfence_block();
+        mbar_arrive(&ctl->desc_full[ds]);
+      }
+      __syncwarp();
+    }
+    // every copy issued must land before the CTA exits
+    if (lane == 0) {
+      for (int i = 0; i < 2; ++i) {
+        if (q_n[i] > 0) mbar_wait_bounded(&ctl->q_full[i], (q_n[i] - 1) & 1, kGWaitNs);
+        if (k_n[i] > 0) mbar_wait_bounded(&ctl->k_full[i], (k_n[i] - 1) & 1, kGWaitNs);
+        if (v_n[i] > 0) mbar_wait_bounded(&ctl->v_full[i], (v_n[i] - 1) & 1, kGWaitNs);
+        if (land_n[i] > 0) mbar_wait_bounded(&ctl->v_land[i], (land_n[i] - 1) & 1, kGWaitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
+      constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
+      int prev_y = 0, prev_last = 0, prev_item = 0;
+      for (int c = 0;; ++c) {
+        const int ds = c % kDescRing;
+        if (!g_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+        const ChunkDesc* d = &ctl->desc[ds];
+        const int end = d->end;
+        const int Y = d->ybuf, last = d->last, item = d->item;
+        if (!end) {
+          const int X = c & 1;
+          // the K buffer of item n completes once per use: phase (n / 2) & 1
+          if (!g_wait(&ctl->k_full[Y], (item >> 1) & 1, ctl, a.err_word)) break;
+          if (!g_wait(&ctl->q_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
+          tc::fence_after_sync();
+          const uint32_t q_addr = smem_u32(q_s + X * kGQBytes);
+          const uint32_t k_addr = smem_u32(k_s + Y * kGTile);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ss(tmem + X * 128, tc::smem_desc_sw128(q_addr + (ks >> 2) * kGHalf + (ks & 3) * 32, 16, 1024),
+                       tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048), kIdescS, ks > 0);
+          tc::commit(&ctl->s_full[X]);
+          tc::commit(&ctl->q_empty[X]);
+        }
+        if (c >= 1) {
+          // PV of the previous chunk: O(X') = P hi V + P lo V, P in S buffer X' (per 32-key group
+          // i: hi words in columns 32 i .. 32 i + 15, lo words in 32 i + 16 .. 32 i + 31)
+          const int cp = c - 1, Xp = cp & 1;
+          if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) break;
+          if (!g_wait(&ctl->v_full[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
+          tc::fence_after_sync();
+          const uint32_t v_addr = smem_u32(v_s + prev_y * kGTile);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t pa = tmem + Xp * 128 + (ks >> 1) * 32 + part * 16 + (ks & 1) * 8;
+              tc::mma_ts(tmem + 256 + Xp * 128, pa, tc::smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), kIdescPV,
+                         !(part == 0 && ks == 0));
+            }
+          }
+          tc::commit(&ctl->pv_done[Xp]);
+          if (prev_last) tc::commit(&ctl->kv_empty[prev_y]);
+          mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
+        }
+        if (end) break;
+        prev_y = Y;
+        prev_last = last;
+        prev_item = item;
+      }
+      // every MMA issued must complete before TMEM is released
+      tc::commit(&ctl->mma_fin);
+      mbar_wait_bounded(&ctl->mma_fin, 0, kGWaitNs);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int X = (warp - 4) >> 2;  // warpgroup: chunks X, X + 2, ...
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // TMEM lane
+    const int j = row / kG, h = row % kG;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t ts = tmem + X * 128 + lane_off;
+    const uint32_t to = tmem + 256 + X * 128 + lane_off;
+    const float sl2 = a.scale_log2;
+    for (int c = X;; c += 2) {
+      const int ds = c % kDescRing;
+      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+      const ChunkDesc* d = &ctl->desc[ds];
+      if (d->end) break;
+      const int n_tok = d->n_tok;
+      const bool valid = j < n_tok;
+      const int lim = valid ? d->lim[j] : 0;
+      if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
+      tc::fence_after_sync();
+      // ---- pass 1: row maximum over the valid keys
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tc::ld32(ts + 32 * cc, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float s = __uint_as_float(v[i]);
+          mx = 32 * cc + i < lim ? fmaxf(mx, s) : mx;
+        }
+      }
+      const float m = lim > 0 ? mx * sl2 : 0.f;
+      // ---- pass 2: P = 2^(s sl2 - m) as bf16 hi + lo over the same columns
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tc::ld32(ts + 32 * cc, v);
+        tc::wait_ld();
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int key = 32 * cc + i;
+          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(v[i]), sl2, -m)) : 0.f;
+          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m)) : 0.f;
+          l0 += p0;
+          l1 += p1;
+          const uint32_t hh = pack_bf16(p0, p1);
+          hi[i >> 1] = hh;
+          lo[i >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
+        }
+        tc::st16(ts + 32 * cc, hi);
+        tc::st16(ts + 32 * cc + 16, lo);
+      }
+      const float l = l0 + l1;
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_full[X]);
+      // ---- epilogue: partial O / l as fp16 scaled by 2^-e
+      if (!g_warp_wait(&ctl->pv_done[X], (c >> 1) & 1, ctl, a.err_word)) break;
+      tc::fence_after_sync();
+      float mo = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tc::ld32(to + 32 * cc, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mo = fmaxf(mo, fabsf(__uint_as_float(v[i])));
+      }
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // e: the exponent that puts max |O / l| into [2^14, 2^15)
+      int e = 0;
+      const float mn = mo * inv_l;
+      if (mn > 0.f) e = static_cast<int>((__float_as_uint(mn) >> 23) & 0xffu) - 127 - 14;
+      e = max(-100, min(100, e));
+      const float sc = inv_l * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      const int tr = valid ? d->tr[j] : 0;
+      const int64_t prow = ((static_cast<int64_t>(tr) * a.num_kv_heads + d->g) * a.k + (valid ? d->slot[j] : 0)) * kG + h;
+      uint16_t* dst = w.part + prow * kHeadDim;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tc::ld32(to + 32 * cc, v);
+        tc::wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float* f = reinterpret_cast<const float*>(&v[8 * q4]);
+            *reinterpret_cast<uint4*>(dst + 32 * cc + 8 * q4) =
+                make_uint4(pack_f16(f[0] * sc, f[1] * sc), pack_f16(f[2] * sc, f[3] * sc), pack_f16(f[4] * sc, f[5] * sc),
+                           pack_f16(f[6] * sc, f[7] * sc));
+          }
+        }
+      }
+      if (valid) *reinterpret_cast<float2*>(w.ml + prow) = make_float2(m + log2f(l), static_cast<float>(e));
+      // ---- ticket per (token, kv head); the chunk that completes a token merges it
+      __threadfence();
+      __syncwarp();
+      bool done = false;
+      int nsel = 0;
+      if (valid && h == 0) {
+        nsel = d->nsel[j];
+        const int old = atomicAdd(w.tickets + static_cast<int64_t>(tr) * a.num_kv_heads + d->g, 1);
+        done = old + 1 == nsel;
+      }
+      uint32_t dm = __ballot_sync(0xffffffffu, done);
+      const int gg = d->g;
+      if (dm) {
+        __threadfence();
+        while (dm) {
+          const int src = __ffs(dm) - 1;
+          dm &= dm - 1;
+          merge_token<kG>(a, w, __shfl_sync(0xffffffffu, tr, src), gg, __shfl_sync(0xffffffffu, nsel, src));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc::fence_after_sync();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool prefill_gather_supported(const AttendArgs& a) {
+  return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
+         a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
+         a.num_pages * a.num_kv_heads <= 0x7fffffffLL && a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
+         reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 &&
+         reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct GatherLayout {
+  size_t part, ml, tok_n, tickets, pairs, buckets, wins, win_ctr, total;
+  int num_win, bcap;
+};
+
+GatherLayout gather_layout(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks) {
+  GatherLayout L = {};
+  L.num_win = static_cast<int>(seg_tokens / kGatherWinTok + 2 * static_cast<int64_t>(num_reqs) + 1);
+  L.bcap = std::min(max_blocks, kGatherWinTok * k);
+  size_t off = 0;
+  L.part = off;
+  off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * kHeadDim * 2);
+  L.ml = off;
+  off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * 8);
+  L.tok_n = off;
+  off = align256(off + static_cast<size_t>(seg_tokens) * 4);
+  L.tickets = off;
+  off = align256(off + static_cast<size_t>(seg_tokens) * num_kv_heads * 4);
+  L.pairs = off;
+  off = align256(off + static_cast<size_t>(L.num_win) * kGatherWinTok * k * 4);
+  L.buckets = off;
+  off = align256(off + static_cast<size_t>(L.num_win) * L.bcap * 16);
+  L.wins = off;
+  off = align256(off + static_cast<size_t>(L.num_win) * 8 * 4);
+  L.win_ctr = off;
+  off = align256(off + static_cast<size_t>(L.num_win) * 4);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+size_t gather_workspace_bytes(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k,
+                              int max_blocks) {
+  return gather_layout(seg_tokens, num_reqs, num_heads, num_kv_heads, k, max_blocks).total;
+}
+
+int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks,
+                              size_t ws_bytes) {
+  if (total_q <= kGatherMaxSegment &&
+      gather_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, k, max_blocks) <= ws_bytes)
+    return total_q;
+  // the largest multiple of the window that fits
+  int64_t lo = 0, hi = std::min(total_q, kGatherMaxSegment) / kGatherWinTok;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (gather_workspace_bytes(mid * kGatherWinTok, num_reqs, num_heads, num_kv_heads, k, max_blocks) <= ws_bytes)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo * kGatherWinTok;
+}
+
+template <int kG>
+cudaError_t launch_gather_g(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  const int64_t seg = gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k, a.max_blocks,
+                                            ws_bytes);
+  if (seg <= 0) return cudaErrorInvalidValue;
+  const GatherLayout L = gather_layout(seg, a.num_reqs, a.num_heads, a.num_kv_heads, a.k, a.max_blocks);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  GatherWs w = {};
+  w.part = reinterpret_cast<uint16_t*>(base + L.part);
+  w.ml = reinterpret_cast<float2*>(base + L.ml);
+  w.tok_n = reinterpret_cast<int32_t*>(base + L.tok_n);
+  w.tickets = reinterpret_cast<int32_t*>(base + L.tickets);
+  w.pairs = reinterpret_cast<int32_t*>(base + L.pairs);
+  w.buckets = reinterpret_cast<int4*>(base + L.buckets);
+  w.wins = reinterpret_cast<int32_t*>(base + L.wins);
+  w.win_ctr = reinterpret_cast<int32_t*>(base + L.win_ctr);
+  w.bcap = L.bcap;
+
+  const size_t idx_smem = static_cast<size_t>(2 * a.max_blocks + kGatherWinTok * a.k) * 4;
+  cudaError_t e = cudaFuncSetAttribute(gather_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(idx_smem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gather_attend_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kGSmem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  for (int64_t t0 = 0; t0 < a.num_rows; t0 += seg) {
+    w.T0 = static_cast<int32_t>(t0);
+    w.T1 = static_cast<int32_t>(std::min<int64_t>(a.num_rows, t0 + seg));
+    w.num_win = static_cast<int32_t>((w.T1 - w.T0) / kGatherWinTok + 2 * static_cast<int64_t>(a.num_reqs) + 1);
+    gather_index_kernel<<<w.num_win, kIdxThreads, idx_smem, stream>>>(a, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    gather_attend_kernel<kG><<<sms, kGThreads, kGSmem, stream>>>(kv_map, q_map, a, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream) {
+  return a.group == 16 ? launch_gather_g<16>(a, kv_map, q_map, ws, ws_bytes, stream)
+                       : launch_gather_g<8>(a, kv_map, q_map, ws, ws_bytes, stream);
+}
+
+}  // namespace pbs

@@ -108,6 +108,41 @@ bool prefill_tc_supported(const AttendArgs& a);
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream);
 
+// Prefill attend by key block (tcgen05, bf16 packed cache, GQA 8 or 16): an index kernel
+// buckets each 256-token window's tokens by selected block, a persistent kernel attends every
+// (block, kv head) bucket 16 gathered tokens at a time and merges each token's per-block
+// partials. Workspace (caller-owned) per segment of tokens: fp16 partials and their
+// (log2-sum-exp, exponent) pairs, per-token counts and tickets, the buckets. A call is processed
+// in segments of at most `gather_segment_tokens` tokens, one index + one attend launch each.
+constexpr int kGatherWinTok = 256;      // tokens per window (request-relative)
+constexpr int kGatherMaxBlocks = 8192;  // page-table width the index kernel's histogram covers
+constexpr int64_t kGatherMaxSegment = int64_t(1) << 20;
+
+struct GatherWs {
+  uint16_t* part;      // fp16 [seg][Hkv][k][G][128]: per-(token, block) output / l * 2^-e
+  float2* ml;          // [seg][Hkv][k][G]: (log2-sum-exp of the block's logits, e)
+  int32_t* tok_n;      // [seg]: blocks the token attends (its partial count)
+  int32_t* tickets;    // [seg][Hkv]: finished partials
+  int32_t* pairs;      // bucket entries: segment token << 6 | partial slot
+  int4* buckets;       // [windows][bcap]: (block, first entry, entries, 0)
+  int32_t* wins;       // [windows][8]: request, first token, context, seq_len, buckets, items
+  int32_t* win_ctr;    // [windows]: items taken
+  int32_t T0, T1;      // segment [T0, T1) of the call's tokens
+  int32_t num_win;     // windows of the segment (upper bound; surplus ones are empty)
+  int32_t bcap;
+};
+
+bool prefill_gather_supported(const AttendArgs& a);
+size_t gather_workspace_bytes(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k,
+                              int max_blocks);
+// Tokens per segment a workspace of `ws_bytes` allows (0: not even one window).
+int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks,
+                              size_t ws_bytes);
+// `kv_map`: the half-row 5-D map of the packed cache; `q_map`: {128, heads, tokens} with a
+// {64, G, 1} box.
+cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream);
+
 // Index-cache insert.
 struct InsertArgs {
   const uint8_t* index_k;

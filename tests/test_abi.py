@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 5
+    assert pbs.abi_version() == 6
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"
@@ -113,6 +113,19 @@ def test_attend_host_checks(L):
     assert _decode_attend(L, ws=N, wsb=16) == 1            # bytes without a pointer
     assert _decode_attend(L, ws=ctypes.c_void_p(0x10008), wsb=need) == 4
     assert _decode_attend(L, ws=A, wsb=need - 1) == 2      # too small for the rows
+
+
+def test_prefill_workspace_bytes(L):
+    f = L.pbs_prefill_workspace_bytes
+    f.restype = ctypes.c_size_t
+    one = f(256, 1, 64, 8, 16, 64)
+    # fp16 partials + (lse, exponent) pairs per (token, query head, top-k slot), plus the buckets
+    assert one >= 256 * 64 * 16 * (2 * 128 + 8)
+    assert f(512, 1, 64, 8, 16, 64) > one and f(256, 1, 64, 8, 32, 64) > one
+    assert f(1 << 21, 1, 64, 8, 16, 64) == f(1 << 20, 1, 64, 8, 16, 64)   # one segment holds at most 2^20 tokens
+    for bad in ((0, 1, 64, 8, 16, 64), (256, 0, 64, 8, 16, 64), (256, 1, 60, 8, 16, 64), (256, 1, 64, 8, 65, 64),
+                (256, 1, 64, 8, 16, 0)):
+        assert f(*bad) == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")

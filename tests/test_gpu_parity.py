@@ -54,17 +54,20 @@ def oracle_tables(b, part):
                                                    np_i32(p.seq_lens), b.block_page_stride)
 
 
-def gpu_attend(pbs, b, part, err=None, workspace=None):
+def gpu_attend(pbs, b, part, err=None, workspace="default"):
+    """The binding's call for one part; workspace "default" leaves the binding's own default
+    (decode: none, prefill: the cached workspace of the gathered-row kernel)."""
+    ws = {} if isinstance(workspace, str) and workspace == "default" else {"workspace": workspace}
     if part == "dec":
         d = b.dec
         out = pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table,
                                           d.seq_lens, d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale,
-                                          b.block_page_stride, err_word=err, workspace=workspace)
+                                          b.block_page_stride, err_word=err, **ws)
     else:
         p = b.pre
         out = pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
                                            p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
-                                           b.block_page_stride, err_word=err, workspace=workspace)
+                                           b.block_page_stride, err_word=err, **ws)
     torch.cuda.synchronize()
     return out.to(torch.float64).cpu().numpy()
 
@@ -269,7 +272,7 @@ def test_attend_lse_decode(pbs, kv_dtype, split, heads, monkeypatch):
     assert_close(dict(enumerate(out.double().cpu().numpy())), oracle_decode(b), kv_dtype, "decode out with lse")
 
 
-@pytest.mark.parametrize("kernel", ["tc", "token"])
+@pytest.mark.parametrize("kernel", ["tc", "token", "gather"])
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
 def test_attend_lse_prefill(pbs, kernel, heads, monkeypatch):
     monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
@@ -386,10 +389,10 @@ PREFILL_CASES = [
 
 
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
-@pytest.mark.parametrize("kernel", ["tc", "token"])
+@pytest.mark.parametrize("kernel", ["tc", "token", "gather"])
 @pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
 def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, heads, monkeypatch):
-    """Both prefill kernels, GQA 8 (tile = 16 tokens x 8 heads) and GQA 16 (8 tokens x 16 heads)."""
+    """Every prefill kernel, GQA 8 (tile = 16 tokens x 8 heads) and GQA 16 (8 tokens x 16 heads)."""
     monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
     b = workloads.small(device=DEV, num_heads=heads[0], num_kv_heads=heads[1], seed=41 + ci, **PREFILL_CASES[ci])
     err = _err()
@@ -398,9 +401,10 @@ def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, heads, monkeypatch):
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", f"prefill {kernel} case {ci}")
 
 
-def test_prefill_tc_duplicate_ids_count_once(pbs, monkeypatch):
-    """The tile kernel reads each selected block once per token, the attend's set reading."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
+@pytest.mark.parametrize("kernel", ["tc", "gather"])
+def test_prefill_tc_duplicate_ids_count_once(pbs, kernel, monkeypatch):
+    """The tcgen05 kernels read each selected block once per token, the attend's set reading."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=6, pre_q_lens=[300], pre_ctx_lens=[400],
                         seed=45)
     tk = b.pre.topk.clone()
@@ -412,8 +416,9 @@ def test_prefill_tc_duplicate_ids_count_once(pbs, monkeypatch):
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill duplicates")
 
 
-def test_prefill_tc_ignores_nan_past_last_token(pbs, monkeypatch):
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
+@pytest.mark.parametrize("kernel", ["tc", "gather"])
+def test_prefill_tc_ignores_nan_past_last_token(pbs, kernel, monkeypatch):
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, pre_q_lens=[77, 200], pre_ctx_lens=[0, 50],
                         seed=46)
     p = b.pre
@@ -480,7 +485,7 @@ def test_attend_topk_64_and_padded_topk_rows(pbs, kv_dtype, monkeypatch):
         assert_close(dict(enumerate(got)), want, kv_dtype, f"top-k 64 {part}")
 
 
-@pytest.mark.parametrize("part", ["dec", "tc", "token"])
+@pytest.mark.parametrize("part", ["dec", "tc", "token", "gather"])
 def test_attend_side_packed_blocks(pbs, part, monkeypatch):
     """block_page_stride 16 ([sparse_pa] minimax_m3_sparse_block_page_stride with packed sides):
     block b's pages are 16 b + j, j < 8; the other 8 pages of each block hold NaN and must not be
@@ -511,3 +516,26 @@ def test_attend_strided_pages(pbs):
     out = pbs.sparse_decode_attention(d.q, view, "bf16", 2, d.topk, d.page_table, d.seq_lens, 1, b.softmax_scale)
     torch.cuda.synchronize()
     assert_close(dict(enumerate(out.double().cpu().numpy())), oracle_decode(b), "bf16", "strided pages")
+
+
+def test_prefill_gather_segments_and_reuse(pbs, monkeypatch):
+    """The gathered-row kernel on a workspace that holds one 256-token segment runs the call in
+    segments; each token's partials and merge do not depend on the segment, so the output is
+    bit-identical to the one-segment run on a larger workspace, and a second call on the same
+    (now stale) workspace gives the same bits again."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "gather")
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, pre_q_lens=[700, 3, 300, 260],
+                        pre_ctx_lens=[1500, 0, 6000, 128], future_prob=0.3, seed=70)
+    p = b.pre
+    nreq, k, mb = p.seq_lens.shape[0], p.topk.shape[-1], p.page_table.shape[1]
+    small = pbs.prefill_workspace_bytes(256, nreq, 64, 8, k, mb)
+    full = pbs.prefill_workspace_bytes(p.q.shape[0], nreq, 64, 8, k, mb)
+    assert 0 < small < full
+    outs = []
+    for nbytes in (full, small, small):
+        ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)   # stale contents: all NaN
+        err = _err()
+        outs.append(gpu_attend(pbs, b, "pre", err, workspace=ws))
+        assert int(err.item()) == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    assert_close(dict(enumerate(outs[0])), oracle_prefill(b), "bf16", "gather segments")
