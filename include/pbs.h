@@ -253,7 +253,7 @@ PBS_API int pbs_sparse_prefill_attention(
 
 /*
  * Bytes of the workspace with which pbs_sparse_prefill_attention runs a call of `total_q`
- * tokens (at most 2^20 per segment) over `num_reqs` requests on its gathered-row kernel in one
+ * tokens (at most 2^19 per segment) over `num_reqs` requests on its gathered-row kernel in one
  * segment; 0 for invalid arguments. No counterpart on the pages. With total_q = 256 it is the
  * smallest workspace that kernel accepts. For Hq query heads and top-k k the size is about
  * total_q * Hq * k * 264 bytes (fp16 partial outputs and their log-sum-exp pairs) plus the

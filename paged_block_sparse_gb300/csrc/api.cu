@@ -149,6 +149,9 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
 // tokens): contexts 0 / 2k-4k / 16k-32k give 462 / 312 / 114 TFLOP/s on the tile kernel and
 // 133 / 139 / 139 on the token-centric one.
 constexpr int kTileMaxBlocksPerTopk = 8;
+// The gathered-row kernel is taken without PBS_PREFILL_KERNEL=gather only once it outruns the
+// other two on the prefill workloads.
+constexpr bool kGatherByDefault = false;
 enum PrefillKernel { kPrefillToken = 0, kPrefillTile = 1, kPrefillGather = 2 };
 
 int prefill_kernel_override() {
@@ -173,7 +176,7 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, PrefillKe
   if ((force == 2 && !tile_fits) || (force == 3 && !gather_fits)) return PBS_ERR_UNSUPPORTED;
   if (force == 1) *kernel = kPrefillToken;
   else if (force == 2) *kernel = kPrefillTile;
-  else if (force == 3 || gather_fits) *kernel = kPrefillGather;
+  else if (force == 3 || (gather_fits && kGatherByDefault)) *kernel = kPrefillGather;
   else if (tile_fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k) *kernel = kPrefillTile;
   else *kernel = kPrefillToken;
   return PBS_OK;

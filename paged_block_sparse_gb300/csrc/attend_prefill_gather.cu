@@ -29,16 +29,19 @@
 //   the chunk's Q rows (one {64 dims, G heads, 1 token} tensor copy per token and half). Warp 1
 //   (one thread) issues S(c) = Q K^T into TMEM buffer c % 2, then PV(c-1), so the softmax of
 //   chunk c overlaps PV(c-1) and S(c+1). Warps 4-7 and 8-11 are two softmax warpgroups taking
-//   chunks alternately; a thread owns one row (TMEM lane).
+//   chunks alternately; a thread owns one row (TMEM lane). Warps 2 and 3 count and merge the
+//   chunks' partials (chunks alternately), off the softmax warps' path.
 // * Softmax of one chunk (one key block): the row maximum over the block's valid keys (first
 //   pass over the S row in TMEM), then P = 2^(s * scale * log2 e - m) written back over S as bf16
 //   hi + lo (32 keys at a time into the same 32 columns), so the PV product (two MMAs, A = P from
 //   TMEM) keeps the output within 2e-3 relative RMS of the fp64 attend.
 // * Epilogue: the row's partial output O / l, scaled by a power of two so that its largest
 //   element lies in [2^14, 2^15), is stored as fp16 together with (log2-sum-exp, exponent).
-//   Each (token, kv head) counts its finished partials with an atomic ticket; the chunk that
-//   completes a token merges its partials (fp32, log-sum-exp weights), writes the bf16 output
-//   and the log-sum-exp, and drops the merged partial lines from L2 without writing them back.
+//   The stores are fenced one softmax phase later (by then they have landed), and the chunk goes
+//   to its merge warp: one atomic ticket per (token, kv head) counts the finished partials, and
+//   the chunk that completes a token merges its partials (fp32, log-sum-exp weights), writes the
+//   bf16 output and the log-sum-exp, and drops the merged partial lines from L2 without writing
+//   them back.
 // * TMEM (512 columns): S / P double buffer (2 x 128) and O double buffer (2 x 128).
 #include <algorithm>
 
@@ -53,7 +56,7 @@ namespace {
 
 constexpr int kGRows = 128;                     // MMA M: tokens x query heads of a chunk
 constexpr int kGThreads = 384;                  // 12 warps
-constexpr int kDescRing = 4;                    // chunk descriptors in flight
+constexpr int kDescRing = 8;                    // chunk descriptors in flight
 constexpr int kGQBytes = kGRows * kHeadDim * 2;  // 32 KiB Q tile
 constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of the Q tile
 constexpr int kGTile = 32768;                   // a block's K (or V) for one kv head
@@ -66,10 +69,9 @@ struct ChunkDesc {
   int32_t b;      // key block
   int32_t g;      // kv head
   int32_t ybuf;   // K/V buffer of the item
-  int32_t last;   // last chunk of the item
   int32_t n_tok;  // tokens in this chunk
   int32_t item;   // the CTA's item number (phase of the K/V buffer barriers)
-  int32_t pad;
+  int32_t pad[2];
   int32_t tr[16];    // segment-relative token index
   int32_t slot[16];  // the token's partial slot for block b
   int32_t lim[16];   // keys of block b the token sees (128, or pos - 128 b + 1 for its own block)
@@ -78,7 +80,8 @@ struct ChunkDesc {
 
 struct GCtl {
   uint64_t desc_full[kDescRing];
-  uint64_t desc_empty[kDescRing];  // 1 (MMA thread) + 4 (softmax warps) arrivals
+  uint64_t desc_empty[kDescRing];  // 1 (MMA thread) + 1 (merge warp) arrivals
+  uint64_t part_done[kDescRing];   // the chunk's partials are stored and fenced: 4 softmax warps
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[2], v_full[2], v_land[2], kv_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
@@ -86,10 +89,35 @@ struct GCtl {
   uint32_t tmem_base;
   int32_t abort;
   ChunkDesc desc[kDescRing];
+  int32_t ents[128];  // bucket entries of the producer's current batch
+};
+
+// A batch of up to 8 consecutive chunks of one window (producer).
+struct Batch {
+  int w, base, nb, r, c0, ctx0, seq_len;
 };
 
 constexpr size_t kGSmem = kGSmemBig + sizeof(GCtl) + 1024;
 static_assert(kGSmem <= 232448, "shared memory layout exceeds 227 KiB");
+
+#ifdef PBS_TRACE
+// Trace build only: one CTA records SM-clock timestamps of the first kGtChunks chunks' pipeline
+// events (producer, MMA, softmax, epilogue, merge) and the number of merges per chunk.
+constexpr int kGtChunks = 64;
+enum GTraceEv { kGtStart, kGtEnd, kGtProd = 2, kGtS = kGtProd + kGtChunks, kGtPV = kGtS + kGtChunks,
+                kGtSm0 = kGtPV + kGtChunks, kGtSm1 = kGtSm0 + kGtChunks, kGtE0 = kGtSm1 + kGtChunks,
+                kGtE1 = kGtE0 + kGtChunks, kGtM0 = kGtE1 + kGtChunks, kGtM1 = kGtM0 + kGtChunks,
+                kGtM2 = kGtM1 + kGtChunks, kGtNM = kGtM2 + kGtChunks, kGtCount = kGtNM + kGtChunks };
+__device__ long long g_gtrace[kGtCount];
+__device__ int g_gtrace_cta;
+#define GTRACE(ev, c) do { if (blockIdx.x == static_cast<unsigned>(g_gtrace_cta) && (c) < kGtChunks) \
+                             g_gtrace[(ev) + (c)] = clock64(); } while (0)
+#define GTRACE_VAL(ev, c, v) do { if (blockIdx.x == static_cast<unsigned>(g_gtrace_cta) && (c) < kGtChunks) \
+                                    g_gtrace[(ev) + (c)] = (v); } while (0)
+#else
+#define GTRACE(ev, c) do { } while (0)
+#define GTRACE_VAL(ev, c, v) do { } while (0)
+#endif
 
 __device__ __forceinline__ bool g_aborted(GCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
 
@@ -129,18 +157,6 @@ __device__ __forceinline__ void g_sts128(uint32_t addr, uint32_t a, uint32_t b, 
 // Drop a 128-byte line from L2 without writing it back (its contents become undefined).
 __device__ __forceinline__ void discard_l2(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
-__device__ __forceinline__ uint4 ldcg16(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ float2 ldcg_f2(const void* p) {
-  float2 r;
-  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(r.x), "=f"(r.y) : "l"(p));
-  return r;
 }
 
 __device__ __forceinline__ float f16_lo(uint32_t x) { return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu))); }
@@ -199,6 +215,9 @@ __device__ __forceinline__ bool find_window(const AttendArgs& a, const GatherWs&
 // index kernel: one CTA per window
 // ------------------------------------------------------------------------------------------
 // Dynamic shared memory: cnt[max_blocks], cur[max_blocks], pairs_s[kGatherWinTok * k].
+// Output per window: the chunk records in processing order (buckets by decreasing block id;
+// within a bucket kv head by kv head, 16 (or 8) tokens per chunk), the bucket entries they point
+// at, and the window record {request, first token, context, seq_len, chunks}.
 __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendArgs a, const GatherWs w) {
   extern __shared__ int32_t ish[];
   int32_t* cnt = ish;
@@ -206,9 +225,11 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   int32_t* pairs_s = cur + a.max_blocks;
   __shared__ int s_win[6];
   __shared__ int s_found, s_np, s_nblk;
-  __shared__ int s_wsum[kIdxThreads / 32], s_wnz[kIdxThreads / 32];
+  __shared__ int s_wsum[kIdxThreads / 32], s_wch[kIdxThreads / 32];
+  __shared__ int s_tn[kGatherWinTok];  // partial count of each window token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = blockIdx.x;
+  const int kTok = w.tok_per_chunk;
   int32_t* wrec = w.wins + static_cast<int64_t>(wi) * 8;
   if (warp == 0) {
     WinInfo info;
@@ -236,8 +257,6 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
     if (threadIdx.x == 0) {
       wrec[0] = -1;
       wrec[4] = 0;
-      wrec[5] = 0;
-      w.win_ctr[wi] = 0;
     }
     return;
   }
@@ -300,7 +319,7 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
         pairs_s[at] = (b1 << 14) | (tt << 6) | r1;
       }
     }
-    if (lane == 0) w.tok_n[tr] = n_t;
+    if (lane == 0) s_tn[tt] = n_t;
     for (int g = lane; g < a.num_kv_heads; g += 32) w.tickets[static_cast<int64_t>(tr) * a.num_kv_heads + g] = 0;
     if (n_t == 0) {
       // nothing to attend (no valid block, or a block past the page table): zero output
@@ -317,66 +336,72 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   }
   __syncthreads();
 
-  // ---- exclusive scan of the counts; buckets numbered by decreasing block id ----------------
+  // ---- scans of the entry counts and the chunk counts over the blocks -------------------------
   const int per = (nblk + kIdxThreads - 1) / kIdxThreads;
   const int lo = min(static_cast<int>(threadIdx.x) * per, nblk), hi = min(lo + per, nblk);
-  int s = 0, z = 0;
+  int s = 0, ch = 0;
   for (int i = lo; i < hi; ++i) {
     s += cnt[i];
-    z += cnt[i] > 0 ? 1 : 0;
+    ch += (cnt[i] + kTok - 1) / kTok;
   }
-  int is = s, iz = z;
+  int is = s, ich = ch;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int vs = __shfl_up_sync(0xffffffffu, is, off), vz = __shfl_up_sync(0xffffffffu, iz, off);
+    const int vs = __shfl_up_sync(0xffffffffu, is, off), vc = __shfl_up_sync(0xffffffffu, ich, off);
     if (lane >= off) {
       is += vs;
-      iz += vz;
+      ich += vc;
     }
   }
   if (lane == 31) {
     s_wsum[warp] = is;
-    s_wnz[warp] = iz;
+    s_wch[warp] = ich;
   }
   __syncthreads();
-  int ws = 0, wz = 0, tz = 0;
+  int ws = 0, wc = 0, tch = 0;
   for (int i = 0; i < kIdxThreads / 32; ++i) {
     if (i < warp) {
       ws += s_wsum[i];
-      wz += s_wnz[i];
+      wc += s_wch[i];
     }
-    tz += s_wnz[i];
+    tch += s_wch[i];
   }
-  int off_s = ws + is - s, off_z = wz + iz - z;  // exclusive prefixes at this thread's first block
+  int off_s = ws + is - s, off_ch = wc + ich - ch;  // exclusive prefixes at this thread's first block
   const int64_t pair_base = static_cast<int64_t>(wi) * kGatherWinTok * a.k;
-  int4* brow = w.buckets + static_cast<int64_t>(wi) * w.bcap;
+  int4* crow = w.chunks + static_cast<int64_t>(wi) * w.ccap;
+  const int hkv = a.num_kv_heads;
   for (int i = lo; i < hi; ++i) {
     const int c = cnt[i];
     cur[i] = off_s;
     if (c > 0) {
-      brow[tz - 1 - off_z] = make_int4(i, static_cast<int>(pair_base + off_s), c, 0);
-      ++off_z;
+      const int nch = (c + kTok - 1) / kTok;
+      // buckets with larger block ids come first; inside a bucket kv head by kv head
+      const int first = (tch - off_ch - nch) * hkv;
+      const int phys = __ldg(a.page_table + static_cast<int64_t>(r) * a.pt_row_stride + i);
+      for (int g = 0; g < hkv; ++g)
+        for (int sl = 0; sl < nch; ++sl)
+          crow[first + g * nch + sl] =
+              make_int4(i | (g << 13), static_cast<int>(pair_base + off_s + sl * kTok), min(kTok, c - sl * kTok), phys);
+      off_ch += nch;
     }
     off_s += c;
   }
   __syncthreads();
 
-  // ---- scatter the pairs into their buckets ---------------------------------------------------
+  // ---- scatter the entries into their buckets: token << 12 | (partials - 1) << 6 | slot -------
   const int np = s_np;
   for (int p = threadIdx.x; p < np; p += kIdxThreads) {
     const int v = pairs_s[p];
     const int b = v >> 14, tt = (v >> 6) & 255, rank = v & 63;
     const int at = atomicAdd(&cur[b], 1);
-    w.pairs[pair_base + at] = ((ta + tt - w.T0) << 6) | rank;
+    w.pairs[pair_base + at] = ((ta + tt - w.T0) << 12) | ((s_tn[tt] - 1) << 6) | rank;
   }
   if (threadIdx.x == 0) {
     wrec[0] = r;
     wrec[1] = c0;
     wrec[2] = ctx0;
     wrec[3] = s_win[5];
-    wrec[4] = tz;                     // buckets
-    wrec[5] = tz * a.num_kv_heads;    // work items
-    w.win_ctr[wi] = 0;
+    wrec[4] = tch * hkv;  // chunk records
   }
 }
 
@@ -384,28 +409,73 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
 // attend kernel: persistent, one CTA per SM
 // ------------------------------------------------------------------------------------------
 
-// Merge the partials of (segment token tr, kv head g) and write its output rows (warp-wide).
+// Merge the partials of (segment token tr, kv head g) and write its output rows (warp-wide):
+// out = v_scale * sum_j w_j O_j / sum_j w_j with w_j = 2^(lse_j - max lse). Each lane owns
+// kE dims of one head; the (lse, exponent) pairs of up to 16 partials are loaded at once and the
+// partial rows in groups, so a merge costs a few L2 round trips, not two per partial.
 template <int kG>
 __device__ __forceinline__ void merge_token(const AttendArgs& a, const GatherWs& w, int tr, int g, int nsel) {
   constexpr int kLanesPerHead = 32 / kG;        // 4 (G = 8) or 2 (G = 16)
   constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
+  constexpr int kV = kE / 8;                    // 16-byte vectors per lane per partial
+  constexpr int kGrp = kG == 8 ? 4 : 2;         // partials loaded together
   const int lane = threadIdx.x & 31;
   const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
   const int64_t base = (static_cast<int64_t>(tr) * a.num_kv_heads + g) * a.k;  // slot 0 of (tr, g)
+  const float2* mlp = w.ml + base * kG + h;
+  const uint16_t* pp = w.part + (base * kG + h) * kHeadDim + d0;
+  float mx[16], me[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float2 v = make_float2(-INFINITY, 0.f);
+    if (j < nsel) v = __ldcg(mlp + j * kG);
+    mx[j] = v.x;
+    me[j] = v.y;
+  }
   float L = -INFINITY;
-  for (int j = 0; j < nsel; ++j) L = fmaxf(L, ldcg_f2(w.ml + (base + j) * kG + h).x);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) L = fmaxf(L, mx[j]);
+  for (int j = 16; j < nsel; ++j) L = fmaxf(L, __ldcg(mlp + j * kG).x);
   float acc[kE];
 #pragma unroll
   for (int i = 0; i < kE; ++i) acc[i] = 0.f;
   float den = 0.f;
-  for (int j = 0; j < nsel; ++j) {
-    const float2 me = ldcg_f2(w.ml + (base + j) * kG + h);
-    den += ex2(me.x - L);
-    const float f = ex2(me.x - L + me.y);
-    const uint16_t* src = w.part + ((base + j) * kG + h) * kHeadDim + d0;
 #pragma unroll
-    for (int q = 0; q < kE / 8; ++q) {
-      const uint4 v = ldcg16(src + 8 * q);
+  for (int j0 = 0; j0 < 16; j0 += kGrp) {
+    if (j0 < nsel) {
+      uint4 v[kGrp][kV];
+#pragma unroll
+      for (int jj = 0; jj < kGrp; ++jj)
+#pragma unroll
+        for (int q = 0; q < kV; ++q)
+          v[jj][q] = j0 + jj < nsel ? __ldcg(reinterpret_cast<const uint4*>(pp + (j0 + jj) * kG * kHeadDim) + q)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int jj = 0; jj < kGrp; ++jj) {
+        const int j = j0 + jj;
+        const float f = j < nsel ? ex2(mx[j] - L + me[j]) : 0.f;
+        den += j < nsel ? ex2(mx[j] - L) : 0.f;
+#pragma unroll
+        for (int q = 0; q < kV; ++q) {
+          acc[8 * q + 0] = fmaf(f, f16_lo(v[jj][q].x), acc[8 * q + 0]);
+          acc[8 * q + 1] = fmaf(f, f16_hi(v[jj][q].x), acc[8 * q + 1]);
+          acc[8 * q + 2] = fmaf(f, f16_lo(v[jj][q].y), acc[8 * q + 2]);
+          acc[8 * q + 3] = fmaf(f, f16_hi(v[jj][q].y), acc[8 * q + 3]);
+          acc[8 * q + 4] = fmaf(f, f16_lo(v[jj][q].z), acc[8 * q + 4]);
+          acc[8 * q + 5] = fmaf(f, f16_hi(v[jj][q].z), acc[8 * q + 5]);
+          acc[8 * q + 6] = fmaf(f, f16_lo(v[jj][q].w), acc[8 * q + 6]);
+          acc[8 * q + 7] = fmaf(f, f16_hi(v[jj][q].w), acc[8 * q + 7]);
+        }
+      }
+    }
+  }
+  for (int j = 16; j < nsel; ++j) {
+    const float2 m2 = __ldcg(mlp + j * kG);
+    den += ex2(m2.x - L);
+    const float f = ex2(m2.x - L + m2.y);
+#pragma unroll
+    for (int q = 0; q < kV; ++q) {
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(pp + j * kG * kHeadDim) + q);
       acc[8 * q + 0] = fmaf(f, f16_lo(v.x), acc[8 * q + 0]);
       acc[8 * q + 1] = fmaf(f, f16_hi(v.x), acc[8 * q + 1]);
       acc[8 * q + 2] = fmaf(f, f16_lo(v.y), acc[8 * q + 2]);
@@ -421,7 +491,7 @@ __device__ __forceinline__ void merge_token(const AttendArgs& a, const GatherWs&
   uint16_t* dst = a.out + static_cast<int64_t>(t) * a.out_row_stride +
                   static_cast<int64_t>(g * kG + h) * a.out_head_stride + d0;
 #pragma unroll
-  for (int q = 0; q < kE / 8; ++q)
+  for (int q = 0; q < kV; ++q)
     *reinterpret_cast<uint4*>(dst + 8 * q) =
         make_uint4(pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
                    pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
@@ -430,7 +500,7 @@ __device__ __forceinline__ void merge_token(const AttendArgs& a, const GatherWs&
   // the merged partials are not read again: drop their lines (128 B = 64 dims) from L2
   __syncwarp();
   if ((d0 & 63) == 0)
-    for (int j = 0; j < nsel; ++j) discard_l2(w.part + ((base + j) * kG + h) * kHeadDim + d0);
+    for (int j = 0; j < nsel; ++j) discard_l2(pp + j * kG * kHeadDim);
 }
 
 template <int kG>
@@ -450,7 +520,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&ctl->desc_full[i], 1);
-      mbar_init(&ctl->desc_empty[i], 5);
+      mbar_init(&ctl->desc_empty[i], 2);
+      mbar_init(&ctl->part_done[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
@@ -472,98 +543,158 @@ __global__ void __launch_bounds__(kGThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
+  if (threadIdx.x == 0) GTRACE(kGtStart, 0);
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer / scheduler
+    // ---------------------------------------------------------------- producer
+    // Windows in order; CTA i takes chunks [i C / G, (i + 1) C / G) of a window with C chunks,
+    // so every window is spread over the whole grid and its partials are merged while in L2.
+    // Chunks go in batches of up to 8: the records of batch n + 2 and the bucket entries of
+    // batch n + 1 are in flight while batch n is issued.
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
     }
-    int cur_w = 0, n_item = 0, c = 0;
+    const int cta = blockIdx.x, grid = gridDim.x;
+    // window records of windows [wc0, wc0 + 32), one per lane
+    int wc0 = -64, wr_r = 0, wr_c0 = 0, wr_ctx0 = 0, wr_sl = 0, wr_C = 0;
+    int cw = 0, cbase = 0, chi = -1;  // cursor: window, next chunk of its slice, slice end (-1: not entered)
+    auto next_batch = [&](Batch& B) {
+      B.nb = 0;
+      while (cw < w.num_win) {
+        if (cw >= wc0 + 32 || cw < wc0) {
+          wc0 = cw & ~31;
+          const int wl = wc0 + lane;
+          if (wl < w.num_win) {
+            const int32_t* wrp = w.wins + static_cast<int64_t>(wl) * 8;
+            wr_r = __ldg(wrp + 0);
+            wr_c0 = __ldg(wrp + 1);
+            wr_ctx0 = __ldg(wrp + 2);
+            wr_sl = __ldg(wrp + 3);
+            wr_C = __ldg(wrp + 4);
+          } else {
+            wr_C = 0;
+          }
+        }
+        const int src = cw - wc0;
+        const int C = __shfl_sync(0xffffffffu, wr_C, src);
+        if (chi < 0) {
+          cbase = static_cast<int>(static_cast<int64_t>(cta) * C / grid);
+          chi = static_cast<int>(static_cast<int64_t>(cta + 1) * C / grid);
+        }
+        if (cbase < chi) {
+          B.w = cw;
+          B.base = cbase;
+          B.nb = min(8, chi - cbase);
+          B.r = __shfl_sync(0xffffffffu, wr_r, src);
+          B.c0 = __shfl_sync(0xffffffffu, wr_c0, src);
+          B.ctx0 = __shfl_sync(0xffffffffu, wr_ctx0, src);
+          B.seq_len = __shfl_sync(0xffffffffu, wr_sl, src);
+          cbase += B.nb;
+          return;
+        }
+        ++cw;
+        chi = -1;
+      }
+    };
+    auto load_recs = [&](const Batch& B) {
+      int4 v = make_int4(0, 0, 0, 0);
+      if (lane < B.nb) v = __ldg(w.chunks + static_cast<int64_t>(B.w) * w.ccap + B.base + lane);
+      return v;
+    };
+    // bucket entries of a batch: entry e = chunk e / kTok, token e % kTok; four per lane
+    auto load_ents = [&](const Batch& B, const int4& rec, int (&e)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int idx = lane + 32 * q;
+        const int j = idx / kTok, l = idx % kTok;
+        const int poff = __shfl_sync(0xffffffffu, rec.y, j & 7);
+        const int ntk = __shfl_sync(0xffffffffu, rec.z, j & 7);
+        e[q] = (j < B.nb && l < ntk) ? __ldg(w.pairs + poff + l) : 0;
+      }
+    };
+    int* ent_s = ctl->ents;
+    int n_item = -1, c = 0;
+    int item_r = -1, item_b = -1, item_g = -1;
     int q_n[2] = {0, 0}, k_n[2] = {0, 0}, v_n[2] = {0, 0}, land_n[2] = {0, 0};
     bool ok = true;
-    while (ok) {
-      // ---- next item: windows in order, items of a window from its counter
-      int item = -1;
-      if (lane == 0) {
-        while (cur_w < w.num_win) {
-          const int n_items = __ldg(w.wins + static_cast<int64_t>(cur_w) * 8 + 5);
-          if (n_items > 0) {
-            const int i = atomicAdd(w.win_ctr + cur_w, 1);
-            if (i < n_items) {
-              item = i;
+    Batch B0, B1, B2;
+    next_batch(B0);
+    int4 rec0 = load_recs(B0);
+    next_batch(B1);
+    int4 rec1 = load_recs(B1);
+    int e_cur[4];
+    load_ents(B0, rec0, e_cur);
+    while (ok && B0.nb > 0) {
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ent_s[lane + 32 * q] = e_cur[q];
+      __syncwarp();
+      next_batch(B2);
+      const int4 rec2 = load_recs(B2);
+      load_ents(B1, rec1, e_cur);
+      for (int jc = 0; jc < B0.nb && ok; ++jc, ++c) {
+        const int rx = __shfl_sync(0xffffffffu, rec0.x, jc);
+        const int b = rx & 8191, g = rx >> 13;
+        const int n_tok = __shfl_sync(0xffffffffu, rec0.z, jc);
+        const int phys = __shfl_sync(0xffffffffu, rec0.w, jc);
+        // ---- a new (request, block, kv head): K and V into the next buffer
+        if (B0.r != item_r || b != item_b || g != item_g) {
+          ++n_item;
+          item_r = B0.r;
+          item_b = b;
+          item_g = g;
+          const int Y = n_item & 1;
+          if (n_item >= 2) {
+            bool go = true;
+            if (lane == 0) go = g_wait(&ctl->kv_empty[Y], ((n_item >> 1) - 1) & 1, ctl, a.err_word);
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+              ok = false;
               break;
             }
           }
-          ++cur_w;
+          const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
+          if (lane == 0 && (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages))
+            set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+          const int last_rows = B0.seq_len - 1 - b * kSparseBlock + 1;  // rows of block b holding written tokens
+          const bool tail = last_rows < kSparseBlock;
+          uint64_t* vbar = tail ? &ctl->v_land[Y] : &ctl->v_full[Y];
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->k_full[Y], kGTile);
+            mbar_arrive_expect_tx(vbar, kGTile);
+          }
+          __syncwarp();
+          // out-of-range pages read as zeros (tensor-map bounds)
+          if (lane < 2 * kPagesPerBlock) {
+            const int pg = lane & 7;
+            const bool isv = lane >= kPagesPerBlock;
+            g_tma_5d((isv ? v_s : k_s) + Y * kGTile + pg * 4096, &kv_map, isv ? vbar : &ctl->k_full[Y], 0, 0,
+                     isv ? 2 : 0, 0, static_cast<int>((pbase + pg) * a.num_kv_heads + g));
+          }
+          ++k_n[Y];
+          if (tail) {
+            // rows past the request's last token may hold anything (unwritten cache rows): zero
+            // them in V before any PV reads the buffer
+            ++land_n[Y];
+            bool go = true;
+            if (lane == 0) go = g_wait(&ctl->v_land[Y], (land_n[Y] - 1) & 1, ctl, a.err_word);
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+              ok = false;
+              break;
+            }
+            const uint32_t vb = smem_u32(v_s + Y * kGTile);
+            const int first = max(last_rows, 0);
+            for (int e = lane; e < (kSparseBlock - first) * 16; e += 32) {
+              const int key = first + (e >> 4), vq = (e >> 3) & 1, chn = e & 7;
+              g_sts128(vb + (key >> 3) * 2048 + vq * 1024 + (key & 7) * 128 + chn * 16, 0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->v_full[Y]);
+          }
+          ++v_n[Y];
         }
-      }
-      item = __shfl_sync(0xffffffffu, item, 0);
-      cur_w = __shfl_sync(0xffffffffu, cur_w, 0);
-      if (item < 0) break;
-      if (g_aborted(ctl)) {
-        ok = false;
-        break;
-      }
-      const int32_t* wrec = w.wins + static_cast<int64_t>(cur_w) * 8;
-      const int r = __ldg(wrec + 0), c0 = __ldg(wrec + 1), ctx0 = __ldg(wrec + 2), seq_len = __ldg(wrec + 3);
-      const int g = item % a.num_kv_heads;
-      const int4 bk = __ldg(w.buckets + static_cast<int64_t>(cur_w) * w.bcap + item / a.num_kv_heads);
-      const int b = bk.x, poff = bk.y, pcnt = bk.z;
-      const int Y = n_item & 1;
-      // ---- K and V of block b, head g
-      if (n_item >= 2) {
-        bool go = true;
-        if (lane == 0) go = g_wait(&ctl->kv_empty[Y], ((n_item >> 1) - 1) & 1, ctl, a.err_word);
-        if (!__shfl_sync(0xffffffffu, go, 0)) {
-          ok = false;
-          break;
-        }
-      }
-      const int phys = __ldg(a.page_table + static_cast<int64_t>(r) * a.pt_row_stride + b);
-      const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
-      if (lane == 0 && (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages)) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-      const int pos_last = seq_len - 1;
-      const int last_rows = pos_last - b * kSparseBlock + 1;  // rows of block b holding written tokens
-      const bool tail = last_rows < kSparseBlock;
-      uint64_t* vbar = tail ? &ctl->v_land[Y] : &ctl->v_full[Y];
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&ctl->k_full[Y], kGTile);
-        mbar_arrive_expect_tx(vbar, kGTile);
-      }
-      __syncwarp();
-      // out-of-range pages read as zeros (tensor-map bounds)
-      if (lane < 2 * kPagesPerBlock) {
-        const int pg = lane & 7;
-        const bool isv = lane >= kPagesPerBlock;
-        g_tma_5d((isv ? v_s : k_s) + Y * kGTile + pg * 4096, &kv_map, isv ? vbar : &ctl->k_full[Y], 0, 0, isv ? 2 : 0, 0,
-                 static_cast<int>((pbase + pg) * a.num_kv_heads + g));
-      }
-      ++k_n[Y];
-      if (tail) {
-        // rows past the request's last token may hold anything (unwritten cache rows): zero
-        // them in V before any PV reads the buffer
-        ++land_n[Y];
-        bool go = true;
-        if (lane == 0) go = g_wait(&ctl->v_land[Y], (land_n[Y] - 1) & 1, ctl, a.err_word);
-        if (!__shfl_sync(0xffffffffu, go, 0)) {
-          ok = false;
-          break;
-        }
-        const uint32_t vb = smem_u32(v_s + Y * kGTile);
-        const int first = max(last_rows, 0);
-        for (int e = lane; e < (kSparseBlock - first) * 16; e += 32) {
-          const int key = first + (e >> 4), vq = (e >> 3) & 1, ch = e & 7;
-          g_sts128(vb + (key >> 3) * 2048 + vq * 1024 + (key & 7) * 128 + ch * 16, 0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->v_full[Y]);
-      }
-      ++v_n[Y];
-      // ---- the item's chunks
-      const int nch = (pcnt + kTok - 1) / kTok;
-      for (int ch = 0; ch < nch && ok; ++ch, ++c) {
+        // ---- the chunk's descriptor
         const int ds = c % kDescRing;
         if (c >= kDescRing) {
           bool go = true;
@@ -574,25 +705,23 @@ __global__ void __launch_bounds__(kGThreads, 1)
           }
         }
         ChunkDesc* d = &ctl->desc[ds];
-        const int n_tok = min(kTok, pcnt - ch * kTok);
         int t_lane = 0;
         if (lane < n_tok) {
-          const int pr = __ldg(w.pairs + poff + ch * kTok + lane);
-          const int tr = pr >> 6;
+          const int en = ent_s[jc * kTok + lane];
+          const int tr = en >> 12;
           const int t = w.T0 + tr;
-          const int pos = ctx0 + (t - c0);
+          const int pos = B0.ctx0 + (t - B0.c0);
           d->tr[lane] = tr;
-          d->slot[lane] = pr & 63;
+          d->slot[lane] = en & 63;
+          d->nsel[lane] = ((en >> 6) & 63) + 1;
           d->lim[lane] = pos / kSparseBlock == b ? pos - b * kSparseBlock + 1 : kSparseBlock;
-          d->nsel[lane] = __ldg(w.tok_n + tr);
           t_lane = t;
         }
         if (lane == 0) {
           d->end = 0;
           d->b = b;
           d->g = g;
-          d->ybuf = Y;
-          d->last = ch == nch - 1 ? 1 : 0;
+          d->ybuf = n_item & 1;
           d->n_tok = n_tok;
           d->item = n_item;
         }
@@ -617,9 +746,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
         ++q_n[qb];
         __threadfence_block();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->desc_full[ds]);
+        if (lane == 0) {
+          mbar_arrive(&ctl->desc_full[ds]);
+          GTRACE(kGtProd, c);
+        }
       }
-      ++n_item;
+      B0 = B1;
+      rec0 = rec1;
+      B1 = B2;
+      rec1 = rec2;
     }
     // ---- end marks: one for each softmax warpgroup (chunks c and c + 1)
     for (int e = 0; e < 2 && ok; ++e, ++c) {
@@ -650,13 +785,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
       constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
-      int prev_y = 0, prev_last = 0, prev_item = 0;
+      int prev_y = 0, prev_item = 0;
       for (int c = 0;; ++c) {
         const int ds = c % kDescRing;
         if (!g_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
         const ChunkDesc* d = &ctl->desc[ds];
         const int end = d->end;
-        const int Y = d->ybuf, last = d->last, item = d->item;
+        const int Y = d->ybuf, item = d->item;
         if (!end) {
           const int X = c & 1;
           // the K buffer of item n completes once per use: phase (n / 2) & 1
@@ -671,6 +806,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                        tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048), kIdescS, ks > 0);
           tc::commit(&ctl->s_full[X]);
           tc::commit(&ctl->q_empty[X]);
+          GTRACE(kGtS, c);
         }
         if (c >= 1) {
           // PV of the previous chunk: O(X') = P hi V + P lo V, P in S buffer X' (per 32-key group
@@ -690,17 +826,54 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
           }
           tc::commit(&ctl->pv_done[Xp]);
-          if (prev_last) tc::commit(&ctl->kv_empty[prev_y]);
+          GTRACE(kGtPV, cp);
+          // the previous chunk was its item's last: its K/V buffer is free once this PV completes
+          if (end || item != prev_item) tc::commit(&ctl->kv_empty[prev_y]);
           mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
         }
         if (end) break;
         prev_y = Y;
-        prev_last = last;
         prev_item = item;
       }
       // every MMA issued must complete before TMEM is released
       tc::commit(&ctl->mma_fin);
       mbar_wait_bounded(&ctl->mma_fin, 0, kGWaitNs);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ---------------------------------------------------------------- merge warps
+    // Warp 2 takes chunks 0, 2, ..., warp 3 chunks 1, 3, ...: once a chunk's partials are stored
+    // and fenced, one ticket per (token, kv head) counts them; the chunk that completes a token
+    // merges it. Then the chunk's descriptor is released.
+    const int m = warp - 2;
+    for (int c = m;; c += 2) {
+      const int ds = c % kDescRing;
+      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+      const ChunkDesc* d = &ctl->desc[ds];
+      if (d->end) break;
+      if (!g_warp_wait(&ctl->part_done[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+      if (lane == 0) GTRACE(kGtM0, c);
+      const int g = d->g, n_tok = d->n_tok;
+      const int tr = lane < n_tok ? d->tr[lane] : 0;
+      const int nsel = lane < n_tok ? d->nsel[lane] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);  // everything needed is in registers
+      __threadfence();
+      bool done = false;
+      if (lane < n_tok) done = atomicAdd(w.tickets + static_cast<int64_t>(tr) * a.num_kv_heads + g, 1) + 1 == nsel;
+      uint32_t dm = __ballot_sync(0xffffffffu, done);
+      if (lane == 0) {
+        GTRACE(kGtM1, c);
+        GTRACE_VAL(kGtNM, c, __popc(dm));
+      }
+      if (dm) {
+        __threadfence();
+        while (dm) {
+          const int src = __ffs(dm) - 1;
+          dm &= dm - 1;
+          merge_token<kG>(a, w, __shfl_sync(0xffffffffu, tr, src), g, __shfl_sync(0xffffffffu, nsel, src));
+        }
+      }
+      if (lane == 0) GTRACE(kGtM2, c);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
@@ -712,6 +885,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const uint32_t ts = tmem + X * 128 + lane_off;
     const uint32_t to = tmem + 256 + X * 128 + lane_off;
     const float sl2 = a.scale_log2;
+    int pending = -1;  // chunk whose partials are stored but not yet fenced and announced
     for (int c = X;; c += 2) {
       const int ds = c % kDescRing;
       if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
@@ -722,33 +896,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int lim = valid ? d->lim[j] : 0;
       if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
       tc::fence_after_sync();
-      // ---- pass 1: row maximum over the valid keys
+      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtSm0, c);
+      // ---- the whole S row in one TMEM round trip; row maximum over the valid keys
+      uint32_t v[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tc::ld32(ts + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * cc]));
+      tc::wait_ld();
       float mx = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tc::ld32(ts + 32 * cc, v);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float s = __uint_as_float(v[i]);
-          mx = 32 * cc + i < lim ? fmaxf(mx, s) : mx;
-        }
-      }
+      for (int i = 0; i < 128; ++i) mx = i < lim ? fmaxf(mx, __uint_as_float(v[i])) : mx;
       const float m = lim > 0 ? mx * sl2 : 0.f;
-      // ---- pass 2: P = 2^(s sl2 - m) as bf16 hi + lo over the same columns
+      // ---- P = 2^(s sl2 - m) as bf16 hi + lo, 32 keys at a time into their own 32 columns
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tc::ld32(ts + 32 * cc, v);
-        tc::wait_ld();
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const int key = 32 * cc + i;
-          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(v[i]), sl2, -m)) : 0.f;
-          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m)) : 0.f;
+          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(v[key]), sl2, -m)) : 0.f;
+          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(v[key + 1]), sl2, -m)) : 0.f;
           l0 += p0;
           l1 += p1;
           const uint32_t hh = pack_bf16(p0, p1);
@@ -763,18 +930,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->p_full[X]);
+      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtSm1, c);
+      // the previous chunk's partial stores have had a softmax phase to land: fence them now and
+      // hand that chunk to its merge warp
+      if (pending >= 0) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
+        pending = -1;
+      }
       // ---- epilogue: partial O / l as fp16 scaled by 2^-e
       if (!g_warp_wait(&ctl->pv_done[X], (c >> 1) & 1, ctl, a.err_word)) break;
       tc::fence_after_sync();
+      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtE0, c);
+      uint32_t o[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tc::ld32(to + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * cc]));
+      tc::wait_ld();
       float mo = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tc::ld32(to + 32 * cc, v);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mo = fmaxf(mo, fabsf(__uint_as_float(v[i])));
-      }
+      for (int i = 0; i < 128; ++i) mo = fmaxf(mo, fabsf(__uint_as_float(o[i])));
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       // e: the exponent that puts max |O / l| into [2^14, 2^15)
       int e = 0;
@@ -785,44 +960,25 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int tr = valid ? d->tr[j] : 0;
       const int64_t prow = ((static_cast<int64_t>(tr) * a.num_kv_heads + d->g) * a.k + (valid ? d->slot[j] : 0)) * kG + h;
       uint16_t* dst = w.part + prow * kHeadDim;
+      if (valid) {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tc::ld32(to + 32 * cc, v);
-        tc::wait_ld();
-        if (valid) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float* f = reinterpret_cast<const float*>(&v[8 * q4]);
-            *reinterpret_cast<uint4*>(dst + 32 * cc + 8 * q4) =
-                make_uint4(pack_f16(f[0] * sc, f[1] * sc), pack_f16(f[2] * sc, f[3] * sc), pack_f16(f[4] * sc, f[5] * sc),
-                           pack_f16(f[6] * sc, f[7] * sc));
-          }
+        for (int q8 = 0; q8 < 16; ++q8) {
+          const uint32_t* f = &o[8 * q8];
+          *reinterpret_cast<uint4*>(dst + 8 * q8) = make_uint4(
+              pack_f16(__uint_as_float(f[0]) * sc, __uint_as_float(f[1]) * sc),
+              pack_f16(__uint_as_float(f[2]) * sc, __uint_as_float(f[3]) * sc),
+              pack_f16(__uint_as_float(f[4]) * sc, __uint_as_float(f[5]) * sc),
+              pack_f16(__uint_as_float(f[6]) * sc, __uint_as_float(f[7]) * sc));
         }
       }
       if (valid) *reinterpret_cast<float2*>(w.ml + prow) = make_float2(m + log2f(l), static_cast<float>(e));
-      // ---- ticket per (token, kv head); the chunk that completes a token merges it
+      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtE1, c);
+      pending = c;
+    }
+    if (pending >= 0) {
       __threadfence();
       __syncwarp();
-      bool done = false;
-      int nsel = 0;
-      if (valid && h == 0) {
-        nsel = d->nsel[j];
-        const int old = atomicAdd(w.tickets + static_cast<int64_t>(tr) * a.num_kv_heads + d->g, 1);
-        done = old + 1 == nsel;
-      }
-      uint32_t dm = __ballot_sync(0xffffffffu, done);
-      const int gg = d->g;
-      if (dm) {
-        __threadfence();
-        while (dm) {
-          const int src = __ffs(dm) - 1;
-          dm &= dm - 1;
-          merge_token<kG>(a, w, __shfl_sync(0xffffffffu, tr, src), gg, __shfl_sync(0xffffffffu, nsel, src));
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);
+      if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
     }
   }
   tc::fence_before_sync();
@@ -831,9 +987,24 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc::fence_after_sync();
     tc::dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) GTRACE(kGtEnd, 0);
 }
 
 }  // namespace
+
+#ifdef PBS_TRACE
+}  // namespace pbs
+// Trace build only: choose the traced CTA, and copy the timestamps out (host buffer of
+// kGtCount int64). Not part of the C ABI.
+extern "C" __attribute__((visibility("default"))) int pbs_debug_gtrace_set(int cta) {
+  return cudaMemcpyToSymbol(pbs::g_gtrace_cta, &cta, sizeof(int)) == cudaSuccess ? 0 : 5;
+}
+extern "C" __attribute__((visibility("default"))) int pbs_debug_gtrace_get(long long* host, int n) {
+  if (n > pbs::kGtCount) n = pbs::kGtCount;
+  return cudaMemcpyFromSymbol(host, pbs::g_gtrace, sizeof(long long) * n) == cudaSuccess ? 0 : 5;
+}
+namespace pbs {
+#endif
 
 bool prefill_gather_supported(const AttendArgs& a) {
   return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
@@ -847,31 +1018,33 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct GatherLayout {
-  size_t part, ml, tok_n, tickets, pairs, buckets, wins, win_ctr, total;
-  int num_win, bcap;
+  size_t part, ml, tickets, pairs, chunks, wins, total;
+  int num_win, ccap;
 };
 
 GatherLayout gather_layout(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks) {
   GatherLayout L = {};
+  const int group = num_heads / num_kv_heads;
+  const int tok = kGRows / (group > 8 ? group : 8);
   L.num_win = static_cast<int>(seg_tokens / kGatherWinTok + 2 * static_cast<int64_t>(num_reqs) + 1);
-  L.bcap = std::min(max_blocks, kGatherWinTok * k);
+  // chunks of one kv head in a window: sum over its buckets of ceil(tokens / tok) <= (entries +
+  // buckets * (tok - 1)) / tok, with entries <= 256 k and buckets <= min(max_blocks, entries)
+  const int64_t entries = static_cast<int64_t>(kGatherWinTok) * k;
+  const int64_t buckets = std::min<int64_t>(max_blocks, entries);
+  L.ccap = static_cast<int>(((entries + buckets * (tok - 1)) / tok + 1) * num_kv_heads);
   size_t off = 0;
   L.part = off;
   off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * kHeadDim * 2);
   L.ml = off;
   off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * 8);
-  L.tok_n = off;
-  off = align256(off + static_cast<size_t>(seg_tokens) * 4);
   L.tickets = off;
   off = align256(off + static_cast<size_t>(seg_tokens) * num_kv_heads * 4);
   L.pairs = off;
   off = align256(off + static_cast<size_t>(L.num_win) * kGatherWinTok * k * 4);
-  L.buckets = off;
-  off = align256(off + static_cast<size_t>(L.num_win) * L.bcap * 16);
+  L.chunks = off;
+  off = align256(off + static_cast<size_t>(L.num_win) * L.ccap * 16);
   L.wins = off;
   off = align256(off + static_cast<size_t>(L.num_win) * 8 * 4);
-  L.win_ctr = off;
-  off = align256(off + static_cast<size_t>(L.num_win) * 4);
   L.total = off;
   return L;
 }
@@ -910,13 +1083,12 @@ cudaError_t launch_gather_g(const AttendArgs& a, const CUtensorMap& kv_map, cons
   GatherWs w = {};
   w.part = reinterpret_cast<uint16_t*>(base + L.part);
   w.ml = reinterpret_cast<float2*>(base + L.ml);
-  w.tok_n = reinterpret_cast<int32_t*>(base + L.tok_n);
   w.tickets = reinterpret_cast<int32_t*>(base + L.tickets);
   w.pairs = reinterpret_cast<int32_t*>(base + L.pairs);
-  w.buckets = reinterpret_cast<int4*>(base + L.buckets);
+  w.chunks = reinterpret_cast<int4*>(base + L.chunks);
   w.wins = reinterpret_cast<int32_t*>(base + L.wins);
-  w.win_ctr = reinterpret_cast<int32_t*>(base + L.win_ctr);
-  w.bcap = L.bcap;
+  w.ccap = L.ccap;
+  w.tok_per_chunk = kGRows / kG;
 
   const size_t idx_smem = static_cast<size_t>(2 * a.max_blocks + kGatherWinTok * a.k) * 4;
   cudaError_t e = cudaFuncSetAttribute(gather_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

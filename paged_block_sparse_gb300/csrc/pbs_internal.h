@@ -116,20 +116,19 @@ cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, co
 // in segments of at most `gather_segment_tokens` tokens, one index + one attend launch each.
 constexpr int kGatherWinTok = 256;      // tokens per window (request-relative)
 constexpr int kGatherMaxBlocks = 8192;  // page-table width the index kernel's histogram covers
-constexpr int64_t kGatherMaxSegment = int64_t(1) << 20;
+constexpr int64_t kGatherMaxSegment = int64_t(1) << 19;
 
 struct GatherWs {
   uint16_t* part;      // fp16 [seg][Hkv][k][G][128]: per-(token, block) output / l * 2^-e
   float2* ml;          // [seg][Hkv][k][G]: (log2-sum-exp of the block's logits, e)
-  int32_t* tok_n;      // [seg]: blocks the token attends (its partial count)
   int32_t* tickets;    // [seg][Hkv]: finished partials
-  int32_t* pairs;      // bucket entries: segment token << 6 | partial slot
-  int4* buckets;       // [windows][bcap]: (block, first entry, entries, 0)
-  int32_t* wins;       // [windows][8]: request, first token, context, seq_len, buckets, items
-  int32_t* win_ctr;    // [windows]: items taken
+  int32_t* pairs;      // bucket entries: segment token << 12 | (partials - 1) << 6 | partial slot
+  int4* chunks;        // [windows][ccap]: (block | kv head << 13, first entry, tokens, physical block)
+  int32_t* wins;       // [windows][8]: request, first token, context, seq_len, chunks
   int32_t T0, T1;      // segment [T0, T1) of the call's tokens
   int32_t num_win;     // windows of the segment (upper bound; surplus ones are empty)
-  int32_t bcap;
+  int32_t ccap;        // chunk records per window
+  int32_t tok_per_chunk;
 };
 
 bool prefill_gather_supported(const AttendArgs& a);
