@@ -55,14 +55,18 @@ namespace pbs {
 namespace {
 
 constexpr int kGRows = 128;                     // MMA M: tokens x query heads of a chunk
-constexpr int kGThreads = 384;                  // 12 warps
+constexpr int kGThreads = 512;                  // 16 warps
 constexpr int kDescRing = 8;                    // chunk descriptors in flight
 constexpr int kGQBytes = kGRows * kHeadDim * 2;  // 32 KiB Q tile
 constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of the Q tile
 constexpr int kGTile = 32768;                   // a block's K (or V) for one kv head
-constexpr int kGSmemBig = 2 * kGQBytes + 4 * kGTile;  // Q x 2, K x 2, V x 2 = 192 KiB
+constexpr int kRingBytes = 10240;               // merge ring of one merge warp: 5 x 2 KiB or 2 x 4 KiB
+constexpr int kMaxSlots = 5;
+constexpr int kTaskQ = 32;                      // completed tokens waiting for their merge, per merge warp
+constexpr int kGSmemBig = 2 * kGQBytes + 4 * kGTile + 2 * kRingBytes;  // Q x 2, K x 2, V x 2, 2 rings
 constexpr unsigned long long kGWaitNs = 100000000ull;  // waits here last microseconds: 100 ms cap
 constexpr int kIdxThreads = 256;
+constexpr int kGatherMaxSms = 1024;
 
 struct ChunkDesc {
   int32_t end;    // 1: no more work for this CTA
@@ -85,11 +89,26 @@ struct GCtl {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[2], v_full[2], v_land[2], kv_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
+  // chunk c's row maxima and sums are in lm[c & 3] (softmax -> epilogue). Four barriers, not
+  // two: the softmax of chunk c + 2 may finish before the epilogue of chunk c waits, while the
+  // softmax of chunk c + 4 needs PV(c + 2), which waits for that epilogue (o_free)
+  uint64_t lm_full[4];
+  uint64_t o_free[2];    // the epilogue has read O buffer X (epilogue -> MMA)
+  uint64_t v_ready[2];   // V buffer Y holds the fp16 copy (epilogue -> MMA)
+  uint64_t ring_full[2][kMaxSlots];
   uint64_t mma_fin;
   uint32_t tmem_base;
   int32_t abort;
   ChunkDesc desc[kDescRing];
   int32_t ents[128];  // bucket entries of the producer's current batch
+  alignas(16) int4 tq[2][kTaskQ];                     // merge tasks: (token, kv head, partials, 0)
+  float lm_m[4][kGRows];                               // chunk c & 3, row: softmax maximum (log2 units)
+  float lm_l[4][2][kGRows];                            // chunk c & 3, key half, row: partial sum
+  float xchg[2][2][kGRows];                            // row maxima of the two key halves
+  int32_t peek;                                        // epilogue: the next chunk's descriptor is out
+  int32_t vexp[2];                                     // V buffer Y holds V * 2^-vexp[Y] as fp16
+  float vmax[4];                                       // per-warp maxima of |V| (epilogue)
+  alignas(16) float2 ring_ml[2][kMaxSlots][16];       // (lse, exponent) of each ring slot's heads
 };
 
 // A batch of up to 8 consecutive chunks of one window (producer).
@@ -320,7 +339,12 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
       }
     }
     if (lane == 0) s_tn[tt] = n_t;
-    for (int g = lane; g < a.num_kv_heads; g += 32) w.tickets[static_cast<int64_t>(tr) * a.num_kv_heads + g] = 0;
+    for (int g = lane; g < a.num_kv_heads; g += 32) {
+      const int64_t x = static_cast<int64_t>(tr) * a.num_kv_heads + g;
+      w.tickets[x] = 0;
+      // the merge task of (token, head): ready at once when there is nothing to merge
+      w.inbox[(x % w.n_mw) * w.inbox_cap + x / w.n_mw] = make_int4(tr, g, n_t, n_t == 0 ? 1 : 0);
+    }
     if (n_t == 0) {
       // nothing to attend (no valid block, or a block past the page table): zero output
       uint16_t* orow = a.out + static_cast<int64_t>(t) * a.out_row_stride;
@@ -409,100 +433,6 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
 // attend kernel: persistent, one CTA per SM
 // ------------------------------------------------------------------------------------------
 
-// Merge the partials of (segment token tr, kv head g) and write its output rows (warp-wide):
-// out = v_scale * sum_j w_j O_j / sum_j w_j with w_j = 2^(lse_j - max lse). Each lane owns
-// kE dims of one head; the (lse, exponent) pairs of up to 16 partials are loaded at once and the
-// partial rows in groups, so a merge costs a few L2 round trips, not two per partial.
-template <int kG>
-__device__ __forceinline__ void merge_token(const AttendArgs& a, const GatherWs& w, int tr, int g, int nsel) {
-  constexpr int kLanesPerHead = 32 / kG;        // 4 (G = 8) or 2 (G = 16)
-  constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
-  constexpr int kV = kE / 8;                    // 16-byte vectors per lane per partial
-  constexpr int kGrp = kG == 8 ? 4 : 2;         // partials loaded together
-  const int lane = threadIdx.x & 31;
-  const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
-  const int64_t base = (static_cast<int64_t>(tr) * a.num_kv_heads + g) * a.k;  // slot 0 of (tr, g)
-  const float2* mlp = w.ml + base * kG + h;
-  const uint16_t* pp = w.part + (base * kG + h) * kHeadDim + d0;
-  float mx[16], me[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float2 v = make_float2(-INFINITY, 0.f);
-    if (j < nsel) v = __ldcg(mlp + j * kG);
-    mx[j] = v.x;
-    me[j] = v.y;
-  }
-  float L = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) L = fmaxf(L, mx[j]);
-  for (int j = 16; j < nsel; ++j) L = fmaxf(L, __ldcg(mlp + j * kG).x);
-  float acc[kE];
-#pragma unroll
-  for (int i = 0; i < kE; ++i) acc[i] = 0.f;
-  float den = 0.f;
-#pragma unroll
-  for (int j0 = 0; j0 < 16; j0 += kGrp) {
-    if (j0 < nsel) {
-      uint4 v[kGrp][kV];
-#pragma unroll
-      for (int jj = 0; jj < kGrp; ++jj)
-#pragma unroll
-        for (int q = 0; q < kV; ++q)
-          v[jj][q] = j0 + jj < nsel ? __ldcg(reinterpret_cast<const uint4*>(pp + (j0 + jj) * kG * kHeadDim) + q)
-                                    : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int jj = 0; jj < kGrp; ++jj) {
-        const int j = j0 + jj;
-        const float f = j < nsel ? ex2(mx[j] - L + me[j]) : 0.f;
-        den += j < nsel ? ex2(mx[j] - L) : 0.f;
-#pragma unroll
-        for (int q = 0; q < kV; ++q) {
-          acc[8 * q + 0] = fmaf(f, f16_lo(v[jj][q].x), acc[8 * q + 0]);
-          acc[8 * q + 1] = fmaf(f, f16_hi(v[jj][q].x), acc[8 * q + 1]);
-          acc[8 * q + 2] = fmaf(f, f16_lo(v[jj][q].y), acc[8 * q + 2]);
-          acc[8 * q + 3] = fmaf(f, f16_hi(v[jj][q].y), acc[8 * q + 3]);
-          acc[8 * q + 4] = fmaf(f, f16_lo(v[jj][q].z), acc[8 * q + 4]);
-          acc[8 * q + 5] = fmaf(f, f16_hi(v[jj][q].z), acc[8 * q + 5]);
-          acc[8 * q + 6] = fmaf(f, f16_lo(v[jj][q].w), acc[8 * q + 6]);
-          acc[8 * q + 7] = fmaf(f, f16_hi(v[jj][q].w), acc[8 * q + 7]);
-        }
-      }
-    }
-  }
-  for (int j = 16; j < nsel; ++j) {
-    const float2 m2 = __ldcg(mlp + j * kG);
-    den += ex2(m2.x - L);
-    const float f = ex2(m2.x - L + m2.y);
-#pragma unroll
-    for (int q = 0; q < kV; ++q) {
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(pp + j * kG * kHeadDim) + q);
-      acc[8 * q + 0] = fmaf(f, f16_lo(v.x), acc[8 * q + 0]);
-      acc[8 * q + 1] = fmaf(f, f16_hi(v.x), acc[8 * q + 1]);
-      acc[8 * q + 2] = fmaf(f, f16_lo(v.y), acc[8 * q + 2]);
-      acc[8 * q + 3] = fmaf(f, f16_hi(v.y), acc[8 * q + 3]);
-      acc[8 * q + 4] = fmaf(f, f16_lo(v.z), acc[8 * q + 4]);
-      acc[8 * q + 5] = fmaf(f, f16_hi(v.z), acc[8 * q + 5]);
-      acc[8 * q + 6] = fmaf(f, f16_lo(v.w), acc[8 * q + 6]);
-      acc[8 * q + 7] = fmaf(f, f16_hi(v.w), acc[8 * q + 7]);
-    }
-  }
-  const int t = w.T0 + tr;
-  const float inv = a.v_scale / den;
-  uint16_t* dst = a.out + static_cast<int64_t>(t) * a.out_row_stride +
-                  static_cast<int64_t>(g * kG + h) * a.out_head_stride + d0;
-#pragma unroll
-  for (int q = 0; q < kV; ++q)
-    *reinterpret_cast<uint4*>(dst + 8 * q) =
-        make_uint4(pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
-                   pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
-  if (a.lse != nullptr && (lane % kLanesPerHead) == 0)
-    a.lse[static_cast<int64_t>(t) * a.lse_row_stride + g * kG + h] = (L + log2f(den)) * kLn2;
-  // the merged partials are not read again: drop their lines (128 B = 64 dims) from L2
-  __syncwarp();
-  if ((d0 & 63) == 0)
-    for (int j = 0; j < nsel; ++j) discard_l2(pp + j * kG * kHeadDim);
-}
-
 template <int kG>
 __global__ void __launch_bounds__(kGThreads, 1)
     gather_attend_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
@@ -514,7 +444,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint8_t* q_s = big;                   // 2 x 32 KiB: [half][rows][128 B]
   uint8_t* k_s = big + 2 * kGQBytes;    // 2 x 32 KiB: [page][row half][quarter][8 rows][128 B]
   uint8_t* v_s = k_s + 2 * kGTile;      // 2 x 32 KiB
-  GCtl* ctl = reinterpret_cast<GCtl*>(v_s + 2 * kGTile);
+  uint8_t* ring_s = v_s + 2 * kGTile;    // 2 x kRingBytes: partial rows being merged
+  GCtl* ctl = reinterpret_cast<GCtl*>(ring_s + 2 * kRingBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -531,9 +462,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_init(&ctl->v_land[i], 1);
       mbar_init(&ctl->kv_empty[i], 1);
       mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->p_full[i], 4);
+      mbar_init(&ctl->p_full[i], 8);
       mbar_init(&ctl->pv_done[i], 1);
+      mbar_init(&ctl->lm_full[2 * i], 8);
+      mbar_init(&ctl->lm_full[2 * i + 1], 8);
+      mbar_init(&ctl->o_free[i], 4);
+      mbar_init(&ctl->v_ready[i], 1);
+      for (int j = 0; j < kMaxSlots; ++j) mbar_init(&ctl->ring_full[i][j], 1);
     }
+
     mbar_init(&ctl->mma_fin, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -616,7 +553,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     int* ent_s = ctl->ents;
     int n_item = -1, c = 0;
     int item_r = -1, item_b = -1, item_g = -1;
-    int q_n[2] = {0, 0}, k_n[2] = {0, 0}, v_n[2] = {0, 0}, land_n[2] = {0, 0};
+    // uses of each buffer so far (their barrier phases); scalars, so they stay in registers
+    int q_n0 = 0, q_n1 = 0, kv_n0 = 0, kv_n1 = 0, land_n0 = 0, land_n1 = 0;
     bool ok = true;
     Batch B0, B1, B2;
     next_batch(B0);
@@ -671,13 +609,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             g_tma_5d((isv ? v_s : k_s) + Y * kGTile + pg * 4096, &kv_map, isv ? vbar : &ctl->k_full[Y], 0, 0,
                      isv ? 2 : 0, 0, static_cast<int>((pbase + pg) * a.num_kv_heads + g));
           }
-          ++k_n[Y];
+          if (Y == 0) ++kv_n0; else ++kv_n1;
           if (tail) {
             // rows past the request's last token may hold anything (unwritten cache rows): zero
             // them in V before any PV reads the buffer
-            ++land_n[Y];
+            const int ln = Y == 0 ? ++land_n0 : ++land_n1;
             bool go = true;
-            if (lane == 0) go = g_wait(&ctl->v_land[Y], (land_n[Y] - 1) & 1, ctl, a.err_word);
+            if (lane == 0) go = g_wait(&ctl->v_land[Y], (ln - 1) & 1, ctl, a.err_word);
             if (!__shfl_sync(0xffffffffu, go, 0)) {
               ok = false;
               break;
@@ -692,7 +630,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->v_full[Y]);
           }
-          ++v_n[Y];
         }
         // ---- the chunk's descriptor
         const int ds = c % kDescRing;
@@ -743,7 +680,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           if (lane < 2 * kTok && j < n_tok)
             g_tma_3d(q_s + qb * kGQBytes + hf * kGHalf + j * kG * 128, &q_map, &ctl->q_full[qb], hf * 64, g * kG, tj);
         }
-        ++q_n[qb];
+        if (qb == 0) ++q_n0; else ++q_n1;
         __threadfence_block();
         __syncwarp();
         if (lane == 0) {
@@ -773,18 +710,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     // every copy issued must land before the CTA exits
     if (lane == 0) {
-      for (int i = 0; i < 2; ++i) {
-        if (q_n[i] > 0) mbar_wait_bounded(&ctl->q_full[i], (q_n[i] - 1) & 1, kGWaitNs);
-        if (k_n[i] > 0) mbar_wait_bounded(&ctl->k_full[i], (k_n[i] - 1) & 1, kGWaitNs);
-        if (v_n[i] > 0) mbar_wait_bounded(&ctl->v_full[i], (v_n[i] - 1) & 1, kGWaitNs);
-        if (land_n[i] > 0) mbar_wait_bounded(&ctl->v_land[i], (land_n[i] - 1) & 1, kGWaitNs);
-      }
+      if (q_n0 > 0) mbar_wait_bounded(&ctl->q_full[0], (q_n0 - 1) & 1, kGWaitNs);
+      if (q_n1 > 0) mbar_wait_bounded(&ctl->q_full[1], (q_n1 - 1) & 1, kGWaitNs);
+      if (kv_n0 > 0) mbar_wait_bounded(&ctl->k_full[0], (kv_n0 - 1) & 1, kGWaitNs);
+      if (kv_n1 > 0) mbar_wait_bounded(&ctl->k_full[1], (kv_n1 - 1) & 1, kGWaitNs);
+      if (kv_n0 > 0) mbar_wait_bounded(&ctl->v_full[0], (kv_n0 - 1) & 1, kGWaitNs);
+      if (kv_n1 > 0) mbar_wait_bounded(&ctl->v_full[1], (kv_n1 - 1) & 1, kGWaitNs);
+      if (land_n0 > 0) mbar_wait_bounded(&ctl->v_land[0], (land_n0 - 1) & 1, kGWaitNs);
+      if (land_n1 > 0) mbar_wait_bounded(&ctl->v_land[1], (land_n1 - 1) & 1, kGWaitNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
-      constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
+      constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, false, false, true);  // fp16 P, fp16 V
       int prev_y = 0, prev_item = 0;
       for (int c = 0;; ++c) {
         const int ds = c % kDescRing;
@@ -809,22 +748,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
           GTRACE(kGtS, c);
         }
         if (c >= 1) {
-          // PV of the previous chunk: O(X') = P hi V + P lo V, P in S buffer X' (per 32-key group
-          // i: hi words in columns 32 i .. 32 i + 15, lo words in 32 i + 16 .. 32 i + 31)
+          // PV of the previous chunk: O(X') = P V, P (fp16, two keys per column) in columns
+          // 0..63 of S buffer X', V the fp16 copy of the item's V
           const int cp = c - 1, Xp = cp & 1;
           if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) break;
-          if (!g_wait(&ctl->v_full[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
+          if (!g_wait(&ctl->v_ready[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
+          // O buffer X' was read by the epilogue of chunk cp - 2
+          if (cp >= 2 && !g_wait(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
           const uint32_t v_addr = smem_u32(v_s + prev_y * kGTile);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t pa = tmem + Xp * 128 + (ks >> 1) * 32 + part * 16 + (ks & 1) * 8;
-              tc::mma_ts(tmem + 256 + Xp * 128, pa, tc::smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), kIdescPV,
-                         !(part == 0 && ks == 0));
-            }
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ts(tmem + 256 + Xp * 128, tmem + Xp * 128 + ks * 8,
+                       tc::smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), kIdescPV, ks > 0);
           tc::commit(&ctl->pv_done[Xp]);
           GTRACE(kGtPV, cp);
           // the previous chunk was its item's last: its K/V buffer is free once this PV completes
@@ -842,137 +778,426 @@ __global__ void __launch_bounds__(kGThreads, 1)
   } else if (warp == 2 || warp == 3) {
     // ---------------------------------------------------------------- merge warps
     // Warp 2 takes chunks 0, 2, ..., warp 3 chunks 1, 3, ...: once a chunk's partials are stored
-    // and fenced, one ticket per (token, kv head) counts them; the chunk that completes a token
-    // merges it. Then the chunk's descriptor is released.
+    // and fenced it releases the descriptor and counts one ticket per (token, kv head); a token
+    // whose count reaches its partial total is queued. Queued tokens' partials (and their
+    // (lse, exponent) pairs) stream through a ring of bulk copies and are merged with a running
+    // maximum, so loads for later partials are in flight while earlier ones are summed. The loop
+    // never blocks on one event while another could make progress.
     const int m = warp - 2;
-    for (int c = m;; c += 2) {
-      const int ds = c % kDescRing;
-      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
-      const ChunkDesc* d = &ctl->desc[ds];
-      if (d->end) break;
-      if (!g_warp_wait(&ctl->part_done[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
-      if (lane == 0) GTRACE(kGtM0, c);
-      const int g = d->g, n_tok = d->n_tok;
-      const int tr = lane < n_tok ? d->tr[lane] : 0;
-      const int nsel = lane < n_tok ? d->nsel[lane] : 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);  // everything needed is in registers
-      __threadfence();
-      bool done = false;
-      if (lane < n_tok) done = atomicAdd(w.tickets + static_cast<int64_t>(tr) * a.num_kv_heads + g, 1) + 1 == nsel;
-      uint32_t dm = __ballot_sync(0xffffffffu, done);
-      if (lane == 0) {
-        GTRACE(kGtM1, c);
-        GTRACE_VAL(kGtNM, c, __popc(dm));
-      }
-      if (dm) {
-        __threadfence();
-        while (dm) {
-          const int src = __ffs(dm) - 1;
-          dm &= dm - 1;
-          merge_token<kG>(a, w, __shfl_sync(0xffffffffu, tr, src), g, __shfl_sync(0xffffffffu, nsel, src));
+    constexpr int kSlotBytes = kG * kHeadDim * 2;  // one partial of one (token, kv head)
+    constexpr int kSlots = kRingBytes / kSlotBytes;
+    static_assert(kSlots <= kMaxSlots, "ring slots");
+    constexpr int kLanesPerHead = 32 / kG;
+    constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
+    uint8_t* ring = ring_s + m * kRingBytes;
+    float2* rml = &ctl->ring_ml[m][0][0];
+    uint64_t* rfull = ctl->ring_full[m];
+    int4* tq = ctl->tq[m];
+    const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
+    const int hkv = a.num_kv_heads;
+    // this warp's inbox: the tasks x = token * Hkv + head with x % n_mw == me, in order of x
+    const int me = static_cast<int>(blockIdx.x) * 2 + m;
+    const int64_t n_x = static_cast<int64_t>(w.T1 - w.T0) * hkv;
+    const int expected = static_cast<int>(n_x / w.n_mw + (n_x % w.n_mw > me ? 1 : 0));
+    const int4* inbox = w.inbox + static_cast<int64_t>(me) * w.inbox_cap;
+    int head = 0;
+    int c = m;
+    bool end_seen = false, have_atom = false;
+    int at_old = 0, at_tr = 0, at_nsel = 0, at_g = 0, at_n = 0;
+    int tq_tail = 0;                          // tokens queued
+    int iss_task = 0, iss_j = 0, ri_iss = 0;  // next partial to load (task, slot, ring sequence)
+    int con_task = 0, con_j = 0, ri_con = 0;  // next partial to merge
+    float acc[kE];
+#pragma unroll
+    for (int i = 0; i < kE; ++i) acc[i] = 0.f;
+    float L = -INFINITY, den = 0.f;
+    unsigned long long idle_t0 = 0;
+    bool failed = false;
+    while (true) {
+      bool progress = false;
+      // (1) the next chunk, once its partials are fenced
+      if (!end_seen && !have_atom) {
+        const int ds = c % kDescRing;
+        const uint32_t ph = (c / kDescRing) & 1;
+        bool got = false;
+        if (lane == 0) got = mbar_try_wait(&ctl->desc_full[ds], ph);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        // once lane 0 has seen the phase complete, every lane waits on it (returns at once) so
+        // that each lane's reads of the descriptor are ordered after it
+        if (got) got = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->desc_full[ds], ph, kGWaitNs));
+        if (got) {
+          const ChunkDesc* d = &ctl->desc[ds];
+          if (d->end) {
+            end_seen = true;
+            progress = true;
+          } else {
+            bool pd = false;
+            if (lane == 0) pd = mbar_try_wait(&ctl->part_done[ds], ph);
+            pd = __shfl_sync(0xffffffffu, pd, 0);
+            if (pd) pd = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->part_done[ds], ph, kGWaitNs));
+            if (pd) {
+              if (lane == 0) GTRACE(kGtM0, c);
+              at_g = d->g;
+              at_n = d->n_tok;
+              at_tr = lane < at_n ? d->tr[lane] : 0;
+              at_nsel = lane < at_n ? d->nsel[lane] : 0;
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);
+              // the softmax warps fenced the partials before announcing them
+              at_old = lane < at_n ? atomicAdd(w.tickets + static_cast<int64_t>(at_tr) * hkv + at_g, 1) : -2;
+              have_atom = true;
+              c += 2;
+              progress = true;
+            }
+          }
         }
       }
-      if (lane == 0) GTRACE(kGtM2, c);
+      // (2) bulk loads of queued partials while the ring has room
+      while (ri_iss - ri_con < kSlots && iss_task < tq_tail) {
+        const int4 t = tq[iss_task % kTaskQ];
+        const int slot = ri_iss % kSlots;
+        const int64_t pidx = (static_cast<int64_t>(t.x) * hkv + t.y) * a.k + iss_j;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&rfull[slot], kSlotBytes + kG * 8);
+          bulk_load(ring + slot * kSlotBytes, w.part + pidx * kG * kHeadDim, kSlotBytes, &rfull[slot]);
+          bulk_load(rml + slot * 16, w.ml + pidx * kG, kG * 8, &rfull[slot]);
+        }
+        if (++iss_j == t.z) {
+          iss_j = 0;
+          ++iss_task;
+        }
+        ++ri_iss;
+        progress = true;
+      }
+      // (3) merge one landed partial
+      if (ri_con < ri_iss) {
+        const int slot = ri_con % kSlots;
+        bool rdy = false;
+        if (lane == 0) rdy = mbar_try_wait(&rfull[slot], (ri_con / kSlots) & 1);
+        rdy = __shfl_sync(0xffffffffu, rdy, 0);
+        if (rdy) rdy = __all_sync(0xffffffffu, mbar_wait_bounded(&rfull[slot], (ri_con / kSlots) & 1, kGWaitNs));
+        if (rdy) {
+          const float2 me = rml[slot * 16 + h];
+          if (me.x > L) {
+            const float sc = ex2(L - me.x);  // 0 while nothing is accumulated
+            den *= sc;
+#pragma unroll
+            for (int i = 0; i < kE; ++i) acc[i] *= sc;
+            L = me.x;
+          }
+          den += ex2(me.x - L);
+          const float f = ex2(me.x - L + me.y);
+          const uint32_t src = smem_u32(ring + slot * kSlotBytes + (h * kHeadDim + d0) * 2);
+#pragma unroll
+          for (int q = 0; q < kE / 8; ++q) {
+            uint32_t x0, x1, x2, x3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(src + 16 * q));
+            acc[8 * q + 0] = fmaf(f, f16_lo(x0), acc[8 * q + 0]);
+            acc[8 * q + 1] = fmaf(f, f16_hi(x0), acc[8 * q + 1]);
+            acc[8 * q + 2] = fmaf(f, f16_lo(x1), acc[8 * q + 2]);
+            acc[8 * q + 3] = fmaf(f, f16_hi(x1), acc[8 * q + 3]);
+            acc[8 * q + 4] = fmaf(f, f16_lo(x2), acc[8 * q + 4]);
+            acc[8 * q + 5] = fmaf(f, f16_hi(x2), acc[8 * q + 5]);
+            acc[8 * q + 6] = fmaf(f, f16_lo(x3), acc[8 * q + 6]);
+            acc[8 * q + 7] = fmaf(f, f16_hi(x3), acc[8 * q + 7]);
+          }
+          // the slot's generic reads precede the next bulk write into it
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          ++ri_con;
+          const int4 t = tq[con_task % kTaskQ];
+          if (++con_j == t.z) {
+            // the token is complete: output rows and log-sum-exp, then drop its partial lines
+            const int tt = w.T0 + t.x;
+            const float inv = a.v_scale / den;
+            uint16_t* dst = a.out + static_cast<int64_t>(tt) * a.out_row_stride +
+                            static_cast<int64_t>(t.y * kG + h) * a.out_head_stride + d0;
+#pragma unroll
+            for (int q = 0; q < kE / 8; ++q)
+              *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(
+                  pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                  pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+            if (a.lse != nullptr && (lane % kLanesPerHead) == 0)
+              a.lse[static_cast<int64_t>(tt) * a.lse_row_stride + t.y * kG + h] = (L + log2f(den)) * kLn2;
+            if ((d0 & 63) == 0) {
+              const uint16_t* pp = w.part + ((static_cast<int64_t>(t.x) * hkv + t.y) * a.k * kG + h) * kHeadDim + d0;
+              for (int j = 0; j < t.z; ++j) discard_l2(pp + static_cast<int64_t>(j) * kG * kHeadDim);
+            }
+#pragma unroll
+            for (int i = 0; i < kE; ++i) acc[i] = 0.f;
+            L = -INFINITY;
+            den = 0.f;
+            con_j = 0;
+            ++con_task;
+          }
+          progress = true;
+        }
+      }
+      // (4) the tickets of the last chunk taken: a token that is now complete is announced to
+      // its merge warp (the fence orders every partial the ticket counted before the flag)
+      if (have_atom) {
+        const bool done = lane < at_n && at_old + 1 == at_nsel;
+        const uint32_t dm = __ballot_sync(0xffffffffu, done);
+        if (dm) {
+          __threadfence();
+          if (done) {
+            const int64_t x = static_cast<int64_t>(at_tr) * hkv + at_g;
+            int* flag = reinterpret_cast<int*>(w.inbox + (x % w.n_mw) * w.inbox_cap + x / w.n_mw) + 3;
+            asm volatile("st.volatile.global.s32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+          }
+        }
+        if (lane == 0) GTRACE_VAL(kGtNM, c - 2, __popc(dm));
+        have_atom = false;
+        progress = true;
+      }
+      // (5) this warp's inbox: the leading run of ready tasks joins the merge queue
+      if (head < expected && tq_tail - con_task < kTaskQ) {
+        const int room = kTaskQ - (tq_tail - con_task);
+        const int p = head + lane;
+        int flag = 0;
+        if (lane < room && p < expected)
+          asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(flag) : "l"(reinterpret_cast<const int*>(inbox + p) + 3));
+        const uint32_t ready = __ballot_sync(0xffffffffu, flag != 0);
+        const int run = ready == 0xffffffffu ? 32 : __ffs(~ready) - 1;
+        if (run > 0) {
+          // acquire the partials the flags announce, for the generic and the bulk-copy proxy
+          __threadfence();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          int4 e = make_int4(0, 0, 0, 0);
+          if (lane < run) e = __ldcg(inbox + p);
+          const bool real = lane < run && e.z > 0;  // tasks with nothing to merge are dropped
+          const uint32_t rm = __ballot_sync(0xffffffffu, real);
+          if (real) tq[(tq_tail + __popc(rm & lanemask_lt())) % kTaskQ] = make_int4(e.x, e.y, e.z, 0);
+          tq_tail += __popc(rm);
+          head += run;
+          __syncwarp();
+          progress = true;
+        }
+      }
+      if (end_seen && !have_atom && head == expected && con_task == tq_tail && ri_con == ri_iss) break;
+      if (progress) {
+        idle_t0 = 0;
+      } else {
+        __nanosleep(64);
+        const unsigned long long now = global_timer_ns();
+        if (idle_t0 == 0) {
+          idle_t0 = now;
+        } else if (now - idle_t0 > kGWaitNs) {
+          failed = true;
+          break;
+        }
+      }
     }
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------------- softmax + epilogue
-    const int X = (warp - 4) >> 2;  // warpgroup: chunks X, X + 2, ...
-    const int quad = warp & 3;
+    if (failed && lane == 0) {
+      set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+      atomicExch(&ctl->abort, 1);
+    }
+    // copies still in flight (only after a give-up) must land before the CTA exits
+    if (lane == 0)
+      for (int r = ri_con; r < ri_iss; ++r) mbar_wait_bounded(&rfull[r % kSlots], (r / kSlots) & 1, kGWaitNs);
+  } else if (warp < 12) {
+    // ---------------------------------------------------------------- softmax
+    // Warps 4-11 take every chunk in turn, two warps per 32-lane TMEM quadrant: warp part p owns
+    // key columns [64 p, 64 p + 64) of its 32 rows, read from TMEM once; the two parts' row
+    // maxima meet in shared memory. P (fp16, two keys per column) goes to columns 32 p .. 32 p
+    // + 31 of the same S buffer once both parts have read their S columns.
+    const int sw = warp - 4, quad = sw & 3, part = sw >> 2;
     const int row = quad * 32 + lane;  // TMEM lane
-    const int j = row / kG, h = row % kG;
+    const int j = row / kG;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t ts = tmem + X * 128 + lane_off;
-    const uint32_t to = tmem + 256 + X * 128 + lane_off;
     const float sl2 = a.scale_log2;
-    int pending = -1;  // chunk whose partials are stored but not yet fenced and announced
-    for (int c = X;; c += 2) {
-      const int ds = c % kDescRing;
+    for (int c = 0;; ++c) {
+      const int ds = c % kDescRing, X = c & 1;
       if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
       const ChunkDesc* d = &ctl->desc[ds];
       if (d->end) break;
       const int n_tok = d->n_tok;
-      const bool valid = j < n_tok;
-      const int lim = valid ? d->lim[j] : 0;
+      const int lim = j < n_tok ? d->lim[j] : 0;
+      const int nval = min(max(lim - 64 * part, 0), 64);  // valid keys among my columns
       if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
       tc::fence_after_sync();
-      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtSm0, c);
-      // ---- the whole S row in one TMEM round trip; row maximum over the valid keys
-      uint32_t v[128];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tc::ld32(ts + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * cc]));
+      if (sw == 0 && lane == 0) GTRACE(kGtSm0, c);
+      const uint32_t ts = tmem + X * 128 + lane_off;
+      uint32_t v[64];
+      tc::ld32(ts + 64 * part, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tc::ld32(ts + 64 * part + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tc::wait_ld();
+      // every lane of the warp has all 64 of its keys valid: no per-key mask
+      const bool full = __all_sync(0xffffffffu, nval == 64);
       float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = i < lim ? fmaxf(mx, __uint_as_float(v[i])) : mx;
+        for (int i = 0; i < 64; i += 2) mx = fmaxf(mx, fmaxf(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mx = i < nval ? fmaxf(mx, __uint_as_float(v[i])) : mx;
+      }
+      ctl->xchg[c & 1][part][row] = mx;
+      // both parts have read their S columns and posted their maxima
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+      mx = fmaxf(mx, ctl->xchg[c & 1][part ^ 1][row]);
       const float m = lim > 0 ? mx * sl2 : 0.f;
-      // ---- P = 2^(s sl2 - m) as bf16 hi + lo, 32 keys at a time into their own 32 columns
       float l0 = 0.f, l1 = 0.f;
+      uint32_t pk[32];
+      if (full) {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int key = 32 * cc + i;
-          const float p0 = key < lim ? ex2(fmaf(__uint_as_float(v[key]), sl2, -m)) : 0.f;
-          const float p1 = key + 1 < lim ? ex2(fmaf(__uint_as_float(v[key + 1]), sl2, -m)) : 0.f;
+        for (int i = 0; i < 64; i += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(v[i]), sl2, -m));
+          const float p1 = ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m));
           l0 += p0;
           l1 += p1;
-          const uint32_t hh = pack_bf16(p0, p1);
-          hi[i >> 1] = hh;
-          lo[i >> 1] = pack_bf16(p0 - bf16_lo(hh), p1 - bf16_hi(hh));
+          pk[i >> 1] = pack_f16(p0, p1);
         }
-        tc::st16(ts + 32 * cc, hi);
-        tc::st16(ts + 32 * cc + 16, lo);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float p0 = i < nval ? ex2(fmaf(__uint_as_float(v[i]), sl2, -m)) : 0.f;
+          const float p1 = i + 1 < nval ? ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m)) : 0.f;
+          l0 += p0;
+          l1 += p1;
+          pk[i >> 1] = pack_f16(p0, p1);
+        }
       }
-      const float l = l0 + l1;
+      tc::st32(ts + 32 * part, pk);
+      // four slots: the epilogue of chunk c reads slot c & 3 before the MMA may issue PV(c + 2),
+      // and the softmax of chunk c + 4 runs only after that
+      if (part == 0) ctl->lm_m[c & 3][row] = m;
+      ctl->lm_l[c & 3][part][row] = l0 + l1;
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->p_full[X]);
-      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtSm1, c);
-      // the previous chunk's partial stores have had a softmax phase to land: fence them now and
-      // hand that chunk to its merge warp
-      if (pending >= 0) {
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
-        pending = -1;
+      if (lane == 0) {
+        mbar_arrive(&ctl->p_full[X]);
+        mbar_arrive(&ctl->lm_full[c & 3]);
       }
-      // ---- epilogue: partial O / l as fp16 scaled by 2^-e
-      if (!g_warp_wait(&ctl->pv_done[X], (c >> 1) & 1, ctl, a.err_word)) break;
-      tc::fence_after_sync();
-      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtE0, c);
-      uint32_t o[128];
+      if (sw == 0 && lane == 0) GTRACE(kGtSm1, c);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    // Warps 12-15 (one per TMEM lane quadrant), every chunk in order: the partial output O / l
+    // as fp16 with the item's V exponent, its (log2-sum-exp, exponent), then (a softmax phase
+    // later) the fence that hands the chunk to its merge warp. Before a chunk whose successor
+    // starts a new item, the next item's V is converted to fp16: V * 2^-e with e chosen so
+    // that max |V| lands in [2^14, 2^15) (the result is exact: 8 significant bits, 29 binades).
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int j = row / kG, h = row % kG;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int et = threadIdx.x - 384;  // 0..127
+    int conv_item = -1;  // last item whose V is converted
+    int pending = -1;
+    // converts the V of the item in descriptor `dn` (all 128 threads)
+    auto convert_v = [&](const ChunkDesc* dn) -> bool {
+      const int Yn = dn->ybuf, itn = dn->item;
+      if (!g_warp_wait(&ctl->v_full[Yn], (itn >> 1) & 1, ctl, a.err_word)) return false;
+      const uint32_t vb = smem_u32(v_s + Yn * kGTile);
+      // 32 KiB = 2048 x 16 B: thread et takes vectors et, et + 128, ...
+      uint32_t mxv = 0;
+#pragma unroll 4
+      for (int q = 0; q < 16; ++q) {
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                     : "r"(vb + (et + 128 * q) * 16));
+        // |bf16| as 16-bit integers compare like the values (NaN aside)
+        mxv = max(mxv, max(max(x0 & 0x7fff7fffu, x1 & 0x7fff7fffu), max(x2 & 0x7fff7fffu, x3 & 0x7fff7fffu)) >> 16);
+        mxv = max(mxv, max(max(x0 & 0x7fffu, x1 & 0x7fffu), max(x2 & 0x7fffu, x3 & 0x7fffu)));
+      }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tc::ld32(to + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * cc]));
-      tc::wait_ld();
-      float mo = 0.f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) mo = fmaxf(mo, fabsf(__uint_as_float(o[i])));
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      // e: the exponent that puts max |O / l| into [2^14, 2^15)
+      for (int off = 16; off > 0; off >>= 1) mxv = max(mxv, __shfl_xor_sync(0xffffffffu, mxv, off));
+      if (lane == 0) ctl->vmax[quad] = __uint_as_float(mxv << 16);
+      asm volatile("bar.sync 9, 128;" ::: "memory");
+      const float vm = fmaxf(fmaxf(ctl->vmax[0], ctl->vmax[1]), fmaxf(ctl->vmax[2], ctl->vmax[3]));
       int e = 0;
-      const float mn = mo * inv_l;
-      if (mn > 0.f) e = static_cast<int>((__float_as_uint(mn) >> 23) & 0xffu) - 127 - 14;
+      if (vm > 0.f) e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 127 - 14;
       e = max(-100, min(100, e));
-      const float sc = inv_l * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll 4
+      for (int q = 0; q < 16; ++q) {
+        const uint32_t ad = vb + (et + 128 * q) * 16;
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(ad));
+        g_sts128(ad, pack_f16(bf16_lo(x0) * sc, bf16_hi(x0) * sc), pack_f16(bf16_lo(x1) * sc, bf16_hi(x1) * sc),
+                 pack_f16(bf16_lo(x2) * sc, bf16_hi(x2) * sc), pack_f16(bf16_lo(x3) * sc, bf16_hi(x3) * sc));
+      }
+      // the tensor core reads the copy through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (et == 0) ctl->vexp[Yn] = e;
+      asm volatile("bar.sync 9, 128;" ::: "memory");
+      if (et == 0) mbar_arrive(&ctl->v_ready[Yn]);
+      conv_item = itn;
+      return true;
+    };
+    bool ok = true;
+    for (int c = 0; ok; ++c) {
+      const int ds = c % kDescRing, X = c & 1;
+      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+      const ChunkDesc* d = &ctl->desc[ds];
+      if (d->end) break;
+      if (d->item != conv_item && !convert_v(d)) break;
+      // the next chunk's item, if it is a new one, gets its V converted before this chunk's PV
+      // is awaited, so the MMA does not wait for the conversion (one thread looks, all follow)
+      {
+        const int dn_s = (c + 1) % kDescRing;
+        const uint32_t dn_ph = ((c + 1) / kDescRing) & 1;
+        if (et == 0) ctl->peek = mbar_try_wait(&ctl->desc_full[dn_s], dn_ph) ? 1 : 0;
+        asm volatile("bar.sync 10, 128;" ::: "memory");
+        const bool nx = ctl->peek != 0;
+        asm volatile("bar.sync 10, 128;" ::: "memory");  // every thread has read peek
+        if (nx) {
+          if (!g_warp_wait(&ctl->desc_full[dn_s], dn_ph, ctl, a.err_word)) break;
+          const ChunkDesc* dn = &ctl->desc[dn_s];
+          if (!dn->end && dn->item != conv_item && !convert_v(dn)) break;
+        }
+      }
+      if (!g_warp_wait(&ctl->pv_done[X], (c >> 1) & 1, ctl, a.err_word)) break;
+      if (!g_warp_wait(&ctl->lm_full[c & 3], (c >> 2) & 1, ctl, a.err_word)) break;
+      tc::fence_after_sync();
+      if (threadIdx.x == 384) GTRACE(kGtE0, c);
+      const float2 ml = make_float2(ctl->lm_m[c & 3][row], ctl->lm_l[c & 3][0][row] + ctl->lm_l[c & 3][1][row]);
+      const bool valid = j < d->n_tok;
+      const float inv_l = ml.y > 0.f ? 1.f / ml.y : 0.f;
       const int tr = valid ? d->tr[j] : 0;
       const int64_t prow = ((static_cast<int64_t>(tr) * a.num_kv_heads + d->g) * a.k + (valid ? d->slot[j] : 0)) * kG + h;
       uint16_t* dst = w.part + prow * kHeadDim;
-      if (valid) {
+      const uint32_t to = tmem + 256 + X * 128 + lane_off;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t o[64];
+        tc::ld32(to + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tc::ld32(to + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tc::wait_ld();
+        if (hf == 1) {
+          // O buffer X is read: PV(c + 2) may overwrite it
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->o_free[X]);
+          // the previous chunk's partial stores, issued an iteration ago, are fenced before this
+          // chunk's stores start (a fence waits for every store the thread has issued), and that
+          // chunk goes to its merge warp
+          if (pending >= 0) {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
+            pending = -1;
+          }
+        }
+        if (valid) {
 #pragma unroll
-        for (int q8 = 0; q8 < 16; ++q8) {
-          const uint32_t* f = &o[8 * q8];
-          *reinterpret_cast<uint4*>(dst + 8 * q8) = make_uint4(
-              pack_f16(__uint_as_float(f[0]) * sc, __uint_as_float(f[1]) * sc),
-              pack_f16(__uint_as_float(f[2]) * sc, __uint_as_float(f[3]) * sc),
-              pack_f16(__uint_as_float(f[4]) * sc, __uint_as_float(f[5]) * sc),
-              pack_f16(__uint_as_float(f[6]) * sc, __uint_as_float(f[7]) * sc));
+          for (int q8 = 0; q8 < 8; ++q8) {
+            const uint32_t* f = &o[8 * q8];
+            *reinterpret_cast<uint4*>(dst + 64 * hf + 8 * q8) = make_uint4(
+                pack_f16(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l),
+                pack_f16(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l),
+                pack_f16(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l),
+                pack_f16(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l));
+          }
         }
       }
-      if (valid) *reinterpret_cast<float2*>(w.ml + prow) = make_float2(m + log2f(l), static_cast<float>(e));
-      if (threadIdx.x == 128 + 128 * X) GTRACE(kGtE1, c);
+      if (valid)
+        *reinterpret_cast<float2*>(w.ml + prow) = make_float2(ml.x + log2f(ml.y), static_cast<float>(ctl->vexp[d->ybuf]));
+      if (threadIdx.x == 384) GTRACE(kGtE1, c);
       pending = c;
     }
     if (pending >= 0) {
@@ -1018,7 +1243,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct GatherLayout {
-  size_t part, ml, tickets, pairs, chunks, wins, total;
+  size_t part, ml, tickets, pairs, chunks, wins, inbox, total;
   int num_win, ccap;
 };
 
@@ -1045,6 +1270,9 @@ GatherLayout gather_layout(int64_t seg_tokens, int num_reqs, int num_heads, int 
   off = align256(off + static_cast<size_t>(L.num_win) * L.ccap * 16);
   L.wins = off;
   off = align256(off + static_cast<size_t>(L.num_win) * 8 * 4);
+  // merge tasks: one per (token, kv head), plus one task of rounding per merge warp
+  L.inbox = off;
+  off = align256(off + (static_cast<size_t>(seg_tokens) * num_kv_heads + 2 * kGatherMaxSms) * 16);
   L.total = off;
   return L;
 }
@@ -1089,6 +1317,7 @@ cudaError_t launch_gather_g(const AttendArgs& a, const CUtensorMap& kv_map, cons
   w.wins = reinterpret_cast<int32_t*>(base + L.wins);
   w.ccap = L.ccap;
   w.tok_per_chunk = kGRows / kG;
+  w.inbox = reinterpret_cast<int4*>(base + L.inbox);
 
   const size_t idx_smem = static_cast<size_t>(2 * a.max_blocks + kGatherWinTok * a.k) * 4;
   cudaError_t e = cudaFuncSetAttribute(gather_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1100,15 +1329,29 @@ cudaError_t launch_gather_g(const AttendArgs& a, const CUtensorMap& kv_map, cons
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  sms = std::min(sms, kGatherMaxSms);
+  // merge warps wait for tasks other CTAs announce, so every CTA must be resident: a
+  // cooperative launch of one CTA per SM guarantees that
+  w.n_mw = 2 * sms;
   for (int64_t t0 = 0; t0 < a.num_rows; t0 += seg) {
     w.T0 = static_cast<int32_t>(t0);
     w.T1 = static_cast<int32_t>(std::min<int64_t>(a.num_rows, t0 + seg));
     w.num_win = static_cast<int32_t>((w.T1 - w.T0) / kGatherWinTok + 2 * static_cast<int64_t>(a.num_reqs) + 1);
+    w.inbox_cap = static_cast<int32_t>((static_cast<int64_t>(w.T1 - w.T0) * a.num_kv_heads + w.n_mw - 1) / w.n_mw);
     gather_index_kernel<<<w.num_win, kIdxThreads, idx_smem, stream>>>(a, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    gather_attend_kernel<kG><<<sms, kGThreads, kGSmem, stream>>>(kv_map, q_map, a, w);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kGSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gather_attend_kernel<kG>, kv_map, q_map, a, w);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -124,6 +124,10 @@ struct GatherWs {
   int32_t* tickets;    // [seg][Hkv]: finished partials
   int32_t* pairs;      // bucket entries: segment token << 12 | (partials - 1) << 6 | partial slot
   int4* chunks;        // [windows][ccap]: (block | kv head << 13, first entry, tokens, physical block)
+  int4* inbox;         // merge tasks: (token, kv head, partials, ready) of x = token * Hkv + head at
+                       // [x % n_mw][x / n_mw]: merge warp x % n_mw merges it
+  int32_t n_mw;        // merge warps of the attend grid
+  int32_t inbox_cap;   // tasks per merge warp
   int32_t* wins;       // [windows][8]: request, first token, context, seq_len, chunks
   int32_t T0, T1;      // segment [T0, T1) of the call's tokens
   int32_t num_win;     // windows of the segment (upper bound; surplus ones are empty)
