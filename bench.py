@@ -154,7 +154,10 @@ def recorded_traffic(profile_name: str, src_hash: str):
     for line in open(p):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            rec[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            if v.startswith("`") and "`" in v[1:]:
+                v = v[1:v.index("`", 1)]  # the backticked value; anything after it is a comment
+            rec[k.strip()] = v
     if rec.get("kernel_source_sha256_16") != src_hash:
         return None
     try:
@@ -235,14 +238,14 @@ def run_decode(pbs, b, steps, warmup, flush, stream):
     return time_steps(step, steps, warmup, flush, stream)
 
 
-def run_prefill(pbs, b, steps, warmup, flush, stream):
+def run_prefill(pbs, b, steps, warmup, flush, stream, workspace=None):
     p = b.pre
     out = torch.empty_like(p.q)
 
     def step():
         pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
                                      p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
-                                     b.block_page_stride, out=out, stream=stream)
+                                     b.block_page_stride, out=out, stream=stream, workspace=workspace)
     return time_steps(step, steps, warmup, flush, stream)
 
 
@@ -316,6 +319,19 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     t = statistics.median(ts)
     res["prefill_varlen_bf16"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                   "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16, "algorithmic_tflop": fl / 1e12}
+    # the same call on the gathered-row kernel (opt-in; 2 GiB workspace, three token segments)
+    os.environ["PBS_PREFILL_KERNEL"] = "gather"
+    try:
+        ws = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, b.topk,
+                                   p.page_table.shape[1], "cuda", stream)
+        t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=ws))
+        res["prefill_varlen_bf16_gathered_rows"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
+                                                    "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
+                                                    "workspace_bytes": ws.numel()}
+        del ws
+    finally:
+        del os.environ["PBS_PREFILL_KERNEL"]
+    pbs._prefill_workspaces.clear()
     del b, p, sbt, ctxb
     torch.cuda.empty_cache()
     # the same prompts with GQA 16 (tile = 8 tokens x 16 heads)

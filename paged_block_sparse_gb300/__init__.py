@@ -359,14 +359,14 @@ def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: in
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                              block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                             workspace="auto", lse=None, return_lse: bool = False):
+                             workspace=None, lse=None, return_lse: bool = False):
     """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
 
-    ``workspace``: "auto" (the default: a cached per-stream buffer from :func:`prefill_workspace`,
-    with which bf16 caches run on the gathered-row kernel), None (no workspace: the tcgen05 tile
-    kernel or the token-centric kernel) or a uint8 CUDA tensor (see ``pbs_sparse_prefill_attention``
-    in include/pbs.h for how each kernel uses it). ``lse`` and ``return_lse`` as in
-    :func:`sparse_decode_attention`."""
+    ``workspace``: None (the default: the tcgen05 tile kernel or the token-centric kernel, no
+    scratch), "auto" (a cached per-stream buffer from :func:`prefill_workspace`, which the
+    gathered-row kernel needs; that kernel runs when PBS_PREFILL_KERNEL=gather) or a uint8 CUDA
+    tensor (see ``pbs_sparse_prefill_attention`` in include/pbs.h for how each kernel uses it).
+    ``lse`` and ``return_lse`` as in :func:`sparse_decode_attention`."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)

@@ -53,10 +53,11 @@ def _decode_parity(pbs, b, nrows, seed):
     return assert_close(got, want, b.kv_dtype, b.name)
 
 
-def _prefill_parity(pbs, b, nrows, seed):
+def _prefill_parity(pbs, b, nrows, seed, workspace=None):
     p = b.pre
     out = pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
-                                       p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale)
+                                       p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
+                                       workspace=workspace)
     torch.cuda.synchronize()
     rows = _sample(p.q.shape[0], nrows, seed)
     want = oracle_prefill(b, rows=rows)
@@ -74,6 +75,14 @@ def test_prefill_varlen_bf16(pbs):
     b = workloads.prefill(device="cuda")
     _check_tables(pbs, b)
     _prefill_parity(pbs, b, 48, 2)
+
+
+def test_prefill_varlen_bf16_gathered(pbs, monkeypatch):
+    """The gathered-row prefill kernel at full size (several token segments on the default
+    2 GiB workspace), sampled rows against the oracle."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "gather")
+    b = workloads.prefill(device="cuda")
+    _prefill_parity(pbs, b, 48, 6, workspace="auto")
 
 
 def test_mtp_fp8(pbs):

@@ -58,6 +58,8 @@ def gpu_attend(pbs, b, part, err=None, workspace="default"):
     """The binding's call for one part; workspace "default" leaves the binding's own default
     (decode: none, prefill: the cached workspace of the gathered-row kernel)."""
     ws = {} if isinstance(workspace, str) and workspace == "default" else {"workspace": workspace}
+    if part != "dec" and not ws and os.environ.get("PBS_PREFILL_KERNEL") == "gather":
+        ws = {"workspace": "auto"}  # the gathered-row kernel runs on a caller workspace
     if part == "dec":
         d = b.dec
         out = pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table,
@@ -280,7 +282,8 @@ def test_attend_lse_prefill(pbs, kernel, heads, monkeypatch):
                         pre_ctx_lens=[0, 700, 3000], future_prob=0.3, seed=61)
     p = b.pre
     out, lse = pbs.sparse_prefill_attention(p.q, b.cache, "bf16", b.num_kv_heads, p.topk, p.page_table,
-                                            p.cu_seqlens_q, p.seq_lens, b.softmax_scale, return_lse=True)
+                                            p.cu_seqlens_q, p.seq_lens, b.softmax_scale, return_lse=True,
+                                            workspace="auto" if kernel == "gather" else None)
     torch.cuda.synchronize()
     _check_lse(lse, _oracle_lse(b, "pre"), f"prefill lse {kernel} {heads}")
 
