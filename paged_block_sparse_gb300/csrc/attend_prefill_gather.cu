@@ -55,7 +55,7 @@ namespace pbs {
 namespace {
 
 constexpr int kGRows = 128;                     // MMA M: tokens x query heads of a chunk
-constexpr int kGThreads = 512;                  // 16 warps
+constexpr int kGThreads = 384;                  // 12 warps
 constexpr int kDescRing = 8;                    // chunk descriptors in flight
 constexpr int kGQBytes = kGRows * kHeadDim * 2;  // 32 KiB Q tile
 constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of the Q tile
@@ -89,12 +89,11 @@ struct GCtl {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[2], v_full[2], v_land[2], kv_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  // chunk c's row maxima and sums are in lm[c & 3] (softmax -> epilogue). Four barriers, not
-  // two: the softmax of chunk c + 2 may finish before the epilogue of chunk c waits, while the
-  // softmax of chunk c + 4 needs PV(c + 2), which waits for that epilogue (o_free)
-  uint64_t lm_full[4];
-  uint64_t o_free[2];    // the epilogue has read O buffer X (epilogue -> MMA)
-  uint64_t v_ready[2];   // V buffer Y holds the fp16 copy (epilogue -> MMA)
+  uint64_t o_free[2];    // O buffer X has been read (softmax warps -> MMA)
+  // item n's V is in fp16 (merge warp n % 2 -> MMA and softmax warps), one barrier per n % 4:
+  // item n + 4 needs the K/V buffer of item n + 2, freed only after every PV of item n + 2,
+  // which comes after the epilogues of item n
+  uint64_t vx_ready[4];
   uint64_t ring_full[2][kMaxSlots];
   uint64_t mma_fin;
   uint32_t tmem_base;
@@ -102,12 +101,10 @@ struct GCtl {
   ChunkDesc desc[kDescRing];
   int32_t ents[128];  // bucket entries of the producer's current batch
   alignas(16) int4 tq[2][kTaskQ];                     // merge tasks: (token, kv head, partials, 0)
-  float lm_m[4][kGRows];                               // chunk c & 3, row: softmax maximum (log2 units)
-  float lm_l[4][2][kGRows];                            // chunk c & 3, key half, row: partial sum
+  float lsum[4][2][kGRows];                             // chunk c & 3, key half, row: partial sum
   float xchg[2][2][kGRows];                            // row maxima of the two key halves
-  int32_t peek;                                        // epilogue: the next chunk's descriptor is out
-  int32_t vexp[2];                                     // V buffer Y holds V * 2^-vexp[Y] as fp16
-  float vmax[4];                                       // per-warp maxima of |V| (epilogue)
+  int32_t vexp[4];                                     // item n's V buffer holds V * 2^-vexp[n % 4]
+  int32_t items_total;                                 // items of this CTA (written before the end)
   alignas(16) float2 ring_ml[2][kMaxSlots][16];       // (lse, exponent) of each ring slot's heads
 };
 
@@ -452,7 +449,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&ctl->desc_full[i], 1);
       mbar_init(&ctl->desc_empty[i], 2);
-      mbar_init(&ctl->part_done[i], 4);
+      mbar_init(&ctl->part_done[i], 8);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
@@ -464,10 +461,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->p_full[i], 8);
       mbar_init(&ctl->pv_done[i], 1);
-      mbar_init(&ctl->lm_full[2 * i], 8);
-      mbar_init(&ctl->lm_full[2 * i + 1], 8);
-      mbar_init(&ctl->o_free[i], 4);
-      mbar_init(&ctl->v_ready[i], 1);
+      mbar_init(&ctl->o_free[i], 8);
+      mbar_init(&ctl->vx_ready[2 * i], 1);
+      mbar_init(&ctl->vx_ready[2 * i + 1], 1);
       for (int j = 0; j < kMaxSlots; ++j) mbar_init(&ctl->ring_full[i][j], 1);
     }
 
@@ -693,7 +689,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
       B1 = B2;
       rec1 = rec2;
     }
-    // ---- end marks: one for each softmax warpgroup (chunks c and c + 1)
+    // ---- end marks: chunks c and c + 1 (each merge warp takes every other chunk)
+    if (lane == 0) ctl->items_total = n_item + 1;
     for (int e = 0; e < 2 && ok; ++e, ++c) {
       const int ds = c % kDescRing;
       if (c >= kDescRing) {
@@ -752,7 +749,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           // 0..63 of S buffer X', V the fp16 copy of the item's V
           const int cp = c - 1, Xp = cp & 1;
           if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) break;
-          if (!g_wait(&ctl->v_ready[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
+          if (!g_wait(&ctl->vx_ready[prev_item & 3], (prev_item >> 2) & 1, ctl, a.err_word)) break;
           // O buffer X' was read by the epilogue of chunk cp - 2
           if (cp >= 2 && !g_wait(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
@@ -801,6 +798,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int expected = static_cast<int>(n_x / w.n_mw + (n_x % w.n_mw > me ? 1 : 0));
     const int4* inbox = w.inbox + static_cast<int64_t>(me) * w.inbox_cap;
     int head = 0;
+    int conv_n = m;  // next item whose V this warp converts (items m, m + 2, ... use V buffer m)
     int c = m;
     bool end_seen = false, have_atom = false;
     int at_old = 0, at_tr = 0, at_nsel = 0, at_g = 0, at_n = 0;
@@ -815,8 +813,68 @@ __global__ void __launch_bounds__(kGThreads, 1)
     bool failed = false;
     while (true) {
       bool progress = false;
+      // (0) the V of this warp's next item, once it has landed: converted in place to fp16 as
+      // V * 2^-e, e putting max |V| at 2^14..2^15 (exact: bf16 has 8 significant bits, fp16 keeps
+      // 29 binades below that maximum), for the single fp16 PV MMA
+      {
+        bool landed = false;
+        if (lane == 0) landed = mbar_try_wait(&ctl->v_full[m], (conv_n >> 1) & 1);
+        landed = __shfl_sync(0xffffffffu, landed, 0);
+        if (landed) landed = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->v_full[m], (conv_n >> 1) & 1, kGWaitNs));
+        if (landed) {
+          const uint32_t vb = smem_u32(v_s + m * kGTile);
+          uint32_t mxv = 0;
+#pragma unroll 8
+          for (int q = 0; q < kGTile / 16 / 32; ++q) {
+            uint32_t x0, x1, x2, x3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(vb + (lane + 32 * q) * 16));
+            // |bf16| bit patterns compare like the magnitudes
+            mxv = max(mxv, max(max(x0 & 0x7fff7fffu, x1 & 0x7fff7fffu), max(x2 & 0x7fff7fffu, x3 & 0x7fff7fffu)) >> 16);
+            mxv = max(mxv, max(max(x0 & 0x7fffu, x1 & 0x7fffu), max(x2 & 0x7fffu, x3 & 0x7fffu)));
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mxv = max(mxv, __shfl_xor_sync(0xffffffffu, mxv, off));
+          const float vm = __uint_as_float(mxv << 16);
+          int e = 0;
+          if (vm > 0.f) e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 127 - 14;
+          e = max(-100, min(100, e));
+          const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll 8
+          for (int q = 0; q < kGTile / 16 / 32; ++q) {
+            const uint32_t ad = vb + (lane + 32 * q) * 16;
+            uint32_t x0, x1, x2, x3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(ad));
+            g_sts128(ad, pack_f16(bf16_lo(x0) * sc, bf16_hi(x0) * sc), pack_f16(bf16_lo(x1) * sc, bf16_hi(x1) * sc),
+                     pack_f16(bf16_lo(x2) * sc, bf16_hi(x2) * sc), pack_f16(bf16_lo(x3) * sc, bf16_hi(x3) * sc));
+          }
+          // the tensor core reads the copy through the async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          if (lane == 0) ctl->vexp[conv_n & 3] = e;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->vx_ready[conv_n & 3]);
+          conv_n += 2;
+          progress = true;
+        }
+      }
+      // the tickets of the last chunk taken (their atomics were issued one step earlier, so the
+      // round trip is mostly over): a token that is now complete is announced to its merge warp
+      // (the fence orders every partial the ticket counted before the flag)
+      auto resolve_tickets = [&]() {
+        const bool done = lane < at_n && at_old + 1 == at_nsel;
+        const uint32_t dm = __ballot_sync(0xffffffffu, done);
+        if (dm) {
+          __threadfence();
+          if (done) {
+            const int64_t x = static_cast<int64_t>(at_tr) * hkv + at_g;
+            int* flag = reinterpret_cast<int*>(w.inbox + (x % w.n_mw) * w.inbox_cap + x / w.n_mw) + 3;
+            asm volatile("st.volatile.global.s32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+          }
+        }
+        have_atom = false;
+      };
       // (1) the next chunk, once its partials are fenced
-      if (!end_seen && !have_atom) {
+      if (!end_seen) {
         const int ds = c % kDescRing;
         const uint32_t ph = (c / kDescRing) & 1;
         bool got = false;
@@ -836,6 +894,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             pd = __shfl_sync(0xffffffffu, pd, 0);
             if (pd) pd = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->part_done[ds], ph, kGWaitNs));
             if (pd) {
+              if (have_atom) resolve_tickets();
               if (lane == 0) GTRACE(kGtM0, c);
               at_g = d->g;
               at_n = d->n_tok;
@@ -851,6 +910,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
           }
         }
+      }
+      if (end_seen && have_atom) {
+        resolve_tickets();
+        progress = true;
       }
       // (2) bulk loads of queued partials while the ring has room
       while (ri_iss - ri_con < kSlots && iss_task < tq_tail) {
@@ -869,8 +932,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         ++ri_iss;
         progress = true;
       }
-      // (3) merge one landed partial
-      if (ri_con < ri_iss) {
+      // (3) merge every landed partial
+      while (ri_con < ri_iss) {
         const int slot = ri_con % kSlots;
         bool rdy = false;
         if (lane == 0) rdy = mbar_try_wait(&rfull[slot], (ri_con / kSlots) & 1);
@@ -933,27 +996,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
             ++con_task;
           }
           progress = true;
+        } else {
+          break;
         }
-      }
-      // (4) the tickets of the last chunk taken: a token that is now complete is announced to
-      // its merge warp (the fence orders every partial the ticket counted before the flag)
-      if (have_atom) {
-        const bool done = lane < at_n && at_old + 1 == at_nsel;
-        const uint32_t dm = __ballot_sync(0xffffffffu, done);
-        if (dm) {
-          __threadfence();
-          if (done) {
-            const int64_t x = static_cast<int64_t>(at_tr) * hkv + at_g;
-            int* flag = reinterpret_cast<int*>(w.inbox + (x % w.n_mw) * w.inbox_cap + x / w.n_mw) + 3;
-            asm volatile("st.volatile.global.s32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
-          }
-        }
-        if (lane == 0) GTRACE_VAL(kGtNM, c - 2, __popc(dm));
-        have_atom = false;
-        progress = true;
       }
       // (5) this warp's inbox: the leading run of ready tasks joins the merge queue
-      if (head < expected && tq_tail - con_task < kTaskQ) {
+      if (head < expected && tq_tail - con_task < 4) {
         const int room = kTaskQ - (tq_tail - con_task);
         const int p = head + lane;
         int flag = 0;
@@ -976,7 +1024,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
           progress = true;
         }
       }
-      if (end_seen && !have_atom && head == expected && con_task == tq_tail && ri_con == ri_iss) break;
+      if (end_seen && !have_atom && head == expected && con_task == tq_tail && ri_con == ri_iss &&
+          conv_n >= *reinterpret_cast<volatile int32_t*>(&ctl->items_total))
+        break;
       if (progress) {
         idle_t0 = 0;
       } else {
@@ -997,208 +1047,140 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // copies still in flight (only after a give-up) must land before the CTA exits
     if (lane == 0)
       for (int r = ri_con; r < ri_iss; ++r) mbar_wait_bounded(&rfull[r % kSlots], (r / kSlots) & 1, kGWaitNs);
-  } else if (warp < 12) {
-    // ---------------------------------------------------------------- softmax
+  } else {
+    // ---------------------------------------------------------------- softmax + epilogue
     // Warps 4-11 take every chunk in turn, two warps per 32-lane TMEM quadrant: warp part p owns
-    // key columns [64 p, 64 p + 64) of its 32 rows, read from TMEM once; the two parts' row
-    // maxima meet in shared memory. P (fp16, two keys per column) goes to columns 32 p .. 32 p
-    // + 31 of the same S buffer once both parts have read their S columns.
+    // key columns [64 p, 64 p + 64) of S and head-dim columns [64 p, 64 p + 64) of O. The two
+    // parts' row maxima meet in shared memory;
+    // P (fp16, two keys per column) goes to columns 32 p .. 32 p + 31 of the same S buffer once
+    // both parts have read their S columns. Then the partial of chunk c - 1 (O / l as fp16 with
+    // its item's V exponent) is stored while PV(c) runs.
     const int sw = warp - 4, quad = sw & 3, part = sw >> 2;
     const int row = quad * 32 + lane;  // TMEM lane
-    const int j = row / kG;
+    const int j = row / kG, h = row % kG;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = a.scale_log2;
+    float m_prev = 0.f, l_prev = 0.f;  // chunk c - 1: row maximum (log2 units), this part's sum
+    int pending = -1;                  // chunk whose partial stores are not yet fenced
+    const ChunkDesc* dprev = nullptr;
     for (int c = 0;; ++c) {
       const int ds = c % kDescRing, X = c & 1;
       if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
       const ChunkDesc* d = &ctl->desc[ds];
-      if (d->end) break;
-      const int n_tok = d->n_tok;
-      const int lim = j < n_tok ? d->lim[j] : 0;
-      const int nval = min(max(lim - 64 * part, 0), 64);  // valid keys among my columns
-      if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
-      tc::fence_after_sync();
-      if (sw == 0 && lane == 0) GTRACE(kGtSm0, c);
-      const uint32_t ts = tmem + X * 128 + lane_off;
+      const bool end = d->end != 0;
       uint32_t v[64];
-      tc::ld32(ts + 64 * part, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tc::ld32(ts + 64 * part + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      if (!end) {
+        if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
+        tc::fence_after_sync();
+        if (sw == 0 && lane == 0) GTRACE(kGtSm0, c);
+        const uint32_t ts = tmem + X * 128 + lane_off + 64 * part;
+        tc::ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tc::ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      }
       tc::wait_ld();
-      // every lane of the warp has all 64 of its keys valid: no per-key mask
+      // ---- softmax of chunk c
+      const int lim = !end && j < d->n_tok ? d->lim[j] : 0;
+      const int nval = min(max(lim - 64 * part, 0), 64);  // valid keys among my columns
       const bool full = __all_sync(0xffffffffu, nval == 64);
       float mx = -INFINITY;
-      if (full) {
+      if (!end) {
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) mx = fmaxf(mx, fmaxf(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
-      } else {
+          for (int i = 0; i < 64; i += 2) mx = fmaxf(mx, fmaxf(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mx = i < nval ? fmaxf(mx, __uint_as_float(v[i])) : mx;
+          for (int i = 0; i < 64; ++i) mx = i < nval ? fmaxf(mx, __uint_as_float(v[i])) : mx;
+        }
+        ctl->xchg[c & 1][part][row] = mx;
       }
-      ctl->xchg[c & 1][part][row] = mx;
-      // both parts have read their S columns and posted their maxima
+      // both parts have read their S columns and posted their maxima (and finished chunk c - 1)
       asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-      mx = fmaxf(mx, ctl->xchg[c & 1][part ^ 1][row]);
-      const float m = lim > 0 ? mx * sl2 : 0.f;
-      float l0 = 0.f, l1 = 0.f;
-      uint32_t pk[32];
-      if (full) {
+      float m = 0.f, lp = 0.f;
+      if (!end) {
+        mx = fmaxf(mx, ctl->xchg[c & 1][part ^ 1][row]);
+        m = lim > 0 ? mx * sl2 : 0.f;
+        float l0 = 0.f, l1 = 0.f;
+        uint32_t pk[32];
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(v[i]), sl2, -m));
-          const float p1 = ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m));
-          l0 += p0;
-          l1 += p1;
-          pk[i >> 1] = pack_f16(p0, p1);
-        }
-      } else {
+          for (int i = 0; i < 64; i += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(v[i]), sl2, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m));
+            l0 += p0;
+            l1 += p1;
+            pk[i >> 1] = pack_f16(p0, p1);
+          }
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float p0 = i < nval ? ex2(fmaf(__uint_as_float(v[i]), sl2, -m)) : 0.f;
-          const float p1 = i + 1 < nval ? ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m)) : 0.f;
-          l0 += p0;
-          l1 += p1;
-          pk[i >> 1] = pack_f16(p0, p1);
-        }
-      }
-      tc::st32(ts + 32 * part, pk);
-      // four slots: the epilogue of chunk c reads slot c & 3 before the MMA may issue PV(c + 2),
-      // and the softmax of chunk c + 4 runs only after that
-      if (part == 0) ctl->lm_m[c & 3][row] = m;
-      ctl->lm_l[c & 3][part][row] = l0 + l1;
-      tc::wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&ctl->p_full[X]);
-        mbar_arrive(&ctl->lm_full[c & 3]);
-      }
-      if (sw == 0 && lane == 0) GTRACE(kGtSm1, c);
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    // Warps 12-15 (one per TMEM lane quadrant), every chunk in order: the partial output O / l
-    // as fp16 with the item's V exponent, its (log2-sum-exp, exponent), then (a softmax phase
-    // later) the fence that hands the chunk to its merge warp. Before a chunk whose successor
-    // starts a new item, the next item's V is converted to fp16: V * 2^-e with e chosen so
-    // that max |V| lands in [2^14, 2^15) (the result is exact: 8 significant bits, 29 binades).
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const int j = row / kG, h = row % kG;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int et = threadIdx.x - 384;  // 0..127
-    int conv_item = -1;  // last item whose V is converted
-    int pending = -1;
-    // converts the V of the item in descriptor `dn` (all 128 threads)
-    auto convert_v = [&](const ChunkDesc* dn) -> bool {
-      const int Yn = dn->ybuf, itn = dn->item;
-      if (!g_warp_wait(&ctl->v_full[Yn], (itn >> 1) & 1, ctl, a.err_word)) return false;
-      const uint32_t vb = smem_u32(v_s + Yn * kGTile);
-      // 32 KiB = 2048 x 16 B: thread et takes vectors et, et + 128, ...
-      uint32_t mxv = 0;
-#pragma unroll 4
-      for (int q = 0; q < 16; ++q) {
-        uint32_t x0, x1, x2, x3;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                     : "r"(vb + (et + 128 * q) * 16));
-        // |bf16| as 16-bit integers compare like the values (NaN aside)
-        mxv = max(mxv, max(max(x0 & 0x7fff7fffu, x1 & 0x7fff7fffu), max(x2 & 0x7fff7fffu, x3 & 0x7fff7fffu)) >> 16);
-        mxv = max(mxv, max(max(x0 & 0x7fffu, x1 & 0x7fffu), max(x2 & 0x7fffu, x3 & 0x7fffu)));
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mxv = max(mxv, __shfl_xor_sync(0xffffffffu, mxv, off));
-      if (lane == 0) ctl->vmax[quad] = __uint_as_float(mxv << 16);
-      asm volatile("bar.sync 9, 128;" ::: "memory");
-      const float vm = fmaxf(fmaxf(ctl->vmax[0], ctl->vmax[1]), fmaxf(ctl->vmax[2], ctl->vmax[3]));
-      int e = 0;
-      if (vm > 0.f) e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 127 - 14;
-      e = max(-100, min(100, e));
-      const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-#pragma unroll 4
-      for (int q = 0; q < 16; ++q) {
-        const uint32_t ad = vb + (et + 128 * q) * 16;
-        uint32_t x0, x1, x2, x3;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(ad));
-        g_sts128(ad, pack_f16(bf16_lo(x0) * sc, bf16_hi(x0) * sc), pack_f16(bf16_lo(x1) * sc, bf16_hi(x1) * sc),
-                 pack_f16(bf16_lo(x2) * sc, bf16_hi(x2) * sc), pack_f16(bf16_lo(x3) * sc, bf16_hi(x3) * sc));
-      }
-      // the tensor core reads the copy through the async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (et == 0) ctl->vexp[Yn] = e;
-      asm volatile("bar.sync 9, 128;" ::: "memory");
-      if (et == 0) mbar_arrive(&ctl->v_ready[Yn]);
-      conv_item = itn;
-      return true;
-    };
-    bool ok = true;
-    for (int c = 0; ok; ++c) {
-      const int ds = c % kDescRing, X = c & 1;
-      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
-      const ChunkDesc* d = &ctl->desc[ds];
-      if (d->end) break;
-      if (d->item != conv_item && !convert_v(d)) break;
-      // the next chunk's item, if it is a new one, gets its V converted before this chunk's PV
-      // is awaited, so the MMA does not wait for the conversion (one thread looks, all follow)
-      {
-        const int dn_s = (c + 1) % kDescRing;
-        const uint32_t dn_ph = ((c + 1) / kDescRing) & 1;
-        if (et == 0) ctl->peek = mbar_try_wait(&ctl->desc_full[dn_s], dn_ph) ? 1 : 0;
-        asm volatile("bar.sync 10, 128;" ::: "memory");
-        const bool nx = ctl->peek != 0;
-        asm volatile("bar.sync 10, 128;" ::: "memory");  // every thread has read peek
-        if (nx) {
-          if (!g_warp_wait(&ctl->desc_full[dn_s], dn_ph, ctl, a.err_word)) break;
-          const ChunkDesc* dn = &ctl->desc[dn_s];
-          if (!dn->end && dn->item != conv_item && !convert_v(dn)) break;
-        }
-      }
-      if (!g_warp_wait(&ctl->pv_done[X], (c >> 1) & 1, ctl, a.err_word)) break;
-      if (!g_warp_wait(&ctl->lm_full[c & 3], (c >> 2) & 1, ctl, a.err_word)) break;
-      tc::fence_after_sync();
-      if (threadIdx.x == 384) GTRACE(kGtE0, c);
-      const float2 ml = make_float2(ctl->lm_m[c & 3][row], ctl->lm_l[c & 3][0][row] + ctl->lm_l[c & 3][1][row]);
-      const bool valid = j < d->n_tok;
-      const float inv_l = ml.y > 0.f ? 1.f / ml.y : 0.f;
-      const int tr = valid ? d->tr[j] : 0;
-      const int64_t prow = ((static_cast<int64_t>(tr) * a.num_kv_heads + d->g) * a.k + (valid ? d->slot[j] : 0)) * kG + h;
-      uint16_t* dst = w.part + prow * kHeadDim;
-      const uint32_t to = tmem + 256 + X * 128 + lane_off;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t o[64];
-        tc::ld32(to + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tc::ld32(to + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tc::wait_ld();
-        if (hf == 1) {
-          // O buffer X is read: PV(c + 2) may overwrite it
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->o_free[X]);
-          // the previous chunk's partial stores, issued an iteration ago, are fenced before this
-          // chunk's stores start (a fence waits for every store the thread has issued), and that
-          // chunk goes to its merge warp
-          if (pending >= 0) {
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
-            pending = -1;
+          for (int i = 0; i < 64; i += 2) {
+            const float p0 = i < nval ? ex2(fmaf(__uint_as_float(v[i]), sl2, -m)) : 0.f;
+            const float p1 = i + 1 < nval ? ex2(fmaf(__uint_as_float(v[i + 1]), sl2, -m)) : 0.f;
+            l0 += p0;
+            l1 += p1;
+            pk[i >> 1] = pack_f16(p0, p1);
           }
         }
+        tc::st32(tmem + X * 128 + lane_off + 32 * part, pk);
+        lp = l0 + l1;
+        // four slots: the partner reads slot c & 3 after the next chunk's quad barrier
+        ctl->lsum[c & 3][part][row] = lp;
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full[X]);
+        if (sw == 0 && lane == 0) GTRACE(kGtSm1, c);
+      }
+      // ---- partial of chunk c - 1
+      if (c >= 1) {
+        // the chunk before it, stored an iteration ago, is fenced and handed to its merge warp
+        if (pending >= 0) {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
+          pending = -1;
+        }
+        if (sw == 0 && lane == 0) GTRACE(kGtE0, c - 1);
+        // O(c - 1), read once P(c) is out (so PV(c) is not held up, and S and O never share the
+        // registers)
+        uint32_t o[64];
+        if (!g_warp_wait(&ctl->pv_done[X ^ 1], ((c - 1) >> 1) & 1, ctl, a.err_word)) break;
+        tc::fence_after_sync();
+        const uint32_t to = tmem + 256 + (X ^ 1) * 128 + lane_off + 64 * part;
+        tc::ld32(to, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tc::ld32(to + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tc::wait_ld();
+        // O buffer (c - 1) % 2 is read: PV(c + 1) may overwrite it
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->o_free[X ^ 1]);
+        const int itp = dprev->item;
+        if (!g_warp_wait(&ctl->vx_ready[itp & 3], (itp >> 2) & 1, ctl, a.err_word)) break;
+        const int e = ctl->vexp[itp & 3];
+        const float lt = l_prev + ctl->lsum[(c - 1) & 3][part ^ 1][row];
+        const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+        const bool valid = j < dprev->n_tok;
         if (valid) {
+          const int64_t prow =
+              ((static_cast<int64_t>(dprev->tr[j]) * a.num_kv_heads + dprev->g) * a.k + dprev->slot[j]) * kG + h;
+          uint16_t* dst = w.part + prow * kHeadDim + 64 * part;
 #pragma unroll
           for (int q8 = 0; q8 < 8; ++q8) {
             const uint32_t* f = &o[8 * q8];
-            *reinterpret_cast<uint4*>(dst + 64 * hf + 8 * q8) = make_uint4(
+            *reinterpret_cast<uint4*>(dst + 8 * q8) = make_uint4(
                 pack_f16(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l),
                 pack_f16(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l),
                 pack_f16(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l),
                 pack_f16(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l));
           }
+          if (part == 0) *reinterpret_cast<float2*>(w.ml + prow) = make_float2(m_prev + log2f(lt), static_cast<float>(e));
         }
+        if (sw == 0 && lane == 0) GTRACE(kGtE1, c - 1);
+        pending = c - 1;
       }
-      if (valid)
-        *reinterpret_cast<float2*>(w.ml + prow) = make_float2(ml.x + log2f(ml.y), static_cast<float>(ctl->vexp[d->ybuf]));
-      if (threadIdx.x == 384) GTRACE(kGtE1, c);
-      pending = c;
+      if (end) break;
+      m_prev = m;
+      l_prev = lp;
+      dprev = d;
     }
     if (pending >= 0) {
       __threadfence();
