@@ -103,6 +103,30 @@ int encode_cache_map_packed(CUtensorMap* map, const void* cache, int kv_dtype, i
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
+// A packed bf16 cache as one box per 128-key block of one kv head: a 5-D map {the first 64
+// elements of a page row, 16 rows, kv head, page, row quarter} (strides: row, one head's 16 rows,
+// the page, 128 B) whose box {64, 16, 1, 8, 2} starts at the block's first page and at quarter
+// 0 (K) or 2 (V). It lands as [quarter][8 pages][16 rows][128 B]: key k of the block at k * 128 B,
+// the block's dims 64..127 16 KiB further, in 128B-swizzle atoms of 8 keys. The block's 8 pages
+// are consecutive (block_page_stride >= 8); pages past the cache read as zeros.
+int encode_cache_map_block(CUtensorMap* map, const void* cache, int num_kv_heads, int64_t num_pages,
+                           int64_t page_stride_bytes) {
+  std::memset(map, 0, sizeof(*map));
+  if (page_stride_bytes != page_content_bytes(PBS_KV_BF16, num_kv_heads)) return PBS_ERR_UNSUPPORTED;
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PBS_ERR_CUDA;
+  const cuuint64_t row = 2 * kHeadDim * 2;  // K and V of one row of one head, bf16
+  const cuuint64_t dims[5] = {kHeadDim / 2, kPageRows, static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_pages), 4};
+  const cuuint64_t strides[4] = {row, row * kPageRows, static_cast<cuuint64_t>(page_stride_bytes), 128};
+  const cuuint32_t box[5] = {kHeadDim / 2, kPageRows, 1, 8, 2};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
+}
+
 // The tensor map the token-centric kernel reads: the packed one when the cache allows it.
 int encode_attend_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
                       int64_t page_stride_bytes, int32_t* packed) {
@@ -583,9 +607,12 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
     e = pbs::launch_attend(a, pbs::kModePrefill, map, cs);
   } else {
-    // both tcgen05 kernels stream K and V separately: one box per (page, head) half row
+    // both tcgen05 kernels stream K and V separately: the gathered-row kernel one box per
+    // (page, head) half row, the tile kernel one box per (block, head) half row
     CUtensorMap half_map;
-    st = encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2);
+    st = kernel == kPrefillGather
+             ? encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2)
+             : encode_cache_map_block(&half_map, kv_cache, num_kv_heads, num_pages, page_stride_bytes);
     if (st != PBS_OK) return st;
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride,

@@ -14,10 +14,11 @@
 //   merged into a sorted union; every union block is streamed once and each row is masked by its
 //   own token's selection.
 // * Warps 0 and 3: TMA producers. Warp 0 loads the Q tile once (3-D tensor map) and streams the
-//   K of each union block, warp 3 its V, each through its own 3-stage ring, one 4 KiB copy per
-//   page (the K or the V half of the page's 16 rows of this kv head) through a 5-D tensor map
-//   over the packed cache, 128B swizzle. A stage is [page][row half][64-dim quarter][8 rows]
-//   [128 B], so 8-key groups sit 2 KiB apart. Warp 1: one thread issues the tcgen05 MMAs, S two
+//   K of each union block, warp 3 its V, each through its own 3-stage ring, one 32 KiB tensor
+//   copy per block (the K or the V half of the 8 pages' 16 rows of this kv head) through a 5-D
+//   map {64 elements, 16 rows, kv head, page, row quarter} over the packed cache, 128B swizzle.
+//   A stage is [64-dim quarter][128 keys][128 B]: 8-key groups 1 KiB apart, the block's second
+//   64 dims 16 KiB further. Warp 1: one thread issues the tcgen05 MMAs, S two
 //   blocks ahead of PV. Warps 4-11: softmax and epilogue, two warps per TMEM lane quadrant.
 // * TMEM (512 columns): S triple buffer (3 x 128, fp32) and the O accumulator (128, fp32). Each
 //   softmax part rewrites its own 64 S columns with P: hi (bf16, two keys per column) in the
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     return;
   }
   uint8_t* q_s = big;
-  // stage st of each ring at + st * kTileBytes; a stage is [page][row half][64-dim quarter][8 rows]
-  // [128 B], so 8-key groups are 2 KiB apart and the two quarters of a row 1 KiB apart
+  // stage st of each ring at + st * kTileBytes; a stage is [64-dim quarter][128 keys][128 B], so
+  // 8-key groups are 1 KiB apart and the two quarters of a key 16 KiB apart
   uint8_t* k_s = big + kQBytes;
   uint8_t* v_s = k_s + kStagesTc * kTileBytes;
 
@@ -393,9 +394,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------------ TMA producers
-    // Warp 0 loads the Q tile and streams the K of each union block, warp 3 its V: one 4 KiB
-    // copy per page (the K or V half of its 16 rows of this kv head: quarter coordinate 0 or 2 of
-    // the half-row map); lanes 0..7 issue the 8 pages of a block.
+    // Warp 0 loads the Q tile and streams the K of each union block, warp 3 its V: one 32 KiB
+    // copy per block (quarter coordinate 0 for K, 2 for V, from the block's first page).
     const bool is_k = warp == 0;
     if (is_k && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
@@ -428,9 +428,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
       __syncwarp();
       // out-of-range pages read as zeros (TMA bounds)
-      if (lane < kPagesPerBlock)
-        tma_load_5d(dst + lane * 4096, &kv_map, &full[st], 0, 0, quarter, 0,
-                    static_cast<int>((base + lane) * a.num_kv_heads + g));
+      if (lane == 0) tma_load_5d(dst, &kv_map, &full[st], 0, 0, g, static_cast<int>(base), quarter);
       if (is_k) TRACE(kEvProdIssue1 + i);
       issued = i + 1;
     }
@@ -459,11 +457,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const uint32_t k_addr = smem_u32(k_s + st * kTileBytes);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            // dims 16ks..: Q half ks/4 (16 KiB apart, 8-row groups 1 KiB apart); K quarter ks/4
-            // (1 KiB apart, 8-key groups 2 KiB apart)
+            // dims 16ks..: Q half ks/4 and K quarter ks/4 (each 16 KiB apart, 8-row groups 1 KiB
+            // apart)
             tc::mma_ss(tm_s0 + sb * 128,
                        tc::smem_desc_sw128(q_addr + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024),
-                       tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048), kIdescS,
+                       tc::smem_desc_sw128(k_addr + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024), kIdescS,
                        ks > 0);
           }
           tc::commit(&ctl->s_full[sb]);
@@ -486,9 +484,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               // keys 16ks..16ks+15 belong to softmax part `owner`
               const int owner = (16 * ks) / kW;
               const uint32_t pa = tm_s0 + sb * 128 + owner * kW + part * (kW / 2) + (16 * ks - owner * kW) / 2;
-              // keys 16ks..16ks+15 = two 8-key groups (2 KiB apart) from key group 2ks; dims in
-              // two 64-wide MN atoms 1 KiB apart
-              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), kIdescPV,
+              // keys 16ks..16ks+15 = two 8-key groups (1 KiB apart) from key group 2ks; dims in
+              // two 64-wide MN atoms 16 KiB apart
+              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
                          !(j == 0 && part == 0 && ks == 0));
             }
           }
@@ -538,8 +536,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t v_base = smem_u32(v_s + st * kTileBytes);
         for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
           const int key = last_rows + (e >> 4), vq = (e >> 3) & 1, chunk = e & 7;
-          // key = 16 page + 8 half + row; 8-key groups 2 KiB apart
-          sts128(v_base + (key >> 3) * 2048 + vq * 1024 + (key & 7) * 128 + chunk * 16, 0, 0, 0, 0);
+          // key k of quarter vq at vq * 16 KiB + k * 128 B
+          sts128(v_base + vq * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }

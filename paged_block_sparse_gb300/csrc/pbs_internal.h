@@ -102,8 +102,10 @@ constexpr int kModePrefill = 1;
 constexpr int kModeMixed = 2;
 cudaError_t launch_attend(const AttendArgs& a, int mode, const CUtensorMap& tmap, cudaStream_t stream);
 
-// Prefill attend on tcgen05 tensor cores (bf16 cache, GQA 8, top-k <= 16, 16-byte aligned q/out
-// rows). `q_map` is a 3-D tensor map {head_dim, heads, tokens} with a {64, 8, 16} box.
+// Prefill attend on tcgen05 tensor cores (bf16 cache, GQA 8 or 16, top-k <= 16, 16-byte aligned
+// q/out rows). `kv_map` is the per-block map of the packed cache (one {64, 16, 1, 8, 2} box per
+// 128-key block of one kv head); `q_map` a 3-D tensor map {head_dim, heads, tokens} with a
+// {64, G, 128 / G} box.
 bool prefill_tc_supported(const AttendArgs& a);
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream);
