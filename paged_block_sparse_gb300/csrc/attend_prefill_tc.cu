@@ -34,6 +34,8 @@
 //   maximum grows by more than 2^8, so most blocks never touch O from the CUDA cores.
 // * Duplicate ids in a token's list count once (set semantics of the attend); the decode path and
 //   the table builders follow the row writer literally. With distinct ids the two agree.
+#include <algorithm>
+
 #include "pbs_device.cuh"
 #include "pbs_internal.h"
 #include "tc_device.cuh"
@@ -55,12 +57,29 @@ constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB: a block's K, o
 constexpr int kStagesTc = 3;                           // stages of the K ring and of the V ring
 constexpr int kSBuf = 3;                               // S buffers in TMEM (S runs 2 blocks ahead of PV)
 constexpr int kBigBytes = kQBytes + 2 * kStagesTc * kTileBytes;  // 224 KiB
-constexpr int kMaxUnion = 256;
+constexpr int kMaxUnion = 128;    // union blocks per tile: the kernel takes page tables <= 128 blocks wide
+constexpr int kSetWords = kMaxUnion / 32;
 constexpr int kTcMaxTopk = 16;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
+// One tile, described by the scheduler warp for the other roles (two slots, used alternately).
+struct TileDesc {
+  int32_t end;  // no tile: the CTA's list is done
+  int32_t req, g, t0, n_tok, c0, ctx0, pos_last;  // request, kv head, first token row, tokens, ...
+  int32_t n_union;
+  int32_t bad_mask;                  // tokens whose row hit an out-of-range block id
+  int16_t own[kTokMax];              // own block of each token (-1: none)
+  int16_t lim[kTokMax];              // keys of the own block the token sees
+  uint16_t union_blk[kMaxUnion];      // the tile's distinct valid blocks, increasing
+  uint32_t blocks[kTokMax][kSetWords];  // bit b: the token selected block b (valid and causal)
+};
+
+// Roles that read a tile slot and release it: the two TMA warps, the MMA thread, the softmax warps.
+constexpr uint32_t kTileUsers = 3 + kSoftWarps;
+
 struct TcCtl {
   uint64_t q_full;
+  uint64_t q_empty;  // the S MMAs of the tile whose Q sits in shared memory have completed
   // K and V stream through separate rings: a K stage is free once S has read it, a V stage once
   // PV has, so K can be loaded three blocks ahead of S while S runs two blocks ahead of PV
   uint64_t k_full[kStagesTc];
@@ -68,21 +87,16 @@ struct TcCtl {
   uint64_t v_full[kStagesTc];
   uint64_t v_empty[kStagesTc];
   uint64_t s_full[kSBuf];
-  // per S buffer (block i uses buffer i % 3): P(i) written, PV(i) done. A barrier cannot be lapped:
-  // block i + 3 needs S(i + 3), which the MMA thread issues only after PV(i).
+  // per S buffer (block i of the CTA's block sequence uses buffer i % 3): P(i) written, PV(i)
+  // done. A barrier cannot be lapped: block i + 3 needs S(i + 3), which the MMA thread issues only
+  // after PV(i).
   uint64_t p_full[kSBuf];
   uint64_t pv_done[kSBuf];
+  uint64_t tile_full[2];
+  uint64_t tile_empty[2];
   uint32_t tmem_base;
-  int32_t n_union;
-  int32_t req, t0, n_tok;
-  int32_t c0, ctx0, pos_last;  // request's first token row, context length, last position
-  int32_t bad_mask;   // tokens whose row hit an out-of-range block id
   int32_t abort;
-  int32_t own[kTokMax];  // own block of each token (-1: none)
-  int32_t lim[kTokMax];  // keys of the own block the token sees
-  int32_t cnt[kTokMax];  // distinct valid blocks per token
-  uint16_t union_blk[kMaxUnion];
-  uint16_t tok_blk[kTokMax][kTcMaxTopk];
+  TileDesc tile[2];
   float xchg[kSplit][kRows];  // per-row partial maxima / sums exchanged within a lane quadrant
 };
 
@@ -97,13 +111,20 @@ constexpr int kTraceBlocks = 64;
 enum TraceEv { kEvStart, kEvSetup, kEvEpi, kEvEnd, kEvProdIssue0, kEvProdIssue1 = kEvProdIssue0 + kTraceBlocks,
                kEvS = kEvProdIssue1 + kTraceBlocks, kEvPV = kEvS + kTraceBlocks,
                kEvSoftIn = kEvPV + kTraceBlocks, kEvSoftMax = kEvSoftIn + kTraceBlocks,
-               kEvSoftOut = kEvSoftMax + kTraceBlocks, kEvCount = kEvSoftOut + kTraceBlocks };
+               kEvSoftOut = kEvSoftMax + kTraceBlocks, kEvDesc = kEvSoftOut + kTraceBlocks,
+               kEvQ = kEvDesc + kTraceBlocks, kEvTileIn = kEvQ + kTraceBlocks, kEvTileOut = kEvTileIn + kTraceBlocks,
+               kEvDesc0 = kEvTileOut + kTraceBlocks, kEvCount = kEvDesc0 + kTraceBlocks };
 __device__ long long g_trace[kEvCount + 4];
 __device__ int g_trace_cta;
-#define TRACE(ev) do { if (blockIdx.x == static_cast<unsigned>(g_trace_cta) && blockIdx.y == 0 && (ev) < kEvCount) \
+__device__ int g_trace_b0;  // first block of the CTA's sequence the per-block events record
+#define TRACE(ev) do { if (blockIdx.x == static_cast<unsigned>(g_trace_cta) && (ev) < kEvCount) \
                          g_trace[(ev)] = clock64(); } while (0)
+#define TRACEB(ev, i) do { if ((i) - g_trace_b0 >= 0 && (i) - g_trace_b0 < kTraceBlocks) TRACE((ev) + (i) - g_trace_b0); } while (0)
+#define TRACET(ev, i) do { if ((i) < kTraceBlocks) TRACE((ev) + (i)); } while (0)
 #else
 #define TRACE(ev) do { } while (0)
+#define TRACEB(ev, i) do { } while (0)
+#define TRACET(ev, i) do { } while (0)
 #endif
 
 // p = 2^(s * sl2 - m) for the first `nval` of this thread's kW key columns (0 beyond), written
@@ -165,6 +186,17 @@ __device__ __forceinline__ void quad_bar(int quad) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + quad), "r"(32 * kSplit) : "memory");
 }
 
+// The quadrant's warps meet at their named barrier and agree whether any thread passed true.
+__device__ __forceinline__ bool quad_any(int quad, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(1 + quad), "r"(32 * kSplit)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -206,6 +238,116 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
 
 __device__ __forceinline__ bool aborted(TcCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
 
+// Scheduler warp: describes tile f of the CTA's list in slot d. Flat tile f is kv head f % Hkv of
+// request tile (tiles - 1 - f / Hkv), request tiles numbered request by request: the list starts
+// at the last request's last tiles, whose tokens see the most blocks.
+template <int kTok>
+__device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int total_tiles, TileDesc* d, int lane) {
+  const int g = f % a.num_kv_heads;
+  const int rt = total_tiles - 1 - f / a.num_kv_heads;
+  int r = -1, t0 = 0, n = 0, c0 = 0, ctx0 = 0, seq_len = 0;
+  int base_tiles = 0;
+  for (int r0 = 0; r0 < a.num_reqs && r < 0; r0 += 32) {
+    const int rr = r0 + lane;
+    // every lane loads its request's bounds and length at once (one round trip)
+    int q_len = 0, cb = 0, sl = 0;
+    if (rr < a.num_reqs) {
+      cb = __ldg(a.cu_seqlens_q + rr);
+      q_len = __ldg(a.cu_seqlens_q + rr + 1) - cb;
+      sl = __ldg(a.seq_lens + rr);
+    }
+    const int tiles = (q_len + kTok - 1) / kTok;
+    int incl = tiles;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - tiles + base_tiles;
+    const uint32_t hit = __ballot_sync(0xffffffffu, rt >= excl && rt < excl + tiles);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      r = r0 + src;
+      const int tile = rt - __shfl_sync(0xffffffffu, excl, src);
+      const int ql = __shfl_sync(0xffffffffu, q_len, src);
+      c0 = __shfl_sync(0xffffffffu, cb, src);
+      seq_len = __shfl_sync(0xffffffffu, sl, src);
+      ctx0 = seq_len - ql;
+      t0 = c0 + tile * kTok;
+      n = min(kTok, ql - tile * kTok);
+    }
+    base_tiles += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  // lane tt: token tt's distinct valid blocks as a 128-bit set (a repeated id sets the same bit:
+  // each selected block counts once), its own block and the keys of it the token sees
+  uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;
+  int own = -1, lim = 0;
+  bool bad = false;
+  if (lane < n) {
+    const int pos = ctx0 + (t0 + lane - c0);
+    const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
+    own = causal_len > 0 ? pos / kSparseBlock : -1;
+    lim = own >= 0 ? causal_len - own * kSparseBlock : 0;
+    const int32_t* row = a.topk + static_cast<int64_t>(t0 + lane) * a.topk_row_stride;
+    int ids[kTcMaxTopk];
+#pragma unroll
+    for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = j < a.k ? __ldg(row + j) : -1;
+#pragma unroll
+    for (int j = 0; j < kTcMaxTopk; ++j) {
+      const int b = ids[j];
+      if (b >= 0 && b <= own) {
+        if (b >= a.max_blocks) {
+          bad = true;
+        } else {
+          const uint32_t bit = 1u << (b & 31);
+          m0 |= (b >> 5) == 0 ? bit : 0u;
+          m1 |= (b >> 5) == 1 ? bit : 0u;
+          m2 |= (b >> 5) == 2 ? bit : 0u;
+          m3 |= (b >> 5) == 3 ? bit : 0u;
+        }
+      }
+    }
+    // a row with an out-of-range id contributes nothing (its output is zero, the error recorded)
+    if (bad) {
+      set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+      m0 = m1 = m2 = m3 = 0u;
+    }
+  }
+  const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad);
+  if (lane < kTok) {
+    d->own[lane] = static_cast<int16_t>(min(own, 32767));
+    d->lim[lane] = static_cast<int16_t>(lim);
+    d->blocks[lane][0] = m0;
+    d->blocks[lane][1] = m1;
+    d->blocks[lane][2] = m2;
+    d->blocks[lane][3] = m3;
+  }
+  // union = set bits in increasing order
+  int nu = 0;
+#pragma unroll
+  for (int w = 0; w < kSetWords; ++w) {
+    const uint32_t word = __reduce_or_sync(0xffffffffu, w == 0 ? m0 : w == 1 ? m1 : w == 2 ? m2 : m3);
+    if ((word >> lane) & 1u) d->union_blk[nu + __popc(word & ((1u << lane) - 1u))] = static_cast<uint16_t>(32 * w + lane);
+    nu += __popc(word);
+  }
+  if (lane == 0) {
+    d->end = 0;
+    d->req = r;
+    d->g = g;
+    d->t0 = t0;
+    d->n_tok = r < 0 ? 0 : n;
+    d->c0 = c0;
+    d->ctx0 = ctx0;
+    d->pos_last = seq_len - 1;
+    d->n_union = r < 0 ? 0 : nu;
+    d->bad_mask = static_cast<int32_t>(bad_mask);
+  }
+}
+
+// One CTA per SM walks its list of tiles (flat tiles blockIdx.x, + gridDim.x, ...). The K / V
+// rings, the S buffers and the MMA order run on across tile boundaries (block counters count
+// the CTA's whole block sequence), so the next tile's S runs while the softmax warps finish the
+// previous tile, and its description, Q tile and first K / V blocks are ready before they do.
 template <int kG>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
@@ -216,7 +358,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   TcCtl* ctl = reinterpret_cast<TcCtl*>(smem_raw + kBigBytes);
   // the 128B-swizzled operands need 1024-byte alignment; the dynamic base provides it
   if ((smem_u32(smem_raw) & 1023u) != 0) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
     return;
   }
   uint8_t* q_s = big;
@@ -226,233 +368,194 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint8_t* v_s = k_s + kStagesTc * kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.y;
-  if (threadIdx.x == 0) TRACE(kEvStart);
-
-  // ---- tile -> (request, first token): tiles are numbered request by request ----------------
-  if (warp == 0) {
-    int r = -1, t0 = 0, n = 0, c0 = 0, ctx0 = 0, seq_len = 0;
-    int base_tiles = 0;
-    for (int r0 = 0; r0 < a.num_reqs && r < 0; r0 += 32) {
-      const int rr = r0 + lane;
-      // every lane loads its request's bounds and length at once (one round trip)
-      int q_len = 0, cb = 0, sl = 0;
-      if (rr < a.num_reqs) {
-        cb = __ldg(a.cu_seqlens_q + rr);
-        q_len = __ldg(a.cu_seqlens_q + rr + 1) - cb;
-        sl = __ldg(a.seq_lens + rr);
-      }
-      const int tiles = (q_len + kTok - 1) / kTok;
-      int incl = tiles;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      const int excl = incl - tiles + base_tiles;
-      const bool mine = static_cast<int>(blockIdx.x) >= excl && static_cast<int>(blockIdx.x) < excl + tiles;
-      const uint32_t hit = __ballot_sync(0xffffffffu, mine);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        r = r0 + src;
-        const int ex = __shfl_sync(0xffffffffu, excl, src);
-        const int ql = __shfl_sync(0xffffffffu, q_len, src);
-        const int tile = static_cast<int>(blockIdx.x) - ex;
-        c0 = __shfl_sync(0xffffffffu, cb, src);
-        seq_len = __shfl_sync(0xffffffffu, sl, src);
-        ctx0 = seq_len - ql;
-        t0 = c0 + tile * kTok;
-        n = min(kTok, ql - tile * kTok);
-      }
-      base_tiles += __shfl_sync(0xffffffffu, incl, 31);
+  if (threadIdx.x == 0) {
+    TRACE(kEvStart);
+    ctl->abort = 0;
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
+    for (int i = 0; i < kStagesTc; ++i) {
+      mbar_init(&ctl->k_full[i], 1);
+      mbar_init(&ctl->k_empty[i], 1);
+      mbar_init(&ctl->v_full[i], 1);
+      mbar_init(&ctl->v_empty[i], 1);
     }
-    if (lane == 0) {
-      // once any CTA has given up on a wait, the rest of the grid does no work
-      const bool gave_up = a.err_word != nullptr &&
-                           (*reinterpret_cast<volatile int32_t*>(a.err_word) & PBS_DEVERR_TIMEOUT) != 0;
-      ctl->req = r;
-      ctl->t0 = t0;
-      ctl->c0 = c0;
-      ctl->ctx0 = ctx0;
-      ctl->pos_last = seq_len - 1;
-      ctl->n_tok = (r < 0 || gave_up) ? 0 : n;
-      ctl->bad_mask = 0;
-      ctl->abort = 0;
-      mbar_init(&ctl->q_full, 1);
-      for (int i = 0; i < kStagesTc; ++i) {
-        mbar_init(&ctl->k_full[i], 1);
-        mbar_init(&ctl->k_empty[i], 1);
-        mbar_init(&ctl->v_full[i], 1);
-        mbar_init(&ctl->v_empty[i], 1);
-      }
-      for (int i = 0; i < kSBuf; ++i) {
-        mbar_init(&ctl->s_full[i], 1);
-        mbar_init(&ctl->p_full[i], kSoftWarps);
-        mbar_init(&ctl->pv_done[i], 1);
-      }
-      fence_mbar_init();
+    for (int i = 0; i < kSBuf; ++i) {
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->p_full[i], kSoftWarps);
+      mbar_init(&ctl->pv_done[i], 1);
     }
-  }
-  __syncthreads();
-  const int req = ctl->req, t0 = ctl->t0, n_tok = ctl->n_tok;
-  if (n_tok <= 0) return;  // surplus tile, or the grid already gave up; uniform across the CTA
-
-  // ---- each token's distinct valid blocks, sorted, plus the union bitmap ---------------------
-  // The union is built as a bitmap over the block ids in the last V stage (free until the loop).
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(v_s + (kStagesTc - 1) * kTileBytes);
-  const int pos_last = ctl->pos_last;  // position of the request's last token
-  // valid block ids are <= pos_last / 128 and < max_blocks (<= 65536): at most 2048 words
-  const int nwords = min(max(pos_last, 0) / kSparseBlock / 32 + 1, (a.max_blocks + 31) / 32);
-  for (int w = threadIdx.x; w < nwords; w += kThreadsTc) bitmap[w] = 0u;
-  __syncthreads();
-  {
-    // every warp takes tokens warp and warp + 12 and loads both top-k rows before working on them
-    constexpr int kWarps = kThreadsTc / 32;
-    const int c0 = ctl->c0, ctx0 = ctl->ctx0;
-    const int tt0 = warp, tt1 = warp + kWarps;
-    const int b0 = (tt0 < n_tok && lane < a.k) ? __ldg(a.topk + static_cast<int64_t>(t0 + tt0) * a.topk_row_stride + lane)
-                                               : -1;
-    const int b1 = (tt1 < n_tok && lane < a.k) ? __ldg(a.topk + static_cast<int64_t>(t0 + tt1) * a.topk_row_stride + lane)
-                                               : -1;
-#pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int tt = u == 0 ? tt0 : tt1;
-      if (tt >= kTok) continue;
-      if (tt >= n_tok) {
-        if (lane == 0) {
-          ctl->cnt[tt] = 0;
-          ctl->own[tt] = -1;
-          ctl->lim[tt] = 0;
-        }
-        continue;
-      }
-      const int t = t0 + tt;
-      const int pos = ctx0 + (t - c0);
-      const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
-      const int own = causal_len > 0 ? pos / kSparseBlock : -1;
-      const int b = u == 0 ? b0 : b1;
-      bool valid = lane < a.k && causal_len > 0 && b >= 0 && b <= own;
-      const bool oob = valid && b >= a.max_blocks;
-      if (__any_sync(0xffffffffu, oob)) {
-        if (lane == 0) {
-          atomicOr(&ctl->bad_mask, 1 << tt);
-          set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
-        }
-        valid = false;
-      }
-      // drop repeated ids: keep the lowest lane of each value
-      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-      const uint32_t same = __match_any_sync(0xffffffffu, valid ? b : -1 - lane);
-      const bool keep = valid && (__ffs(same & vmask) - 1) == lane;
-      const uint32_t kmask = __ballot_sync(0xffffffffu, keep);
-      int rank = 0;
-      for (int j = 0; j < 32; ++j) {
-        const int bj = __shfl_sync(0xffffffffu, b, j);
-        if (((kmask >> j) & 1u) && bj < b) ++rank;
-      }
-      if (keep) {
-        ctl->tok_blk[tt][rank] = static_cast<uint16_t>(b);
-        atomicOr(&bitmap[b >> 5], 1u << (b & 31));
-      }
-      if (lane == 0) {
-        ctl->cnt[tt] = __popc(kmask);
-        ctl->own[tt] = own;
-        ctl->lim[tt] = causal_len - own * kSparseBlock;
-      }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->tile_full[i], 1);
+      mbar_init(&ctl->tile_empty[i], kTileUsers);
     }
+    fence_mbar_init();
   }
   if (warp == 2) tc::alloc(&ctl->tmem_base, 512);
-  __syncthreads();
-  // union = set bits in increasing order (one warp; a handful of words per tile)
-  if (warp == 0) {
-    // 32 words per step; each non-empty word is expanded by the whole warp, lane = bit
-    int at = 0;
-    for (int w0 = 0; w0 < nwords; w0 += 32) {
-      const uint32_t mine = w0 + lane < nwords ? bitmap[w0 + lane] : 0u;
-      uint32_t nz = __ballot_sync(0xffffffffu, mine != 0u);
-      while (nz) {
-        const int src = __ffs(nz) - 1;
-        nz &= nz - 1;
-        const uint32_t word = __shfl_sync(0xffffffffu, mine, src);
-        const int o = at + __popc(word & ((1u << lane) - 1u));
-        if (((word >> lane) & 1u) && o < kMaxUnion)
-          ctl->union_blk[o] = static_cast<uint16_t>(((w0 + src) << 5) + lane);
-        at += __popc(word);
-      }
-    }
-    if (lane == 0) ctl->n_union = at < kMaxUnion ? at : kMaxUnion;
-  }
-  // the bitmap's generic writes precede the copy engine's writes into the same stage
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const int nU = ctl->n_union;
-  if (threadIdx.x == 0) TRACE(kEvSetup);
   const uint32_t tmem = ctl->tmem_base;
   const uint32_t tm_s0 = tmem, tm_o = tmem + kSBuf * 128;
 
-  if (warp == 0 || warp == 3) {
+  if (warp == 2) {
+    // ------------------------------------------------------------------ tile scheduler
+    // request tiles in the batch (lane-parallel over requests)
+    int total = 0;
+    for (int r0 = 0; r0 < a.num_reqs; r0 += 32) {
+      const int rr = r0 + lane;
+      const int q_len = rr < a.num_reqs ? __ldg(a.cu_seqlens_q + rr + 1) - __ldg(a.cu_seqlens_q + rr) : 0;
+      total += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>((q_len + kTok - 1) / kTok));
+    }
+    const int flat = total * a.num_kv_heads;
+    for (int k = 0, f = blockIdx.x;; ++k, f += gridDim.x) {
+      const int sl = k & 1;
+      TileDesc* d = &ctl->tile[sl];
+      // the slot's previous tile (k - 2) has been released by every role
+      bool go = true;
+      if (lane == 0 && k >= 2) go = wait_or_abort(&ctl->tile_empty[sl], ((k >> 1) - 1) & 1, ctl, a.err_word);
+      go = __shfl_sync(0xffffffffu, go, 0);
+      // once any CTA has given up on a wait, the rest of the grid does no work
+      if (lane == 0)
+        go = go && !aborted(ctl) &&
+             !(a.err_word != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err_word) & PBS_DEVERR_TIMEOUT) != 0);
+      go = __shfl_sync(0xffffffffu, go, 0);
+      const bool last = !go || f >= flat;
+      if (lane == 0) TRACET(kEvDesc0, k);
+      if (!last) describe_tile<kTok>(a, f, total, d, lane);
+      if (lane == 0 && last) d->end = 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->tile_full[sl]);
+      if (lane == 0) TRACET(kEvDesc, k);
+      if (last) break;
+      // the tile's Q, once the previous tile's S MMAs have read theirs
+      if (lane == 0 && (k == 0 || wait_or_abort(&ctl->q_empty, (k - 1) & 1, ctl, a.err_word))) {
+        mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+        tma_load_3d(q_s, &q_map, &ctl->q_full, 0, d->g * kG, d->t0);
+        tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, d->g * kG, d->t0);
+        TRACET(kEvQ, k);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------------ TMA producers
-    // Warp 0 loads the Q tile and streams the K of each union block, warp 3 its V: one 32 KiB
-    // copy per block (quarter coordinate 0 for K, 2 for V, from the block's first page).
+    // Warp 0 streams the K of each tile's union blocks, warp 3 their V: one 32 KiB copy per block
+    // (quarter coordinate 0 for K, 2 for V, from the block's first page).
     const bool is_k = warp == 0;
     if (is_k && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
-      mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
-      tma_load_3d(q_s, &q_map, &ctl->q_full, 0, g * kG, t0);
-      tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, g * kG, t0);
     }
     uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
     uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
     uint8_t* ring = is_k ? k_s : v_s;
     const int quarter = is_k ? 0 : 2;
-    const int32_t* bt_row = a.page_table + static_cast<int64_t>(req) * a.pt_row_stride;
-    int phys_lane = 0;
-    int issued = 0;
-    for (int i = 0; i < nU; ++i) {
-      const int st = i % kStagesTc;
-      if ((i & 31) == 0) phys_lane = i + lane < nU ? __ldg(bt_row + ctl->union_blk[i + lane]) : 0;
-      const int phys = __shfl_sync(0xffffffffu, phys_lane, i & 31);
-      bool go = true;
-      if (lane == 0 && i >= kStagesTc) go = wait_or_abort(&empty[st], ((i / kStagesTc) - 1) & 1, ctl, a.err_word);
-      if (lane == 0) go = go && !aborted(ctl);
+    int gb = 0;  // blocks this warp has issued, over the CTA's tiles
+    bool go = true;
+    for (int k = 0; go; ++k) {
+      const int sl = k & 1;
+      if (lane == 0) go = wait_or_abort(&ctl->tile_full[sl], (k >> 1) & 1, ctl, a.err_word);
       go = __shfl_sync(0xffffffffu, go, 0);
       if (!go) break;
-      const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
-      if (is_k && lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages))
-        set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-      uint8_t* dst = ring + st * kTileBytes;
-      if (is_k) TRACE(kEvProdIssue0 + i);
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
+      const TileDesc* d = &ctl->tile[sl];
+      if (d->end) break;
+      const int nU = d->n_union, g = d->g;
+      const int32_t* bt_row = a.page_table + static_cast<int64_t>(d->req) * a.pt_row_stride;
+      int phys_lane = 0;
+      for (int i = 0; go && i < nU; ++i, ++gb) {
+        const int st = gb % kStagesTc;
+        if ((i & 31) == 0) phys_lane = i + lane < nU ? __ldg(bt_row + d->union_blk[i + lane]) : 0;
+        const int phys = __shfl_sync(0xffffffffu, phys_lane, i & 31);
+        if (lane == 0 && gb >= kStagesTc) go = wait_or_abort(&empty[st], ((gb / kStagesTc) - 1) & 1, ctl, a.err_word);
+        if (lane == 0) go = go && !aborted(ctl);
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) break;
+        const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
+        if (is_k && lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages))
+          set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+        if (is_k) TRACEB(kEvProdIssue0, gb);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[st], kTileBytes);
+          // out-of-range pages read as zeros (TMA bounds)
+          tma_load_5d(ring + st * kTileBytes, &kv_map, &full[st], 0, 0, g, static_cast<int>(base), quarter);
+        }
+        if (is_k) TRACEB(kEvProdIssue1, gb);
+      }
       __syncwarp();
-      // out-of-range pages read as zeros (TMA bounds)
-      if (lane == 0) tma_load_5d(dst, &kv_map, &full[st], 0, 0, g, static_cast<int>(base), quarter);
-      if (is_k) TRACE(kEvProdIssue1 + i);
-      issued = i + 1;
+      if (lane == 0) mbar_arrive(&ctl->tile_empty[sl]);
     }
-    if (lane == 0) {
-      for (int i = max(0, issued - kStagesTc); i < issued; ++i)
-        if (!mbar_wait_bounded(&full[i % kStagesTc], (i / kStagesTc) & 1, kTcWaitNs))
-          set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-      if (is_k && !mbar_wait_bounded(&ctl->q_full, 0, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-    }
+    // every copy issued must land before the CTA exits
+    if (lane == 0)
+      for (int i = max(0, gb - kStagesTc); i < gb; ++i)
+        if (!mbar_wait_bounded(&full[i % kStagesTc], (i / kStagesTc) & 1, kTcWaitNs)) set_err(a.err_word, PBS_DEVERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
       constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
       const uint32_t q_addr = smem_u32(q_s);
-      bool ok = nU == 0 || wait_or_abort(&ctl->q_full, 0, ctl, a.err_word);
-      int issued_pv = 0;
-      // issue order S(0), S(1), S(2), PV(0), S(3), PV(1), ...: S runs two blocks ahead of PV, so
-      // the softmax of block i + 1 finds S(i + 1) done while PV(i - 1) is still queued. S(i) reuses
-      // buffer i % 3, whose last reader PV(i - 3) was issued before it.
-      for (int i = 0; ok && i < nU + 2; ++i) {
-        if (i < nU) {
-          const int st = i % kStagesTc, sb = i % kSBuf;
-          if (!wait_or_abort(&ctl->k_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) break;
+      int gs = 0, gp = 0;      // next block for S, for PV, over the CTA's tiles
+      uint32_t first = 0u;     // bit (i & 31): block i is its tile's first (its PV starts O afresh)
+      int prev_start = 0;      // first block of the previous tile
+      bool ok = true;
+      // O += P(j) V(j): in S buffer j % 3 each softmax part's 64 columns hold P hi (bf16, two keys
+      // per column) in their first 32 and P lo in their last 32
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j % kStagesTc, sb = j % kSBuf;
+        if (!wait_or_abort(&ctl->p_full[sb], (j / kSBuf) & 1, ctl, a.err_word)) return false;
+        if (!wait_or_abort(&ctl->v_full[st], (j / kStagesTc) & 1, ctl, a.err_word)) return false;
+        tc::fence_after_sync();
+        const uint32_t v_addr = smem_u32(v_s + st * kTileBytes);
+        const bool fresh = (first >> (j & 31)) & 1u;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            // keys 16ks..16ks+15 belong to softmax part `owner`
+            const int owner = (16 * ks) / kW;
+            const uint32_t pa = tm_s0 + sb * 128 + owner * kW + part * (kW / 2) + (16 * ks - owner * kW) / 2;
+            // keys 16ks..16ks+15 = two 8-key groups (1 KiB apart) from key group 2ks; dims in
+            // two 64-wide MN atoms 16 KiB apart
+            tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
+                       !(fresh && part == 0 && ks == 0));
+          }
+        }
+        tc::commit(&ctl->pv_done[sb]);
+        TRACEB(kEvPV, j);
+        tc::commit(&ctl->v_empty[st]);
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        const int sl = k & 1;
+        // Tile k's slot is tile k - 2's, which its softmax warps release only after that tile's
+        // last PV: blocks of tiles before the previous one (after tiles of fewer than two blocks)
+        // get their PV now instead of after two more S.
+        while (ok && gp < prev_start) {
+          if (!issue_pv(gp)) ok = false;
+          ++gp;
+        }
+        if (!ok || !wait_or_abort(&ctl->tile_full[sl], (k >> 1) & 1, ctl, a.err_word)) break;
+        const TileDesc* d = &ctl->tile[sl];
+        if (d->end) break;
+        const int nU = d->n_union;
+        // the previous tile's last PVs go before this tile's S: its epilogue, on the softmax
+        // warps' path, waits for them, while this tile's first S runs during that epilogue
+        while (ok && gp < gs) {
+          if (!issue_pv(gp)) ok = false;
+          ++gp;
+        }
+        if (!ok || !wait_or_abort(&ctl->q_full, k & 1, ctl, a.err_word)) break;
+        tc::fence_after_sync();
+        const int start = gs;
+        // issue order S(0), S(1), S(2), PV(0), S(3), PV(1), ... over the CTA's block sequence: S
+        // runs two blocks ahead of PV, so the softmax of block i + 1 finds S(i + 1) done while
+        // PV(i - 1) is still queued. S(i) reuses buffer i % 3, whose last reader PV(i - 3) was
+        // issued before it.
+        for (int i = 0; i < nU; ++i, ++gs) {
+          const int st = gs % kStagesTc, sb = gs % kSBuf;
+          if (!wait_or_abort(&ctl->k_full[st], (gs / kStagesTc) & 1, ctl, a.err_word)) {
+            ok = false;
+            break;
+          }
           tc::fence_after_sync();
           const uint32_t k_addr = smem_u32(k_s + st * kTileBytes);
 #pragma unroll
@@ -466,41 +569,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           }
           tc::commit(&ctl->s_full[sb]);
           tc::commit(&ctl->k_empty[st]);  // the K stage is free once S(i) has read it
-          TRACE(kEvS + i);
-        }
-        const int j = i - 2;
-        if (j >= 0) {
-          // O += P(j) V(j): in S buffer j % 3 each softmax part's 64 columns hold P hi (bf16, two
-          // keys per column) in their first 32 and P lo in their last 32
-          const int st = j % kStagesTc, sb = j % kSBuf;
-          if (!wait_or_abort(&ctl->p_full[sb], (j / kSBuf) & 1, ctl, a.err_word)) break;
-          if (!wait_or_abort(&ctl->v_full[st], (j / kStagesTc) & 1, ctl, a.err_word)) break;
-          tc::fence_after_sync();
-          const uint32_t v_addr = smem_u32(v_s + st * kTileBytes);
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              // keys 16ks..16ks+15 belong to softmax part `owner`
-              const int owner = (16 * ks) / kW;
-              const uint32_t pa = tm_s0 + sb * 128 + owner * kW + part * (kW / 2) + (16 * ks - owner * kW) / 2;
-              // keys 16ks..16ks+15 = two 8-key groups (1 KiB apart) from key group 2ks; dims in
-              // two 64-wide MN atoms 16 KiB apart
-              tc::mma_ts(tm_o, pa, tc::smem_desc_sw128(v_addr + ks * 2048, kHalf, 1024), kIdescPV,
-                         !(j == 0 && part == 0 && ks == 0));
+          TRACEB(kEvS, gs);
+          first = i == 0 ? (first | (1u << (gs & 31))) : (first & ~(1u << (gs & 31)));
+          if (gs - gp >= 2) {
+            if (!issue_pv(gp)) {
+              ok = false;
+              break;
             }
+            ++gp;
           }
-          tc::commit(&ctl->pv_done[sb]);
-          TRACE(kEvPV + j);
-          tc::commit(&ctl->v_empty[st]);
-          issued_pv = j + 1;
         }
+        // the tile's Q is free once its S MMAs have completed
+        tc::commit(&ctl->q_empty);
+        mbar_arrive(&ctl->tile_empty[sl]);
+        prev_start = start;
+      }
+      while (ok && gp < gs) {
+        if (!issue_pv(gp)) break;
+        ++gp;
       }
       // every MMA issued must complete before TMEM is released
-      if (issued_pv > 0)
-        mbar_wait_bounded(&ctl->pv_done[(issued_pv - 1) % kSBuf], ((issued_pv - 1) / kSBuf) & 1, kTcWaitNs);
+      if (gp > 0) mbar_wait_bounded(&ctl->pv_done[(gp - 1) % kSBuf], ((gp - 1) / kSBuf) & 1, kTcWaitNs);
+      if (gs > gp) mbar_wait_bounded(&ctl->s_full[(gs - 1) % kSBuf], ((gs - 1) / kSBuf) & 1, kTcWaitNs);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------------ softmax + epilogue
     // kSplit warps share each 32-lane quadrant of TMEM; warp part p owns S / O columns
     // [p*kW, p*kW + kW) of its 32 rows. Row maxima and sums are combined through shared memory.
@@ -508,153 +600,167 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int row = quad * 32 + lane;  // = TMEM lane
     const int col0 = part * kW;
     const int tt = row / kG, h = row % kG;
-    const bool live = tt < n_tok && !((ctl->bad_mask >> tt) & 1);
-    const int cnt_t = live ? ctl->cnt[tt] : 0;
-    const int own_t = ctl->own[tt], lim_t = ctl->lim[tt];
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = a.scale_log2;
-    const int last_blk = pos_last / kSparseBlock;
-    const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
-    float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
-    bool started = false;              // the row has had an active block (same in every part)
-    int ptr = 0;
-    bool ok = true;
-    // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
-    // the blocks, so the two warps of a quadrant always meet at the same named barriers.
-    for (int i = 0; i < nU; ++i) {
-      const int sb = i % kSBuf, st = i % kStagesTc;
-      const int b = ctl->union_blk[i];
-      while (ptr < cnt_t && ctl->tok_blk[tt][ptr] < b) ++ptr;
-      const bool active = ptr < cnt_t && ctl->tok_blk[tt][ptr] == b;
-      const int lim = b == own_t ? lim_t : kSparseBlock;
-      if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (i / kSBuf) & 1, ctl, a.err_word)) ok = false;
-      tc::fence_after_sync();
-      if (sw == 0 && lane == 0) TRACE(kEvSoftIn + i);
-      // rows past the request's last token in its last block may hold anything: zero that V
-      if (b == last_blk && last_rows < kSparseBlock) {
-        if (ok && !warp_wait_or_abort(&ctl->v_full[st], (i / kStagesTc) & 1, ctl, a.err_word)) ok = false;
-        const uint32_t v_base = smem_u32(v_s + st * kTileBytes);
-        for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
-          const int key = last_rows + (e >> 4), vq = (e >> 3) & 1, chunk = e & 7;
-          // key k of quarter vq at vq * 16 KiB + k * 128 B
-          sts128(v_base + vq * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
+    int gb = 0;  // blocks of the CTA's sequence this warp has processed
+    for (int k = 0;; ++k) {
+      const int sl = k & 1;
+      const bool got = warp_wait_or_abort(&ctl->tile_full[sl], (k >> 1) & 1, ctl, a.err_word);
+      const TileDesc* d = &ctl->tile[sl];
+      // both warps of the quadrant leave together (they meet at named barriers below)
+      if (quad_any(quad, !got || d->end != 0 || aborted(ctl))) break;
+      const int nU = d->n_union, n_tok = d->n_tok, t0 = d->t0, g = d->g;
+      if (sw == 0 && lane == 0) TRACET(kEvTileIn, k);
+      const bool live = tt < n_tok && !((d->bad_mask >> tt) & 1);
+      const int own_t = d->own[tt], lim_t = d->lim[tt];
+      const int pos_last = d->pos_last;
+      const int last_blk = pos_last / kSparseBlock;
+      const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
+      float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
+      bool started = false;              // the row has had an active block (same in every part)
+      bool ok = true;
+      // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
+      // the blocks, so the two warps of a quadrant always meet at the same named barriers.
+      for (int i = 0; i < nU; ++i, ++gb) {
+        const int sb = gb % kSBuf, st = gb % kStagesTc;
+        const int b = d->union_blk[i];
+        const bool active = live && ((d->blocks[tt][b >> 5] >> (b & 31)) & 1u);
+        const int lim = b == own_t ? lim_t : kSparseBlock;
+        if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (gb / kSBuf) & 1, ctl, a.err_word)) ok = false;
+        tc::fence_after_sync();
+        if (sw == 0 && lane == 0) TRACEB(kEvSoftIn, gb);
+        // rows past the request's last token in its last block may hold anything: zero that V
+        if (b == last_blk && last_rows < kSparseBlock) {
+          if (ok && !warp_wait_or_abort(&ctl->v_full[st], (gb / kStagesTc) & 1, ctl, a.err_word)) ok = false;
+          const uint32_t v_base = smem_u32(v_s + st * kTileBytes);
+          for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
+            const int key = last_rows + (e >> 4), vq = (e >> 3) & 1, chunk = e & 7;
+            // key k of quarter vq at vq * 16 KiB + k * 128 B
+            sts128(v_base + vq * kHalf + key * 128 + chunk * 16, 0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      const uint32_t ts = tm_s0 + sb * 128 + lane_off;
-      // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
-      // take part in this block are masked arithmetically (their P row becomes zero). Activity
-      // depends only on the row, so the kSplit warps of a quadrant always agree.
-      // Activity depends only on the row, so both warps of a quadrant take the same branches
-      // around the named barriers below.
-      if (__any_sync(0xffffffffu, active)) {
-        const int nval = active ? min(max(lim - col0, 0), kW) : 0;  // valid keys among my columns
-        // a part whose columns hold no valid key (they may lie past the last token) writes zeros
-        const bool any_valid = __any_sync(0xffffffffu, nval > 0);
-        uint32_t v[kW];
-        bool prefix = false;
-        float pm = -INFINITY, psum = 0.f;
-        if (any_valid) {
+        const uint32_t ts = tm_s0 + sb * 128 + lane_off;
+        // tcgen05.ld / st are warp-collective: every lane of the warp issues them; rows that do not
+        // take part in this block are masked arithmetically (their P row becomes zero). Activity
+        // depends only on the row, so the kSplit warps of a quadrant always agree and take the same
+        // branches around the named barriers below.
+        if (__any_sync(0xffffffffu, active)) {
+          const int nval = active ? min(max(lim - col0, 0), kW) : 0;  // valid keys among my columns
+          // a part whose columns hold no valid key (they may lie past the last token) writes zeros
+          const bool any_valid = __any_sync(0xffffffffu, nval > 0);
+          uint32_t v[kW];
+          bool prefix = false;
+          float pm = -INFINITY, psum = 0.f;
+          if (any_valid) {
 #pragma unroll
-          for (int c = 0; c < kW / 32; ++c) tc::ld32(ts + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-          tc::wait_ld();
-          prefix = __any_sync(0xffffffffu, nval != 0 && nval != kW);
-          // P with the running reference (the common case), and this part's maximum
-          psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm)
-                        : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm);
+            for (int c = 0; c < kW / 32; ++c) tc::ld32(ts + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+            tc::wait_ld();
+            prefix = __any_sync(0xffffffffu, nval != 0 && nval != kW);
+            // P with the running reference (the common case), and this part's maximum
+            psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm)
+                          : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm);
+          } else {
+            zero_p(ts + col0, ts + col0 + kW / 2);
+          }
+          ctl->xchg[part][row] = pm;
+          quad_bar(quad);
+          float mx = pm;
+#pragma unroll
+          for (int q = 0; q < kSplit; ++q) mx = fmaxf(mx, ctl->xchg[q][row]);
+          quad_bar(quad);  // every part has read before the next block overwrites
+          if (sw == 0 && lane == 0) TRACEB(kEvSoftMax, gb);
+          mx *= sl2;
+          // the reference moves only when the row maximum passes it by 2^8 (or on the row's first
+          // block); then O is rescaled and this block's P recomputed
+          const bool grow = active && (m_ref == -INFINITY || mx > m_ref + kRescaleLog2);
+          if (__any_sync(0xffffffffu, grow)) {
+            const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
+            // O's dim columns hold contributions of every key part once the row has started
+            const bool resc = grow && started;
+            const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+            if (__any_sync(0xffffffffu, resc)) {
+              // O holds this tile's PV(i-1) once that completes (S(i) done implies PV(i-2) done)
+              if (ok && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
+                ok = false;
+              tc::fence_after_sync();
+#pragma unroll
+              for (int c = 0; c < kW / 32; ++c) {
+                uint32_t o[32];
+                tc::ld32(tm_o + lane_off + col0 + 32 * c, o);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tc::st32(tm_o + lane_off + col0 + 32 * c, o);
+              }
+            }
+            l *= alpha;
+            m_ref = m_new;
+            if (any_valid) {
+              float unused;
+              psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused)
+                            : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused);
+            }
+          }
+          l += psum;
+          started = started || active;
         } else {
           zero_p(ts + col0, ts + col0 + kW / 2);
         }
-        ctl->xchg[part][row] = pm;
-        quad_bar(quad);
-        float mx = pm;
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
+        if (sw == 0 && lane == 0) TRACEB(kEvSoftOut, gb);
+      }
+      if (sw == 0 && lane == 0) TRACE(kEvEpi);
+      // ---- epilogue: O / l -> bf16 (row sum combined over the parts of the quadrant). The next
+      // tile's first PV, which starts O afresh, waits for this warp's arrival on its P.
+      if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
+        ok = false;
+      tc::fence_after_sync();
+      ctl->xchg[part][row] = l;
+      quad_bar(quad);
+      float lsum = 0.f;
 #pragma unroll
-        for (int q = 0; q < kSplit; ++q) mx = fmaxf(mx, ctl->xchg[q][row]);
-        quad_bar(quad);  // every part has read before the next block overwrites
-        if (sw == 0 && lane == 0) TRACE(kEvSoftMax + i);
-        mx *= sl2;
-        // the reference moves only when the row maximum passes it by 2^8 (or on the row's first
-        // block); then O is rescaled and this block's P recomputed
-        const bool grow = active && (m_ref == -INFINITY || mx > m_ref + kRescaleLog2);
-        if (__any_sync(0xffffffffu, grow)) {
-          const float m_new = grow ? fmaxf(mx, m_ref) : m_ref;
-          // O's dim columns hold contributions of every key part once the row has started
-          const bool resc = grow && started;
-          const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
-          if (__any_sync(0xffffffffu, resc)) {
-            // O holds PV(i-1) once that completes (S(i) done implies PV(i-2) done)
-            if (ok && i > 0 && !warp_wait_or_abort(&ctl->pv_done[(i - 1) % kSBuf], ((i - 1) / kSBuf) & 1, ctl, a.err_word))
-              ok = false;
-            tc::fence_after_sync();
+      for (int q = 0; q < kSplit; ++q) lsum += ctl->xchg[q][row];
+      quad_bar(quad);  // every part has read before the next tile's first block overwrites
+      {
+        // warp-collective TMEM reads for every lane; only rows of real tokens are stored
+        uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
+                        static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
+        const float inv = (live && lsum > 0.f && ok) ? a.v_scale / lsum : 0.f;
+        // p = 2^(t - m_ref), so the row's base-2 log-sum-exp is m_ref + log2(sum p)
+        if (a.lse != nullptr && part == 0 && tt < n_tok)
+          a.lse[static_cast<int64_t>(t0 + tt) * a.lse_row_stride + g * kG + h] =
+              (live && lsum > 0.f && ok) ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kW / 32; ++c) {
-              uint32_t o[32];
-              tc::ld32(tm_o + lane_off + col0 + 32 * c, o);
-              tc::wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tc::st32(tm_o + lane_off + col0 + 32 * c, o);
-            }
+        for (int c = 0; c < kW / 32; ++c) {
+          uint32_t v[32];
+          if (nU > 0) {
+            tc::ld32(tm_o + lane_off + col0 + 32 * c, v);
+            tc::wait_ld();
           }
-          l *= alpha;
-          m_ref = m_new;
-          if (any_valid) {
-            float unused;
-            psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused)
-                          : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float o0 = nU > 0 ? __uint_as_float(v[j]) * inv : 0.f;
+            const float o1 = nU > 0 ? __uint_as_float(v[j + 1]) * inv : 0.f;
+            w[j >> 1] = pack_bf16(o0, o1);
+          }
+          if (tt < n_tok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
           }
         }
-        l += psum;
-        started = started || active;
-      } else {
-        zero_p(ts + col0, ts + col0 + kW / 2);
       }
-      tc::wait_st();
+      // O has been read: the next tile's PVs may overwrite it (they wait for this warp's P)
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
-      if (sw == 0 && lane == 0) TRACE(kEvSoftOut + i);
-    }
-    if (sw == 0 && lane == 0) TRACE(kEvEpi);
-    // ---- epilogue: O / l -> bf16 (row sum combined over the parts of the quadrant)
-    if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(nU - 1) % kSBuf], ((nU - 1) / kSBuf) & 1, ctl, a.err_word))
-      ok = false;
-    tc::fence_after_sync();
-    ctl->xchg[part][row] = l;
-    quad_bar(quad);
-    float lsum = 0.f;
-#pragma unroll
-    for (int q = 0; q < kSplit; ++q) lsum += ctl->xchg[q][row];
-    {
-      // warp-collective TMEM reads for every lane; only rows of real tokens are stored
-      uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
-                      static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
-      const float inv = (live && lsum > 0.f && ok) ? a.v_scale / lsum : 0.f;
-      // p = 2^(t - m_ref), so the row's base-2 log-sum-exp is m_ref + log2(sum p)
-      if (a.lse != nullptr && part == 0 && tt < n_tok)
-        a.lse[static_cast<int64_t>(t0 + tt) * a.lse_row_stride + g * kG + h] =
-            (live && lsum > 0.f && ok) ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kW / 32; ++c) {
-        uint32_t v[32];
-        if (nU > 0) {
-          tc::ld32(tm_o + lane_off + col0 + 32 * c, v);
-          tc::wait_ld();
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float o0 = nU > 0 ? __uint_as_float(v[j]) * inv : 0.f;
-          const float o1 = nU > 0 ? __uint_as_float(v[j + 1]) * inv : 0.f;
-          w[j >> 1] = pack_bf16(o0, o1);
-        }
-        if (tt < n_tok) {
-          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&ctl->tile_empty[sl]);
+      if (sw == 0 && lane == 0) TRACET(kEvTileOut, k);
     }
   }
   tc::fence_before_sync();
@@ -675,6 +781,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_set(int cta) {
   return cudaMemcpyToSymbol(pbs::g_trace_cta, &cta, sizeof(int)) == cudaSuccess ? 0 : 5;
 }
+extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_window(int b0) {
+  return cudaMemcpyToSymbol(pbs::g_trace_b0, &b0, sizeof(int)) == cudaSuccess ? 0 : 5;
+}
 extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_get(long long* host, int n) {
   if (n > pbs::kEvCount) n = pbs::kEvCount;
   return cudaMemcpyFromSymbol(host, pbs::g_trace, sizeof(long long) * n) == cudaSuccess ? 0 : 5;
@@ -683,7 +792,7 @@ namespace pbs {
 #endif
 
 bool prefill_tc_supported(const AttendArgs& a) {
-  return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.k <= kTcMaxTopk && a.max_blocks <= 65536 &&
+  return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.k <= kTcMaxTopk && a.max_blocks <= kMaxUnion &&
          a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
          a.num_pages * a.num_kv_heads <= 0x7fffffffLL &&
          a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
@@ -696,10 +805,14 @@ cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUte
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kTcSmem));
   if (e != cudaSuccess) return e;
-  // tiles are numbered request by request; the grid is an upper bound and surplus CTAs exit
-  const unsigned tiles = static_cast<unsigned>(a.num_rows / (kRows / kG) + a.num_reqs + 1);
-  prefill_tc_kernel<kG><<<dim3(tiles, static_cast<unsigned>(a.num_kv_heads)), kThreadsTc, kTcSmem, stream>>>(
-      kv_map, q_map, a);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM; at most one per tile (an upper bound: tiles are counted on the device)
+  const int64_t tiles = (static_cast<int64_t>(a.num_rows) / (kRows / kG) + a.num_reqs + 1) * a.num_kv_heads;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(std::max(sms, 1), tiles));
+  prefill_tc_kernel<kG><<<grid, kThreadsTc, kTcSmem, stream>>>(kv_map, q_map, a);
   return cudaGetLastError();
 }
 
