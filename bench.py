@@ -238,7 +238,7 @@ def run_decode(pbs, b, steps, warmup, flush, stream):
     return time_steps(step, steps, warmup, flush, stream)
 
 
-def run_prefill(pbs, b, steps, warmup, flush, stream, workspace=None):
+def run_prefill(pbs, b, steps, warmup, flush, stream, workspace="auto"):
     p = b.pre
     out = torch.empty_like(p.q)
 
@@ -319,6 +319,10 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     t = statistics.median(ts)
     res["prefill_varlen_bf16"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                   "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16, "algorithmic_tflop": fl / 1e12}
+    # the same call without a workspace: the tile kernel applies bf16 P as hi + lo parts
+    t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=None))
+    res["prefill_varlen_bf16_no_workspace"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
+                                               "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16}
     # the same call on the gathered-row kernel (opt-in; 2 GiB workspace, three token segments)
     os.environ["PBS_PREFILL_KERNEL"] = "gather"
     try:

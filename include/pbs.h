@@ -233,10 +233,15 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
  *               and out rows) run on it: per-block partial outputs and the per-window token buckets
  *               live in the workspace, and the call is processed in as many token segments as its
  *               size requires (pbs_prefill_workspace_bytes(total_q, ...) bytes: one segment).
- *               Otherwise the tcgen05 tile kernel or the token-centric kernel runs; the latter
- *               merges split rows through the workspace when it holds pbs_attend_workspace_bytes
- *               (zeroed before first use, as described there) and ignores a smaller one.
- *               Calls that share one workspace must not run concurrently.
+ *               Otherwise the tcgen05 tile kernel or the token-centric kernel runs. The tile
+ *               kernel, given a 256-byte aligned workspace of at least
+ *               pbs_prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks) bytes, first
+ *               converts the V of every (request, block, kv head) the call can read to fp16 there
+ *               (V * 2^-e per block, exact) and then applies P in fp16, one MMA per 16 keys;
+ *               without it, it applies bf16 P as hi + lo parts (two MMAs, same accuracy). The
+ *               token-centric kernel merges split rows through the workspace when it holds
+ *               pbs_attend_workspace_bytes (zeroed before first use, as described there) and
+ *               ignores a smaller one. Calls that share one workspace must not run concurrently.
  */
 PBS_API int pbs_sparse_prefill_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -261,6 +266,14 @@ PBS_API int pbs_sparse_prefill_attention(
  */
 PBS_API size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads,
                                            int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks);
+
+/*
+ * Bytes of the workspace with which pbs_sparse_prefill_attention's tcgen05 tile kernel runs its
+ * fp16-V path: num_reqs * max_blocks * num_kv_heads converted V blocks of 32 KiB plus one int32
+ * exponent each (rounded up to 256 bytes); 0 for invalid arguments or max_blocks > 128 (the tile
+ * kernel's limit). No counterpart on the pages.
+ */
+PBS_API size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks);
 
 /*
  * Mixed batch in one call ([flashinfer] forward with both parts: decode rows q[:nd], prefill

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
     L.pbs_attend_workspace_bytes.argtypes = [i64, i32, i32]
     L.pbs_prefill_workspace_bytes.restype = ctypes.c_size_t
     L.pbs_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.pbs_prefill_tile_workspace_bytes.restype = ctypes.c_size_t
+    L.pbs_prefill_tile_workspace_bytes.argtypes = [i32, i32, i32]
     table_common = [vp, i64, i32, i32, vp, i64, i32]
     L.pbs_build_sparse_block_table_decode.restype = ctypes.c_int
     L.pbs_build_sparse_block_table_decode.argtypes = table_common + [vp, i32, i32, i32, vp, i64, vp, vp, vp]
@@ -269,6 +271,35 @@ def prefill_workspace_bytes(total_q: int, num_reqs: int, num_heads: int, num_kv_
                                                  int(topk), int(max_blocks)))
 
 
+def prefill_tile_workspace_bytes(num_reqs: int, num_kv_heads: int, max_blocks: int) -> int:
+    """Bytes with which the prefill attend's tcgen05 tile kernel converts V to fp16 once per
+    (request, block, kv head) and applies P in fp16 (0: the tile kernel cannot take this shape)."""
+    return int(lib().pbs_prefill_tile_workspace_bytes(int(num_reqs), int(num_kv_heads), int(max_blocks)))
+
+
+# the tile kernel's converted-V workspace is allocated by default up to this size
+TILE_WORKSPACE_CAP = 1 << 30
+_tile_workspaces: dict = {}
+
+
+def prefill_tile_workspace(num_reqs: int, num_kv_heads: int, max_blocks: int, device, stream=None):
+    """The tile kernel's converted-V workspace, cached per (device, stream) and grown on demand;
+    None when the shape does not take it or it would exceed ``TILE_WORKSPACE_CAP`` (the kernel
+    then applies bf16 P as hi + lo parts). Needs no initial value."""
+    need = prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks)
+    if need == 0 or need > TILE_WORKSPACE_CAP:
+        return None
+    device = torch.device(device)
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device.index, s.cuda_stream)
+    ws = _tile_workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        _tile_workspaces[key] = ws = None
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        _tile_workspaces[key] = ws
+    return ws
+
+
 # the default prefill workspace is capped; larger calls run in several token segments
 PREFILL_WORKSPACE_CAP = 2 << 30
 _prefill_workspaces: dict = {}
@@ -359,20 +390,24 @@ def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: in
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                              block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                             workspace=None, lse=None, return_lse: bool = False):
+                             workspace="auto", lse=None, return_lse: bool = False):
     """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
 
-    ``workspace``: None (the default: the tcgen05 tile kernel or the token-centric kernel, no
-    scratch), "auto" (a cached per-stream buffer from :func:`prefill_workspace`, which the
-    gathered-row kernel needs; that kernel runs when PBS_PREFILL_KERNEL=gather) or a uint8 CUDA
-    tensor (see ``pbs_sparse_prefill_attention`` in include/pbs.h for how each kernel uses it).
-    ``lse`` and ``return_lse`` as in :func:`sparse_decode_attention`."""
+    ``workspace``: "auto" (the default: a cached per-stream buffer, from :func:`prefill_workspace`
+    when PBS_PREFILL_KERNEL=gather asks for the gathered-row kernel, else the tile kernel's
+    converted-V buffer from :func:`prefill_tile_workspace`), None (no scratch: the tile kernel
+    applies bf16 P as hi + lo parts) or a uint8 CUDA tensor (see ``pbs_sparse_prefill_attention``
+    in include/pbs.h for how each kernel uses it). ``lse`` and ``return_lse`` as in
+    :func:`sparse_decode_attention`."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     if isinstance(workspace, str) and workspace == "auto":
-        workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1], pt.shape[1],
-                                      q.device, stream)
+        if os.environ.get("PBS_PREFILL_KERNEL") == "gather":
+            workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
+                                          pt.shape[1], q.device, stream)
+        else:
+            workspace = prefill_tile_workspace(sl.shape[0], num_kv_heads, pt.shape[1], q.device, stream)
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
     st = lib().pbs_sparse_prefill_attention(

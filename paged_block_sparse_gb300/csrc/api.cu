@@ -398,7 +398,7 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 6; }
+int pbs_abi_version(void) { return 7; }
 
 size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
   if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
@@ -618,10 +618,24 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride,
                       kernel == kPrefillGather ? 1 : 0);
     if (st != PBS_OK) return st;
+    if (kernel == kPrefillTile && workspace != nullptr && aligned(workspace, 256) && num_reqs <= 65535) {
+      // with room for the converted V of every (request, block, kv head), the tile kernel applies
+      // P in fp16 with one MMA per 16 keys instead of bf16 hi + lo
+      const size_t need = pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks);
+      if (need != 0 && workspace_bytes >= need) {
+        a.vconv = static_cast<uint8_t*>(workspace);
+        a.vconv_exp = reinterpret_cast<int32_t*>(a.vconv + static_cast<int64_t>(num_reqs) * max_blocks * num_kv_heads *
+                                                              pbs::kTileVBytes);
+      }
+    }
     e = kernel == kPrefillGather ? pbs::launch_prefill_gather(a, half_map, qmap, workspace, workspace_bytes, cs)
                                  : pbs::launch_prefill_tc(a, half_map, qmap, cs);
   }
   return e == cudaSuccess ? PBS_OK : PBS_ERR_CUDA;
+}
+
+size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks) {
+  return pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks);
 }
 
 size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads, int32_t num_kv_heads,

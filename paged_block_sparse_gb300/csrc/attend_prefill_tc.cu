@@ -61,6 +61,10 @@ constexpr int kMaxUnion = 128;    // union blocks per tile: the kernel takes pag
 constexpr int kSetWords = kMaxUnion / 32;
 constexpr int kTcMaxTopk = 16;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
+// fp16-V path: P' = P * 2^(e_b - E) in fp16. P <= 2^8 under the lazy rescale, so e_b - E <= 7 keeps
+// P' below 2^15; below -8 the block's largest weights would leave fp16's normal range. Outside
+// that window E moves to e_b and O is rescaled by the power of two.
+constexpr int kExpUp = 7, kExpDown = -8;
 
 // One tile, described by the scheduler warp for the other roles (two slots, used alternately).
 struct TileDesc {
@@ -72,6 +76,7 @@ struct TileDesc {
   int16_t lim[kTokMax];              // keys of the own block the token sees
   uint16_t union_blk[kMaxUnion];      // the tile's distinct valid blocks, increasing
   uint32_t blocks[kTokMax][kSetWords];  // bit b: the token selected block b (valid and causal)
+  int8_t vexp[kMaxUnion];             // fp16-V path: union block u's V image is V * 2^-vexp[u]
 };
 
 // Roles that read a tile slot and release it: the two TMA warps, the MMA thread, the softmax warps.
@@ -182,6 +187,65 @@ __device__ __forceinline__ void zero_p(uint32_t t_hi, uint32_t t_lo) {
   }
 }
 
+// fp16-V path: p = 2^(s * sl2 - m) for the thread's kW keys as fp16 pairs over the first kW / 2
+// of its own S columns; otherwise as write_p.
+template <bool kPrefix>
+__device__ __forceinline__ float write_p16(const uint32_t (&v)[kW], int nval, float sl2, float m, uint32_t t_p,
+                                           float& smax) {
+  float psum0 = 0.f, psum1 = 0.f, mx = -INFINITY;
+  const float mu = (!kPrefix && nval == 0) ? INFINITY : m;
+#pragma unroll
+  for (int c = 0; c < kW / 32; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const int k = 32 * c + j;
+      float s0 = __uint_as_float(v[k]), s1 = __uint_as_float(v[k + 1]);
+      float p0, p1;
+      if (kPrefix) {
+        s0 = k < nval ? s0 : -INFINITY;
+        s1 = k + 1 < nval ? s1 : -INFINITY;
+        p0 = k < nval ? ex2(fmaf(s0, sl2, -mu)) : 0.f;
+        p1 = k + 1 < nval ? ex2(fmaf(s1, sl2, -mu)) : 0.f;
+      } else {
+        p0 = ex2(fmaf(s0, sl2, -mu));
+        p1 = ex2(fmaf(s1, sl2, -mu));
+      }
+      mx = fmaxf(mx, fmaxf(s0, s1));
+      psum0 += p0;
+      psum1 += p1;
+      pk[j >> 1] = pack_f16(p0, p1);
+    }
+    tc::st16(t_p + 16 * c, pk);
+  }
+  smax = (!kPrefix && nval == 0) ? -INFINITY : mx;
+  return psum0 + psum1;
+}
+
+__device__ __forceinline__ void zero_p16(uint32_t t_p) {
+  uint32_t z[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) z[j] = 0u;
+#pragma unroll
+  for (int c = 0; c < kW / 32; ++c) tc::st16(t_p + 16 * c, z);
+}
+
+// 2^n as a float, exact for -126 <= n <= 127.
+__device__ __forceinline__ float exp2i(int n) { return __uint_as_float(static_cast<uint32_t>(127 + n) << 23); }
+
+// O columns [col, col + kW) of this warp's 32 rows times f.
+__device__ __forceinline__ void scale_o(uint32_t t_o, float f) {
+#pragma unroll
+  for (int c = 0; c < kW / 32; ++c) {
+    uint32_t o[32];
+    tc::ld32(t_o + 32 * c, o);
+    tc::wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+    tc::st32(t_o + 32 * c, o);
+  }
+}
+
 __device__ __forceinline__ void quad_bar(int quad) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + quad), "r"(32 * kSplit) : "memory");
 }
@@ -238,10 +302,71 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
 
 __device__ __forceinline__ bool aborted(TcCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
 
+// fp16-V path, before the attend: the V of block b of request r and kv head g (CTA (b, r, g))
+// as the 32 KiB shared-memory image a V stage holds ([64-dim quarter][128 keys][128 B], 128B
+// swizzle: 16-byte chunk c of key k at chunk c ^ (k % 8)), in fp16 as V * 2^-e with e putting
+// the block's max |V| at 2^14..2^15 (exact: bf16 has 8 significant bits and fp16 keeps 28
+// binades below its maximum normal). Keys past the request's last token, or on pages past the
+// cache, become zeros. Thread t converts key t.
+__global__ void __launch_bounds__(128) convert_v_kernel(const AttendArgs a) {
+  const int b = blockIdx.x, r = blockIdx.y, g = blockIdx.z, t = threadIdx.x;
+  const int seq_len = __ldg(a.seq_lens + r);
+  if (b * kSparseBlock >= seq_len) return;  // no token of the request sees this block
+  const int nv = min(kSparseBlock, seq_len - b * kSparseBlock);
+  const int64_t page = static_cast<int64_t>(__ldg(a.page_table + static_cast<int64_t>(r) * a.pt_row_stride + b)) *
+                           a.block_page_stride + t / kPageRows;
+  const bool in_cache = page >= 0 && page < a.num_pages;
+  if (t < nv && !in_cache) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+  uint32_t x[16][4];
+  uint32_t mx2 = 0u;
+  if (t < nv && in_cache) {
+    // the V half (bytes 256..511) of the key's 512-byte row of this kv head
+    const uint4* src = reinterpret_cast<const uint4*>(a.kv_cache + page * a.page_stride_bytes + g * 8192 +
+                                                      (t % kPageRows) * 512 + 256);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 u = __ldg(src + c);
+      x[c][0] = u.x;
+      x[c][1] = u.y;
+      x[c][2] = u.z;
+      x[c][3] = u.w;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) x[c][0] = x[c][1] = x[c][2] = x[c][3] = 0u;
+  }
+  // |bf16| bit patterns compare like the magnitudes
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mx2 = max(mx2, max((x[c][q] & 0x7fff7fffu) >> 16, x[c][q] & 0x7fffu));
+  __shared__ uint32_t wmax[4];
+  uint32_t mx = __reduce_max_sync(0xffffffffu, mx2);
+  if ((t & 31) == 0) wmax[t >> 5] = mx;
+  __syncthreads();
+  mx = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
+  const float vm = __uint_as_float(mx << 16);
+  int e = 0;
+  if (vm > 0.f) e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 127 - 14;
+  e = max(-100, min(100, e));
+  const float sc = exp2i(-e);
+  uint8_t* dst = a.vconv + ((static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g) * kTileBytes;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int q = c >> 3, c8 = c & 7;
+    *reinterpret_cast<uint4*>(dst + q * kHalf + t * 128 + ((c8 ^ (t & 7)) << 4)) =
+        make_uint4(pack_f16(bf16_lo(x[c][0]) * sc, bf16_hi(x[c][0]) * sc),
+                   pack_f16(bf16_lo(x[c][1]) * sc, bf16_hi(x[c][1]) * sc),
+                   pack_f16(bf16_lo(x[c][2]) * sc, bf16_hi(x[c][2]) * sc),
+                   pack_f16(bf16_lo(x[c][3]) * sc, bf16_hi(x[c][3]) * sc));
+  }
+  if (t == 0) a.vconv_exp[(static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g] = e;
+}
+
 // Scheduler warp: describes tile f of the CTA's list in slot d. Flat tile f is kv head f % Hkv of
 // request tile (tiles - 1 - f / Hkv), request tiles numbered request by request: the list starts
 // at the last request's last tiles, whose tokens see the most blocks.
-template <int kTok>
+template <int kTok, bool kF16V>
 __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int total_tiles, TileDesc* d, int lane) {
   const int g = f % a.num_kv_heads;
   const int rt = total_tiles - 1 - f / a.num_kv_heads;
@@ -327,7 +452,13 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
 #pragma unroll
   for (int w = 0; w < kSetWords; ++w) {
     const uint32_t word = __reduce_or_sync(0xffffffffu, w == 0 ? m0 : w == 1 ? m1 : w == 2 ? m2 : m3);
-    if ((word >> lane) & 1u) d->union_blk[nu + __popc(word & ((1u << lane) - 1u))] = static_cast<uint16_t>(32 * w + lane);
+    if ((word >> lane) & 1u) {
+      const int u = nu + __popc(word & ((1u << lane) - 1u)), b = 32 * w + lane;
+      d->union_blk[u] = static_cast<uint16_t>(b);
+      if (kF16V)
+        d->vexp[u] = static_cast<int8_t>(
+            __ldg(a.vconv_exp + (static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g));
+    }
     nu += __popc(word);
   }
   if (lane == 0) {
@@ -348,7 +479,7 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
 // rings, the S buffers and the MMA order run on across tile boundaries (block counters count
 // the CTA's whole block sequence), so the next tile's S runs while the softmax warps finish the
 // previous tile, and its description, Q tile and first K / V blocks are ready before they do.
-template <int kG>
+template <int kG, bool kF16V>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const AttendArgs a) {
@@ -421,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       go = __shfl_sync(0xffffffffu, go, 0);
       const bool last = !go || f >= flat;
       if (lane == 0) TRACET(kEvDesc0, k);
-      if (!last) describe_tile<kTok>(a, f, total, d, lane);
+      if (!last) describe_tile<kTok, kF16V>(a, f, total, d, lane);
       if (lane == 0 && last) d->end = 1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->tile_full[sl]);
@@ -439,7 +570,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------------ TMA producers
     // Warp 0 streams the K of each tile's union blocks, warp 3 their V: one 32 KiB copy per block
-    // (quarter coordinate 0 for K, 2 for V, from the block's first page).
+    // (quarter coordinate 0 for K, 2 for V, from the block's first page; on the fp16-V path V is
+    // the block's converted image, one bulk copy).
     const bool is_k = warp == 0;
     if (is_k && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
@@ -475,8 +607,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (is_k) TRACEB(kEvProdIssue0, gb);
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[st], kTileBytes);
-          // out-of-range pages read as zeros (TMA bounds)
-          tma_load_5d(ring + st * kTileBytes, &kv_map, &full[st], 0, 0, g, static_cast<int>(base), quarter);
+          if (kF16V && !is_k)
+            bulk_load(ring + st * kTileBytes,
+                      a.vconv + ((static_cast<int64_t>(d->req) * a.max_blocks + d->union_blk[i]) * a.num_kv_heads + g) *
+                                    kTileBytes,
+                      kTileBytes, &full[st]);
+          else  // out-of-range pages read as zeros (TMA bounds)
+            tma_load_5d(ring + st * kTileBytes, &kv_map, &full[st], 0, 0, g, static_cast<int>(base), quarter);
         }
         if (is_k) TRACEB(kEvProdIssue1, gb);
       }
@@ -491,14 +628,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
-      constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, true, false, true);
+      constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, !kF16V, false, true);  // bf16, or fp16 P and V
       const uint32_t q_addr = smem_u32(q_s);
       int gs = 0, gp = 0;      // next block for S, for PV, over the CTA's tiles
       uint32_t first = 0u;     // bit (i & 31): block i is its tile's first (its PV starts O afresh)
       int prev_start = 0;      // first block of the previous tile
       bool ok = true;
       // O += P(j) V(j): in S buffer j % 3 each softmax part's 64 columns hold P hi (bf16, two keys
-      // per column) in their first 32 and P lo in their last 32
+      // per column) in their first 32 and P lo in their last 32; on the fp16-V path the first 32
+      // hold P as fp16 pairs and one MMA per 16 keys does
       auto issue_pv = [&](int j) -> bool {
         const int st = j % kStagesTc, sb = j % kSBuf;
         if (!wait_or_abort(&ctl->p_full[sb], (j / kSBuf) & 1, ctl, a.err_word)) return false;
@@ -507,7 +645,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t v_addr = smem_u32(v_s + st * kTileBytes);
         const bool fresh = (first >> (j & 31)) & 1u;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        for (int part = 0; part < (kF16V ? 1 : 2); ++part) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             // keys 16ks..16ks+15 belong to softmax part `owner`
@@ -618,6 +756,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
       float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
       bool started = false;              // the row has had an active block (same in every part)
+      int E = 0;                         // fp16-V path: O holds sum(P V) * 2^-E (set by the first block)
       bool ok = true;
       // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
       // the blocks, so the two warps of a quadrant always meet at the same named barriers.
@@ -629,8 +768,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (gb / kSBuf) & 1, ctl, a.err_word)) ok = false;
         tc::fence_after_sync();
         if (sw == 0 && lane == 0) TRACEB(kEvSoftIn, gb);
+        // fp16-V path: this block's P' = P * 2^de; E is CTA-uniform, so every warp moves it (and
+        // rescales its O columns) at the same block
+        int de = 0;
+        if (kF16V) {
+          const int eb = d->vexp[i];
+          if (i == 0) E = eb;
+          if (eb - E > kExpUp || eb - E < kExpDown) {
+            // O holds this tile's PV(i-1) once that completes (S(i) done implies PV(i-2) done)
+            if (ok && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
+              ok = false;
+            tc::fence_after_sync();
+            scale_o(tm_o + lane_off + col0, exp2i(E - eb));
+            tc::wait_st();
+            E = eb;
+          }
+          de = eb - E;
+        }
+        const float unshift = exp2i(-de);  // psum' * 2^-de = psum
         // rows past the request's last token in its last block may hold anything: zero that V
-        if (b == last_blk && last_rows < kSparseBlock) {
+        // (the converted images already hold zeros there)
+        if (!kF16V && b == last_blk && last_rows < kSparseBlock) {
           if (ok && !warp_wait_or_abort(&ctl->v_full[st], (gb / kStagesTc) & 1, ctl, a.err_word)) ok = false;
           const uint32_t v_base = smem_u32(v_s + st * kTileBytes);
           for (int e = sw * 32 + lane; e < (kSparseBlock - last_rows) * 16; e += 32 * kSoftWarps) {
@@ -658,8 +816,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::wait_ld();
             prefix = __any_sync(0xffffffffu, nval != 0 && nval != kW);
             // P with the running reference (the common case), and this part's maximum
-            psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm)
-                          : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm);
+            if (kF16V)
+              psum = prefix ? write_p16<true>(v, nval, sl2, m_ref - de, ts + col0, pm)
+                            : write_p16<false>(v, nval, sl2, m_ref - de, ts + col0, pm);
+            else
+              psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm)
+                            : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, pm);
+          } else if (kF16V) {
+            zero_p16(ts + col0);
           } else {
             zero_p(ts + col0, ts + col0 + kW / 2);
           }
@@ -684,26 +848,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               if (ok && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
                 ok = false;
               tc::fence_after_sync();
-#pragma unroll
-              for (int c = 0; c < kW / 32; ++c) {
-                uint32_t o[32];
-                tc::ld32(tm_o + lane_off + col0 + 32 * c, o);
-                tc::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                tc::st32(tm_o + lane_off + col0 + 32 * c, o);
-              }
+              scale_o(tm_o + lane_off + col0, alpha);
             }
             l *= alpha;
             m_ref = m_new;
             if (any_valid) {
               float unused;
-              psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused)
-                            : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused);
+              if (kF16V)
+                psum = prefix ? write_p16<true>(v, nval, sl2, m_ref - de, ts + col0, unused)
+                              : write_p16<false>(v, nval, sl2, m_ref - de, ts + col0, unused);
+              else
+                psum = prefix ? write_p<true>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused)
+                              : write_p<false>(v, nval, sl2, m_ref, ts + col0, ts + col0 + kW / 2, unused);
             }
           }
-          l += psum;
+          l += psum * unshift;
           started = started || active;
+        } else if (kF16V) {
+          zero_p16(ts + col0);
         } else {
           zero_p(ts + col0, ts + col0 + kW / 2);
         }
@@ -729,7 +891,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // warp-collective TMEM reads for every lane; only rows of real tokens are stored
         uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
                         static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
-        const float inv = (live && lsum > 0.f && ok) ? a.v_scale / lsum : 0.f;
+        const float inv = (live && lsum > 0.f && ok) ? a.v_scale * (kF16V ? exp2i(E) : 1.f) / lsum : 0.f;
         // p = 2^(t - m_ref), so the row's base-2 log-sum-exp is m_ref + log2(sum p)
         if (a.lse != nullptr && part == 0 && tt < n_tok)
           a.lse[static_cast<int64_t>(t0 + tt) * a.lse_row_stride + g * kG + h] =
@@ -800,25 +962,41 @@ bool prefill_tc_supported(const AttendArgs& a) {
          reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
 }
 
-template <int kG>
+template <int kG, bool kF16V>
 cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<kG, kF16V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kTcSmem));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  if (kF16V) {
+    convert_v_kernel<<<dim3(static_cast<unsigned>(a.max_blocks), static_cast<unsigned>(a.num_reqs),
+                            static_cast<unsigned>(a.num_kv_heads)),
+                       128, 0, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // one CTA per SM; at most one per tile (an upper bound: tiles are counted on the device)
   const int64_t tiles = (static_cast<int64_t>(a.num_rows) / (kRows / kG) + a.num_reqs + 1) * a.num_kv_heads;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(std::max(sms, 1), tiles));
-  prefill_tc_kernel<kG><<<grid, kThreadsTc, kTcSmem, stream>>>(kv_map, q_map, a);
+  prefill_tc_kernel<kG, kF16V><<<grid, kThreadsTc, kTcSmem, stream>>>(kv_map, q_map, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream) {
-  return a.group == 16 ? launch_tc<16>(a, kv_map, q_map, stream) : launch_tc<8>(a, kv_map, q_map, stream);
+  if (a.vconv != nullptr)
+    return a.group == 16 ? launch_tc<16, true>(a, kv_map, q_map, stream) : launch_tc<8, true>(a, kv_map, q_map, stream);
+  return a.group == 16 ? launch_tc<16, false>(a, kv_map, q_map, stream) : launch_tc<8, false>(a, kv_map, q_map, stream);
+}
+
+size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_t max_blocks) {
+  if (num_reqs <= 0 || num_kv_heads <= 0 || max_blocks <= 0 || max_blocks > kMaxUnion) return 0;
+  const int64_t n = num_reqs * max_blocks * num_kv_heads;
+  const int64_t bytes = n * kTileBytes + ((n * 4 + 255) / 256) * 256;
+  return static_cast<size_t>(bytes);
 }
 
 }  // namespace pbs

@@ -73,6 +73,10 @@ struct AttendArgs {
   int32_t packed_map;         // tmap is the 5-D one-box-per-(page, head) map of a packed cache
   float* split_ws;            // non-null: splits merge through this workspace, not a cluster
   int32_t* split_tickets;     // one arrival counter per (row, head group), zero between calls
+  // prefill tile kernel: V of every (request, block, kv head) converted to fp16 as a 32 KiB
+  // shared-memory image, and its exponents (null: the kernel applies bf16 P as hi + lo)
+  uint8_t* vconv;
+  int32_t* vconv_exp;
 };
 
 // ln 2: a base-2 log-sum-exp (what the kernels track) times this is the natural-log one.
@@ -107,6 +111,10 @@ cudaError_t launch_attend(const AttendArgs& a, int mode, const CUtensorMap& tmap
 // 128-key block of one kv head); `q_map` a 3-D tensor map {head_dim, heads, tokens} with a
 // {64, G, 128 / G} box.
 bool prefill_tc_supported(const AttendArgs& a);
+// Bytes of the tile kernel's converted-V workspace (0: arguments out of range): one 32 KiB image
+// (kTileVBytes) per (request, block, kv head), then one int32 exponent each.
+constexpr int64_t kTileVBytes = 32768;
+size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_t max_blocks);
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream);
 

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 6
+    assert pbs.abi_version() == 7
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"
@@ -126,6 +126,19 @@ def test_prefill_workspace_bytes(L):
     for bad in ((0, 1, 64, 8, 16, 64), (256, 0, 64, 8, 16, 64), (256, 1, 60, 8, 16, 64), (256, 1, 64, 8, 65, 64),
                 (256, 1, 64, 8, 16, 0)):
         assert f(*bad) == 0
+
+
+def test_prefill_tile_workspace_bytes(L):
+    f = L.pbs_prefill_tile_workspace_bytes
+    f.restype = ctypes.c_size_t
+    # one 32 KiB fp16 image per (request, block, kv head), then the int32 exponents (256-aligned)
+    assert f(4, 8, 64) == 4 * 64 * 8 * 32768 + 8192
+    assert f(1, 1, 1) == 32768 + 256
+    assert f(3, 2, 128) > f(3, 2, 64)
+    for bad in ((0, 8, 64), (4, 0, 64), (4, 8, 0), (4, 8, 129)):
+        assert f(*bad) == 0
+    import paged_block_sparse_gb300 as pbs
+    assert pbs.prefill_tile_workspace_bytes(4, 8, 64) == f(4, 8, 64)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")

@@ -392,14 +392,15 @@ PREFILL_CASES = [
 
 
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
-@pytest.mark.parametrize("kernel", ["tc", "token", "gather"])
+@pytest.mark.parametrize("kernel", ["tc", "tc_hilo", "token", "gather"])
 @pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
 def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, heads, monkeypatch):
-    """Every prefill kernel, GQA 8 (tile = 16 tokens x 8 heads) and GQA 16 (8 tokens x 16 heads)."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
+    """Every prefill kernel, GQA 8 (tile = 16 tokens x 8 heads) and GQA 16 (8 tokens x 16 heads);
+    tc_hilo: the tile kernel without a workspace (bf16 P as hi + lo instead of converted fp16 V)."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc" if kernel == "tc_hilo" else kernel)
     b = workloads.small(device=DEV, num_heads=heads[0], num_kv_heads=heads[1], seed=41 + ci, **PREFILL_CASES[ci])
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err)
+    got = gpu_attend(pbs, b, "pre", err, workspace=None if kernel == "tc_hilo" else "default")
     assert int(err.item()) == 0
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", f"prefill {kernel} case {ci}")
 
@@ -417,6 +418,31 @@ def test_prefill_tc_duplicate_ids_count_once(pbs, kernel, monkeypatch):
     got = gpu_attend(pbs, b, "pre", err)
     assert int(err.item()) == 0
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill duplicates")
+
+
+@pytest.mark.parametrize("workspace", ["default", None])
+def test_prefill_tc_v_scales_across_blocks(pbs, workspace, monkeypatch):
+    """V blocks whose magnitudes differ by up to 2^40: on the converted-V path the tile kernel moves
+    its exponent reference and rescales O by powers of two; outputs compared row-normalised."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, pre_q_lens=[300, 40],
+                        pre_ctx_lens=[900, 2000], seed=47)
+    p = b.pre
+    pt = np_i32(p.page_table)
+    rng = np.random.default_rng(3)
+    for r, L in enumerate(np_i32(p.seq_lens)):
+        for blk in range((int(L) + 127) // 128):
+            f = 2.0 ** int(rng.integers(-20, 21))
+            for pg in range(8):
+                page = int(pt[r, blk]) * b.block_page_stride + pg
+                b.cache[page].view(b.num_kv_heads, 16, -1)[:, :, 256:].view(torch.bfloat16).mul_(f)
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err, workspace=workspace)
+    assert int(err.item()) == 0
+    want = oracle_prefill(b)
+    norm = {r: np.abs(want[r]).max() for r in want}
+    assert_close({r: got[r] / norm[r] for r in want}, {r: want[r] / norm[r] for r in want}, "bf16",
+                 "prefill V scales")
 
 
 @pytest.mark.parametrize("kernel", ["tc", "gather"])
