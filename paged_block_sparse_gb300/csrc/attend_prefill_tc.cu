@@ -632,7 +632,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t q_addr = smem_u32(q_s);
       int gs = 0, gp = 0;      // next block for S, for PV, over the CTA's tiles
       uint32_t first = 0u;     // bit (i & 31): block i is its tile's first (its PV starts O afresh)
-      int prev_start = 0;      // first block of the previous tile
       bool ok = true;
       // O += P(j) V(j): in S buffer j % 3 each softmax part's 64 columns hold P hi (bf16, two keys
       // per column) in their first 32 and P lo in their last 32; on the fp16-V path the first 32
@@ -664,10 +663,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       };
       for (int k = 0; ok; ++k) {
         const int sl = k & 1;
-        // Tile k's slot is tile k - 2's, which its softmax warps release only after that tile's
-        // last PV: blocks of tiles before the previous one (after tiles of fewer than two blocks)
-        // get their PV now instead of after two more S.
-        while (ok && gp < prev_start) {
+        // The previous tile's last PVs go first, before waiting for this tile's description: its
+        // epilogue, on the softmax warps' path, waits for them (and the description of tile k
+        // waits for tile k - 2's epilogue), while this tile's first S runs during that epilogue.
+        while (ok && gp < gs) {
           if (!issue_pv(gp)) ok = false;
           ++gp;
         }
@@ -675,15 +674,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const TileDesc* d = &ctl->tile[sl];
         if (d->end) break;
         const int nU = d->n_union;
-        // the previous tile's last PVs go before this tile's S: its epilogue, on the softmax
-        // warps' path, waits for them, while this tile's first S runs during that epilogue
-        while (ok && gp < gs) {
-          if (!issue_pv(gp)) ok = false;
-          ++gp;
-        }
-        if (!ok || !wait_or_abort(&ctl->q_full, k & 1, ctl, a.err_word)) break;
+        if (!wait_or_abort(&ctl->q_full, k & 1, ctl, a.err_word)) break;
         tc::fence_after_sync();
-        const int start = gs;
         // issue order S(0), S(1), S(2), PV(0), S(3), PV(1), ... over the CTA's block sequence: S
         // runs two blocks ahead of PV, so the softmax of block i + 1 finds S(i + 1) done while
         // PV(i - 1) is still queued. S(i) reuses buffer i % 3, whose last reader PV(i - 3) was
@@ -720,7 +712,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // the tile's Q is free once its S MMAs have completed
         tc::commit(&ctl->q_empty);
         mbar_arrive(&ctl->tile_empty[sl]);
-        prev_start = start;
       }
       while (ok && gp < gs) {
         if (!issue_pv(gp)) break;
