@@ -240,8 +240,9 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
  *               (V * 2^-e per block, exact) and then applies P in fp16, one MMA per 16 keys;
  *               without it, it applies bf16 P as hi + lo parts (two MMAs, same accuracy). The
  *               token-centric kernel merges split rows through the workspace when it holds
- *               pbs_attend_workspace_bytes (zeroed before first use, as described there) and
- *               ignores a smaller one. Calls that share one workspace must not run concurrently.
+ *               pbs_attend_workspace_bytes (its tickets are cleared by the call, so here the
+ *               workspace needs no zeroing) and ignores a smaller one. Calls that share one
+ *               workspace must not run concurrently.
  */
 PBS_API int pbs_sparse_prefill_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,

@@ -300,6 +300,16 @@ def prefill_tile_workspace(num_reqs: int, num_kv_heads: int, max_blocks: int, de
     return ws
 
 
+def _tile_kernel_runs(kv_dtype, num_heads, num_kv_heads, topk, max_blocks, page_stride_bytes, forced) -> bool:
+    """Whether a prefill call goes to the tcgen05 tile kernel (the library's rule: bf16 packed cache,
+    GQA 8 or 16, top-k <= 16, a page table at most 8 x top-k blocks wide, or PBS_PREFILL_KERNEL=tc)."""
+    if forced == "token" or kv_dtype != "bf16" or num_heads % num_kv_heads or topk > 16:
+        return False
+    if num_heads // num_kv_heads not in (8, 16) or page_stride_bytes != num_kv_heads * 8192 or max_blocks > 128:
+        return False
+    return forced == "tc" or max_blocks <= 8 * topk
+
+
 # the default prefill workspace is capped; larger calls run in several token segments
 PREFILL_WORKSPACE_CAP = 2 << 30
 _prefill_workspaces: dict = {}
@@ -403,11 +413,14 @@ def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     if isinstance(workspace, str) and workspace == "auto":
-        if os.environ.get("PBS_PREFILL_KERNEL") == "gather":
+        forced = os.environ.get("PBS_PREFILL_KERNEL")
+        if forced == "gather":
             workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
                                           pt.shape[1], q.device, stream)
-        else:
+        elif _tile_kernel_runs(kv_dtype, q.shape[1], num_kv_heads, tk.shape[1], pt.shape[1], psb, forced):
             workspace = prefill_tile_workspace(sl.shape[0], num_kv_heads, pt.shape[1], q.device, stream)
+        else:
+            workspace = None  # the token-centric kernel merges its splits in a cluster
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
     st = lib().pbs_sparse_prefill_attention(

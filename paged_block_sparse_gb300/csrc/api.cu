@@ -603,6 +603,9 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     if (workspace != nullptr && workspace_bytes >= pbs::attend_workspace_bytes(units)) {
       st = attach_workspace(&a, units, workspace, workspace_bytes);
       if (st != PBS_OK) return st;
+      // a prefill workspace may hold anything (the tcgen05 kernels' data): clear the tickets
+      if (cudaMemsetAsync(a.split_tickets, 0, static_cast<size_t>(units) * sizeof(int32_t), cs) != cudaSuccess)
+        return PBS_ERR_CUDA;
     }
     a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
     e = pbs::launch_attend(a, pbs::kModePrefill, map, cs);
