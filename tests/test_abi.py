@@ -168,3 +168,22 @@ def test_binding_insert_shape_checks():
     with pytest.raises(ValueError):
         pbs.insert_index_cache(k, torch.zeros(2, 8, 4).transpose(1, 2), torch.zeros(4, dtype=torch.int64))
     pbs.insert_index_cache(torch.zeros(0, 8), torch.zeros(2, 4, 8), torch.zeros(0, dtype=torch.int64))
+
+
+def test_binding_tile_workspace_rule():
+    """The binding hands its converted-V workspace only to calls the tile kernel takes (the token
+    kernel would read a workspace as split scratch); the rule mirrors the library's dispatch."""
+    import paged_block_sparse_gb300 as pbs
+    run = pbs._tile_kernel_runs
+    packed = 8 * 8192
+    assert run("bf16", 64, 8, 16, 64, packed, None)
+    assert run("bf16", 64, 4, 16, 128, 4 * 8192, None)         # GQA 16, table 8 x top-k wide
+    assert not run("bf16", 64, 8, 16, 129, packed, None)       # wider than 8 x top-k
+    assert not run("bf16", 64, 8, 8, 65, packed, None)         # 8 x top-k = 64 blocks
+    assert run("bf16", 64, 8, 8, 65, packed, "tc")             # forced: up to 128 blocks
+    assert not run("bf16", 64, 8, 8, 129, packed, "tc")
+    assert not run("bf16", 64, 8, 16, 64, packed, "token")
+    assert not run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, None)
+    assert not run("bf16", 32, 8, 16, 64, packed, None)        # GQA 4
+    assert not run("bf16", 64, 8, 17, 64, packed, None)        # top-k above 16
+    assert not run("bf16", 64, 8, 16, 64, packed + 16, None)   # pages strided inside a larger allocation
