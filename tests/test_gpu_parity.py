@@ -421,6 +421,20 @@ def test_prefill_tc_duplicate_ids_count_once(pbs, kernel, monkeypatch):
 
 
 @pytest.mark.parametrize("workspace", ["default", None])
+def test_prefill_tc_widest_page_table(pbs, workspace, monkeypatch):
+    """Contexts reaching block 127: the tile kernel's 128-bit block sets filled to the last bit."""
+    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, pre_q_lens=[40, 17],
+                        pre_ctx_lens=[16344, 9000], future_prob=0.2, seed=48)
+    p = b.pre
+    assert p.page_table.shape[1] <= 128 and int(p.seq_lens.max()) > 127 * 128
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err, workspace=workspace)
+    assert int(err.item()) == 0
+    assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill widest table")
+
+
+@pytest.mark.parametrize("workspace", ["default", None])
 def test_prefill_tc_v_scales_across_blocks(pbs, workspace, monkeypatch):
     """V blocks whose magnitudes differ by up to 2^40: on the converted-V path the tile kernel moves
     its exponent reference and rescales O by powers of two; outputs compared row-normalised."""
