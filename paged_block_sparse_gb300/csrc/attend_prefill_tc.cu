@@ -9,23 +9,29 @@
 //
 // GB300 design
 // ------------
-// * A CTA owns a tile of consecutive tokens of one request and one kv head: 16 tokens x 8 query
-//   heads, or 8 tokens x 16 heads, = 128 rows, one MMA M-tile. The tile's selected blocks are
-//   merged into a sorted union; every union block is streamed once and each row is masked by its
-//   own token's selection.
-// * Warps 0 and 3: TMA producers. Warp 0 loads the Q tile once (3-D tensor map) and streams the
-//   K of each union block, warp 3 its V, each through its own 3-stage ring, one 32 KiB tensor
-//   copy per block (the K or the V half of the 8 pages' 16 rows of this kv head) through a 5-D
-//   map {64 elements, 16 rows, kv head, page, row quarter} over the packed cache, 128B swizzle.
-//   A stage is [64-dim quarter][128 keys][128 B]: 8-key groups 1 KiB apart, the block's second
-//   64 dims 16 KiB further. Warp 1: one thread issues the tcgen05 MMAs, S two
-//   blocks ahead of PV. Warps 4-11: softmax and epilogue, two warps per TMEM lane quadrant.
+// * A tile is 16 consecutive tokens of one request and one kv head x 8 query heads, or 8 tokens
+//   x 16 heads, = 128 rows, one MMA M-tile. The tile's selected blocks are merged into a sorted
+//   union; every union block is streamed once and each row is masked by its own token's
+//   selection.
+// * Persistent: one CTA per SM walks a list of tiles, longest first. Warp 2 (scheduler) writes
+//   the description of the tile after next (request, tokens, per-token 128-bit block sets, the
+//   union) into one of two shared-memory slots and loads each tile's Q (3-D tensor map). The
+//   rings, the S buffers and the MMA order run on across tiles.
+// * Warps 0 and 3: TMA producers. Warp 0 streams the K of each union block, warp 3 its V, each
+//   through its own 3-stage ring, one 32 KiB copy per block: K (and V without a workspace)
+//   through a 5-D map {64 elements, 16 rows, kv head, page, row quarter} over the packed cache,
+//   128B swizzle; with a workspace, V as the block's fp16 image that convert_v_kernel wrote
+//   there. A stage is [64-dim quarter][128 keys][128 B]: 8-key groups 1 KiB apart, the block's
+//   second 64 dims 16 KiB further. Warp 1: one thread issues the tcgen05 MMAs, S two blocks
+//   ahead of PV. Warps 4-11: softmax and epilogue, two warps per TMEM lane quadrant.
 // * TMEM (512 columns): S triple buffer (3 x 128, fp32) and the O accumulator (128, fp32). Each
-//   softmax part rewrites its own 64 S columns with P: hi (bf16, two keys per column) in the
-//   first 32, lo in the last 32, once all 64 S values are in its registers.
-// * S = Q K^T: A = Q (K-major smem), B = K tile (K-major smem). O += P V: A = P read from TMEM,
-//   B = V tile (MN-major smem). P is split into bf16 hi + lo halves, two MMAs, so the result
-//   stays within 2e-3 relative RMS of the fp64 attend.
+//   softmax part rewrites its own 64 S columns with P once all 64 S values are in its registers:
+//   fp16 P in the first 32 (converted-V path), or bf16 hi in the first 32 and lo in the last 32.
+// * S = Q K^T: A = Q (K-major smem), B = K tile (K-major smem), bf16. O += P V: A = P read from
+//   TMEM, B = V tile (MN-major smem). Converted-V path: V * 2^-e per block in fp16 (exact), P as
+//   P * 2^(e - E) in fp16 against a per-tile reference E, one MMA per 16 keys. Otherwise P is
+//   split into bf16 hi + lo halves, two MMAs. Either way the result stays within 2e-3 relative
+//   RMS of the fp64 attend (bf16 P alone would not).
 // * The MMAs of one thread execute in issue order, so S(i) may reuse the buffer whose P(i-3)
 //   was read by PV(i-3), issued before it; the softmax of block i waits only for S(i), and for
 //   PV(i-1) when it has to rescale O. K stages are released when S has read them, V stages when
