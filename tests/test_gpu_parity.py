@@ -388,6 +388,7 @@ PREFILL_CASES = [
     dict(pre_q_lens=[3] * 40, pre_ctx_lens=[i * 50 for i in range(40)], topk=8),   # > 32 requests
     dict(pre_q_lens=[500], pre_ctx_lens=[7], topk=12, future_prob=0.5),
     dict(pre_q_lens=[130, 260], pre_ctx_lens=[0, 0], topk=2),
+    dict(pre_q_lens=[20, 0, 33, 0], pre_ctx_lens=[100, 500, 1300, 0], topk=8),   # requests without tokens
 ]
 
 
