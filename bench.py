@@ -456,10 +456,19 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
     if pg:
         pg.barrier()
     with ClockSampler(local) as clk:
-        if args.workload in ("prefill", "prefill_g16") or (args.workload == "mixed_nvfp4" and args.part == "prefill"):
+        part = "prefill" if args.workload in ("prefill", "prefill_g16") else args.part
+        launches = 1  # per step
+        if part == "prefill":
             work = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
             times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream)
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
+            p = b.pre
+            # the binding's default call on the tile kernel: V conversion, then the attend
+            if pbs._tile_kernel_runs(b.kv_dtype, b.num_heads, b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
+                                     b.page_bytes, os.environ.get("PBS_PREFILL_KERNEL")) and \
+                    0 < pbs.prefill_tile_workspace_bytes(p.seq_lens.shape[0], b.num_kv_heads,
+                                                         p.page_table.shape[1]) <= pbs.TILE_WORKSPACE_CAP:
+                launches = 2
         else:
             work = decode_bytes(b, decode_ctx(pbs, b))
             times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
@@ -476,12 +485,12 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             "metric": metric, "value": job_rate(world, work, ms) / scale, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if b.kv_dtype == "bf16" else b.kv_dtype,
-            "data": "synthetic", "config": {"workload": b.name, "part": args.part,
+            "data": "synthetic", "config": {"workload": b.name, "part": part,
                                             "l2": L2_NOTE},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                          "traffic": traffic, "peak_source": f"{peak_src} (burst, kernel timed alone)",
                          "algorithmic_work_per_launch": work},
-            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+            "gpu_launches": args.steps * launches, "clocks": clk.summary()}), flush=True)
     if pg:
         pg.barrier()
         pg.destroy_process_group()
