@@ -481,7 +481,7 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
   }
 }
 
-// One CTA per SM walks its list of tiles (flat tiles blockIdx.x, + gridDim.x, ...). The K / V
+// One CTA per SM walks its list of tiles (one flat tile per round of gridDim.x). The K / V
 // rings, the S buffers and the MMA order run on across tile boundaries (block counters count
 // the CTA's whole block sequence), so the next tile's S runs while the softmax warps finish the
 // previous tile, and its description, Q tile and first K / V blocks are ready before they do.
@@ -544,7 +544,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       total += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>((q_len + kTok - 1) / kTok));
     }
     const int flat = total * a.num_kv_heads;
-    for (int k = 0, f = blockIdx.x;; ++k, f += gridDim.x) {
+    for (int k = 0;; ++k) {
+      // round k of the list: its gridDim.x tiles dealt in alternating directions, so a CTA that
+      // took a longer tile of one round takes a shorter one of the next (costs fall along the list)
+      const int f = k * static_cast<int>(gridDim.x) +
+                    ((k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
       const int sl = k & 1;
       TileDesc* d = &ctl->tile[sl];
       // the slot's previous tile (k - 2) has been released by every role
