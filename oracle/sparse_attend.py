@@ -27,9 +27,10 @@ Sources are three vLLM API pages:
    request id and absolute position).
 2. Sparse block table ([sparse_pa] row writer): a selected logical 128-token
    block b is valid iff the row's causal length max(p+1, 0) is positive and
-   0 <= b <= p // 128. Valid blocks before the query's own block are "full"
-   and are packed in top-k order; a valid block equal to the own block is the
-   "tail" and goes right after the full ones. Each packed block expands to
+   0 <= b <= p // 128. A block id listed more than once in a row is one
+   selection (only its first entry counts). Valid blocks before the query's
+   own block are "full" and are packed in top-k order; a valid block equal to
+   the own block is the "tail" and goes right after the full ones. Each packed block expands to
    PAGES_PER_BLOCK page-16 ids  page_table[b]*block_page_stride + j. The row
    is zero past the used slots, and the context length is
    128*n_full + (p+1 - 128*(p//128)) when a tail is present, else
@@ -50,10 +51,13 @@ Sources are three vLLM API pages:
 
 Readings where the pages are silent (each listed in the design notes too):
 SPARSE_BLOCK_SIZE = 128, page rows = 16, PAGES_PER_BLOCK = 8; a page-table
-entry is a physical *block* id; rows with no attended key give a zero output;
-duplicate ids in one top-k row are followed literally by the table (a second
-copy of the own block lands on the same slot and the slots it would have
-taken are zero); the attend definition in step 3 assumes distinct ids.
+entry is a physical *block* id; rows with no attended key give a zero output.
+Repeated ids in one top-k row: a top-k row is read as a SET of blocks. The
+row writer itself treats a repeated own block that way (every copy lands on
+slot n_full and ctx counts its keys once, through n_full); the same rule for
+a repeated full block makes the table, ctx and the attend agree, so the
+table of a row equals the row writer applied to the row with its later
+repeats removed, and the attend reads every selected block once.
 """
 from __future__ import annotations
 
@@ -104,7 +108,12 @@ def sparse_block_table_row(topk_row, bt_row, abs_pos: int, block_page_stride: in
     causal_len = max(abs_pos + 1, 0)
     own = abs_pos // SPARSE_BLOCK_SIZE
     full, tail = [], []
+    seen = set()
     for b in (int(x) for x in topk_row):
+        # a block listed again is the same selection: only its first entry is kept
+        if b in seen:
+            continue
+        seen.add(b)
         if causal_len == 0 or b < 0 or b > own:
             continue
         if b == own:
@@ -122,7 +131,7 @@ def sparse_block_table_row(topk_row, bt_row, abs_pos: int, block_page_stride: in
 
     for slot, b in enumerate(full):
         place(slot, b)
-    for b in tail:                      # every copy of the own block takes slot n_full
+    for b in tail:                      # at most one: the own block, after the full ones
         place(len(full), b)
     n_valid = len(full) + len(tail)
     if tail:
@@ -165,7 +174,7 @@ def build_sparse_block_table_prefill(topk, page_table, cu_seqlens_q, seq_lens,
 # ------------------------------------------------------------------------------------------
 
 def attended_positions(topk_row, abs_pos: int) -> np.ndarray:
-    """Logical key positions a query attends (set reading; distinct ids assumed)."""
+    """Logical key positions a query attends: each selected block once, however often listed."""
     if abs_pos < 0:
         return np.zeros(0, dtype=np.int64)
     own = abs_pos // SPARSE_BLOCK_SIZE

@@ -95,6 +95,44 @@ def test_table_walk_equals_direct_mapping():
             assert walked == direct
 
 
+def test_table_walk_with_repeated_ids_reads_each_block_once():
+    """Brute force on rows whose ids repeat (drawn with replacement): walking keys 0..ctx-1
+    through the table visits every attended (page, row) exactly once, and ctx is the closed
+    form counted over the row's distinct blocks (the writer's own treatment of a repeated own
+    block, one slot and its keys counted once, applied to every block)."""
+    rng = np.random.default_rng(7)
+    bt = rng.permutation(40)
+    rows, poss = _random_rows(rng, 400, 8, 4500, distinct=False)
+    assert sum(len(set(r) - {-1}) < len([b for b in r if b >= 0]) for r in rows) > 100
+    for row, p in zip(rows, poss):
+        sbt, ctx = oracle.sparse_block_table_row(row, bt, p)
+        walked = [(int(sbt[n // 16]), n % 16) for n in range(ctx)]
+        assert len(walked) == len(set(walked))
+        direct = sorted((int(bt[x // 128]) * 8 + (x % 128) // 16, x % 16) for x in oracle.attended_positions(row, p))
+        assert sorted(walked) == direct
+        if p >= 0:
+            own = p // 128
+            distinct = {b for b in row if 0 <= b <= own}
+            n_full = len(distinct - {own})
+            assert ctx == 128 * n_full + (p - 128 * own + 1 if own in distinct else 0)
+
+
+def test_table_repeats_equal_row_without_them():
+    """A repeated id is one selection: replacing every later copy of an id by -1 leaves the row
+    and ctx unchanged, bit for bit (written for any mix of full and own-block repeats)."""
+    rng = np.random.default_rng(8)
+    bt = rng.permutation(40)
+    rows, poss = _random_rows(rng, 300, 7, 4500, distinct=False)
+    for row, p in zip(rows, poss):
+        seen, stripped = set(), []
+        for b in row:
+            stripped.append(-1 if b in seen else b)
+            seen.add(b)
+        a, ca = oracle.sparse_block_table_row(row, bt, p)
+        b_, cb = oracle.sparse_block_table_row(stripped, bt, p)
+        assert ca == cb and np.array_equal(a, b_)
+
+
 def test_table_order_and_padding_invariance():
     """Permuting a row's ids or moving its -1s keeps ctx and the set of 8-page groups."""
     rng = np.random.default_rng(3)
@@ -328,6 +366,26 @@ def test_zero_query_is_mean_of_values():
                                           0.1, 1.0, 2.0)[0]
     keys = list(range(0, 128)) + list(range(384, 391))
     want = 2.0 * Vb.double().numpy()[:, keys, :].mean(axis=1)
+    for h in range(4):
+        np.testing.assert_allclose(out[h], want[h // 2], rtol=0, atol=1e-12)
+
+
+def test_zero_query_with_repeated_blocks_is_mean_over_distinct_keys():
+    """Closed form with repeated ids: q = 0 gives uniform weights over the attended keys, and a
+    block listed twice (full block 1, own block 3) contributes its keys once, so out is the
+    plain mean of V over blocks 0, 1 and keys 384..390 (computed here from the unpaged values)."""
+    rng = np.random.default_rng(16)
+    Hkv, L, D = 2, 400, 128
+    Vb = torch.randn(Hkv, L, D).to(torch.bfloat16)
+    Kb = torch.randn(Hkv, L, D).to(torch.bfloat16)
+    cache, bt = _paged_cache_from_logical(Kb.view(torch.int16).numpy().view(np.uint16),
+                                          Vb.view(torch.int16).numpy().view(np.uint16), "bf16", rng)
+    p = 390
+    topk = np.array([[[1, 3, 0, 1, 3, -1]]], np.int32)
+    out = oracle.sparse_prefill_attention(np.zeros((1, 4, D)), cache, "bf16", Hkv, topk, bt[None], [0, 1], [p + 1],
+                                          0.1, 1.0, 1.0)[0]
+    keys = list(range(0, 256)) + list(range(384, 391))
+    want = Vb.double().numpy()[:, keys, :].mean(axis=1)
     for h in range(4):
         np.testing.assert_allclose(out[h], want[h // 2], rtol=0, atol=1e-12)
 
