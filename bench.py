@@ -206,16 +206,45 @@ def time_steps(fn, steps: int, warmup: int, flush: L2Flush, stream: torch.cuda.S
     return [s.elapsed_time(e) for s, e in evs]
 
 
+KV_ROW_BYTES = {"bf16": 2 * 128 * 2, "fp8_e4m3": 2 * 128, "nvfp4": 2 * 72}
+
+
 def decode_bytes(b, ctx: torch.Tensor) -> float:
-    """Algorithmic HBM bytes of one decode attend: every attended K/V row once, Q, O, top-k and
-    the page-table entries of the selected blocks."""
+    """Algorithmic HBM bytes of one decode attend: every attended K/V row once per query row (the
+    per-row sum), Q, O, top-k and the page-table entries of the selected blocks."""
     d = b.dec
     rows = d.q.shape[0]
-    per_row_kv = {"bf16": 2 * 128 * 2, "fp8_e4m3": 2 * 128, "nvfp4": 2 * 72}[b.kv_dtype]
-    kv = float(ctx.to(torch.int64).sum().item()) * b.num_kv_heads * per_row_kv
+    kv = float(ctx.to(torch.int64).sum().item()) * b.num_kv_heads * KV_ROW_BYTES[b.kv_dtype]
     qo = 2.0 * rows * b.num_heads * 128 * 2
     meta = rows * b.topk * 4 * 2 + rows * 4
     return kv + qo + meta
+
+
+def decode_union_bytes(b) -> float:
+    """decode_bytes with the K/V rows counted once per (request, kv head) over the request's
+    decode_query_len right-aligned rows: the union of the keys the rows attend. Within a block a
+    row attends a prefix (all 128 keys of a full block, keys up to its position of its own block),
+    so the union over rows is, per selected block, the longest prefix any row attends."""
+    d = b.dec
+    tk = d.topk.reshape(-1, d.topk.shape[-1]).cpu().numpy()
+    sl = d.seq_lens.cpu().numpy()
+    dql = d.decode_query_len
+    union = 0
+    for req, L in enumerate(sl.tolist()):
+        longest = {}
+        for i in range(dql):
+            pos = L - dql + i
+            if pos < 0:
+                continue
+            own = pos // 128
+            for blk in set(int(x) for x in tk[req * dql + i]):
+                if 0 <= blk <= own:
+                    n = 128 if blk < own else pos - 128 * own + 1
+                    longest[blk] = max(longest.get(blk, 0), n)
+        union += sum(longest.values())
+    rows = d.q.shape[0]
+    kv = float(union) * b.num_kv_heads * KV_ROW_BYTES[b.kv_dtype]
+    return kv + 2.0 * rows * b.num_heads * 128 * 2 + rows * b.topk * 4 * 2 + rows * 4
 
 
 def prefill_flops(ctx: torch.Tensor, num_heads: int) -> float:
@@ -227,25 +256,26 @@ def prefill_flops(ctx: torch.Tensor, num_heads: int) -> float:
 # our arm
 # --------------------------------------------------------------------------------------------
 
-def run_decode(pbs, b, steps, warmup, flush, stream):
+def run_decode(pbs, b, steps, warmup, flush, stream, sparse_table=None):
     d = b.dec
     out = torch.empty_like(d.q)
 
     def step():
         pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table, d.seq_lens,
                                     d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale, b.block_page_stride,
-                                    out=out, stream=stream)
+                                    out=out, stream=stream, sparse_table=sparse_table)
     return time_steps(step, steps, warmup, flush, stream)
 
 
-def run_prefill(pbs, b, steps, warmup, flush, stream, workspace="auto"):
+def run_prefill(pbs, b, steps, warmup, flush, stream, workspace="auto", kernel=None, sparse_table=None):
     p = b.pre
     out = torch.empty_like(p.q)
 
     def step():
         pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
                                      p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
-                                     b.block_page_stride, out=out, stream=stream, workspace=workspace)
+                                     b.block_page_stride, out=out, stream=stream, workspace=workspace, kernel=kernel,
+                                     sparse_table=sparse_table)
     return time_steps(step, steps, warmup, flush, stream)
 
 
@@ -301,6 +331,18 @@ def e2e_decode(pbs, b, steps, warmup, stream):
 
 def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     res = {}
+    # the decode workload fed its prebuilt table (built once per step, shared by every sparse
+    # layer) next to the fused call that compacts each row itself
+    b = workloads.decode(device="cuda")
+    d = b.dec
+    tbl = pbs.build_sparse_block_table_decode(d.topk, d.page_table, d.seq_lens, d.decode_query_len, 8)
+    by = decode_bytes(b, tbl[1]) + tbl[0].numel() * 4 + tbl[1].numel() * 4
+    t = statistics.median(run_decode(pbs, b, steps, warmup, flush, stream, sparse_table=tbl))
+    tf = statistics.median(run_decode(pbs, b, steps, warmup, flush, stream))
+    res["decode_b64_bf16_prebuilt_table"] = {"ms": t, "fused_ms": tf, "GB/s": by / (t * 1e-3) / 1e9,
+                                             "frac_of_hbm_peak": by / (t * 1e-3) / 1e9 / hbm}
+    del b, d, tbl
+    torch.cuda.empty_cache()
     # decode table build alone (the standalone G1 kernel)
     b = workloads.prefill(device="cuda")
     p = b.pre
@@ -324,18 +366,21 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     res["prefill_varlen_bf16_no_workspace"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                                "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16}
     # the same call on the gathered-row kernel (opt-in; 2 GiB workspace, three token segments)
-    os.environ["PBS_PREFILL_KERNEL"] = "gather"
-    try:
-        ws = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, b.topk,
-                                   p.page_table.shape[1], "cuda", stream)
-        t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=ws))
-        res["prefill_varlen_bf16_gathered_rows"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
-                                                    "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
-                                                    "workspace_bytes": ws.numel()}
-        del ws
-    finally:
-        del os.environ["PBS_PREFILL_KERNEL"]
+    ws = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, b.topk,
+                               p.page_table.shape[1], "cuda", stream)
+    t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=ws,
+                                      kernel="gather"))
+    res["prefill_varlen_bf16_gathered_rows"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
+                                                "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
+                                                "workspace_bytes": ws.numel()}
+    del ws
     pbs._prefill_workspaces.clear()
+    # the same call fed the prebuilt prefill table (built once, as every sparse layer would share it)
+    tbl = pbs.build_sparse_block_table_prefill(p.topk, p.page_table, p.cu_seqlens_q, p.seq_lens, 8)
+    t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, sparse_table=tbl))
+    res["prefill_varlen_bf16_prebuilt_table"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
+                                                 "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16}
+    del tbl
     del b, p, sbt, ctxb
     torch.cuda.empty_cache()
     # the same prompts with GQA 16 (tile = 8 tokens x 16 heads)
@@ -347,15 +392,29 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
                                         "algorithmic_tflop": fl / 1e12}
     del b
     torch.cuda.empty_cache()
-    # fp8 MTP decode
+    # fp8 MTP decode: algorithmic bytes = the union of each request's K/V rows over its two
+    # right-aligned rows (each kernel CTA serves one row, so the per-row sum is what it reads)
     b = workloads.mtp_fp8(device="cuda")
     ctx = decode_ctx(pbs, b)
     by = decode_bytes(b, ctx)
+    byu = decode_union_bytes(b)
     t = statistics.median(run_decode(pbs, b, steps, warmup, flush, stream))
-    res["mtp_fp8_decode"] = {"ms": t, "tokens/s": b.dec.q.shape[0] / (t * 1e-3), "GB/s": by / (t * 1e-3) / 1e9,
-                             "frac_of_hbm_peak": by / (t * 1e-3) / 1e9 / hbm}
+    res["mtp_fp8_decode"] = {"ms": t, "tokens/s": b.dec.q.shape[0] / (t * 1e-3),
+                             "union_bytes": byu, "per_row_sum_bytes": by,
+                             "GB/s": byu / (t * 1e-3) / 1e9, "frac_of_hbm_peak": byu / (t * 1e-3) / 1e9 / hbm,
+                             "per_row_sum_GB/s": by / (t * 1e-3) / 1e9,
+                             "per_row_sum_frac_of_hbm_peak": by / (t * 1e-3) / 1e9 / hbm}
     del b
     torch.cuda.empty_cache()
+    # the decode workload's shape on fp8 and NVFP4 caches
+    for kv in ("fp8_e4m3", "nvfp4"):
+        b = workloads.decode(device="cuda", kv_dtype=kv)
+        by = decode_bytes(b, decode_ctx(pbs, b))
+        t = statistics.median(run_decode(pbs, b, steps, warmup, flush, stream))
+        res[f"decode_b64_{kv}"] = {"ms": t, "tokens/s": b.dec.q.shape[0] / (t * 1e-3), "GB/s": by / (t * 1e-3) / 1e9,
+                                   "frac_of_hbm_peak": by / (t * 1e-3) / 1e9 / hbm, "algorithmic_bytes": by}
+        del b
+        torch.cuda.empty_cache()
     # mixed NVFP4: decode then prefill in one stream
     b = workloads.mixed_nvfp4(device="cuda")
     ctx = decode_ctx(pbs, b)
@@ -450,9 +509,12 @@ def reference_arm(args, world, rank):
 def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, peak_src):
     """One JSON line for a non-headline workload (prefill TFLOP/s, or decode GB/s for fp8/NVFP4)."""
     make = {"prefill": workloads.prefill, "mtp_fp8": workloads.mtp_fp8, "mixed_nvfp4": workloads.mixed_nvfp4,
-            "prefill_g16": workloads.prefill_g16}
+            "prefill_g16": workloads.prefill_g16,
+            "decode_fp8": lambda device, seed: workloads.decode(device=device, seed=seed, kv_dtype="fp8_e4m3"),
+            "decode_nvfp4": lambda device, seed: workloads.decode(device=device, seed=seed, kv_dtype="nvfp4")}
     b = make[args.workload](device="cuda", seed={"prefill": 1002, "mtp_fp8": 1003, "mixed_nvfp4": 1004,
-                                                 "prefill_g16": 1005}[args.workload] + 17 * rank)
+                                                 "prefill_g16": 1005, "decode_fp8": 1001,
+                                                 "decode_nvfp4": 1001}[args.workload] + 17 * rank)
     if pg:
         pg.barrier()
     with ClockSampler(local) as clk:
@@ -464,13 +526,15 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
             p = b.pre
             # the binding's default call on the tile kernel: V conversion, then the attend
-            if pbs._tile_kernel_runs(b.kv_dtype, b.num_heads, b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
-                                     b.page_bytes, os.environ.get("PBS_PREFILL_KERNEL")) and \
+            if pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes, b.num_heads,
+                                         b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1]) == "tile" and \
                     0 < pbs.prefill_tile_workspace_bytes(p.seq_lens.shape[0], b.num_kv_heads,
                                                          p.page_table.shape[1]) <= pbs.TILE_WORKSPACE_CAP:
                 launches = 2
         else:
-            work = decode_bytes(b, decode_ctx(pbs, b))
+            # rows of one request share their K/V rows: the union counts each once
+            per_row = decode_bytes(b, decode_ctx(pbs, b))
+            work = decode_union_bytes(b) if b.dec.decode_query_len > 1 else per_row
             times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
             unit, bound, peak, metric = "GB/s", "hbm", hbm, "decode HBM GB/s"
     ms = max_over_ranks(statistics.mean(times), pg, "cuda")
@@ -489,7 +553,9 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                                             "l2": L2_NOTE},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                          "traffic": traffic, "peak_source": f"{peak_src} (burst, kernel timed alone)",
-                         "algorithmic_work_per_launch": work},
+                         "algorithmic_work_per_launch": work,
+                         **({"per_row_sum_bytes": per_row, "per_row_sum_frac": per_row / (statistics.mean(times) * 1e-3)
+                             / scale / peak} if part != "prefill" and b.dec.decode_query_len > 1 else {})},
             "gpu_launches": args.steps * launches, "clocks": clk.summary()}), flush=True)
     if pg:
         pg.barrier()
@@ -513,7 +579,8 @@ def main():
                     help="decode requests (64 is the headline workload; smaller only for profiling)")
     ap.add_argument("--part", choices=["decode", "prefill"], default="decode",
                     help="which half of the mixed NVFP4 batch --workload mixed_nvfp4 times")
-    ap.add_argument("--workload", choices=["decode", "prefill", "prefill_g16", "mtp_fp8", "mixed_nvfp4"],
+    ap.add_argument("--workload", choices=["decode", "prefill", "prefill_g16", "mtp_fp8", "mixed_nvfp4", "decode_fp8",
+                                           "decode_nvfp4"],
                     default="decode",
                     help="timed workload (the headline line is decode; the others for profiling and tuning)")
     args = ap.parse_args()

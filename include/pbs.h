@@ -77,6 +77,10 @@ typedef struct CUstream_st* pbs_stream_t;
 #define PBS_DEVERR_PAGE_OOB   2  /* a physical page id >= num_pages (row attends nothing) */
 #define PBS_DEVERR_SLOT_OOB   4  /* an index-cache slot >= num_blocks * block_tokens (row skipped) */
 #define PBS_DEVERR_TIMEOUT    8  /* a bounded wait on a copy gave up (output of that row is undefined) */
+#define PBS_DEVERR_TABLE     16  /* a prebuilt table row the kernel cannot read: ctx outside
+                                    [0, topk_k * 128], or (prefill tile kernel) a slot whose page ids
+                                    are not page_table[r][b] * block_page_stride + j of a block b of
+                                    the row's request (the row attends nothing) */
 
 /* ---- KV cache formats -------------------------------------------------------------------- */
 #define PBS_KV_BF16      0  /* page = [Hkv][16 rows][K(head_dim) | V(head_dim)] bf16 ([flashinfer]: K|V
@@ -87,6 +91,36 @@ typedef struct CUstream_st* pbs_stream_t;
                                scales). A slot is 16 rows x 64 B of e2m1 codes (element 2i in the
                                low nibble of byte i) then 16 rows x 8 B of e4m3 scales (scale j
                                covers elements 16j..16j+15). head_dim must be 128. */
+
+/* ---- attend options ---------------------------------------------------------------------- */
+/* Prefill kernels (pbs_attend_options.prefill_kernel and the return value of
+ * pbs_prefill_kernel_choice). */
+#define PBS_PREFILL_AUTO    0  /* the library's rule (see pbs_prefill_kernel_choice) */
+#define PBS_PREFILL_TOKEN   1  /* token-centric kernel: any shape, mma.sync, one row per CTA group */
+#define PBS_PREFILL_TILE    2  /* tcgen05 tile kernel: bf16 packed cache, GQA 8 or 16, top-k <= 16,
+                                  page table <= 128 blocks, 16-byte aligned q / out rows */
+#define PBS_PREFILL_GATHER  3  /* tcgen05 gathered-row kernel: as the tile kernel but page tables up to
+                                  8192 blocks and top-k <= 64; needs its workspace; no prebuilt table */
+
+/*
+ * Optional tuning of one attend call (a NULL pointer or an all-zero struct = the library's own
+ * choices). No counterpart on the pages; there are no global switches: every choice the caller
+ * can override is an argument of the call.
+ *   prefill_kernel  PBS_PREFILL_*: run this prefill kernel; PBS_ERR_UNSUPPORTED when it cannot
+ *                   take the call. Decode calls ignore it.
+ *   splits          0, or 1 / 2 / 4 / 8: CTAs per (row, head group) of the decode and token-centric
+ *                   prefill kernel (the library otherwise splits rows only while they cannot fill
+ *                   the GPU); any other value is PBS_ERR_ARG.
+ *   cache_map       0, or 1: read a packed bf16 / fp8 cache through the per-row-quarter tensor map
+ *                   instead of the one-box-per-page map (token-centric kernel; testing).
+ *   reserved        must be 0.
+ */
+typedef struct pbs_attend_options {
+  int32_t prefill_kernel;
+  int32_t splits;
+  int32_t cache_map;
+  int32_t reserved;
+} pbs_attend_options;
 
 /* Text for a status code (static storage; never NULL). */
 PBS_API const char* pbs_status_string(int status);
@@ -154,7 +188,8 @@ PBS_API int pbs_build_sparse_block_table_prefill(
 /*
  * Sparse decode attention ([flashinfer] msa_sparse_decode_attention call in forward;
  * [nvfp4] minimax_m3_nvfp4_sparse_decode_fly call). Builds each row's table itself
- * (same rule as pbs_build_sparse_block_table_decode) and attends over it.
+ * (same rule as pbs_build_sparse_block_table_decode) and attends over it, or attends a
+ * prebuilt table.
  *
  *   q           [num_rows, num_heads, head_dim] bf16; element (r, h, d) at
  *               q + r*q_row_stride + h*q_head_stride + d
@@ -173,7 +208,20 @@ PBS_API int pbs_build_sparse_block_table_prefill(
  *               each head's scaled logits, ln sum_n exp(softmax_scale * k_scale * q_h . k_n), over
  *               the row's attended keys; -inf for a row with none. Not on the pages: it lets a
  *               caller merge this attend with another over disjoint keys.
+ *   sparse_bt, sbt_row_stride, sparse_ctx: optional prebuilt table (both NULL: the kernel
+ *               compacts each row from topk and page_table itself). Given, row r attends keys
+ *               n < sparse_ctx[r] at page sparse_bt[r * sbt_row_stride + n / 16], row n % 16,
+ *               exactly as [sparse_pa] tables are read; topk is then not read (it may be NULL)
+ *               and page_table only by the prefill tile kernel. This is the table
+ *               pbs_build_sparse_block_table_decode / _prefill write, which the pages build once
+ *               per step and share across sparse layers ([sparse_pa]
+ *               minimax_m3_rebase_block_table_to_page16: every sparse layer resolves its
+ *               selection through the same table). sbt_row_stride >= topk_k * 8 and both
+ *               pointers 4-byte aligned, else PBS_ERR_SHAPE / PBS_ERR_ALIGN; one of the two
+ *               NULL -> PBS_ERR_ARG. A ctx outside [0, topk_k * 128] sets PBS_DEVERR_TABLE and a
+ *               page id >= num_pages PBS_DEVERR_PAGE_OOB; such a row attends nothing.
  *   workspace   optional (NULL, 0): see pbs_attend_workspace_bytes; too small -> PBS_ERR_SHAPE.
+ *   options     optional (NULL): see pbs_attend_options.
  */
 PBS_API int pbs_sparse_decode_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -182,10 +230,12 @@ PBS_API int pbs_sparse_decode_attention(
     const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
     const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
     const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
+    const int32_t* sparse_bt, int64_t sbt_row_stride, const int32_t* sparse_ctx,
     float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
     float* lse, int64_t lse_row_stride,
     void* workspace, size_t workspace_bytes,
+    const pbs_attend_options* options,
     int32_t* err_word, pbs_stream_t stream);
 
 /*
@@ -202,11 +252,15 @@ PBS_API int pbs_sparse_decode_attention(
  * and nothing is launched. Unsplit calls have no limit.
  * Setup: the first call on each device looks up the array's device address with the device
  * current (a CUDA runtime call that may load the library's device module); make that first
- * call before any stream capture begins. A failed lookup returns PBS_ERR_CUDA.
+ * call before any stream capture begins. A failed lookup returns PBS_ERR_CUDA. The address is
+ * kept with the device's current context and looked up again when that context changes (after
+ * a device reset, for instance, which also reloads the array, zeroed).
  * State: the tickets start at zero (static device memory is zero at module load) and every
  * completed call leaves them zero. All calls on one device share the array: calls whose
  * kernels could run at the same time (other streams, unordered host threads) race on it and
  * must be serialised by the caller, e.g. by issuing them on one stream.
+ * options: optional (NULL); its `splits` forces the split count as for the other entries (the
+ * limits above still apply), the other fields are ignored.
  * Arguments, layouts and error behaviour otherwise as in pbs_sparse_decode_attention.
  */
 PBS_API int pbs_sparse_decode_attention_noalloc(
@@ -218,13 +272,18 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
     const int32_t* seq_lens, int32_t batch, int32_t decode_query_len, int32_t block_page_stride,
     float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
+    const pbs_attend_options* options,
     int32_t* err_word, pbs_stream_t stream);
 
 /*
  * Sparse prefill attention, varlen ([flashinfer] msa_sparse_attention call with cu_seqlens_q;
  * [nvfp4] minimax_m3_nvfp4_sparse_prefill call). Token positions as in
- * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention,
- * except the workspace:
+ * pbs_build_sparse_block_table_prefill; everything else as in pbs_sparse_decode_attention
+ * (including the optional prebuilt table: the token-centric kernel reads its page ids as they
+ * are; the tile kernel, which streams whole 128-key blocks shared by a tile's tokens, maps each
+ * slot back to the block of the request's page table whose 8 pages it lists, so a slot must
+ * hold page_table[r][b] * block_page_stride + j, j < 8, as the builders write it), except the
+ * workspace:
  *   workspace   optional (NULL, 0), caller-owned device memory, contents need no initial value.
  *               With a 256-byte aligned workspace of at least
  *               pbs_prefill_workspace_bytes(256, num_reqs, num_heads, num_kv_heads, topk_k,
@@ -251,11 +310,32 @@ PBS_API int pbs_sparse_prefill_attention(
     const int32_t* topk, int64_t topk_row_stride, int32_t topk_k,
     const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
     const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs, int32_t total_q,
-    int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
+    int32_t block_page_stride,
+    const int32_t* sparse_bt, int64_t sbt_row_stride, const int32_t* sparse_ctx,
+    float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
     float* lse, int64_t lse_row_stride,
     void* workspace, size_t workspace_bytes,
+    const pbs_attend_options* options,
     int32_t* err_word, pbs_stream_t stream);
+
+/*
+ * Which prefill kernel pbs_sparse_prefill_attention runs for a call of this shape: returns
+ * PBS_PREFILL_TOKEN, _TILE or _GATHER, or minus a PBS_ERR_* status (-PBS_ERR_UNSUPPORTED when
+ * options ask for a kernel that cannot take the call, -PBS_ERR_ARG for bad arguments). No
+ * counterpart on the pages; a caller uses it to size the workspace the chosen kernel wants.
+ * The rule: options->prefill_kernel when set; else the tile kernel while it can take the call
+ * (PBS_PREFILL_TILE above) and the page table is at most 8 x topk_k blocks wide (a tile streams
+ * the union of its tokens' selections, which grows with the context they choose from); else the
+ * token-centric kernel. The answer assumes 16-byte aligned q and out rows; a call whose rows are
+ * not takes the token-centric kernel (or PBS_ERR_UNSUPPORTED when a tcgen05 kernel was asked for).
+ *   with_table       non-zero: the call passes a prebuilt table
+ *   workspace_bytes  the workspace the call will pass (0 for none), 256-byte aligned
+ */
+PBS_API int pbs_prefill_kernel_choice(int32_t total_q, int32_t num_reqs, int32_t kv_dtype, int64_t page_stride_bytes,
+                                      int32_t num_heads, int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks,
+                                      int32_t with_table, size_t workspace_bytes,
+                                      const pbs_attend_options* options);
 
 /*
  * Bytes of the workspace with which pbs_sparse_prefill_attention runs a call of `total_q`
@@ -282,11 +362,12 @@ PBS_API size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv
  * decode_query_len, are decode rows read with dec_page_table / dec_seq_lens / decode_query_len
  * as in pbs_sparse_decode_attention; rows [nd, nd + total_q) are prefill tokens read with
  * pre_page_table / cu_seqlens_q / pre_seq_lens as in pbs_sparse_prefill_attention. q, topk,
- * out and lse are indexed by that row over both parts. Where the prefill part takes the tcgen05
- * tile kernel this issues the two calls on `stream`, decode first (what the page's forward
- * does); otherwise it is one launch of the token-centric kernel, whose CTAs take their part by
- * row, so the decode rows run beside the prefill tokens. No workspace. Errors as in the two
- * calls; with no rows in one part it is that part's call.
+ * out, lse and the optional prebuilt table (sparse_bt / sparse_ctx rows, as in the two calls)
+ * are indexed by that row over both parts. Where the prefill part takes a tcgen05 kernel this
+ * issues the two calls on `stream`, decode first (what the page's forward does); otherwise it is
+ * one launch of the token-centric kernel, whose CTAs take their part by row, so the decode rows
+ * run beside the prefill tokens. No workspace (the tile kernel runs its bf16 hi + lo path).
+ * Errors as in the two calls; with no rows in one part it is that part's call.
  */
 PBS_API int pbs_sparse_mixed_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -297,9 +378,12 @@ PBS_API int pbs_sparse_mixed_attention(
     const int32_t* dec_seq_lens, int32_t batch, int32_t decode_query_len,
     const int32_t* pre_page_table, int64_t pre_pt_row_stride, int32_t pre_max_blocks,
     const int32_t* cu_seqlens_q, const int32_t* pre_seq_lens, int32_t num_reqs, int32_t total_q,
-    int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
+    int32_t block_page_stride,
+    const int32_t* sparse_bt, int64_t sbt_row_stride, const int32_t* sparse_ctx,
+    float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
     float* lse, int64_t lse_row_stride,
+    const pbs_attend_options* options,
     int32_t* err_word, pbs_stream_t stream);
 
 /*

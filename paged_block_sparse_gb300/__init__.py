@@ -21,14 +21,25 @@ __all__ = [
     "abi_version", "status_string", "build_sparse_block_table_decode", "build_sparse_block_table_prefill",
     "sparse_decode_attention", "sparse_prefill_attention", "insert_index_cache", "DEVERR",
     "attend_workspace_bytes", "attend_workspace", "sparse_decode_attention_noalloc", "sparse_mixed_attention",
-    "prefill_workspace_bytes", "prefill_workspace",
+    "prefill_workspace_bytes", "prefill_workspace", "prefill_tile_workspace_bytes", "prefill_tile_workspace",
+    "prefill_kernel_choice", "PREFILL_KERNELS",
 ]
 
 SPARSE_BLOCK_SIZE = 128
 PAGE_ROWS = 16
 PAGES_PER_BLOCK = 8
 KV_DTYPES = {"bf16": 0, "fp8_e4m3": 1, "nvfp4": 2}
-DEVERR = {"block_oob": 1, "page_oob": 2, "slot_oob": 4, "timeout": 8}
+DEVERR = {"block_oob": 1, "page_oob": 2, "slot_oob": 4, "timeout": 8, "table": 16}
+# prefill kernels (pbs_attend_options.prefill_kernel / pbs_prefill_kernel_choice)
+PREFILL_KERNELS = {"auto": 0, "token": 1, "tile": 2, "gather": 3}
+_PREFILL_NAMES = {v: k for k, v in PREFILL_KERNELS.items()}
+
+
+class _Options(ctypes.Structure):
+    """pbs_attend_options (include/pbs.h)."""
+    _fields_ = [("prefill_kernel", ctypes.c_int32), ("splits", ctypes.c_int32), ("cache_map", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -65,24 +76,28 @@ def lib() -> ctypes.CDLL:
     L.pbs_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     L.pbs_prefill_tile_workspace_bytes.restype = ctypes.c_size_t
     L.pbs_prefill_tile_workspace_bytes.argtypes = [i32, i32, i32]
+    L.pbs_prefill_kernel_choice.restype = ctypes.c_int
+    L.pbs_prefill_kernel_choice.argtypes = [i32, i32, i32, i64, i32, i32, i32, i32, i32, ctypes.c_size_t, vp]
     table_common = [vp, i64, i32, i32, vp, i64, i32]
     L.pbs_build_sparse_block_table_decode.restype = ctypes.c_int
     L.pbs_build_sparse_block_table_decode.argtypes = table_common + [vp, i32, i32, i32, vp, i64, vp, vp, vp]
     L.pbs_build_sparse_block_table_prefill.restype = ctypes.c_int
     L.pbs_build_sparse_block_table_prefill.argtypes = table_common + [vp, vp, i32, i32, vp, i64, vp, vp, vp]
     attend_head = [vp, i64, i64, vp, i64, i64, i32, i32, i32, i32, vp, i64, i32, vp, i64, i32]
+    table = [vp, i64, vp]
     L.pbs_sparse_decode_attention.restype = ctypes.c_int
-    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64, vp, i64,
-                                                            vp, ctypes.c_size_t, vp, vp]
+    L.pbs_sparse_decode_attention.argtypes = attend_head + [vp, i32, i32, i32] + table + [
+        f32, f32, f32, vp, i64, i64, vp, i64, vp, ctypes.c_size_t, vp, vp, vp]
     L.pbs_sparse_decode_attention_noalloc.restype = ctypes.c_int
     L.pbs_sparse_decode_attention_noalloc.argtypes = attend_head + [vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
-                                                                    vp, vp]
+                                                                    vp, vp, vp]
     L.pbs_sparse_prefill_attention.restype = ctypes.c_int
-    L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32, f32, f32, f32, vp, i64, i64,
-                                                             vp, i64, vp, ctypes.c_size_t, vp, vp]
+    L.pbs_sparse_prefill_attention.argtypes = attend_head + [vp, vp, i32, i32, i32] + table + [
+        f32, f32, f32, vp, i64, i64, vp, i64, vp, ctypes.c_size_t, vp, vp, vp]
     L.pbs_sparse_mixed_attention.restype = ctypes.c_int
     L.pbs_sparse_mixed_attention.argtypes = attend_head[:13] + [vp, i64, i32, vp, i32, i32, vp, i64, i32, vp, vp, i32,
-                                                                i32, i32, f32, f32, f32, vp, i64, i64, vp, i64, vp, vp]
+                                                                i32, i32] + table + [
+        f32, f32, f32, vp, i64, i64, vp, i64, vp, vp, vp]
     L.pbs_insert_index_cache.restype = ctypes.c_int
     L.pbs_insert_index_cache.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32, vp, i64, i32, vp, vp]
     del sz
@@ -146,6 +161,34 @@ def _table2d(t: torch.Tensor, name: str) -> torch.Tensor:
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError(f"{name} must be [rows, cols] with a contiguous last dimension")
     return t
+
+
+def _options(kernel=None, splits=None, cache_map=None):
+    """A pbs_attend_options pointer for the call (None: the library's own choices).
+
+    kernel: None / "auto" / "token" / "tile" / "gather" (prefill); splits: None or 1, 2, 4, 8;
+    cache_map: None or "quarter" (the token-centric kernel's per-row-quarter cache map)."""
+    if kernel in (None, "auto") and splits is None and cache_map is None:
+        return None
+    if kernel not in (None, *PREFILL_KERNELS):
+        raise ValueError(f"kernel must be one of {sorted(PREFILL_KERNELS)}")
+    if cache_map not in (None, "quarter"):
+        raise ValueError('cache_map must be None or "quarter"')
+    o = _Options(PREFILL_KERNELS[kernel or "auto"], int(splits or 0), 1 if cache_map == "quarter" else 0, 0)
+    return ctypes.byref(o)
+
+
+def _table_args(sparse_table, rows):
+    """(sparse_bt pointer, row stride, sparse_ctx pointer) of an optional prebuilt table
+    ``(sparse_bt [rows, >= topk*8] int32, sparse_ctx [rows] int32)`` as the builders return it."""
+    if sparse_table is None:
+        return ctypes.c_void_p(0), 0, ctypes.c_void_p(0)
+    sbt, ctx = sparse_table
+    _table2d(sbt, "sparse_bt")
+    _dev(ctx, "sparse_ctx", torch.int32)
+    if sbt.shape[0] != rows or ctx.shape[0] != rows or ctx.dim() != 1 or (rows > 1 and ctx.stride(0) != 1):
+        raise ValueError(f"sparse_table must be ([{rows}, >= topk*8], [{rows}]) int32 with contiguous rows")
+    return _ptr(sbt), sbt.stride(0), _ptr(ctx)
 
 
 def _cache_geometry(kv_cache: torch.Tensor):
@@ -300,14 +343,18 @@ def prefill_tile_workspace(num_reqs: int, num_kv_heads: int, max_blocks: int, de
     return ws
 
 
-def _tile_kernel_runs(kv_dtype, num_heads, num_kv_heads, topk, max_blocks, page_stride_bytes, forced) -> bool:
-    """Whether a prefill call goes to the tcgen05 tile kernel (the library's rule: bf16 packed cache,
-    GQA 8 or 16, top-k <= 16, a page table at most 8 x top-k blocks wide, or PBS_PREFILL_KERNEL=tc)."""
-    if forced == "token" or kv_dtype != "bf16" or num_heads % num_kv_heads or topk > 16:
-        return False
-    if num_heads // num_kv_heads not in (8, 16) or page_stride_bytes != num_kv_heads * 8192 or max_blocks > 128:
-        return False
-    return forced == "tc" or max_blocks <= 8 * topk
+def prefill_kernel_choice(total_q: int, num_reqs: int, kv_dtype: str, page_stride_bytes: int, num_heads: int,
+                          num_kv_heads: int, topk: int, max_blocks: int, with_table: bool = False,
+                          workspace_bytes: int = 0, kernel=None) -> str:
+    """The prefill kernel the library runs for a call of this shape ("token", "tile" or "gather"),
+    asked from the library itself (pbs_prefill_kernel_choice): the binding sizes the workspace the
+    chosen kernel wants from it."""
+    r = int(lib().pbs_prefill_kernel_choice(int(total_q), int(num_reqs), KV_DTYPES[kv_dtype], int(page_stride_bytes),
+                                            int(num_heads), int(num_kv_heads), int(topk), int(max_blocks),
+                                            1 if with_table else 0, int(workspace_bytes), _options(kernel)))
+    if r < 0:
+        raise PbsError(-r, "pbs_prefill_kernel_choice")
+    return _PREFILL_NAMES[r]
 
 
 # the default prefill workspace is capped; larger calls run in several token segments
@@ -350,7 +397,8 @@ def _lse_arg(lse, return_lse, q):
 def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
                             decode_query_len: int, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                             block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                            workspace=None, lse=None, return_lse: bool = False):
+                            workspace=None, lse=None, return_lse: bool = False, sparse_table=None, splits=None,
+                            cache_map=None):
     """Sparse decode attend (vLLM flashinfer msa_sparse_decode_attention / nvfp4 decode call).
 
     q [rows, Hq, 128] bf16 with rows = batch * decode_query_len; kv_cache [num_pages, ...] in the
@@ -359,17 +407,23 @@ def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk,
     per-stream buffer) or a zeroed uint8 tensor of at least
     ``attend_workspace_bytes(rows, Hq, num_kv_heads)`` bytes; with one, splits merge through it.
     With ``return_lse`` (or an ``lse`` tensor [rows, Hq] fp32) the natural-log log-sum-exp of each
-    head's scaled logits is written too and ``(out, lse)`` is returned."""
+    head's scaled logits is written too and ``(out, lse)`` is returned. ``sparse_table``: an
+    optional prebuilt ``(sparse_bt, sparse_ctx)`` pair (what :func:`build_sparse_block_table_decode`
+    returns, built once and shared by every sparse layer of a step): the kernel attends it
+    instead of compacting each row from ``topk``. ``splits`` / ``cache_map``: see
+    ``pbs_attend_options``."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
+    tb, ts, tc = _table_args(sparse_table, q.shape[0])
     st = lib().pbs_sparse_decode_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
-        _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), float(softmax_scale),
+        _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), tb, ts, tc, float(softmax_scale),
         float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
-        lse.stride(0) if lse is not None else 0, wp, wb, _ptr(err_word), _stream(stream, q.device))
+        lse.stride(0) if lse is not None else 0, wp, wb, _options(None, splits, cache_map), _ptr(err_word),
+        _stream(stream, q.device))
     _check(st, "pbs_sparse_decode_attention")
     return (out, lse) if lse is not None else out
 
@@ -377,12 +431,12 @@ def sparse_decode_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk,
 def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, seq_lens,
                                     decode_query_len: int, softmax_scale: float, out, k_scale: float = 1.0,
                                     v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK, err_word=None,
-                                    stream=None):
+                                    stream=None, splits=None):
     """:func:`sparse_decode_attention` for callers that may not allocate device memory: split
     partials go to a fixed 4 MiB scratch inside the library, and ``out`` must be given (this
     wrapper allocates nothing either). Calls that could overlap on one device (other streams,
     unordered threads) race on the scratch; the first call on a device does a one-time address
-    lookup and should come before any stream capture."""
+    lookup and should come before any stream capture. ``splits`` forces the split count."""
     if out is None:
         raise ValueError("out is required: the no-allocation entry allocates nothing")
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
@@ -391,8 +445,8 @@ def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: in
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
         _ptr(sl), sl.shape[0], int(decode_query_len), int(block_page_stride), float(softmax_scale),
-        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(err_word),
-        _stream(stream, q.device))
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _options(None, splits),
+        _ptr(err_word), _stream(stream, q.device))
     _check(st, "pbs_sparse_decode_attention_noalloc")
     return out
 
@@ -400,35 +454,40 @@ def sparse_decode_attention_noalloc(q, kv_cache, kv_dtype: str, num_kv_heads: in
 def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, page_table, cu_seqlens_q,
                              seq_lens, softmax_scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                              block_page_stride: int = PAGES_PER_BLOCK, out=None, err_word=None, stream=None,
-                             workspace="auto", lse=None, return_lse: bool = False):
+                             workspace="auto", lse=None, return_lse: bool = False, sparse_table=None, kernel=None,
+                             splits=None, cache_map=None):
     """Sparse prefill attend, varlen (vLLM flashinfer msa_sparse_attention / nvfp4 prefill call).
 
-    ``workspace``: "auto" (the default: a cached per-stream buffer, from :func:`prefill_workspace`
-    when PBS_PREFILL_KERNEL=gather asks for the gathered-row kernel, else the tile kernel's
-    converted-V buffer from :func:`prefill_tile_workspace`), None (no scratch: the tile kernel
-    applies bf16 P as hi + lo parts) or a uint8 CUDA tensor (see ``pbs_sparse_prefill_attention``
-    in include/pbs.h for how each kernel uses it). ``lse`` and ``return_lse`` as in
-    :func:`sparse_decode_attention`."""
+    ``workspace``: "auto" (the default: a cached per-stream buffer sized for the kernel the library
+    picks, :func:`prefill_kernel_choice`: the gathered-row kernel's :func:`prefill_workspace`, the
+    tile kernel's converted-V :func:`prefill_tile_workspace`, none for the token-centric kernel),
+    None (no scratch: the tile kernel applies bf16 P as hi + lo parts) or a uint8 CUDA tensor (see
+    ``pbs_sparse_prefill_attention`` in include/pbs.h for how each kernel uses it). ``lse`` and
+    ``return_lse`` as in :func:`sparse_decode_attention`; ``sparse_table`` the optional prebuilt
+    ``(sparse_bt, sparse_ctx)`` of :func:`build_sparse_block_table_prefill`; ``kernel`` ("token",
+    "tile", "gather"), ``splits`` and ``cache_map``: see ``pbs_attend_options``."""
     num_pages, psb, tk, pt, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, page_table, out)
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     if isinstance(workspace, str) and workspace == "auto":
-        forced = os.environ.get("PBS_PREFILL_KERNEL")
-        if forced == "gather":
+        if kernel == "gather":
             workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
                                           pt.shape[1], q.device, stream)
-        elif _tile_kernel_runs(kv_dtype, q.shape[1], num_kv_heads, tk.shape[1], pt.shape[1], psb, forced):
+        elif prefill_kernel_choice(q.shape[0], sl.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads, tk.shape[1],
+                                   pt.shape[1], sparse_table is not None, 0, kernel) == "tile":
             workspace = prefill_tile_workspace(sl.shape[0], num_kv_heads, pt.shape[1], q.device, stream)
         else:
             workspace = None  # the token-centric kernel merges its splits in a cluster
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
+    tb, ts, tc = _table_args(sparse_table, q.shape[0])
     st = lib().pbs_sparse_prefill_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt), pt.stride(0), pt.shape[1],
-        _ptr(cu), _ptr(sl), sl.shape[0], q.shape[0], int(block_page_stride), float(softmax_scale), float(k_scale),
-        float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0) if lse is not None else 0,
-        wp, wb, _ptr(err_word), _stream(stream, q.device))
+        _ptr(cu), _ptr(sl), sl.shape[0], q.shape[0], int(block_page_stride), tb, ts, tc, float(softmax_scale),
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
+        lse.stride(0) if lse is not None else 0, wp, wb, _options(kernel, splits, cache_map), _ptr(err_word),
+        _stream(stream, q.device))
     _check(st, "pbs_sparse_prefill_attention")
     return (out, lse) if lse is not None else out
 
@@ -436,10 +495,11 @@ def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk
 def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, dec_page_table, dec_seq_lens,
                            decode_query_len: int, pre_page_table, cu_seqlens_q, pre_seq_lens, softmax_scale: float,
                            k_scale: float = 1.0, v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK,
-                           out=None, err_word=None, stream=None, lse=None, return_lse: bool = False):
+                           out=None, err_word=None, stream=None, lse=None, return_lse: bool = False,
+                           sparse_table=None, kernel=None, splits=None, cache_map=None):
     """Decode rows then prefill tokens in one call (vLLM flashinfer forward with both parts):
-    q [nd + total_q, Hq, 128] with nd = len(dec_seq_lens) * decode_query_len; topk one row per
-    q row. Returns out (and lse)."""
+    q [nd + total_q, Hq, 128] with nd = len(dec_seq_lens) * decode_query_len; topk (and the
+    optional prebuilt ``sparse_table``) one row per q row. Returns out (and lse)."""
     num_pages, psb, tk, pt_d, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, dec_page_table, out)
     pt_p = _table2d(pre_page_table, "pre_page_table")
     sl_d = _dev(dec_seq_lens, "dec_seq_lens", torch.int32)
@@ -450,13 +510,15 @@ def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, 
     if total_q < 0:
         raise ValueError(f"q has {q.shape[0]} rows, fewer than the {nd} decode rows")
     lse = _lse_arg(lse, return_lse, q)
+    tb, ts, tc = _table_args(sparse_table, q.shape[0])
     st = lib().pbs_sparse_mixed_attention(
         _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), psb, num_pages, KV_DTYPES[kv_dtype], q.shape[1],
         int(num_kv_heads), q.shape[2], _ptr(tk), tk.stride(0), tk.shape[1], _ptr(pt_d), pt_d.stride(0),
         pt_d.shape[1], _ptr(sl_d), sl_d.shape[0], int(decode_query_len), _ptr(pt_p), pt_p.stride(0), pt_p.shape[1],
-        _ptr(cu), _ptr(sl_p), sl_p.shape[0], total_q, int(block_page_stride), float(softmax_scale), float(k_scale),
-        float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0) if lse is not None else 0,
-        _ptr(err_word), _stream(stream, q.device))
+        _ptr(cu), _ptr(sl_p), sl_p.shape[0], total_q, int(block_page_stride), tb, ts, tc, float(softmax_scale),
+        float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
+        lse.stride(0) if lse is not None else 0, _options(kernel, splits, cache_map), _ptr(err_word),
+        _stream(stream, q.device))
     _check(st, "pbs_sparse_mixed_attention")
     return (out, lse) if lse is not None else out
 

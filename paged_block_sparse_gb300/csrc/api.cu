@@ -2,7 +2,6 @@
 // launch-shape choice and dispatch to the kernels. Nothing here allocates device memory.
 #include <algorithm>
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -74,7 +73,7 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_
 // (page, kv head): a 5-D map {row bytes' first 128 B, 8 rows, q, 2 row halves, page * Hkv + head}
 // whose box lands as [row half][q][8 rows][128 B], q = the four 64-element quarters of a bf16 row
 // (K lo, K hi, V lo, V hi) or the two halves of an fp8 row (K, V): 128B-swizzle atoms of 8 rows.
-// Every address stays inside its own (page, head) chunk. PBS_CACHE_MAP=4d disables it (tests).
+// Every address stays inside its own (page, head) chunk.
 // With quarters_per_box = 2 (bf16 only) a box holds either the K or the V half of every row
 // (quarter coordinate 0 or 2), landing as [row half][2][8 rows][128 B].
 int encode_cache_map_packed(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
@@ -83,8 +82,6 @@ int encode_cache_map_packed(CUtensorMap* map, const void* cache, int kv_dtype, i
   if (kv_dtype != PBS_KV_BF16 && kv_dtype != PBS_KV_FP8_E4M3) return PBS_ERR_UNSUPPORTED;
   if (page_stride_bytes != page_content_bytes(kv_dtype, num_kv_heads)) return PBS_ERR_UNSUPPORTED;
   if (num_pages * num_kv_heads > 0x7fffffffLL) return PBS_ERR_UNSUPPORTED;
-  if (const char* env = std::getenv("PBS_CACHE_MAP"))
-    if (std::strcmp(env, "4d") == 0) return PBS_ERR_UNSUPPORTED;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return PBS_ERR_CUDA;
   const bool bf = kv_dtype == PBS_KV_BF16;
@@ -127,11 +124,13 @@ int encode_cache_map_block(CUtensorMap* map, const void* cache, int num_kv_heads
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
-// The tensor map the token-centric kernel reads: the packed one when the cache allows it.
+// The tensor map the token-centric kernel reads: the packed one when the cache allows it and the
+// caller did not ask for the per-quarter map.
 int encode_attend_map(CUtensorMap* map, const void* cache, int kv_dtype, int num_kv_heads, int64_t num_pages,
-                      int64_t page_stride_bytes, int32_t* packed) {
+                      int64_t page_stride_bytes, bool quarter_map, int32_t* packed) {
   *packed = 0;
-  if (encode_cache_map_packed(map, cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes) == PBS_OK) {
+  if (!quarter_map &&
+      encode_cache_map_packed(map, cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes) == PBS_OK) {
     *packed = 1;
     return PBS_OK;
   }
@@ -158,12 +157,12 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
-// Which prefill kernel runs. With a workspace that holds at least one 256-token segment, shapes
-// the gathered-row kernel takes (bf16 packed cache, GQA 8 or 16, page table <= 8192 blocks) run
-// on it: its MMA rows are the tokens that selected a block, so its work does not grow with the
-// context the selections are spread over. Otherwise the tcgen05 tile kernel where it applies,
-// the token-centric kernel elsewhere. PBS_PREFILL_KERNEL=gather|tc|token requires that kernel
-// (tests, tuning).
+// Which prefill kernel runs: the caller's choice (pbs_attend_options.prefill_kernel) when given,
+// else the tcgen05 tile kernel where it applies and the token-centric kernel elsewhere. The
+// gathered-row kernel (bf16 packed cache, GQA 8 or 16, page table <= 8192 blocks, a workspace of
+// at least one 256-token segment) runs only when asked for: its MMA rows are the tokens that
+// selected a block, so its work does not grow with the context the selections are spread over,
+// but its partial outputs cost more than the tile kernel's waste on the measured workloads.
 //
 // The tile kernel streams the union of its 16 tokens' selections to all of them, so its waste
 // grows with the context a token chooses from: a token at block s selects k of s + 1 blocks,
@@ -173,36 +172,42 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
 // tokens): contexts 0 / 2k-4k / 16k-32k give 462 / 312 / 114 TFLOP/s on the tile kernel and
 // 133 / 139 / 139 on the token-centric one.
 constexpr int kTileMaxBlocksPerTopk = 8;
-// The gathered-row kernel is taken without PBS_PREFILL_KERNEL=gather only once it outruns the
-// other two on the prefill workloads.
-constexpr bool kGatherByDefault = false;
-enum PrefillKernel { kPrefillToken = 0, kPrefillTile = 1, kPrefillGather = 2 };
 
-int prefill_kernel_override() {
-  if (const char* env = std::getenv("PBS_PREFILL_KERNEL")) {
-    if (std::strcmp(env, "token") == 0) return 1;
-    if (std::strcmp(env, "tc") == 0) return 2;
-    if (std::strcmp(env, "gather") == 0) return 3;
-  }
-  return 0;
+// The caller's options, checked (a null pointer reads as all zero).
+struct Options {
+  int prefill_kernel = PBS_PREFILL_AUTO;
+  int splits = 0;
+  bool quarter_map = false;
+};
+
+int read_options(const pbs_attend_options* o, Options* out) {
+  *out = Options();
+  if (o == nullptr) return PBS_OK;
+  if (o->prefill_kernel < PBS_PREFILL_AUTO || o->prefill_kernel > PBS_PREFILL_GATHER) return PBS_ERR_ARG;
+  if (o->splits != 0 && o->splits != 1 && o->splits != 2 && o->splits != 4 && o->splits != 8) return PBS_ERR_ARG;
+  if (o->cache_map != 0 && o->cache_map != 1) return PBS_ERR_ARG;
+  if (o->reserved != 0) return PBS_ERR_ARG;
+  out->prefill_kernel = o->prefill_kernel;
+  out->splits = o->splits;
+  out->quarter_map = o->cache_map == 1;
+  return PBS_OK;
 }
 
-// Sets *kernel for a prefill call whose AttendArgs (map already encoded) are `a`, given the
-// caller's workspace size; PBS_ERR_UNSUPPORTED when PBS_PREFILL_KERNEL asks for a kernel that
-// cannot run the call.
-int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, PrefillKernel* kernel) {
-  const int force = prefill_kernel_override();
+// Sets *kernel (PBS_PREFILL_TOKEN / _TILE / _GATHER) for a prefill call whose AttendArgs (map
+// already encoded, table attached) are `a`, given the caller's workspace size and option;
+// PBS_ERR_UNSUPPORTED when the option asks for a kernel that cannot run the call. The one rule
+// behind both the call and pbs_prefill_kernel_choice.
+int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int forced, int* kernel) {
   // the tcgen05 kernels read the packed bf16 cache through the 5-D map
   const bool tile_fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
   const bool gather_fits = a.packed_map != 0 && pbs::prefill_gather_supported(a) && a.num_rows < (1 << 25) &&
                            pbs::gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k,
                                                       a.max_blocks, workspace_bytes) > 0;
-  if ((force == 2 && !tile_fits) || (force == 3 && !gather_fits)) return PBS_ERR_UNSUPPORTED;
-  if (force == 1) *kernel = kPrefillToken;
-  else if (force == 2) *kernel = kPrefillTile;
-  else if (force == 3 || (gather_fits && kGatherByDefault)) *kernel = kPrefillGather;
-  else if (tile_fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k) *kernel = kPrefillTile;
-  else *kernel = kPrefillToken;
+  if ((forced == PBS_PREFILL_TILE && !tile_fits) || (forced == PBS_PREFILL_GATHER && !gather_fits))
+    return PBS_ERR_UNSUPPORTED;
+  if (forced != PBS_PREFILL_AUTO) *kernel = forced;
+  else if (tile_fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k) *kernel = PBS_PREFILL_TILE;
+  else *kernel = PBS_PREFILL_TOKEN;
   return PBS_OK;
 }
 
@@ -211,8 +216,7 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, PrefillKe
 // per split; measured on the 64-request decode workload (512 row x head units, 2 CTAs per SM)
 // one CTA per unit streams at 75% of HBM peak against 61% / 57% / 43% for 2 / 4 / 8 splits.
 // So rows are split only while the units alone cannot fill every SM twice, and only while
-// each split keeps at least four 128-key slots. PBS_ATTEND_SPLITS in {1, 2, 4, 8} overrides
-// (tuning and tests).
+// each split keeps at least four 128-key slots. The caller's option (1, 2, 4 or 8) overrides.
 //
 // With a workspace the splits merge through it instead (no cluster, no waiting: the last chunk
 // of a row merges), so any split count up to 8 schedules freely; a row is cut into chunks while
@@ -224,11 +228,8 @@ int num_sms() {
   return sms;
 }
 
-int choose_splits(int64_t units, int k, bool workspace) {
-  if (const char* env = std::getenv("PBS_ATTEND_SPLITS")) {
-    const int s = std::atoi(env);
-    if (s == 1 || s == 2 || s == 4 || s == 8) return s;
-  }
+int choose_splits(int64_t units, int k, bool workspace, int forced) {
+  if (forced != 0) return forced;
   const int64_t sms = num_sms();
   int s = 1;
   if (workspace) {
@@ -266,8 +267,8 @@ int attach_workspace(AttendArgs* a, int64_t units, void* workspace, size_t works
 }
 
 int check_common_table(const int32_t* topk, int64_t topk_row_stride, int32_t topk_k, const int32_t* page_table,
-                       int64_t pt_row_stride, int32_t max_blocks, int32_t block_page_stride) {
-  if (topk == nullptr || page_table == nullptr) return PBS_ERR_ARG;
+                       int64_t pt_row_stride, int32_t max_blocks, int32_t block_page_stride, bool topk_optional = false) {
+  if ((topk == nullptr && !topk_optional) || page_table == nullptr) return PBS_ERR_ARG;
   if (topk_k <= 0 || max_blocks <= 0) return PBS_ERR_ARG;
   if (topk_k > kMaxTopk) return PBS_ERR_UNSUPPORTED;
   if (topk_row_stride < topk_k || pt_row_stride < max_blocks) return PBS_ERR_SHAPE;
@@ -294,6 +295,21 @@ int check_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride, con
   if (!aligned(kv_cache, 16) || page_stride_bytes % 16 != 0) return PBS_ERR_ALIGN;
   if (!aligned(q, 4) || q_row_stride % 2 != 0 || q_head_stride % 2 != 0) return PBS_ERR_ALIGN;
   if (!aligned(out, 2)) return PBS_ERR_ALIGN;
+  return PBS_OK;
+}
+
+// An optional prebuilt table ([rows, >= k * 8] page ids and per-row ctx): both or neither.
+int attach_table(AttendArgs* a, const int32_t* sparse_bt, int64_t sbt_row_stride, const int32_t* sparse_ctx) {
+  a->sparse_bt = nullptr;
+  a->sbt_row_stride = 0;
+  a->sparse_ctx = nullptr;
+  if (sparse_bt == nullptr && sparse_ctx == nullptr) return PBS_OK;
+  if (sparse_bt == nullptr || sparse_ctx == nullptr) return PBS_ERR_ARG;
+  if (sbt_row_stride < static_cast<int64_t>(a->k) * kBlockPages) return PBS_ERR_SHAPE;
+  if (!aligned(sparse_bt, 4) || !aligned(sparse_ctx, 4)) return PBS_ERR_ALIGN;
+  a->sparse_bt = sparse_bt;
+  a->sbt_row_stride = sbt_row_stride;
+  a->sparse_ctx = sparse_ctx;
   return PBS_OK;
 }
 
@@ -363,18 +379,42 @@ namespace {
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+CUcontext g_noalloc_ctx[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per device (the lookup
-// may load this library's device module, which is why the first call should come before any
-// stream capture begins).
+// The driver's cuCtxGetCurrent, reached through the runtime's entry-point query (the library
+// links no driver library).
+PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  return fn;
+}
+
+// Device address of the scratch on the current device, looked up once per device and context
+// (the lookup may load this library's device module, which is why the first call should come
+// before any stream capture begins). A new context on the device (after a reset the module, and
+// the array with it, is loaded again) triggers a new lookup, so a stale address is never used.
 int noalloc_scratch(void** addr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return PBS_ERR_CUDA;
+  auto get_ctx = ctx_getter();
+  if (get_ctx == nullptr) return PBS_ERR_CUDA;
+  // null until the runtime has made the device's context current (the lookup below does)
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return PBS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  if (g_noalloc_addr[dev] == nullptr || ctx == nullptr || g_noalloc_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PBS_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return PBS_ERR_CUDA;
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *addr = g_noalloc_addr[dev];
   return PBS_OK;
@@ -398,7 +438,7 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 7; }
+int pbs_abi_version(void) { return 8; }
 
 size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
   if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
@@ -476,19 +516,23 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                 int32_t num_kv_heads, int32_t head_dim, const int32_t* topk, int64_t topk_row_stride,
                                 int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
                                 const int32_t* seq_lens, int32_t batch, int32_t decode_query_len,
-                                int32_t block_page_stride, float softmax_scale, float k_scale, float v_scale,
+                                int32_t block_page_stride, const int32_t* sparse_bt, int64_t sbt_row_stride,
+                                const int32_t* sparse_ctx, float softmax_scale, float k_scale, float v_scale,
                                 void* out, int64_t out_row_stride, int64_t out_head_stride, float* lse,
-                                int64_t lse_row_stride, void* workspace, size_t workspace_bytes, int32_t* err_word,
-                                pbs_stream_t stream) {
+                                int64_t lse_row_stride, void* workspace, size_t workspace_bytes,
+                                const pbs_attend_options* options, int32_t* err_word, pbs_stream_t stream) {
   if (batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
   const int64_t rows = static_cast<int64_t>(batch) * decode_query_len;
   if (rows == 0) return PBS_OK;
   if (rows > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
-  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
-                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
-                        out_head_stride);
+  Options opt;
+  int st = read_options(options, &opt);
   if (st != PBS_OK) return st;
-  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                    num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride,
+                          sparse_bt != nullptr);
   if (st != PBS_OK) return st;
   if (seq_lens == nullptr) return PBS_ERR_ARG;
   AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
@@ -497,14 +541,17 @@ int pbs_sparse_decode_attention(const void* q, int64_t q_row_stride, int64_t q_h
                                   out_row_stride, out_head_stride, err_word);
   a.decode_query_len = decode_query_len;
   a.num_rows = static_cast<int32_t>(rows);
+  st = attach_table(&a, sparse_bt, sbt_row_stride, sparse_ctx);
+  if (st != PBS_OK) return st;
   st = attach_lse(&a, lse, lse_row_stride);
   if (st != PBS_OK) return st;
   const int64_t units = pbs::attend_units(rows, num_kv_heads, a.group);
   st = attach_workspace(&a, units, workspace, workspace_bytes);
   if (st != PBS_OK) return st;
-  a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
+  a.splits = choose_splits(units, topk_k, a.split_ws != nullptr, opt.splits);
   CUtensorMap map;
-  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, opt.quarter_map,
+                         &a.packed_map);
   if (st != PBS_OK) return st;
   return pbs::launch_attend(a, pbs::kModeDecode, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
                                                                                                   : PBS_ERR_CUDA;
@@ -518,12 +565,15 @@ int pbs_sparse_decode_attention_noalloc(const void* q, int64_t q_row_stride, int
                                         const int32_t* seq_lens, int32_t batch, int32_t decode_query_len,
                                         int32_t block_page_stride, float softmax_scale, float k_scale,
                                         float v_scale, void* out, int64_t out_row_stride, int64_t out_head_stride,
-                                        int32_t* err_word, pbs_stream_t stream) {
+                                        const pbs_attend_options* options, int32_t* err_word, pbs_stream_t stream) {
   if (batch < 0 || decode_query_len <= 0) return PBS_ERR_ARG;
   const int64_t rows = static_cast<int64_t>(batch) * decode_query_len;
   if (rows == 0) return PBS_OK;
   if (rows > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
-  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+  Options opt;
+  int st = read_options(options, &opt);
+  if (st != PBS_OK) return st;
+  st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
                         num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
                         out_head_stride);
   if (st != PBS_OK) return st;
@@ -542,7 +592,7 @@ int pbs_sparse_decode_attention_noalloc(const void* q, int64_t q_row_stride, int
   st = noalloc_scratch(&scratch);
   if (st != PBS_OK) return st;
   const int64_t units = pbs::attend_units(rows, num_kv_heads, a.group);
-  a.splits = choose_splits(units, topk_k, true);
+  a.splits = choose_splits(units, topk_k, true, opt.splits);
   a.split_ws = nullptr;
   a.split_tickets = nullptr;
   if (a.splits > 1) {
@@ -552,7 +602,7 @@ int pbs_sparse_decode_attention_noalloc(const void* q, int64_t q_row_stride, int
     a.split_tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kNoAllocScratchBytes) - units;
   }
   CUtensorMap map;
-  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, false, &a.packed_map);
   if (st != PBS_OK) return st;
   return pbs::launch_attend(a, pbs::kModeDecode, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PBS_OK
                                                                                                   : PBS_ERR_CUDA;
@@ -563,19 +613,24 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
                                  int32_t num_kv_heads, int32_t head_dim, const int32_t* topk, int64_t topk_row_stride,
                                  int32_t topk_k, const int32_t* page_table, int64_t pt_row_stride, int32_t max_blocks,
                                  const int32_t* cu_seqlens_q, const int32_t* seq_lens, int32_t num_reqs,
-                                 int32_t total_q, int32_t block_page_stride, float softmax_scale, float k_scale,
-                                 float v_scale, void* out, int64_t out_row_stride, int64_t out_head_stride,
-                                 float* lse, int64_t lse_row_stride, void* workspace, size_t workspace_bytes,
-                                 int32_t* err_word, pbs_stream_t stream) {
+                                 int32_t total_q, int32_t block_page_stride, const int32_t* sparse_bt,
+                                 int64_t sbt_row_stride, const int32_t* sparse_ctx, float softmax_scale,
+                                 float k_scale, float v_scale, void* out, int64_t out_row_stride,
+                                 int64_t out_head_stride, float* lse, int64_t lse_row_stride, void* workspace,
+                                 size_t workspace_bytes, const pbs_attend_options* options, int32_t* err_word,
+                                 pbs_stream_t stream) {
   if (total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
   if (total_q == 0) return PBS_OK;
   if (num_reqs == 0) return PBS_ERR_SHAPE;
   if (total_q > 0x7fffffff / 8) return PBS_ERR_UNSUPPORTED;
-  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
-                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
-                        out_head_stride);
+  Options opt;
+  int st = read_options(options, &opt);
   if (st != PBS_OK) return st;
-  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride);
+  st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                    num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride);
+  if (st != PBS_OK) return st;
+  st = check_common_table(topk, topk_row_stride, topk_k, page_table, pt_row_stride, max_blocks, block_page_stride,
+                          sparse_bt != nullptr);
   if (st != PBS_OK) return st;
   if (cu_seqlens_q == nullptr || seq_lens == nullptr) return PBS_ERR_ARG;
   AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
@@ -585,19 +640,27 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
   a.cu_seqlens_q = cu_seqlens_q;
   a.num_reqs = num_reqs;
   a.num_rows = total_q;
+  st = attach_table(&a, sparse_bt, sbt_row_stride, sparse_ctx);
+  if (st != PBS_OK) return st;
   st = attach_lse(&a, lse, lse_row_stride);
   if (st != PBS_OK) return st;
   if (workspace == nullptr && workspace_bytes != 0) return PBS_ERR_ARG;
   CUtensorMap map;
-  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &a.packed_map);
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, false, &a.packed_map);
   if (st != PBS_OK) return st;
   // the gathered-row kernel lays its arrays out from a 256-byte aligned workspace base
-  PrefillKernel kernel = kPrefillToken;
-  st = choose_prefill_kernel(a, workspace != nullptr && aligned(workspace, 256) ? workspace_bytes : 0, &kernel);
+  int kernel = PBS_PREFILL_TOKEN;
+  st = choose_prefill_kernel(a, workspace != nullptr && aligned(workspace, 256) ? workspace_bytes : 0,
+                             opt.prefill_kernel, &kernel);
   if (st != PBS_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (kernel == kPrefillToken) {
+  if (kernel == PBS_PREFILL_TOKEN) {
+    if (opt.quarter_map) {  // the per-quarter map on request (it applies to this kernel only)
+      st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, true,
+                             &a.packed_map);
+      if (st != PBS_OK) return st;
+    }
     // the workspace, when it holds the split partials, merges split rows
     const int64_t units = pbs::attend_units(total_q, num_kv_heads, a.group);
     if (workspace != nullptr && workspace_bytes >= pbs::attend_workspace_bytes(units)) {
@@ -607,21 +670,21 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
       if (cudaMemsetAsync(a.split_tickets, 0, static_cast<size_t>(units) * sizeof(int32_t), cs) != cudaSuccess)
         return PBS_ERR_CUDA;
     }
-    a.splits = choose_splits(units, topk_k, a.split_ws != nullptr);
+    a.splits = choose_splits(units, topk_k, a.split_ws != nullptr, opt.splits);
     e = pbs::launch_attend(a, pbs::kModePrefill, map, cs);
   } else {
     // both tcgen05 kernels stream K and V separately: the gathered-row kernel one box per
     // (page, head) half row, the tile kernel one box per (block, head) half row
     CUtensorMap half_map;
-    st = kernel == kPrefillGather
+    st = kernel == PBS_PREFILL_GATHER
              ? encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2)
              : encode_cache_map_block(&half_map, kv_cache, num_kv_heads, num_pages, page_stride_bytes);
     if (st != PBS_OK) return st;
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride,
-                      kernel == kPrefillGather ? 1 : 0);
+                      kernel == PBS_PREFILL_GATHER ? 1 : 0);
     if (st != PBS_OK) return st;
-    if (kernel == kPrefillTile && workspace != nullptr && aligned(workspace, 256) && num_reqs <= 65535) {
+    if (kernel == PBS_PREFILL_TILE && workspace != nullptr && aligned(workspace, 256) && num_reqs <= 65535) {
       // with room for the converted V of every (request, block, kv head), the tile kernel applies
       // P in fp16 with one MMA per 16 keys instead of bf16 hi + lo
       const size_t need = pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks);
@@ -631,10 +694,42 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
                                                               pbs::kTileVBytes);
       }
     }
-    e = kernel == kPrefillGather ? pbs::launch_prefill_gather(a, half_map, qmap, workspace, workspace_bytes, cs)
-                                 : pbs::launch_prefill_tc(a, half_map, qmap, cs);
+    e = kernel == PBS_PREFILL_GATHER ? pbs::launch_prefill_gather(a, half_map, qmap, workspace, workspace_bytes, cs)
+                                     : pbs::launch_prefill_tc(a, half_map, qmap, cs);
   }
   return e == cudaSuccess ? PBS_OK : PBS_ERR_CUDA;
+}
+
+int pbs_prefill_kernel_choice(int32_t total_q, int32_t num_reqs, int32_t kv_dtype, int64_t page_stride_bytes,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks,
+                              int32_t with_table, size_t workspace_bytes, const pbs_attend_options* options) {
+  Options opt;
+  int st = read_options(options, &opt);
+  if (st != PBS_OK) return -st;
+  if (total_q <= 0 || num_reqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      topk_k <= 0 || topk_k > kMaxTopk || max_blocks <= 0 || page_content_bytes(kv_dtype, num_kv_heads) < 0)
+    return -PBS_ERR_ARG;
+  // the shape as a call would see it, with 16-byte aligned q / out rows and a cache small enough
+  // for the packed map
+  AttendArgs a = {};
+  a.kv_dtype = kv_dtype;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_heads / num_kv_heads;
+  a.k = topk_k;
+  a.max_blocks = max_blocks;
+  a.num_rows = total_q;
+  a.num_reqs = num_reqs;
+  a.page_stride_bytes = page_stride_bytes;
+  a.num_pages = 1;
+  a.q_row_stride = a.q_head_stride = a.out_row_stride = a.out_head_stride = 8;
+  static const int32_t dummy_table = 0;
+  a.sparse_bt = with_table ? &dummy_table : nullptr;
+  a.packed_map = (kv_dtype == PBS_KV_BF16 || kv_dtype == PBS_KV_FP8_E4M3) &&
+                 page_stride_bytes == page_content_bytes(kv_dtype, num_kv_heads);
+  int kernel = PBS_PREFILL_TOKEN;
+  st = choose_prefill_kernel(a, workspace_bytes, opt.prefill_kernel, &kernel);
+  return st == PBS_OK ? kernel : -st;
 }
 
 size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks) {
@@ -657,10 +752,11 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
                                int32_t dec_max_blocks, const int32_t* dec_seq_lens, int32_t batch,
                                int32_t decode_query_len, const int32_t* pre_page_table, int64_t pre_pt_row_stride,
                                int32_t pre_max_blocks, const int32_t* cu_seqlens_q, const int32_t* pre_seq_lens,
-                               int32_t num_reqs, int32_t total_q, int32_t block_page_stride, float softmax_scale,
-                               float k_scale, float v_scale, void* out, int64_t out_row_stride,
-                               int64_t out_head_stride, float* lse, int64_t lse_row_stride, int32_t* err_word,
-                               pbs_stream_t stream) {
+                               int32_t num_reqs, int32_t total_q, int32_t block_page_stride,
+                               const int32_t* sparse_bt, int64_t sbt_row_stride, const int32_t* sparse_ctx,
+                               float softmax_scale, float k_scale, float v_scale, void* out, int64_t out_row_stride,
+                               int64_t out_head_stride, float* lse, int64_t lse_row_stride,
+                               const pbs_attend_options* options, int32_t* err_word, pbs_stream_t stream) {
   if (batch < 0 || decode_query_len <= 0 || total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
   const int64_t nd = static_cast<int64_t>(batch) * decode_query_len;
   // one part only: the plain entry points
@@ -668,33 +764,37 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
     return pbs_sparse_decode_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
                                        kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,
                                        dec_page_table, dec_pt_row_stride, dec_max_blocks, dec_seq_lens, batch,
-                                       decode_query_len, block_page_stride, softmax_scale, k_scale, v_scale, out,
-                                       out_row_stride, out_head_stride, lse, lse_row_stride, nullptr, 0, err_word,
-                                       stream);
+                                       decode_query_len, block_page_stride, sparse_bt, sbt_row_stride, sparse_ctx,
+                                       softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride, lse,
+                                       lse_row_stride, nullptr, 0, options, err_word, stream);
   if (nd == 0)
     return pbs_sparse_prefill_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
                                         kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,
                                         pre_page_table, pre_pt_row_stride, pre_max_blocks, cu_seqlens_q, pre_seq_lens,
-                                        num_reqs, total_q, block_page_stride, softmax_scale, k_scale, v_scale, out,
-                                        out_row_stride, out_head_stride, lse, lse_row_stride, nullptr, 0, err_word,
-                                        stream);
+                                        num_reqs, total_q, block_page_stride, sparse_bt, sbt_row_stride, sparse_ctx,
+                                        softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride, lse,
+                                        lse_row_stride, nullptr, 0, options, err_word, stream);
   if (num_reqs == 0) return PBS_ERR_SHAPE;
   if (nd + total_q > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
-  int st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
-                        num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride,
-                        out_head_stride);
+  Options opt;
+  int st = read_options(options, &opt);
+  if (st != PBS_OK) return st;
+  st = check_attend(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype, num_heads,
+                    num_kv_heads, head_dim, softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride);
   if (st != PBS_OK) return st;
   st = check_common_table(topk, topk_row_stride, topk_k, dec_page_table, dec_pt_row_stride, dec_max_blocks,
-                          block_page_stride);
+                          block_page_stride, sparse_bt != nullptr);
   if (st != PBS_OK) return st;
   st = check_common_table(topk, topk_row_stride, topk_k, pre_page_table, pre_pt_row_stride, pre_max_blocks,
-                          block_page_stride);
+                          block_page_stride, sparse_bt != nullptr);
   if (st != PBS_OK) return st;
   if (dec_seq_lens == nullptr || cu_seqlens_q == nullptr || pre_seq_lens == nullptr) return PBS_ERR_ARG;
 
   // the prefill part as its own call would see: rows from nd on
   const void* q_pre = static_cast<const uint8_t*>(q) + nd * q_row_stride * 2;
-  const int32_t* topk_pre = topk + nd * topk_row_stride;
+  const int32_t* topk_pre = topk != nullptr ? topk + nd * topk_row_stride : nullptr;
+  const int32_t* sbt_pre = sparse_bt != nullptr ? sparse_bt + nd * sbt_row_stride : nullptr;
+  const int32_t* ctx_pre = sparse_ctx != nullptr ? sparse_ctx + nd : nullptr;
   void* out_pre = static_cast<uint8_t*>(out) + nd * out_row_stride * 2;
   float* lse_pre = lse != nullptr ? lse + nd * lse_row_stride : nullptr;
   AttendArgs p = make_attend_args(q_pre, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
@@ -702,29 +802,39 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
                                   pre_page_table, pre_pt_row_stride, pre_max_blocks, pre_seq_lens,
                                   block_page_stride, softmax_scale, k_scale, v_scale, out_pre, out_row_stride,
                                   out_head_stride, err_word);
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.num_reqs = num_reqs;
+  p.num_rows = total_q;
+  st = attach_table(&p, sbt_pre, sbt_row_stride, ctx_pre);
+  if (st != PBS_OK) return st;
   CUtensorMap map;
-  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, &p.packed_map);
+  st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, false, &p.packed_map);
   if (st != PBS_OK) return st;
-  PrefillKernel kernel = kPrefillToken;
-  st = choose_prefill_kernel(p, 0, &kernel);
+  int kernel = PBS_PREFILL_TOKEN;
+  st = choose_prefill_kernel(p, 0, opt.prefill_kernel, &kernel);
   if (st != PBS_OK) return st;
-  if (kernel != kPrefillToken) {
-    // the prefill part runs on the tcgen05 tile kernel: two launches, decode first
+  if (kernel != PBS_PREFILL_TOKEN) {
+    // the prefill part runs on a tcgen05 kernel: two launches, decode first
     st = pbs_sparse_decode_attention(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
                                      kv_dtype, num_heads, num_kv_heads, head_dim, topk, topk_row_stride, topk_k,
                                      dec_page_table, dec_pt_row_stride, dec_max_blocks, dec_seq_lens, batch,
-                                     decode_query_len, block_page_stride, softmax_scale, k_scale, v_scale, out,
-                                     out_row_stride, out_head_stride, lse, lse_row_stride, nullptr, 0, err_word,
-                                     stream);
+                                     decode_query_len, block_page_stride, sparse_bt, sbt_row_stride, sparse_ctx,
+                                     softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride, lse,
+                                     lse_row_stride, nullptr, 0, options, err_word, stream);
     if (st != PBS_OK) return st;
     return pbs_sparse_prefill_attention(q_pre, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages,
                                         kv_dtype, num_heads, num_kv_heads, head_dim, topk_pre, topk_row_stride,
                                         topk_k, pre_page_table, pre_pt_row_stride, pre_max_blocks, cu_seqlens_q,
-                                        pre_seq_lens, num_reqs, total_q, block_page_stride, softmax_scale, k_scale,
-                                        v_scale, out_pre, out_row_stride, out_head_stride, lse_pre, lse_row_stride,
-                                        nullptr, 0, err_word, stream);
+                                        pre_seq_lens, num_reqs, total_q, block_page_stride, sbt_pre, sbt_row_stride,
+                                        ctx_pre, softmax_scale, k_scale, v_scale, out_pre, out_row_stride,
+                                        out_head_stride, lse_pre, lse_row_stride, nullptr, 0, options, err_word,
+                                        stream);
   }
   // both parts on the token-centric kernel: one launch, each CTA picks its part by row
+  if (opt.quarter_map) {
+    st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, true, &p.packed_map);
+    if (st != PBS_OK) return st;
+  }
   AttendArgs a = make_attend_args(q, q_row_stride, q_head_stride, kv_cache, page_stride_bytes, num_pages, kv_dtype,
                                   num_heads, num_kv_heads, topk, topk_row_stride, topk_k, dec_page_table,
                                   dec_pt_row_stride, dec_max_blocks, dec_seq_lens, block_page_stride, softmax_scale,
@@ -739,9 +849,11 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
   a.pre_seq_lens = pre_seq_lens;
   a.num_rows = static_cast<int32_t>(nd + total_q);
   a.packed_map = p.packed_map;
+  st = attach_table(&a, sparse_bt, sbt_row_stride, sparse_ctx);
+  if (st != PBS_OK) return st;
   st = attach_lse(&a, lse, lse_row_stride);
   if (st != PBS_OK) return st;
-  a.splits = choose_splits(pbs::attend_units(nd + total_q, num_kv_heads, a.group), topk_k, false);
+  a.splits = choose_splits(pbs::attend_units(nd + total_q, num_kv_heads, a.group), topk_k, false, opt.splits);
   return pbs::launch_attend(a, pbs::kModeMixed, map, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PBS_OK
              : PBS_ERR_CUDA;

@@ -90,6 +90,7 @@ struct Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int32_t slot_base[kMaxTopk];
+  int32_t page_id[kMaxTopk * kPagesPerBlock];  // page of the row's 16-key group n (n < ceil(ctx / 16))
   int32_t ctx;
   int32_t abort;
   int32_t last;  // this chunk arrived last for its (row, kv head)
@@ -240,22 +241,41 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     max_blocks = a.pre_max_blocks;
   }
 
-  // ---- producer warp: the row's compaction; consumers: Q fragments --------------------------
+  // ---- producer warp: the row's table (compacted here, or a prebuilt one); consumers: Q --------
   uint32_t qf[8][2];
   if (warp == kConsumerWarps) {
-    RowCompaction rc = compact_row(a.topk + static_cast<int64_t>(row) * a.topk_row_stride, a.k, abs_pos,
-                                   pt + static_cast<int64_t>(req) * pt_stride, max_blocks,
-                                   a.block_page_stride, ctl->slot_base);
+    int ctx;
+    bool row_bad = false;  // block id past the page table, or an unreadable prebuilt row
+    if (a.sparse_bt == nullptr) {
+      const RowCompaction rc = compact_row(a.topk + static_cast<int64_t>(row) * a.topk_row_stride, a.k, abs_pos,
+                                           pt + static_cast<int64_t>(req) * pt_stride, max_blocks,
+                                           a.block_page_stride, ctl->slot_base);
+      ctx = rc.ctx;
+      row_bad = rc.bad;
+      // slot s holds the 8 consecutive pages from slot_base[s]
+      for (int n = lane; n < rc.n_written * kPagesPerBlock; n += 32)
+        ctl->page_id[n] = ctl->slot_base[n / kPagesPerBlock] + (n % kPagesPerBlock);
+    } else {
+      // prebuilt: the row's ctx and page ids as the [sparse_pa] builders wrote them
+      ctx = __ldg(a.sparse_ctx + row);
+      row_bad = ctx < 0 || ctx > a.k * kSparseBlock;
+      if (row_bad) ctx = 0;
+      const int32_t* trow = a.sparse_bt + static_cast<int64_t>(row) * a.sbt_row_stride;
+      for (int n = lane; n < (ctx + kPageRows - 1) / kPageRows; n += 32) ctl->page_id[n] = __ldg(trow + n);
+    }
+    __syncwarp();
+    // every page the row reads must lie in the cache
     bool page_bad = false;
-    for (int s = lane; s < rc.n_written; s += 32) {
-      const int64_t base = ctl->slot_base[s];
-      page_bad |= base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages;
+    for (int n = lane; n < (ctx + kPageRows - 1) / kPageRows; n += 32) {
+      const int id = ctl->page_id[n];
+      page_bad |= id < 0 || id >= a.num_pages;
     }
     page_bad = __any_sync(0xffffffffu, page_bad);
     if (lane == 0) {
-      if (rc.bad && split == 0 && gv == 0) set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+      if (row_bad && split == 0 && gv == 0)
+        set_err(a.err_word, a.sparse_bt == nullptr ? PBS_DEVERR_BLOCK_OOB : PBS_DEVERR_TABLE);
       if (page_bad && split == 0 && gv == 0) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-      ctl->ctx = page_bad ? 0 : rc.ctx;
+      ctl->ctx = page_bad ? 0 : ctx;
     }
   } else {
     const int hh = lane >> 2, c = lane & 3;
@@ -313,13 +333,13 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
         }
         if (*reinterpret_cast<volatile int32_t*>(&ctl->abort)) break;
         const int kp = (key0 >> 4) + p;
-        const int page = ctl->slot_base[kp >> 3] + (kp & 7);
+        const int page = ctl->page_id[kp];
         uint8_t* dst = stages + stage * kStage;
 #ifdef PBS_CHECKED
         // checked build: every copy's source and destination are validated before issue
         {
           int bad = 0;
-          if ((kp >> 3) >= kMaxTopk || kp < 0) bad |= 1 << 16;
+          if (kp >= kMaxTopk * kPagesPerBlock || kp < 0) bad |= 1 << 16;
           if (page < 0 || page >= a.num_pages) bad |= 1 << 17;
           if (g < 0 || g >= a.num_kv_heads) bad |= 1 << 18;
           if ((smem_u32(dst) & 1023u) != 0 || dst + kStage > reinterpret_cast<uint8_t*>(mg)) bad |= 1 << 19;

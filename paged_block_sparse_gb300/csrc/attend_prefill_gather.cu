@@ -1214,7 +1214,8 @@ namespace pbs {
 #endif
 
 bool prefill_gather_supported(const AttendArgs& a) {
-  return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
+  // buckets are built from top-k ids; a prebuilt table carries page ids only
+  return a.sparse_bt == nullptr && a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
          a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
          a.num_pages * a.num_kv_heads <= 0x7fffffffLL && a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
          reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 &&

@@ -38,8 +38,8 @@
 //   PV has, so K is fetched up to three blocks ahead of S.
 // * Online softmax in base 2 with lazy rescaling: the O row is rescaled only when the running
 //   maximum grows by more than 2^8, so most blocks never touch O from the CUDA cores.
-// * Duplicate ids in a token's list count once (set semantics of the attend); the decode path and
-//   the table builders follow the row writer literally. With distinct ids the two agree.
+// * A token's top-k row is a set of blocks: an id listed twice counts once, as in the table
+//   builders and the token-centric kernel.
 #include <algorithm>
 
 #include "pbs_device.cuh"
@@ -414,34 +414,103 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
   uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;
   int own = -1, lim = 0;
   bool bad = false;
-  if (lane < n) {
-    const int pos = ctx0 + (t0 + lane - c0);
-    const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
-    own = causal_len > 0 ? pos / kSparseBlock : -1;
-    lim = own >= 0 ? causal_len - own * kSparseBlock : 0;
-    const int32_t* row = a.topk + static_cast<int64_t>(t0 + lane) * a.topk_row_stride;
-    int ids[kTcMaxTopk];
+  auto add_block = [&](int b) {
+    const uint32_t bit = 1u << (b & 31);
+    m0 |= (b >> 5) == 0 ? bit : 0u;
+    m1 |= (b >> 5) == 1 ? bit : 0u;
+    m2 |= (b >> 5) == 2 ? bit : 0u;
+    m3 |= (b >> 5) == 3 ? bit : 0u;
+  };
+  if (a.sparse_bt == nullptr) {
+    if (lane < n) {
+      const int pos = ctx0 + (t0 + lane - c0);
+      const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
+      own = causal_len > 0 ? pos / kSparseBlock : -1;
+      lim = own >= 0 ? causal_len - own * kSparseBlock : 0;
+      const int32_t* row = a.topk + static_cast<int64_t>(t0 + lane) * a.topk_row_stride;
+      int ids[kTcMaxTopk];
 #pragma unroll
-    for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = j < a.k ? __ldg(row + j) : -1;
+      for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = j < a.k ? __ldg(row + j) : -1;
 #pragma unroll
-    for (int j = 0; j < kTcMaxTopk; ++j) {
-      const int b = ids[j];
-      if (b >= 0 && b <= own) {
-        if (b >= a.max_blocks) {
-          bad = true;
-        } else {
-          const uint32_t bit = 1u << (b & 31);
-          m0 |= (b >> 5) == 0 ? bit : 0u;
-          m1 |= (b >> 5) == 1 ? bit : 0u;
-          m2 |= (b >> 5) == 2 ? bit : 0u;
-          m3 |= (b >> 5) == 3 ? bit : 0u;
+      for (int j = 0; j < kTcMaxTopk; ++j) {
+        const int b = ids[j];
+        if (b >= 0 && b <= own) {
+          if (b >= a.max_blocks) bad = true;
+          else add_block(b);
         }
       }
+      // a row with an out-of-range id contributes nothing (its output is zero, the error recorded)
+      if (bad) {
+        set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
+        m0 = m1 = m2 = m3 = 0u;
+      }
     }
-    // a row with an out-of-range id contributes nothing (its output is zero, the error recorded)
-    if (bad) {
-      set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
-      m0 = m1 = m2 = m3 = 0u;
+  } else {
+    // Prebuilt table: slot j of the token's row lists the pages of one block; the block is found
+    // by walking the request's page-table row (a slot's first page is page_table[r][b] *
+    // block_page_stride). Keys of slot j: min(128, ctx - 128 j), so only the last slot can be
+    // partial; it plays the own block's part (lim keys).
+    int first[kTcMaxTopk], blk[kTcMaxTopk];
+    int n_slots = 0, tctx = 0;
+    if (lane < n) {
+      tctx = __ldg(a.sparse_ctx + t0 + lane);
+      if (tctx < 0 || tctx > a.k * kSparseBlock) {
+        bad = true;
+        tctx = 0;
+      }
+      n_slots = (tctx + kSparseBlock - 1) / kSparseBlock;
+    }
+    const int32_t* trow = a.sparse_bt + static_cast<int64_t>(t0 + min(lane, max(n - 1, 0))) * a.sbt_row_stride;
+#pragma unroll
+    for (int j = 0; j < kTcMaxTopk; ++j) {
+      first[j] = j < n_slots ? __ldg(trow + j * kPagesPerBlock) : -1;
+      blk[j] = -1;
+    }
+    // the last block any of the tile's tokens can see bounds the walk
+    const int pos_max = ctx0 + (t0 + max(n, 1) - 1 - c0);
+    const int walk = min(a.max_blocks, pos_max >= 0 ? pos_max / kSparseBlock + 1 : 0);
+    const int32_t* pt_row = a.page_table + static_cast<int64_t>(max(r, 0)) * a.pt_row_stride;
+    for (int b0 = 0; b0 < walk; b0 += 32) {
+      const int bb = b0 + lane;
+      const int64_t base64 = bb < walk ? static_cast<int64_t>(__ldg(pt_row + bb)) * a.block_page_stride : -1;
+      const int base = base64 >= 0 && base64 <= 0x7fffffffLL ? static_cast<int>(base64) : -2;
+      const int nj = min(32, walk - b0);
+      for (int j = 0; j < nj; ++j) {
+        const int x = __shfl_sync(0xffffffffu, base, j);
+#pragma unroll
+        for (int s = 0; s < kTcMaxTopk; ++s)
+          if (blk[s] < 0 && first[s] == x) blk[s] = b0 + j;
+      }
+    }
+    if (lane < n && !bad) {
+#pragma unroll
+      for (int s = 0; s < kTcMaxTopk; ++s) {
+        if (s < n_slots) {
+          // a slot that names no block of the request, or a block in two slots (no table the
+          // builders write: a row is a set of blocks), makes the row unreadable
+          const int b = blk[s];
+          const int w = (b >> 5) & 3;
+          const uint32_t word = w == 0 ? m0 : w == 1 ? m1 : w == 2 ? m2 : m3;
+          bad |= b < 0 || ((word >> (b & 31)) & 1u) != 0;
+          if (b >= 0) add_block(b);
+          if (s == n_slots - 1) {
+            own = b;
+            lim = tctx - s * kSparseBlock;
+          }
+        }
+      }
+      // every page a slot's keys reach must be the block's own page (the kernel copies the block)
+      for (int s = 0; s < n_slots && !bad; ++s) {
+        const int f = __ldg(trow + s * kPagesPerBlock);
+        const int keys = min(kSparseBlock, tctx - s * kSparseBlock);
+        for (int j = 1; j < (keys + kPageRows - 1) / kPageRows; ++j) bad |= __ldg(trow + s * kPagesPerBlock + j) != f + j;
+      }
+      if (bad) {
+        set_err(a.err_word, PBS_DEVERR_TABLE);
+        m0 = m1 = m2 = m3 = 0u;
+      }
+    } else if (lane < n && bad) {
+      set_err(a.err_word, PBS_DEVERR_TABLE);
     }
   }
   const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad);

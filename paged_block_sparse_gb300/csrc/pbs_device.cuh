@@ -230,9 +230,12 @@ struct RowCompaction {
 // Compacts one query row's top-k list (vLLM page vllm.models.minimax_m3.amd.ops.sparse_pa,
 // _write_sparse_block_table_row_from_values): a block b is valid iff the causal length
 // max(abs_pos+1, 0) is positive and 0 <= b <= abs_pos/128; valid blocks before the own block
-// are numbered in top-k order (ballot + popc prefix), the own block takes slot n_full. Slot
-// s's first page id (page_table[b] * block_page_stride) goes to slot_base[s] (shared memory,
-// kMaxTopk entries). All 32 lanes must call this; the result is warp-uniform.
+// are numbered in top-k order (ballot + popc prefix), the own block takes slot n_full. A row
+// is a set of blocks: an entry whose id an earlier entry already holds is dropped (the writer
+// files every copy of the own block under one slot and counts its keys once; repeated full
+// blocks are read the same way). Slot s's first page id (page_table[b] * block_page_stride)
+// goes to slot_base[s] (shared memory, kMaxTopk entries). All 32 lanes must call this; the
+// result is warp-uniform.
 __device__ __forceinline__ RowCompaction compact_row(const int32_t* __restrict__ topk_row, int k, int abs_pos,
                                                      const int32_t* __restrict__ bt_row, int max_blocks,
                                                      int block_page_stride, int32_t* slot_base) {
@@ -245,7 +248,22 @@ __device__ __forceinline__ RowCompaction compact_row(const int32_t* __restrict__
   for (int h = 0; h < 2; ++h) {
     const int e = lane + 32 * h;
     b[h] = e < k ? __ldg(topk_row + e) : -1;
-    valid[h] = e < k && causal_len > 0 && b[h] >= 0 && b[h] <= own;
+  }
+  // entry lane (lane + 32) repeats an earlier one: a lower lane of its half holds the same id,
+  // or (second half) any lane of the first half does
+  const uint32_t lt = lanemask_lt();
+  bool rep[2];
+  rep[0] = (__match_any_sync(0xffffffffu, b[0]) & lt) != 0;
+  rep[1] = false;
+  if (k > 32) {  // warp-uniform
+    bool r1 = (__match_any_sync(0xffffffffu, b[1]) & lt) != 0;
+    for (int j = 0; j < 32; ++j) r1 |= __shfl_sync(0xffffffffu, b[0], j) == b[1];
+    rep[1] = r1;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = lane + 32 * h;
+    valid[h] = e < k && !rep[h] && causal_len > 0 && b[h] >= 0 && b[h] <= own;
     full[h] = valid[h] && b[h] < own;
   }
   const uint32_t f0 = __ballot_sync(0xffffffffu, full[0]), f1 = __ballot_sync(0xffffffffu, full[1]);
@@ -253,7 +271,6 @@ __device__ __forceinline__ RowCompaction compact_row(const int32_t* __restrict__
   const int n_full = __popc(f0) + __popc(f1);
   const int n_valid = __popc(v0) + __popc(v1);
   const bool has_tail = n_valid > n_full;
-  const uint32_t lt = lanemask_lt();
   bool oob = false;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {

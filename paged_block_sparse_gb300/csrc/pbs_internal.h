@@ -61,6 +61,11 @@ struct AttendArgs {
   const int32_t* pre_seq_lens;
   int32_t num_rows;
   int32_t block_page_stride;
+  // optional prebuilt table ([rows, >= k * 8] page ids, row stride sbt_row_stride; ctx per row):
+  // non-null, the kernels attend it instead of compacting each row from top-k
+  const int32_t* sparse_bt;
+  int64_t sbt_row_stride;
+  const int32_t* sparse_ctx;
   float scale_log2;           // softmax_scale * k_scale * log2(e)
   float v_scale;
   uint16_t* out;              // bf16 bits

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 7
+    assert pbs.abi_version() == 8
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"
@@ -76,15 +76,21 @@ def test_table_host_checks(L):
     assert st == 2                                        # tokens but no request
 
 
+class _Opts(ctypes.Structure):
+    _fields_ = [("prefill_kernel", ctypes.c_int32), ("splits", ctypes.c_int32), ("cache_map", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 def _decode_attend(L, **kw):
     a = dict(q=A, qrs=1024, qhs=128, kv=A, psb=65536, npages=100, dt=0, hq=64, hkv=8, hd=128, topk=A, trs=16,
-             k=16, pt=A, pts=64, mb=64, sl=A, batch=4, dql=1, bps=8, sc=0.088, ks=1.0, vs=1.0, out=A, ors=8192,
-             ohs=128, lse=N, lses=0, ws=N, wsb=0)
+             k=16, pt=A, pts=64, mb=64, sl=A, batch=4, dql=1, bps=8, sbt=N, sbts=0, sctx=N, sc=0.088, ks=1.0, vs=1.0,
+             out=A, ors=8192, ohs=128, lse=N, lses=0, ws=N, wsb=0, opt=N)
     a.update(kw)
     return L.pbs_sparse_decode_attention(a["q"], a["qrs"], a["qhs"], a["kv"], a["psb"], a["npages"], a["dt"],
                                          a["hq"], a["hkv"], a["hd"], a["topk"], a["trs"], a["k"], a["pt"], a["pts"],
-                                         a["mb"], a["sl"], a["batch"], a["dql"], a["bps"], a["sc"], a["ks"], a["vs"],
-                                         a["out"], a["ors"], a["ohs"], a["lse"], a["lses"], a["ws"], a["wsb"], N, S)
+                                         a["mb"], a["sl"], a["batch"], a["dql"], a["bps"], a["sbt"], a["sbts"],
+                                         a["sctx"], a["sc"], a["ks"], a["vs"], a["out"], a["ors"], a["ohs"], a["lse"],
+                                         a["lses"], a["ws"], a["wsb"], a["opt"], N, S)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
@@ -113,6 +119,15 @@ def test_attend_host_checks(L):
     assert _decode_attend(L, ws=N, wsb=16) == 1            # bytes without a pointer
     assert _decode_attend(L, ws=ctypes.c_void_p(0x10008), wsb=need) == 4
     assert _decode_attend(L, ws=A, wsb=need - 1) == 2      # too small for the rows
+    # prebuilt table: both pointers or neither, rows at least top-k x 8 wide, 4-byte aligned
+    assert _decode_attend(L, sbt=A, sbts=128) == 1          # table without its ctx
+    assert _decode_attend(L, sctx=A) == 1                   # ctx without its table
+    assert _decode_attend(L, sbt=A, sbts=127, sctx=A) == 2
+    assert _decode_attend(L, sbt=ctypes.c_void_p(0x10002), sbts=128, sctx=A) == 4
+    assert _decode_attend(L, topk=N) == 1                   # no table: top-k is needed
+    # options: every field checked
+    for bad in (_Opts(4, 0, 0, 0), _Opts(0, 3, 0, 0), _Opts(0, 16, 0, 0), _Opts(0, 0, 2, 0), _Opts(0, 0, 0, 1)):
+        assert _decode_attend(L, opt=ctypes.byref(bad)) == 1
 
 
 def test_prefill_workspace_bytes(L):
@@ -170,20 +185,33 @@ def test_binding_insert_shape_checks():
     pbs.insert_index_cache(torch.zeros(0, 8), torch.zeros(2, 4, 8), torch.zeros(0, dtype=torch.int64))
 
 
-def test_binding_tile_workspace_rule():
-    """The binding hands its converted-V workspace only to calls the tile kernel takes (the token
-    kernel would read a workspace as split scratch); the rule mirrors the library's dispatch."""
+def test_prefill_kernel_choice_rule():
+    """The library's prefill dispatch, asked through pbs_prefill_kernel_choice (the binding sizes its
+    workspace from the same answer, so there is one rule)."""
     import paged_block_sparse_gb300 as pbs
-    run = pbs._tile_kernel_runs
     packed = 8 * 8192
-    assert run("bf16", 64, 8, 16, 64, packed, None)
-    assert run("bf16", 64, 4, 16, 128, 4 * 8192, None)         # GQA 16, table 8 x top-k wide
-    assert not run("bf16", 64, 8, 16, 129, packed, None)       # wider than 8 x top-k
-    assert not run("bf16", 64, 8, 8, 65, packed, None)         # 8 x top-k = 64 blocks
-    assert run("bf16", 64, 8, 8, 65, packed, "tc")             # forced: up to 128 blocks
-    assert not run("bf16", 64, 8, 8, 129, packed, "tc")
-    assert not run("bf16", 64, 8, 16, 64, packed, "token")
-    assert not run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, None)
-    assert not run("bf16", 32, 8, 16, 64, packed, None)        # GQA 4
-    assert not run("bf16", 64, 8, 17, 64, packed, None)        # top-k above 16
-    assert not run("bf16", 64, 8, 16, 64, packed + 16, None)   # pages strided inside a larger allocation
+
+    def run(kv, hq, hkv, k, mb, psb, kernel=None, table=False, ws=0, total_q=4096):
+        try:
+            return pbs.prefill_kernel_choice(total_q, 4, kv, psb, hq, hkv, k, mb, table, ws, kernel)
+        except pbs.PbsError as e:
+            return e.status
+    assert run("bf16", 64, 8, 16, 64, packed) == "tile"
+    assert run("bf16", 64, 4, 16, 128, 4 * 8192) == "tile"          # GQA 16, table 8 x top-k wide
+    assert run("bf16", 64, 8, 16, 129, packed) == "token"            # wider than 8 x top-k
+    assert run("bf16", 64, 8, 8, 65, packed) == "token"              # 8 x top-k = 64 blocks
+    assert run("bf16", 64, 8, 8, 65, packed, "tile") == "tile"       # asked for: up to 128 blocks
+    assert run("bf16", 64, 8, 8, 129, packed, "tile") == 3           # the tile kernel cannot take it
+    assert run("bf16", 64, 8, 16, 64, packed, "token") == "token"
+    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096) == "token"
+    assert run("bf16", 32, 8, 16, 64, packed) == "token"             # GQA 4
+    assert run("bf16", 64, 8, 17, 64, packed) == "token"             # top-k above 16
+    assert run("bf16", 64, 8, 16, 64, packed + 16) == "token"        # pages strided inside a larger allocation
+    assert run("bf16", 64, 8, 16, 64, packed, table=True) == "tile"  # a prebuilt table: the tile kernel reads it
+    # the gathered-row kernel only on request, with a workspace of at least one 256-token window
+    need = pbs.prefill_workspace_bytes(256, 4, 64, 8, 16, 64)
+    assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need) == "gather"
+    assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need - 256) == 3
+    assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need, table=True) == 3   # it reads top-k only
+    assert run("bf16", 64, 8, 16, 64, packed, ws=need) == "tile"     # never taken unasked
+    assert run("bf16", 60, 8, 16, 64, packed) == 1

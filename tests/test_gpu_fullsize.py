@@ -53,11 +53,11 @@ def _decode_parity(pbs, b, nrows, seed):
     return assert_close(got, want, b.kv_dtype, b.name)
 
 
-def _prefill_parity(pbs, b, nrows, seed, workspace=None):
+def _prefill_parity(pbs, b, nrows, seed, workspace="auto", kernel=None):
     p = b.pre
     out = pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
                                        p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
-                                       workspace=workspace)
+                                       workspace=workspace, kernel=kernel)
     torch.cuda.synchronize()
     rows = _sample(p.q.shape[0], nrows, seed)
     want = oracle_prefill(b, rows=rows)
@@ -77,12 +77,11 @@ def test_prefill_varlen_bf16(pbs):
     _prefill_parity(pbs, b, 48, 2)
 
 
-def test_prefill_varlen_bf16_gathered(pbs, monkeypatch):
+def test_prefill_varlen_bf16_gathered(pbs):
     """The gathered-row prefill kernel at full size (several token segments on the default
     2 GiB workspace), sampled rows against the oracle."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "gather")
     b = workloads.prefill(device="cuda")
-    _prefill_parity(pbs, b, 48, 6, workspace="auto")
+    _prefill_parity(pbs, b, 48, 6, kernel="gather")
 
 
 def test_mtp_fp8(pbs):

@@ -3,8 +3,6 @@
 Tables and context lengths must match bit for bit; attention outputs within max-abs 1e-2 /
 relative-RMS 2e-3 (bf16 KV) or 5e-2 / 1e-2 (fp8 / NVFP4 KV, against the oracle on the same
 dequantised values)."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -54,22 +52,23 @@ def oracle_tables(b, part):
                                                    np_i32(p.seq_lens), b.block_page_stride)
 
 
-def gpu_attend(pbs, b, part, err=None, workspace="default"):
+def gpu_attend(pbs, b, part, err=None, workspace="default", kernel=None, splits=None, cache_map=None,
+               sparse_table=None):
     """The binding's call for one part; workspace "default" leaves the binding's own default
-    (decode: none, prefill: the cached workspace of the gathered-row kernel)."""
-    ws = {} if isinstance(workspace, str) and workspace == "default" else {"workspace": workspace}
-    if part != "dec" and not ws and os.environ.get("PBS_PREFILL_KERNEL") == "gather":
-        ws = {"workspace": "auto"}  # the gathered-row kernel runs on a caller workspace
+    (decode: none; prefill: the workspace the chosen kernel wants). kernel / splits / cache_map are
+    the call's options; sparse_table an optional prebuilt (sparse_bt, sparse_ctx)."""
+    kw = {} if isinstance(workspace, str) and workspace == "default" else {"workspace": workspace}
+    kw.update(splits=splits, cache_map=cache_map, sparse_table=sparse_table)
     if part == "dec":
         d = b.dec
         out = pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table,
                                           d.seq_lens, d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale,
-                                          b.block_page_stride, err_word=err, **ws)
+                                          b.block_page_stride, err_word=err, **kw)
     else:
         p = b.pre
         out = pbs.sparse_prefill_attention(p.q, b.cache, b.kv_dtype, b.num_kv_heads, p.topk, p.page_table,
                                            p.cu_seqlens_q, p.seq_lens, b.softmax_scale, b.k_scale, b.v_scale,
-                                           b.block_page_stride, err_word=err, **ws)
+                                           b.block_page_stride, err_word=err, kernel=kernel, **kw)
     torch.cuda.synchronize()
     return out.to(torch.float64).cpu().numpy()
 
@@ -107,7 +106,8 @@ def test_tables_small_variants(pbs, case):
 
 
 def test_tables_duplicates_strides_and_side_packed(pbs):
-    """Duplicate ids follow the row writer literally; a strided top-k view and block stride 16."""
+    """Repeated ids (a row is a set of blocks: later repeats dropped, as the oracle reads it); a
+    strided top-k view and block stride 16."""
     rng = np.random.default_rng(5)
     rows, k = 300, 12
     seq = rng.integers(1, 6000, size=rows).astype(np.int32)
@@ -182,21 +182,19 @@ def test_attend_small_prefill(pbs, kv_dtype):
 
 @pytest.mark.parametrize("workspace", [None, "auto"])
 @pytest.mark.parametrize("splits", ["1", "2", "4", "8"])
-def test_attend_split_counts_agree(pbs, splits, workspace, monkeypatch):
+def test_attend_split_counts_agree(pbs, splits, workspace):
     """Every split count gives the oracle's answer, merged through a cluster's shared memory
     (no workspace) or through the workspace by the last chunk to finish."""
-    monkeypatch.setenv("PBS_ATTEND_SPLITS", splits)
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, dec_seq_lens=[3000, 9000, 700],
                         seed=33)
-    got = gpu_attend(pbs, b, "dec", workspace=workspace)
+    got = gpu_attend(pbs, b, "dec", workspace=workspace, splits=int(splits))
     assert_close(dict(enumerate(got)), oracle_decode(b), "bf16", f"splits={splits} workspace={workspace}")
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
-def test_attend_workspace_leaves_tickets_zero(pbs, kv_dtype, monkeypatch):
+def test_attend_workspace_leaves_tickets_zero(pbs, kv_dtype):
     """Two calls in a row on one caller workspace: both match the oracle, and each leaves the
     per-(row, kv head) arrival counters at zero for the next call."""
-    monkeypatch.setenv("PBS_ATTEND_SPLITS", "8")
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=4, topk=16,
                         dec_seq_lens=[1, 2100, 7000, 0, 4000], decode_query_len=2, seed=38)
     rows, hkv = b.dec.q.shape[0], b.num_kv_heads
@@ -204,26 +202,25 @@ def test_attend_workspace_leaves_tickets_zero(pbs, kv_dtype, monkeypatch):
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     want = oracle_decode(b)
     for call in range(2):
-        got = gpu_attend(pbs, b, "dec", workspace=ws)
+        got = gpu_attend(pbs, b, "dec", workspace=ws, splits=8)
         assert_close(dict(enumerate(got)), want, kv_dtype, f"workspace call {call}")
         assert int(ws[nbytes - rows * hkv * 4:].view(torch.int32).abs().sum()) == 0
     # a smaller call on the same buffer (its tickets sit in the same tail) still matches
     sub = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=4, topk=16,
                           dec_seq_lens=[5000], decode_query_len=1, seed=40)
-    got = gpu_attend(pbs, sub, "dec", workspace=ws)
+    got = gpu_attend(pbs, sub, "dec", workspace=ws, splits=8)
     assert_close(dict(enumerate(got)), oracle_decode(sub), kv_dtype, "smaller call after")
     assert int(ws[nbytes - rows * hkv * 4:].view(torch.int32).abs().sum()) == 0
-    got = gpu_attend(pbs, b, "dec", workspace=ws)
+    got = gpu_attend(pbs, b, "dec", workspace=ws, splits=8)
     assert_close(dict(enumerate(got)), want, kv_dtype, "larger call again")
 
 
-def test_prefill_token_kernel_workspace_splits(pbs, monkeypatch):
+def test_prefill_token_kernel_workspace_splits(pbs):
     """The token-centric prefill kernel with its splits merged through the workspace."""
-    monkeypatch.setenv("PBS_ATTEND_SPLITS", "4")
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "token")
     b = workloads.small(device=DEV, kv_dtype="fp8_e4m3", num_heads=64, num_kv_heads=8, topk=16,
                         pre_q_lens=[200, 1, 90], pre_ctx_lens=[3000, 700, 5000], future_prob=0.3, seed=39)
-    got = gpu_attend(pbs, b, "pre")
+    ws = pbs.attend_workspace(b.pre.q.shape[0], b.num_heads, b.num_kv_heads, DEV)
+    got = gpu_attend(pbs, b, "pre", workspace=ws, kernel="token", splits=4)
     assert_close(dict(enumerate(got)), oracle_prefill(b), "fp8_e4m3", "prefill workspace splits")
 
 
@@ -260,30 +257,29 @@ def _check_lse(got, want, what):
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
 @pytest.mark.parametrize("split", ["1", "4", "4ws"])
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
-def test_attend_lse_decode(pbs, kv_dtype, split, heads, monkeypatch):
+def test_attend_lse_decode(pbs, kv_dtype, split, heads):
     """The optional log-sum-exp of every row and head, through each merge path."""
-    monkeypatch.setenv("PBS_ATTEND_SPLITS", split[0])
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=heads[0], num_kv_heads=heads[1], topk=16,
                         dec_seq_lens=[0, 129, 2000, 9000, 1170], decode_query_len=2, seed=60)
     d = b.dec
     out, lse = pbs.sparse_decode_attention(d.q, b.cache, kv_dtype, b.num_kv_heads, d.topk, d.page_table, d.seq_lens,
                                            d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale,
-                                           workspace="auto" if split.endswith("ws") else None, return_lse=True)
+                                           workspace="auto" if split.endswith("ws") else None, return_lse=True,
+                                           splits=int(split[0]))
     torch.cuda.synchronize()
     _check_lse(lse, _oracle_lse(b, "dec"), f"decode lse {kv_dtype} S={split} {heads}")
     assert_close(dict(enumerate(out.double().cpu().numpy())), oracle_decode(b), kv_dtype, "decode out with lse")
 
 
-@pytest.mark.parametrize("kernel", ["tc", "token", "gather"])
+@pytest.mark.parametrize("kernel", ["tile", "token", "gather"])
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
-def test_attend_lse_prefill(pbs, kernel, heads, monkeypatch):
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
+def test_attend_lse_prefill(pbs, kernel, heads):
     b = workloads.small(device=DEV, num_heads=heads[0], num_kv_heads=heads[1], topk=8, pre_q_lens=[37, 200, 1],
                         pre_ctx_lens=[0, 700, 3000], future_prob=0.3, seed=61)
     p = b.pre
     out, lse = pbs.sparse_prefill_attention(p.q, b.cache, "bf16", b.num_kv_heads, p.topk, p.page_table,
                                             p.cu_seqlens_q, p.seq_lens, b.softmax_scale, return_lse=True,
-                                            workspace="auto" if kernel == "gather" else None)
+                                            workspace="auto" if kernel == "gather" else None, kernel=kernel)
     torch.cuda.synchronize()
     _check_lse(lse, _oracle_lse(b, "pre"), f"prefill lse {kernel} {heads}")
 
@@ -393,53 +389,82 @@ PREFILL_CASES = [
 
 
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
-@pytest.mark.parametrize("kernel", ["tc", "tc_hilo", "token", "gather"])
+@pytest.mark.parametrize("kernel", ["tile", "tile_hilo", "token", "gather"])
 @pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
-def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, heads, monkeypatch):
+def test_prefill_kernels_agree_with_oracle(pbs, kernel, ci, heads):
     """Every prefill kernel, GQA 8 (tile = 16 tokens x 8 heads) and GQA 16 (8 tokens x 16 heads);
-    tc_hilo: the tile kernel without a workspace (bf16 P as hi + lo instead of converted fp16 V)."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc" if kernel == "tc_hilo" else kernel)
+    tile_hilo: the tile kernel without a workspace (bf16 P as hi + lo instead of converted fp16 V)."""
     b = workloads.small(device=DEV, num_heads=heads[0], num_kv_heads=heads[1], seed=41 + ci, **PREFILL_CASES[ci])
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err, workspace=None if kernel == "tc_hilo" else "default")
+    got = gpu_attend(pbs, b, "pre", err, workspace=None if kernel == "tile_hilo" else "default",
+                     kernel="tile" if kernel == "tile_hilo" else kernel)
     assert int(err.item()) == 0
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", f"prefill {kernel} case {ci}")
 
 
-@pytest.mark.parametrize("kernel", ["tc", "gather"])
-def test_prefill_tc_duplicate_ids_count_once(pbs, kernel, monkeypatch):
-    """The tcgen05 kernels read each selected block once per token, the attend's set reading."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
-    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=6, pre_q_lens=[300], pre_ctx_lens=[400],
-                        seed=45)
-    tk = b.pre.topk.clone()
-    tk[0, :, 1] = tk[0, :, 0]                                       # duplicate the first slot
-    b.pre.topk = tk
+def _with_repeats(topk):
+    """A copy of a top-k buffer [1, rows, k] in which rows repeat ids: slot 1 copies slot 0 in every
+    row, and in every third row the last slot copies the row's largest id (often the own block)."""
+    tk = topk.clone()
+    tk[0, :, 1] = tk[0, :, 0]
+    rows = torch.arange(0, tk.shape[1], 3, device=tk.device)
+    tk[0, rows, -1] = tk[0, rows].max(dim=1).values
+    return tk
+
+
+@pytest.mark.parametrize("entry", ["dec", "dec_ws", "dec_split8", "dec_split8_ws", "tile", "tile_hilo", "token",
+                                   "gather", "mixed"])
+def test_repeated_ids_read_once_by_every_kernel(pbs, entry):
+    """A top-k row is a set of blocks: rows with repeated full and own-block ids give the oracle's
+    answer (each selected block read once) on every kernel and merge path, and the table builders
+    write the oracle's table for them."""
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=6, dec_seq_lens=[3000, 700, 9000, 129],
+                        decode_query_len=2, pre_q_lens=[300, 40], pre_ctx_lens=[400, 2000], future_prob=0.2, seed=45)
+    b.dec.topk = _with_repeats(b.dec.topk)
+    b.pre.topk = _with_repeats(b.pre.topk)
+    assert int((b.pre.topk[0, :, 0] >= 0).sum()) > 0
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err)
+    if entry.startswith("dec"):
+        for part in ("dec", "pre"):
+            sbt, ctx, terr = gpu_tables(pbs, b, part)
+            o_sbt, o_ctx = oracle_tables(b, part)
+            assert terr == 0 and np.array_equal(sbt, o_sbt) and np.array_equal(ctx, o_ctx)
+        ws = "auto" if entry.endswith("_ws") else None
+        got = gpu_attend(pbs, b, "dec", err, workspace=ws, splits=8 if "split8" in entry else None)
+        want = oracle_decode(b)
+    elif entry == "mixed":
+        d, p = b.dec, b.pre
+        out = pbs.sparse_mixed_attention(torch.cat([d.q, p.q]), b.cache, "bf16", 8, torch.cat([d.topk[0], p.topk[0]]),
+                                         d.page_table, d.seq_lens, d.decode_query_len, p.page_table, p.cu_seqlens_q,
+                                         p.seq_lens, b.softmax_scale, err_word=err)
+        torch.cuda.synchronize()
+        got = out.double().cpu().numpy()
+        want = {**oracle_decode(b), **{d.q.shape[0] + r: v for r, v in oracle_prefill(b).items()}}
+    else:
+        kernel = "tile" if entry == "tile_hilo" else entry
+        got = gpu_attend(pbs, b, "pre", err, workspace=None if entry == "tile_hilo" else "default", kernel=kernel)
+        want = oracle_prefill(b)
     assert int(err.item()) == 0
-    assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill duplicates")
+    assert_close(dict(enumerate(got)), want, "bf16", f"repeated ids {entry}")
 
 
 @pytest.mark.parametrize("workspace", ["default", None])
-def test_prefill_tc_widest_page_table(pbs, workspace, monkeypatch):
+def test_prefill_tc_widest_page_table(pbs, workspace):
     """Contexts reaching block 127: the tile kernel's 128-bit block sets filled to the last bit."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, pre_q_lens=[40, 17],
                         pre_ctx_lens=[16344, 9000], future_prob=0.2, seed=48)
     p = b.pre
     assert p.page_table.shape[1] <= 128 and int(p.seq_lens.max()) > 127 * 128
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err, workspace=workspace)
+    got = gpu_attend(pbs, b, "pre", err, workspace=workspace, kernel="tile")
     assert int(err.item()) == 0
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill widest table")
 
 
 @pytest.mark.parametrize("workspace", ["default", None])
-def test_prefill_tc_v_scales_across_blocks(pbs, workspace, monkeypatch):
+def test_prefill_tc_v_scales_across_blocks(pbs, workspace):
     """V blocks whose magnitudes differ by up to 2^40: on the converted-V path the tile kernel moves
     its exponent reference and rescales O by powers of two; outputs compared row-normalised."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "tc")
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, pre_q_lens=[300, 40],
                         pre_ctx_lens=[900, 2000], seed=47)
     p = b.pre
@@ -452,7 +477,7 @@ def test_prefill_tc_v_scales_across_blocks(pbs, workspace, monkeypatch):
                 page = int(pt[r, blk]) * b.block_page_stride + pg
                 b.cache[page].view(b.num_kv_heads, 16, -1)[:, :, 256:].view(torch.bfloat16).mul_(f)
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err, workspace=workspace)
+    got = gpu_attend(pbs, b, "pre", err, workspace=workspace, kernel="tile")
     assert int(err.item()) == 0
     want = oracle_prefill(b)
     norm = {r: np.abs(want[r]).max() for r in want}
@@ -460,9 +485,8 @@ def test_prefill_tc_v_scales_across_blocks(pbs, workspace, monkeypatch):
                  "prefill V scales")
 
 
-@pytest.mark.parametrize("kernel", ["tc", "gather"])
-def test_prefill_tc_ignores_nan_past_last_token(pbs, kernel, monkeypatch):
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", kernel)
+@pytest.mark.parametrize("kernel", ["tile", "gather"])
+def test_prefill_tc_ignores_nan_past_last_token(pbs, kernel):
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, pre_q_lens=[77, 200], pre_ctx_lens=[0, 50],
                         seed=46)
     p = b.pre
@@ -472,28 +496,29 @@ def test_prefill_tc_ignores_nan_past_last_token(pbs, kernel, monkeypatch):
             page = int(pt[r, x // 128]) * 8 + (x % 128) // 16
             b.cache[page].view(b.num_kv_heads, 16, -1)[:, x % 16, :] = 0xFF
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err)
+    got = gpu_attend(pbs, b, "pre", err, kernel=kernel)
     assert int(err.item()) == 0
     assert_close(dict(enumerate(got)), oracle_prefill(b), "bf16", "prefill NaN past the end")
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
-def test_attend_per_quarter_map(pbs, kv_dtype, monkeypatch):
+def test_attend_per_quarter_map(pbs, kv_dtype):
     """The token-centric kernel on the per-quarter (4-D) cache map as well as the packed one."""
-    monkeypatch.setenv("PBS_CACHE_MAP", "4d")
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8, topk=9,
-                        dec_seq_lens=[129, 2000, 5000], decode_query_len=2, seed=51)
-    assert_close(dict(enumerate(gpu_attend(pbs, b, "dec"))), oracle_decode(b), kv_dtype, "decode 4-D map")
+                        dec_seq_lens=[129, 2000, 5000], decode_query_len=2, pre_q_lens=[50, 200],
+                        pre_ctx_lens=[900, 0], seed=51)
+    assert_close(dict(enumerate(gpu_attend(pbs, b, "dec", cache_map="quarter"))), oracle_decode(b), kv_dtype,
+                 "decode 4-D map")
+    assert_close(dict(enumerate(gpu_attend(pbs, b, "pre", kernel="token", cache_map="quarter"))), oracle_prefill(b),
+                 kv_dtype, "prefill 4-D map")
 
 
-@pytest.mark.parametrize("kv_dtype,prefill_kernel", [("bf16", "tc"), ("bf16", "token"), ("fp8_e4m3", None),
+@pytest.mark.parametrize("kv_dtype,prefill_kernel", [("bf16", "tile"), ("bf16", "token"), ("fp8_e4m3", None),
                                                      ("nvfp4", None)])
-def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel, monkeypatch):
+def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel):
     """Decode rows then prefill tokens through pbs_sparse_mixed_attention: one fused launch of the
     token-centric kernel, or decode + tile kernel when the prefill part takes the tile kernel;
     outputs and log-sum-exp against the oracle's decode and prefill attends."""
-    if prefill_kernel:
-        monkeypatch.setenv("PBS_PREFILL_KERNEL", prefill_kernel)
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8, topk=12,
                         dec_seq_lens=[2500, 0, 9000], decode_query_len=2, pre_q_lens=[150, 1, 60],
                         pre_ctx_lens=[0, 900, 2000], future_prob=0.3, seed=54)
@@ -503,7 +528,7 @@ def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel, monkeypatch):
     topk = torch.cat([d.topk[0], p.topk[0]])
     out, lse = pbs.sparse_mixed_attention(q, b.cache, kv_dtype, b.num_kv_heads, topk, d.page_table, d.seq_lens,
                                           d.decode_query_len, p.page_table, p.cu_seqlens_q, p.seq_lens,
-                                          b.softmax_scale, b.k_scale, b.v_scale, return_lse=True)
+                                          b.softmax_scale, b.k_scale, b.v_scale, return_lse=True, kernel=prefill_kernel)
     torch.cuda.synchronize()
     got = out.double().cpu().numpy()
     assert_close(dict(enumerate(got[:nd])), oracle_decode(b), kv_dtype, "mixed: decode rows")
@@ -513,7 +538,7 @@ def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel, monkeypatch):
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
-def test_attend_topk_64_and_padded_topk_rows(pbs, kv_dtype, monkeypatch):
+def test_attend_topk_64_and_padded_topk_rows(pbs, kv_dtype):
     """The largest top-k the boundary accepts (64), four query rows per decode request, and top-k
     rows read through a padded row stride (a [rows, 80] buffer viewed as [rows, 64])."""
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=16, num_kv_heads=2, topk=64,
@@ -529,13 +554,11 @@ def test_attend_topk_64_and_padded_topk_rows(pbs, kv_dtype, monkeypatch):
         assert_close(dict(enumerate(got)), want, kv_dtype, f"top-k 64 {part}")
 
 
-@pytest.mark.parametrize("part", ["dec", "tc", "token", "gather"])
-def test_attend_side_packed_blocks(pbs, part, monkeypatch):
+@pytest.mark.parametrize("part", ["dec", "tile", "token", "gather"])
+def test_attend_side_packed_blocks(pbs, part):
     """block_page_stride 16 ([sparse_pa] minimax_m3_sparse_block_page_stride with packed sides):
     block b's pages are 16 b + j, j < 8; the other 8 pages of each block hold NaN and must not be
     read."""
-    if part != "dec":
-        monkeypatch.setenv("PBS_PREFILL_KERNEL", part)
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, dec_seq_lens=[3000, 700],
                         pre_q_lens=[200, 40], pre_ctx_lens=[900, 0], future_prob=0.3, seed=53)
     nblk = b.num_pages // 8
@@ -544,7 +567,7 @@ def test_attend_side_packed_blocks(pbs, part, monkeypatch):
     b.cache = wide
     b.block_page_stride = 16
     err = _err()
-    got = gpu_attend(pbs, b, "dec" if part == "dec" else "pre", err)
+    got = gpu_attend(pbs, b, "dec" if part == "dec" else "pre", err, kernel=None if part == "dec" else part)
     assert int(err.item()) == 0
     want = oracle_decode(b) if part == "dec" else oracle_prefill(b)
     assert_close(dict(enumerate(got)), want, "bf16", f"side-packed {part}")
@@ -562,12 +585,11 @@ def test_attend_strided_pages(pbs):
     assert_close(dict(enumerate(out.double().cpu().numpy())), oracle_decode(b), "bf16", "strided pages")
 
 
-def test_prefill_gather_segments_and_reuse(pbs, monkeypatch):
+def test_prefill_gather_segments_and_reuse(pbs):
     """The gathered-row kernel on a workspace that holds one 256-token segment runs the call in
     segments; each token's partials and merge do not depend on the segment, so the output is
     bit-identical to the one-segment run on a larger workspace, and a second call on the same
     (now stale) workspace gives the same bits again."""
-    monkeypatch.setenv("PBS_PREFILL_KERNEL", "gather")
     b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=16, pre_q_lens=[700, 3, 300, 260],
                         pre_ctx_lens=[1500, 0, 6000, 128], future_prob=0.3, seed=70)
     p = b.pre
@@ -579,7 +601,83 @@ def test_prefill_gather_segments_and_reuse(pbs, monkeypatch):
     for nbytes in (full, small, small):
         ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)   # stale contents: all NaN
         err = _err()
-        outs.append(gpu_attend(pbs, b, "pre", err, workspace=ws))
+        outs.append(gpu_attend(pbs, b, "pre", err, workspace=ws, kernel="gather"))
         assert int(err.item()) == 0
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
     assert_close(dict(enumerate(outs[0])), oracle_prefill(b), "bf16", "gather segments")
+
+
+# ------------------------------------------------------------------------------------------
+# prebuilt sparse tables: built once, shared by the attends of several layers
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("entry", ["dec", "dec_ws", "dec_split4", "pre_token", "pre_tile", "pre_tile_hilo", "mixed"])
+def test_prebuilt_table_shared_by_two_layers(pbs, entry):
+    """The tables are built once with the builders ([sparse_pa] minimax_m3_build_sparse_block_table_*)
+    and fed to the attends of two "layers" (different queries, one selection). Each table-fed call
+    matches the oracle and is bit-identical to the same kernel compacting from top-k itself."""
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=8, dec_seq_lens=[3000, 700, 9000, 0],
+                        decode_query_len=2, pre_q_lens=[300, 40, 17], pre_ctx_lens=[400, 2000, 0], future_prob=0.3,
+                        seed=80)
+    d, p = b.dec, b.pre
+    sbt_d, ctx_d = pbs.build_sparse_block_table_decode(d.topk, d.page_table, d.seq_lens, d.decode_query_len)
+    sbt_p, ctx_p = pbs.build_sparse_block_table_prefill(p.topk, p.page_table, p.cu_seqlens_q, p.seq_lens)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(81)
+    for layer in range(2):
+        if layer == 1:  # the next layer: new queries, the same selection and tables
+            d.q = torch.randn(d.q.shape, generator=g, device=DEV).to(torch.bfloat16)
+            p.q = torch.randn(p.q.shape, generator=g, device=DEV).to(torch.bfloat16)
+        err = _err()
+        if entry == "mixed":
+            nd = d.q.shape[0]
+            args = (torch.cat([d.q, p.q]), b.cache, "bf16", 8, torch.cat([d.topk[0], p.topk[0]]), d.page_table,
+                    d.seq_lens, d.decode_query_len, p.page_table, p.cu_seqlens_q, p.seq_lens, b.softmax_scale)
+            fused = pbs.sparse_mixed_attention(*args)
+            tabled = pbs.sparse_mixed_attention(*args, err_word=err,
+                                                sparse_table=(torch.cat([sbt_d, sbt_p]), torch.cat([ctx_d, ctx_p])))
+            torch.cuda.synchronize()
+            fused, tabled = fused.double().cpu().numpy(), tabled.double().cpu().numpy()
+            want = {**oracle_decode(b), **{nd + r: v for r, v in oracle_prefill(b).items()}}
+        elif entry.startswith("dec"):
+            kw = dict(workspace="auto" if entry == "dec_ws" else None, splits=4 if entry == "dec_split4" else None)
+            fused = gpu_attend(pbs, b, "dec", **kw)
+            tabled = gpu_attend(pbs, b, "dec", err, sparse_table=(sbt_d, ctx_d), **kw)
+            want = oracle_decode(b)
+        else:
+            kernel = "token" if entry == "pre_token" else "tile"
+            ws = None if entry == "pre_tile_hilo" else "default"
+            fused = gpu_attend(pbs, b, "pre", workspace=ws, kernel=kernel)
+            tabled = gpu_attend(pbs, b, "pre", err, workspace=ws, kernel=kernel, sparse_table=(sbt_p, ctx_p))
+            want = oracle_prefill(b)
+        assert int(err.item()) == 0
+        assert np.array_equal(fused, tabled), f"{entry} layer {layer}: table-fed call differs from the fused one"
+        assert_close(dict(enumerate(tabled)), want, "bf16", f"prebuilt table {entry} layer {layer}")
+
+
+@pytest.mark.parametrize("kernel", ["dec", "token", "tile"])
+def test_prebuilt_table_unreadable_rows(pbs, kernel):
+    """A ctx past top-k x 128 (every kernel), or a slot that names no block of the request's page table
+    (the tile kernel, which streams whole blocks), sets PBS_DEVERR_TABLE and the row attends nothing;
+    the other rows are unaffected."""
+    b = workloads.small(device=DEV, num_heads=64, num_kv_heads=8, topk=4, dec_seq_lens=[900, 1500],
+                        pre_q_lens=[20], pre_ctx_lens=[700], seed=82)
+    part = "dec" if kernel == "dec" else "pre"
+    src = b.dec if part == "dec" else b.pre
+    if part == "dec":
+        sbt, ctx = pbs.build_sparse_block_table_decode(src.topk, src.page_table, src.seq_lens, 1)
+    else:
+        sbt, ctx = pbs.build_sparse_block_table_prefill(src.topk, src.page_table, src.cu_seqlens_q, src.seq_lens)
+    ctx[0] = 4 * 128 + 1
+    if kernel == "tile":
+        sbt[1, 0] += 1                     # slot 0 of row 1 no longer starts a block
+    err = _err()
+    got = gpu_attend(pbs, b, part, err, kernel=None if kernel == "dec" else kernel, sparse_table=(sbt, ctx))
+    assert int(err.item()) & pbs.DEVERR["table"]
+    assert np.all(got[0] == 0)
+    bad = {0, 1} if kernel == "tile" else {0}
+    if kernel == "tile":
+        assert np.all(got[1] == 0)
+    want = oracle_decode(b) if part == "dec" else oracle_prefill(b)
+    assert_close({r: got[r] for r in want if r not in bad}, {r: v for r, v in want.items() if r not in bad}, "bf16",
+                 "rows beside the unreadable ones")

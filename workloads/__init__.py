@@ -345,11 +345,12 @@ def tiny(device="cpu", seed: int = 1000, kv_dtype: str = "bf16") -> Batch:
     return b
 
 
-def decode(device="cuda", seed: int = 1001, batch: int = 64) -> Batch:
+def decode(device="cuda", seed: int = 1001, batch: int = 64, kv_dtype: str = "bf16") -> Batch:
+    """The decode workload; kv_dtype "fp8_e4m3" / "nvfp4" gives the same shape on those caches."""
     gen = torch.Generator()
     gen.manual_seed(seed + 3)
     sl = torch.randint(16384, 32768 + 1, (batch,), generator=gen).tolist()
-    return make_batch("decode_b64_16k-32k_top16_bf16", kv_dtype="bf16", num_heads=64, num_kv_heads=8,
+    return make_batch(f"decode_b{batch}_16k-32k_top16_{kv_dtype}", kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8,
                       head_dim=128, topk=16, dec_seq_lens=sl, seed=seed, device=device)
 
 
