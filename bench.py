@@ -247,6 +247,16 @@ def decode_union_bytes(b) -> float:
     return kv + 2.0 * rows * b.num_heads * 128 * 2 + rows * b.topk * 4 * 2 + rows * 4
 
 
+def table_bytes(b, ctx: torch.Tensor) -> float:
+    """Algorithmic bytes of one prefill table build: every top-k row read, one page-table entry per
+    causally valid distinct block (ceil(ctx / 128) of them per row), the table rows and ctx
+    written."""
+    p = b.pre
+    tk = p.topk.reshape(-1, p.topk.shape[-1])
+    valid = int(((ctx.to(torch.int64) + 127) // 128).sum().item())
+    return float(tk.numel() * 4 + valid * 4 + tk.shape[0] * b.topk * 8 * 4 + tk.shape[0] * 4)
+
+
 def prefill_flops(ctx: torch.Tensor, num_heads: int) -> float:
     """Algorithmic FLOPs: QK^T and PV over the attended keys only, 4 * Hq * D per (token, key)."""
     return 4.0 * num_heads * 128 * float(ctx.to(torch.int64).sum().item())
@@ -256,14 +266,14 @@ def prefill_flops(ctx: torch.Tensor, num_heads: int) -> float:
 # our arm
 # --------------------------------------------------------------------------------------------
 
-def run_decode(pbs, b, steps, warmup, flush, stream, sparse_table=None):
+def run_decode(pbs, b, steps, warmup, flush, stream, sparse_table=None, splits=None):
     d = b.dec
     out = torch.empty_like(d.q)
 
     def step():
         pbs.sparse_decode_attention(d.q, b.cache, b.kv_dtype, b.num_kv_heads, d.topk, d.page_table, d.seq_lens,
                                     d.decode_query_len, b.softmax_scale, b.k_scale, b.v_scale, b.block_page_stride,
-                                    out=out, stream=stream, sparse_table=sparse_table)
+                                    out=out, stream=stream, sparse_table=sparse_table, splits=splits)
     return time_steps(step, steps, warmup, flush, stream)
 
 
@@ -353,9 +363,10 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
         pbs.build_sparse_block_table_prefill(p.topk, p.page_table, p.cu_seqlens_q, p.seq_lens, 8, sparse_bt=sbt,
                                              sparse_ctx=ctxb, stream=stream)
     t = statistics.median(time_steps(tstep, steps, warmup, flush, stream))
-    tb = p.topk.numel() * 4 + sbt.numel() * 4 + ctxb.numel() * 4
-    res["table_build_prefill_22528rows"] = {"ms": t, "GB/s": tb / (t * 1e-3) / 1e9}
     ctx = prefill_ctx(pbs, b)
+    tb = table_bytes(b, ctx)
+    res["table_build_prefill_22528rows"] = {"ms": t, "GB/s": tb / (t * 1e-3) / 1e9,
+                                            "frac_of_hbm_peak": tb / (t * 1e-3) / 1e9 / hbm, "algorithmic_bytes": tb}
     fl = prefill_flops(ctx, b.num_heads)
     ts = run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream)
     t = statistics.median(ts)
@@ -509,33 +520,51 @@ def reference_arm(args, world, rank):
 def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, peak_src):
     """One JSON line for a non-headline workload (prefill TFLOP/s, or decode GB/s for fp8/NVFP4)."""
     make = {"prefill": workloads.prefill, "mtp_fp8": workloads.mtp_fp8, "mixed_nvfp4": workloads.mixed_nvfp4,
-            "prefill_g16": workloads.prefill_g16,
+            "prefill_g16": workloads.prefill_g16, "table_prefill": workloads.prefill,
             "decode_fp8": lambda device, seed: workloads.decode(device=device, seed=seed, kv_dtype="fp8_e4m3"),
             "decode_nvfp4": lambda device, seed: workloads.decode(device=device, seed=seed, kv_dtype="nvfp4")}
     b = make[args.workload](device="cuda", seed={"prefill": 1002, "mtp_fp8": 1003, "mixed_nvfp4": 1004,
-                                                 "prefill_g16": 1005, "decode_fp8": 1001,
-                                                 "decode_nvfp4": 1001}[args.workload] + 17 * rank)
+                                                 "prefill_g16": 1005, "decode_fp8": 1001, "decode_nvfp4": 1001,
+                                                 "table_prefill": 1002}[args.workload] + 17 * rank)
     if pg:
         pg.barrier()
     with ClockSampler(local) as clk:
-        part = "prefill" if args.workload in ("prefill", "prefill_g16") else args.part
+        part = {"prefill": "prefill", "prefill_g16": "prefill", "table_prefill": "table"}.get(args.workload,
+                                                                                              args.part)
         launches = 1  # per step
-        if part == "prefill":
+        kernel = None if args.prefill_kernel == "auto" else args.prefill_kernel
+        if part == "table":
+            # the standalone prefill table build: top-k rows, the page-table entries they name, the
+            # table and ctx written
+            p = b.pre
+            sbt = torch.empty(p.q.shape[0], b.topk * 8, dtype=torch.int32, device="cuda")
+            ctxb = torch.empty(p.q.shape[0], dtype=torch.int32, device="cuda")
+
+            def tstep():
+                pbs.build_sparse_block_table_prefill(p.topk, p.page_table, p.cu_seqlens_q, p.seq_lens, 8,
+                                                     sparse_bt=sbt, sparse_ctx=ctxb, stream=stream)
+            times = time_steps(tstep, args.steps, args.warmup, flush, stream)
+            work = table_bytes(b, prefill_ctx(pbs, b))
+            unit, bound, peak, metric = "GB/s", "hbm", hbm, "table build HBM GB/s"
+        elif part == "prefill":
             work = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
-            times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream)
+            times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream, kernel=kernel)
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
             p = b.pre
-            # the binding's default call on the tile kernel: V conversion, then the attend
-            if pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes, b.num_heads,
-                                         b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1]) == "tile" and \
-                    0 < pbs.prefill_tile_workspace_bytes(p.seq_lens.shape[0], b.num_kv_heads,
-                                                         p.page_table.shape[1]) <= pbs.TILE_WORKSPACE_CAP:
+            # the binding's default call on the tile kernel: V conversion, then the attend; the
+            # gathered-row kernel: its index kernel, then the attend, per token segment
+            chosen = pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes,
+                                               b.num_heads, b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
+                                               kernel=kernel,
+                                               workspace_bytes=1 << 62 if kernel == "gather" else 0)
+            if chosen == "tile" and 0 < pbs.prefill_tile_workspace_bytes(p.seq_lens.shape[0], b.num_kv_heads,
+                                                                         p.page_table.shape[1]) <= pbs.TILE_WORKSPACE_CAP:
                 launches = 2
         else:
             # rows of one request share their K/V rows: the union counts each once
             per_row = decode_bytes(b, decode_ctx(pbs, b))
             work = decode_union_bytes(b) if b.dec.decode_query_len > 1 else per_row
-            times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
+            times = run_decode(pbs, b, args.steps, args.warmup, flush, stream, splits=args.splits)
             unit, bound, peak, metric = "GB/s", "hbm", hbm, "decode HBM GB/s"
     ms = max_over_ranks(statistics.mean(times), pg, "cuda")
     scale = 1e12 if unit == "TFLOP/s" else 1e9
@@ -555,7 +584,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                          "traffic": traffic, "peak_source": f"{peak_src} (burst, kernel timed alone)",
                          "algorithmic_work_per_launch": work,
                          **({"per_row_sum_bytes": per_row, "per_row_sum_frac": per_row / (statistics.mean(times) * 1e-3)
-                             / scale / peak} if part != "prefill" and b.dec.decode_query_len > 1 else {})},
+                             / scale / peak} if part == "decode" and b.dec.decode_query_len > 1 else {})},
             "gpu_launches": args.steps * launches, "clocks": clk.summary()}), flush=True)
     if pg:
         pg.barrier()
@@ -579,8 +608,12 @@ def main():
                     help="decode requests (64 is the headline workload; smaller only for profiling)")
     ap.add_argument("--part", choices=["decode", "prefill"], default="decode",
                     help="which half of the mixed NVFP4 batch --workload mixed_nvfp4 times")
+    ap.add_argument("--splits", type=int, choices=[1, 2, 4, 8], default=None,
+                    help="force the decode attend's split count (profiling and tuning)")
+    ap.add_argument("--prefill-kernel", choices=["auto", "token", "tile", "gather"], default="auto",
+                    help="force the prefill kernel of --workload prefill / prefill_g16 / mixed_nvfp4 --part prefill")
     ap.add_argument("--workload", choices=["decode", "prefill", "prefill_g16", "mtp_fp8", "mixed_nvfp4", "decode_fp8",
-                                           "decode_nvfp4"],
+                                           "decode_nvfp4", "table_prefill"],
                     default="decode",
                     help="timed workload (the headline line is decode; the others for profiling and tuning)")
     args = ap.parse_args()
@@ -618,7 +651,7 @@ def main():
         pg.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        times = run_decode(pbs, b, args.steps, args.warmup, flush, stream)
+        times = run_decode(pbs, b, args.steps, args.warmup, flush, stream, splits=args.splits)
     torch.cuda.synchronize()
     ms = max_over_ranks(statistics.mean(times), pg, "cuda")
     if pg:
