@@ -40,12 +40,27 @@ namespace {
 // (512 row x kv-head CTAs) runs in a single wave.
 constexpr int kConsumerWarps = 3;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-// Page p goes to stage p % kStages and to consumer warp p % kConsumerWarps. With kStages a
-// multiple of kConsumerWarps every stage is always consumed by the same warp, one phase after
-// the other, so a parity wait can never be answered by a phase two steps behind (with 6 stages
-// and 4 warps a warp would skip every other phase of a stage and could pass its wait early).
-constexpr int kStages = 6;
-static_assert(kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
+// A consumer warp takes kPagesPerIter<FMT> consecutive pages per iteration: one for bf16 (the
+// kernel is HBM-bound there), two for fp8 / NVFP4, whose per-page work (dequantisation, two
+// dependent MMA chains, a softmax round) is the limit: two pages give each warp two independent
+// chains and one softmax round per 32 keys. Page p goes to stage p % kStages<FMT> and to
+// consumer warp (p / kPagesPerIter) % kConsumerWarps. With the stage count a multiple of
+// kPagesPerIter * kConsumerWarps every stage is always consumed by the same warp, one phase
+// after the other, so a parity wait can never be answered by a phase two steps behind (with 6
+// stages and 4 single-page warps a warp would skip every other phase of a stage and could pass
+// its wait early). fp8 / NVFP4 pages are smaller, so twice the stages keep as many bytes in
+// flight.
+template <int FMT>
+constexpr int kPagesPerIter = FMT == PBS_KV_BF16 ? 1 : 2;
+template <int FMT>
+constexpr int kStagesF = FMT == PBS_KV_BF16 ? 6 : 12;
+// fp8 / NVFP4 softmax: the running reference moves only by more than 2^8 (log2 domain)
+constexpr float kLazyRescaleLog2 = 8.0f;
+constexpr int kMaxStages = 12;
+static_assert(kStagesF<PBS_KV_BF16> % (kPagesPerIter<PBS_KV_BF16> * kConsumerWarps) == 0 &&
+                  kStagesF<PBS_KV_FP8_E4M3> % (kPagesPerIter<PBS_KV_FP8_E4M3> * kConsumerWarps) == 0 &&
+                  kStagesF<PBS_KV_NVFP4> % (kPagesPerIter<PBS_KV_NVFP4> * kConsumerWarps) == 0,
+              "each stage must belong to one consumer warp");
 constexpr int kTileHeads = 8;  // the n8 tile of the MMA: up to 8 query heads per kv head
 
 template <int FMT>
@@ -87,8 +102,8 @@ struct Merge {
 };
 
 struct Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   int32_t slot_base[kMaxTopk];
   int32_t page_id[kMaxTopk * kPagesPerBlock];  // page of the row's 16-key group n (n < ceil(ctx / 16))
   int32_t ctx;
@@ -99,7 +114,7 @@ struct Ctl {
 // The merge buffer reuses the stage ring once every page has been consumed.
 template <int FMT>
 constexpr size_t ring_bytes() {
-  return size_t(kStages) * StageBytes<FMT>::v > sizeof(Merge) ? size_t(kStages) * StageBytes<FMT>::v
+  return size_t(kStagesF<FMT>) * StageBytes<FMT>::v > sizeof(Merge) ? size_t(kStagesF<FMT>) * StageBytes<FMT>::v
                                                                : ((sizeof(Merge) + 1023) / 1024) * 1024;
 }
 template <int FMT>
@@ -182,6 +197,144 @@ __device__ __forceinline__ void zero_v_tail(uint32_t st, int nv, int lane) {
   __syncwarp();
 }
 
+// S^T = K Q^T for the 16 keys of each of NP page stages (addresses st[0..NP)), the first n_live
+// of which hold pages: keys as the MMA's M, the (up to) 8 query heads as its N; lane holds keys
+// hh, hh + 8 (hh = lane / 4) of heads 2c, 2c + 1 (c = lane % 4) in s[i][0..3]. The stages' MMA
+// chains are interleaved step by step, so each MMA's wait on its accumulator overlaps the other
+// chain. qf: the warp's Q fragments (bf16, or converted to f16).
+template <int FMT, bool PACKED, int NP>
+__device__ __forceinline__ void page_scores(const uint32_t (&st)[NP], int n_live, const uint32_t (&qf)[8][2], int lane,
+                                            float (&s)[NP][4]) {
+  const int hh = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+  if (FMT == PBS_KV_BF16) {
+    const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int hi = lane >> 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int chunk = 2 * (j & 3) + hi;
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        if (i >= n_live) continue;
+        uint32_t af[4];
+        ldsm_x4(st[i] + line_off<FMT, PACKED>(key, j >> 2) + ((chunk ^ (key & 7)) << 4), af);
+        mma_bf16(s[i], af, qf[j][0], qf[j][1]);
+      }
+    }
+  } else if (FMT == PBS_KV_FP8_E4M3) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        if (i >= n_live) continue;
+        const uint32_t w0 = lds32(st[i] + line_off<FMT, PACKED>(hh, 0) + ((j ^ hh) << 4) + 4 * c);
+        const uint32_t w1 = lds32(st[i] + line_off<FMT, PACKED>(hh + 8, 0) + ((j ^ hh) << 4) + 4 * c);
+        uint32_t af[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
+                          e4m3x2_to_f16x2(w1 >> 16)};
+        mma_f16(s[i], af, qf[j][0], qf[j][1]);
+      }
+    }
+  } else {
+    uint4 k0[NP], k1[NP];
+    uint32_t s0lo[NP], s0hi[NP], s1lo[NP], s1hi[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      if (i >= n_live) continue;
+      k0[i] = lds128(st[i] + hh * 64 + 16 * c);
+      k1[i] = lds128(st[i] + (hh + 8) * 64 + 16 * c);
+      const uint32_t sc0 = e4m3x2_to_f16x2(lds16(st[i] + 1024 + hh * 8 + 2 * c));
+      const uint32_t sc1 = e4m3x2_to_f16x2(lds16(st[i] + 1024 + (hh + 8) * 8 + 2 * c));
+      s0lo[i] = prmt(sc0, sc0, 0x1010);
+      s0hi[i] = prmt(sc0, sc0, 0x3232);
+      s1lo[i] = prmt(sc1, sc1, 0x1010);
+      s1hi[i] = prmt(sc1, sc1, 0x3232);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        if (i >= n_live) continue;
+        const uint32_t w0 = word_of(k0[i], j >> 1) >> (16 * (j & 1));
+        const uint32_t w1 = word_of(k1[i], j >> 1) >> (16 * (j & 1));
+        const uint32_t sa = j < 4 ? s0lo[i] : s0hi[i], sb = j < 4 ? s1lo[i] : s1hi[i];
+        uint32_t af[4] = {hmul2(e2m1x2_to_f16x2(w0), sa), hmul2(e2m1x2_to_f16x2(w1), sb),
+                          hmul2(e2m1x2_to_f16x2(w0 >> 8), sa), hmul2(e2m1x2_to_f16x2(w1 >> 8), sb)};
+        mma_f16(s[i], af, qf[j][0], qf[j][1]);
+      }
+    }
+  }
+}
+
+// O^T += V^T P^T for one page stage, given this lane's probabilities p0..p3 (keys hh, hh + 8 of
+// heads 2c, 2c + 1, laid out as page_scores returns them). bf16 V: P split into bf16 hi + lo
+// (two MMAs); fp8 / NVFP4 V: dequantised to f16, P in f16.
+template <int FMT, bool PACKED>
+__device__ __forceinline__ void page_pv(uint32_t st, float p0, float p1, float p2, float p3, int lane,
+                                        float (&o)[8][4]) {
+  const int hh = lane >> 2, c = lane & 3;
+  if (FMT == PBS_KV_BF16) {
+    const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+    const uint32_t l01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+    const uint32_t l23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+    const int mi = lane >> 3;
+    const int key = (lane & 7) + 8 * (mi >> 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int chunk = 2 * (i & 3) + (mi & 1);
+      uint32_t vf[4];
+      ldsm_x4_trans(st + line_off<FMT, PACKED>(key, 2 + (i >> 2)) + ((chunk ^ (key & 7)) << 4), vf);
+      mma_bf16(o[i], vf, bh0, bh1);
+      mma_bf16(o[i], vf, bl0, bl1);
+    }
+  } else {
+    const uint32_t b0 = movmatrix_trans(pack_f16(p0, p1)), b1 = movmatrix_trans(pack_f16(p2, p3));
+    if (FMT == PBS_KV_FP8_E4M3) {
+      const uint4 va = lds128(st + line_off<FMT, PACKED>(2 * c, 1) + ((hh ^ ((2 * c) & 7)) << 4));
+      const uint4 vbb = lds128(st + line_off<FMT, PACKED>(2 * c + 1, 1) + ((hh ^ ((2 * c + 1) & 7)) << 4));
+      const uint4 vc = lds128(st + line_off<FMT, PACKED>(2 * c + 8, 1) + ((hh ^ ((2 * c + 8) & 7)) << 4));
+      const uint4 vd = lds128(st + line_off<FMT, PACKED>(2 * c + 9, 1) + ((hh ^ ((2 * c + 9) & 7)) << 4));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x = prmt(word_of(va, i >> 1), word_of(vbb, i >> 1), sel);
+        const uint32_t y = prmt(word_of(vc, i >> 1), word_of(vd, i >> 1), sel);
+        uint32_t af[4] = {e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y),
+                          e4m3x2_to_f16x2(y >> 16)};
+        mma_f16(o[i], af, b0, b1);
+      }
+    } else {
+      const uint32_t vc0 = st + kNvfp4Slot, vs0 = st + kNvfp4Slot + 1024;
+      const uint2 wa = lds64(vc0 + (2 * c) * 64 + 8 * hh);
+      const uint2 wb = lds64(vc0 + (2 * c + 1) * 64 + 8 * hh);
+      const uint2 wc = lds64(vc0 + (2 * c + 8) * 64 + 8 * hh);
+      const uint2 wd = lds64(vc0 + (2 * c + 9) * 64 + 8 * hh);
+      const uint32_t sab = e4m3x2_to_f16x2(lds8(vs0 + (2 * c) * 8 + hh) | (lds8(vs0 + (2 * c + 1) * 8 + hh) << 8));
+      const uint32_t scd = e4m3x2_to_f16x2(lds8(vs0 + (2 * c + 8) * 8 + hh) | (lds8(vs0 + (2 * c + 9) * 8 + hh) << 8));
+#pragma unroll
+      for (int wh = 0; wh < 2; ++wh) {
+        const uint32_t A = wh ? wa.y : wa.x, B = wh ? wb.y : wb.x;
+        const uint32_t C = wh ? wc.y : wc.x, D = wh ? wd.y : wd.x;
+        const uint32_t lo_ab = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
+        const uint32_t hi_ab = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
+        const uint32_t lo_cd = (C & 0x0F0F0F0Fu) | ((D & 0x0F0F0F0Fu) << 4);
+        const uint32_t hi_cd = ((C >> 4) & 0x0F0F0F0Fu) | (D & 0xF0F0F0F0u);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int i = 4 * wh + b;
+          uint32_t af[4] = {hmul2(e2m1x2_to_f16x2(lo_ab >> (8 * b)), sab),
+                            hmul2(e2m1x2_to_f16x2(hi_ab >> (8 * b)), sab),
+                            hmul2(e2m1x2_to_f16x2(lo_cd >> (8 * b)), scd),
+                            hmul2(e2m1x2_to_f16x2(hi_cd >> (8 * b)), scd)};
+          mma_f16(o[i], af, b0, b1);
+        }
+      }
+    }
+  }
+}
+
 #ifdef PBS_TRACE
 // Trace build only: per CTA {SM id, start, first page landed, end} in global-timer ns.
 constexpr int kDTraceCtas = 8192;
@@ -217,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     DTRACE(0, smid);
     DTRACE(1, global_timer_ns());
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kStagesF<FMT>; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], 1);
     }
@@ -323,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     if (lane == 0) {
       int issued = 0;
       for (int p = 0; p < npages; ++p) {
-        const int stage = p % kStages;
-        if (p >= kStages) {
-          if (!mbar_wait_bounded(&ctl->empty[stage], ((p / kStages) - 1) & 1)) {
+        const int stage = p % kStagesF<FMT>;
+        if (p >= kStagesF<FMT>) {
+          if (!mbar_wait_bounded(&ctl->empty[stage], ((p / kStagesF<FMT>) - 1) & 1)) {
             set_err(a.err_word, PBS_DEVERR_TIMEOUT);
             atomicExch(&ctl->abort, 1);
             break;
@@ -370,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
         issued = p + 1;
       }
       // every copy this CTA issued must land before its shared memory goes away
-      for (int p = max(0, issued - kStages); p < issued; ++p) {
-        if (!mbar_wait_bounded(&ctl->full[p % kStages], (p / kStages) & 1)) {
+      for (int p = max(0, issued - kStagesF<FMT>); p < issued; ++p) {
+        if (!mbar_wait_bounded(&ctl->full[p % kStagesF<FMT>], (p / kStagesF<FMT>) & 1)) {
           set_err(a.err_word, PBS_DEVERR_TIMEOUT);
           break;
         }
@@ -379,153 +532,118 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    const int hh = lane >> 2, c = lane & 3;
+    constexpr int kPP = kPagesPerIter<FMT>;
+    constexpr int kNS = kStagesF<FMT>;
+    const int hh = lane >> 2;
     float o[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const float sl2 = a.scale_log2;
 
-    for (int p = warp; p < npages; p += kConsumerWarps) {
-      const int stage = p % kStages;
-      if (!mbar_wait_bounded(&ctl->full[stage], (p / kStages) & 1)) {
-        set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-        atomicExch(&ctl->abort, 1);
-        break;
+    for (int p0 = warp * kPP; p0 < npages; p0 += kPP * kConsumerWarps) {
+      // the iteration's pages p0 .. p0 + kPP - 1 that exist (a row's last iteration may have fewer)
+      const int n_live = min(kPP, npages - p0);
+      uint32_t st[kPP];
+      int nv[kPP];
+      bool ok = true;
+#pragma unroll
+      for (int i = 0; i < kPP; ++i) {
+        const int p = p0 + i;
+        st[i] = smem_u32(stages + (p % kNS) * kStage);
+        nv[i] = 0;
+        if (i >= n_live) continue;
+        if (!mbar_wait_bounded(&ctl->full[p % kNS], (p / kNS) & 1)) {
+          set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+          atomicExch(&ctl->abort, 1);
+          ok = false;
+          break;
+        }
+        if (p == 0 && lane == 0) DTRACE(2, global_timer_ns());
+        nv[i] = min(kPageRows, key1 - (key0 + p * kPageRows));
+        if (nv[i] < kPageRows) zero_v_tail<FMT, PACKED>(st[i], nv[i], lane);
       }
-      const uint32_t st = smem_u32(stages + stage * kStage);
-      if (p == 0 && lane == 0) DTRACE(2, global_timer_ns());
-      const int nv = min(kPageRows, key1 - (key0 + p * kPageRows));
-      if (nv < kPageRows) zero_v_tail<FMT, PACKED>(st, nv, lane);
-
-      // ---- S^T = K Q^T (16 keys x 8 heads)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      if (FMT == PBS_KV_BF16) {
-        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int hi = lane >> 4;
+      if (!ok) break;
+      // ---- S^T = K Q^T (16 keys x 8 heads per page)
+      float sc[kPP][4];
+      page_scores<FMT, PACKED, kPP>(st, n_live, qf, lane, sc);
+      float t[kPP][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int chunk = 2 * (j & 3) + hi;
-          uint32_t af[4];
-          ldsm_x4(st + line_off<FMT, PACKED>(key, j >> 2) + ((chunk ^ (key & 7)) << 4), af);
-          mma_bf16(s, af, qf[j][0], qf[j][1]);
-        }
-      } else if (FMT == PBS_KV_FP8_E4M3) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w0 = lds32(st + line_off<FMT, PACKED>(hh, 0) + ((j ^ hh) << 4) + 4 * c);
-          const uint32_t w1 = lds32(st + line_off<FMT, PACKED>(hh + 8, 0) + ((j ^ hh) << 4) + 4 * c);
-          uint32_t af[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
-                            e4m3x2_to_f16x2(w1 >> 16)};
-          mma_f16(s, af, qf[j][0], qf[j][1]);
-        }
-      } else {
-        const uint4 k0 = lds128(st + hh * 64 + 16 * c);
-        const uint4 k1 = lds128(st + (hh + 8) * 64 + 16 * c);
-        const uint32_t sc0 = e4m3x2_to_f16x2(lds16(st + 1024 + hh * 8 + 2 * c));
-        const uint32_t sc1 = e4m3x2_to_f16x2(lds16(st + 1024 + (hh + 8) * 8 + 2 * c));
-        const uint32_t s0lo = prmt(sc0, sc0, 0x1010), s0hi = prmt(sc0, sc0, 0x3232);
-        const uint32_t s1lo = prmt(sc1, sc1, 0x1010), s1hi = prmt(sc1, sc1, 0x3232);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w0 = word_of(k0, j >> 1) >> (16 * (j & 1));
-          const uint32_t w1 = word_of(k1, j >> 1) >> (16 * (j & 1));
-          const uint32_t sa = j < 4 ? s0lo : s0hi, sb = j < 4 ? s1lo : s1hi;
-          uint32_t af[4] = {hmul2(e2m1x2_to_f16x2(w0), sa), hmul2(e2m1x2_to_f16x2(w1), sb),
-                            hmul2(e2m1x2_to_f16x2(w0 >> 8), sa), hmul2(e2m1x2_to_f16x2(w1 >> 8), sb)};
-          mma_f16(s, af, qf[j][0], qf[j][1]);
-        }
+      for (int i = 0; i < kPP; ++i) {
+        // keys past the range (or a page that does not exist: nv 0) take no weight
+        const bool ok_lo = hh < nv[i], ok_hi = hh + 8 < nv[i];
+        t[i][0] = ok_lo ? sc[i][0] * sl2 : -INFINITY;
+        t[i][1] = ok_lo ? sc[i][1] * sl2 : -INFINITY;
+        t[i][2] = ok_hi ? sc[i][2] * sl2 : -INFINITY;
+        t[i][3] = ok_hi ? sc[i][3] * sl2 : -INFINITY;
       }
 
-      // ---- online softmax (log2 domain); lane holds keys hh, hh+8 of heads 2c, 2c+1
-      const bool ok_lo = hh < nv, ok_hi = hh + 8 < nv;
-      const float t0 = ok_lo ? s[0] * sl2 : -INFINITY, t1 = ok_lo ? s[1] * sl2 : -INFINITY;
-      const float t2 = ok_hi ? s[2] * sl2 : -INFINITY, t3 = ok_hi ? s[3] * sl2 : -INFINITY;
-      float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+      // ---- online softmax (log2 domain) over the iteration's keys
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kPP; ++i) {
+        mx0 = fmaxf(mx0, fmaxf(t[i][0], t[i][2]));
+        mx1 = fmaxf(mx1, fmaxf(t[i][1], t[i][3]));
+      }
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-      const float p0 = ex2(t0 - mu0), p1 = ex2(t1 - mu1), p2 = ex2(t2 - mu0), p3 = ex2(t3 - mu1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[i][0] *= al0;
-        o[i][1] *= al1;
-        o[i][2] *= al0;
-        o[i][3] *= al1;
+      float mu0, mu1, al0, al1;
+      if (kPP == 1) {
+        // exact running maximum (bf16 P, split into hi + lo, keeps full precision either way)
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        al0 = ex2(m0 - mu0);
+        al1 = ex2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+      } else {
+        // lazy reference (f16 P): m moves, and O and l are rescaled, only when the iteration's
+        // maximum passes it by 2^8, so P stays below 2^8 and most iterations skip the rescale
+        const bool g0 = mx0 > m0 + kLazyRescaleLog2, g1 = mx1 > m1 + kLazyRescaleLog2;
+        al0 = g0 ? ex2(m0 - mx0) : 1.f;
+        al1 = g1 ? ex2(m1 - mx1) : 1.f;
+        m0 = g0 ? mx0 : m0;
+        m1 = g1 ? mx1 : m1;
+        mu0 = m0 == -INFINITY ? 0.f : m0;
+        mu1 = m1 == -INFINITY ? 0.f : m1;
       }
-
-      // ---- O^T += V^T P^T
-      if (FMT == PBS_KV_BF16) {
-        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-        const uint32_t l01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t l23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-        const int mi = lane >> 3;
-        const int key = (lane & 7) + 8 * (mi >> 1);
+      float pr[kPP][4];
+      float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPP; ++i) {
+        pr[i][0] = ex2(t[i][0] - mu0);
+        pr[i][1] = ex2(t[i][1] - mu1);
+        pr[i][2] = ex2(t[i][2] - mu0);
+        pr[i][3] = ex2(t[i][3] - mu1);
+        add0 += pr[i][0] + pr[i][2];
+        add1 += pr[i][1] + pr[i][3];
+      }
+      l0 = l0 * al0 + add0;
+      l1 = l1 * al1 + add1;
+      if (kPP == 1 || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int chunk = 2 * (i & 3) + (mi & 1);
-          uint32_t vf[4];
-          ldsm_x4_trans(st + line_off<FMT, PACKED>(key, 2 + (i >> 2)) + ((chunk ^ (key & 7)) << 4), vf);
-          mma_bf16(o[i], vf, bh0, bh1);
-          mma_bf16(o[i], vf, bl0, bl1);
-        }
-      } else {
-        const uint32_t b0 = movmatrix_trans(pack_f16(p0, p1)), b1 = movmatrix_trans(pack_f16(p2, p3));
-        if (FMT == PBS_KV_FP8_E4M3) {
-          const uint4 va = lds128(st + line_off<FMT, PACKED>(2 * c, 1) + ((hh ^ ((2 * c) & 7)) << 4));
-          const uint4 vbb = lds128(st + line_off<FMT, PACKED>(2 * c + 1, 1) + ((hh ^ ((2 * c + 1) & 7)) << 4));
-          const uint4 vc = lds128(st + line_off<FMT, PACKED>(2 * c + 8, 1) + ((hh ^ ((2 * c + 8) & 7)) << 4));
-          const uint4 vd = lds128(st + line_off<FMT, PACKED>(2 * c + 9, 1) + ((hh ^ ((2 * c + 9) & 7)) << 4));
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-            const uint32_t x = prmt(word_of(va, i >> 1), word_of(vbb, i >> 1), sel);
-            const uint32_t y = prmt(word_of(vc, i >> 1), word_of(vd, i >> 1), sel);
-            uint32_t af[4] = {e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y),
-                              e4m3x2_to_f16x2(y >> 16)};
-            mma_f16(o[i], af, b0, b1);
-          }
-        } else {
-          const uint32_t vc0 = st + kNvfp4Slot, vs0 = st + kNvfp4Slot + 1024;
-          const uint2 wa = lds64(vc0 + (2 * c) * 64 + 8 * hh);
-          const uint2 wb = lds64(vc0 + (2 * c + 1) * 64 + 8 * hh);
-          const uint2 wc = lds64(vc0 + (2 * c + 8) * 64 + 8 * hh);
-          const uint2 wd = lds64(vc0 + (2 * c + 9) * 64 + 8 * hh);
-          const uint32_t sab = e4m3x2_to_f16x2(lds8(vs0 + (2 * c) * 8 + hh) | (lds8(vs0 + (2 * c + 1) * 8 + hh) << 8));
-          const uint32_t scd = e4m3x2_to_f16x2(lds8(vs0 + (2 * c + 8) * 8 + hh) | (lds8(vs0 + (2 * c + 9) * 8 + hh) << 8));
-#pragma unroll
-          for (int wh = 0; wh < 2; ++wh) {
-            const uint32_t A = wh ? wa.y : wa.x, B = wh ? wb.y : wb.x;
-            const uint32_t C = wh ? wc.y : wc.x, D = wh ? wd.y : wd.x;
-            const uint32_t lo_ab = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
-            const uint32_t hi_ab = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
-            const uint32_t lo_cd = (C & 0x0F0F0F0Fu) | ((D & 0x0F0F0F0Fu) << 4);
-            const uint32_t hi_cd = ((C >> 4) & 0x0F0F0F0Fu) | (D & 0xF0F0F0F0u);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const int i = 4 * wh + b;
-              uint32_t af[4] = {hmul2(e2m1x2_to_f16x2(lo_ab >> (8 * b)), sab),
-                                hmul2(e2m1x2_to_f16x2(hi_ab >> (8 * b)), sab),
-                                hmul2(e2m1x2_to_f16x2(lo_cd >> (8 * b)), scd),
-                                hmul2(e2m1x2_to_f16x2(hi_cd >> (8 * b)), scd)};
-              mma_f16(o[i], af, b0, b1);
-            }
-          }
+          o[i][0] *= al0;
+          o[i][1] *= al1;
+          o[i][2] *= al0;
+          o[i][3] *= al1;
         }
       }
+
+      // ---- O^T += V^T P^T, page by page (a page that does not exist holds no V to read)
+#pragma unroll
+      for (int i = 0; i < kPP; ++i)
+        if (i < n_live) page_pv<FMT, PACKED>(st[i], pr[i][0], pr[i][1], pr[i][2], pr[i][3], lane, o);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->empty[stage]);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kPP; ++i)
+          if (i < n_live) mbar_arrive(&ctl->empty[(p0 + i) % kNS]);
+      }
     }
 
     // ---- this warp's row sums; the partials go to shared memory once the ring is drained
