@@ -444,9 +444,20 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
                                    d.decode_query_len, p.page_table, p.cu_seqlens_q, p.seq_lens, b.softmax_scale,
                                    b.k_scale, b.v_scale, b.block_page_stride, out=om, stream=stream)
     tm = statistics.median(time_steps(mstep, max(2, steps // 4), min(warmup, 3), flush, stream))
+    chosen = pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes, b.num_heads,
+                                       b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
+                                       workspace_bytes=1 << 62)
     res["mixed_nvfp4"] = {"decode_ms": td, "decode_GB/s": by / (td * 1e-3) / 1e9,
-                          "prefill_ms": tp, "prefill_TFLOP/s": fl / (tp * 1e-3) / 1e12, "total_ms": td + tp,
-                          "one_call_ms": tm}
+                          "decode_frac_of_hbm_peak": by / (td * 1e-3) / 1e9 / hbm,
+                          "prefill_ms": tp, "prefill_TFLOP/s": fl / (tp * 1e-3) / 1e12,
+                          "prefill_frac_of_bf16_peak": fl / (tp * 1e-3) / 1e12 / bf16, "prefill_kernel": chosen,
+                          "total_ms": td + tp, "one_call_ms": tm}
+    # the prefill part on each prefill kernel (tile: NVFP4 K / V converted to images, then tcgen05)
+    for kern in ("tile", "token"):
+        t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, kernel=kern))
+        res["mixed_nvfp4"][f"prefill_{kern}_ms"] = t
+        res["mixed_nvfp4"][f"prefill_{kern}_TFLOP/s"] = fl / (t * 1e-3) / 1e12
+    pbs._tile_workspaces.clear()
     del qm, tkm, om
     del b
     torch.cuda.empty_cache()
@@ -555,10 +566,9 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             # gathered-row kernel: its index kernel, then the attend, per token segment
             chosen = pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes,
                                                b.num_heads, b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
-                                               kernel=kernel,
-                                               workspace_bytes=1 << 62 if kernel == "gather" else 0)
-            if chosen == "tile" and 0 < pbs.prefill_tile_workspace_bytes(p.seq_lens.shape[0], b.num_kv_heads,
-                                                                         p.page_table.shape[1]) <= pbs.TILE_WORKSPACE_CAP:
+                                               kernel=kernel, workspace_bytes=1 << 62)
+            if chosen == "tile" and 0 < pbs.prefill_tile_workspace_bytes(
+                    p.seq_lens.shape[0], b.num_kv_heads, p.page_table.shape[1], b.kv_dtype) <= pbs.TILE_WORKSPACE_CAP:
                 launches = 2
         else:
             # rows of one request share their K/V rows: the union counts each once

@@ -97,8 +97,9 @@ typedef struct CUstream_st* pbs_stream_t;
  * pbs_prefill_kernel_choice). */
 #define PBS_PREFILL_AUTO    0  /* the library's rule (see pbs_prefill_kernel_choice) */
 #define PBS_PREFILL_TOKEN   1  /* token-centric kernel: any shape, mma.sync, one row per CTA group */
-#define PBS_PREFILL_TILE    2  /* tcgen05 tile kernel: bf16 packed cache, GQA 8 or 16, top-k <= 16,
-                                  page table <= 128 blocks, 16-byte aligned q / out rows */
+#define PBS_PREFILL_TILE    2  /* tcgen05 tile kernel: GQA 8 or 16, top-k <= 16, page table <= 65535
+                                  blocks, 16-byte aligned q / out rows; a packed bf16 cache, or an
+                                  fp8 / NVFP4 cache with its workspace (pbs_prefill_tile_workspace_bytes) */
 #define PBS_PREFILL_GATHER  3  /* tcgen05 gathered-row kernel: as the tile kernel but page tables up to
                                   8192 blocks and top-k <= 64; needs its workspace; no prebuilt table */
 
@@ -294,10 +295,11 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
  *               size requires (pbs_prefill_workspace_bytes(total_q, ...) bytes: one segment).
  *               Otherwise the tcgen05 tile kernel or the token-centric kernel runs. The tile
  *               kernel, given a 256-byte aligned workspace of at least
- *               pbs_prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks) bytes, first
- *               converts the V of every (request, block, kv head) the call can read to fp16 there
- *               (V * 2^-e per block, exact) and then applies P in fp16, one MMA per 16 keys;
- *               without it, it applies bf16 P as hi + lo parts (two MMAs, same accuracy). The
+ *               pbs_prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks, kv_dtype)
+ *               bytes, first converts the V of every (request, block, kv head) the call can read
+ *               to fp16 there (V * 2^-e per block, exact), and for fp8 / NVFP4 caches K to bf16,
+ *               and then applies P in fp16, one MMA per 16 keys; without it (bf16 caches only) it
+ *               applies bf16 P as hi + lo parts (two MMAs, same accuracy). The
  *               token-centric kernel merges split rows through the workspace when it holds
  *               pbs_attend_workspace_bytes (its tickets are cleared by the call, so here the
  *               workspace needs no zeroing) and ignores a smaller one. Calls that share one
@@ -349,12 +351,15 @@ PBS_API size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, in
                                            int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks);
 
 /*
- * Bytes of the workspace with which pbs_sparse_prefill_attention's tcgen05 tile kernel runs its
- * fp16-V path: num_reqs * max_blocks * num_kv_heads converted V blocks of 32 KiB plus one int32
- * exponent each (rounded up to 256 bytes); 0 for invalid arguments or max_blocks > 128 (the tile
- * kernel's limit). No counterpart on the pages.
+ * Bytes of the workspace with which pbs_sparse_prefill_attention's tcgen05 tile kernel runs on a
+ * cache of format kv_dtype: num_reqs * max_blocks * num_kv_heads converted V blocks of 32 KiB
+ * (fp16), one int32 exponent each (rounded up to 256 bytes), and for fp8 / NVFP4 as many converted
+ * K blocks of 32 KiB (bf16, exact). With it a bf16 call applies P in fp16 (one MMA per 16 keys);
+ * an fp8 / NVFP4 call needs it to run on the tile kernel at all. 0 for invalid arguments,
+ * num_reqs > 65535 or max_blocks > 65535. No counterpart on the pages.
  */
-PBS_API size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks);
+PBS_API size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks,
+                                                int32_t kv_dtype);
 
 /*
  * Mixed batch in one call ([flashinfer] forward with both parts: decode rows q[:nd], prefill

@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
     L.pbs_prefill_workspace_bytes.restype = ctypes.c_size_t
     L.pbs_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     L.pbs_prefill_tile_workspace_bytes.restype = ctypes.c_size_t
-    L.pbs_prefill_tile_workspace_bytes.argtypes = [i32, i32, i32]
+    L.pbs_prefill_tile_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.pbs_prefill_kernel_choice.restype = ctypes.c_int
     L.pbs_prefill_kernel_choice.argtypes = [i32, i32, i32, i64, i32, i32, i32, i32, i32, ctypes.c_size_t, vp]
     table_common = [vp, i64, i32, i32, vp, i64, i32]
@@ -314,22 +314,28 @@ def prefill_workspace_bytes(total_q: int, num_reqs: int, num_heads: int, num_kv_
                                                  int(topk), int(max_blocks)))
 
 
-def prefill_tile_workspace_bytes(num_reqs: int, num_kv_heads: int, max_blocks: int) -> int:
-    """Bytes with which the prefill attend's tcgen05 tile kernel converts V to fp16 once per
-    (request, block, kv head) and applies P in fp16 (0: the tile kernel cannot take this shape)."""
-    return int(lib().pbs_prefill_tile_workspace_bytes(int(num_reqs), int(num_kv_heads), int(max_blocks)))
+def prefill_tile_workspace_bytes(num_reqs: int, num_kv_heads: int, max_blocks: int, kv_dtype: str = "bf16") -> int:
+    """Bytes with which the prefill attend's tcgen05 tile kernel converts V to fp16 (and, for fp8 /
+    NVFP4 caches, K to bf16) once per (request, block, kv head) and applies P in fp16 (0: the tile
+    kernel cannot take this shape)."""
+    return int(lib().pbs_prefill_tile_workspace_bytes(int(num_reqs), int(num_kv_heads), int(max_blocks),
+                                                      KV_DTYPES[kv_dtype]))
 
 
 # the tile kernel's converted-V workspace is allocated by default up to this size
 TILE_WORKSPACE_CAP = 1 << 30
+# "the call will pass whatever workspace the chosen kernel asks for" (pbs_prefill_kernel_choice)
+_ANY_WORKSPACE = (1 << 63) - 1
 _tile_workspaces: dict = {}
 
 
-def prefill_tile_workspace(num_reqs: int, num_kv_heads: int, max_blocks: int, device, stream=None):
-    """The tile kernel's converted-V workspace, cached per (device, stream) and grown on demand;
-    None when the shape does not take it or it would exceed ``TILE_WORKSPACE_CAP`` (the kernel
-    then applies bf16 P as hi + lo parts). Needs no initial value."""
-    need = prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks)
+def prefill_tile_workspace(num_reqs: int, num_kv_heads: int, max_blocks: int, device, stream=None,
+                           kv_dtype: str = "bf16"):
+    """The tile kernel's workspace (converted V, and K for fp8 / NVFP4), cached per (device, stream)
+    and grown on demand; None when the shape does not take it or it would exceed
+    ``TILE_WORKSPACE_CAP`` (a bf16 call then applies P as hi + lo parts, an fp8 / NVFP4 call runs
+    on the token-centric kernel). Needs no initial value."""
+    need = prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks, kv_dtype)
     if need == 0 or need > TILE_WORKSPACE_CAP:
         return None
     device = torch.device(device)
@@ -474,8 +480,8 @@ def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk
             workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
                                           pt.shape[1], q.device, stream)
         elif prefill_kernel_choice(q.shape[0], sl.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads, tk.shape[1],
-                                   pt.shape[1], sparse_table is not None, 0, kernel) == "tile":
-            workspace = prefill_tile_workspace(sl.shape[0], num_kv_heads, pt.shape[1], q.device, stream)
+                                   pt.shape[1], sparse_table is not None, _ANY_WORKSPACE, kernel) == "tile":
+            workspace = prefill_tile_workspace(sl.shape[0], num_kv_heads, pt.shape[1], q.device, stream, kv_dtype)
         else:
             workspace = None  # the token-centric kernel merges its splits in a cluster
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)

@@ -198,8 +198,11 @@ int read_options(const pbs_attend_options* o, Options* out) {
 // PBS_ERR_UNSUPPORTED when the option asks for a kernel that cannot run the call. The one rule
 // behind both the call and pbs_prefill_kernel_choice.
 int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int forced, int* kernel) {
-  // the tcgen05 kernels read the packed bf16 cache through the 5-D map
-  const bool tile_fits = a.packed_map != 0 && pbs::prefill_tc_supported(a);
+  // the tile kernel reads a packed bf16 cache through its block map, an fp8 / NVFP4 cache through
+  // the images its conversion kernel writes into the workspace
+  const size_t tile_ws = pbs::prefill_tc_workspace_bytes(a.num_reqs, a.num_kv_heads, a.max_blocks, a.kv_dtype);
+  const bool tile_fits = (a.kv_dtype != PBS_KV_BF16 || a.packed_map != 0) &&
+                         pbs::prefill_tc_supported(a, tile_ws != 0 && workspace_bytes >= tile_ws);
   const bool gather_fits = a.packed_map != 0 && pbs::prefill_gather_supported(a) && a.num_rows < (1 << 25) &&
                            pbs::gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k,
                                                       a.max_blocks, workspace_bytes) > 0;
@@ -674,11 +677,14 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     e = pbs::launch_attend(a, pbs::kModePrefill, map, cs);
   } else {
     // both tcgen05 kernels stream K and V separately: the gathered-row kernel one box per
-    // (page, head) half row, the tile kernel one box per (block, head) half row
+    // (page, head) half row, the tile kernel one box per (block, head) half row (bf16; fp8 / NVFP4
+    // blocks come from converted images, and the map is unused)
     CUtensorMap half_map;
-    st = kernel == PBS_PREFILL_GATHER
-             ? encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2)
-             : encode_cache_map_block(&half_map, kv_cache, num_kv_heads, num_pages, page_stride_bytes);
+    std::memset(&half_map, 0, sizeof(half_map));
+    if (kernel == PBS_PREFILL_GATHER)
+      st = encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2);
+    else if (kv_dtype == PBS_KV_BF16)
+      st = encode_cache_map_block(&half_map, kv_cache, num_kv_heads, num_pages, page_stride_bytes);
     if (st != PBS_OK) return st;
     CUtensorMap qmap;
     st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride,
@@ -686,12 +692,15 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     if (st != PBS_OK) return st;
     if (kernel == PBS_PREFILL_TILE && workspace != nullptr && aligned(workspace, 256) && num_reqs <= 65535) {
       // with room for the converted V of every (request, block, kv head), the tile kernel applies
-      // P in fp16 with one MMA per 16 keys instead of bf16 hi + lo
-      const size_t need = pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks);
+      // P in fp16 with one MMA per 16 keys instead of bf16 hi + lo; fp8 / NVFP4 K comes from
+      // converted bf16 images after them (the kernel choice made sure the workspace holds them)
+      const size_t need = pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, kv_dtype);
       if (need != 0 && workspace_bytes >= need) {
+        const int64_t n = static_cast<int64_t>(num_reqs) * max_blocks * num_kv_heads;
         a.vconv = static_cast<uint8_t*>(workspace);
-        a.vconv_exp = reinterpret_cast<int32_t*>(a.vconv + static_cast<int64_t>(num_reqs) * max_blocks * num_kv_heads *
-                                                              pbs::kTileVBytes);
+        a.vconv_exp = reinterpret_cast<int32_t*>(a.vconv + n * pbs::kTileVBytes);
+        if (kv_dtype != PBS_KV_BF16)
+          a.kconv = a.vconv + n * pbs::kTileVBytes + ((n * 4 + 255) / 256) * 256;
       }
     }
     e = kernel == PBS_PREFILL_GATHER ? pbs::launch_prefill_gather(a, half_map, qmap, workspace, workspace_bytes, cs)
@@ -732,8 +741,8 @@ int pbs_prefill_kernel_choice(int32_t total_q, int32_t num_reqs, int32_t kv_dtyp
   return st == PBS_OK ? kernel : -st;
 }
 
-size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks) {
-  return pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks);
+size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv_heads, int32_t max_blocks, int32_t kv_dtype) {
+  return pbs::prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, kv_dtype);
 }
 
 size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads, int32_t num_kv_heads,

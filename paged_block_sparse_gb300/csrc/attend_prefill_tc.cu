@@ -63,8 +63,11 @@ constexpr int kTileBytes = 2 * kHalf;                  // 32 KiB: a block's K, o
 constexpr int kStagesTc = 3;                           // stages of the K ring and of the V ring
 constexpr int kSBuf = 3;                               // S buffers in TMEM (S runs 2 blocks ahead of PV)
 constexpr int kBigBytes = kQBytes + 2 * kStagesTc * kTileBytes;  // 224 KiB
-constexpr int kMaxUnion = 128;    // union blocks per tile: the kernel takes page tables <= 128 blocks wide
-constexpr int kSetWords = kMaxUnion / 32;
+// Union entries per tile descriptor. A tile's union (at most 16 tokens x top-k 16 = 256 distinct
+// blocks) spans one or two descriptors; block ids travel as 16 bits, so page tables may be up to
+// kTcMaxBlocks blocks wide.
+constexpr int kMaxUnion = 128;
+constexpr int kTcMaxBlocks = 65535;
 constexpr int kTcMaxTopk = 16;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 // fp16-V path: P' = P * 2^(e_b - E) in fp16. P <= 2^8 under the lazy rescale, so e_b - E <= 7 keeps
@@ -72,17 +75,25 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 // that window E moves to e_b and O is rescaled by the power of two.
 constexpr int kExpUp = 7, kExpDown = -8;
 
-// One tile, described by the scheduler warp for the other roles (two slots, used alternately).
+// One descriptor, written by the scheduler warp for the other roles (two slots, used
+// alternately): a tile's tokens and up to kMaxUnion entries of its sorted union of selected
+// blocks. A tile whose union is longer continues in the next descriptor (`more` here, `cont`
+// there): same tokens, O and the softmax state carry on, Q stays loaded.
 struct TileDesc {
   int32_t end;  // no tile: the CTA's list is done
   int32_t req, g, t0, n_tok, c0, ctx0, pos_last;  // request, kv head, first token row, tokens, ...
-  int32_t n_union;
-  int32_t bad_mask;                  // tokens whose row hit an out-of-range block id
-  int16_t own[kTokMax];              // own block of each token (-1: none)
+  int32_t n_union;                   // entries in this descriptor
+  int32_t bad_mask;                  // tokens whose row could not be read (the row attends nothing)
+  int32_t cont;                      // continues the previous descriptor's tile
+  int32_t more;                      // the tile continues in the next descriptor
+  int32_t by_block;                  // masks are indexed by block id (all of the tile's blocks < 128)
+  int32_t own[kTokMax];              // own block of each token (-1: none)
   int16_t lim[kTokMax];              // keys of the own block the token sees
-  uint16_t union_blk[kMaxUnion];      // the tile's distinct valid blocks, increasing
-  uint32_t blocks[kTokMax][kSetWords];  // bit b: the token selected block b (valid and causal)
-  int8_t vexp[kMaxUnion];             // fp16-V path: union block u's V image is V * 2^-vexp[u]
+  uint16_t union_blk[kMaxUnion];     // the entries' blocks, increasing
+  // bit x of masks[t]: token t selected the block of entry x of this descriptor (by_block 0) or
+  // block x (by_block 1)
+  uint32_t masks[kTokMax][kMaxUnion / 32];
+  int8_t vexp[kMaxUnion];            // fp16-V path: the entry's V image is V * 2^-vexp
 };
 
 // Roles that read a tile slot and release it: the two TMA warps, the MMA thread, the softmax warps.
@@ -369,11 +380,216 @@ __global__ void __launch_bounds__(128) convert_v_kernel(const AttendArgs a) {
   if (t == 0) a.vconv_exp[(static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g] = e;
 }
 
-// Scheduler warp: describes tile f of the CTA's list in slot d. Flat tile f is kv head f % Hkv of
-// request tile (tiles - 1 - f / Hkv), request tiles numbered request by request: the list starts
-// at the last request's last tiles, whose tokens see the most blocks.
+// fp8 / NVFP4 caches, before the attend: K and V of block b of request r and kv head g (CTA
+// (b, r, g)) as the images the tile kernel's stages hold, K as bf16 (an e4m3 value, or an e2m1
+// code times its e4m3 block scale, has at most 6 significant bits and fits bf16's range: exact)
+// and V as fp16 times 2^-e like convert_v_kernel (exact: the values fit fp16's normal range once
+// the block's maximum sits at 2^14..2^15). The per-tensor scales stay folded as for bf16. Keys
+// past the request's last token, or on pages past the cache, become zeros. Thread t converts key
+// t, 8 elements (one 16-byte image chunk) at a time.
+// The lower / upper half of an f16x2 word as float (exact).
+__device__ __forceinline__ float f16x2_lo(uint32_t x) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(x));
+  return f;
+}
+__device__ __forceinline__ float f16x2_hi(uint32_t x) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}" : "=f"(f) : "r"(x));
+  return f;
+}
+
+// Elements 8c .. 8c + 7 of one side (K or V) of a key, dequantised to float (exact).
+template <int FMT>
+__device__ __forceinline__ void dequant8(const uint8_t* side, int row, int c, float (&v)[8]) {
+  if (FMT == PBS_KV_FP8_E4M3) {
+    const uint2 w = *reinterpret_cast<const uint2*>(side + 8 * c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t h2 = e4m3x2_to_f16x2(((i < 2 ? w.x : w.y) >> (16 * (i & 1))) & 0xffffu);
+      v[2 * i] = f16x2_lo(h2);
+      v[2 * i + 1] = f16x2_hi(h2);
+    }
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(side + row * 64 + 4 * c);
+    // scale j covers elements 16j .. 16j + 15, so chunk c uses scale c / 2
+    const float sc = f16x2_lo(e4m3x2_to_f16x2(side[1024 + row * 8 + c / 2]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t h2 = e2m1x2_to_f16x2((w >> (8 * i)) & 0xffu);
+      v[2 * i] = f16x2_lo(h2) * sc;
+      v[2 * i + 1] = f16x2_hi(h2) * sc;
+    }
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(128) convert_kv_kernel(const AttendArgs a) {
+  const int b = blockIdx.x, r = blockIdx.y, g = blockIdx.z, t = threadIdx.x;
+  const int seq_len = __ldg(a.seq_lens + r);
+  if (b * kSparseBlock >= seq_len) return;  // no token of the request sees this block
+  const int nv = min(kSparseBlock, seq_len - b * kSparseBlock);
+  const int64_t page = static_cast<int64_t>(__ldg(a.page_table + static_cast<int64_t>(r) * a.pt_row_stride + b)) *
+                           a.block_page_stride + t / kPageRows;
+  const bool in_cache = page >= 0 && page < a.num_pages;
+  if (t < nv && !in_cache) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+  const bool live = t < nv && in_cache;
+  const int row = t % kPageRows;
+  const uint8_t* base = a.kv_cache + (live ? page : 0) * a.page_stride_bytes;
+  // fp8: [Hkv][16 rows][K 128 B | V 128 B]; NVFP4: [2 Hkv slots of 1152 B], slot 2g = K, 2g + 1 = V
+  const uint8_t* kside = FMT == PBS_KV_FP8_E4M3 ? base + g * 4096 + row * 256 : base + (2 * g) * 1152;
+  const uint8_t* vside = FMT == PBS_KV_FP8_E4M3 ? kside + 128 : kside + 1152;
+  const int64_t image = (static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g;
+  // K: bf16 image
+  uint8_t* kdst = a.kconv + image * kTileBytes;
+#pragma unroll 4
+  for (int c = 0; c < 16; ++c) {
+    float v[8];
+    if (live) dequant8<FMT>(kside, row, c, v);
+    else
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    const int q = c >> 3, c8 = c & 7;
+    *reinterpret_cast<uint4*>(kdst + q * kHalf + t * 128 + ((c8 ^ (t & 7)) << 4)) =
+        make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+  }
+  // V: the block's maximum |V|, then fp16 V * 2^-e
+  float mx = 0.f;
+  for (int c = 0; c < 16; ++c) {
+    float v[8];
+    if (live) {
+      dequant8<FMT>(vside, row, c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    }
+  }
+  __shared__ float wmax[4];
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  if ((t & 31) == 0) wmax[t >> 5] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  int e = 0;
+  if (mx > 0.f) e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127 - 14;
+  e = max(-100, min(100, e));
+  const float sc = exp2i(-e);
+  uint8_t* vdst = a.vconv + image * kTileBytes;
+#pragma unroll 4
+  for (int c = 0; c < 16; ++c) {
+    float v[8];
+    if (live) dequant8<FMT>(vside, row, c, v);
+    else
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    const int q = c >> 3, c8 = c & 7;
+    *reinterpret_cast<uint4*>(vdst + q * kHalf + t * 128 + ((c8 ^ (t & 7)) << 4)) =
+        make_uint4(pack_f16(v[0] * sc, v[1] * sc), pack_f16(v[2] * sc, v[3] * sc), pack_f16(v[4] * sc, v[5] * sc),
+                   pack_f16(v[6] * sc, v[7] * sc));
+  }
+  if (t == 0) a.vconv_exp[image] = e;
+}
+
+// ---- the scheduler warp's tile union --------------------------------------------------------
+// A tile's (token, selected block) pairs as 256 keys block << 16 | 1 << token, held 8 per lane
+// (element e = 32 r + lane), sorted by a bitonic network; runs of one block are then ORed into
+// their first element (the run's head), which also gets the block's index in the tile's union.
+constexpr uint32_t kNoKey = 0xffffffffu;
+
+// Compare-exchange of elements (r, lane) and (r ^ RJ, lane) of one lane (a stage of distance
+// 32 RJ), ascending where bit k of the element index is clear.
+template <int RJ>
+__device__ __forceinline__ void bitonic_in_lane(uint32_t (&key)[8], int lane, int k) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    if (r & RJ) continue;
+    const bool up = ((32 * r + lane) & k) == 0;
+    const uint32_t x = key[r], y = key[r | RJ];
+    const bool sw = up ? (x > y) : (x < y);
+    key[r] = sw ? y : x;
+    key[r | RJ] = sw ? x : y;
+  }
+}
+
+// Bitonic sort of the 256 keys, ascending (element e = 32 r + lane). The stages run as loops, so
+// the scheduler's code stays small next to the pipeline's hot loops.
+__device__ __forceinline__ void sort_keys(uint32_t (&key)[8], int lane) {
+#pragma unroll 1
+  for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        if (j == 32) bitonic_in_lane<1>(key, lane, k);
+        else if (j == 64) bitonic_in_lane<2>(key, lane, k);
+        else bitonic_in_lane<4>(key, lane, k);
+      } else {
+        const bool lower = (lane & j) == 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const bool up = ((32 * r + lane) & k) == 0;
+          const uint32_t other = __shfl_xor_sync(0xffffffffu, key[r], j);
+          key[r] = (lower == up) ? min(key[r], other) : max(key[r], other);
+        }
+      }
+    }
+  }
+}
+
+// acc[e] |= acc[e + d] for every element whose element e + d holds the same block (sorted keys:
+// then so does every element between them); after d = 1, 2, ..., 128 each element holds the OR of
+// its run's tail.
+template <int RD>
+__device__ __forceinline__ void run_or_in_lane(const uint32_t (&key)[8], uint32_t (&acc)[8]) {
+#pragma unroll
+  for (int r = 0; r < 8 - RD; ++r) {
+    // ascending r: acc[r + RD] is still the value before this step
+    const bool same = key[r] != kNoKey && key[r + RD] != kNoKey && (key[r + RD] >> 16) == (key[r] >> 16);
+    acc[r] |= same ? acc[r + RD] : 0u;
+  }
+}
+
+__device__ __forceinline__ void run_or(const uint32_t (&key)[8], uint32_t (&acc)[8], int lane) {
+#pragma unroll 1
+  for (int d = 1; d < 32; d <<= 1) {
+    const int src = (lane + d) & 31;
+    const bool same_reg = lane + d < 32;
+    uint32_t nacc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const uint32_t k0 = __shfl_sync(0xffffffffu, key[r], src), a0 = __shfl_sync(0xffffffffu, acc[r], src);
+      const uint32_t k1 = __shfl_sync(0xffffffffu, key[(r + 1) & 7], src);
+      const uint32_t a1 = __shfl_sync(0xffffffffu, acc[(r + 1) & 7], src);
+      const uint32_t ok_key = same_reg ? k0 : (r + 1 < 8 ? k1 : kNoKey);
+      const uint32_t ok_acc = same_reg ? a0 : a1;
+      const bool same = key[r] != kNoKey && ok_key != kNoKey && (ok_key >> 16) == (key[r] >> 16);
+      nacc[r] = acc[r] | (same ? ok_acc : 0u);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = nacc[r];
+  }
+  run_or_in_lane<1>(key, acc);
+  run_or_in_lane<2>(key, acc);
+  run_or_in_lane<4>(key, acc);
+}
+
+struct TileUnion {
+  uint32_t key[8];  // sorted keys; at a head, the low 16 bits hold the OR of the run's token bits
+  int32_t u[8];     // union index of a head element
+  uint32_t heads;   // bit r: element (r, lane) heads its block's run
+  int32_t n;        // distinct blocks of the tile
+  bool direct;      // the tile's only descriptor is already written (blocks below 128: masks)
+};
+
+// The tile's request and tokens (flat tile f of the CTA's list: kv head f % Hkv of request tile
+// tiles - 1 - f / Hkv, request tiles numbered request by request, so the list starts at the
+// last request's last tiles, whose tokens see the most blocks), each token's own block and
+// visible keys of it, and the sorted union of the tokens' selections. Lane t < kTok owns token
+// t's row; the rest of the warp helps with the loads, the sort and the scans.
 template <int kTok, bool kF16V>
-__device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int total_tiles, TileDesc* d, int lane) {
+__device__ __forceinline__ void build_tile(const AttendArgs& a, int f, int total_tiles, int lane, TileDesc* d,
+                                           TileUnion& un) {
   const int g = f % a.num_kv_heads;
   const int rt = total_tiles - 1 - f / a.num_kv_heads;
   int r = -1, t0 = 0, n = 0, c0 = 0, ctx0 = 0, seq_len = 0;
@@ -409,18 +625,14 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
     }
     base_tiles += __shfl_sync(0xffffffffu, incl, 31);
   }
-  // lane tt: token tt's distinct valid blocks as a 128-bit set (a repeated id sets the same bit:
-  // each selected block counts once), its own block and the keys of it the token sees
-  uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;
+  if (r < 0) n = 0;
+  // lane t < n: token t's selected blocks (ids[j], -1 where none), its own block and the keys of
+  // it the token sees
+  int ids[kTcMaxTopk];
   int own = -1, lim = 0;
   bool bad = false;
-  auto add_block = [&](int b) {
-    const uint32_t bit = 1u << (b & 31);
-    m0 |= (b >> 5) == 0 ? bit : 0u;
-    m1 |= (b >> 5) == 1 ? bit : 0u;
-    m2 |= (b >> 5) == 2 ? bit : 0u;
-    m3 |= (b >> 5) == 3 ? bit : 0u;
-  };
+#pragma unroll
+  for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = -1;
   if (a.sparse_bt == nullptr) {
     if (lane < n) {
       const int pos = ctx0 + (t0 + lane - c0);
@@ -428,29 +640,23 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
       own = causal_len > 0 ? pos / kSparseBlock : -1;
       lim = own >= 0 ? causal_len - own * kSparseBlock : 0;
       const int32_t* row = a.topk + static_cast<int64_t>(t0 + lane) * a.topk_row_stride;
-      int ids[kTcMaxTopk];
-#pragma unroll
-      for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = j < a.k ? __ldg(row + j) : -1;
 #pragma unroll
       for (int j = 0; j < kTcMaxTopk; ++j) {
-        const int b = ids[j];
+        const int b = j < a.k ? __ldg(row + j) : -1;
         if (b >= 0 && b <= own) {
           if (b >= a.max_blocks) bad = true;
-          else add_block(b);
+          else ids[j] = b;  // a repeated id gives the same key twice: the run OR merges it
         }
       }
       // a row with an out-of-range id contributes nothing (its output is zero, the error recorded)
-      if (bad) {
-        set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
-        m0 = m1 = m2 = m3 = 0u;
-      }
+      if (bad) set_err(a.err_word, PBS_DEVERR_BLOCK_OOB);
     }
   } else {
     // Prebuilt table: slot j of the token's row lists the pages of one block; the block is found
     // by walking the request's page-table row (a slot's first page is page_table[r][b] *
     // block_page_stride). Keys of slot j: min(128, ctx - 128 j), so only the last slot can be
     // partial; it plays the own block's part (lim keys).
-    int first[kTcMaxTopk], blk[kTcMaxTopk];
+    int first[kTcMaxTopk];
     int n_slots = 0, tctx = 0;
     if (lane < n) {
       tctx = __ldg(a.sparse_ctx + t0 + lane);
@@ -462,10 +668,7 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
     }
     const int32_t* trow = a.sparse_bt + static_cast<int64_t>(t0 + min(lane, max(n - 1, 0))) * a.sbt_row_stride;
 #pragma unroll
-    for (int j = 0; j < kTcMaxTopk; ++j) {
-      first[j] = j < n_slots ? __ldg(trow + j * kPagesPerBlock) : -1;
-      blk[j] = -1;
-    }
+    for (int j = 0; j < kTcMaxTopk; ++j) first[j] = j < n_slots ? __ldg(trow + j * kPagesPerBlock) : -1;
     // the last block any of the tile's tokens can see bounds the walk
     const int pos_max = ctx0 + (t0 + max(n, 1) - 1 - c0);
     const int walk = min(a.max_blocks, pos_max >= 0 ? pos_max / kSparseBlock + 1 : 0);
@@ -478,75 +681,204 @@ __device__ __forceinline__ void describe_tile(const AttendArgs& a, int f, int to
       for (int j = 0; j < nj; ++j) {
         const int x = __shfl_sync(0xffffffffu, base, j);
 #pragma unroll
-        for (int s = 0; s < kTcMaxTopk; ++s)
-          if (blk[s] < 0 && first[s] == x) blk[s] = b0 + j;
+        for (int sl = 0; sl < kTcMaxTopk; ++sl)
+          if (ids[sl] < 0 && first[sl] == x) ids[sl] = b0 + j;
       }
     }
     if (lane < n && !bad) {
+      uint32_t seen[4] = {0u, 0u, 0u, 0u};  // blocks of this row so far, hashed to 128 bits
 #pragma unroll
-      for (int s = 0; s < kTcMaxTopk; ++s) {
-        if (s < n_slots) {
-          // a slot that names no block of the request, or a block in two slots (no table the
-          // builders write: a row is a set of blocks), makes the row unreadable
-          const int b = blk[s];
-          const int w = (b >> 5) & 3;
-          const uint32_t word = w == 0 ? m0 : w == 1 ? m1 : w == 2 ? m2 : m3;
-          bad |= b < 0 || ((word >> (b & 31)) & 1u) != 0;
-          if (b >= 0) add_block(b);
-          if (s == n_slots - 1) {
-            own = b;
-            lim = tctx - s * kSparseBlock;
+      for (int sl = 0; sl < kTcMaxTopk; ++sl) {
+        if (sl < n_slots) {
+          // a slot that names no block of the request makes the row unreadable
+          const int b = ids[sl];
+          bad |= b < 0;
+          if (b >= 0) {
+            // a block in two slots is no table the builders write (a row is a set of blocks)
+            const uint32_t bit = 1u << (b & 31);
+            const int w = (b >> 5) & 3;
+            for (int sl2 = 0; sl2 < sl; ++sl2) bad |= ids[sl2] == b && (seen[w] & bit) != 0;
+            seen[w] |= bit;
           }
+          if (sl == n_slots - 1) {
+            own = b;
+            lim = tctx - sl * kSparseBlock;
+          }
+        } else {
+          ids[sl] = -1;
         }
       }
       // every page a slot's keys reach must be the block's own page (the kernel copies the block)
-      for (int s = 0; s < n_slots && !bad; ++s) {
-        const int f = __ldg(trow + s * kPagesPerBlock);
-        const int keys = min(kSparseBlock, tctx - s * kSparseBlock);
-        for (int j = 1; j < (keys + kPageRows - 1) / kPageRows; ++j) bad |= __ldg(trow + s * kPagesPerBlock + j) != f + j;
+      for (int sl = 0; sl < n_slots && !bad; ++sl) {
+        const int fp = __ldg(trow + sl * kPagesPerBlock);
+        const int keys = min(kSparseBlock, tctx - sl * kSparseBlock);
+        for (int j = 1; j < (keys + kPageRows - 1) / kPageRows; ++j) bad |= __ldg(trow + sl * kPagesPerBlock + j) != fp + j;
       }
-      if (bad) {
-        set_err(a.err_word, PBS_DEVERR_TABLE);
-        m0 = m1 = m2 = m3 = 0u;
-      }
-    } else if (lane < n && bad) {
-      set_err(a.err_word, PBS_DEVERR_TABLE);
     }
-  }
-  const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad);
-  if (lane < kTok) {
-    d->own[lane] = static_cast<int16_t>(min(own, 32767));
-    d->lim[lane] = static_cast<int16_t>(lim);
-    d->blocks[lane][0] = m0;
-    d->blocks[lane][1] = m1;
-    d->blocks[lane][2] = m2;
-    d->blocks[lane][3] = m3;
-  }
-  // union = set bits in increasing order
-  int nu = 0;
+    if (lane >= n) {
 #pragma unroll
-  for (int w = 0; w < kSetWords; ++w) {
-    const uint32_t word = __reduce_or_sync(0xffffffffu, w == 0 ? m0 : w == 1 ? m1 : w == 2 ? m2 : m3);
-    if ((word >> lane) & 1u) {
-      const int u = nu + __popc(word & ((1u << lane) - 1u)), b = 32 * w + lane;
-      d->union_blk[u] = static_cast<uint16_t>(b);
-      if (kF16V)
-        d->vexp[u] = static_cast<int8_t>(
-            __ldg(a.vconv_exp + (static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g));
+      for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = -1;
     }
-    nu += __popc(word);
+    if (lane < n && bad) set_err(a.err_word, PBS_DEVERR_TABLE);
+  }
+  if (bad) {
+#pragma unroll
+    for (int j = 0; j < kTcMaxTopk; ++j) ids[j] = -1;
+  }
+  const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad && lane < n);
+  // the last block any token of the tile can see
+  const int pos_max = ctx0 + (t0 + max(n, 1) - 1 - c0);
+  const int own_max = pos_max >= 0 ? pos_max / kSparseBlock : -1;
+  un.heads = 0u;
+  const uint32_t lt = lanemask_lt();
+  un.direct = false;
+  if (own_max < 128) {
+    // every selected block is below 128: each token's blocks as a 128-bit set (a repeated id sets
+    // the same bit) that the softmax warps test per block, and the union, the OR of the sets,
+    // listed in increasing order straight into the tile's only descriptor
+    uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;
+#pragma unroll
+    for (int j = 0; j < kTcMaxTopk; ++j) {
+      const int b = ids[j];
+      if (b >= 0) {
+        const uint32_t bit = 1u << (b & 31);
+        m0 |= (b >> 5) == 0 ? bit : 0u;
+        m1 |= (b >> 5) == 1 ? bit : 0u;
+        m2 |= (b >> 5) == 2 ? bit : 0u;
+        m3 |= (b >> 5) == 3 ? bit : 0u;
+      }
+    }
+    if (lane < kTok) {
+      d->masks[lane][0] = m0;
+      d->masks[lane][1] = m1;
+      d->masks[lane][2] = m2;
+      d->masks[lane][3] = m3;
+    }
+    int nu = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t word = __reduce_or_sync(0xffffffffu, w == 0 ? m0 : w == 1 ? m1 : w == 2 ? m2 : m3);
+      if ((word >> lane) & 1u) {
+        const int u = nu + __popc(word & lt), b = 32 * w + lane;
+        d->union_blk[u] = static_cast<uint16_t>(b);
+        if (kF16V)
+          d->vexp[u] = static_cast<int8_t>(
+              __ldg(a.vconv_exp + (static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g));
+      }
+      nu += __popc(word);
+    }
+    un.n = nu;
+    un.direct = true;
+  } else {
+    // keys: lane l holds token l % kTok's ids j = l / kTok + (32 / kTok) r; sorted, then each run
+    // of one block ORed into its head
+    constexpr int kLpt = 32 / kTok;
+    const int tl = lane % kTok;
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) un.key[rr] = kNoKey;
+#pragma unroll
+    for (int j = 0; j < kTcMaxTopk; ++j) {
+      const int v = __shfl_sync(0xffffffffu, ids[j], tl);
+      if (j % kLpt == lane / kTok && j / kLpt < 8)
+        un.key[j / kLpt] = v >= 0 ? (static_cast<uint32_t>(v) << 16) | (1u << tl) : kNoKey;
+    }
+    sort_keys(un.key, lane);
+    uint32_t acc[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) acc[rr] = un.key[rr] & 0xffffu;
+    run_or(un.key, acc, lane);
+    // heads (the first element of each block's run) and their union indices
+    int before = 0;
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const uint32_t up = __shfl_up_sync(0xffffffffu, un.key[rr], 1);
+      const uint32_t prev_last = __shfl_sync(0xffffffffu, un.key[(rr + 7) & 7], 31);
+      const uint32_t prev = lane > 0 ? up : (rr > 0 ? prev_last : kNoKey);
+      const bool head = un.key[rr] != kNoKey && (prev == kNoKey || (prev >> 16) != (un.key[rr] >> 16));
+      const uint32_t hb = __ballot_sync(0xffffffffu, head);
+      un.u[rr] = before + __popc(hb & lt);
+      before += __popc(hb);
+      if (head) {
+        un.heads |= 1u << rr;
+        un.key[rr] = (un.key[rr] & 0xffff0000u) | (acc[rr] & 0xffffu);
+      }
+    }
+    un.n = before;
+  }
+  // the descriptor fields every part of the tile shares
+  if (lane < kTok) {
+    d->own[lane] = own;
+    d->lim[lane] = static_cast<int16_t>(lim);
   }
   if (lane == 0) {
     d->end = 0;
     d->req = r;
     d->g = g;
     d->t0 = t0;
-    d->n_tok = r < 0 ? 0 : n;
+    d->n_tok = n;
     d->c0 = c0;
     d->ctx0 = ctx0;
     d->pos_last = seq_len - 1;
-    d->n_union = r < 0 ? 0 : nu;
     d->bad_mask = static_cast<int32_t>(bad_mask);
+  }
+}
+
+// Part `part` of a tile's union (entries kMaxUnion * part ..) into descriptor d; copies the shared
+// fields from the tile's first descriptor `d0` when the part is a continuation.
+template <bool kF16V>
+__device__ __forceinline__ void write_tile_part(const AttendArgs& a, const TileUnion& un, int part, TileDesc* d,
+                                                const TileDesc* d0, int lane) {
+  const int u0 = part * kMaxUnion;
+  const int nu = min(kMaxUnion, max(un.n - u0, 0));
+  if (un.direct) {  // the block-mask path wrote the tile's only descriptor
+    if (lane == 0) {
+      d->n_union = d->req < 0 ? 0 : nu;
+      d->cont = 0;
+      d->more = 0;
+      d->by_block = 1;
+    }
+    return;
+  }
+  // token masks over this part's entries: cleared, then each head ORs in its tokens' bits
+  for (int i = lane; i < kTokMax * (kMaxUnion / 32); i += 32) (&d->masks[0][0])[i] = 0u;
+  __syncwarp();
+  if (part > 0) {
+    // the tile's shared fields, from the descriptor its first part went to
+    if (lane < kTokMax) {
+      d->own[lane] = d0->own[lane];
+      d->lim[lane] = d0->lim[lane];
+    }
+    if (lane == 0) {
+      d->end = 0;
+      d->req = d0->req;
+      d->g = d0->g;
+      d->t0 = d0->t0;
+      d->n_tok = d0->n_tok;
+      d->c0 = d0->c0;
+      d->ctx0 = d0->ctx0;
+      d->pos_last = d0->pos_last;
+      d->bad_mask = d0->bad_mask;
+    }
+  }
+  const int req = part > 0 ? d0->req : d->req, g = part > 0 ? d0->g : d->g;
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int u = un.u[rr] - u0;
+    if (((un.heads >> rr) & 1u) && u >= 0 && u < kMaxUnion) {
+      const int b = static_cast<int>(un.key[rr] >> 16);
+      d->union_blk[u] = static_cast<uint16_t>(b);
+      for (uint32_t toks = un.key[rr] & 0xffffu; toks != 0u; toks &= toks - 1u)
+        atomicOr(&d->masks[__ffs(toks) - 1][u >> 5], 1u << (u & 31));
+      if (kF16V)
+        d->vexp[u] = static_cast<int8_t>(
+            __ldg(a.vconv_exp + (static_cast<int64_t>(req) * a.max_blocks + b) * a.num_kv_heads + g));
+    }
+  }
+  if (lane == 0) {
+    d->n_union = req < 0 ? 0 : nu;
+    d->cont = part > 0;
+    d->more = u0 + kMaxUnion < un.n;
+    d->by_block = 0;
   }
 }
 
@@ -613,38 +945,64 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       total += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>((q_len + kTok - 1) / kTok));
     }
     const int flat = total * a.num_kv_heads;
-    for (int k = 0;; ++k) {
-      // round k of the list: its gridDim.x tiles dealt in alternating directions, so a CTA that
+    int k = 0;   // descriptors written (slot k & 1)
+    int nq = 0;  // Q tiles loaded
+    bool done = false;
+    for (int kt = 0; !done; ++kt) {
+      // round kt of the list: its gridDim.x tiles dealt in alternating directions, so a CTA that
       // took a longer tile of one round takes a shorter one of the next (costs fall along the list)
-      const int f = k * static_cast<int>(gridDim.x) +
-                    ((k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
-      const int sl = k & 1;
-      TileDesc* d = &ctl->tile[sl];
-      // the slot's previous tile (k - 2) has been released by every role
-      bool go = true;
-      if (lane == 0 && k >= 2) go = wait_or_abort(&ctl->tile_empty[sl], ((k >> 1) - 1) & 1, ctl, a.err_word);
-      go = __shfl_sync(0xffffffffu, go, 0);
-      // once any CTA has given up on a wait, the rest of the grid does no work
-      if (lane == 0)
-        go = go && !aborted(ctl) &&
-             !(a.err_word != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err_word) & PBS_DEVERR_TIMEOUT) != 0);
-      go = __shfl_sync(0xffffffffu, go, 0);
-      const bool last = !go || f >= flat;
-      if (lane == 0) TRACET(kEvDesc0, k);
-      if (!last) describe_tile<kTok, kF16V>(a, f, total, d, lane);
-      if (lane == 0 && last) d->end = 1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->tile_full[sl]);
-      if (lane == 0) TRACET(kEvDesc, k);
-      if (last) break;
-      // the tile's Q, once the previous tile's S MMAs have read theirs
-      if (lane == 0 && (k == 0 || wait_or_abort(&ctl->q_empty, (k - 1) & 1, ctl, a.err_word))) {
-        mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
-        tma_load_3d(q_s, &q_map, &ctl->q_full, 0, d->g * kG, d->t0);
-        tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, d->g * kG, d->t0);
-        TRACET(kEvQ, k);
+      const int f = kt * static_cast<int>(gridDim.x) +
+                    ((kt & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                              : static_cast<int>(blockIdx.x));
+      TileUnion un;
+      un.n = 0;
+      TileDesc* d0 = nullptr;
+      for (int part = 0;; ++part, ++k) {
+        const int sl = k & 1;
+        TileDesc* d = &ctl->tile[sl];
+        // the slot's previous descriptor (k - 2) has been released by every role
+        bool go = true;
+        if (lane == 0 && k >= 2) go = wait_or_abort(&ctl->tile_empty[sl], ((k >> 1) - 1) & 1, ctl, a.err_word);
+        go = __shfl_sync(0xffffffffu, go, 0);
+        // once any CTA has given up on a wait, the rest of the grid does no work
+        if (lane == 0)
+          go = go && !aborted(ctl) &&
+               !(a.err_word != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err_word) & PBS_DEVERR_TIMEOUT) != 0);
+        go = __shfl_sync(0xffffffffu, go, 0);
+        const bool last = !go || f >= flat;
+        if (lane == 0) TRACET(kEvDesc0, k);
+        if (!last) {
+          if (part == 0) {
+            build_tile<kTok, kF16V>(a, f, total, lane, d, un);
+            d0 = d;
+          }
+          __syncwarp();
+          write_tile_part<kF16V>(a, un, part, d, d0, lane);
+        }
+        if (lane == 0 && last) d->end = 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tile_full[sl]);
+        if (lane == 0) TRACET(kEvDesc, k);
+        if (last) {
+          done = true;
+          break;
+        }
+        if (part == 0) {
+          // the tile's Q, once the previous tile's S MMAs have read theirs
+          if (lane == 0 && (nq == 0 || wait_or_abort(&ctl->q_empty, (nq - 1) & 1, ctl, a.err_word))) {
+            mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+            tma_load_3d(q_s, &q_map, &ctl->q_full, 0, d->g * kG, d->t0);
+            tma_load_3d(q_s + kHalf, &q_map, &ctl->q_full, 64, d->g * kG, d->t0);
+            TRACET(kEvQ, kt);
+          }
+          ++nq;
+          __syncwarp();
+        }
+        if ((part + 1) * kMaxUnion >= un.n) {
+          ++k;
+          break;
+        }
       }
-      __syncwarp();
     }
   } else if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------------ TMA producers
@@ -652,8 +1010,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // (quarter coordinate 0 for K, 2 for V, from the block's first page; on the fp16-V path V is
     // the block's converted image, one bulk copy).
     const bool is_k = warp == 0;
+    // K from the cache through the block map (bf16 caches), or from its converted bf16 image
+    const bool k_image = a.kconv != nullptr;
     if (is_k && lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
+      if (!k_image) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
     }
     uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
@@ -674,23 +1034,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       int phys_lane = 0;
       for (int i = 0; go && i < nU; ++i, ++gb) {
         const int st = gb % kStagesTc;
-        if ((i & 31) == 0) phys_lane = i + lane < nU ? __ldg(bt_row + d->union_blk[i + lane]) : 0;
+        if ((i & 31) == 0) phys_lane = i + lane < nU && !(k_image && is_k) && !(kF16V && !is_k)
+                                         ? __ldg(bt_row + d->union_blk[i + lane]) : 0;
         const int phys = __shfl_sync(0xffffffffu, phys_lane, i & 31);
         if (lane == 0 && gb >= kStagesTc) go = wait_or_abort(&empty[st], ((gb / kStagesTc) - 1) & 1, ctl, a.err_word);
         if (lane == 0) go = go && !aborted(ctl);
         go = __shfl_sync(0xffffffffu, go, 0);
         if (!go) break;
         const int64_t base = static_cast<int64_t>(phys) * a.block_page_stride;
-        if (is_k && lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages))
+        // (with converted images the conversion kernel checked the pages)
+        if (is_k && !k_image && lane == 0 && (base < 0 || base + (kPagesPerBlock - 1) >= a.num_pages))
           set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
         if (is_k) TRACEB(kEvProdIssue0, gb);
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[st], kTileBytes);
+          const int64_t image = (static_cast<int64_t>(d->req) * a.max_blocks + d->union_blk[i]) * a.num_kv_heads + g;
           if (kF16V && !is_k)
-            bulk_load(ring + st * kTileBytes,
-                      a.vconv + ((static_cast<int64_t>(d->req) * a.max_blocks + d->union_blk[i]) * a.num_kv_heads + g) *
-                                    kTileBytes,
-                      kTileBytes, &full[st]);
+            bulk_load(ring + st * kTileBytes, a.vconv + image * kTileBytes, kTileBytes, &full[st]);
+          else if (is_k && k_image)
+            bulk_load(ring + st * kTileBytes, a.kconv + image * kTileBytes, kTileBytes, &full[st]);
           else  // out-of-range pages read as zeros (TMA bounds)
             tma_load_5d(ring + st * kTileBytes, &kv_map, &full[st], 0, 0, g, static_cast<int>(base), quarter);
         }
@@ -740,11 +1102,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc::commit(&ctl->v_empty[st]);
         return true;
       };
+      int nq = 0;  // Q tiles consumed
       for (int k = 0; ok; ++k) {
         const int sl = k & 1;
-        // The previous tile's last PVs go first, before waiting for this tile's description: its
-        // epilogue, on the softmax warps' path, waits for them (and the description of tile k
-        // waits for tile k - 2's epilogue), while this tile's first S runs during that epilogue.
+        // The previous descriptor's last PVs go first, before waiting for this one: a tile's
+        // epilogue, on the softmax warps' path, waits for them (and descriptor k waits for
+        // descriptor k - 2's release), while this descriptor's first S runs during that epilogue.
         while (ok && gp < gs) {
           if (!issue_pv(gp)) ok = false;
           ++gp;
@@ -753,7 +1116,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const TileDesc* d = &ctl->tile[sl];
         if (d->end) break;
         const int nU = d->n_union;
-        if (!wait_or_abort(&ctl->q_full, k & 1, ctl, a.err_word)) break;
+        const bool cont = d->cont != 0, more = d->more != 0;
+        // a continuation uses the Q its tile's first descriptor loaded
+        if (!cont) {
+          if (!wait_or_abort(&ctl->q_full, nq & 1, ctl, a.err_word)) break;
+          ++nq;
+        }
         tc::fence_after_sync();
         // issue order S(0), S(1), S(2), PV(0), S(3), PV(1), ... over the CTA's block sequence: S
         // runs two blocks ahead of PV, so the softmax of block i + 1 finds S(i + 1) done while
@@ -779,7 +1147,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc::commit(&ctl->s_full[sb]);
           tc::commit(&ctl->k_empty[st]);  // the K stage is free once S(i) has read it
           TRACEB(kEvS, gs);
-          first = i == 0 ? (first | (1u << (gs & 31))) : (first & ~(1u << (gs & 31)));
+          first = (i == 0 && !cont) ? (first | (1u << (gs & 31))) : (first & ~(1u << (gs & 31)));
           if (gs - gp >= 2) {
             if (!issue_pv(gp)) {
               ok = false;
@@ -788,8 +1156,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             ++gp;
           }
         }
-        // the tile's Q is free once its S MMAs have completed
-        tc::commit(&ctl->q_empty);
+        // the tile's Q is free once the S MMAs of its last descriptor have completed
+        if (!more) tc::commit(&ctl->q_empty);
         mbar_arrive(&ctl->tile_empty[sl]);
       }
       while (ok && gp < gs) {
@@ -811,6 +1179,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = a.scale_log2;
     int gb = 0;  // blocks of the CTA's sequence this warp has processed
+    // a tile's softmax state, kept across its descriptors
+    float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
+    bool started = false;              // the row has had an active block (same in every part)
+    int E = 0;                         // fp16-V path: O holds sum(P V) * 2^-E (set by the first block)
+    bool ok = true;
     for (int k = 0;; ++k) {
       const int sl = k & 1;
       const bool got = warp_wait_or_abort(&ctl->tile_full[sl], (k >> 1) & 1, ctl, a.err_word);
@@ -818,22 +1191,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // both warps of the quadrant leave together (they meet at named barriers below)
       if (quad_any(quad, !got || d->end != 0 || aborted(ctl))) break;
       const int nU = d->n_union, n_tok = d->n_tok, t0 = d->t0, g = d->g;
+      const bool cont = d->cont != 0, more = d->more != 0, by_block = d->by_block != 0;
       if (sw == 0 && lane == 0) TRACET(kEvTileIn, k);
       const bool live = tt < n_tok && !((d->bad_mask >> tt) & 1);
       const int own_t = d->own[tt], lim_t = d->lim[tt];
       const int pos_last = d->pos_last;
       const int last_blk = pos_last / kSparseBlock;
       const int last_rows = pos_last - last_blk * kSparseBlock + 1;  // valid rows of the request's last block
-      float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
-      bool started = false;              // the row has had an active block (same in every part)
-      int E = 0;                         // fp16-V path: O holds sum(P V) * 2^-E (set by the first block)
-      bool ok = true;
+      // a continuation descriptor carries on the tile's softmax state and O
+      if (!cont) {
+        m_ref = -INFINITY;
+        l = 0.f;
+        started = false;
+        E = 0;
+        ok = true;
+      }
       // A wait that gives up clears `ok`; the warp then stops waiting but keeps stepping through
       // the blocks, so the two warps of a quadrant always meet at the same named barriers.
       for (int i = 0; i < nU; ++i, ++gb) {
         const int sb = gb % kSBuf, st = gb % kStagesTc;
         const int b = d->union_blk[i];
-        const bool active = live && ((d->blocks[tt][b >> 5] >> (b & 31)) & 1u);
+        const int x = by_block ? b : i;
+        const bool active = live && ((d->masks[tt][x >> 5] >> (x & 31)) & 1u);
         const int lim = b == own_t ? lim_t : kSparseBlock;
         if (ok && !warp_wait_or_abort(&ctl->s_full[sb], (gb / kSBuf) & 1, ctl, a.err_word)) ok = false;
         tc::fence_after_sync();
@@ -843,7 +1222,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         int de = 0;
         if (kF16V) {
           const int eb = d->vexp[i];
-          if (i == 0) E = eb;
+          if (i == 0 && !cont) E = eb;
           if (eb - E > kExpUp || eb - E < kExpDown) {
             // O holds this tile's PV(i-1) once that completes (S(i) done implies PV(i-2) done)
             if (ok && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
@@ -946,45 +1325,48 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (sw == 0 && lane == 0) TRACEB(kEvSoftOut, gb);
       }
       if (sw == 0 && lane == 0) TRACE(kEvEpi);
-      // ---- epilogue: O / l -> bf16 (row sum combined over the parts of the quadrant). The next
-      // tile's first PV, which starts O afresh, waits for this warp's arrival on its P.
-      if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
-        ok = false;
-      tc::fence_after_sync();
-      ctl->xchg[part][row] = l;
-      quad_bar(quad);
-      float lsum = 0.f;
+      // ---- epilogue, at the tile's last descriptor: O / l -> bf16 (row sum combined over the parts
+      // of the quadrant). The next tile's first PV, which starts O afresh, waits for this warp's
+      // arrival on its P.
+      if (!more) {
+        if (ok && nU > 0 && !warp_wait_or_abort(&ctl->pv_done[(gb - 1) % kSBuf], ((gb - 1) / kSBuf) & 1, ctl, a.err_word))
+          ok = false;
+        tc::fence_after_sync();
+        ctl->xchg[part][row] = l;
+        quad_bar(quad);
+        float lsum = 0.f;
 #pragma unroll
-      for (int q = 0; q < kSplit; ++q) lsum += ctl->xchg[q][row];
-      quad_bar(quad);  // every part has read before the next tile's first block overwrites
-      {
-        // warp-collective TMEM reads for every lane; only rows of real tokens are stored
-        uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
-                        static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
-        const float inv = (live && lsum > 0.f && ok) ? a.v_scale * (kF16V ? exp2i(E) : 1.f) / lsum : 0.f;
-        // p = 2^(t - m_ref), so the row's base-2 log-sum-exp is m_ref + log2(sum p)
-        if (a.lse != nullptr && part == 0 && tt < n_tok)
-          a.lse[static_cast<int64_t>(t0 + tt) * a.lse_row_stride + g * kG + h] =
-              (live && lsum > 0.f && ok) ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
+        for (int q = 0; q < kSplit; ++q) lsum += ctl->xchg[q][row];
+        quad_bar(quad);  // every part has read before the next tile's first block overwrites
+        {
+          // warp-collective TMEM reads for every lane; only rows of real tokens are stored
+          uint16_t* out = a.out + static_cast<int64_t>(t0 + tt) * a.out_row_stride +
+                          static_cast<int64_t>(g * kG + h) * a.out_head_stride + col0;
+          const float inv = (live && lsum > 0.f && ok) ? a.v_scale * (kF16V ? exp2i(E) : 1.f) / lsum : 0.f;
+          // p = 2^(t - m_ref), so the row's base-2 log-sum-exp is m_ref + log2(sum p)
+          if (a.lse != nullptr && part == 0 && tt < n_tok)
+            a.lse[static_cast<int64_t>(t0 + tt) * a.lse_row_stride + g * kG + h] =
+                (live && lsum > 0.f && ok) ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kW / 32; ++c) {
-          uint32_t v[32];
-          if (nU > 0) {
-            tc::ld32(tm_o + lane_off + col0 + 32 * c, v);
-            tc::wait_ld();
-          }
-          uint32_t w[16];
+          for (int c = 0; c < kW / 32; ++c) {
+            uint32_t v[32];
+            if (nU > 0) {
+              tc::ld32(tm_o + lane_off + col0 + 32 * c, v);
+              tc::wait_ld();
+            }
+            uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float o0 = nU > 0 ? __uint_as_float(v[j]) * inv : 0.f;
-            const float o1 = nU > 0 ? __uint_as_float(v[j + 1]) * inv : 0.f;
-            w[j >> 1] = pack_bf16(o0, o1);
-          }
-          if (tt < n_tok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+            for (int j = 0; j < 32; j += 2) {
+              const float o0 = nU > 0 ? __uint_as_float(v[j]) * inv : 0.f;
+              const float o1 = nU > 0 ? __uint_as_float(v[j + 1]) * inv : 0.f;
+              w[j >> 1] = pack_bf16(o0, o1);
+            }
+            if (tt < n_tok) {
+              uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+              for (int q4 = 0; q4 < 4; ++q4)
+                dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+            }
           }
         }
       }
@@ -1023,10 +1405,13 @@ extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_get(long l
 namespace pbs {
 #endif
 
-bool prefill_tc_supported(const AttendArgs& a) {
-  return a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.k <= kTcMaxTopk && a.max_blocks <= kMaxUnion &&
-         a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
-         a.num_pages * a.num_kv_heads <= 0x7fffffffLL &&
+bool prefill_tc_supported(const AttendArgs& a, bool with_workspace) {
+  // bf16: K (and V without a workspace) through the block map of a packed cache; fp8 / NVFP4: K
+  // and V from images the conversion kernel writes into the workspace
+  const bool cache_ok = a.kv_dtype == PBS_KV_BF16 ? a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192
+                                                  : with_workspace;
+  return cache_ok && (a.group == 8 || a.group == 16) && a.k <= kTcMaxTopk && a.max_blocks <= kTcMaxBlocks &&
+         a.num_pages * a.num_kv_heads <= 0x7fffffffLL && a.num_reqs <= 65535 &&
          a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
          reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 &&
          reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
@@ -1042,9 +1427,12 @@ cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUte
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (kF16V) {
-    convert_v_kernel<<<dim3(static_cast<unsigned>(a.max_blocks), static_cast<unsigned>(a.num_reqs),
-                            static_cast<unsigned>(a.num_kv_heads)),
-                       128, 0, stream>>>(a);
+    // the images the attend streams: V (bf16 caches; K comes through the block map), or K and V
+    const dim3 cgrid(static_cast<unsigned>(a.max_blocks), static_cast<unsigned>(a.num_reqs),
+                     static_cast<unsigned>(a.num_kv_heads));
+    if (a.kv_dtype == PBS_KV_FP8_E4M3) convert_kv_kernel<PBS_KV_FP8_E4M3><<<cgrid, 128, 0, stream>>>(a);
+    else if (a.kv_dtype == PBS_KV_NVFP4) convert_kv_kernel<PBS_KV_NVFP4><<<cgrid, 128, 0, stream>>>(a);
+    else convert_v_kernel<<<cgrid, 128, 0, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1057,15 +1445,20 @@ cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUte
 
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream) {
+  // fp8 / NVFP4 caches are read only through the converted images
+  if (a.kv_dtype != PBS_KV_BF16 && (a.vconv == nullptr || a.kconv == nullptr)) return cudaErrorInvalidValue;
   if (a.vconv != nullptr)
     return a.group == 16 ? launch_tc<16, true>(a, kv_map, q_map, stream) : launch_tc<8, true>(a, kv_map, q_map, stream);
   return a.group == 16 ? launch_tc<16, false>(a, kv_map, q_map, stream) : launch_tc<8, false>(a, kv_map, q_map, stream);
 }
 
-size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_t max_blocks) {
-  if (num_reqs <= 0 || num_kv_heads <= 0 || max_blocks <= 0 || max_blocks > kMaxUnion) return 0;
+size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_t max_blocks, int kv_dtype) {
+  if (num_reqs <= 0 || num_reqs > 65535 || num_kv_heads <= 0 || max_blocks <= 0 || max_blocks > kTcMaxBlocks) return 0;
+  if (kv_dtype != PBS_KV_BF16 && kv_dtype != PBS_KV_FP8_E4M3 && kv_dtype != PBS_KV_NVFP4) return 0;
   const int64_t n = num_reqs * max_blocks * num_kv_heads;
-  const int64_t bytes = n * kTileBytes + ((n * 4 + 255) / 256) * 256;
+  // V images, their exponents, then (fp8 / NVFP4) the K images
+  int64_t bytes = n * kTileBytes + ((n * 4 + 255) / 256) * 256;
+  if (kv_dtype != PBS_KV_BF16) bytes += n * kTileBytes;
   return static_cast<size_t>(bytes);
 }
 

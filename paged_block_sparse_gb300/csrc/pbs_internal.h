@@ -79,9 +79,11 @@ struct AttendArgs {
   float* split_ws;            // non-null: splits merge through this workspace, not a cluster
   int32_t* split_tickets;     // one arrival counter per (row, head group), zero between calls
   // prefill tile kernel: V of every (request, block, kv head) converted to fp16 as a 32 KiB
-  // shared-memory image, and its exponents (null: the kernel applies bf16 P as hi + lo)
+  // shared-memory image, and its exponents (null: the kernel applies bf16 P as hi + lo); for fp8
+  // / NVFP4 caches also K as bf16 images
   uint8_t* vconv;
   int32_t* vconv_exp;
+  uint8_t* kconv;
 };
 
 // ln 2: a base-2 log-sum-exp (what the kernels track) times this is the natural-log one.
@@ -111,15 +113,17 @@ constexpr int kModePrefill = 1;
 constexpr int kModeMixed = 2;
 cudaError_t launch_attend(const AttendArgs& a, int mode, const CUtensorMap& tmap, cudaStream_t stream);
 
-// Prefill attend on tcgen05 tensor cores (bf16 cache, GQA 8 or 16, top-k <= 16, 16-byte aligned
-// q/out rows). `kv_map` is the per-block map of the packed cache (one {64, 16, 1, 8, 2} box per
-// 128-key block of one kv head); `q_map` a 3-D tensor map {head_dim, heads, tokens} with a
-// {64, G, 128 / G} box.
-bool prefill_tc_supported(const AttendArgs& a);
-// Bytes of the tile kernel's converted-V workspace (0: arguments out of range): one 32 KiB image
-// (kTileVBytes) per (request, block, kv head), then one int32 exponent each.
+// Prefill attend on tcgen05 tensor cores (GQA 8 or 16, top-k <= 16, page tables up to 65535
+// blocks, 16-byte aligned q/out rows): a packed bf16 cache, or (with the workspace) an fp8 /
+// NVFP4 cache through converted images. `kv_map` is the per-block map of a packed bf16 cache (one
+// {64, 16, 1, 8, 2} box per 128-key block of one kv head; unused for fp8 / NVFP4); `q_map` a 3-D
+// tensor map {head_dim, heads, tokens} with a {64, G, 128 / G} box.
+bool prefill_tc_supported(const AttendArgs& a, bool with_workspace);
+// Bytes of the tile kernel's workspace (0: arguments out of range): one 32 KiB fp16 V image
+// (kTileVBytes) per (request, block, kv head), then one int32 exponent each (rounded up to 256
+// bytes), then for fp8 / NVFP4 one 32 KiB bf16 K image each.
 constexpr int64_t kTileVBytes = 32768;
-size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_t max_blocks);
+size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_t max_blocks, int kv_dtype);
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream);
 

@@ -146,14 +146,17 @@ def test_prefill_workspace_bytes(L):
 def test_prefill_tile_workspace_bytes(L):
     f = L.pbs_prefill_tile_workspace_bytes
     f.restype = ctypes.c_size_t
-    # one 32 KiB fp16 image per (request, block, kv head), then the int32 exponents (256-aligned)
-    assert f(4, 8, 64) == 4 * 64 * 8 * 32768 + 8192
-    assert f(1, 1, 1) == 32768 + 256
-    assert f(3, 2, 128) > f(3, 2, 64)
-    for bad in ((0, 8, 64), (4, 0, 64), (4, 8, 0), (4, 8, 129)):
+    # one 32 KiB fp16 V image per (request, block, kv head), then the int32 exponents (256-aligned);
+    # fp8 / NVFP4 add a 32 KiB bf16 K image each
+    assert f(4, 8, 64, 0) == 4 * 64 * 8 * 32768 + 8192
+    assert f(1, 1, 1, 0) == 32768 + 256
+    assert f(4, 8, 64, 1) == f(4, 8, 64, 2) == f(4, 8, 64, 0) + 4 * 64 * 8 * 32768
+    assert f(3, 2, 300, 0) > f(3, 2, 64, 0)                   # page tables wider than 128 blocks
+    for bad in ((0, 8, 64, 0), (4, 0, 64, 0), (4, 8, 0, 0), (4, 8, 65536, 0), (65536, 8, 64, 0), (4, 8, 64, 3)):
         assert f(*bad) == 0
     import paged_block_sparse_gb300 as pbs
-    assert pbs.prefill_tile_workspace_bytes(4, 8, 64) == f(4, 8, 64)
+    assert pbs.prefill_tile_workspace_bytes(4, 8, 64) == f(4, 8, 64, 0)
+    assert pbs.prefill_tile_workspace_bytes(4, 8, 64, "nvfp4") == f(4, 8, 64, 2)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
@@ -200,10 +203,20 @@ def test_prefill_kernel_choice_rule():
     assert run("bf16", 64, 4, 16, 128, 4 * 8192) == "tile"          # GQA 16, table 8 x top-k wide
     assert run("bf16", 64, 8, 16, 129, packed) == "token"            # wider than 8 x top-k
     assert run("bf16", 64, 8, 8, 65, packed) == "token"              # 8 x top-k = 64 blocks
-    assert run("bf16", 64, 8, 8, 65, packed, "tile") == "tile"       # asked for: up to 128 blocks
-    assert run("bf16", 64, 8, 8, 129, packed, "tile") == 3           # the tile kernel cannot take it
+    assert run("bf16", 64, 8, 8, 65, packed, "tile") == "tile"       # asked for: wider page tables too
+    assert run("bf16", 64, 8, 8, 4000, packed, "tile") == "tile"
+    assert run("bf16", 64, 8, 8, 65536, packed, "tile") == 3         # block ids travel as 16 bits
+    assert run("bf16", 64, 8, 17, 64, packed, "tile") == 3           # top-k above 16
     assert run("bf16", 64, 8, 16, 64, packed, "token") == "token"
+    # fp8 / NVFP4 caches take the tile kernel only with its workspace (K and V images)
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096) == "token"
+    big = 1 << 62
+    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, ws=big) == "tile"
+    assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, ws=big) == "tile"
+    assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, "tile") == 3        # asked for without the workspace
+    need = pbs.prefill_tile_workspace_bytes(4, 8, 64, "fp8_e4m3")
+    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, "tile", ws=need) == "tile"
+    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, "tile", ws=need - 256) == 3
     assert run("bf16", 32, 8, 16, 64, packed) == "token"             # GQA 4
     assert run("bf16", 64, 8, 17, 64, packed) == "token"             # top-k above 16
     assert run("bf16", 64, 8, 16, 64, packed + 16) == "token"        # pages strided inside a larger allocation

@@ -97,5 +97,8 @@ def test_mixed_nvfp4(pbs):
     _check_tables(pbs, b)
     _decode_parity(pbs, b, 12, 4)
     _prefill_parity(pbs, b, 24, 5)
+    # the prefill part on the tcgen05 tile kernel (NVFP4 K / V converted to bf16 / fp16 images;
+    # contexts of 16k and 32k keys: page tables of 160 and 288 blocks)
+    _prefill_parity(pbs, b, 24, 8, kernel="tile")
     del b
     torch.cuda.empty_cache()

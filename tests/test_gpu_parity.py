@@ -681,3 +681,64 @@ def test_prebuilt_table_unreadable_rows(pbs, kernel):
     want = oracle_decode(b) if part == "dec" else oracle_prefill(b)
     assert_close({r: got[r] for r in want if r not in bad}, {r: v for r, v in want.items() if r not in bad}, "bf16",
                  "rows beside the unreadable ones")
+
+
+# ------------------------------------------------------------------------------------------
+# tile kernel: fp8 / NVFP4 caches through converted images; long contexts; two-part unions
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "nvfp4"])
+@pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
+@pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
+def test_prefill_tile_kernel_fp8_nvfp4(pbs, kv_dtype, heads, ci):
+    """fp8 and NVFP4 caches on the tcgen05 tile kernel: K converted to bf16 and V to fp16 images once
+    per (request, block, kv head), both exact, then the same tile pipeline as bf16."""
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=heads[0], num_kv_heads=heads[1], seed=141 + ci,
+                        **PREFILL_CASES[ci])
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err, kernel="tile")
+    assert int(err.item()) == 0
+    assert_close(dict(enumerate(got)), oracle_prefill(b), kv_dtype, f"tile {kv_dtype} case {ci}")
+
+
+def _largest_tile_union(b, tok):
+    """Distinct valid blocks of the first `tok` tokens of each request (one tile each)."""
+    p = b.pre
+    tk = np_i32(p.topk)[0]
+    cu = np_i32(p.cu_seqlens_q)
+    sl = np_i32(p.seq_lens)
+    best = 0
+    for r in range(len(sl)):
+        ctx = int(sl[r]) - int(cu[r + 1] - cu[r])
+        blocks = set()
+        for t in range(int(cu[r]), min(int(cu[r]) + tok, int(cu[r + 1]))):
+            pos = ctx + t - int(cu[r])
+            blocks.update(int(x) for x in tk[t] if 0 <= x <= pos // 128)
+        best = max(best, len(blocks))
+    return best
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "nvfp4"])
+@pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
+def test_prefill_tile_long_context_two_part_unions(pbs, kv_dtype, heads):
+    """Page tables far wider than 128 blocks (contexts of 30k-41k keys) and tiles whose union of
+    selected blocks exceeds one descriptor's 128 entries, so a tile continues in a second descriptor
+    (O and the softmax state carried over); with and without the workspace (bf16), and fed the
+    prebuilt table (bit-identical to the self-compacting call)."""
+    b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=heads[0], num_kv_heads=heads[1], topk=16,
+                        pre_q_lens=[40, 17, 3], pre_ctx_lens=[30000, 41000, 2000], future_prob=0.05, seed=150)
+    p = b.pre
+    assert p.page_table.shape[1] > 128
+    tok = 16 if heads == (64, 8) else 8
+    if tok == 16:
+        assert _largest_tile_union(b, tok) > 128
+    want = oracle_prefill(b)
+    for ws in (("default", None) if kv_dtype == "bf16" else ("default",)):
+        err = _err()
+        got = gpu_attend(pbs, b, "pre", err, workspace=ws, kernel="tile")
+        assert int(err.item()) == 0
+        assert_close(dict(enumerate(got)), want, kv_dtype, f"tile long context {kv_dtype} workspace={ws}")
+        tbl = pbs.build_sparse_block_table_prefill(p.topk, p.page_table, p.cu_seqlens_q, p.seq_lens)
+        tabled = gpu_attend(pbs, b, "pre", err, workspace=ws, kernel="tile", sparse_table=tbl)
+        assert int(err.item()) == 0
+        assert np.array_equal(got, tabled), "table-fed tile call differs from the fused one"
