@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const __grid_consta
 
     for (int p0 = warp * kPP; p0 < npages; p0 += kPP * kConsumerWarps) {
       // the iteration's pages p0 .. p0 + kPP - 1 that exist (a row's last iteration may have fewer)
-      const int n_live = min(kPP, npages - p0);
+      const int n_live = kPP == 1 ? 1 : min(kPP, npages - p0);  // p0 < npages: one page at least
       uint32_t st[kPP];
       int nv[kPP];
       bool ok = true;
