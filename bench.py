@@ -403,6 +403,22 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
                                         "algorithmic_tflop": fl / 1e12}
     del b
     torch.cuda.empty_cache()
+    # the prefill prompts on fp8 and NVFP4 caches, on the tile kernel (K and V converted to images
+    # first) and on the token-centric kernel
+    for kv in ("fp8_e4m3", "nvfp4"):
+        b = workloads.prefill(device="cuda", kv_dtype=kv)
+        fl = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
+        r = {}
+        for kern in ("tile", "token"):
+            t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream,
+                                              kernel=kern))
+            r[f"{kern}_ms"] = t
+            r[f"{kern}_TFLOP/s"] = fl / (t * 1e-3) / 1e12
+            r[f"{kern}_frac_of_bf16_peak"] = fl / (t * 1e-3) / 1e12 / bf16
+        res[f"prefill_varlen_{kv}"] = r
+        pbs._tile_workspaces.clear()
+        del b
+        torch.cuda.empty_cache()
     # fp8 MTP decode: algorithmic bytes = the union of each request's K/V rows over its two
     # right-aligned rows (each kernel CTA serves one row, so the per-row sum is what it reads)
     b = workloads.mtp_fp8(device="cuda")

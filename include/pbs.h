@@ -327,9 +327,10 @@ PBS_API int pbs_sparse_prefill_attention(
  * options ask for a kernel that cannot take the call, -PBS_ERR_ARG for bad arguments). No
  * counterpart on the pages; a caller uses it to size the workspace the chosen kernel wants.
  * The rule: options->prefill_kernel when set; else the tile kernel while it can take the call
- * (PBS_PREFILL_TILE above) and the page table is at most 8 x topk_k blocks wide (a tile streams
- * the union of its tokens' selections, which grows with the context they choose from); else the
- * token-centric kernel. The answer assumes 16-byte aligned q and out rows; a call whose rows are
+ * (PBS_PREFILL_TILE above) and, for a bf16 cache, the page table is at most 8 x topk_k blocks wide
+ * (a tile streams the union of its tokens' selections, which grows with the context they choose
+ * from); else the token-centric kernel. fp8 / NVFP4 calls with the tile kernel's workspace take
+ * it at any width (the token-centric kernel dequantises every gathered row per token). The answer assumes 16-byte aligned q and out rows; a call whose rows are
  * not takes the token-centric kernel (or PBS_ERR_UNSUPPORTED when a tcgen05 kernel was asked for).
  *   with_table       non-zero: the call passes a prebuilt table
  *   workspace_bytes  the workspace the call will pass (0 for none), 256-byte aligned

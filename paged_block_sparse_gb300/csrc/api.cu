@@ -208,8 +208,12 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int force
                                                       a.max_blocks, workspace_bytes) > 0;
   if ((forced == PBS_PREFILL_TILE && !tile_fits) || (forced == PBS_PREFILL_GATHER && !gather_fits))
     return PBS_ERR_UNSUPPORTED;
+  // fp8 / NVFP4: the token-centric kernel dequantises every gathered row per token, the tile kernel
+  // once per block; measured faster at every page-table width (prefill prompts 3.3x / 3.6x,
+  // contexts of 16k / 32k keys 1.04x)
   if (forced != PBS_PREFILL_AUTO) *kernel = forced;
-  else if (tile_fits && a.max_blocks <= kTileMaxBlocksPerTopk * a.k) *kernel = PBS_PREFILL_TILE;
+  else if (tile_fits && (a.kv_dtype != PBS_KV_BF16 || a.max_blocks <= kTileMaxBlocksPerTopk * a.k))
+    *kernel = PBS_PREFILL_TILE;
   else *kernel = PBS_PREFILL_TOKEN;
   return PBS_OK;
 }

@@ -399,21 +399,49 @@ __device__ __forceinline__ float f16x2_hi(uint32_t x) {
   return f;
 }
 
-// Elements 8c .. 8c + 7 of one side (K or V) of a key, dequantised to float (exact).
+// One side (K or V) of one key as stored: fp8 128 bytes; NVFP4 64 bytes of e2m1 codes (element
+// 2i in the low nibble of byte i) and 8 e4m3 block scales (scale j covers elements 16j .. 16j + 15).
+// Loaded with 16-byte (codes) and 8-byte (scales) vector loads.
 template <int FMT>
-__device__ __forceinline__ void dequant8(const uint8_t* side, int row, int c, float (&v)[8]) {
+struct KeySide {
+  uint4 w[FMT == PBS_KV_FP8_E4M3 ? 8 : 4];
+  uint2 sc;
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_side(const uint8_t* side, int row, KeySide<FMT>& k) {
   if (FMT == PBS_KV_FP8_E4M3) {
-    const uint2 w = *reinterpret_cast<const uint2*>(side + 8 * c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) k.w[i] = __ldg(reinterpret_cast<const uint4*>(side) + i);
+    k.sc = make_uint2(0u, 0u);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k.w[i] = __ldg(reinterpret_cast<const uint4*>(side + row * 64) + i);
+    k.sc = __ldg(reinterpret_cast<const uint2*>(side + 1024 + row * 8));
+  }
+}
+
+__device__ __forceinline__ uint32_t word4(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Elements 8c .. 8c + 7 of a key side, dequantised to float (exact). c must be a compile-time
+// constant after unrolling.
+template <int FMT>
+__device__ __forceinline__ void dequant8(const KeySide<FMT>& k, int c, float (&v)[8]) {
+  if (FMT == PBS_KV_FP8_E4M3) {
+    const uint4& q = k.w[c >> 1];
+    const uint32_t lo = word4(q, 2 * (c & 1)), hi = word4(q, 2 * (c & 1) + 1);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t h2 = e4m3x2_to_f16x2(((i < 2 ? w.x : w.y) >> (16 * (i & 1))) & 0xffffu);
+      const uint32_t h2 = e4m3x2_to_f16x2(((i < 2 ? lo : hi) >> (16 * (i & 1))) & 0xffffu);
       v[2 * i] = f16x2_lo(h2);
       v[2 * i + 1] = f16x2_hi(h2);
     }
   } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(side + row * 64 + 4 * c);
-    // scale j covers elements 16j .. 16j + 15, so chunk c uses scale c / 2
-    const float sc = f16x2_lo(e4m3x2_to_f16x2(side[1024 + row * 8 + c / 2]));
+    const uint32_t w = word4(k.w[c >> 2], c & 3);
+    const uint32_t sb = ((c >> 1) < 4 ? k.sc.x : k.sc.y) >> (8 * ((c >> 1) & 3));
+    const float sc = f16x2_lo(e4m3x2_to_f16x2(sb & 0xffu));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t h2 = e2m1x2_to_f16x2((w >> (8 * i)) & 0xffu);
@@ -439,13 +467,18 @@ __global__ void __launch_bounds__(128) convert_kv_kernel(const AttendArgs a) {
   // fp8: [Hkv][16 rows][K 128 B | V 128 B]; NVFP4: [2 Hkv slots of 1152 B], slot 2g = K, 2g + 1 = V
   const uint8_t* kside = FMT == PBS_KV_FP8_E4M3 ? base + g * 4096 + row * 256 : base + (2 * g) * 1152;
   const uint8_t* vside = FMT == PBS_KV_FP8_E4M3 ? kside + 128 : kside + 1152;
+  KeySide<FMT> ks, vs;
+  if (live) {
+    load_side<FMT>(kside, row, ks);
+    load_side<FMT>(vside, row, vs);
+  }
   const int64_t image = (static_cast<int64_t>(r) * a.max_blocks + b) * a.num_kv_heads + g;
   // K: bf16 image
   uint8_t* kdst = a.kconv + image * kTileBytes;
-#pragma unroll 4
+#pragma unroll
   for (int c = 0; c < 16; ++c) {
     float v[8];
-    if (live) dequant8<FMT>(kside, row, c, v);
+    if (live) dequant8<FMT>(ks, c, v);
     else
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = 0.f;
@@ -455,10 +488,11 @@ __global__ void __launch_bounds__(128) convert_kv_kernel(const AttendArgs a) {
   }
   // V: the block's maximum |V|, then fp16 V * 2^-e
   float mx = 0.f;
-  for (int c = 0; c < 16; ++c) {
-    float v[8];
-    if (live) {
-      dequant8<FMT>(vside, row, c, v);
+  if (live) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float v[8];
+      dequant8<FMT>(vs, c, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
     }
@@ -477,10 +511,10 @@ __global__ void __launch_bounds__(128) convert_kv_kernel(const AttendArgs a) {
   e = max(-100, min(100, e));
   const float sc = exp2i(-e);
   uint8_t* vdst = a.vconv + image * kTileBytes;
-#pragma unroll 4
+#pragma unroll
   for (int c = 0; c < 16; ++c) {
     float v[8];
-    if (live) dequant8<FMT>(vside, row, c, v);
+    if (live) dequant8<FMT>(vs, c, v);
     else
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = 0.f;

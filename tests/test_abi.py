@@ -214,6 +214,8 @@ def test_prefill_kernel_choice_rule():
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, ws=big) == "tile"
     assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, ws=big) == "tile"
     assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, "tile") == 3        # asked for without the workspace
+    assert run("nvfp4", 64, 8, 16, 400, 8 * 2304, ws=big) == "tile"  # fp8 / NVFP4: any page-table width
+    assert run("bf16", 64, 8, 16, 400, packed, ws=big) == "token"
     need = pbs.prefill_tile_workspace_bytes(4, 8, 64, "fp8_e4m3")
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, "tile", ws=need) == "tile"
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, "tile", ws=need - 256) == 3

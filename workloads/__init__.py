@@ -354,8 +354,9 @@ def decode(device="cuda", seed: int = 1001, batch: int = 64, kv_dtype: str = "bf
                       head_dim=128, topk=16, dec_seq_lens=sl, seed=seed, device=device)
 
 
-def prefill(device="cuda", seed: int = 1002) -> Batch:
-    return make_batch("prefill_varlen_2k4k8k8k_top16_bf16", kv_dtype="bf16", num_heads=64,
+def prefill(device="cuda", seed: int = 1002, kv_dtype: str = "bf16") -> Batch:
+    """The varlen prefill workload; kv_dtype "fp8_e4m3" / "nvfp4" gives the same prompts on those caches."""
+    return make_batch(f"prefill_varlen_2k4k8k8k_top16_{kv_dtype}", kv_dtype=kv_dtype, num_heads=64,
                       num_kv_heads=8, head_dim=128, topk=16, pre_q_lens=[2048, 4096, 8192, 8192],
                       future_prob=0.3, seed=seed, device=device)
 
