@@ -370,10 +370,13 @@ PBS_API size_t pbs_prefill_tile_workspace_bytes(int32_t num_reqs, int32_t num_kv
  * pre_page_table / cu_seqlens_q / pre_seq_lens as in pbs_sparse_prefill_attention. q, topk,
  * out, lse and the optional prebuilt table (sparse_bt / sparse_ctx rows, as in the two calls)
  * are indexed by that row over both parts. Where the prefill part takes a tcgen05 kernel this
- * issues the two calls on `stream`, decode first (what the page's forward does); otherwise it is
- * one launch of the token-centric kernel, whose CTAs take their part by row, so the decode rows
- * run beside the prefill tokens. No workspace (the tile kernel runs its bf16 hi + lo path).
- * Errors as in the two calls; with no rows in one part it is that part's call.
+ * issues the two calls on `stream`, decode first (what the page's forward does), and passes the
+ * optional workspace (NULL, 0) to the prefill call exactly as pbs_sparse_prefill_attention takes
+ * it (the tile kernel's images; fp8 / NVFP4 prefill parts need it to run on the tile kernel);
+ * otherwise it is one launch of the token-centric kernel, whose CTAs take their part by row, so
+ * the decode rows run beside the prefill tokens, and the workspace is not used. The kernel choice
+ * for the prefill part is pbs_prefill_kernel_choice's for its shape and this workspace. Errors as
+ * in the two calls; with no rows in one part it is that part's call.
  */
 PBS_API int pbs_sparse_mixed_attention(
     const void* q, int64_t q_row_stride, int64_t q_head_stride,
@@ -389,6 +392,7 @@ PBS_API int pbs_sparse_mixed_attention(
     float softmax_scale, float k_scale, float v_scale,
     void* out, int64_t out_row_stride, int64_t out_head_stride,
     float* lse, int64_t lse_row_stride,
+    void* workspace, size_t workspace_bytes,
     const pbs_attend_options* options,
     int32_t* err_word, pbs_stream_t stream);
 

@@ -97,7 +97,7 @@ def lib() -> ctypes.CDLL:
     L.pbs_sparse_mixed_attention.restype = ctypes.c_int
     L.pbs_sparse_mixed_attention.argtypes = attend_head[:13] + [vp, i64, i32, vp, i32, i32, vp, i64, i32, vp, vp, i32,
                                                                 i32, i32] + table + [
-        f32, f32, f32, vp, i64, i64, vp, i64, vp, vp, vp]
+        f32, f32, f32, vp, i64, i64, vp, i64, vp, ctypes.c_size_t, vp, vp, vp]
     L.pbs_insert_index_cache.restype = ctypes.c_int
     L.pbs_insert_index_cache.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32, vp, i64, i32, vp, vp]
     del sz
@@ -502,10 +502,13 @@ def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, 
                            decode_query_len: int, pre_page_table, cu_seqlens_q, pre_seq_lens, softmax_scale: float,
                            k_scale: float = 1.0, v_scale: float = 1.0, block_page_stride: int = PAGES_PER_BLOCK,
                            out=None, err_word=None, stream=None, lse=None, return_lse: bool = False,
-                           sparse_table=None, kernel=None, splits=None, cache_map=None):
+                           sparse_table=None, kernel=None, splits=None, cache_map=None, workspace="auto"):
     """Decode rows then prefill tokens in one call (vLLM flashinfer forward with both parts):
     q [nd + total_q, Hq, 128] with nd = len(dec_seq_lens) * decode_query_len; topk (and the
-    optional prebuilt ``sparse_table``) one row per q row. Returns out (and lse)."""
+    optional prebuilt ``sparse_table``) one row per q row. ``workspace`` is the prefill part's, as in
+    :func:`sparse_prefill_attention` ("auto": sized for the kernel the library picks for that part;
+    None: none, so fp8 / NVFP4 prefill parts stay on the token-centric kernel). Returns out (and
+    lse)."""
     num_pages, psb, tk, pt_d, out = _attend_prologue(q, kv_cache, kv_dtype, num_kv_heads, topk, dec_page_table, out)
     pt_p = _table2d(pre_page_table, "pre_page_table")
     sl_d = _dev(dec_seq_lens, "dec_seq_lens", torch.int32)
@@ -515,6 +518,17 @@ def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, 
     total_q = q.shape[0] - nd
     if total_q < 0:
         raise ValueError(f"q has {q.shape[0]} rows, fewer than the {nd} decode rows")
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = None
+        if total_q > 0 and nd > 0:
+            if kernel == "gather":
+                workspace = prefill_workspace(total_q, sl_p.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
+                                              pt_p.shape[1], q.device, stream)
+            elif prefill_kernel_choice(total_q, sl_p.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads, tk.shape[1],
+                                       pt_p.shape[1], sparse_table is not None, _ANY_WORKSPACE, kernel) == "tile":
+                workspace = prefill_tile_workspace(sl_p.shape[0], num_kv_heads, pt_p.shape[1], q.device, stream,
+                                                   kv_dtype)
+    wp, wb = _workspace_args(workspace, total_q, q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
     tb, ts, tc = _table_args(sparse_table, q.shape[0])
     st = lib().pbs_sparse_mixed_attention(
@@ -523,7 +537,7 @@ def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, 
         pt_d.shape[1], _ptr(sl_d), sl_d.shape[0], int(decode_query_len), _ptr(pt_p), pt_p.stride(0), pt_p.shape[1],
         _ptr(cu), _ptr(sl_p), sl_p.shape[0], total_q, int(block_page_stride), tb, ts, tc, float(softmax_scale),
         float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
-        lse.stride(0) if lse is not None else 0, _options(kernel, splits, cache_map), _ptr(err_word),
+        lse.stride(0) if lse is not None else 0, wp, wb, _options(kernel, splits, cache_map), _ptr(err_word),
         _stream(stream, q.device))
     _check(st, "pbs_sparse_mixed_attention")
     return (out, lse) if lse is not None else out

@@ -445,7 +445,7 @@ const char* pbs_status_string(int status) {
   }
 }
 
-int pbs_abi_version(void) { return 8; }
+int pbs_abi_version(void) { return 9; }
 
 size_t pbs_attend_workspace_bytes(int64_t num_rows, int32_t num_heads, int32_t num_kv_heads) {
   if (num_rows <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
@@ -768,9 +768,11 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
                                int32_t num_reqs, int32_t total_q, int32_t block_page_stride,
                                const int32_t* sparse_bt, int64_t sbt_row_stride, const int32_t* sparse_ctx,
                                float softmax_scale, float k_scale, float v_scale, void* out, int64_t out_row_stride,
-                               int64_t out_head_stride, float* lse, int64_t lse_row_stride,
-                               const pbs_attend_options* options, int32_t* err_word, pbs_stream_t stream) {
+                               int64_t out_head_stride, float* lse, int64_t lse_row_stride, void* workspace,
+                               size_t workspace_bytes, const pbs_attend_options* options, int32_t* err_word,
+                               pbs_stream_t stream) {
   if (batch < 0 || decode_query_len <= 0 || total_q < 0 || num_reqs < 0) return PBS_ERR_ARG;
+  if (workspace == nullptr && workspace_bytes != 0) return PBS_ERR_ARG;
   const int64_t nd = static_cast<int64_t>(batch) * decode_query_len;
   // one part only: the plain entry points
   if (total_q == 0)
@@ -786,7 +788,7 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
                                         pre_page_table, pre_pt_row_stride, pre_max_blocks, cu_seqlens_q, pre_seq_lens,
                                         num_reqs, total_q, block_page_stride, sparse_bt, sbt_row_stride, sparse_ctx,
                                         softmax_scale, k_scale, v_scale, out, out_row_stride, out_head_stride, lse,
-                                        lse_row_stride, nullptr, 0, options, err_word, stream);
+                                        lse_row_stride, workspace, workspace_bytes, options, err_word, stream);
   if (num_reqs == 0) return PBS_ERR_SHAPE;
   if (nd + total_q > 0x7fffffffLL / 8) return PBS_ERR_UNSUPPORTED;
   Options opt;
@@ -824,7 +826,8 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
   st = encode_attend_map(&map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, false, &p.packed_map);
   if (st != PBS_OK) return st;
   int kernel = PBS_PREFILL_TOKEN;
-  st = choose_prefill_kernel(p, 0, opt.prefill_kernel, &kernel);
+  st = choose_prefill_kernel(p, workspace != nullptr && aligned(workspace, 256) ? workspace_bytes : 0,
+                             opt.prefill_kernel, &kernel);
   if (st != PBS_OK) return st;
   if (kernel != PBS_PREFILL_TOKEN) {
     // the prefill part runs on a tcgen05 kernel: two launches, decode first
@@ -840,8 +843,8 @@ int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_he
                                         topk_k, pre_page_table, pre_pt_row_stride, pre_max_blocks, cu_seqlens_q,
                                         pre_seq_lens, num_reqs, total_q, block_page_stride, sbt_pre, sbt_row_stride,
                                         ctx_pre, softmax_scale, k_scale, v_scale, out_pre, out_row_stride,
-                                        out_head_stride, lse_pre, lse_row_stride, nullptr, 0, options, err_word,
-                                        stream);
+                                        out_head_stride, lse_pre, lse_row_stride, workspace, workspace_bytes, options,
+                                        err_word, stream);
   }
   // both parts on the token-centric kernel: one launch, each CTA picks its part by row
   if (opt.quarter_map) {

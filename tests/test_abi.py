@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings(L):
     import paged_block_sparse_gb300 as pbs
-    assert pbs.abi_version() == 8
+    assert pbs.abi_version() == 9
     texts = {pbs.status_string(s) for s in range(6)}
     assert len(texts) == 6 and "ok" in texts
     assert pbs.status_string(99) == "unknown status"
@@ -157,6 +157,24 @@ def test_prefill_tile_workspace_bytes(L):
     import paged_block_sparse_gb300 as pbs
     assert pbs.prefill_tile_workspace_bytes(4, 8, 64) == f(4, 8, 64, 0)
     assert pbs.prefill_tile_workspace_bytes(4, 8, 64, "nvfp4") == f(4, 8, 64, 2)
+
+
+def _mixed_attend(L, **kw):
+    args = dict(batch=2, dql=1, nreqs=1, tq=4, ws=N, wsb=0, dmb=8, pmb=8)
+    args.update(kw)
+    return L.pbs_sparse_mixed_attention(A, 8192, 128, A, 65536, 64, 0, 64, 8, 128, A, 16, 16, A, 8, args["dmb"],
+                                        A, args["batch"], args["dql"], A, 8, args["pmb"], A, A, args["nreqs"],
+                                        args["tq"], 8, N, 0, N, 0.125, 1.0, 1.0, A, 8192, 128, N, 0, args["ws"],
+                                        args["wsb"], N, N, S)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")
+def test_mixed_host_checks(L):
+    assert _mixed_attend(L, batch=-1) == 1
+    assert _mixed_attend(L, dql=0) == 1
+    assert _mixed_attend(L, ws=N, wsb=16) == 1             # workspace bytes without a pointer
+    assert _mixed_attend(L, batch=0, tq=0) == 0            # nothing to attend
+    assert _mixed_attend(L, nreqs=0) == 2                  # prefill tokens without a request
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-check tests use fake device addresses")

@@ -514,10 +514,11 @@ def test_attend_per_quarter_map(pbs, kv_dtype):
 
 
 @pytest.mark.parametrize("kv_dtype,prefill_kernel", [("bf16", "tile"), ("bf16", "token"), ("fp8_e4m3", None),
-                                                     ("nvfp4", None)])
+                                                     ("fp8_e4m3", "token"), ("nvfp4", None), ("nvfp4", "token")])
 def test_mixed_batch_in_one_call(pbs, kv_dtype, prefill_kernel):
     """Decode rows then prefill tokens through pbs_sparse_mixed_attention: one fused launch of the
-    token-centric kernel, or decode + tile kernel when the prefill part takes the tile kernel;
+    token-centric kernel, or decode + tile kernel when the prefill part takes the tile kernel (the
+    default here, with the binding's workspace: fp8 / NVFP4 parts through converted K / V images);
     outputs and log-sum-exp against the oracle's decode and prefill attends."""
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=64, num_kv_heads=8, topk=12,
                         dec_seq_lens=[2500, 0, 9000], decode_query_len=2, pre_q_lens=[150, 1, 60],
