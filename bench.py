@@ -30,7 +30,7 @@ import subprocess
 import sys
 import time
 
-# The oracle leg runs single-threaded so the reported core count is exact.
+# Every oracle worker process runs one numpy thread, so the reported core count is exact.
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -289,6 +289,27 @@ def run_prefill(pbs, b, steps, warmup, flush, stream, workspace="auto", kernel=N
     return time_steps(step, steps, warmup, flush, stream)
 
 
+def gather_segments(pbs, b, ws_bytes):
+    """Token segments the gathered-row kernel cuts a prefill call into on a workspace of ws_bytes
+    (the largest multiple of 256 tokens whose workspace fits, or the whole call)."""
+    p = b.pre
+    T = p.q.shape[0]
+
+    def need(tokens):
+        return pbs.prefill_workspace_bytes(tokens, p.seq_lens.shape[0], b.num_heads, b.num_kv_heads,
+                                           p.topk.shape[-1], p.page_table.shape[1])
+    if need(T) <= ws_bytes:
+        return 1
+    lo, hi = 0, T // 256
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if need(mid * 256) <= ws_bytes:
+            lo = mid
+        else:
+            hi = mid - 1
+    return -(-T // (lo * 256)) if lo > 0 else 0
+
+
 def decode_ctx(pbs, b):
     d = b.dec
     _, ctx = pbs.build_sparse_block_table_decode(d.topk, d.page_table, d.seq_lens, d.decode_query_len,
@@ -376,14 +397,15 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=None))
     res["prefill_varlen_bf16_no_workspace"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                                "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16}
-    # the same call on the gathered-row kernel (opt-in; 2 GiB workspace, three token segments)
+    # the same call on the gathered-row kernel (the binding's default workspace: its token segments)
     ws = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, b.topk,
                                p.page_table.shape[1], "cuda", stream)
     t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=ws,
                                       kernel="gather"))
     res["prefill_varlen_bf16_gathered_rows"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                                 "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
-                                                "workspace_bytes": ws.numel()}
+                                                "workspace_bytes": ws.numel(),
+                                                "segments": gather_segments(pbs, b, ws.numel())}
     del ws
     pbs._prefill_workspaces.clear()
     # the same call fed the prebuilt prefill table (built once, as every sparse layer would share it)
@@ -398,18 +420,21 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     b = workloads.prefill_g16(device="cuda")
     fl = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
     t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream))
+    tg = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, kernel="gather"))
     res["prefill_varlen_gqa16_bf16"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                         "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
-                                        "algorithmic_tflop": fl / 1e12}
+                                        "algorithmic_tflop": fl / 1e12, "gather_ms": tg,
+                                        "gather_TFLOP/s": fl / (tg * 1e-3) / 1e12}
+    pbs._prefill_workspaces.clear()
     del b
     torch.cuda.empty_cache()
-    # the prefill prompts on fp8 and NVFP4 caches, on the tile kernel (K and V converted to images
-    # first) and on the token-centric kernel
+    # the prefill prompts on fp8 and NVFP4 caches, on both tcgen05 kernels (K and V converted to
+    # images first) and on the token-centric kernel
     for kv in ("fp8_e4m3", "nvfp4"):
         b = workloads.prefill(device="cuda", kv_dtype=kv)
         fl = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
         r = {}
-        for kern in ("tile", "token"):
+        for kern in ("tile", "gather", "token"):
             t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream,
                                               kernel=kern))
             r[f"{kern}_ms"] = t
@@ -417,6 +442,7 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
             r[f"{kern}_frac_of_bf16_peak"] = fl / (t * 1e-3) / 1e12 / bf16
         res[f"prefill_varlen_{kv}"] = r
         pbs._tile_workspaces.clear()
+        pbs._prefill_workspaces.clear()
         del b
         torch.cuda.empty_cache()
     # fp8 MTP decode: algorithmic bytes = the union of each request's K/V rows over its two
@@ -468,12 +494,14 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
                           "prefill_ms": tp, "prefill_TFLOP/s": fl / (tp * 1e-3) / 1e12,
                           "prefill_frac_of_bf16_peak": fl / (tp * 1e-3) / 1e12 / bf16, "prefill_kernel": chosen,
                           "total_ms": td + tp, "one_call_ms": tm}
-    # the prefill part on each prefill kernel (tile: NVFP4 K / V converted to images, then tcgen05)
-    for kern in ("tile", "token"):
+    # the prefill part on each prefill kernel (tile and gathered rows: NVFP4 K / V converted to
+    # images, then tcgen05)
+    for kern in ("gather", "tile", "token"):
         t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, kernel=kern))
         res["mixed_nvfp4"][f"prefill_{kern}_ms"] = t
         res["mixed_nvfp4"][f"prefill_{kern}_TFLOP/s"] = fl / (t * 1e-3) / 1e12
     pbs._tile_workspaces.clear()
+    pbs._prefill_workspaces.clear()
     del qm, tkm, om
     del b
     torch.cuda.empty_cache()
@@ -484,39 +512,34 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
 # oracle (cpu_baseline leg and the reference arm)
 # --------------------------------------------------------------------------------------------
 
-def oracle_decode_rate(b, budget_s: float, max_rows: int | None = None):
-    """Oracle decode tokens/s on the host: sampled rows, their pages fetched to host first."""
-    import oracle
+def oracle_row_pages(b):
+    """Host copies of the cache pages each decode row reads (plumbing, before any timing)."""
     d = b.dec
-    rows = d.q.shape[0]
-    order = list(range(rows)) if max_rows is None else list(range(min(rows, max_rows)))
     tk = d.topk.cpu().numpy()
     pt = d.page_table.cpu().numpy()
-    sl = d.seq_lens.cpu().numpy()
-    q = d.q.cpu().to(torch.float64).numpy()
-    done, t_cpu = 0, 0.0
-    for r in order:
-        # plumbing (untimed): copy this row's candidate pages to the host
+    out = []
+    for r in range(d.q.shape[0]):
         req = r // d.decode_query_len
         blocks = sorted({int(x) for x in tk[0, r] if 0 <= x < pt.shape[1]})
         pages = np.array([int(pt[req, x]) * b.block_page_stride + j for x in blocks for j in range(8)], np.int64)
         host = {}
         if len(pages):
-            data = b.cache.index_select(0, torch.from_numpy(pages).cuda()).cpu().numpy()
+            data = b.cache.index_select(0, torch.from_numpy(pages).to(b.cache.device)).cpu().numpy()
             host = {int(pg): data[i] for i, pg in enumerate(pages)}
+        out.append(host)
+    return out
 
-        class Pages:
-            def __getitem__(self, ids):
-                return np.stack([host[int(i)] for i in ids])
 
-        t0 = time.perf_counter()
-        oracle.sparse_decode_attention(q, Pages(), b.kv_dtype, b.num_kv_heads, tk, pt, sl, d.decode_query_len,
-                                       b.softmax_scale, b.k_scale, b.v_scale, b.block_page_stride, rows=[r])
-        t_cpu += time.perf_counter() - t0
-        done += 1
-        if t_cpu >= budget_s:
-            break
-    return done / t_cpu, done, t_cpu
+def oracle_pool(b):
+    """The oracle on every host core: one spawn-started worker per core, each holding its share of
+    the decode rows and their pages (see oracle/host_rows.py)."""
+    from oracle.host_rows import DecodeRowPool, host_cores
+    d = b.dec
+    return DecodeRowPool(host_cores(), oracle_row_pages(b), q=d.q.cpu().to(torch.float64).numpy(),
+                         kv_dtype=b.kv_dtype, num_kv_heads=b.num_kv_heads, topk=d.topk.cpu().numpy(),
+                         page_table=d.page_table.cpu().numpy(), seq_lens=d.seq_lens.cpu().numpy(),
+                         decode_query_len=d.decode_query_len, softmax_scale=b.softmax_scale, k_scale=b.k_scale,
+                         v_scale=b.v_scale, block_page_stride=b.block_page_stride)
 
 
 def reference_arm(args, world, rank):
@@ -525,10 +548,13 @@ def reference_arm(args, world, rank):
     torch.cuda.set_device(0)
     b = workloads.decode(device="cuda")
     rates = []
-    for i in range(args.warmup + args.steps):
-        rate, done, t = oracle_decode_rate(b, budget_s=max(2.0, 20.0 / max(args.steps, 1)), max_rows=None)
-        if i >= args.warmup:
-            rates.append((rate, done, t))
+    budget = max(2.0, 20.0 / max(args.steps, 1))
+    with oracle_pool(b) as pool:
+        for i in range(args.warmup + args.steps):
+            rate, done, t = pool.run(budget)
+            if i >= args.warmup:
+                rates.append((rate, done, t))
+        workers = pool.workers
     rate = statistics.median(r for r, _, _ in rates)
     ms = 1e3 * b.dec.q.shape[0] / rate
     line = {
@@ -537,8 +563,10 @@ def reference_arm(args, world, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": b.name, "batch": 64, "heads": "64/8", "head_dim": 128, "topk_blocks": 16,
                    "kv": "bf16 paged, page 16", "l2": "oracle on host"},
-        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rates[0][1]} decode rows per step of the 64-row batch, fp64 numpy, 1 thread"},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+                         "sample": f"{rates[0][1]} decode rows per step ({budget:.1f} s on each of {workers} "
+                                   f"worker processes, one numpy thread each, rows of the 64-row batch dealt "
+                                   f"round-robin; pages copied to host before timing)"},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -578,14 +606,19 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream, kernel=kernel)
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
             p = b.pre
-            # the binding's default call on the tile kernel: V conversion, then the attend; the
-            # gathered-row kernel: its index kernel, then the attend, per token segment
+            # the binding's default call on the tile kernel: V conversion, then the attend; on the
+            # gathered-row kernel: the conversion, then index, attend and merge per token segment
             chosen = pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes,
                                                b.num_heads, b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
                                                kernel=kernel, workspace_bytes=1 << 62)
             if chosen == "tile" and 0 < pbs.prefill_tile_workspace_bytes(
                     p.seq_lens.shape[0], b.num_kv_heads, p.page_table.shape[1], b.kv_dtype) <= pbs.TILE_WORKSPACE_CAP:
                 launches = 2
+            elif chosen == "gather":
+                # the conversion kernel, then per token segment the index, attend and merge kernels
+                wsb = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads,
+                                            p.topk.shape[-1], p.page_table.shape[1], "cuda", stream).numel()
+                launches = 1 + 3 * gather_segments(pbs, b, wsb)
         else:
             # rows of one request share their K/V rows: the union counts each once
             per_row = decode_bytes(b, decode_ctx(pbs, b))
@@ -703,10 +736,12 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         bb = workloads.decode(device="cuda", seed=1001)
-        rate, done, t = oracle_decode_rate(bb, budget_s=12.0)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{done} of the 64 decode rows ({t:.1f} s of fp64 numpy on 1 thread; pages copied to "
-                         f"host before timing)"}
+        with oracle_pool(bb) as pool:
+            rate, done, t = pool.run(10.0)
+            workers = pool.workers
+        cpu = {"value": rate, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+               "sample": f"{done} decode rows of the 64-row batch ({t:.1f} s on each of {workers} worker "
+                         f"processes, one fp64 numpy thread each; pages copied to host before timing)"}
         del bb
 
     if rank == 0:

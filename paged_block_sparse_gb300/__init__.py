@@ -364,7 +364,7 @@ def prefill_kernel_choice(total_q: int, num_reqs: int, kv_dtype: str, page_strid
 
 
 # the default prefill workspace is capped; larger calls run in several token segments
-PREFILL_WORKSPACE_CAP = 2 << 30
+PREFILL_WORKSPACE_CAP = 4 << 30
 _prefill_workspaces: dict = {}
 
 
@@ -386,6 +386,19 @@ def prefill_workspace(total_q: int, num_reqs: int, num_heads: int, num_kv_heads:
             ws = torch.empty(need, dtype=torch.uint8, device=device)
         _prefill_workspaces[key] = ws
     return ws
+
+
+def _prefill_auto_workspace(total_q, num_reqs, kv_dtype, psb, num_heads, num_kv_heads, topk, max_blocks, with_table,
+                            kernel, device, stream):
+    """The workspace the library's choice of prefill kernel for this shape wants (given any
+    workspace): the gathered-row kernel's, the tile kernel's images, or none."""
+    chosen = prefill_kernel_choice(total_q, num_reqs, kv_dtype, psb, num_heads, num_kv_heads, topk, max_blocks,
+                                   with_table, _ANY_WORKSPACE, kernel)
+    if chosen == "gather":
+        return prefill_workspace(total_q, num_reqs, num_heads, num_kv_heads, topk, max_blocks, device, stream)
+    if chosen == "tile":
+        return prefill_tile_workspace(num_reqs, num_kv_heads, max_blocks, device, stream, kv_dtype)
+    return None  # the token-centric kernel merges its splits in a cluster
 
 
 def _lse_arg(lse, return_lse, q):
@@ -476,14 +489,9 @@ def sparse_prefill_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk
     cu = _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     sl = _dev(seq_lens, "seq_lens", torch.int32)
     if isinstance(workspace, str) and workspace == "auto":
-        if kernel == "gather":
-            workspace = prefill_workspace(q.shape[0], sl.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
-                                          pt.shape[1], q.device, stream)
-        elif prefill_kernel_choice(q.shape[0], sl.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads, tk.shape[1],
-                                   pt.shape[1], sparse_table is not None, _ANY_WORKSPACE, kernel) == "tile":
-            workspace = prefill_tile_workspace(sl.shape[0], num_kv_heads, pt.shape[1], q.device, stream, kv_dtype)
-        else:
-            workspace = None  # the token-centric kernel merges its splits in a cluster
+        workspace = _prefill_auto_workspace(q.shape[0], sl.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads,
+                                            tk.shape[1], pt.shape[1], sparse_table is not None, kernel, q.device,
+                                            stream)
     wp, wb = _workspace_args(workspace, q.shape[0], q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
     tb, ts, tc = _table_args(sparse_table, q.shape[0])
@@ -521,13 +529,9 @@ def sparse_mixed_attention(q, kv_cache, kv_dtype: str, num_kv_heads: int, topk, 
     if isinstance(workspace, str) and workspace == "auto":
         workspace = None
         if total_q > 0 and nd > 0:
-            if kernel == "gather":
-                workspace = prefill_workspace(total_q, sl_p.shape[0], q.shape[1], num_kv_heads, tk.shape[1],
-                                              pt_p.shape[1], q.device, stream)
-            elif prefill_kernel_choice(total_q, sl_p.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads, tk.shape[1],
-                                       pt_p.shape[1], sparse_table is not None, _ANY_WORKSPACE, kernel) == "tile":
-                workspace = prefill_tile_workspace(sl_p.shape[0], num_kv_heads, pt_p.shape[1], q.device, stream,
-                                                   kv_dtype)
+            workspace = _prefill_auto_workspace(total_q, sl_p.shape[0], kv_dtype, psb, q.shape[1], num_kv_heads,
+                                                tk.shape[1], pt_p.shape[1], sparse_table is not None, kernel,
+                                                q.device, stream)
     wp, wb = _workspace_args(workspace, total_q, q.shape[1], num_kv_heads, q.device, stream)
     lse = _lse_arg(lse, return_lse, q)
     tb, ts, tc = _table_args(sparse_table, q.shape[0])

@@ -157,20 +157,44 @@ int encode_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int 
   return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
 }
 
+// The query rows of one token and one kv head as a single tensor copy (the gathered-row kernel):
+// a 5-D view {64 dims, 8 heads, dim half, head octet, token} of q ([tokens, heads, 128] with the
+// caller's strides) with a {64, 8, 2, group / 8, 1} box. Shared memory then holds the token's
+// rows as [octet][half][8 heads][128 B] (128B swizzle): 1 KiB atoms, K halves 1 KiB apart and
+// consecutive 8-row atoms of the M dimension 2 KiB apart.
+int encode_q_map_tokens(CUtensorMap* map, const void* q, int num_heads, int group, int total_q, int64_t q_row_stride,
+                        int64_t q_head_stride) {
+  std::memset(map, 0, sizeof(*map));
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PBS_ERR_CUDA;
+  if (num_heads % 8 != 0 || group % 8 != 0) return PBS_ERR_UNSUPPORTED;
+  const cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(num_heads / 8), static_cast<cuuint64_t>(total_q)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(q_head_stride) * 2, 128,
+                                 static_cast<cuuint64_t>(q_head_stride) * 2 * 8, static_cast<cuuint64_t>(q_row_stride) * 2};
+  const cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(group / 8), 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(q), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PBS_OK : PBS_ERR_CUDA;
+}
+
 // Which prefill kernel runs: the caller's choice (pbs_attend_options.prefill_kernel) when given,
-// else the tcgen05 tile kernel where it applies and the token-centric kernel elsewhere. The
-// gathered-row kernel (bf16 packed cache, GQA 8 or 16, page table <= 8192 blocks, a workspace of
-// at least one 256-token segment) runs only when asked for: its MMA rows are the tokens that
-// selected a block, so its work does not grow with the context the selections are spread over,
-// but its partial outputs cost more than the tile kernel's waste on the measured workloads.
+// else by the page table's width (the only bound on the contexts that the host sees without a
+// device read):
 //
 // The tile kernel streams the union of its 16 tokens' selections to all of them, so its waste
 // grows with the context a token chooses from: a token at block s selects k of s + 1 blocks,
-// and the union nears min(s + 1, 16 k). The page table's width bounds every context, and only
-// the host sees it without a device read, so the tile kernel is taken while
-// max_blocks <= kTileMaxBlocksPerTopk * k. Measured (bf16, 64/8 heads, top-k 16, 2 x 4096
-// tokens): contexts 0 / 2k-4k / 16k-32k give 462 / 312 / 114 TFLOP/s on the tile kernel and
-// 133 / 139 / 139 on the token-centric one.
+// and the union nears min(s + 1, 16 k). The gathered-row kernel's MMA rows are the tokens that
+// selected a block, so its work does not grow with the context, but every (token, block) pair
+// costs a partial output written and merged through the workspace. So page tables up to
+// kTileMaxBlocksPerTopk * k blocks take the tile kernel, wider ones the gathered-row kernel (with
+// a workspace that holds at least one 256-token segment; otherwise fp8 / NVFP4 stay on the tile
+// kernel and bf16 takes the token-centric kernel). Measured (64/8 heads, top-k 16): the varlen
+// prompts of 2k-8k tokens (64-block table) take 2.39 ms on the tile kernel and 2.37 on the
+// gathered-row kernel; 2 x 4096 tokens after 16k / 32k of context on NVFP4 take 4.69 and 1.89
+// ms; bf16 on the tile kernel gives 462 / 312 / 114 TFLOP/s for contexts 0 / 2k-4k / 16k-32k,
+// the token-centric kernel about 139 throughout.
 constexpr int kTileMaxBlocksPerTopk = 8;
 
 // The caller's options, checked (a null pointer reads as all zero).
@@ -203,7 +227,8 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int force
   const size_t tile_ws = pbs::prefill_tc_workspace_bytes(a.num_reqs, a.num_kv_heads, a.max_blocks, a.kv_dtype);
   const bool tile_fits = (a.kv_dtype != PBS_KV_BF16 || a.packed_map != 0) &&
                          pbs::prefill_tc_supported(a, tile_ws != 0 && workspace_bytes >= tile_ws);
-  const bool gather_fits = a.packed_map != 0 && pbs::prefill_gather_supported(a) && a.num_rows < (1 << 25) &&
+  const bool gather_fits = (a.kv_dtype != PBS_KV_BF16 || a.packed_map != 0) && pbs::prefill_gather_supported(a) &&
+                           a.num_rows < (1 << 25) &&
                            pbs::gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k,
                                                       a.max_blocks, workspace_bytes) > 0;
   if ((forced == PBS_PREFILL_TILE && !tile_fits) || (forced == PBS_PREFILL_GATHER && !gather_fits))
@@ -211,9 +236,10 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int force
   // fp8 / NVFP4: the token-centric kernel dequantises every gathered row per token, the tile kernel
   // once per block; measured faster at every page-table width (prefill prompts 3.3x / 3.6x,
   // contexts of 16k / 32k keys 1.04x)
+  const bool wide = a.max_blocks > kTileMaxBlocksPerTopk * a.k;
   if (forced != PBS_PREFILL_AUTO) *kernel = forced;
-  else if (tile_fits && (a.kv_dtype != PBS_KV_BF16 || a.max_blocks <= kTileMaxBlocksPerTopk * a.k))
-    *kernel = PBS_PREFILL_TILE;
+  else if (wide && gather_fits) *kernel = PBS_PREFILL_GATHER;
+  else if (tile_fits && (a.kv_dtype != PBS_KV_BF16 || !wide)) *kernel = PBS_PREFILL_TILE;
   else *kernel = PBS_PREFILL_TOKEN;
   return PBS_OK;
 }
@@ -680,19 +706,17 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     a.splits = choose_splits(units, topk_k, a.split_ws != nullptr, opt.splits);
     e = pbs::launch_attend(a, pbs::kModePrefill, map, cs);
   } else {
-    // both tcgen05 kernels stream K and V separately: the gathered-row kernel one box per
-    // (page, head) half row, the tile kernel one box per (block, head) half row (bf16; fp8 / NVFP4
-    // blocks come from converted images, and the map is unused)
+    // both tcgen05 kernels read a bf16 K through one box per (block, head) half row, and V (and
+    // fp8 / NVFP4 K) from converted images (the map is then unused)
     CUtensorMap half_map;
     std::memset(&half_map, 0, sizeof(half_map));
-    if (kernel == PBS_PREFILL_GATHER)
-      st = encode_cache_map_packed(&half_map, kv_cache, kv_dtype, num_kv_heads, num_pages, page_stride_bytes, 2);
-    else if (kv_dtype == PBS_KV_BF16)
+    if (kv_dtype == PBS_KV_BF16)
       st = encode_cache_map_block(&half_map, kv_cache, num_kv_heads, num_pages, page_stride_bytes);
     if (st != PBS_OK) return st;
     CUtensorMap qmap;
-    st = encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride,
-                      kernel == PBS_PREFILL_GATHER ? 1 : 0);
+    st = kernel == PBS_PREFILL_GATHER
+             ? encode_q_map_tokens(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride)
+             : encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
     if (kernel == PBS_PREFILL_TILE && workspace != nullptr && aligned(workspace, 256) && num_reqs <= 65535) {
       // with room for the converted V of every (request, block, kv head), the tile kernel applies

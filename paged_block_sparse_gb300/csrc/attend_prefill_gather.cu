@@ -1,5 +1,5 @@
 // Prefill attend by key block ("gathered rows") on the 5th-generation tensor cores (tcgen05 +
-// TMEM), bf16 KV cache, GQA 8 or 16.
+// TMEM): bf16, fp8-e4m3 and NVFP4 caches, GQA 8 or 16.
 //
 // What it computes (vLLM page vllm.models.minimax_m3.nvidia.sparse_attention_flashinfer, forward:
 // the varlen msa_sparse_attention call; row rule of vllm.models.minimax_m3.amd.ops.sparse_pa,
@@ -18,34 +18,31 @@
 // x 16 heads at GQA 16). Every row of every tile does useful work except in a bucket's last
 // chunk.
 //
+// * Images (before the attend; the tile kernel's conversion kernels): the V of every (request,
+//   block, kv head) as fp16 V * 2^-e in the 128B-swizzled layout of a shared-memory stage, and
+//   for fp8 / NVFP4 caches K as bf16 likewise (exact). A bf16 K comes straight from the packed
+//   cache through the per-block tensor map.
 // * Index kernel (one CTA per window): each token's distinct valid blocks, sorted, give the
-//   token's partial slots; tokens are bucketed by block (shared-memory histogram, block scan,
-//   scatter). Tokens with no valid block get zero output here.
-// * Attend kernel (persistent, one CTA per SM): windows are taken in order and the items of a
-//   window from a per-window counter, so the partial results of a window are written and
-//   merged while they sit in L2. Per item, warp 0 loads K_b and V_b of head g (one 4 KiB tensor
-//   copy per page and half row, 128B swizzle) into one of two K/V buffers, then per chunk writes
-//   a descriptor (tokens, partial slots, own-block key limits) into a 4-deep ring and gathers
-//   the chunk's Q rows (one {64 dims, G heads, 1 token} tensor copy per token and half). Warp 1
-//   (one thread) issues S(c) = Q K^T into TMEM buffer c % 2, then PV(c-1), so the softmax of
-//   chunk c overlaps PV(c-1) and S(c+1). Warps 4-7 and 8-11 are two softmax warpgroups taking
-//   chunks alternately; a thread owns one row (TMEM lane). Warps 2 and 3 count and merge the
-//   chunks' partials (chunks alternately), off the softmax warps' path.
-// * Softmax of one chunk (one key block): the row maximum over the block's valid keys (first
-//   pass over the S row in TMEM), then P = 2^(s * scale * log2 e - m) written back over S as bf16
-//   hi + lo (32 keys at a time into the same 32 columns), so the PV product (two MMAs, A = P from
-//   TMEM) keeps the output within 2e-3 relative RMS of the fp64 attend.
-// * Epilogue: the row's partial output O / l, scaled by a power of two so that its largest
-//   element lies in [2^14, 2^15), is stored as fp16 together with (log2-sum-exp, exponent).
-//   The stores are fenced one softmax phase later (by then they have landed), and the chunk goes
-//   to its merge warp: one atomic ticket per (token, kv head) counts the finished partials, and
-//   the chunk that completes a token merges its partials (fp32, log-sum-exp weights), writes the
-//   bf16 output and the log-sum-exp, and drops the merged partial lines from L2 without writing
-//   them back.
+//   token's partial slots and count; tokens are bucketed by block (shared-memory histogram,
+//   block scan, scatter). Tokens with no valid block get zero output here.
+// * Attend kernel (persistent, one CTA per SM): windows are taken in order and CTA i takes chunks
+//   [i C / G, (i + 1) C / G) of a window with C chunks, so every CTA works on the same few
+//   windows at a time and their Q rows and K / V images stay in L2. Warp 0 loads K and V of a
+//   (block, kv head) item (one 32 KiB copy each) into one of two buffers, writes each chunk's
+//   descriptor (tokens, partial slots, own-block key limits, the V image's exponent) into an
+//   8-deep ring and gathers the chunk's Q rows (one tensor copy per token: its G heads, both
+//   64-dim halves). Warp 1 (one thread) issues S(c) = Q K^T into TMEM buffer c % 2, then
+//   PV(c - 1), so the softmax of chunk c overlaps PV(c - 1) and S(c + 1). Warps 4-11 (two per
+//   TMEM lane quadrant, 64 keys each) take the softmax of chunk c, writing P as fp16 over S,
+//   then store chunk c - 1's partial while PV(c) runs.
+// * Softmax of one chunk (one key block): the row maximum over the block's valid keys (row
+//   maxima of the two key halves meet in shared memory), P = 2^(s * scale * log2 e - m) <= 1 as
+//   fp16 (one PV MMA per 16 keys against the fp16 V image). The partial is O / l (the image's
+//   V * 2^-e keeps it below 2^15) as fp16 with (log2-sum-exp, e).
+// * Merge kernel (one warp per (token, kv head)): the token's partials weighted by 2^(lse - max),
+//   the bf16 output and the log-sum-exp.
 // * TMEM (512 columns): S / P double buffer (2 x 128) and O double buffer (2 x 128).
 #include <algorithm>
-
-#include <cuda_fp16.h>
 
 #include "pbs_device.cuh"
 #include "pbs_internal.h"
@@ -58,15 +55,13 @@ constexpr int kGRows = 128;                     // MMA M: tokens x query heads o
 constexpr int kGThreads = 384;                  // 12 warps
 constexpr int kDescRing = 8;                    // chunk descriptors in flight
 constexpr int kGQBytes = kGRows * kHeadDim * 2;  // 32 KiB Q tile
-constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of the Q tile
+constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of a Q, K or V tile: [128 rows][128 B]
 constexpr int kGTile = 32768;                   // a block's K (or V) for one kv head
-constexpr int kRingBytes = 10240;               // merge ring of one merge warp: 5 x 2 KiB or 2 x 4 KiB
-constexpr int kMaxSlots = 5;
-constexpr int kTaskQ = 32;                      // completed tokens waiting for their merge, per merge warp
-constexpr int kGSmemBig = 2 * kGQBytes + 4 * kGTile + 2 * kRingBytes;  // Q x 2, K x 2, V x 2, 2 rings
+constexpr int kGSmemBig = 2 * kGQBytes + 4 * kGTile;  // Q x 2, K x 2, V x 2
 constexpr unsigned long long kGWaitNs = 100000000ull;  // waits here last microseconds: 100 ms cap
-constexpr int kIdxThreads = 256;
-constexpr int kGatherMaxSms = 1024;
+constexpr int kIdxThreads = 1024;                // index kernel: 32 warps, 8 tokens of a window each
+constexpr int kSoftWarpsG = 8;                  // softmax warps (4 - 11)
+constexpr int kMergeWarps = 8;                  // warps per merge CTA
 
 struct ChunkDesc {
   int32_t end;    // 1: no more work for this CTA
@@ -75,37 +70,30 @@ struct ChunkDesc {
   int32_t ybuf;   // K/V buffer of the item
   int32_t n_tok;  // tokens in this chunk
   int32_t item;   // the CTA's item number (phase of the K/V buffer barriers)
-  int32_t pad[2];
+  int32_t req;    // request (the item's images are those of (req, b, g))
+  int32_t pad;
   int32_t tr[16];    // segment-relative token index
   int32_t slot[16];  // the token's partial slot for block b
   int32_t lim[16];   // keys of block b the token sees (128, or pos - 128 b + 1 for its own block)
-  int32_t nsel[16];  // the token's number of partials
 };
 
 struct GCtl {
   uint64_t desc_full[kDescRing];
-  uint64_t desc_empty[kDescRing];  // 1 (MMA thread) + 1 (merge warp) arrivals
-  uint64_t part_done[kDescRing];   // the chunk's partials are stored and fenced: 4 softmax warps
+  // released by the MMA thread (PV issued), the V producer and the softmax warps (partial stored)
+  uint64_t desc_empty[kDescRing];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[2], v_full[2], v_land[2], kv_empty[2];
+  // K buffer Y is free once the S of its item's last chunk has completed, V buffer Y once its PV
+  // has: each is reloaded two items later, so both are fetched about two chunks ahead
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t o_free[2];    // O buffer X has been read (softmax warps -> MMA)
-  // item n's V is in fp16 (merge warp n % 2 -> MMA and softmax warps), one barrier per n % 4:
-  // item n + 4 needs the K/V buffer of item n + 2, freed only after every PV of item n + 2,
-  // which comes after the epilogues of item n
-  uint64_t vx_ready[4];
-  uint64_t ring_full[2][kMaxSlots];
+  uint64_t o_free[2];  // O buffer X has been read (softmax warps -> MMA)
   uint64_t mma_fin;
   uint32_t tmem_base;
   int32_t abort;
   ChunkDesc desc[kDescRing];
-  int32_t ents[128];  // bucket entries of the producer's current batch
-  alignas(16) int4 tq[2][kTaskQ];                     // merge tasks: (token, kv head, partials, 0)
-  float lsum[4][2][kGRows];                             // chunk c & 3, key half, row: partial sum
-  float xchg[2][2][kGRows];                            // row maxima of the two key halves
-  int32_t vexp[4];                                     // item n's V buffer holds V * 2^-vexp[n % 4]
-  int32_t items_total;                                 // items of this CTA (written before the end)
-  alignas(16) float2 ring_ml[2][kMaxSlots][16];       // (lse, exponent) of each ring slot's heads
+  int32_t ents[128];         // bucket entries of the producer's current batch
+  float lsum[4][2][kGRows];  // chunk c & 3, key half, row: partial sum
+  float xchg[2][2][kGRows];  // row maxima of the two key halves
 };
 
 // A batch of up to 8 consecutive chunks of one window (producer).
@@ -118,24 +106,19 @@ static_assert(kGSmem <= 232448, "shared memory layout exceeds 227 KiB");
 
 #ifdef PBS_TRACE
 // Trace build only: one CTA records SM-clock timestamps of the first kGtChunks chunks' pipeline
-// events (producer, MMA, softmax, epilogue, merge) and the number of merges per chunk.
+// events.
 constexpr int kGtChunks = 64;
-enum GTraceEv { kGtStart, kGtEnd, kGtProd = 2, kGtS = kGtProd + kGtChunks, kGtPV = kGtS + kGtChunks,
-                kGtSm0 = kGtPV + kGtChunks, kGtSm1 = kGtSm0 + kGtChunks, kGtE0 = kGtSm1 + kGtChunks,
-                kGtE1 = kGtE0 + kGtChunks, kGtM0 = kGtE1 + kGtChunks, kGtM1 = kGtM0 + kGtChunks,
-                kGtM2 = kGtM1 + kGtChunks, kGtNM = kGtM2 + kGtChunks, kGtCount = kGtNM + kGtChunks };
+enum GTraceEv { kGtStart, kGtEnd, kGtProd = 2, kGtK = kGtProd + kGtChunks, kGtV = kGtK + kGtChunks,
+                kGtS = kGtV + kGtChunks, kGtPV = kGtS + kGtChunks, kGtSm0 = kGtPV + kGtChunks,
+                kGtSm1 = kGtSm0 + kGtChunks, kGtE0 = kGtSm1 + kGtChunks, kGtE1 = kGtE0 + kGtChunks,
+                kGtCount = kGtE1 + kGtChunks };
 __device__ long long g_gtrace[kGtCount];
 __device__ int g_gtrace_cta;
 #define GTRACE(ev, c) do { if (blockIdx.x == static_cast<unsigned>(g_gtrace_cta) && (c) < kGtChunks) \
                              g_gtrace[(ev) + (c)] = clock64(); } while (0)
-#define GTRACE_VAL(ev, c, v) do { if (blockIdx.x == static_cast<unsigned>(g_gtrace_cta) && (c) < kGtChunks) \
-                                    g_gtrace[(ev) + (c)] = (v); } while (0)
 #else
 #define GTRACE(ev, c) do { } while (0)
-#define GTRACE_VAL(ev, c, v) do { } while (0)
 #endif
-
-__device__ __forceinline__ bool g_aborted(GCtl* ctl) { return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0; }
 
 __device__ __forceinline__ bool g_wait(uint64_t* bar, uint32_t parity, GCtl* ctl, int32_t* err) {
   if (mbar_wait_bounded(bar, parity, kGWaitNs)) return true;
@@ -149,14 +132,6 @@ __device__ __forceinline__ bool g_warp_wait(uint64_t* bar, uint32_t parity, GCtl
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void g_tma_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 __device__ __forceinline__ void g_tma_5d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2, int c3,
                                          int c4) {
   asm volatile(
@@ -166,17 +141,24 @@ __device__ __forceinline__ void g_tma_5d(void* dst, const void* tmap, uint64_t* 
       : "memory");
 }
 
-__device__ __forceinline__ void g_sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// 32 bytes to global memory in one store (32-byte aligned address).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
-// Drop a 128-byte line from L2 without writing it back (its contents become undefined).
-__device__ __forceinline__ void discard_l2(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+// The lower / upper half of an f16x2 word as float (exact).
+__device__ __forceinline__ float g_f16_lo(uint32_t x) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(x));
+  return f;
 }
-
-__device__ __forceinline__ float f16_lo(uint32_t x) { return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu))); }
-__device__ __forceinline__ float f16_hi(uint32_t x) { return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16))); }
+__device__ __forceinline__ float g_f16_hi(uint32_t x) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}" : "=f"(f) : "r"(x));
+  return f;
+}
 
 // Window of the segment [T0, T1) with index `wi`: windows are numbered request by request, each
 // request's tokens cut at multiples of kGatherWinTok from its first token. Warp-collective.
@@ -335,12 +317,9 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
         pairs_s[at] = (b1 << 14) | (tt << 6) | r1;
       }
     }
-    if (lane == 0) s_tn[tt] = n_t;
-    for (int g = lane; g < a.num_kv_heads; g += 32) {
-      const int64_t x = static_cast<int64_t>(tr) * a.num_kv_heads + g;
-      w.tickets[x] = 0;
-      // the merge task of (token, head): ready at once when there is nothing to merge
-      w.inbox[(x % w.n_mw) * w.inbox_cap + x / w.n_mw] = make_int4(tr, g, n_t, n_t == 0 ? 1 : 0);
+    if (lane == 0) {
+      s_tn[tt] = n_t;
+      w.nparts[tr] = n_t;  // the merge kernel's partial count for this token
     }
     if (n_t == 0) {
       // nothing to attend (no valid block, or a block past the page table): zero output
@@ -426,6 +405,7 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   }
 }
 
+
 // ------------------------------------------------------------------------------------------
 // attend kernel: persistent, one CTA per SM
 // ------------------------------------------------------------------------------------------
@@ -438,35 +418,29 @@ __global__ void __launch_bounds__(kGThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the 128B-swizzled operands need 1024-byte alignment
   uint8_t* big = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = big;                   // 2 x 32 KiB: [half][rows][128 B]
-  uint8_t* k_s = big + 2 * kGQBytes;    // 2 x 32 KiB: [page][row half][quarter][8 rows][128 B]
-  uint8_t* v_s = k_s + 2 * kGTile;      // 2 x 32 KiB
-  uint8_t* ring_s = v_s + 2 * kGTile;    // 2 x kRingBytes: partial rows being merged
-  GCtl* ctl = reinterpret_cast<GCtl*>(ring_s + 2 * kRingBytes);
+  uint8_t* q_s = big;                 // 2 x 32 KiB: [row atom][half][8 rows][128 B]
+  uint8_t* k_s = big + 2 * kGQBytes;  // 2 x 32 KiB: [half][128 keys][128 B]
+  uint8_t* v_s = k_s + 2 * kGTile;    // 2 x 32 KiB: [half][128 keys][128 B] (fp16 image)
+  GCtl* ctl = reinterpret_cast<GCtl*>(v_s + 2 * kGTile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&ctl->desc_full[i], 1);
-      mbar_init(&ctl->desc_empty[i], 2);
-      mbar_init(&ctl->part_done[i], 8);
+      mbar_init(&ctl->desc_empty[i], 2 + kSoftWarpsG);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
       mbar_init(&ctl->q_empty[i], 1);
       mbar_init(&ctl->k_full[i], 1);
+      mbar_init(&ctl->k_empty[i], 1);
       mbar_init(&ctl->v_full[i], 1);
-      mbar_init(&ctl->v_land[i], 1);
-      mbar_init(&ctl->kv_empty[i], 1);
+      mbar_init(&ctl->v_empty[i], 1);
       mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->p_full[i], 8);
+      mbar_init(&ctl->p_full[i], kSoftWarpsG);
       mbar_init(&ctl->pv_done[i], 1);
-      mbar_init(&ctl->o_free[i], 8);
-      mbar_init(&ctl->vx_ready[2 * i], 1);
-      mbar_init(&ctl->vx_ready[2 * i + 1], 1);
-      for (int j = 0; j < kMaxSlots; ++j) mbar_init(&ctl->ring_full[i][j], 1);
+      mbar_init(&ctl->o_free[i], kSoftWarpsG);
     }
-
     mbar_init(&ctl->mma_fin, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -479,13 +453,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (threadIdx.x == 0) GTRACE(kGtStart, 0);
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    // Windows in order; CTA i takes chunks [i C / G, (i + 1) C / G) of a window with C chunks,
-    // so every window is spread over the whole grid and its partials are merged while in L2.
+    // ---------------------------------------------------------------- producer (Q, K, descriptors)
+    // Windows in order; CTA i takes chunks [i C / G, (i + 1) C / G) of a window with C chunks.
     // Chunks go in batches of up to 8: the records of batch n + 2 and the bucket entries of
     // batch n + 1 are in flight while batch n is issued.
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
+      if (a.kconv == nullptr)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q_map)) : "memory");
     }
     const int cta = blockIdx.x, grid = gridDim.x;
@@ -550,7 +524,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     int n_item = -1, c = 0;
     int item_r = -1, item_b = -1, item_g = -1;
     // uses of each buffer so far (their barrier phases); scalars, so they stay in registers
-    int q_n0 = 0, q_n1 = 0, kv_n0 = 0, kv_n1 = 0, land_n0 = 0, land_n1 = 0;
+    int q_n0 = 0, q_n1 = 0, kv_n0 = 0, kv_n1 = 0;
     bool ok = true;
     Batch B0, B1, B2;
     next_batch(B0);
@@ -572,7 +546,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int b = rx & 8191, g = rx >> 13;
         const int n_tok = __shfl_sync(0xffffffffu, rec0.z, jc);
         const int phys = __shfl_sync(0xffffffffu, rec0.w, jc);
-        // ---- a new (request, block, kv head): K and V into the next buffer
+        // ---- a new (request, block, kv head): its K into the next K buffer (warp 3 loads V)
         if (B0.r != item_r || b != item_b || g != item_g) {
           ++n_item;
           item_r = B0.r;
@@ -581,51 +555,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int Y = n_item & 1;
           if (n_item >= 2) {
             bool go = true;
-            if (lane == 0) go = g_wait(&ctl->kv_empty[Y], ((n_item >> 1) - 1) & 1, ctl, a.err_word);
+            if (lane == 0) go = g_wait(&ctl->k_empty[Y], ((n_item >> 1) - 1) & 1, ctl, a.err_word);
             if (!__shfl_sync(0xffffffffu, go, 0)) {
               ok = false;
               break;
             }
           }
-          const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
-          if (lane == 0 && (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages))
-            set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-          const int last_rows = B0.seq_len - 1 - b * kSparseBlock + 1;  // rows of block b holding written tokens
-          const bool tail = last_rows < kSparseBlock;
-          uint64_t* vbar = tail ? &ctl->v_land[Y] : &ctl->v_full[Y];
           if (lane == 0) {
             mbar_arrive_expect_tx(&ctl->k_full[Y], kGTile);
-            mbar_arrive_expect_tx(vbar, kGTile);
-          }
-          __syncwarp();
-          // out-of-range pages read as zeros (tensor-map bounds)
-          if (lane < 2 * kPagesPerBlock) {
-            const int pg = lane & 7;
-            const bool isv = lane >= kPagesPerBlock;
-            g_tma_5d((isv ? v_s : k_s) + Y * kGTile + pg * 4096, &kv_map, isv ? vbar : &ctl->k_full[Y], 0, 0,
-                     isv ? 2 : 0, 0, static_cast<int>((pbase + pg) * a.num_kv_heads + g));
+            if (a.kconv != nullptr) {
+              const int64_t image = (static_cast<int64_t>(B0.r) * a.max_blocks + b) * a.num_kv_heads + g;
+              bulk_load(k_s + Y * kGTile, a.kconv + image * kGTile, kGTile, &ctl->k_full[Y]);
+            } else {
+              // one {64, 16 rows, head, 8 pages, K half} box; pages past the cache read as zeros
+              const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
+              if (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+              g_tma_5d(k_s + Y * kGTile, &kv_map, &ctl->k_full[Y], 0, 0, g, static_cast<int>(pbase), 0);
+            }
           }
           if (Y == 0) ++kv_n0; else ++kv_n1;
-          if (tail) {
-            // rows past the request's last token may hold anything (unwritten cache rows): zero
-            // them in V before any PV reads the buffer
-            const int ln = Y == 0 ? ++land_n0 : ++land_n1;
-            bool go = true;
-            if (lane == 0) go = g_wait(&ctl->v_land[Y], (ln - 1) & 1, ctl, a.err_word);
-            if (!__shfl_sync(0xffffffffu, go, 0)) {
-              ok = false;
-              break;
-            }
-            const uint32_t vb = smem_u32(v_s + Y * kGTile);
-            const int first = max(last_rows, 0);
-            for (int e = lane; e < (kSparseBlock - first) * 16; e += 32) {
-              const int key = first + (e >> 4), vq = (e >> 3) & 1, chn = e & 7;
-              g_sts128(vb + (key >> 3) * 2048 + vq * 1024 + (key & 7) * 128 + chn * 16, 0, 0, 0, 0);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->v_full[Y]);
-          }
+          if (lane == 0) GTRACE(kGtK, c);
         }
         // ---- the chunk's descriptor
         const int ds = c % kDescRing;
@@ -646,7 +595,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int pos = B0.ctx0 + (t - B0.c0);
           d->tr[lane] = tr;
           d->slot[lane] = en & 63;
-          d->nsel[lane] = ((en >> 6) & 63) + 1;
           d->lim[lane] = pos / kSparseBlock == b ? pos - b * kSparseBlock + 1 : kSparseBlock;
           t_lane = t;
         }
@@ -657,8 +605,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
           d->ybuf = n_item & 1;
           d->n_tok = n_tok;
           d->item = n_item;
+          d->req = B0.r;
         }
-        // ---- gather the chunk's Q rows: token j, half hf -> rows j*G.., dims 64 hf..
+        // ---- gather the chunk's Q rows: token j -> its G rows, one {64, 8, 2, G / 8, 1} copy
         const int qb = c & 1;
         if (c >= 2) {
           bool go = true;
@@ -670,12 +619,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         if (lane == 0) mbar_arrive_expect_tx(&ctl->q_full[qb], n_tok * 2 * kG * 128);
         __syncwarp();
-        {
-          const int j = lane % kTok, hf = lane / kTok;
-          const int tj = __shfl_sync(0xffffffffu, t_lane, j);
-          if (lane < 2 * kTok && j < n_tok)
-            g_tma_3d(q_s + qb * kGQBytes + hf * kGHalf + j * kG * 128, &q_map, &ctl->q_full[qb], hf * 64, g * kG, tj);
-        }
+        if (lane < n_tok)
+          g_tma_5d(q_s + qb * kGQBytes + lane * kG * 256, &q_map, &ctl->q_full[qb], 0, 0, 0, g * (kG / 8), t_lane);
         if (qb == 0) ++q_n0; else ++q_n1;
         __threadfence_block();
         __syncwarp();
@@ -689,16 +634,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
       B1 = B2;
       rec1 = rec2;
     }
-    // ---- end marks: chunks c and c + 1 (each merge warp takes every other chunk)
-    if (lane == 0) ctl->items_total = n_item + 1;
-    for (int e = 0; e < 2 && ok; ++e, ++c) {
+    // ---- end mark
+    if (ok) {
       const int ds = c % kDescRing;
-      if (c >= kDescRing) {
-        bool go = true;
-        if (lane == 0) go = g_wait(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1, ctl, a.err_word);
-        if (!__shfl_sync(0xffffffffu, go, 0)) break;
-      }
-      if (lane == 0) {
+      bool go = true;
+      if (c >= kDescRing && lane == 0) go = g_wait(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1, ctl, a.err_word);
+      if (__shfl_sync(0xffffffffu, go, 0) && lane == 0) {
         ctl->desc[ds].end = 1;
         __threadfence_block();
         mbar_arrive(&ctl->desc_full[ds]);
@@ -711,10 +652,35 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (q_n1 > 0) mbar_wait_bounded(&ctl->q_full[1], (q_n1 - 1) & 1, kGWaitNs);
       if (kv_n0 > 0) mbar_wait_bounded(&ctl->k_full[0], (kv_n0 - 1) & 1, kGWaitNs);
       if (kv_n1 > 0) mbar_wait_bounded(&ctl->k_full[1], (kv_n1 - 1) & 1, kGWaitNs);
-      if (kv_n0 > 0) mbar_wait_bounded(&ctl->v_full[0], (kv_n0 - 1) & 1, kGWaitNs);
-      if (kv_n1 > 0) mbar_wait_bounded(&ctl->v_full[1], (kv_n1 - 1) & 1, kGWaitNs);
-      if (land_n0 > 0) mbar_wait_bounded(&ctl->v_land[0], (land_n0 - 1) & 1, kGWaitNs);
-      if (land_n1 > 0) mbar_wait_bounded(&ctl->v_land[1], (land_n1 - 1) & 1, kGWaitNs);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- V producer
+    // Follows the descriptors: the first chunk of every item loads the item's fp16 V image into
+    // V buffer item % 2 once the PV of the item two before has completed.
+    int v_n0 = 0, v_n1 = 0, prev_item = -1;
+    for (int c = 0;; ++c) {
+      const int ds = c % kDescRing;
+      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+      const ChunkDesc* d = &ctl->desc[ds];
+      if (d->end) break;
+      const int item = d->item, Y = d->ybuf;
+      if (item != prev_item) {
+        prev_item = item;
+        if (item >= 2 && !g_warp_wait(&ctl->v_empty[Y], ((item >> 1) - 1) & 1, ctl, a.err_word)) break;
+        if (lane == 0) {
+          const int64_t image = (static_cast<int64_t>(d->req) * a.max_blocks + d->b) * a.num_kv_heads + d->g;
+          mbar_arrive_expect_tx(&ctl->v_full[Y], kGTile);
+          bulk_load(v_s + Y * kGTile, a.vconv + image * kGTile, kGTile, &ctl->v_full[Y]);
+          GTRACE(kGtV, c);
+        }
+        if (Y == 0) ++v_n0; else ++v_n1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);
+    }
+    if (lane == 0) {
+      if (v_n0 > 0) mbar_wait_bounded(&ctl->v_full[0], (v_n0 - 1) & 1, kGWaitNs);
+      if (v_n1 > 0) mbar_wait_bounded(&ctl->v_full[1], (v_n1 - 1) & 1, kGWaitNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -728,6 +694,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const ChunkDesc* d = &ctl->desc[ds];
         const int end = d->end;
         const int Y = d->ybuf, item = d->item;
+        // chunk c starts a new item (or there is none): the S of the previous item's last chunk,
+        // issued before, is the last reader of its K buffer
+        if (c >= 1 && (end || item != prev_item)) tc::commit(&ctl->k_empty[prev_y]);
         if (!end) {
           const int X = c & 1;
           // the K buffer of item n completes once per use: phase (n / 2) & 1
@@ -736,32 +705,36 @@ __global__ void __launch_bounds__(kGThreads, 1)
           tc::fence_after_sync();
           const uint32_t q_addr = smem_u32(q_s + X * kGQBytes);
           const uint32_t k_addr = smem_u32(k_s + Y * kGTile);
+          // dims 16ks..: Q half ks/4 1 KiB into each 2 KiB pair of 8-row atoms; K half ks/4 16 KiB
+          // apart, its 8-key groups 1 KiB apart
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ss(tmem + X * 128, tc::smem_desc_sw128(q_addr + (ks >> 2) * kGHalf + (ks & 3) * 32, 16, 1024),
-                       tc::smem_desc_sw128(k_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048), kIdescS, ks > 0);
+            tc::mma_ss(tmem + X * 128, tc::smem_desc_sw128(q_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048),
+                       tc::smem_desc_sw128(k_addr + (ks >> 2) * kGHalf + (ks & 3) * 32, 16, 1024), kIdescS, ks > 0);
           tc::commit(&ctl->s_full[X]);
           tc::commit(&ctl->q_empty[X]);
           GTRACE(kGtS, c);
         }
         if (c >= 1) {
           // PV of the previous chunk: O(X') = P V, P (fp16, two keys per column) in columns
-          // 0..63 of S buffer X', V the fp16 copy of the item's V
+          // 0..63 of S buffer X', V the item's fp16 image
           const int cp = c - 1, Xp = cp & 1;
           if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) break;
-          if (!g_wait(&ctl->vx_ready[prev_item & 3], (prev_item >> 2) & 1, ctl, a.err_word)) break;
+          if (!g_wait(&ctl->v_full[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
           // O buffer X' was read by the epilogue of chunk cp - 2
           if (cp >= 2 && !g_wait(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1, ctl, a.err_word)) break;
           tc::fence_after_sync();
           const uint32_t v_addr = smem_u32(v_s + prev_y * kGTile);
+          // keys 16ks..16ks+15 = two 8-key groups (1 KiB apart); dims in two 64-wide MN atoms
+          // 16 KiB apart
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             tc::mma_ts(tmem + 256 + Xp * 128, tmem + Xp * 128 + ks * 8,
-                       tc::smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), kIdescPV, ks > 0);
+                       tc::smem_desc_sw128(v_addr + ks * 2048, kGHalf, 1024), kIdescPV, ks > 0);
           tc::commit(&ctl->pv_done[Xp]);
           GTRACE(kGtPV, cp);
-          // the previous chunk was its item's last: its K/V buffer is free once this PV completes
-          if (end || item != prev_item) tc::commit(&ctl->kv_empty[prev_y]);
+          // the previous chunk was its item's last: its V buffer is free once this PV completes
+          if (end || item != prev_item) tc::commit(&ctl->v_empty[prev_y]);
           mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
         }
         if (end) break;
@@ -772,296 +745,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
       tc::commit(&ctl->mma_fin);
       mbar_wait_bounded(&ctl->mma_fin, 0, kGWaitNs);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ---------------------------------------------------------------- merge warps
-    // Warp 2 takes chunks 0, 2, ..., warp 3 chunks 1, 3, ...: once a chunk's partials are stored
-    // and fenced it releases the descriptor and counts one ticket per (token, kv head); a token
-    // whose count reaches its partial total is queued. Queued tokens' partials (and their
-    // (lse, exponent) pairs) stream through a ring of bulk copies and are merged with a running
-    // maximum, so loads for later partials are in flight while earlier ones are summed. The loop
-    // never blocks on one event while another could make progress.
-    const int m = warp - 2;
-    constexpr int kSlotBytes = kG * kHeadDim * 2;  // one partial of one (token, kv head)
-    constexpr int kSlots = kRingBytes / kSlotBytes;
-    static_assert(kSlots <= kMaxSlots, "ring slots");
-    constexpr int kLanesPerHead = 32 / kG;
-    constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
-    uint8_t* ring = ring_s + m * kRingBytes;
-    float2* rml = &ctl->ring_ml[m][0][0];
-    uint64_t* rfull = ctl->ring_full[m];
-    int4* tq = ctl->tq[m];
-    const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
-    const int hkv = a.num_kv_heads;
-    // this warp's inbox: the tasks x = token * Hkv + head with x % n_mw == me, in order of x
-    const int me = static_cast<int>(blockIdx.x) * 2 + m;
-    const int64_t n_x = static_cast<int64_t>(w.T1 - w.T0) * hkv;
-    const int expected = static_cast<int>(n_x / w.n_mw + (n_x % w.n_mw > me ? 1 : 0));
-    const int4* inbox = w.inbox + static_cast<int64_t>(me) * w.inbox_cap;
-    int head = 0;
-    int conv_n = m;  // next item whose V this warp converts (items m, m + 2, ... use V buffer m)
-    int c = m;
-    bool end_seen = false, have_atom = false;
-    int at_old = 0, at_tr = 0, at_nsel = 0, at_g = 0, at_n = 0;
-    int tq_tail = 0;                          // tokens queued
-    int iss_task = 0, iss_j = 0, ri_iss = 0;  // next partial to load (task, slot, ring sequence)
-    int con_task = 0, con_j = 0, ri_con = 0;  // next partial to merge
-    float acc[kE];
-#pragma unroll
-    for (int i = 0; i < kE; ++i) acc[i] = 0.f;
-    float L = -INFINITY, den = 0.f;
-    unsigned long long idle_t0 = 0;
-    bool failed = false;
-    while (true) {
-      bool progress = false;
-      // (0) the V of this warp's next item, once it has landed: converted in place to fp16 as
-      // V * 2^-e, e putting max |V| at 2^14..2^15 (exact: bf16 has 8 significant bits, fp16 keeps
-      // 29 binades below that maximum), for the single fp16 PV MMA
-      {
-        bool landed = false;
-        if (lane == 0) landed = mbar_try_wait(&ctl->v_full[m], (conv_n >> 1) & 1);
-        landed = __shfl_sync(0xffffffffu, landed, 0);
-        if (landed) landed = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->v_full[m], (conv_n >> 1) & 1, kGWaitNs));
-        if (landed) {
-          const uint32_t vb = smem_u32(v_s + m * kGTile);
-          uint32_t mxv = 0;
-#pragma unroll 8
-          for (int q = 0; q < kGTile / 16 / 32; ++q) {
-            uint32_t x0, x1, x2, x3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                         : "r"(vb + (lane + 32 * q) * 16));
-            // |bf16| bit patterns compare like the magnitudes
-            mxv = max(mxv, max(max(x0 & 0x7fff7fffu, x1 & 0x7fff7fffu), max(x2 & 0x7fff7fffu, x3 & 0x7fff7fffu)) >> 16);
-            mxv = max(mxv, max(max(x0 & 0x7fffu, x1 & 0x7fffu), max(x2 & 0x7fffu, x3 & 0x7fffu)));
-          }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mxv = max(mxv, __shfl_xor_sync(0xffffffffu, mxv, off));
-          const float vm = __uint_as_float(mxv << 16);
-          int e = 0;
-          if (vm > 0.f) e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 127 - 14;
-          e = max(-100, min(100, e));
-          const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-#pragma unroll 8
-          for (int q = 0; q < kGTile / 16 / 32; ++q) {
-            const uint32_t ad = vb + (lane + 32 * q) * 16;
-            uint32_t x0, x1, x2, x3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(ad));
-            g_sts128(ad, pack_f16(bf16_lo(x0) * sc, bf16_hi(x0) * sc), pack_f16(bf16_lo(x1) * sc, bf16_hi(x1) * sc),
-                     pack_f16(bf16_lo(x2) * sc, bf16_hi(x2) * sc), pack_f16(bf16_lo(x3) * sc, bf16_hi(x3) * sc));
-          }
-          // the tensor core reads the copy through the async proxy
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          if (lane == 0) ctl->vexp[conv_n & 3] = e;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->vx_ready[conv_n & 3]);
-          conv_n += 2;
-          progress = true;
-        }
-      }
-      // the tickets of the last chunk taken (their atomics were issued one step earlier, so the
-      // round trip is mostly over): a token that is now complete is announced to its merge warp
-      // (the fence orders every partial the ticket counted before the flag)
-      auto resolve_tickets = [&]() {
-        const bool done = lane < at_n && at_old + 1 == at_nsel;
-        const uint32_t dm = __ballot_sync(0xffffffffu, done);
-        if (dm) {
-          __threadfence();
-          if (done) {
-            const int64_t x = static_cast<int64_t>(at_tr) * hkv + at_g;
-            int* flag = reinterpret_cast<int*>(w.inbox + (x % w.n_mw) * w.inbox_cap + x / w.n_mw) + 3;
-            asm volatile("st.volatile.global.s32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
-          }
-        }
-        have_atom = false;
-      };
-      // (1) the next chunk, once its partials are fenced
-      if (!end_seen) {
-        const int ds = c % kDescRing;
-        const uint32_t ph = (c / kDescRing) & 1;
-        bool got = false;
-        if (lane == 0) got = mbar_try_wait(&ctl->desc_full[ds], ph);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        // once lane 0 has seen the phase complete, every lane waits on it (returns at once) so
-        // that each lane's reads of the descriptor are ordered after it
-        if (got) got = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->desc_full[ds], ph, kGWaitNs));
-        if (got) {
-          const ChunkDesc* d = &ctl->desc[ds];
-          if (d->end) {
-            end_seen = true;
-            progress = true;
-          } else {
-            bool pd = false;
-            if (lane == 0) pd = mbar_try_wait(&ctl->part_done[ds], ph);
-            pd = __shfl_sync(0xffffffffu, pd, 0);
-            if (pd) pd = __all_sync(0xffffffffu, mbar_wait_bounded(&ctl->part_done[ds], ph, kGWaitNs));
-            if (pd) {
-              if (have_atom) resolve_tickets();
-              if (lane == 0) GTRACE(kGtM0, c);
-              at_g = d->g;
-              at_n = d->n_tok;
-              at_tr = lane < at_n ? d->tr[lane] : 0;
-              at_nsel = lane < at_n ? d->nsel[lane] : 0;
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);
-              // the softmax warps fenced the partials before announcing them
-              at_old = lane < at_n ? atomicAdd(w.tickets + static_cast<int64_t>(at_tr) * hkv + at_g, 1) : -2;
-              have_atom = true;
-              c += 2;
-              progress = true;
-            }
-          }
-        }
-      }
-      if (end_seen && have_atom) {
-        resolve_tickets();
-        progress = true;
-      }
-      // (2) bulk loads of queued partials while the ring has room
-      while (ri_iss - ri_con < kSlots && iss_task < tq_tail) {
-        const int4 t = tq[iss_task % kTaskQ];
-        const int slot = ri_iss % kSlots;
-        const int64_t pidx = (static_cast<int64_t>(t.x) * hkv + t.y) * a.k + iss_j;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&rfull[slot], kSlotBytes + kG * 8);
-          bulk_load(ring + slot * kSlotBytes, w.part + pidx * kG * kHeadDim, kSlotBytes, &rfull[slot]);
-          bulk_load(rml + slot * 16, w.ml + pidx * kG, kG * 8, &rfull[slot]);
-        }
-        if (++iss_j == t.z) {
-          iss_j = 0;
-          ++iss_task;
-        }
-        ++ri_iss;
-        progress = true;
-      }
-      // (3) merge every landed partial
-      while (ri_con < ri_iss) {
-        const int slot = ri_con % kSlots;
-        bool rdy = false;
-        if (lane == 0) rdy = mbar_try_wait(&rfull[slot], (ri_con / kSlots) & 1);
-        rdy = __shfl_sync(0xffffffffu, rdy, 0);
-        if (rdy) rdy = __all_sync(0xffffffffu, mbar_wait_bounded(&rfull[slot], (ri_con / kSlots) & 1, kGWaitNs));
-        if (rdy) {
-          const float2 me = rml[slot * 16 + h];
-          if (me.x > L) {
-            const float sc = ex2(L - me.x);  // 0 while nothing is accumulated
-            den *= sc;
-#pragma unroll
-            for (int i = 0; i < kE; ++i) acc[i] *= sc;
-            L = me.x;
-          }
-          den += ex2(me.x - L);
-          const float f = ex2(me.x - L + me.y);
-          const uint32_t src = smem_u32(ring + slot * kSlotBytes + (h * kHeadDim + d0) * 2);
-#pragma unroll
-          for (int q = 0; q < kE / 8; ++q) {
-            uint32_t x0, x1, x2, x3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                         : "r"(src + 16 * q));
-            acc[8 * q + 0] = fmaf(f, f16_lo(x0), acc[8 * q + 0]);
-            acc[8 * q + 1] = fmaf(f, f16_hi(x0), acc[8 * q + 1]);
-            acc[8 * q + 2] = fmaf(f, f16_lo(x1), acc[8 * q + 2]);
-            acc[8 * q + 3] = fmaf(f, f16_hi(x1), acc[8 * q + 3]);
-            acc[8 * q + 4] = fmaf(f, f16_lo(x2), acc[8 * q + 4]);
-            acc[8 * q + 5] = fmaf(f, f16_hi(x2), acc[8 * q + 5]);
-            acc[8 * q + 6] = fmaf(f, f16_lo(x3), acc[8 * q + 6]);
-            acc[8 * q + 7] = fmaf(f, f16_hi(x3), acc[8 * q + 7]);
-          }
-          // the slot's generic reads precede the next bulk write into it
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          ++ri_con;
-          const int4 t = tq[con_task % kTaskQ];
-          if (++con_j == t.z) {
-            // the token is complete: output rows and log-sum-exp, then drop its partial lines
-            const int tt = w.T0 + t.x;
-            const float inv = a.v_scale / den;
-            uint16_t* dst = a.out + static_cast<int64_t>(tt) * a.out_row_stride +
-                            static_cast<int64_t>(t.y * kG + h) * a.out_head_stride + d0;
-#pragma unroll
-            for (int q = 0; q < kE / 8; ++q)
-              *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(
-                  pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
-                  pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
-            if (a.lse != nullptr && (lane % kLanesPerHead) == 0)
-              a.lse[static_cast<int64_t>(tt) * a.lse_row_stride + t.y * kG + h] = (L + log2f(den)) * kLn2;
-            if ((d0 & 63) == 0) {
-              const uint16_t* pp = w.part + ((static_cast<int64_t>(t.x) * hkv + t.y) * a.k * kG + h) * kHeadDim + d0;
-              for (int j = 0; j < t.z; ++j) discard_l2(pp + static_cast<int64_t>(j) * kG * kHeadDim);
-            }
-#pragma unroll
-            for (int i = 0; i < kE; ++i) acc[i] = 0.f;
-            L = -INFINITY;
-            den = 0.f;
-            con_j = 0;
-            ++con_task;
-          }
-          progress = true;
-        } else {
-          break;
-        }
-      }
-      // (5) this warp's inbox: the leading run of ready tasks joins the merge queue
-      if (head < expected && tq_tail - con_task < 4) {
-        const int room = kTaskQ - (tq_tail - con_task);
-        const int p = head + lane;
-        int flag = 0;
-        if (lane < room && p < expected)
-          asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(flag) : "l"(reinterpret_cast<const int*>(inbox + p) + 3));
-        const uint32_t ready = __ballot_sync(0xffffffffu, flag != 0);
-        const int run = ready == 0xffffffffu ? 32 : __ffs(~ready) - 1;
-        if (run > 0) {
-          // acquire the partials the flags announce, for the generic and the bulk-copy proxy
-          __threadfence();
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          int4 e = make_int4(0, 0, 0, 0);
-          if (lane < run) e = __ldcg(inbox + p);
-          const bool real = lane < run && e.z > 0;  // tasks with nothing to merge are dropped
-          const uint32_t rm = __ballot_sync(0xffffffffu, real);
-          if (real) tq[(tq_tail + __popc(rm & lanemask_lt())) % kTaskQ] = make_int4(e.x, e.y, e.z, 0);
-          tq_tail += __popc(rm);
-          head += run;
-          __syncwarp();
-          progress = true;
-        }
-      }
-      if (end_seen && !have_atom && head == expected && con_task == tq_tail && ri_con == ri_iss &&
-          conv_n >= *reinterpret_cast<volatile int32_t*>(&ctl->items_total))
-        break;
-      if (progress) {
-        idle_t0 = 0;
-      } else {
-        __nanosleep(64);
-        const unsigned long long now = global_timer_ns();
-        if (idle_t0 == 0) {
-          idle_t0 = now;
-        } else if (now - idle_t0 > kGWaitNs) {
-          failed = true;
-          break;
-        }
-      }
-    }
-    if (failed && lane == 0) {
-      set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-      atomicExch(&ctl->abort, 1);
-    }
-    // copies still in flight (only after a give-up) must land before the CTA exits
-    if (lane == 0)
-      for (int r = ri_con; r < ri_iss; ++r) mbar_wait_bounded(&rfull[r % kSlots], (r / kSlots) & 1, kGWaitNs);
-  } else {
-    // ---------------------------------------------------------------- softmax + epilogue
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax + partials
     // Warps 4-11 take every chunk in turn, two warps per 32-lane TMEM quadrant: warp part p owns
     // key columns [64 p, 64 p + 64) of S and head-dim columns [64 p, 64 p + 64) of O. The two
-    // parts' row maxima meet in shared memory;
-    // P (fp16, two keys per column) goes to columns 32 p .. 32 p + 31 of the same S buffer once
-    // both parts have read their S columns. Then the partial of chunk c - 1 (O / l as fp16 with
-    // its item's V exponent) is stored while PV(c) runs.
+    // parts' row maxima meet in shared memory; P (fp16, two keys per column) goes to columns
+    // 32 p .. 32 p + 31 of the same S buffer once both parts have read their S columns. Then the
+    // partial of chunk c - 1 (O / l as fp16, with (log2-sum-exp, V exponent)) is stored while
+    // PV(c) runs.
     const int sw = warp - 4, quad = sw & 3, part = sw >> 2;
     const int row = quad * 32 + lane;  // TMEM lane
     const int j = row / kG, h = row % kG;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = a.scale_log2;
     float m_prev = 0.f, l_prev = 0.f;  // chunk c - 1: row maximum (log2 units), this part's sum
-    int pending = -1;                  // chunk whose partial stores are not yet fenced
+    int e_prev = 0;                    // chunk c - 1: its V image holds V * 2^-e
     const ChunkDesc* dprev = nullptr;
     for (int c = 0;; ++c) {
       const int ds = c % kDescRing, X = c & 1;
@@ -1069,6 +767,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const ChunkDesc* d = &ctl->desc[ds];
       const bool end = d->end != 0;
       uint32_t v[64];
+      // the exponent of this chunk's V image, for its partial one iteration later
+      const int e_cur = end ? 0 : __ldg(a.vconv_exp + (static_cast<int64_t>(d->req) * a.max_blocks + d->b) *
+                                                          a.num_kv_heads + d->g);
       if (!end) {
         if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
         tc::fence_after_sync();
@@ -1122,7 +823,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         tc::st32(tmem + X * 128 + lane_off + 32 * part, pk);
         lp = l0 + l1;
-        // four slots: the partner reads slot c & 3 after the next chunk's quad barrier
+        // four slots: the partner reads slot c & 3 in the next iteration
         ctl->lsum[c & 3][part][row] = lp;
         tc::wait_st();
         tc::fence_before_sync();
@@ -1132,19 +833,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
       // ---- partial of chunk c - 1
       if (c >= 1) {
-        // the chunk before it, stored an iteration ago, is fenced and handed to its merge warp
-        if (pending >= 0) {
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
-          pending = -1;
-        }
-        if (sw == 0 && lane == 0) GTRACE(kGtE0, c - 1);
         // O(c - 1), read once P(c) is out (so PV(c) is not held up, and S and O never share the
         // registers)
         uint32_t o[64];
         if (!g_warp_wait(&ctl->pv_done[X ^ 1], ((c - 1) >> 1) & 1, ctl, a.err_word)) break;
         tc::fence_after_sync();
+        if (sw == 0 && lane == 0) GTRACE(kGtE0, c - 1);
         const uint32_t to = tmem + 256 + (X ^ 1) * 128 + lane_off + 64 * part;
         tc::ld32(to, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
         tc::ld32(to + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
@@ -1153,39 +847,35 @@ __global__ void __launch_bounds__(kGThreads, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->o_free[X ^ 1]);
-        const int itp = dprev->item;
-        if (!g_warp_wait(&ctl->vx_ready[itp & 3], (itp >> 2) & 1, ctl, a.err_word)) break;
-        const int e = ctl->vexp[itp & 3];
         const float lt = l_prev + ctl->lsum[(c - 1) & 3][part ^ 1][row];
         const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-        const bool valid = j < dprev->n_tok;
-        if (valid) {
+        if (j < dprev->n_tok) {
           const int64_t prow =
               ((static_cast<int64_t>(dprev->tr[j]) * a.num_kv_heads + dprev->g) * a.k + dprev->slot[j]) * kG + h;
+          // 128 bytes of the row as four 32-byte stores: every store fills whole sectors
           uint16_t* dst = w.part + prow * kHeadDim + 64 * part;
 #pragma unroll
-          for (int q8 = 0; q8 < 8; ++q8) {
-            const uint32_t* f = &o[8 * q8];
-            *reinterpret_cast<uint4*>(dst + 8 * q8) = make_uint4(
-                pack_f16(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l),
-                pack_f16(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l),
-                pack_f16(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l),
-                pack_f16(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l));
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t* f = &o[16 * q];
+            uint32_t wv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              wv[i] = pack_f16(__uint_as_float(f[2 * i]) * inv_l, __uint_as_float(f[2 * i + 1]) * inv_l);
+            st_global_v8(dst + 16 * q, wv);
           }
-          if (part == 0) *reinterpret_cast<float2*>(w.ml + prow) = make_float2(m_prev + log2f(lt), static_cast<float>(e));
+          if (part == 0)
+            w.ml[prow] = make_float2(m_prev + log2f(lt), static_cast<float>(e_prev));
         }
+        // this warp is done with descriptor c - 1
         if (sw == 0 && lane == 0) GTRACE(kGtE1, c - 1);
-        pending = c - 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->desc_empty[(c - 1) % kDescRing]);
       }
       if (end) break;
       m_prev = m;
       l_prev = lp;
+      e_prev = e_cur;
       dprev = d;
-    }
-    if (pending >= 0) {
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->part_done[pending % kDescRing]);
     }
   }
   tc::fence_before_sync();
@@ -1195,6 +885,61 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc::dealloc(tmem, 512);
   }
   if (threadIdx.x == 0) GTRACE(kGtEnd, 0);
+}
+
+// ------------------------------------------------------------------------------------------
+// merge kernel: one warp per (segment token, kv head)
+// ------------------------------------------------------------------------------------------
+// The token's n partials P_s (O_s / l_s stored as fp16 times 2^-e_s) and their base-2
+// log-sum-exps L_s combine to out = v_scale * sum_s 2^(L_s - M) 2^e_s P_s / sum_s 2^(L_s - M)
+// with M = max_s L_s; the row's log-sum-exp is M + log2(sum_s 2^(L_s - M)) (times ln 2).
+template <int kG>
+__global__ void __launch_bounds__(kMergeWarps * 32) gather_merge_kernel(const AttendArgs a, const GatherWs w) {
+  constexpr int kLanesPerHead = 32 / kG;        // 4 (GQA 8) or 2 (GQA 16)
+  constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
+  const int lane = threadIdx.x & 31;
+  const int hkv = a.num_kv_heads;
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (x >= static_cast<int64_t>(w.T1 - w.T0) * hkv) return;
+  const int tr = static_cast<int>(x / hkv), g = static_cast<int>(x % hkv);
+  const int n = __ldg(w.nparts + tr);
+  if (n <= 0) return;  // the index kernel wrote this token's zero output
+  const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
+  const int64_t prow0 = x * a.k * kG + h;  // partial row of slot s: prow0 + s * kG
+  float M = -INFINITY;
+  for (int s = 0; s < n; ++s) M = fmaxf(M, __ldg(&w.ml[prow0 + static_cast<int64_t>(s) * kG].x));
+  float L = 0.f;
+  float acc[kE];
+#pragma unroll
+  for (int i = 0; i < kE; ++i) acc[i] = 0.f;
+  for (int s = 0; s < n; ++s) {
+    const int64_t prow = prow0 + static_cast<int64_t>(s) * kG;
+    const float2 ml = __ldg(&w.ml[prow]);
+    const float wl = exp2f(ml.x - M);
+    L += wl;
+    const float f = wl * exp2f(ml.y);
+    const uint4* src = reinterpret_cast<const uint4*>(w.part + prow * kHeadDim + d0);
+#pragma unroll
+    for (int q = 0; q < kE / 8; ++q) {
+      const uint4 u = __ldg(src + q);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[8 * q + 2 * i] = fmaf(f, g_f16_lo(wd[i]), acc[8 * q + 2 * i]);
+        acc[8 * q + 2 * i + 1] = fmaf(f, g_f16_hi(wd[i]), acc[8 * q + 2 * i + 1]);
+      }
+    }
+  }
+  const float inv = a.v_scale / L;
+  const int64_t t = static_cast<int64_t>(w.T0) + tr;
+  uint16_t* dst = a.out + t * a.out_row_stride + static_cast<int64_t>(g * kG + h) * a.out_head_stride + d0;
+#pragma unroll
+  for (int q = 0; q < kE / 8; ++q)
+    *reinterpret_cast<uint4*>(dst + 8 * q) =
+        make_uint4(pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                   pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+  if (a.lse != nullptr && lane % kLanesPerHead == 0)
+    a.lse[t * a.lse_row_stride + g * kG + h] = (M + log2f(L)) * kLn2;
 }
 
 }  // namespace
@@ -1214,19 +959,25 @@ namespace pbs {
 #endif
 
 bool prefill_gather_supported(const AttendArgs& a) {
-  // buckets are built from top-k ids; a prebuilt table carries page ids only
-  return a.sparse_bt == nullptr && a.kv_dtype == PBS_KV_BF16 && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
-         a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192 &&
-         a.num_pages * a.num_kv_heads <= 0x7fffffffLL && a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 &&
-         reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 &&
-         reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
+  // buckets are built from top-k ids (a prebuilt table carries page ids only); a bf16 K comes
+  // through the per-block map of a packed cache, fp8 / NVFP4 K and V from converted images
+  const bool cache_ok =
+      a.kv_dtype != PBS_KV_BF16 || a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192;
+  return a.sparse_bt == nullptr && cache_ok && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
+         a.num_reqs <= 65535 && a.num_pages * a.num_kv_heads <= 0x7fffffffLL && a.out_head_stride % 8 == 0 &&
+         a.out_row_stride % 8 == 0 && reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 &&
+         a.q_row_stride % 8 == 0 && reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
 }
 
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The workspace: the conversion kernels' images (V and its exponents, then K, for every (request,
+// block, kv head); the K images are used by fp8 / NVFP4 caches only), then per segment the
+// partials, their (log2-sum-exp, exponent) pairs, each token's partial count, the bucket entries,
+// the chunk records and the window records.
 struct GatherLayout {
-  size_t part, ml, tickets, pairs, chunks, wins, inbox, total;
+  size_t images, part, ml, nparts, pairs, chunks, wins, total;
   int num_win, ccap;
 };
 
@@ -1241,21 +992,20 @@ GatherLayout gather_layout(int64_t seg_tokens, int num_reqs, int num_heads, int 
   const int64_t buckets = std::min<int64_t>(max_blocks, entries);
   L.ccap = static_cast<int>(((entries + buckets * (tok - 1)) / tok + 1) * num_kv_heads);
   size_t off = 0;
+  L.images = off;
+  off = align256(off + prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, PBS_KV_FP8_E4M3));
   L.part = off;
   off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * kHeadDim * 2);
   L.ml = off;
   off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * 8);
-  L.tickets = off;
-  off = align256(off + static_cast<size_t>(seg_tokens) * num_kv_heads * 4);
+  L.nparts = off;
+  off = align256(off + static_cast<size_t>(seg_tokens) * 4);
   L.pairs = off;
   off = align256(off + static_cast<size_t>(L.num_win) * kGatherWinTok * k * 4);
   L.chunks = off;
   off = align256(off + static_cast<size_t>(L.num_win) * L.ccap * 16);
   L.wins = off;
   off = align256(off + static_cast<size_t>(L.num_win) * 8 * 4);
-  // merge tasks: one per (token, kv head), plus one task of rounding per merge warp
-  L.inbox = off;
-  off = align256(off + (static_cast<size_t>(seg_tokens) * num_kv_heads + 2 * kGatherMaxSms) * 16);
   L.total = off;
   return L;
 }
@@ -1263,11 +1013,13 @@ GatherLayout gather_layout(int64_t seg_tokens, int num_reqs, int num_heads, int 
 
 size_t gather_workspace_bytes(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k,
                               int max_blocks) {
+  if (prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, PBS_KV_FP8_E4M3) == 0) return 0;
   return gather_layout(seg_tokens, num_reqs, num_heads, num_kv_heads, k, max_blocks).total;
 }
 
 int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks,
                               size_t ws_bytes) {
+  if (gather_workspace_bytes(kGatherWinTok, num_reqs, num_heads, num_kv_heads, k, max_blocks) == 0) return 0;
   if (total_q <= kGatherMaxSegment &&
       gather_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, k, max_blocks) <= ws_bytes)
     return total_q;
@@ -1284,57 +1036,58 @@ int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int 
 }
 
 template <int kG>
-cudaError_t launch_gather_g(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
+cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
                             size_t ws_bytes, cudaStream_t stream) {
-  const int64_t seg = gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k, a.max_blocks,
-                                            ws_bytes);
+  const int64_t seg = gather_segment_tokens(args.num_rows, args.num_reqs, args.num_heads, args.num_kv_heads, args.k,
+                                            args.max_blocks, ws_bytes);
   if (seg <= 0) return cudaErrorInvalidValue;
-  const GatherLayout L = gather_layout(seg, a.num_reqs, a.num_heads, a.num_kv_heads, a.k, a.max_blocks);
+  const GatherLayout L = gather_layout(seg, args.num_reqs, args.num_heads, args.num_kv_heads, args.k, args.max_blocks);
   uint8_t* base = static_cast<uint8_t*>(ws);
+  // the images: V (fp16) and its exponents for every cache format, K (bf16) for fp8 / NVFP4
+  AttendArgs a = args;
+  const int64_t n_img = static_cast<int64_t>(a.num_reqs) * a.max_blocks * a.num_kv_heads;
+  a.vconv = base + L.images;
+  a.vconv_exp = reinterpret_cast<int32_t*>(a.vconv + n_img * kTileVBytes);
+  a.kconv = a.kv_dtype == PBS_KV_BF16 ? nullptr : a.vconv + n_img * kTileVBytes + ((n_img * 4 + 255) / 256) * 256;
+  cudaError_t e = launch_convert_images(a, stream);
+  if (e != cudaSuccess) return e;
+
   GatherWs w = {};
   w.part = reinterpret_cast<uint16_t*>(base + L.part);
   w.ml = reinterpret_cast<float2*>(base + L.ml);
-  w.tickets = reinterpret_cast<int32_t*>(base + L.tickets);
+  w.nparts = reinterpret_cast<int32_t*>(base + L.nparts);
   w.pairs = reinterpret_cast<int32_t*>(base + L.pairs);
   w.chunks = reinterpret_cast<int4*>(base + L.chunks);
   w.wins = reinterpret_cast<int32_t*>(base + L.wins);
   w.ccap = L.ccap;
   w.tok_per_chunk = kGRows / kG;
-  w.inbox = reinterpret_cast<int4*>(base + L.inbox);
 
   const size_t idx_smem = static_cast<size_t>(2 * a.max_blocks + kGatherWinTok * a.k) * 4;
-  cudaError_t e = cudaFuncSetAttribute(gather_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(idx_smem));
+  e = cudaFuncSetAttribute(gather_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(idx_smem));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(gather_attend_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kGSmem));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  sms = std::min(sms, kGatherMaxSms);
-  // merge warps wait for tasks other CTAs announce, so every CTA must be resident: a
-  // cooperative launch of one CTA per SM guarantees that
-  w.n_mw = 2 * sms;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   for (int64_t t0 = 0; t0 < a.num_rows; t0 += seg) {
     w.T0 = static_cast<int32_t>(t0);
     w.T1 = static_cast<int32_t>(std::min<int64_t>(a.num_rows, t0 + seg));
     w.num_win = static_cast<int32_t>((w.T1 - w.T0) / kGatherWinTok + 2 * static_cast<int64_t>(a.num_reqs) + 1);
-    w.inbox_cap = static_cast<int32_t>((static_cast<int64_t>(w.T1 - w.T0) * a.num_kv_heads + w.n_mw - 1) / w.n_mw);
     gather_index_kernel<<<w.num_win, kIdxThreads, idx_smem, stream>>>(a, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sms));
-    cfg.blockDim = dim3(kGThreads);
-    cfg.dynamicSmemBytes = kGSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gather_attend_kernel<kG>, kv_map, q_map, a, w);
+    gather_attend_kernel<kG><<<static_cast<unsigned>(std::max(sms, 1)), kGThreads, kGSmem, stream>>>(kv_map, q_map,
+                                                                                                      a, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t units = static_cast<int64_t>(w.T1 - w.T0) * a.num_kv_heads;
+    gather_merge_kernel<kG><<<static_cast<unsigned>((units + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0,
+                              stream>>>(a, w);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

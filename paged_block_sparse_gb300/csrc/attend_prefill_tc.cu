@@ -1439,6 +1439,15 @@ extern "C" __attribute__((visibility("default"))) int pbs_debug_trace_get(long l
 namespace pbs {
 #endif
 
+cudaError_t launch_convert_images(const AttendArgs& a, cudaStream_t stream) {
+  const dim3 cgrid(static_cast<unsigned>(a.max_blocks), static_cast<unsigned>(a.num_reqs),
+                   static_cast<unsigned>(a.num_kv_heads));
+  if (a.kv_dtype == PBS_KV_FP8_E4M3) convert_kv_kernel<PBS_KV_FP8_E4M3><<<cgrid, 128, 0, stream>>>(a);
+  else if (a.kv_dtype == PBS_KV_NVFP4) convert_kv_kernel<PBS_KV_NVFP4><<<cgrid, 128, 0, stream>>>(a);
+  else convert_v_kernel<<<cgrid, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 bool prefill_tc_supported(const AttendArgs& a, bool with_workspace) {
   // bf16: K (and V without a workspace) through the block map of a packed cache; fp8 / NVFP4: K
   // and V from images the conversion kernel writes into the workspace
@@ -1462,12 +1471,7 @@ cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUte
   if (e != cudaSuccess) return e;
   if (kF16V) {
     // the images the attend streams: V (bf16 caches; K comes through the block map), or K and V
-    const dim3 cgrid(static_cast<unsigned>(a.max_blocks), static_cast<unsigned>(a.num_reqs),
-                     static_cast<unsigned>(a.num_kv_heads));
-    if (a.kv_dtype == PBS_KV_FP8_E4M3) convert_kv_kernel<PBS_KV_FP8_E4M3><<<cgrid, 128, 0, stream>>>(a);
-    else if (a.kv_dtype == PBS_KV_NVFP4) convert_kv_kernel<PBS_KV_NVFP4><<<cgrid, 128, 0, stream>>>(a);
-    else convert_v_kernel<<<cgrid, 128, 0, stream>>>(a);
-    e = cudaGetLastError();
+    e = launch_convert_images(a, stream);
     if (e != cudaSuccess) return e;
   }
   // one CTA per SM; at most one per tile (an upper bound: tiles are counted on the device)

@@ -127,12 +127,14 @@ size_t prefill_tc_workspace_bytes(int64_t num_reqs, int64_t num_kv_heads, int64_
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                               cudaStream_t stream);
 
-// Prefill attend by key block (tcgen05, bf16 packed cache, GQA 8 or 16): an index kernel
-// buckets each 256-token window's tokens by selected block, a persistent kernel attends every
-// (block, kv head) bucket 16 gathered tokens at a time and merges each token's per-block
-// partials. Workspace (caller-owned) per segment of tokens: fp16 partials and their
-// (log2-sum-exp, exponent) pairs, per-token counts and tickets, the buckets. A call is processed
-// in segments of at most `gather_segment_tokens` tokens, one index + one attend launch each.
+// Prefill attend by key block (tcgen05; bf16 packed cache, or fp8 / NVFP4 through converted
+// images; GQA 8 or 16): the tile kernel's conversion kernels write the V (and fp8 / NVFP4 K)
+// images, an index kernel buckets each 256-token window's tokens by selected block, a
+// persistent kernel attends every (block, kv head) bucket 16 gathered tokens at a time and
+// stores one partial per (token, block), and a merge kernel combines each token's partials.
+// Workspace (caller-owned): the images, then per segment of tokens the fp16 partials and their
+// (log2-sum-exp, exponent) pairs, per-token partial counts and the buckets. A call is processed
+// in segments of at most `gather_segment_tokens` tokens, one index + attend + merge launch each.
 constexpr int kGatherWinTok = 256;      // tokens per window (request-relative)
 constexpr int kGatherMaxBlocks = 8192;  // page-table width the index kernel's histogram covers
 constexpr int64_t kGatherMaxSegment = int64_t(1) << 19;
@@ -140,13 +142,9 @@ constexpr int64_t kGatherMaxSegment = int64_t(1) << 19;
 struct GatherWs {
   uint16_t* part;      // fp16 [seg][Hkv][k][G][128]: per-(token, block) output / l * 2^-e
   float2* ml;          // [seg][Hkv][k][G]: (log2-sum-exp of the block's logits, e)
-  int32_t* tickets;    // [seg][Hkv]: finished partials
+  int32_t* nparts;     // [seg]: partials of each token (its distinct valid blocks)
   int32_t* pairs;      // bucket entries: segment token << 12 | (partials - 1) << 6 | partial slot
   int4* chunks;        // [windows][ccap]: (block | kv head << 13, first entry, tokens, physical block)
-  int4* inbox;         // merge tasks: (token, kv head, partials, ready) of x = token * Hkv + head at
-                       // [x % n_mw][x / n_mw]: merge warp x % n_mw merges it
-  int32_t n_mw;        // merge warps of the attend grid
-  int32_t inbox_cap;   // tasks per merge warp
   int32_t* wins;       // [windows][8]: request, first token, context, seq_len, chunks
   int32_t T0, T1;      // segment [T0, T1) of the call's tokens
   int32_t num_win;     // windows of the segment (upper bound; surplus ones are empty)
@@ -160,10 +158,13 @@ size_t gather_workspace_bytes(int64_t seg_tokens, int num_reqs, int num_heads, i
 // Tokens per segment a workspace of `ws_bytes` allows (0: not even one window).
 int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks,
                               size_t ws_bytes);
-// `kv_map`: the half-row 5-D map of the packed cache; `q_map`: {128, heads, tokens} with a
-// {64, G, 1} box.
+// `kv_map`: the per-block map of a packed bf16 cache (as for the tile kernel; unused for fp8 /
+// NVFP4); `q_map`: {128, heads, tokens} with a {64, G, 1} box.
 cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
                                   size_t ws_bytes, cudaStream_t stream);
+// The conversion kernels of both tcgen05 prefill kernels: V (and for fp8 / NVFP4 caches K) of
+// every (request, block, kv head) into a.vconv / a.vconv_exp (/ a.kconv).
+cudaError_t launch_convert_images(const AttendArgs& a, cudaStream_t stream);
 
 // Index-cache insert.
 struct InsertArgs {

@@ -232,8 +232,16 @@ def test_prefill_kernel_choice_rule():
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, ws=big) == "tile"
     assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, ws=big) == "tile"
     assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, "tile") == 3        # asked for without the workspace
-    assert run("nvfp4", 64, 8, 16, 400, 8 * 2304, ws=big) == "tile"  # fp8 / NVFP4: any page-table width
-    assert run("bf16", 64, 8, 16, 400, packed, ws=big) == "token"
+    # page tables wider than 8 x top-k: the gathered-row kernel when its workspace is given
+    assert run("nvfp4", 64, 8, 16, 400, 8 * 2304, ws=big) == "gather"
+    assert run("bf16", 64, 8, 16, 400, packed, ws=big) == "gather"
+    assert run("bf16", 64, 8, 16, 400, packed) == "token"
+    tile_need = pbs.prefill_tile_workspace_bytes(4, 8, 400, "nvfp4")
+    assert run("nvfp4", 64, 8, 16, 400, 8 * 2304, ws=tile_need) == "tile"   # room for the images only
+    gneed = pbs.prefill_workspace_bytes(256, 4, 64, 8, 16, 400)
+    assert run("bf16", 64, 8, 16, 400, packed, ws=gneed) == "gather"
+    assert run("bf16", 64, 8, 16, 400, packed, ws=gneed - 256) == "token"
+    assert run("bf16", 64, 8, 16, 400, packed, ws=big, table=True) == "token"  # the gathered rows need top-k
     need = pbs.prefill_tile_workspace_bytes(4, 8, 64, "fp8_e4m3")
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, "tile", ws=need) == "tile"
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, "tile", ws=need - 256) == 3
@@ -241,10 +249,10 @@ def test_prefill_kernel_choice_rule():
     assert run("bf16", 64, 8, 17, 64, packed) == "token"             # top-k above 16
     assert run("bf16", 64, 8, 16, 64, packed + 16) == "token"        # pages strided inside a larger allocation
     assert run("bf16", 64, 8, 16, 64, packed, table=True) == "tile"  # a prebuilt table: the tile kernel reads it
-    # the gathered-row kernel only on request, with a workspace of at least one 256-token window
+    # the gathered-row kernel on request, with a workspace of at least one 256-token window
     need = pbs.prefill_workspace_bytes(256, 4, 64, 8, 16, 64)
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need) == "gather"
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need - 256) == 3
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need, table=True) == 3   # it reads top-k only
-    assert run("bf16", 64, 8, 16, 64, packed, ws=need) == "tile"     # never taken unasked
+    assert run("bf16", 64, 8, 16, 64, packed, ws=need) == "tile"     # not unasked for page tables of 8 x top-k
     assert run("bf16", 60, 8, 16, 64, packed) == 1

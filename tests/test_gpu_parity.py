@@ -688,18 +688,19 @@ def test_prebuilt_table_unreadable_rows(pbs, kernel):
 # tile kernel: fp8 / NVFP4 caches through converted images; long contexts; two-part unions
 # ------------------------------------------------------------------------------------------
 
+@pytest.mark.parametrize("kernel", ["tile", "gather"])
 @pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "nvfp4"])
 @pytest.mark.parametrize("heads", [(64, 8), (32, 2)])
 @pytest.mark.parametrize("ci", range(len(PREFILL_CASES)))
-def test_prefill_tile_kernel_fp8_nvfp4(pbs, kv_dtype, heads, ci):
-    """fp8 and NVFP4 caches on the tcgen05 tile kernel: K converted to bf16 and V to fp16 images once
-    per (request, block, kv head), both exact, then the same tile pipeline as bf16."""
+def test_prefill_tc_kernels_fp8_nvfp4(pbs, kv_dtype, heads, ci, kernel):
+    """fp8 and NVFP4 caches on both tcgen05 prefill kernels: K converted to bf16 and V to fp16
+    images once per (request, block, kv head), both exact, then the same pipelines as bf16."""
     b = workloads.small(device=DEV, kv_dtype=kv_dtype, num_heads=heads[0], num_kv_heads=heads[1], seed=141 + ci,
                         **PREFILL_CASES[ci])
     err = _err()
-    got = gpu_attend(pbs, b, "pre", err, kernel="tile")
+    got = gpu_attend(pbs, b, "pre", err, kernel=kernel)
     assert int(err.item()) == 0
-    assert_close(dict(enumerate(got)), oracle_prefill(b), kv_dtype, f"tile {kv_dtype} case {ci}")
+    assert_close(dict(enumerate(got)), oracle_prefill(b), kv_dtype, f"{kernel} {kv_dtype} case {ci}")
 
 
 def _largest_tile_union(b, tok):
@@ -743,3 +744,8 @@ def test_prefill_tile_long_context_two_part_unions(pbs, kv_dtype, heads):
         tabled = gpu_attend(pbs, b, "pre", err, workspace=ws, kernel="tile", sparse_table=tbl)
         assert int(err.item()) == 0
         assert np.array_equal(got, tabled), "table-fed tile call differs from the fused one"
+    # the gathered-row kernel on the same long contexts (its buckets hold a few tokens each)
+    err = _err()
+    got = gpu_attend(pbs, b, "pre", err, kernel="gather")
+    assert int(err.item()) == 0
+    assert_close(dict(enumerate(got)), want, kv_dtype, f"gather long context {kv_dtype}")
