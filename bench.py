@@ -289,6 +289,27 @@ def run_prefill(pbs, b, steps, warmup, flush, stream, workspace="auto", kernel=N
     return time_steps(step, steps, warmup, flush, stream)
 
 
+def gather_segments(pbs, b, ws_bytes):
+    """Token segments the gathered-row kernel cuts a prefill call into on a workspace of ws_bytes
+    (the largest multiple of 256 tokens whose workspace fits, or the whole call)."""
+    p = b.pre
+    T = p.q.shape[0]
+
+    def need(tokens):
+        return pbs.prefill_workspace_bytes(tokens, p.seq_lens.shape[0], b.num_heads, b.num_kv_heads,
+                                           p.topk.shape[-1], p.page_table.shape[1])
+    if need(T) <= ws_bytes:
+        return 1
+    lo, hi = 0, T // 256
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if need(mid * 256) <= ws_bytes:
+            lo = mid
+        else:
+            hi = mid - 1
+    return -(-T // (lo * 256)) if lo > 0 else 0
+
+
 def decode_ctx(pbs, b):
     d = b.dec
     _, ctx = pbs.build_sparse_block_table_decode(d.topk, d.page_table, d.seq_lens, d.decode_query_len,
@@ -376,14 +397,15 @@ def extra_measurements(pbs, steps, warmup, flush, stream, hbm, bf16):
     t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=None))
     res["prefill_varlen_bf16_no_workspace"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                                "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16}
-    # the same call on the gathered-row kernel (its workspace: images, partial ring, buckets)
+    # the same call on the gathered-row kernel (the binding's default workspace: its token segments)
     ws = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, b.topk,
                                p.page_table.shape[1], "cuda", stream)
     t = statistics.median(run_prefill(pbs, b, max(2, steps // 4), min(warmup, 3), flush, stream, workspace=ws,
                                       kernel="gather"))
     res["prefill_varlen_bf16_gathered_rows"] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                                                 "frac_of_bf16_peak": fl / (t * 1e-3) / 1e12 / bf16,
-                                                "workspace_bytes": ws.numel()}
+                                                "workspace_bytes": ws.numel(),
+                                                "segments": gather_segments(pbs, b, ws.numel())}
     del ws
     pbs._prefill_workspaces.clear()
     # the same call fed the prebuilt prefill table (built once, as every sparse layer would share it)
@@ -585,7 +607,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
             p = b.pre
             # the binding's default call on the tile kernel: V conversion, then the attend; on the
-            # gathered-row kernel: the conversion, the index kernel, then the attend (with its merges)
+            # gathered-row kernel: the conversion, then index, attend and merge per token segment
             chosen = pbs.prefill_kernel_choice(p.q.shape[0], p.seq_lens.shape[0], b.kv_dtype, b.page_bytes,
                                                b.num_heads, b.num_kv_heads, p.topk.shape[-1], p.page_table.shape[1],
                                                kernel=kernel, workspace_bytes=1 << 62)
@@ -593,7 +615,10 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                     p.seq_lens.shape[0], b.num_kv_heads, p.page_table.shape[1], b.kv_dtype) <= pbs.TILE_WORKSPACE_CAP:
                 launches = 2
             elif chosen == "gather":
-                launches = 3  # the conversion, index and attend kernels
+                # the conversion kernel, then per token segment the index, attend and merge kernels
+                wsb = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads,
+                                            p.topk.shape[-1], p.page_table.shape[1], "cuda", stream).numel()
+                launches = 1 + 3 * gather_segments(pbs, b, wsb)
         else:
             # rows of one request share their K/V rows: the union counts each once
             per_row = decode_bytes(b, decode_ctx(pbs, b))

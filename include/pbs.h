@@ -100,10 +100,8 @@ typedef struct CUstream_st* pbs_stream_t;
 #define PBS_PREFILL_TILE    2  /* tcgen05 tile kernel: GQA 8 or 16, top-k <= 16, page table <= 65535
                                   blocks, 16-byte aligned q / out rows; a packed bf16 cache, or an
                                   fp8 / NVFP4 cache with its workspace (pbs_prefill_tile_workspace_bytes) */
-#define PBS_PREFILL_GATHER  3  /* tcgen05 gathered-row kernel: GQA 8 or 16, top-k <= 64, page table
-                                  <= 8192 blocks, a packed bf16 cache or an fp8 / NVFP4 cache, 16-byte
-                                  aligned q / out rows; needs its workspace
-                                  (pbs_prefill_workspace_bytes); no prebuilt table */
+#define PBS_PREFILL_GATHER  3  /* tcgen05 gathered-row kernel: as the tile kernel but page tables up to
+                                  8192 blocks and top-k <= 64; needs its workspace; no prebuilt table */
 
 /*
  * Optional tuning of one attend call (a NULL pointer or an all-zero struct = the library's own
@@ -289,11 +287,12 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
  * workspace:
  *   workspace   optional (NULL, 0), caller-owned device memory, contents need no initial value.
  *               With a 256-byte aligned workspace of at least
- *               pbs_prefill_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, topk_k,
- *               max_blocks) bytes, calls the gathered-row kernel takes (see PBS_PREFILL_GATHER and
- *               pbs_prefill_kernel_choice) run on it: the converted K / V images, the per-window
- *               token buckets and a ring of per-block partial outputs for two 256-token windows
- *               live in the workspace (the partials are merged inside the call, from L2).
+ *               pbs_prefill_workspace_bytes(256, num_reqs, num_heads, num_kv_heads, topk_k,
+ *               max_blocks) bytes, calls the gathered-row kernel takes (bf16 cache packed as
+ *               [pages][Hkv][16 rows][K | V], GQA 8 or 16, max_blocks <= 8192, 16-byte aligned q
+ *               and out rows) run on it: per-block partial outputs and the per-window token buckets
+ *               live in the workspace, and the call is processed in as many token segments as its
+ *               size requires (pbs_prefill_workspace_bytes(total_q, ...) bytes: one segment).
  *               Otherwise the tcgen05 tile kernel or the token-centric kernel runs. The tile
  *               kernel, given a 256-byte aligned workspace of at least
  *               pbs_prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks, kv_dtype)
@@ -343,11 +342,11 @@ PBS_API int pbs_prefill_kernel_choice(int32_t total_q, int32_t num_reqs, int32_t
 
 /*
  * Bytes of the workspace with which pbs_sparse_prefill_attention runs a call of `total_q`
- * tokens (at most 2^24) over `num_reqs` requests on its gathered-row kernel; 0 for invalid
- * arguments. No counterpart on the pages. The size is the K and V images of every (request,
- * block, kv head) (64 KiB each, as pbs_prefill_tile_workspace_bytes for an fp8 cache), a ring of
- * 2 x 256 x Hq x k fp16 partial rows of 128 dims with their log-sum-exp pairs (about
- * 2 x 256 x Hq x k x 264 bytes), and about total_q * k * 4 bytes of token buckets.
+ * tokens (at most 2^19 per segment) over `num_reqs` requests on its gathered-row kernel in one
+ * segment; 0 for invalid arguments. No counterpart on the pages. With total_q = 256 it is the
+ * smallest workspace that kernel accepts. For Hq query heads and top-k k the size is about
+ * total_q * Hq * k * 264 bytes (fp16 partial outputs and their log-sum-exp pairs) plus the
+ * buckets.
  */
 PBS_API size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads,
                                            int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks);

@@ -308,8 +308,8 @@ def _workspace_args(workspace, rows, num_heads, num_kv_heads, device, stream):
 
 def prefill_workspace_bytes(total_q: int, num_reqs: int, num_heads: int, num_kv_heads: int, topk: int,
                             max_blocks: int) -> int:
-    """Bytes with which the prefill attend runs ``total_q`` tokens on its gathered-row kernel (the
-    K / V images, a two-window partial ring and the token buckets; 0: out of range)."""
+    """Bytes with which the prefill attend runs ``total_q`` tokens on its gathered-row kernel in
+    one segment (``total_q = 256``: the smallest workspace that kernel takes)."""
     return int(lib().pbs_prefill_workspace_bytes(int(total_q), int(num_reqs), int(num_heads), int(num_kv_heads),
                                                  int(topk), int(max_blocks)))
 
@@ -371,14 +371,14 @@ _prefill_workspaces: dict = {}
 def prefill_workspace(total_q: int, num_reqs: int, num_heads: int, num_kv_heads: int, topk: int, max_blocks: int,
                       device, stream=None) -> torch.Tensor:
     """A workspace for the prefill attend's gathered-row kernel, cached per (device, stream) and
-    grown on demand; None when the call does not take it or it would exceed
-    ``PREFILL_WORKSPACE_CAP``. Needs no initial value."""
+    grown on demand: one segment for the whole call when that fits ``PREFILL_WORKSPACE_CAP``,
+    else the cap (the call then runs in segments). Needs no initial value."""
     device = torch.device(device)
     s = stream if stream is not None else torch.cuda.current_stream(device)
     key = (device.index, s.cuda_stream)
-    need = prefill_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, topk, max_blocks)
-    if need == 0 or need > PREFILL_WORKSPACE_CAP:
-        return None
+    full = prefill_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, topk, max_blocks)
+    least = prefill_workspace_bytes(min(total_q, 256), num_reqs, num_heads, num_kv_heads, topk, max_blocks)
+    need = max(min(full, PREFILL_WORKSPACE_CAP), least)
     ws = _prefill_workspaces.get(key)
     if ws is None or ws.numel() < need:
         _prefill_workspaces.pop(key, None)

@@ -189,8 +189,8 @@ int encode_q_map_tokens(CUtensorMap* map, const void* q, int num_heads, int grou
 // selected a block, so its work does not grow with the context, but every (token, block) pair
 // costs a partial output written and merged through the workspace. So page tables up to
 // kTileMaxBlocksPerTopk * k blocks take the tile kernel, wider ones the gathered-row kernel (with
-// its workspace; otherwise fp8 / NVFP4 stay on the tile kernel and bf16 takes the token-centric
-// kernel). Measured (64/8 heads, top-k 16): the varlen
+// a workspace that holds at least one 256-token segment; otherwise fp8 / NVFP4 stay on the tile
+// kernel and bf16 takes the token-centric kernel). Measured (64/8 heads, top-k 16): the varlen
 // prompts of 2k-8k tokens (64-block table) take 2.39 ms on the tile kernel and 2.37 on the
 // gathered-row kernel; 2 x 4096 tokens after 16k / 32k of context on NVFP4 take 4.69 and 1.89
 // ms; bf16 on the tile kernel gives 462 / 312 / 114 TFLOP/s for contexts 0 / 2k-4k / 16k-32k,
@@ -227,10 +227,10 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int force
   const size_t tile_ws = pbs::prefill_tc_workspace_bytes(a.num_reqs, a.num_kv_heads, a.max_blocks, a.kv_dtype);
   const bool tile_fits = (a.kv_dtype != PBS_KV_BF16 || a.packed_map != 0) &&
                          pbs::prefill_tc_supported(a, tile_ws != 0 && workspace_bytes >= tile_ws);
-  const size_t gather_ws =
-      pbs::gather_workspace_bytes(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k, a.max_blocks);
   const bool gather_fits = (a.kv_dtype != PBS_KV_BF16 || a.packed_map != 0) && pbs::prefill_gather_supported(a) &&
-                           gather_ws != 0 && workspace_bytes >= gather_ws;
+                           a.num_rows < (1 << 25) &&
+                           pbs::gather_segment_tokens(a.num_rows, a.num_reqs, a.num_heads, a.num_kv_heads, a.k,
+                                                      a.max_blocks, workspace_bytes) > 0;
   if ((forced == PBS_PREFILL_TILE && !tile_fits) || (forced == PBS_PREFILL_GATHER && !gather_fits))
     return PBS_ERR_UNSUPPORTED;
   // fp8 / NVFP4: the token-centric kernel dequantises every gathered row per token, the tile kernel
@@ -778,7 +778,8 @@ size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t nu
   if (total_q <= 0 || num_reqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
       topk_k <= 0 || topk_k > kMaxTopk || max_blocks <= 0)
     return 0;
-  return pbs::gather_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, topk_k, max_blocks);
+  const int64_t seg = std::min<int64_t>(total_q, pbs::kGatherMaxSegment);
+  return pbs::gather_workspace_bytes(seg, num_reqs, num_heads, num_kv_heads, topk_k, max_blocks);
 }
 
 int pbs_sparse_mixed_attention(const void* q, int64_t q_row_stride, int64_t q_head_stride, const void* kv_cache,

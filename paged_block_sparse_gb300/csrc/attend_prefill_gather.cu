@@ -25,27 +25,22 @@
 // * Index kernel (one CTA per window): each token's distinct valid blocks, sorted, give the
 //   token's partial slots and count; tokens are bucketed by block (shared-memory histogram,
 //   block scan, scatter). Tokens with no valid block get zero output here.
-// * Attend kernel (persistent, one CTA per SM, cooperative launch): windows are taken in order
-//   and CTA i takes chunks [i C / G, (i + 1) C / G) of a window with C chunks, so every CTA works
-//   on the same few windows at a time and their Q rows, images and partials stay in L2. Warp 0
-//   loads K of a (block, kv head) item and its V image into one of two buffers each (one 32 KiB
-//   copy each; V as soon as the PV two items back has freed its buffer), writes each chunk's
-//   descriptor (tokens, partial slots, own-block key limits) into an 8-deep ring and gathers the
-//   chunk's Q rows (one tensor copy per token: its G heads, both 64-dim halves). Warp 1 (one
-//   thread) issues S(c) = Q K^T into TMEM buffer c % 2, then PV(c - 1), so the softmax of chunk
-//   c overlaps PV(c - 1) and S(c + 1). Warps 4-11 (two per TMEM lane quadrant, 64 keys each)
-//   take the softmax of chunk c, writing P as fp16 over S, then store chunk c - 1's partial while
-//   PV(c) runs. Warps 2 and 3 merge.
+// * Attend kernel (persistent, one CTA per SM): windows are taken in order and CTA i takes chunks
+//   [i C / G, (i + 1) C / G) of a window with C chunks, so every CTA works on the same few
+//   windows at a time and their Q rows and K / V images stay in L2. Warp 0 loads K and V of a
+//   (block, kv head) item (one 32 KiB copy each) into one of two buffers, writes each chunk's
+//   descriptor (tokens, partial slots, own-block key limits, the V image's exponent) into an
+//   8-deep ring and gathers the chunk's Q rows (one tensor copy per token: its G heads, both
+//   64-dim halves). Warp 1 (one thread) issues S(c) = Q K^T into TMEM buffer c % 2, then
+//   PV(c - 1), so the softmax of chunk c overlaps PV(c - 1) and S(c + 1). Warps 4-11 (two per
+//   TMEM lane quadrant, 64 keys each) take the softmax of chunk c, writing P as fp16 over S,
+//   then store chunk c - 1's partial while PV(c) runs.
 // * Softmax of one chunk (one key block): the row maximum over the block's valid keys (row
 //   maxima of the two key halves meet in shared memory), P = 2^(s * scale * log2 e - m) <= 1 as
 //   fp16 (one PV MMA per 16 keys against the fp16 V image). The partial is O / l (the image's
-//   V * 2^-e keeps it below 2^15) as fp16 with (log2-sum-exp, e), stored in the slot of its
-//   window in a ring of two windows (so it is merged from L2).
-// * Merges: once every CTA that attended window w has counted its partials stored (a GPU-scope
-//   release per softmax warp after the window's last chunk, which stores its partial at once),
-//   the grid's merge warps split the window's (token, kv head) units, weight each token's
-//   partials by 2^(lse - max) into the bf16 output and the log-sum-exp, and count the window
-//   merged. Window w + 2 reuses window w's slots only after that count is complete.
+//   V * 2^-e keeps it below 2^15) as fp16 with (log2-sum-exp, e).
+// * Merge kernel (one warp per (token, kv head)): the token's partials weighted by 2^(lse - max),
+//   the bf16 output and the log-sum-exp.
 // * TMEM (512 columns): S / P double buffer (2 x 128) and O double buffer (2 x 128).
 #include <algorithm>
 
@@ -60,14 +55,13 @@ constexpr int kGRows = 128;                     // MMA M: tokens x query heads o
 constexpr int kGThreads = 384;                  // 12 warps
 constexpr int kDescRing = 8;                    // chunk descriptors in flight
 constexpr int kGQBytes = kGRows * kHeadDim * 2;  // 32 KiB Q tile
-constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of a K or V tile: [128 rows][128 B]
+constexpr int kGHalf = kGQBytes / 2;            // one 64-dim half of a Q, K or V tile: [128 rows][128 B]
 constexpr int kGTile = 32768;                   // a block's K (or V) for one kv head
 constexpr int kGSmemBig = 2 * kGQBytes + 4 * kGTile;  // Q x 2, K x 2, V x 2
 constexpr unsigned long long kGWaitNs = 100000000ull;  // waits here last microseconds: 100 ms cap
-constexpr int kIdxThreads = 1024;               // index kernel: 32 warps, 8 tokens of a window each
+constexpr int kIdxThreads = 1024;                // index kernel: 32 warps, 8 tokens of a window each
 constexpr int kSoftWarpsG = 8;                  // softmax warps (4 - 11)
-constexpr int kMergeWarpsG = 2;                 // merge warps (2 and 3)
-constexpr int kVQueue = 4;                      // items whose V load the producer may owe
+constexpr int kMergeWarps = 8;                  // warps per merge CTA
 
 struct ChunkDesc {
   int32_t end;    // 1: no more work for this CTA
@@ -77,17 +71,15 @@ struct ChunkDesc {
   int32_t n_tok;  // tokens in this chunk
   int32_t item;   // the CTA's item number (phase of the K/V buffer barriers)
   int32_t req;    // request (the item's images are those of (req, b, g))
-  int32_t win;    // window
-  int32_t wlast;  // the CTA's last chunk of its window: its PV and partial do not wait for the next chunk
-  int32_t pad[3];
-  int32_t tl[16];    // window-relative token index
+  int32_t pad;
+  int32_t tr[16];    // segment-relative token index
   int32_t slot[16];  // the token's partial slot for block b
   int32_t lim[16];   // keys of block b the token sees (128, or pos - 128 b + 1 for its own block)
 };
 
 struct GCtl {
   uint64_t desc_full[kDescRing];
-  // released by the MMA thread (PV issued) and the softmax warps (partial stored)
+  // released by the MMA thread (PV issued), the V producer and the softmax warps (partial stored)
   uint64_t desc_empty[kDescRing];
   uint64_t q_full[2], q_empty[2];
   // K buffer Y is free once the S of its item's last chunk has completed, V buffer Y once its PV
@@ -99,7 +91,6 @@ struct GCtl {
   uint32_t tmem_base;
   int32_t abort;
   ChunkDesc desc[kDescRing];
-  int64_t vq[kVQueue];       // image of item n % kVQueue, whose V the producer loads when buffer n % 2 frees
   int32_t ents[128];         // bucket entries of the producer's current batch
   float lsum[4][2][kGRows];  // chunk c & 3, key half, row: partial sum
   float xchg[2][2][kGRows];  // row maxima of the two key halves
@@ -107,7 +98,7 @@ struct GCtl {
 
 // A batch of up to 8 consecutive chunks of one window (producer).
 struct Batch {
-  int w, base, nb, r, c0, ctx0, seq_len, ta, last;  // last: the batch ends the CTA's slice of the window
+  int w, base, nb, r, c0, ctx0, seq_len;
 };
 
 constexpr size_t kGSmem = kGSmemBig + sizeof(GCtl) + 1024;
@@ -129,10 +120,6 @@ __device__ int g_gtrace_cta;
 #define GTRACE(ev, c) do { } while (0)
 #endif
 
-__device__ __forceinline__ bool g_aborted_ctl(GCtl* ctl) {
-  return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0;
-}
-
 __device__ __forceinline__ bool g_wait(uint64_t* bar, uint32_t parity, GCtl* ctl, int32_t* err) {
   if (mbar_wait_bounded(bar, parity, kGWaitNs)) return true;
   set_err(err, PBS_DEVERR_TIMEOUT);
@@ -140,48 +127,9 @@ __device__ __forceinline__ bool g_wait(uint64_t* bar, uint32_t parity, GCtl* ctl
   return false;
 }
 
-// Set by any CTA that gave up waiting: the other CTAs stop waiting for windows it will not finish.
-__device__ __forceinline__ bool grid_aborted(const GatherWs& w) {
-  return *reinterpret_cast<const volatile int32_t*>(w.abort_all) != 0;
-}
-
 __device__ __forceinline__ bool g_warp_wait(uint64_t* bar, uint32_t parity, GCtl* ctl, int32_t* err) {
   const bool ok = g_wait(bar, parity, ctl, err);
   return __all_sync(0xffffffffu, ok);
-}
-
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Cross-CTA counters: a GPU-scope acquire load, and an increment that releases the caller's prior
-// memory operations (and those ordered before them in its CTA) at GPU scope.
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void add_release_gpu(int32_t* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Loads of data other CTAs wrote during this kernel: cached in L2 only.
-__device__ __forceinline__ uint4 ldcg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float2 ldcg_f2(const void* p) {
-  float2 v;
-  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ void g_tma_5d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2, int c3,
@@ -212,9 +160,9 @@ __device__ __forceinline__ float g_f16_hi(uint32_t x) {
   return f;
 }
 
-// Window `wi` of the call: windows are numbered request by request, each request's tokens cut at
-// multiples of kGatherWinTok from its first token. Warp-collective. Returns false when wi is past
-// the last window.
+// Window of the segment [T0, T1) with index `wi`: windows are numbered request by request, each
+// request's tokens cut at multiples of kGatherWinTok from its first token. Warp-collective.
+// Returns false when wi is past the last window.
 struct WinInfo {
   int r, ta, tb, c0, ctx0, seq_len;
 };
@@ -230,7 +178,7 @@ __device__ __forceinline__ bool find_window(const AttendArgs& a, const GatherWs&
       c1 = __ldg(a.cu_seqlens_q + rr + 1);
       sl = __ldg(a.seq_lens + rr);
     }
-    const int lo = c0, hi = c1;
+    const int lo = max(c0, w.T0), hi = min(c1, w.T1);
     const int nw = lo < hi ? (hi - 1 - c0) / kGatherWinTok - (lo - c0) / kGatherWinTok + 1 : 0;
     int incl = nw;
 #pragma unroll
@@ -246,7 +194,7 @@ __device__ __forceinline__ bool find_window(const AttendArgs& a, const GatherWs&
       const int sc0 = __shfl_sync(0xffffffffu, c0, src);
       const int sc1 = __shfl_sync(0xffffffffu, c1, src);
       const int ssl = __shfl_sync(0xffffffffu, sl, src);
-      const int slo = sc0, shi = sc1;
+      const int slo = max(sc0, w.T0), shi = min(sc1, w.T1);
       const int wrel = (slo - sc0) / kGatherWinTok + (wi - ex);
       out.r = r0 + src;
       out.c0 = sc0;
@@ -267,8 +215,7 @@ __device__ __forceinline__ bool find_window(const AttendArgs& a, const GatherWs&
 // Dynamic shared memory: cnt[max_blocks], cur[max_blocks], pairs_s[kGatherWinTok * k].
 // Output per window: the chunk records in processing order (buckets by decreasing block id;
 // within a bucket kv head by kv head, 16 (or 8) tokens per chunk), the bucket entries they point
-// at, the window record {request, request's first token, context, seq_len, chunks, window's first
-// token, end token}, each token's partial count, and the window's two completion counters zeroed.
+// at, and the window record {request, first token, context, seq_len, chunks}.
 __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendArgs a, const GatherWs w) {
   extern __shared__ int32_t ish[];
   int32_t* cnt = ish;
@@ -281,7 +228,6 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = blockIdx.x;
   const int kTok = w.tok_per_chunk;
-  if (wi == 0 && threadIdx.x == 0) *w.abort_all = 0;
   int32_t* wrec = w.wins + static_cast<int64_t>(wi) * 8;
   if (warp == 0) {
     WinInfo info;
@@ -309,9 +255,6 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
     if (threadIdx.x == 0) {
       wrec[0] = -1;
       wrec[4] = 0;
-      wrec[5] = wrec[6] = 0;
-      w.done[wi] = 0;
-      w.merged[wi] = 0;
     }
     return;
   }
@@ -324,6 +267,7 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   const int n = tb - ta;
   for (int tt = warp; tt < n; tt += kIdxThreads / 32) {
     const int t = ta + tt;
+    const int tr = t - w.T0;
     const int pos = ctx0 + (t - c0);
     const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
     const int own = causal_len > 0 ? pos / kSparseBlock : -1;
@@ -375,7 +319,7 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
     }
     if (lane == 0) {
       s_tn[tt] = n_t;
-      w.nparts[t] = n_t;  // the merge warps' partial count for this token
+      w.nparts[tr] = n_t;  // the merge kernel's partial count for this token
     }
     if (n_t == 0) {
       // nothing to attend (no valid block, or a block past the page table): zero output
@@ -450,7 +394,7 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
     const int v = pairs_s[p];
     const int b = v >> 14, tt = (v >> 6) & 255, rank = v & 63;
     const int at = atomicAdd(&cur[b], 1);
-    w.pairs[pair_base + at] = (tt << 12) | ((s_tn[tt] - 1) << 6) | rank;
+    w.pairs[pair_base + at] = ((ta + tt - w.T0) << 12) | ((s_tn[tt] - 1) << 6) | rank;
   }
   if (threadIdx.x == 0) {
     wrec[0] = r;
@@ -458,19 +402,12 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
     wrec[2] = ctx0;
     wrec[3] = s_win[5];
     wrec[4] = tch * hkv;  // chunk records
-    wrec[5] = ta;
-    wrec[6] = tb;
-    w.done[wi] = 0;
-    w.merged[wi] = 0;
   }
 }
 
 
 // ------------------------------------------------------------------------------------------
-
-// ------------------------------------------------------------------------------------------
-// attend kernel: persistent, one CTA per SM, cooperative launch (every CTA's merge warps wait
-// for windows that all CTAs attend, and every producer for windows that all merge warps merged)
+// attend kernel: persistent, one CTA per SM
 // ------------------------------------------------------------------------------------------
 
 template <int kG>
@@ -486,12 +423,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint8_t* v_s = k_s + 2 * kGTile;    // 2 x 32 KiB: [half][128 keys][128 B] (fp16 image)
   GCtl* ctl = reinterpret_cast<GCtl*>(v_s + 2 * kGTile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_merge_warps = static_cast<int>(gridDim.x) * kMergeWarpsG;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&ctl->desc_full[i], 1);
-      mbar_init(&ctl->desc_empty[i], 1 + kSoftWarpsG);
+      mbar_init(&ctl->desc_empty[i], 2 + kSoftWarpsG);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
@@ -517,11 +453,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (threadIdx.x == 0) GTRACE(kGtStart, 0);
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer (Q, K, V, descriptors)
+    // ---------------------------------------------------------------- producer (Q, K, descriptors)
     // Windows in order; CTA i takes chunks [i C / G, (i + 1) C / G) of a window with C chunks.
     // Chunks go in batches of up to 8: the records of batch n + 2 and the bucket entries of
-    // batch n + 1 are in flight while batch n is issued. Window w's first chunk waits until
-    // every merge warp has merged window w - kGatherRing, whose partial slots it reuses.
+    // batch n + 1 are in flight while batch n is issued.
     if (lane == 0) {
       if (a.kconv == nullptr)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kv_map)) : "memory");
@@ -529,7 +464,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     const int cta = blockIdx.x, grid = gridDim.x;
     // window records of windows [wc0, wc0 + 32), one per lane
-    int wc0 = -64, wr_r = 0, wr_c0 = 0, wr_ctx0 = 0, wr_sl = 0, wr_C = 0, wr_ta = 0;
+    int wc0 = -64, wr_r = 0, wr_c0 = 0, wr_ctx0 = 0, wr_sl = 0, wr_C = 0;
     int cw = 0, cbase = 0, chi = -1;  // cursor: window, next chunk of its slice, slice end (-1: not entered)
     auto next_batch = [&](Batch& B) {
       B.nb = 0;
@@ -544,7 +479,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
             wr_ctx0 = __ldg(wrp + 2);
             wr_sl = __ldg(wrp + 3);
             wr_C = __ldg(wrp + 4);
-            wr_ta = __ldg(wrp + 5);
           } else {
             wr_C = 0;
           }
@@ -563,9 +497,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           B.c0 = __shfl_sync(0xffffffffu, wr_c0, src);
           B.ctx0 = __shfl_sync(0xffffffffu, wr_ctx0, src);
           B.seq_len = __shfl_sync(0xffffffffu, wr_sl, src);
-          B.ta = __shfl_sync(0xffffffffu, wr_ta, src);
           cbase += B.nb;
-          B.last = cbase == chi ? 1 : 0;
           return;
         }
         ++cw;
@@ -590,45 +522,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     };
     int* ent_s = ctl->ents;
     int n_item = -1, c = 0;
-    int item_r = -1, item_b = -1, item_g = -1, gate_w = -1;
+    int item_r = -1, item_b = -1, item_g = -1;
     // uses of each buffer so far (their barrier phases); scalars, so they stay in registers
-    int q_n0 = 0, q_n1 = 0, kv_n0 = 0, kv_n1 = 0, v_n0 = 0, v_n1 = 0;
-    int v_next = 0;  // lane 0: the next item whose V load is owed
-    // Lane 0 loads the V image of every owed item as soon as its buffer frees (the PV of the item
-    // two before has completed): from every wait below, so a waiting producer never holds up a PV.
-    auto service_v = [&]() {
-      while (v_next <= n_item) {
-        const int Y = v_next & 1;
-        if (v_next >= 2 && !mbar_test(&ctl->v_empty[Y], ((v_next >> 1) - 1) & 1)) return;
-        mbar_arrive_expect_tx(&ctl->v_full[Y], kGTile);
-        bulk_load(v_s + Y * kGTile, a.vconv + ctl->vq[v_next % kVQueue] * kGTile, kGTile, &ctl->v_full[Y]);
-        GTRACE(kGtV, v_next);
-        if (Y == 0) ++v_n0; else ++v_n1;
-        ++v_next;
-      }
-    };
-    auto give_up = [&]() {
-      set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-      atomicExch(&ctl->abort, 1);
-      atomicExch(w.abort_all, 1);
-      return false;
-    };
-    auto wait_serving = [&](uint64_t* bar, uint32_t parity) -> bool {  // lane 0
-      const unsigned long long t0 = global_timer_ns();
-      while (!mbar_test(bar, parity)) {
-        service_v();
-        if (global_timer_ns() - t0 > kGWaitNs) return give_up();
-      }
-      return true;
-    };
-    auto wait_count_serving = [&](const int32_t* p, int target) -> bool {  // lane 0
-      const unsigned long long t0 = global_timer_ns();
-      while (ld_acquire_gpu(p) < target) {
-        service_v();
-        if (global_timer_ns() - t0 > kGWaitNs || grid_aborted(w)) return give_up();
-      }
-      return true;
-    };
+    int q_n0 = 0, q_n1 = 0, kv_n0 = 0, kv_n1 = 0;
     bool ok = true;
     Batch B0, B1, B2;
     next_batch(B0);
@@ -650,59 +546,41 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int b = rx & 8191, g = rx >> 13;
         const int n_tok = __shfl_sync(0xffffffffu, rec0.z, jc);
         const int phys = __shfl_sync(0xffffffffu, rec0.w, jc);
-        // ---- window gate: the partial slots of window w were last used by window w - kGatherRing
-        if (B0.w != gate_w) {
-          gate_w = B0.w;
-          bool go = true;
-          if (lane == 0 && B0.w >= kGatherRing) go = wait_count_serving(w.merged + (B0.w - kGatherRing), n_merge_warps);
-          if (!__shfl_sync(0xffffffffu, go, 0)) {
-            ok = false;
-            break;
-          }
-        }
-        // ---- a new (request, block, kv head): its K into the next K buffer, its V owed
+        // ---- a new (request, block, kv head): its K into the next K buffer (warp 3 loads V)
         if (B0.r != item_r || b != item_b || g != item_g) {
           ++n_item;
           item_r = B0.r;
           item_b = b;
           item_g = g;
           const int Y = n_item & 1;
-          bool go = true;
-          if (lane == 0) {
-            // at most kVQueue owed V loads
-            const unsigned long long t0 = global_timer_ns();
-            while (go && n_item - v_next >= kVQueue) {
-              service_v();
-              if (n_item - v_next >= kVQueue && global_timer_ns() - t0 > kGWaitNs) go = give_up();
-            }
-            if (go && n_item >= 2) go = wait_serving(&ctl->k_empty[Y], ((n_item >> 1) - 1) & 1);
-            if (go) {
-              const int64_t image = (static_cast<int64_t>(B0.r) * a.max_blocks + b) * a.num_kv_heads + g;
-              mbar_arrive_expect_tx(&ctl->k_full[Y], kGTile);
-              if (a.kconv != nullptr) {
-                bulk_load(k_s + Y * kGTile, a.kconv + image * kGTile, kGTile, &ctl->k_full[Y]);
-              } else {
-                // one {64, 16 rows, head, 8 pages, K half} box; pages past the cache read as zeros
-                const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
-                if (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
-                g_tma_5d(k_s + Y * kGTile, &kv_map, &ctl->k_full[Y], 0, 0, g, static_cast<int>(pbase), 0);
-              }
-              ctl->vq[n_item % kVQueue] = image;
-              GTRACE(kGtK, c);
-              service_v();
+          if (n_item >= 2) {
+            bool go = true;
+            if (lane == 0) go = g_wait(&ctl->k_empty[Y], ((n_item >> 1) - 1) & 1, ctl, a.err_word);
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+              ok = false;
+              break;
             }
           }
-          if (!__shfl_sync(0xffffffffu, go, 0)) {
-            ok = false;
-            break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl->k_full[Y], kGTile);
+            if (a.kconv != nullptr) {
+              const int64_t image = (static_cast<int64_t>(B0.r) * a.max_blocks + b) * a.num_kv_heads + g;
+              bulk_load(k_s + Y * kGTile, a.kconv + image * kGTile, kGTile, &ctl->k_full[Y]);
+            } else {
+              // one {64, 16 rows, head, 8 pages, K half} box; pages past the cache read as zeros
+              const int64_t pbase = static_cast<int64_t>(phys) * a.block_page_stride;
+              if (pbase < 0 || pbase + (kPagesPerBlock - 1) >= a.num_pages) set_err(a.err_word, PBS_DEVERR_PAGE_OOB);
+              g_tma_5d(k_s + Y * kGTile, &kv_map, &ctl->k_full[Y], 0, 0, g, static_cast<int>(pbase), 0);
+            }
           }
           if (Y == 0) ++kv_n0; else ++kv_n1;
+          if (lane == 0) GTRACE(kGtK, c);
         }
         // ---- the chunk's descriptor
         const int ds = c % kDescRing;
         if (c >= kDescRing) {
           bool go = true;
-          if (lane == 0) go = wait_serving(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1);
+          if (lane == 0) go = g_wait(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1, ctl, a.err_word);
           if (!__shfl_sync(0xffffffffu, go, 0)) {
             ok = false;
             break;
@@ -712,10 +590,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
         int t_lane = 0;
         if (lane < n_tok) {
           const int en = ent_s[jc * kTok + lane];
-          const int tl = en >> 12;
-          const int t = B0.ta + tl;
+          const int tr = en >> 12;
+          const int t = w.T0 + tr;
           const int pos = B0.ctx0 + (t - B0.c0);
-          d->tl[lane] = tl;
+          d->tr[lane] = tr;
           d->slot[lane] = en & 63;
           d->lim[lane] = pos / kSparseBlock == b ? pos - b * kSparseBlock + 1 : kSparseBlock;
           t_lane = t;
@@ -728,14 +606,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
           d->n_tok = n_tok;
           d->item = n_item;
           d->req = B0.r;
-          d->win = B0.w;
-          d->wlast = B0.last != 0 && jc == B0.nb - 1 ? 1 : 0;
         }
         // ---- gather the chunk's Q rows: token j -> its G rows, one {64, 8, 2, G / 8, 1} copy
         const int qb = c & 1;
         if (c >= 2) {
           bool go = true;
-          if (lane == 0) go = wait_serving(&ctl->q_empty[qb], ((c >> 1) - 1) & 1);
+          if (lane == 0) go = g_wait(&ctl->q_empty[qb], ((c >> 1) - 1) & 1, ctl, a.err_word);
           if (!__shfl_sync(0xffffffffu, go, 0)) {
             ok = false;
             break;
@@ -751,7 +627,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (lane == 0) {
           mbar_arrive(&ctl->desc_full[ds]);
           GTRACE(kGtProd, c);
-          service_v();
         }
       }
       B0 = B1;
@@ -759,11 +634,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
       B1 = B2;
       rec1 = rec2;
     }
-    // ---- end mark, then every owed V load
+    // ---- end mark
     if (ok) {
       const int ds = c % kDescRing;
       bool go = true;
-      if (lane == 0 && c >= kDescRing) go = wait_serving(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1);
+      if (c >= kDescRing && lane == 0) go = g_wait(&ctl->desc_empty[ds], ((c / kDescRing) - 1) & 1, ctl, a.err_word);
       if (__shfl_sync(0xffffffffu, go, 0) && lane == 0) {
         ctl->desc[ds].end = 1;
         __threadfence_block();
@@ -771,20 +646,39 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
       __syncwarp();
     }
+    // every copy issued must land before the CTA exits
     if (lane == 0) {
-      const unsigned long long t0 = global_timer_ns();
-      while (v_next <= n_item && !g_aborted_ctl(ctl)) {
-        service_v();
-        if (v_next <= n_item && global_timer_ns() - t0 > kGWaitNs) {
-          give_up();
-          break;
-        }
-      }
-      // every copy issued must land before the CTA exits
       if (q_n0 > 0) mbar_wait_bounded(&ctl->q_full[0], (q_n0 - 1) & 1, kGWaitNs);
       if (q_n1 > 0) mbar_wait_bounded(&ctl->q_full[1], (q_n1 - 1) & 1, kGWaitNs);
       if (kv_n0 > 0) mbar_wait_bounded(&ctl->k_full[0], (kv_n0 - 1) & 1, kGWaitNs);
       if (kv_n1 > 0) mbar_wait_bounded(&ctl->k_full[1], (kv_n1 - 1) & 1, kGWaitNs);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- V producer
+    // Follows the descriptors: the first chunk of every item loads the item's fp16 V image into
+    // V buffer item % 2 once the PV of the item two before has completed.
+    int v_n0 = 0, v_n1 = 0, prev_item = -1;
+    for (int c = 0;; ++c) {
+      const int ds = c % kDescRing;
+      if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
+      const ChunkDesc* d = &ctl->desc[ds];
+      if (d->end) break;
+      const int item = d->item, Y = d->ybuf;
+      if (item != prev_item) {
+        prev_item = item;
+        if (item >= 2 && !g_warp_wait(&ctl->v_empty[Y], ((item >> 1) - 1) & 1, ctl, a.err_word)) break;
+        if (lane == 0) {
+          const int64_t image = (static_cast<int64_t>(d->req) * a.max_blocks + d->b) * a.num_kv_heads + d->g;
+          mbar_arrive_expect_tx(&ctl->v_full[Y], kGTile);
+          bulk_load(v_s + Y * kGTile, a.vconv + image * kGTile, kGTile, &ctl->v_full[Y]);
+          GTRACE(kGtV, c);
+        }
+        if (Y == 0) ++v_n0; else ++v_n1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->desc_empty[ds]);
+    }
+    if (lane == 0) {
       if (v_n0 > 0) mbar_wait_bounded(&ctl->v_full[0], (v_n0 - 1) & 1, kGWaitNs);
       if (v_n1 > 0) mbar_wait_bounded(&ctl->v_full[1], (v_n1 - 1) & 1, kGWaitNs);
     }
@@ -793,37 +687,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
       constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, false, false, true);  // fp16 P, fp16 V
-      // O(X) = P V for chunk cp: P (fp16, two keys per column) in columns 0..63 of S buffer X, V the
-      // item's fp16 image (keys 16ks.. = two 8-key groups 1 KiB apart; dims in two 64-wide MN
-      // atoms 16 KiB apart)
-      auto issue_pv = [&](int cp, int y, int item) -> bool {
-        const int Xp = cp & 1;
-        if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) return false;
-        if (!g_wait(&ctl->v_full[y], (item >> 1) & 1, ctl, a.err_word)) return false;
-        // O buffer X' was read by the partial of chunk cp - 2
-        if (cp >= 2 && !g_wait(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1, ctl, a.err_word)) return false;
-        tc::fence_after_sync();
-        const uint32_t v_addr = smem_u32(v_s + y * kGTile);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_ts(tmem + 256 + Xp * 128, tmem + Xp * 128 + ks * 8,
-                     tc::smem_desc_sw128(v_addr + ks * 2048, kGHalf, 1024), kIdescPV, ks > 0);
-        tc::commit(&ctl->pv_done[Xp]);
-        GTRACE(kGtPV, cp);
-        return true;
-      };
       int prev_y = 0, prev_item = 0;
-      bool prev_pv = true;  // the previous chunk's PV has been issued (it was its window's last)
       for (int c = 0;; ++c) {
         const int ds = c % kDescRing;
         if (!g_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
         const ChunkDesc* d = &ctl->desc[ds];
         const int end = d->end;
-        const int Y = d->ybuf, item = d->item, wlast = d->wlast;
-        const bool new_item = c >= 1 && (end || item != prev_item);
+        const int Y = d->ybuf, item = d->item;
         // chunk c starts a new item (or there is none): the S of the previous item's last chunk,
         // issued before, is the last reader of its K buffer
-        if (new_item) tc::commit(&ctl->k_empty[prev_y]);
+        if (c >= 1 && (end || item != prev_item)) tc::commit(&ctl->k_empty[prev_y]);
         if (!end) {
           const int X = c & 1;
           // the K buffer of item n completes once per use: phase (n / 2) & 1
@@ -843,21 +716,28 @@ __global__ void __launch_bounds__(kGThreads, 1)
           GTRACE(kGtS, c);
         }
         if (c >= 1) {
-          if (!prev_pv) {
-            if (!issue_pv(c - 1, prev_y, prev_item)) break;
-            mbar_arrive(&ctl->desc_empty[(c - 1) % kDescRing]);
-          }
-          // the previous chunk was its item's last: its V buffer is free once its PV completes
-          if (new_item) tc::commit(&ctl->v_empty[prev_y]);
+          // PV of the previous chunk: O(X') = P V, P (fp16, two keys per column) in columns
+          // 0..63 of S buffer X', V the item's fp16 image
+          const int cp = c - 1, Xp = cp & 1;
+          if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) break;
+          if (!g_wait(&ctl->v_full[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
+          // O buffer X' was read by the epilogue of chunk cp - 2
+          if (cp >= 2 && !g_wait(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1, ctl, a.err_word)) break;
+          tc::fence_after_sync();
+          const uint32_t v_addr = smem_u32(v_s + prev_y * kGTile);
+          // keys 16ks..16ks+15 = two 8-key groups (1 KiB apart); dims in two 64-wide MN atoms
+          // 16 KiB apart
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ts(tmem + 256 + Xp * 128, tmem + Xp * 128 + ks * 8,
+                       tc::smem_desc_sw128(v_addr + ks * 2048, kGHalf, 1024), kIdescPV, ks > 0);
+          tc::commit(&ctl->pv_done[Xp]);
+          GTRACE(kGtPV, cp);
+          // the previous chunk was its item's last: its V buffer is free once this PV completes
+          if (end || item != prev_item) tc::commit(&ctl->v_empty[prev_y]);
+          mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
         }
         if (end) break;
-        // a window's last chunk: PV now, so its partial never waits for a descriptor that a
-        // producer may hold back at the next window's gate
-        prev_pv = wlast != 0;
-        if (prev_pv) {
-          if (!issue_pv(c, Y, item)) break;
-          mbar_arrive(&ctl->desc_empty[ds]);
-        }
         prev_y = Y;
         prev_item = item;
       }
@@ -865,173 +745,29 @@ __global__ void __launch_bounds__(kGThreads, 1)
       tc::commit(&ctl->mma_fin);
       mbar_wait_bounded(&ctl->mma_fin, 0, kGWaitNs);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ---------------------------------------------------------------- merge warps
-    // Windows in order: merge warp i of the grid takes units [i U / M, (i + 1) U / M) of a window
-    // with U (token, kv head) units, once every CTA that attended the window has stored its
-    // partials, and counts the window merged. A unit's n partials P_s (O_s / l_s as fp16 times
-    // 2^-e_s) with base-2 log-sum-exps L_s give out = v_scale * sum_s 2^(L_s - M + e_s) P_s /
-    // sum_s 2^(L_s - M), M = max_s L_s, and the row's log-sum-exp M + log2(sum_s 2^(L_s - M)).
-    constexpr int kLanesPerHead = 32 / kG;        // 4 (GQA 8) or 2 (GQA 16)
-    constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
-    constexpr int kGrp = kG == 8 ? 4 : 2;         // partials loaded together
-    const int mw = static_cast<int>(blockIdx.x) * kMergeWarpsG + (warp - 2);
-    const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
-    const int hkv = a.num_kv_heads;
-    bool ok = true;
-    for (int m = 0; m < w.num_win && ok; ++m) {
-      const int32_t* wr = w.wins + static_cast<int64_t>(m) * 8;
-      const int r = __ldg(wr), C = __ldg(wr + 4), ta = __ldg(wr + 5), tb = __ldg(wr + 6);
-      if (r >= 0 && tb > ta) {
-        const int units = (tb - ta) * hkv;
-        const int u0 = static_cast<int>(static_cast<int64_t>(mw) * units / n_merge_warps);
-        const int u1 = static_cast<int>(static_cast<int64_t>(mw + 1) * units / n_merge_warps);
-        const int expect = kSoftWarpsG * min(C, static_cast<int>(gridDim.x));
-        if (u0 < u1 && expect > 0) {
-          if (lane == 0) {
-            const unsigned long long t0 = global_timer_ns();
-            while (ld_acquire_gpu(w.done + m) < expect) {
-              if (global_timer_ns() - t0 > kGWaitNs || g_aborted_ctl(ctl) || grid_aborted(w)) {
-                set_err(a.err_word, PBS_DEVERR_TIMEOUT);
-                atomicExch(&ctl->abort, 1);
-                atomicExch(w.abort_all, 1);
-                ok = false;
-                break;
-              }
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-        }
-        const int slot0 = (m % kGatherRing) * kGatherWinTok;
-        for (int u = u0; u < u1; ++u) {
-          const int tl = u / hkv, g = u % hkv;
-          const int t = ta + tl;
-          const int n = __ldg(w.nparts + t);
-          if (n <= 0) continue;  // the index kernel wrote this token's zero output
-          const int64_t prow0 = (static_cast<int64_t>(slot0 + tl) * hkv + g) * a.k * kG + h;
-          // M: the lanes of head h share the n log-sum-exps (n <= 64), then meet by shuffles
-          const int sub = lane % kLanesPerHead;
-          float M = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 64 / kLanesPerHead; ++i) {
-            const int s = sub + i * kLanesPerHead;
-            if (s < n) M = fmaxf(M, ldcg_f2(w.ml + prow0 + static_cast<int64_t>(s) * kG).x);
-          }
-#pragma unroll
-          for (int off = 1; off < kLanesPerHead; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-          float L = 0.f;
-          float acc[kE];
-#pragma unroll
-          for (int i = 0; i < kE; ++i) acc[i] = 0.f;
-          for (int s0 = 0; s0 < n; s0 += kGrp) {
-            float2 mlv[kGrp];
-            uint4 u4[kGrp][kE / 8];
-#pragma unroll
-            for (int s1 = 0; s1 < kGrp; ++s1)
-              if (s0 + s1 < n) {
-                const int64_t prow = prow0 + static_cast<int64_t>(s0 + s1) * kG;
-                mlv[s1] = ldcg_f2(w.ml + prow);
-                const uint16_t* src = w.part + prow * kHeadDim + d0;
-#pragma unroll
-                for (int q = 0; q < kE / 8; ++q) u4[s1][q] = ldcg_v4(src + 8 * q);
-              }
-#pragma unroll
-            for (int s1 = 0; s1 < kGrp; ++s1)
-              if (s0 + s1 < n) {
-                const float wl = exp2f(mlv[s1].x - M);
-                L += wl;
-                const float f = wl * exp2f(mlv[s1].y);
-#pragma unroll
-                for (int q = 0; q < kE / 8; ++q) {
-                  const uint32_t wd[4] = {u4[s1][q].x, u4[s1][q].y, u4[s1][q].z, u4[s1][q].w};
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    acc[8 * q + 2 * i] = fmaf(f, g_f16_lo(wd[i]), acc[8 * q + 2 * i]);
-                    acc[8 * q + 2 * i + 1] = fmaf(f, g_f16_hi(wd[i]), acc[8 * q + 2 * i + 1]);
-                  }
-                }
-              }
-          }
-          const float inv = a.v_scale / L;
-          uint16_t* dst = a.out + static_cast<int64_t>(t) * a.out_row_stride +
-                          static_cast<int64_t>(g * kG + h) * a.out_head_stride + d0;
-#pragma unroll
-          for (int q = 0; q < kE / 8; ++q)
-            *reinterpret_cast<uint4*>(dst + 8 * q) =
-                make_uint4(pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv),
-                           pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
-                           pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
-                           pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
-          if (a.lse != nullptr && lane % kLanesPerHead == 0)
-            a.lse[static_cast<int64_t>(t) * a.lse_row_stride + g * kG + h] = (M + log2f(L)) * kLn2;
-        }
-      }
-      // this warp is done with window m (its reads of the window's partials included)
-      __syncwarp();
-      if (lane == 0) add_release_gpu(w.merged + m, 1);
-    }
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + partials
     // Warps 4-11 take every chunk in turn, two warps per 32-lane TMEM quadrant: warp part p owns
     // key columns [64 p, 64 p + 64) of S and head-dim columns [64 p, 64 p + 64) of O. The two
     // parts' row maxima meet in shared memory; P (fp16, two keys per column) goes to columns
     // 32 p .. 32 p + 31 of the same S buffer once both parts have read their S columns. Then the
     // partial of chunk c - 1 (O / l as fp16, with (log2-sum-exp, V exponent)) is stored while
-    // PV(c) runs; a window's last chunk stores its own partial at once and counts the window done.
+    // PV(c) runs.
     const int sw = warp - 4, quad = sw & 3, part = sw >> 2;
     const int row = quad * 32 + lane;  // TMEM lane
     const int j = row / kG, h = row % kG;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = a.scale_log2;
-    // the partial of chunk cp: O read from TMEM buffer cp % 2 once its PV is done, scaled by 1 / l
-    // and stored as fp16 rows with their (log2-sum-exp, exponent)
-    auto store_partial = [&](int cp, const ChunkDesc* dp, float m_row, float l_part, int e) -> bool {
-      const int Xp = cp & 1;
-      uint32_t o[64];
-      if (!g_warp_wait(&ctl->pv_done[Xp], (cp >> 1) & 1, ctl, a.err_word)) return false;
-      tc::fence_after_sync();
-      if (sw == 0 && lane == 0) GTRACE(kGtE0, cp);
-      const uint32_t to = tmem + 256 + Xp * 128 + lane_off + 64 * part;
-      tc::ld32(to, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-      tc::ld32(to + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-      tc::wait_ld();
-      // O buffer cp % 2 is read: PV(cp + 2) may overwrite it
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->o_free[Xp]);
-      const float lt = l_part + ctl->lsum[cp & 3][part ^ 1][row];
-      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      if (j < dp->n_tok) {
-        const int64_t prow =
-            ((static_cast<int64_t>((dp->win % kGatherRing) * kGatherWinTok + dp->tl[j]) * a.num_kv_heads + dp->g) *
-                 a.k + dp->slot[j]) * kG + h;
-        // 128 bytes of the row as four 32-byte stores: every store fills whole sectors
-        uint16_t* dst = w.part + prow * kHeadDim + 64 * part;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t* f = &o[16 * q];
-          uint32_t wv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            wv[i] = pack_f16(__uint_as_float(f[2 * i]) * inv_l, __uint_as_float(f[2 * i + 1]) * inv_l);
-          st_global_v8(dst + 16 * q, wv);
-        }
-        if (part == 0) *reinterpret_cast<float2*>(w.ml + prow) = make_float2(m_row + log2f(lt), static_cast<float>(e));
-      }
-      if (sw == 0 && lane == 0) GTRACE(kGtE1, cp);
-      return true;
-    };
-    float m_prev = 0.f, l_prev = 0.f;  // the pending chunk: row maximum (log2 units), this part's sum
-    int e_prev = 0;                    // the pending chunk: its V image holds V * 2^-e
-    const ChunkDesc* dprev = nullptr;  // the pending chunk (its partial not yet stored)
+    float m_prev = 0.f, l_prev = 0.f;  // chunk c - 1: row maximum (log2 units), this part's sum
+    int e_prev = 0;                    // chunk c - 1: its V image holds V * 2^-e
+    const ChunkDesc* dprev = nullptr;
     for (int c = 0;; ++c) {
       const int ds = c % kDescRing, X = c & 1;
       if (!g_warp_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
       const ChunkDesc* d = &ctl->desc[ds];
       const bool end = d->end != 0;
       uint32_t v[64];
-      // the exponent of this chunk's V image, for its partial
+      // the exponent of this chunk's V image, for its partial one iteration later
       const int e_cur = end ? 0 : __ldg(a.vconv_exp + (static_cast<int64_t>(d->req) * a.max_blocks + d->b) *
                                                           a.num_kv_heads + d->g);
       if (!end) {
@@ -1087,7 +823,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         tc::st32(tmem + X * 128 + lane_off + 32 * part, pk);
         lp = l0 + l1;
-        // four slots: the partner reads slot c & 3 when it stores this chunk's partial
+        // four slots: the partner reads slot c & 3 in the next iteration
         ctl->lsum[c & 3][part][row] = lp;
         tc::wait_st();
         tc::fence_before_sync();
@@ -1095,43 +831,51 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (lane == 0) mbar_arrive(&ctl->p_full[X]);
         if (sw == 0 && lane == 0) GTRACE(kGtSm1, c);
       }
-      // ---- partials: the pending chunk's (c - 1), then, for the CTA's last chunk of its window,
-      // chunk c's at once (one code path for both)
-      bool fail = false;
-#pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        int cp = c - 1;
-        if (pass == 1) {
-          if (end || !d->wlast) break;
-          // the partner's row sum of chunk c is posted before this barrier
-          asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-          m_prev = m;
-          l_prev = lp;
-          e_prev = e_cur;
-          dprev = d;
-          cp = c;
-        } else if (dprev == nullptr) {
-          continue;
-        }
-        if (!store_partial(cp, dprev, m_prev, l_prev, e_prev)) {
-          fail = true;
-          break;
-        }
+      // ---- partial of chunk c - 1
+      if (c >= 1) {
+        // O(c - 1), read once P(c) is out (so PV(c) is not held up, and S and O never share the
+        // registers)
+        uint32_t o[64];
+        if (!g_warp_wait(&ctl->pv_done[X ^ 1], ((c - 1) >> 1) & 1, ctl, a.err_word)) break;
+        tc::fence_after_sync();
+        if (sw == 0 && lane == 0) GTRACE(kGtE0, c - 1);
+        const uint32_t to = tmem + 256 + (X ^ 1) * 128 + lane_off + 64 * part;
+        tc::ld32(to, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tc::ld32(to + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tc::wait_ld();
+        // O buffer (c - 1) % 2 is read: PV(c + 1) may overwrite it
+        tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
-          // this warp's partials of the window are stored
-          if (pass == 1) add_release_gpu(w.done + dprev->win, 1);
+        if (lane == 0) mbar_arrive(&ctl->o_free[X ^ 1]);
+        const float lt = l_prev + ctl->lsum[(c - 1) & 3][part ^ 1][row];
+        const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+        if (j < dprev->n_tok) {
+          const int64_t prow =
+              ((static_cast<int64_t>(dprev->tr[j]) * a.num_kv_heads + dprev->g) * a.k + dprev->slot[j]) * kG + h;
+          // 128 bytes of the row as four 32-byte stores: every store fills whole sectors
+          uint16_t* dst = w.part + prow * kHeadDim + 64 * part;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t* f = &o[16 * q];
+            uint32_t wv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              wv[i] = pack_f16(__uint_as_float(f[2 * i]) * inv_l, __uint_as_float(f[2 * i + 1]) * inv_l);
+            st_global_v8(dst + 16 * q, wv);
+          }
+          if (part == 0)
+            w.ml[prow] = make_float2(m_prev + log2f(lt), static_cast<float>(e_prev));
         }
-        dprev = nullptr;
+        // this warp is done with descriptor c - 1
+        if (sw == 0 && lane == 0) GTRACE(kGtE1, c - 1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->desc_empty[(c - 1) % kDescRing]);
       }
-      if (fail || end) break;
-      if (!d->wlast) {
-        m_prev = m;
-        l_prev = lp;
-        e_prev = e_cur;
-        dprev = d;
-      }
+      if (end) break;
+      m_prev = m;
+      l_prev = lp;
+      e_prev = e_cur;
+      dprev = d;
     }
   }
   tc::fence_before_sync();
@@ -1141,6 +885,61 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc::dealloc(tmem, 512);
   }
   if (threadIdx.x == 0) GTRACE(kGtEnd, 0);
+}
+
+// ------------------------------------------------------------------------------------------
+// merge kernel: one warp per (segment token, kv head)
+// ------------------------------------------------------------------------------------------
+// The token's n partials P_s (O_s / l_s stored as fp16 times 2^-e_s) and their base-2
+// log-sum-exps L_s combine to out = v_scale * sum_s 2^(L_s - M) 2^e_s P_s / sum_s 2^(L_s - M)
+// with M = max_s L_s; the row's log-sum-exp is M + log2(sum_s 2^(L_s - M)) (times ln 2).
+template <int kG>
+__global__ void __launch_bounds__(kMergeWarps * 32) gather_merge_kernel(const AttendArgs a, const GatherWs w) {
+  constexpr int kLanesPerHead = 32 / kG;        // 4 (GQA 8) or 2 (GQA 16)
+  constexpr int kE = kHeadDim / kLanesPerHead;  // dims per lane: 32 or 64
+  const int lane = threadIdx.x & 31;
+  const int hkv = a.num_kv_heads;
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (x >= static_cast<int64_t>(w.T1 - w.T0) * hkv) return;
+  const int tr = static_cast<int>(x / hkv), g = static_cast<int>(x % hkv);
+  const int n = __ldg(w.nparts + tr);
+  if (n <= 0) return;  // the index kernel wrote this token's zero output
+  const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
+  const int64_t prow0 = x * a.k * kG + h;  // partial row of slot s: prow0 + s * kG
+  float M = -INFINITY;
+  for (int s = 0; s < n; ++s) M = fmaxf(M, __ldg(&w.ml[prow0 + static_cast<int64_t>(s) * kG].x));
+  float L = 0.f;
+  float acc[kE];
+#pragma unroll
+  for (int i = 0; i < kE; ++i) acc[i] = 0.f;
+  for (int s = 0; s < n; ++s) {
+    const int64_t prow = prow0 + static_cast<int64_t>(s) * kG;
+    const float2 ml = __ldg(&w.ml[prow]);
+    const float wl = exp2f(ml.x - M);
+    L += wl;
+    const float f = wl * exp2f(ml.y);
+    const uint4* src = reinterpret_cast<const uint4*>(w.part + prow * kHeadDim + d0);
+#pragma unroll
+    for (int q = 0; q < kE / 8; ++q) {
+      const uint4 u = __ldg(src + q);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[8 * q + 2 * i] = fmaf(f, g_f16_lo(wd[i]), acc[8 * q + 2 * i]);
+        acc[8 * q + 2 * i + 1] = fmaf(f, g_f16_hi(wd[i]), acc[8 * q + 2 * i + 1]);
+      }
+    }
+  }
+  const float inv = a.v_scale / L;
+  const int64_t t = static_cast<int64_t>(w.T0) + tr;
+  uint16_t* dst = a.out + t * a.out_row_stride + static_cast<int64_t>(g * kG + h) * a.out_head_stride + d0;
+#pragma unroll
+  for (int q = 0; q < kE / 8; ++q)
+    *reinterpret_cast<uint4*>(dst + 8 * q) =
+        make_uint4(pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv), pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                   pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv), pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+  if (a.lse != nullptr && lane % kLanesPerHead == 0)
+    a.lse[t * a.lse_row_stride + g * kG + h] = (M + log2f(L)) * kLn2;
 }
 
 }  // namespace
@@ -1165,75 +964,84 @@ bool prefill_gather_supported(const AttendArgs& a) {
   const bool cache_ok =
       a.kv_dtype != PBS_KV_BF16 || a.page_stride_bytes == static_cast<int64_t>(a.num_kv_heads) * 8192;
   return a.sparse_bt == nullptr && cache_ok && (a.group == 8 || a.group == 16) && a.max_blocks <= kGatherMaxBlocks &&
-         a.num_reqs <= 65535 && a.num_rows <= kGatherMaxTokens && a.num_pages * a.num_kv_heads <= 0x7fffffffLL &&
-         a.out_head_stride % 8 == 0 && a.out_row_stride % 8 == 0 && reinterpret_cast<uintptr_t>(a.out) % 16 == 0 &&
-         a.q_head_stride % 8 == 0 && a.q_row_stride % 8 == 0 && reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
+         a.num_reqs <= 65535 && a.num_pages * a.num_kv_heads <= 0x7fffffffLL && a.out_head_stride % 8 == 0 &&
+         a.out_row_stride % 8 == 0 && reinterpret_cast<uintptr_t>(a.out) % 16 == 0 && a.q_head_stride % 8 == 0 &&
+         a.q_row_stride % 8 == 0 && reinterpret_cast<uintptr_t>(a.q) % 16 == 0;
 }
 
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // The workspace: the conversion kernels' images (V and its exponents, then K, for every (request,
-// block, kv head); the K images are used by fp8 / NVFP4 caches only), the partial ring (the
-// partials and their (log2-sum-exp, exponent) pairs of kGatherRing windows), each token's partial
-// count, the bucket entries, the chunk records, the window records and the windows' counters.
+// block, kv head); the K images are used by fp8 / NVFP4 caches only), then per segment the
+// partials, their (log2-sum-exp, exponent) pairs, each token's partial count, the bucket entries,
+// the chunk records and the window records.
 struct GatherLayout {
-  size_t images, part, ml, nparts, pairs, chunks, wins, done, merged, abort_all, total;
+  size_t images, part, ml, nparts, pairs, chunks, wins, total;
   int num_win, ccap;
 };
 
-GatherLayout gather_layout(int64_t tokens, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks) {
+GatherLayout gather_layout(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks) {
   GatherLayout L = {};
   const int group = num_heads / num_kv_heads;
   const int tok = kGRows / (group > 8 ? group : 8);
-  L.num_win = static_cast<int>(tokens / kGatherWinTok + 2 * static_cast<int64_t>(num_reqs) + 1);
+  L.num_win = static_cast<int>(seg_tokens / kGatherWinTok + 2 * static_cast<int64_t>(num_reqs) + 1);
   // chunks of one kv head in a window: sum over its buckets of ceil(tokens / tok) <= (entries +
   // buckets * (tok - 1)) / tok, with entries <= 256 k and buckets <= min(max_blocks, entries)
   const int64_t entries = static_cast<int64_t>(kGatherWinTok) * k;
   const int64_t buckets = std::min<int64_t>(max_blocks, entries);
   L.ccap = static_cast<int>(((entries + buckets * (tok - 1)) / tok + 1) * num_kv_heads);
-  const size_t ring_rows = static_cast<size_t>(kGatherRing) * kGatherWinTok * num_heads * k;
   size_t off = 0;
   L.images = off;
   off = align256(off + prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, PBS_KV_FP8_E4M3));
   L.part = off;
-  off = align256(off + ring_rows * kHeadDim * 2);
+  off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * kHeadDim * 2);
   L.ml = off;
-  off = align256(off + ring_rows * 8);
+  off = align256(off + static_cast<size_t>(seg_tokens) * num_heads * k * 8);
   L.nparts = off;
-  off = align256(off + static_cast<size_t>(tokens) * 4);
+  off = align256(off + static_cast<size_t>(seg_tokens) * 4);
   L.pairs = off;
   off = align256(off + static_cast<size_t>(L.num_win) * kGatherWinTok * k * 4);
   L.chunks = off;
   off = align256(off + static_cast<size_t>(L.num_win) * L.ccap * 16);
   L.wins = off;
   off = align256(off + static_cast<size_t>(L.num_win) * 8 * 4);
-  L.done = off;
-  off = align256(off + static_cast<size_t>(L.num_win) * 4);
-  L.merged = off;
-  off = align256(off + static_cast<size_t>(L.num_win) * 4);
-  L.abort_all = off;
-  off = align256(off + 4);
   L.total = off;
   return L;
 }
 }  // namespace
 
-size_t gather_workspace_bytes(int64_t tokens, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks) {
-  if (tokens <= 0 || tokens > kGatherMaxTokens || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
-      prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, PBS_KV_FP8_E4M3) == 0)
-    return 0;
-  return gather_layout(tokens, num_reqs, num_heads, num_kv_heads, k, max_blocks).total;
+size_t gather_workspace_bytes(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k,
+                              int max_blocks) {
+  if (prefill_tc_workspace_bytes(num_reqs, num_kv_heads, max_blocks, PBS_KV_FP8_E4M3) == 0) return 0;
+  return gather_layout(seg_tokens, num_reqs, num_heads, num_kv_heads, k, max_blocks).total;
+}
+
+int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks,
+                              size_t ws_bytes) {
+  if (gather_workspace_bytes(kGatherWinTok, num_reqs, num_heads, num_kv_heads, k, max_blocks) == 0) return 0;
+  if (total_q <= kGatherMaxSegment &&
+      gather_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, k, max_blocks) <= ws_bytes)
+    return total_q;
+  // the largest multiple of the window that fits
+  int64_t lo = 0, hi = std::min(total_q, kGatherMaxSegment) / kGatherWinTok;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (gather_workspace_bytes(mid * kGatherWinTok, num_reqs, num_heads, num_kv_heads, k, max_blocks) <= ws_bytes)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo * kGatherWinTok;
 }
 
 template <int kG>
 cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
                             size_t ws_bytes, cudaStream_t stream) {
-  const size_t need = gather_workspace_bytes(args.num_rows, args.num_reqs, args.num_heads, args.num_kv_heads, args.k,
-                                             args.max_blocks);
-  if (need == 0 || ws_bytes < need) return cudaErrorInvalidValue;
-  const GatherLayout L =
-      gather_layout(args.num_rows, args.num_reqs, args.num_heads, args.num_kv_heads, args.k, args.max_blocks);
+  const int64_t seg = gather_segment_tokens(args.num_rows, args.num_reqs, args.num_heads, args.num_kv_heads, args.k,
+                                            args.max_blocks, ws_bytes);
+  if (seg <= 0) return cudaErrorInvalidValue;
+  const GatherLayout L = gather_layout(seg, args.num_reqs, args.num_heads, args.num_kv_heads, args.k, args.max_blocks);
   uint8_t* base = static_cast<uint8_t*>(ws);
   // the images: V (fp16) and its exponents for every cache format, K (bf16) for fp8 / NVFP4
   AttendArgs a = args;
@@ -1251,10 +1059,6 @@ cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, c
   w.pairs = reinterpret_cast<int32_t*>(base + L.pairs);
   w.chunks = reinterpret_cast<int4*>(base + L.chunks);
   w.wins = reinterpret_cast<int32_t*>(base + L.wins);
-  w.done = reinterpret_cast<int32_t*>(base + L.done);
-  w.merged = reinterpret_cast<int32_t*>(base + L.merged);
-  w.abort_all = reinterpret_cast<int32_t*>(base + L.abort_all);
-  w.num_win = L.num_win;
   w.ccap = L.ccap;
   w.tok_per_chunk = kGRows / kG;
 
@@ -1265,26 +1069,28 @@ cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, c
   e = cudaFuncSetAttribute(gather_attend_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kGSmem));
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
+  int dev = 0, sms = 148;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  gather_index_kernel<<<w.num_win, kIdxThreads, idx_smem, stream>>>(a, w);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // the merge warps of every CTA wait for windows that all CTAs attend: every CTA must be
-  // resident, which a cooperative launch of one CTA per SM guarantees
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(std::max(sms, 1)));
-  cfg.blockDim = dim3(kGThreads);
-  cfg.dynamicSmemBytes = kGSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gather_attend_kernel<kG>, kv_map, q_map, a, w);
+  for (int64_t t0 = 0; t0 < a.num_rows; t0 += seg) {
+    w.T0 = static_cast<int32_t>(t0);
+    w.T1 = static_cast<int32_t>(std::min<int64_t>(a.num_rows, t0 + seg));
+    w.num_win = static_cast<int32_t>((w.T1 - w.T0) / kGatherWinTok + 2 * static_cast<int64_t>(a.num_reqs) + 1);
+    gather_index_kernel<<<w.num_win, kIdxThreads, idx_smem, stream>>>(a, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    gather_attend_kernel<kG><<<static_cast<unsigned>(std::max(sms, 1)), kGThreads, kGSmem, stream>>>(kv_map, q_map,
+                                                                                                      a, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t units = static_cast<int64_t>(w.T1 - w.T0) * a.num_kv_heads;
+    gather_merge_kernel<kG><<<static_cast<unsigned>((units + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0,
+                              stream>>>(a, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,

@@ -129,36 +129,37 @@ cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, co
 
 // Prefill attend by key block (tcgen05; bf16 packed cache, or fp8 / NVFP4 through converted
 // images; GQA 8 or 16): the tile kernel's conversion kernels write the V (and fp8 / NVFP4 K)
-// images, an index kernel buckets each 256-token window's tokens by selected block, and a
-// persistent cooperative kernel attends every (block, kv head) bucket 16 gathered tokens at a
-// time, stores one partial per (token, block) into a ring of kGatherRing windows and merges each
-// window's partials once every CTA has stored them. Workspace (caller-owned): the images, the
-// partial ring, per-token partial counts, the buckets and the windows' counters.
+// images, an index kernel buckets each 256-token window's tokens by selected block, a
+// persistent kernel attends every (block, kv head) bucket 16 gathered tokens at a time and
+// stores one partial per (token, block), and a merge kernel combines each token's partials.
+// Workspace (caller-owned): the images, then per segment of tokens the fp16 partials and their
+// (log2-sum-exp, exponent) pairs, per-token partial counts and the buckets. A call is processed
+// in segments of at most `gather_segment_tokens` tokens, one index + attend + merge launch each.
 constexpr int kGatherWinTok = 256;      // tokens per window (request-relative)
 constexpr int kGatherMaxBlocks = 8192;  // page-table width the index kernel's histogram covers
-constexpr int kGatherRing = 2;          // windows whose partials are live at once
-constexpr int64_t kGatherMaxTokens = int64_t(1) << 24;
+constexpr int64_t kGatherMaxSegment = int64_t(1) << 19;
 
 struct GatherWs {
-  uint16_t* part;      // fp16 [ring][256][Hkv][k][G][128]: per-(token, block) output / l * 2^-e
-  float2* ml;          // [ring][256][Hkv][k][G]: (log2-sum-exp of the block's logits, e)
-  int32_t* nparts;     // [tokens]: partials of each token (its distinct valid blocks)
-  int32_t* pairs;      // bucket entries: window token << 12 | (partials - 1) << 6 | partial slot
+  uint16_t* part;      // fp16 [seg][Hkv][k][G][128]: per-(token, block) output / l * 2^-e
+  float2* ml;          // [seg][Hkv][k][G]: (log2-sum-exp of the block's logits, e)
+  int32_t* nparts;     // [seg]: partials of each token (its distinct valid blocks)
+  int32_t* pairs;      // bucket entries: segment token << 12 | (partials - 1) << 6 | partial slot
   int4* chunks;        // [windows][ccap]: (block | kv head << 13, first entry, tokens, physical block)
-  int32_t* wins;       // [windows][8]: request, its first token, context, seq_len, chunks, first and end token
-  int32_t* done;       // [windows]: softmax warps whose partials of the window are stored
-  int32_t* merged;     // [windows]: merge warps that have merged the window
-  int32_t* abort_all;  // set by a CTA that gave up waiting
-  int32_t num_win;     // windows of the call (upper bound; surplus ones are empty)
+  int32_t* wins;       // [windows][8]: request, first token, context, seq_len, chunks
+  int32_t T0, T1;      // segment [T0, T1) of the call's tokens
+  int32_t num_win;     // windows of the segment (upper bound; surplus ones are empty)
   int32_t ccap;        // chunk records per window
   int32_t tok_per_chunk;
 };
 
 bool prefill_gather_supported(const AttendArgs& a);
-// Workspace bytes of a call with `tokens` prefill tokens (0: out of range).
-size_t gather_workspace_bytes(int64_t tokens, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks);
+size_t gather_workspace_bytes(int64_t seg_tokens, int num_reqs, int num_heads, int num_kv_heads, int k,
+                              int max_blocks);
+// Tokens per segment a workspace of `ws_bytes` allows (0: not even one window).
+int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int num_kv_heads, int k, int max_blocks,
+                              size_t ws_bytes);
 // `kv_map`: the per-block map of a packed bf16 cache (as for the tile kernel; unused for fp8 /
-// NVFP4); `q_map`: the 5-D {64, 8, 2, heads / 8, tokens} map with a {64, 8, 2, G / 8, 1} box.
+// NVFP4); `q_map`: {128, heads, tokens} with a {64, G, 1} box.
 cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
                                   size_t ws_bytes, cudaStream_t stream);
 // The conversion kernels of both tcgen05 prefill kernels: V (and for fp8 / NVFP4 caches K) of

@@ -78,8 +78,8 @@ def test_prefill_varlen_bf16(pbs):
 
 
 def test_prefill_varlen_bf16_gathered(pbs):
-    """The gathered-row prefill kernel at full size (88 windows through its two-window partial
-    ring), sampled rows against the oracle."""
+    """The gathered-row prefill kernel at full size (several token segments on the default
+    2 GiB workspace), sampled rows against the oracle."""
     b = workloads.prefill(device="cuda")
     _prefill_parity(pbs, b, 48, 6, kernel="gather")
 
