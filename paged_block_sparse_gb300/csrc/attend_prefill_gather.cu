@@ -148,6 +148,17 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
                : "memory");
 }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The lower / upper half of an f16x2 word as float (exact).
 __device__ __forceinline__ float g_f16_lo(uint32_t x) {
   float f;
@@ -688,54 +699,72 @@ __global__ void __launch_bounds__(kGThreads, 1)
       constexpr uint32_t kIdescS = tc::idesc_f16(128, 128, true, false, false);
       constexpr uint32_t kIdescPV = tc::idesc_f16(128, 128, false, false, true);  // fp16 P, fp16 V
       int prev_y = 0, prev_item = 0;
-      for (int c = 0;; ++c) {
+      bool ok = true;
+      for (int c = 0; ok; ++c) {
         const int ds = c % kDescRing;
         if (!g_wait(&ctl->desc_full[ds], (c / kDescRing) & 1, ctl, a.err_word)) break;
         const ChunkDesc* d = &ctl->desc[ds];
         const int end = d->end;
         const int Y = d->ybuf, item = d->item;
+        const bool new_item = c >= 1 && (end || item != prev_item);
         // chunk c starts a new item (or there is none): the S of the previous item's last chunk,
         // issued before, is the last reader of its K buffer
-        if (c >= 1 && (end || item != prev_item)) tc::commit(&ctl->k_empty[prev_y]);
-        if (!end) {
-          const int X = c & 1;
+        if (new_item) tc::commit(&ctl->k_empty[prev_y]);
+        // S(c) and PV(c - 1), whichever has its operands first: S(c) waits for the chunk's Q and K,
+        // PV(c - 1) for P(c - 1), its V and a free O buffer, and neither holds up the other. S(c)
+        // reuses the S buffer of chunk c - 2, whose PV was issued in the previous iteration.
+        bool s_todo = !end, pv_todo = c >= 1;
+        const int X = c & 1, cp = c - 1, Xp = cp & 1;
+        const unsigned long long t0 = global_timer_ns();
+        while (s_todo || pv_todo) {
+          bool progressed = false;
+          if (pv_todo && mbar_test(&ctl->p_full[Xp], (cp >> 1) & 1) &&
+              mbar_test(&ctl->v_full[prev_y], (prev_item >> 1) & 1) &&
+              (cp < 2 || mbar_test(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1))) {
+            // O(X') = P V: P (fp16, two keys per column) in columns 0..63 of S buffer X', V the
+            // item's fp16 image (keys 16ks.. = two 8-key groups 1 KiB apart; dims in two 64-wide
+            // MN atoms 16 KiB apart)
+            tc::fence_after_sync();
+            const uint32_t v_addr = smem_u32(v_s + prev_y * kGTile);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              tc::mma_ts(tmem + 256 + Xp * 128, tmem + Xp * 128 + ks * 8,
+                         tc::smem_desc_sw128(v_addr + ks * 2048, kGHalf, 1024), kIdescPV, ks > 0);
+            tc::commit(&ctl->pv_done[Xp]);
+            GTRACE(kGtPV, cp);
+            // the previous chunk was its item's last: its V buffer is free once this PV completes
+            if (new_item) tc::commit(&ctl->v_empty[prev_y]);
+            mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
+            pv_todo = false;
+            progressed = true;
+          }
           // the K buffer of item n completes once per use: phase (n / 2) & 1
-          if (!g_wait(&ctl->k_full[Y], (item >> 1) & 1, ctl, a.err_word)) break;
-          if (!g_wait(&ctl->q_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
-          tc::fence_after_sync();
-          const uint32_t q_addr = smem_u32(q_s + X * kGQBytes);
-          const uint32_t k_addr = smem_u32(k_s + Y * kGTile);
-          // dims 16ks..: Q half ks/4 1 KiB into each 2 KiB pair of 8-row atoms; K half ks/4 16 KiB
-          // apart, its 8-key groups 1 KiB apart
+          if (s_todo && mbar_test(&ctl->k_full[Y], (item >> 1) & 1) && mbar_test(&ctl->q_full[X], (c >> 1) & 1)) {
+            tc::fence_after_sync();
+            const uint32_t q_addr = smem_u32(q_s + X * kGQBytes);
+            const uint32_t k_addr = smem_u32(k_s + Y * kGTile);
+            // dims 16ks..: Q half ks/4 1 KiB into each 2 KiB pair of 8-row atoms; K half ks/4 16
+            // KiB apart, its 8-key groups 1 KiB apart
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ss(tmem + X * 128, tc::smem_desc_sw128(q_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048),
-                       tc::smem_desc_sw128(k_addr + (ks >> 2) * kGHalf + (ks & 3) * 32, 16, 1024), kIdescS, ks > 0);
-          tc::commit(&ctl->s_full[X]);
-          tc::commit(&ctl->q_empty[X]);
-          GTRACE(kGtS, c);
-        }
-        if (c >= 1) {
-          // PV of the previous chunk: O(X') = P V, P (fp16, two keys per column) in columns
-          // 0..63 of S buffer X', V the item's fp16 image
-          const int cp = c - 1, Xp = cp & 1;
-          if (!g_wait(&ctl->p_full[Xp], (cp >> 1) & 1, ctl, a.err_word)) break;
-          if (!g_wait(&ctl->v_full[prev_y], (prev_item >> 1) & 1, ctl, a.err_word)) break;
-          // O buffer X' was read by the epilogue of chunk cp - 2
-          if (cp >= 2 && !g_wait(&ctl->o_free[Xp], ((cp >> 1) - 1) & 1, ctl, a.err_word)) break;
-          tc::fence_after_sync();
-          const uint32_t v_addr = smem_u32(v_s + prev_y * kGTile);
-          // keys 16ks..16ks+15 = two 8-key groups (1 KiB apart); dims in two 64-wide MN atoms
-          // 16 KiB apart
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ts(tmem + 256 + Xp * 128, tmem + Xp * 128 + ks * 8,
-                       tc::smem_desc_sw128(v_addr + ks * 2048, kGHalf, 1024), kIdescPV, ks > 0);
-          tc::commit(&ctl->pv_done[Xp]);
-          GTRACE(kGtPV, cp);
-          // the previous chunk was its item's last: its V buffer is free once this PV completes
-          if (end || item != prev_item) tc::commit(&ctl->v_empty[prev_y]);
-          mbar_arrive(&ctl->desc_empty[cp % kDescRing]);
+            for (int ks = 0; ks < 8; ++ks)
+              tc::mma_ss(tmem + X * 128, tc::smem_desc_sw128(q_addr + (ks >> 2) * 1024 + (ks & 3) * 32, 16, 2048),
+                         tc::smem_desc_sw128(k_addr + (ks >> 2) * kGHalf + (ks & 3) * 32, 16, 1024), kIdescS,
+                         ks > 0);
+            tc::commit(&ctl->s_full[X]);
+            tc::commit(&ctl->q_empty[X]);
+            GTRACE(kGtS, c);
+            s_todo = false;
+            progressed = true;
+          }
+          if (!progressed) {
+            if (global_timer_ns() - t0 > kGWaitNs) {
+              set_err(a.err_word, PBS_DEVERR_TIMEOUT);
+              atomicExch(&ctl->abort, 1);
+              ok = false;
+              break;
+            }
+            __nanosleep(20);
+          }
         }
         if (end) break;
         prev_y = Y;
