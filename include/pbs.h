@@ -100,8 +100,10 @@ typedef struct CUstream_st* pbs_stream_t;
 #define PBS_PREFILL_TILE    2  /* tcgen05 tile kernel: GQA 8 or 16, top-k <= 16, page table <= 65535
                                   blocks, 16-byte aligned q / out rows; a packed bf16 cache, or an
                                   fp8 / NVFP4 cache with its workspace (pbs_prefill_tile_workspace_bytes) */
-#define PBS_PREFILL_GATHER  3  /* tcgen05 gathered-row kernel: as the tile kernel but page tables up to
-                                  8192 blocks and top-k <= 64; needs its workspace; no prebuilt table */
+#define PBS_PREFILL_GATHER  3  /* tcgen05 gathered-row kernel: GQA 8 or 16, top-k <= 64, page table
+                                  <= 8192 blocks, a packed bf16 cache or an fp8 / NVFP4 cache, 16-byte
+                                  aligned q / out rows; needs its workspace
+                                  (pbs_prefill_workspace_bytes); no prebuilt table */
 
 /*
  * Optional tuning of one attend call (a NULL pointer or an all-zero struct = the library's own
@@ -287,12 +289,12 @@ PBS_API int pbs_sparse_decode_attention_noalloc(
  * workspace:
  *   workspace   optional (NULL, 0), caller-owned device memory, contents need no initial value.
  *               With a 256-byte aligned workspace of at least
- *               pbs_prefill_workspace_bytes(256, num_reqs, num_heads, num_kv_heads, topk_k,
- *               max_blocks) bytes, calls the gathered-row kernel takes (bf16 cache packed as
- *               [pages][Hkv][16 rows][K | V], GQA 8 or 16, max_blocks <= 8192, 16-byte aligned q
- *               and out rows) run on it: per-block partial outputs and the per-window token buckets
- *               live in the workspace, and the call is processed in as many token segments as its
- *               size requires (pbs_prefill_workspace_bytes(total_q, ...) bytes: one segment).
+ *               pbs_prefill_workspace_bytes(512, num_reqs, num_heads, num_kv_heads, topk_k,
+ *               max_blocks) bytes, calls the gathered-row kernel takes (see PBS_PREFILL_GATHER and
+ *               pbs_prefill_kernel_choice) run on it: the converted K / V images, per-block partial
+ *               outputs and the per-window token buckets live in the workspace, and the call is
+ *               processed in as many token segments as its size requires
+ *               (pbs_prefill_workspace_bytes(total_q, ...) bytes: one segment).
  *               Otherwise the tcgen05 tile kernel or the token-centric kernel runs. The tile
  *               kernel, given a 256-byte aligned workspace of at least
  *               pbs_prefill_tile_workspace_bytes(num_reqs, num_kv_heads, max_blocks, kv_dtype)
@@ -343,10 +345,11 @@ PBS_API int pbs_prefill_kernel_choice(int32_t total_q, int32_t num_reqs, int32_t
 /*
  * Bytes of the workspace with which pbs_sparse_prefill_attention runs a call of `total_q`
  * tokens (at most 2^19 per segment) over `num_reqs` requests on its gathered-row kernel in one
- * segment; 0 for invalid arguments. No counterpart on the pages. With total_q = 256 it is the
- * smallest workspace that kernel accepts. For Hq query heads and top-k k the size is about
- * total_q * Hq * k * 264 bytes (fp16 partial outputs and their log-sum-exp pairs) plus the
- * buckets.
+ * segment; 0 for invalid arguments. No counterpart on the pages. With total_q = 512 (one window
+ * of the kernel's token buckets) it is the smallest workspace that kernel accepts. For Hq query
+ * heads and top-k k the size is about total_q * Hq * k * 264 bytes (fp16 partial outputs and
+ * their log-sum-exp pairs), plus the buckets and 64 KiB per (request, block, kv head) of K and
+ * V images (as pbs_prefill_tile_workspace_bytes for an fp8 cache).
  */
 PBS_API size_t pbs_prefill_workspace_bytes(int32_t total_q, int32_t num_reqs, int32_t num_heads,
                                            int32_t num_kv_heads, int32_t topk_k, int32_t max_blocks);

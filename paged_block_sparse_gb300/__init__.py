@@ -309,7 +309,7 @@ def _workspace_args(workspace, rows, num_heads, num_kv_heads, device, stream):
 def prefill_workspace_bytes(total_q: int, num_reqs: int, num_heads: int, num_kv_heads: int, topk: int,
                             max_blocks: int) -> int:
     """Bytes with which the prefill attend runs ``total_q`` tokens on its gathered-row kernel in
-    one segment (``total_q = 256``: the smallest workspace that kernel takes)."""
+    one segment (``total_q = 512``, one window: the smallest workspace that kernel takes)."""
     return int(lib().pbs_prefill_workspace_bytes(int(total_q), int(num_reqs), int(num_heads), int(num_kv_heads),
                                                  int(topk), int(max_blocks)))
 
@@ -377,7 +377,7 @@ def prefill_workspace(total_q: int, num_reqs: int, num_heads: int, num_kv_heads:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     key = (device.index, s.cuda_stream)
     full = prefill_workspace_bytes(total_q, num_reqs, num_heads, num_kv_heads, topk, max_blocks)
-    least = prefill_workspace_bytes(min(total_q, 256), num_reqs, num_heads, num_kv_heads, topk, max_blocks)
+    least = prefill_workspace_bytes(min(total_q, 512), num_reqs, num_heads, num_kv_heads, topk, max_blocks)
     need = max(min(full, PREFILL_WORKSPACE_CAP), least)
     ws = _prefill_workspaces.get(key)
     if ws is None or ws.numel() < need:

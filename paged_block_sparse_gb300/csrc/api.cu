@@ -189,7 +189,7 @@ int encode_q_map_tokens(CUtensorMap* map, const void* q, int num_heads, int grou
 // selected a block, so its work does not grow with the context, but every (token, block) pair
 // costs a partial output written and merged through the workspace. So page tables up to
 // kTileMaxBlocksPerTopk * k blocks take the tile kernel, wider ones the gathered-row kernel (with
-// a workspace that holds at least one 256-token segment; otherwise fp8 / NVFP4 stay on the tile
+// a workspace that holds at least one 512-token segment; otherwise fp8 / NVFP4 stay on the tile
 // kernel and bf16 takes the token-centric kernel). Measured (64/8 heads, top-k 16): the varlen
 // prompts of 2k-8k tokens (64-block table) take 2.39 ms on the tile kernel and 2.37 on the
 // gathered-row kernel; 2 x 4096 tokens after 16k / 32k of context on NVFP4 take 4.69 and 1.89

@@ -13,7 +13,7 @@
 // A tile of consecutive tokens shares few of its selected blocks when the selections are
 // spread over a long context, so a tile that streams the union of its tokens' blocks wastes
 // most of its MMA rows. Here the work is inverted: a work item is one (key block b, kv head g)
-// of a window of 256 consecutive tokens of one request, and its MMA rows are the window's
+// of a window of 512 consecutive tokens of one request, and its MMA rows are the window's
 // tokens that selected b, gathered 16 at a time (x 8 query heads = the 128-row M tile; 8 tokens
 // x 16 heads at GQA 16). Every row of every tile does useful work except in a bucket's last
 // chunk.
@@ -320,12 +320,12 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
       if (k0) {
         atomicAdd(&cnt[b0], 1);
         const int at = atomicAdd(&s_np, 1);
-        pairs_s[at] = (b0 << 14) | (tt << 6) | r0;
+        pairs_s[at] = (b0 << 16) | (tt << 6) | r0;
       }
       if (k1) {
         atomicAdd(&cnt[b1], 1);
         const int at = atomicAdd(&s_np, 1);
-        pairs_s[at] = (b1 << 14) | (tt << 6) | r1;
+        pairs_s[at] = (b1 << 16) | (tt << 6) | r1;
       }
     }
     if (lane == 0) {
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   const int np = s_np;
   for (int p = threadIdx.x; p < np; p += kIdxThreads) {
     const int v = pairs_s[p];
-    const int b = v >> 14, tt = (v >> 6) & 255, rank = v & 63;
+    const int b = v >> 16, tt = (v >> 6) & 1023, rank = v & 63;
     const int at = atomicAdd(&cur[b], 1);
     w.pairs[pair_base + at] = ((ta + tt - w.T0) << 12) | ((s_tn[tt] - 1) << 6) | rank;
   }

@@ -135,7 +135,7 @@ cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, co
 // Workspace (caller-owned): the images, then per segment of tokens the fp16 partials and their
 // (log2-sum-exp, exponent) pairs, per-token partial counts and the buckets. A call is processed
 // in segments of at most `gather_segment_tokens` tokens, one index + attend + merge launch each.
-constexpr int kGatherWinTok = 256;      // tokens per window (request-relative)
+constexpr int kGatherWinTok = 512;      // tokens per window (request-relative)
 constexpr int kGatherMaxBlocks = 8192;  // page-table width the index kernel's histogram covers
 constexpr int64_t kGatherMaxSegment = int64_t(1) << 19;
 

@@ -238,7 +238,7 @@ def test_prefill_kernel_choice_rule():
     assert run("bf16", 64, 8, 16, 400, packed) == "token"
     tile_need = pbs.prefill_tile_workspace_bytes(4, 8, 400, "nvfp4")
     assert run("nvfp4", 64, 8, 16, 400, 8 * 2304, ws=tile_need) == "tile"   # room for the images only
-    gneed = pbs.prefill_workspace_bytes(256, 4, 64, 8, 16, 400)
+    gneed = pbs.prefill_workspace_bytes(512, 4, 64, 8, 16, 400)
     assert run("bf16", 64, 8, 16, 400, packed, ws=gneed) == "gather"
     assert run("bf16", 64, 8, 16, 400, packed, ws=gneed - 256) == "token"
     assert run("bf16", 64, 8, 16, 400, packed, ws=big, table=True) == "token"  # the gathered rows need top-k
@@ -249,8 +249,8 @@ def test_prefill_kernel_choice_rule():
     assert run("bf16", 64, 8, 17, 64, packed) == "token"             # top-k above 16
     assert run("bf16", 64, 8, 16, 64, packed + 16) == "token"        # pages strided inside a larger allocation
     assert run("bf16", 64, 8, 16, 64, packed, table=True) == "tile"  # a prebuilt table: the tile kernel reads it
-    # the gathered-row kernel on request, with a workspace of at least one 256-token window
-    need = pbs.prefill_workspace_bytes(256, 4, 64, 8, 16, 64)
+    # the gathered-row kernel on request, with a workspace of at least one 512-token window
+    need = pbs.prefill_workspace_bytes(512, 4, 64, 8, 16, 64)
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need) == "gather"
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need - 256) == 3
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need, table=True) == 3   # it reads top-k only

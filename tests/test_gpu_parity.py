@@ -587,7 +587,7 @@ def test_attend_strided_pages(pbs):
 
 
 def test_prefill_gather_segments_and_reuse(pbs):
-    """The gathered-row kernel on a workspace that holds one 256-token segment runs the call in
+    """The gathered-row kernel on a workspace that holds one 512-token segment runs the call in
     segments; each token's partials and merge do not depend on the segment, so the output is
     bit-identical to the one-segment run on a larger workspace, and a second call on the same
     (now stale) workspace gives the same bits again."""
@@ -595,7 +595,7 @@ def test_prefill_gather_segments_and_reuse(pbs):
                         pre_ctx_lens=[1500, 0, 6000, 128], future_prob=0.3, seed=70)
     p = b.pre
     nreq, k, mb = p.seq_lens.shape[0], p.topk.shape[-1], p.page_table.shape[1]
-    small = pbs.prefill_workspace_bytes(256, nreq, 64, 8, k, mb)
+    small = pbs.prefill_workspace_bytes(512, nreq, 64, 8, k, mb)
     full = pbs.prefill_workspace_bytes(p.q.shape[0], nreq, 64, 8, k, mb)
     assert 0 < small < full
     outs = []
