@@ -317,15 +317,18 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
           r1 += bj < b1 ? 1 : 0;
         }
       }
+      // the token's pairs take n_t consecutive entries (one atomic per token, not per pair)
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_np, n_t);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const uint32_t lt = lanemask_lt();
       if (k0) {
         atomicAdd(&cnt[b0], 1);
-        const int at = atomicAdd(&s_np, 1);
-        pairs_s[at] = (b0 << 16) | (tt << 6) | r0;
+        pairs_s[base + __popc(km0 & lt)] = (b0 << 16) | (tt << 6) | r0;
       }
       if (k1) {
         atomicAdd(&cnt[b1], 1);
-        const int at = atomicAdd(&s_np, 1);
-        pairs_s[at] = (b1 << 16) | (tt << 6) | r1;
+        pairs_s[base + __popc(km0) + __popc(km1 & lt)] = (b1 << 16) | (tt << 6) | r1;
       }
     }
     if (lane == 0) {
@@ -400,12 +403,22 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
   __syncthreads();
 
   // ---- scatter the entries into their buckets: token << 12 | (partials - 1) << 6 | slot -------
+  // lanes of a warp that fill the same bucket take consecutive places with one atomic
   const int np = s_np;
-  for (int p = threadIdx.x; p < np; p += kIdxThreads) {
-    const int v = pairs_s[p];
-    const int b = v >> 16, tt = (v >> 6) & 1023, rank = v & 63;
-    const int at = atomicAdd(&cur[b], 1);
-    w.pairs[pair_base + at] = ((ta + tt - w.T0) << 12) | ((s_tn[tt] - 1) << 6) | rank;
+  for (int p0 = 0; p0 < np; p0 += kIdxThreads) {
+    const int p = p0 + threadIdx.x;
+    const bool act = p < np;
+    const int v = act ? pairs_s[p] : 0;
+    const int b = act ? v >> 16 : -1 - lane;  // idle lanes in groups of their own
+    const uint32_t grp = __match_any_sync(0xffffffffu, b);
+    const int leader = __ffs(grp) - 1;
+    int at = 0;
+    if (act && lane == leader) at = atomicAdd(&cur[b], __popc(grp));
+    at = __shfl_sync(0xffffffffu, at, leader) + __popc(grp & lanemask_lt());
+    if (act) {
+      const int tt = (v >> 6) & 1023, rank = v & 63;
+      w.pairs[pair_base + at] = ((ta + tt - w.T0) << 12) | ((s_tn[tt] - 1) << 6) | rank;
+    }
   }
   if (threadIdx.x == 0) {
     wrec[0] = r;
@@ -935,29 +948,50 @@ __global__ void __launch_bounds__(kMergeWarps * 32) gather_merge_kernel(const At
   if (n <= 0) return;  // the index kernel wrote this token's zero output
   const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kE;
   const int64_t prow0 = x * a.k * kG + h;  // partial row of slot s: prow0 + s * kG
+  // M: the lanes of head h share the n log-sum-exps (n <= 64), then meet by shuffles
+  const int sub = lane % kLanesPerHead;
   float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, __ldg(&w.ml[prow0 + static_cast<int64_t>(s) * kG].x));
+#pragma unroll
+  for (int i = 0; i < 64 / kLanesPerHead; ++i) {
+    const int s = sub + i * kLanesPerHead;
+    if (s < n) M = fmaxf(M, __ldg(&w.ml[prow0 + static_cast<int64_t>(s) * kG].x));
+  }
+#pragma unroll
+  for (int off = 1; off < kLanesPerHead; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float L = 0.f;
   float acc[kE];
 #pragma unroll
   for (int i = 0; i < kE; ++i) acc[i] = 0.f;
-  for (int s = 0; s < n; ++s) {
-    const int64_t prow = prow0 + static_cast<int64_t>(s) * kG;
-    const float2 ml = __ldg(&w.ml[prow]);
-    const float wl = exp2f(ml.x - M);
-    L += wl;
-    const float f = wl * exp2f(ml.y);
-    const uint4* src = reinterpret_cast<const uint4*>(w.part + prow * kHeadDim + d0);
+  // partials in groups whose loads are all in flight together
+  constexpr int kGrp = kG == 8 ? 4 : 2;
+  for (int s0 = 0; s0 < n; s0 += kGrp) {
+    float2 mlv[kGrp];
+    uint4 u4[kGrp][kE / 8];
 #pragma unroll
-    for (int q = 0; q < kE / 8; ++q) {
-      const uint4 u = __ldg(src + q);
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+    for (int s1 = 0; s1 < kGrp; ++s1)
+      if (s0 + s1 < n) {
+        const int64_t prow = prow0 + static_cast<int64_t>(s0 + s1) * kG;
+        mlv[s1] = __ldg(&w.ml[prow]);
+        const uint4* src = reinterpret_cast<const uint4*>(w.part + prow * kHeadDim + d0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[8 * q + 2 * i] = fmaf(f, g_f16_lo(wd[i]), acc[8 * q + 2 * i]);
-        acc[8 * q + 2 * i + 1] = fmaf(f, g_f16_hi(wd[i]), acc[8 * q + 2 * i + 1]);
+        for (int q = 0; q < kE / 8; ++q) u4[s1][q] = __ldg(src + q);
       }
-    }
+#pragma unroll
+    for (int s1 = 0; s1 < kGrp; ++s1)
+      if (s0 + s1 < n) {
+        const float wl = exp2f(mlv[s1].x - M);
+        L += wl;
+        const float f = wl * exp2f(mlv[s1].y);
+#pragma unroll
+        for (int q = 0; q < kE / 8; ++q) {
+          const uint32_t wd[4] = {u4[s1][q].x, u4[s1][q].y, u4[s1][q].z, u4[s1][q].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[8 * q + 2 * i] = fmaf(f, g_f16_lo(wd[i]), acc[8 * q + 2 * i]);
+            acc[8 * q + 2 * i + 1] = fmaf(f, g_f16_hi(wd[i]), acc[8 * q + 2 * i + 1]);
+          }
+        }
+      }
   }
   const float inv = a.v_scale / L;
   const int64_t t = static_cast<int64_t>(w.T0) + tr;
