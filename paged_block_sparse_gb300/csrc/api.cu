@@ -713,11 +713,15 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
     if (kv_dtype == PBS_KV_BF16)
       st = encode_cache_map_block(&half_map, kv_cache, num_kv_heads, num_pages, page_stride_bytes);
     if (st != PBS_OK) return st;
-    CUtensorMap qmap;
+    CUtensorMap qmap, tile_qmap;
     st = kernel == PBS_PREFILL_GATHER
              ? encode_q_map_tokens(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride)
              : encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
+    // the gathered-row kernel hands the call's dense leading tiles to the tile kernel
+    const bool tile_part = kernel == PBS_PREFILL_GATHER &&
+                           encode_q_map(&tile_qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride) ==
+                               PBS_OK;
     if (kernel == PBS_PREFILL_TILE && workspace != nullptr && aligned(workspace, 256) && num_reqs <= 65535) {
       // with room for the converted V of every (request, block, kv head), the tile kernel applies
       // P in fp16 with one MMA per 16 keys instead of bf16 hi + lo; fp8 / NVFP4 K comes from
@@ -731,8 +735,10 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
           a.kconv = a.vconv + n * pbs::kTileVBytes + ((n * 4 + 255) / 256) * 256;
       }
     }
-    e = kernel == PBS_PREFILL_GATHER ? pbs::launch_prefill_gather(a, half_map, qmap, workspace, workspace_bytes, cs)
-                                     : pbs::launch_prefill_tc(a, half_map, qmap, cs);
+    e = kernel == PBS_PREFILL_GATHER
+            ? pbs::launch_prefill_gather(a, half_map, qmap, tile_part ? &tile_qmap : nullptr, workspace,
+                                         workspace_bytes, cs)
+            : pbs::launch_prefill_tc(a, half_map, qmap, cs);
   }
   return e == cudaSuccess ? PBS_OK : PBS_ERR_CUDA;
 }

@@ -276,9 +276,18 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
 
   // ---- each token's distinct valid blocks, sorted; count per block -------------------------
   const int n = tb - ta;
+  // tokens of the request's leading tiles belong to the tile kernel (AttendArgs::tile_pos_limit)
+  const int dense_tiles = a.tile_pos_limit > 0 ? leading_tiles(s_win[5] - ctx0, ctx0, a.tile_pos_limit, kTok) : 0;
   for (int tt = warp; tt < n; tt += kIdxThreads / 32) {
     const int t = ta + tt;
     const int tr = t - w.T0;
+    if ((t - c0) / kTok < dense_tiles) {
+      if (lane == 0) {
+        s_tn[tt] = 0;
+        w.nparts[tr] = 0;
+      }
+      continue;
+    }
     const int pos = ctx0 + (t - c0);
     const int causal_len = pos + 1 > 0 ? pos + 1 : 0;
     const int own = causal_len > 0 ? pos / kSparseBlock : -1;
@@ -1099,8 +1108,8 @@ int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int 
 }
 
 template <int kG>
-cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
-                            size_t ws_bytes, cudaStream_t stream) {
+cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                            const CUtensorMap* tile_q_map, void* ws, size_t ws_bytes, cudaStream_t stream) {
   const int64_t seg = gather_segment_tokens(args.num_rows, args.num_reqs, args.num_heads, args.num_kv_heads, args.k,
                                             args.max_blocks, ws_bytes);
   if (seg <= 0) return cudaErrorInvalidValue;
@@ -1114,6 +1123,14 @@ cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, c
   a.kconv = a.kv_dtype == PBS_KV_BF16 ? nullptr : a.vconv + n_img * kTileVBytes + ((n_img * 4 + 255) / 256) * 256;
   cudaError_t e = launch_convert_images(a, stream);
   if (e != cudaSuccess) return e;
+  // Tokens whose tile's last position is below 128 k may select every block they see: the tile
+  // kernel takes those tiles on the same images (no union waste, no partials), this kernel the rest.
+  a.tile_pos_limit = 0;
+  if (tile_q_map != nullptr && a.k <= 16 && prefill_tc_supported(a, true)) {
+    a.tile_pos_limit = a.k * kSparseBlock;
+    e = launch_prefill_tc_attend(a, kv_map, *tile_q_map, stream);
+    if (e != cudaSuccess) return e;
+  }
 
   GatherWs w = {};
   w.part = reinterpret_cast<uint16_t*>(base + L.part);
@@ -1156,10 +1173,10 @@ cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, c
   return cudaSuccess;
 }
 
-cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
-                                  size_t ws_bytes, cudaStream_t stream) {
-  return a.group == 16 ? launch_gather_g<16>(a, kv_map, q_map, ws, ws_bytes, stream)
-                       : launch_gather_g<8>(a, kv_map, q_map, ws, ws_bytes, stream);
+cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                                  const CUtensorMap* tile_q_map, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return a.group == 16 ? launch_gather_g<16>(a, kv_map, q_map, tile_q_map, ws, ws_bytes, stream)
+                       : launch_gather_g<8>(a, kv_map, q_map, tile_q_map, ws, ws_bytes, stream);
 }
 
 }  // namespace pbs

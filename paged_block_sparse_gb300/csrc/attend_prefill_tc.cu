@@ -637,7 +637,7 @@ __device__ __forceinline__ void build_tile(const AttendArgs& a, int f, int total
       q_len = __ldg(a.cu_seqlens_q + rr + 1) - cb;
       sl = __ldg(a.seq_lens + rr);
     }
-    const int tiles = (q_len + kTok - 1) / kTok;
+    const int tiles = rr < a.num_reqs ? leading_tiles(q_len, sl - q_len, a.tile_pos_limit, kTok) : 0;
     int incl = tiles;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -975,8 +975,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     int total = 0;
     for (int r0 = 0; r0 < a.num_reqs; r0 += 32) {
       const int rr = r0 + lane;
-      const int q_len = rr < a.num_reqs ? __ldg(a.cu_seqlens_q + rr + 1) - __ldg(a.cu_seqlens_q + rr) : 0;
-      total += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>((q_len + kTok - 1) / kTok));
+      int tiles = 0;
+      if (rr < a.num_reqs) {
+        const int q_len = __ldg(a.cu_seqlens_q + rr + 1) - __ldg(a.cu_seqlens_q + rr);
+        tiles = leading_tiles(q_len, __ldg(a.seq_lens + rr) - q_len, a.tile_pos_limit, kTok);
+      }
+      total += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(tiles));
     }
     const int flat = total * a.num_kv_heads;
     int k = 0;   // descriptors written (slot k & 1)
@@ -1479,6 +1483,28 @@ cudaError_t launch_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUte
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(std::max(sms, 1), tiles));
   prefill_tc_kernel<kG, kF16V><<<grid, kThreadsTc, kTcSmem, stream>>>(kv_map, q_map, a);
   return cudaGetLastError();
+}
+
+template <int kG>
+cudaError_t launch_tc_attend(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                             cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<kG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kTcSmem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (static_cast<int64_t>(a.num_rows) / (kRows / kG) + a.num_reqs + 1) * a.num_kv_heads;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(std::max(sms, 1), tiles));
+  prefill_tc_kernel<kG, true><<<grid, kThreadsTc, kTcSmem, stream>>>(kv_map, q_map, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc_attend(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                                     cudaStream_t stream) {
+  if (a.vconv == nullptr || (a.kv_dtype != PBS_KV_BF16 && a.kconv == nullptr)) return cudaErrorInvalidValue;
+  return a.group == 16 ? launch_tc_attend<16>(a, kv_map, q_map, stream) : launch_tc_attend<8>(a, kv_map, q_map, stream);
 }
 
 cudaError_t launch_prefill_tc(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,

@@ -84,7 +84,19 @@ struct AttendArgs {
   uint8_t* vconv;
   int32_t* vconv_exp;
   uint8_t* kconv;
+  // prefill split between the two tcgen05 kernels (0: none): the tile kernel takes the tiles of
+  // tokens before this position (128 k: every token of the tile may select every block it sees,
+  // so the tile wastes no rows on unselected blocks), the gathered-row kernel every other token
+  int32_t tile_pos_limit;
 };
+
+// Leading tiles of a request (q_len tokens after ctx0 tokens of context) whose last token lies
+// before `limit`; with limit <= 0, all of its ceil(q_len / tok) tiles.
+__host__ __device__ inline int leading_tiles(int q_len, int ctx0, int limit, int tok) {
+  const int tiles = (q_len + tok - 1) / tok;
+  if (limit <= 0 || ctx0 + q_len <= limit) return tiles;
+  return ctx0 >= limit ? 0 : (limit - ctx0) / tok;
+}
 
 // ln 2: a base-2 log-sum-exp (what the kernels track) times this is the natural-log one.
 constexpr float kLn2 = 0.693147180559945309f;
@@ -160,11 +172,16 @@ int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int 
                               size_t ws_bytes);
 // `kv_map`: the per-block map of a packed bf16 cache (as for the tile kernel; unused for fp8 /
 // NVFP4); `q_map`: {128, heads, tokens} with a {64, G, 1} box.
-cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map, void* ws,
-                                  size_t ws_bytes, cudaStream_t stream);
+// `tile_q_map`: the tile kernel's Q map, with which the tile kernel takes the call's dense tiles
+// when it can run the call (AttendArgs::tile_pos_limit); null: the gathered-row kernel takes all.
+cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                                  const CUtensorMap* tile_q_map, void* ws, size_t ws_bytes, cudaStream_t stream);
 // The conversion kernels of both tcgen05 prefill kernels: V (and for fp8 / NVFP4 caches K) of
 // every (request, block, kv head) into a.vconv / a.vconv_exp (/ a.kconv).
 cudaError_t launch_convert_images(const AttendArgs& a, cudaStream_t stream);
+// The tile kernel's attend alone, on images already converted (a.vconv set).
+cudaError_t launch_prefill_tc_attend(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                                     cudaStream_t stream);
 
 // Index-cache insert.
 struct InsertArgs {
