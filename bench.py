@@ -618,7 +618,8 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                 # the conversion kernel, then per token segment the index, attend and merge kernels
                 wsb = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads,
                                             p.topk.shape[-1], p.page_table.shape[1], "cuda", stream).numel()
-                launches = 1 + 3 * gather_segments(pbs, b, wsb)
+                # (and the tile kernel's attend over the requests' dense leading tiles, top-k <= 16)
+                launches = 1 + (1 if p.topk.shape[-1] <= 16 else 0) + 3 * gather_segments(pbs, b, wsb)
         else:
             # rows of one request share their K/V rows: the union counts each once
             per_row = decode_bytes(b, decode_ctx(pbs, b))
@@ -629,9 +630,15 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     achieved = work / (statistics.mean(times) * 1e-3) / scale
     traffic = None
-    if args.workload == "prefill":
-        traffic = recorded_traffic("prefill_tc_prefill_varlen_bf16.md",
-                                   kernel_source_hash("attend_prefill_tc.cu", "tc_device.cuh", "pbs_device.cuh"))
+    if args.workload == "prefill" and part == "prefill":
+        # DRAM bytes per launch of the step's dominant kernel, from its committed ncu summary
+        if chosen == "gather":
+            traffic = recorded_traffic("gather_attend_prefill_varlen.md",
+                                       kernel_source_hash("attend_prefill_gather.cu", "tc_device.cuh",
+                                                          "pbs_device.cuh"))
+        elif chosen == "tile":
+            traffic = recorded_traffic("prefill_tc_prefill_varlen_bf16.md",
+                                       kernel_source_hash("attend_prefill_tc.cu", "tc_device.cuh", "pbs_device.cuh"))
     if rank == 0:
         print(json.dumps({
             "metric": metric, "value": job_rate(world, work, ms) / scale, "unit": unit, "n_gpus": world,

@@ -181,20 +181,21 @@ int encode_q_map_tokens(CUtensorMap* map, const void* q, int num_heads, int grou
 
 // Which prefill kernel runs: the caller's choice (pbs_attend_options.prefill_kernel) when given,
 // else by the page table's width (the only bound on the contexts that the host sees without a
-// device read):
+// device read) and the GQA ratio:
 //
 // The tile kernel streams the union of its 16 tokens' selections to all of them, so its waste
 // grows with the context a token chooses from: a token at block s selects k of s + 1 blocks,
 // and the union nears min(s + 1, 16 k). The gathered-row kernel's MMA rows are the tokens that
 // selected a block, so its work does not grow with the context, but every (token, block) pair
-// costs a partial output written and merged through the workspace. So page tables up to
-// kTileMaxBlocksPerTopk * k blocks take the tile kernel, wider ones the gathered-row kernel (with
-// a workspace that holds at least one 512-token segment; otherwise fp8 / NVFP4 stay on the tile
-// kernel and bf16 takes the token-centric kernel). Measured (64/8 heads, top-k 16): the varlen
-// prompts of 2k-8k tokens (64-block table) take 2.39 ms on the tile kernel and 2.37 on the
-// gathered-row kernel; 2 x 4096 tokens after 16k / 32k of context on NVFP4 take 4.69 and 1.89
-// ms; bf16 on the tile kernel gives 462 / 312 / 114 TFLOP/s for contexts 0 / 2k-4k / 16k-32k,
-// the token-centric kernel about 139 throughout.
+// costs a partial output written and merged through the workspace; it hands the dense leading
+// tiles of every request (tokens before position 128 k, which select every block they see) to
+// the tile kernel. With its workspace the gathered-row kernel is taken at GQA 8, and at GQA 16
+// for page tables wider than kTileMaxBlocksPerTopk * k blocks; otherwise the tile kernel (fp8 /
+// NVFP4 with its images; bf16 only up to that width) or the token-centric kernel. Measured (64
+// query heads, top-k 16): the varlen prompts of 2k-8k tokens (64-block table) take 2.37 ms on
+// the tile kernel, 2.22 on the gathered rows (2.10 / 2.45 at GQA 16); 2 x 4096 NVFP4 tokens
+// after 16k / 32k of context take 4.71 and 1.59 ms; bf16 on the tile kernel gives 462 / 312 / 114
+// TFLOP/s for contexts 0 / 2k-4k / 16k-32k, the token-centric kernel about 139 throughout.
 constexpr int kTileMaxBlocksPerTopk = 8;
 
 // The caller's options, checked (a null pointer reads as all zero).
@@ -238,7 +239,7 @@ int choose_prefill_kernel(const AttendArgs& a, size_t workspace_bytes, int force
   // contexts of 16k / 32k keys 1.04x)
   const bool wide = a.max_blocks > kTileMaxBlocksPerTopk * a.k;
   if (forced != PBS_PREFILL_AUTO) *kernel = forced;
-  else if (wide && gather_fits) *kernel = PBS_PREFILL_GATHER;
+  else if (gather_fits && (wide || a.group == 8)) *kernel = PBS_PREFILL_GATHER;
   else if (tile_fits && (a.kv_dtype != PBS_KV_BF16 || !wide)) *kernel = PBS_PREFILL_TILE;
   else *kernel = PBS_PREFILL_TOKEN;
   return PBS_OK;

@@ -229,8 +229,10 @@ def test_prefill_kernel_choice_rule():
     # fp8 / NVFP4 caches take the tile kernel only with its workspace (K and V images)
     assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096) == "token"
     big = 1 << 62
-    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, ws=big) == "tile"
-    assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, ws=big) == "tile"
+    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, ws=big) == "gather"   # GQA 8: the gathered rows first
+    assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, ws=big) == "gather"
+    assert run("fp8_e4m3", 64, 8, 16, 64, 8 * 4096, ws=pbs.prefill_tile_workspace_bytes(4, 8, 64, "fp8_e4m3")) == "tile"
+    assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, ws=pbs.prefill_tile_workspace_bytes(4, 8, 64, "nvfp4")) == "tile"
     assert run("nvfp4", 64, 8, 16, 64, 8 * 2304, "tile") == 3        # asked for without the workspace
     # page tables wider than 8 x top-k: the gathered-row kernel when its workspace is given
     assert run("nvfp4", 64, 8, 16, 400, 8 * 2304, ws=big) == "gather"
@@ -254,5 +256,7 @@ def test_prefill_kernel_choice_rule():
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need) == "gather"
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need - 256) == 3
     assert run("bf16", 64, 8, 16, 64, packed, "gather", ws=need, table=True) == 3   # it reads top-k only
-    assert run("bf16", 64, 8, 16, 64, packed, ws=need) == "tile"     # not unasked for page tables of 8 x top-k
+    assert run("bf16", 64, 8, 16, 64, packed, ws=need) == "gather"   # GQA 8 with its workspace
+    assert run("bf16", 64, 4, 16, 64, 4 * 8192, ws=big) == "tile"    # GQA 16: only for wider page tables
+    assert run("bf16", 64, 4, 16, 400, 4 * 8192, ws=big) == "gather"
     assert run("bf16", 60, 8, 16, 64, packed) == 1
