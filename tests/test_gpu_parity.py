@@ -634,8 +634,9 @@ def test_prebuilt_table_shared_by_two_layers(pbs, entry):
             nd = d.q.shape[0]
             args = (torch.cat([d.q, p.q]), b.cache, "bf16", 8, torch.cat([d.topk[0], p.topk[0]]), d.page_table,
                     d.seq_lens, d.decode_query_len, p.page_table, p.cu_seqlens_q, p.seq_lens, b.softmax_scale)
-            fused = pbs.sparse_mixed_attention(*args)
-            tabled = pbs.sparse_mixed_attention(*args, err_word=err,
+            # the prefill part on the tile kernel in both calls (the gathered rows read top-k only)
+            fused = pbs.sparse_mixed_attention(*args, kernel="tile")
+            tabled = pbs.sparse_mixed_attention(*args, err_word=err, kernel="tile",
                                                 sparse_table=(torch.cat([sbt_d, sbt_p]), torch.cat([ctx_d, ctx_p])))
             torch.cuda.synchronize()
             fused, tabled = fused.double().cpu().numpy(), tabled.double().cpu().numpy()
