@@ -603,7 +603,14 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
             unit, bound, peak, metric = "GB/s", "hbm", hbm, "table build HBM GB/s"
         elif part == "prefill":
             work = prefill_flops(prefill_ctx(pbs, b), b.num_heads)
-            times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream, kernel=kernel)
+            ws = "auto"
+            if args.prefill_segment_tokens > 0:
+                # a workspace for segments of this many tokens (smaller device footprint, for profiling)
+                p = b.pre
+                ws = torch.empty(pbs.prefill_workspace_bytes(args.prefill_segment_tokens, p.seq_lens.shape[0],
+                                                             b.num_heads, b.num_kv_heads, p.topk.shape[-1],
+                                                             p.page_table.shape[1]), dtype=torch.uint8, device="cuda")
+            times = run_prefill(pbs, b, args.steps, args.warmup, flush, stream, kernel=kernel, workspace=ws)
             unit, bound, peak, metric = "TFLOP/s", "tensor", bf16, "prefill TFLOP/s"
             p = b.pre
             # the binding's default call on the tile kernel: V conversion, then the attend; on the
@@ -616,8 +623,9 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                 launches = 2
             elif chosen == "gather":
                 # the conversion kernel, then per token segment the index, attend and merge kernels
-                wsb = pbs.prefill_workspace(p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads,
-                                            p.topk.shape[-1], p.page_table.shape[1], "cuda", stream).numel()
+                wsb = ws.numel() if isinstance(ws, torch.Tensor) else pbs.prefill_workspace(
+                    p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, p.topk.shape[-1],
+                    p.page_table.shape[1], "cuda", stream).numel()
                 # (and the tile kernel's attend over the requests' dense leading tiles, top-k <= 16)
                 launches = 1 + (1 if p.topk.shape[-1] <= 16 else 0) + 3 * gather_segments(pbs, b, wsb)
         else:
@@ -678,6 +686,8 @@ def main():
                     help="force the decode attend's split count (profiling and tuning)")
     ap.add_argument("--prefill-kernel", choices=["auto", "token", "tile", "gather"], default="auto",
                     help="force the prefill kernel of --workload prefill / prefill_g16 / mixed_nvfp4 --part prefill")
+    ap.add_argument("--prefill-segment-tokens", type=int, default=0,
+                    help="gathered-row prefill: a workspace for segments of this many tokens (profiling)")
     ap.add_argument("--workload", choices=["decode", "prefill", "prefill_g16", "mtp_fp8", "mixed_nvfp4", "decode_fp8",
                                            "decode_nvfp4", "table_prefill"],
                     default="decode",
