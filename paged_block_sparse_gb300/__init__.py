@@ -364,7 +364,7 @@ def prefill_kernel_choice(total_q: int, num_reqs: int, kv_dtype: str, page_strid
 
 
 # the default prefill workspace is capped; larger calls run in several token segments
-PREFILL_WORKSPACE_CAP = 4 << 30
+PREFILL_WORKSPACE_CAP = 8 << 30
 _prefill_workspaces: dict = {}
 
 

@@ -306,12 +306,18 @@ __global__ void __launch_bounds__(kIdxThreads) gather_index_kernel(const AttendA
       const uint32_t vm0 = __ballot_sync(0xffffffffu, v0), vm1 = __ballot_sync(0xffffffffu, v1);
       bool k0 = v0, k1 = v1;
       const int kk = a.k;
-      for (int j = 0; j < kk; ++j) {
-        const int bj = j < 32 ? __shfl_sync(0xffffffffu, b0, j) : __shfl_sync(0xffffffffu, b1, j - 32);
-        const bool vj = ((j < 32 ? vm0 >> j : vm1 >> (j - 32)) & 1u) != 0;
-        if (vj) {
-          if (j < lane && bj == b0) k0 = false;
-          if (j < lane + 32 && bj == b1) k1 = false;
+      if (kk <= 32) {
+        // one entry per lane: the lanes holding one value form one match group, its lowest keeps it
+        const uint32_t grp = __match_any_sync(0xffffffffu, v0 ? b0 : -1 - lane);
+        k0 = v0 && __ffs(grp) - 1 == lane;
+      } else {
+        for (int j = 0; j < kk; ++j) {
+          const int bj = j < 32 ? __shfl_sync(0xffffffffu, b0, j) : __shfl_sync(0xffffffffu, b1, j - 32);
+          const bool vj = ((j < 32 ? vm0 >> j : vm1 >> (j - 32)) & 1u) != 0;
+          if (vj) {
+            if (j < lane && bj == b0) k0 = false;
+            if (j < lane + 32 && bj == b1) k1 = false;
+          }
         }
       }
       const uint32_t km0 = __ballot_sync(0xffffffffu, k0), km1 = __ballot_sync(0xffffffffu, k1);
