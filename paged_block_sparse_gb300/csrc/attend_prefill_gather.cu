@@ -1129,11 +1129,14 @@ cudaError_t launch_gather_g(const AttendArgs& args, const CUtensorMap& kv_map, c
   a.kconv = a.kv_dtype == PBS_KV_BF16 ? nullptr : a.vconv + n_img * kTileVBytes + ((n_img * 4 + 255) / 256) * 256;
   cudaError_t e = launch_convert_images(a, stream);
   if (e != cudaSuccess) return e;
-  // Tokens whose tile's last position is below 128 k may select every block they see: the tile
-  // kernel takes those tiles on the same images (no union waste, no partials), this kernel the rest.
+  // Tokens before position 128 k may select every block they see, and up to 1.5 x 128 k at least
+  // two thirds of them, so a 16-token tile there wastes few MMA rows: the tile kernel takes each
+  // request's leading tiles up to that position on the same images (no partials), this kernel
+  // the rest. (Measured on the varlen prompts: limits of 1, 1.5, 2 and 3 x 128 k gave 2.10,
+  // 2.03, 2.04 and 2.18 ms.)
   a.tile_pos_limit = 0;
   if (tile_q_map != nullptr && a.k <= 16 && prefill_tc_supported(a, true)) {
-    a.tile_pos_limit = a.k * kSparseBlock;
+    a.tile_pos_limit = 3 * a.k * kSparseBlock / 2;
     e = launch_prefill_tc_attend(a, kv_map, *tile_q_map, stream);
     if (e != cudaSuccess) return e;
   }

@@ -84,9 +84,10 @@ struct AttendArgs {
   uint8_t* vconv;
   int32_t* vconv_exp;
   uint8_t* kconv;
-  // prefill split between the two tcgen05 kernels (0: none): the tile kernel takes the tiles of
-  // tokens before this position (128 k: every token of the tile may select every block it sees,
-  // so the tile wastes no rows on unselected blocks), the gathered-row kernel every other token
+  // prefill split between the two tcgen05 kernels (0: none): the tile kernel takes each
+  // request's leading tiles of tokens before this position (1.5 x 128 k: such a token selects at
+  // least two thirds of the blocks it sees, so its tile wastes few rows), the gathered-row kernel
+  // every other token
   int32_t tile_pos_limit;
 };
 
