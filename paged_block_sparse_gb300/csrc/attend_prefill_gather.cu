@@ -114,9 +114,11 @@ enum GTraceEv { kGtStart, kGtEnd, kGtProd = 2, kGtK = kGtProd + kGtChunks, kGtV 
                 kGtCount = kGtE1 + kGtChunks };
 __device__ long long g_gtrace[kGtCount];
 __device__ int g_gtrace_cta;
-#define GTRACE(ev, c) do { if (blockIdx.x == static_cast<unsigned>(g_gtrace_cta) && (c) < kGtChunks) \
-                             g_gtrace[(ev) + (c)] = clock64(); } while (0)
+// the traced CTA is read once per thread, so an event costs one clock read and one store
+#define GTRACE_INIT const bool gt_on_ = blockIdx.x == static_cast<unsigned>(g_gtrace_cta)
+#define GTRACE(ev, c) do { if (gt_on_ && (c) < kGtChunks) g_gtrace[(ev) + (c)] = clock64(); } while (0)
 #else
+#define GTRACE_INIT do { } while (0)
 #define GTRACE(ev, c) do { } while (0)
 #endif
 
@@ -462,6 +464,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint8_t* v_s = k_s + 2 * kGTile;    // 2 x 32 KiB: [half][128 keys][128 B] (fp16 image)
   GCtl* ctl = reinterpret_cast<GCtl*>(v_s + 2 * kGTile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  GTRACE_INIT;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDescRing; ++i) {
