@@ -626,7 +626,7 @@ def secondary_line(pbs, args, world, rank, local, pg, stream, flush, hbm, bf16, 
                 wsb = ws.numel() if isinstance(ws, torch.Tensor) else pbs.prefill_workspace(
                     p.q.shape[0], p.seq_lens.shape[0], b.num_heads, b.num_kv_heads, p.topk.shape[-1],
                     p.page_table.shape[1], "cuda", stream).numel()
-                # (and the tile kernel's attend over the requests' dense leading tiles, top-k <= 16)
+                # (and the tile kernel's attend over the requests' leading tiles, top-k <= 16)
                 launches = 1 + (1 if p.topk.shape[-1] <= 16 else 0) + 3 * gather_segments(pbs, b, wsb)
         else:
             # rows of one request share their K/V rows: the union counts each once

@@ -719,7 +719,7 @@ int pbs_sparse_prefill_attention(const void* q, int64_t q_row_stride, int64_t q_
              ? encode_q_map_tokens(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride)
              : encode_q_map(&qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride);
     if (st != PBS_OK) return st;
-    // the gathered-row kernel hands the call's dense leading tiles to the tile kernel
+    // the gathered-row kernel hands the call's leading tiles to the tile kernel
     const bool tile_part = kernel == PBS_PREFILL_GATHER &&
                            encode_q_map(&tile_qmap, q, num_heads, a.group, total_q, q_row_stride, q_head_stride) ==
                                PBS_OK;

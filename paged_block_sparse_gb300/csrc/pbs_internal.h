@@ -173,7 +173,7 @@ int64_t gather_segment_tokens(int64_t total_q, int num_reqs, int num_heads, int 
                               size_t ws_bytes);
 // `kv_map`: the per-block map of a packed bf16 cache (as for the tile kernel; unused for fp8 /
 // NVFP4); `q_map`: {128, heads, tokens} with a {64, G, 1} box.
-// `tile_q_map`: the tile kernel's Q map, with which the tile kernel takes the call's dense tiles
+// `tile_q_map`: the tile kernel's Q map, with which the tile kernel takes the call's leading tiles
 // when it can run the call (AttendArgs::tile_pos_limit); null: the gathered-row kernel takes all.
 cudaError_t launch_prefill_gather(const AttendArgs& a, const CUtensorMap& kv_map, const CUtensorMap& q_map,
                                   const CUtensorMap* tile_q_map, void* ws, size_t ws_bytes, cudaStream_t stream);
