@@ -71,7 +71,7 @@ struct ChunkDesc {
   int32_t n_tok;  // tokens in this chunk
   int32_t item;   // the CTA's item number (phase of the K/V buffer barriers)
   int32_t req;    // request (the item's images are those of (req, b, g))
-  int32_t pad;
+  int32_t vexp;   // the item's V image holds V * 2^-vexp
   int32_t tr[16];    // segment-relative token index
   int32_t slot[16];  // the token's partial slot for block b
   int32_t lim[16];   // keys of block b the token sees (128, or pos - 128 b + 1 for its own block)
@@ -551,6 +551,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (lane < B.nb) v = __ldg(w.chunks + static_cast<int64_t>(B.w) * w.ccap + B.base + lane);
       return v;
     };
+    // the V image exponent of each chunk of a batch whose records are in hand, one per lane
+    auto load_exps = [&](const Batch& B, const int4& rec) {
+      int e = 0;
+      if (lane < B.nb)
+        e = __ldg(a.vconv_exp + (static_cast<int64_t>(B.r) * a.max_blocks + (rec.x & 8191)) * a.num_kv_heads +
+                  (rec.x >> 13));
+      return e;
+    };
     // bucket entries of a batch: entry e = chunk e / kTok, token e % kTok; four per lane
     auto load_ents = [&](const Batch& B, const int4& rec, int (&e)[4]) {
 #pragma unroll
@@ -571,6 +579,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     Batch B0, B1, B2;
     next_batch(B0);
     int4 rec0 = load_recs(B0);
+    int x0 = load_exps(B0, rec0);
     next_batch(B1);
     int4 rec1 = load_recs(B1);
     int e_cur[4];
@@ -583,11 +592,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
       next_batch(B2);
       const int4 rec2 = load_recs(B2);
       load_ents(B1, rec1, e_cur);
+      const int x1 = load_exps(B1, rec1);
       for (int jc = 0; jc < B0.nb && ok; ++jc, ++c) {
         const int rx = __shfl_sync(0xffffffffu, rec0.x, jc);
         const int b = rx & 8191, g = rx >> 13;
         const int n_tok = __shfl_sync(0xffffffffu, rec0.z, jc);
         const int phys = __shfl_sync(0xffffffffu, rec0.w, jc);
+        const int vexp = __shfl_sync(0xffffffffu, x0, jc);
         // ---- a new (request, block, kv head): its K into the next K buffer (warp 3 loads V)
         if (B0.r != item_r || b != item_b || g != item_g) {
           ++n_item;
@@ -648,6 +659,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           d->n_tok = n_tok;
           d->item = n_item;
           d->req = B0.r;
+          d->vexp = vexp;
         }
         // ---- gather the chunk's Q rows: token j -> its G rows, one {64, 8, 2, G / 8, 1} copy
         const int qb = c & 1;
@@ -673,6 +685,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
       B0 = B1;
       rec0 = rec1;
+      x0 = x1;
       B1 = B2;
       rec1 = rec2;
     }
@@ -828,8 +841,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const bool end = d->end != 0;
       uint32_t v[64];
       // the exponent of this chunk's V image, for its partial one iteration later
-      const int e_cur = end ? 0 : __ldg(a.vconv_exp + (static_cast<int64_t>(d->req) * a.max_blocks + d->b) *
-                                                          a.num_kv_heads + d->g);
+      const int e_cur = end ? 0 : d->vexp;
       if (!end) {
         if (!g_warp_wait(&ctl->s_full[X], (c >> 1) & 1, ctl, a.err_word)) break;
         tc::fence_after_sync();
