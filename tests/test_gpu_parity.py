@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads
-from helpers import TOL, assert_close, cache_source, np_i32, oracle_decode, oracle_prefill, q64
+from helpers import assert_close, cache_source, np_i32, oracle_decode, oracle_prefill, q64
 
 pytestmark = pytest.mark.gpu
 
