@@ -282,6 +282,32 @@ def test_dense_topk_equals_causal_attention(kv_dtype, Hq, Hkv):
     np.testing.assert_allclose(ours, ref, rtol=0, atol=1e-12)
 
 
+def test_partials_over_disjoint_key_sets_combine_by_lse():
+    """Attention over a key set split into disjoint parts: each part's output weighted by
+    exp(lse_part - lse_all), summed, is the output over the whole set, and lse_all is the
+    log-sum-exp of the parts' lse (the identity behind per-block partials merged by their
+    log-sum-exp; a dropped or mis-signed term in either oracle function breaks it)."""
+    rng = np.random.default_rng(31)
+    Hq, Hkv, n, D = 8, 2, 300, 64
+    q = rng.standard_normal((Hq, D))
+    K = rng.standard_normal((Hkv, n, D))
+    V = rng.standard_normal((Hkv, n, D))
+    scale, ks, vs = 0.11, 1.5, 0.75
+    full = oracle.attend(q, K, V, scale, ks, vs)
+    lse_full = oracle.attend_lse(q, K, scale, ks)
+    cuts = [0, 1, 128, 131, 300]  # parts of 1, 127, 3 and 169 keys
+    outs, lses = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        outs.append(oracle.attend(q, K[:, a:b], V[:, a:b], scale, ks, vs))
+        lses.append(oracle.attend_lse(q, K[:, a:b], scale, ks))
+    lses = np.stack(lses)                      # [parts, Hq]
+    m = lses.max(axis=0)
+    lse_comb = m + np.log(np.exp(lses - m).sum(axis=0))
+    np.testing.assert_allclose(lse_comb, lse_full, rtol=0, atol=1e-12)
+    comb = sum(np.exp(l - lse_full)[:, None] * o for l, o in zip(lses, outs))
+    np.testing.assert_allclose(comb, full, rtol=0, atol=1e-12)
+
+
 def test_dense_lse_equals_torch_logsumexp():
     """Log-sum-exp output, dense top-k: equals torch.logsumexp of the causal logits computed on
     the unpaged sequence (a library routine on an independent path from the paged gather)."""
