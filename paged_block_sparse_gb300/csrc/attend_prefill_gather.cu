@@ -27,14 +27,18 @@
 //   block scan, scatter). Tokens with no valid block get zero output here.
 // * Attend kernel (persistent, one CTA per SM): windows are taken in order and CTA i takes chunks
 //   [i C / G, (i + 1) C / G) of a window with C chunks, so every CTA works on the same few
-//   windows at a time and their Q rows and K / V images stay in L2. Warp 0 loads K and V of a
-//   (block, kv head) item (one 32 KiB copy each) into one of two buffers, writes each chunk's
+//   windows at a time and their Q rows and K / V images stay in L2. Warp 0 loads the K of a
+//   (block, kv head) item (one 32 KiB copy) into one of two buffers, writes each chunk's
 //   descriptor (tokens, partial slots, own-block key limits, the V image's exponent) into an
 //   8-deep ring and gathers the chunk's Q rows (one tensor copy per token: its G heads, both
-//   64-dim halves). Warp 1 (one thread) issues S(c) = Q K^T into TMEM buffer c % 2, then
-//   PV(c - 1), so the softmax of chunk c overlaps PV(c - 1) and S(c + 1). Warps 4-11 (two per
-//   TMEM lane quadrant, 64 keys each) take the softmax of chunk c, writing P as fp16 over S,
+//   64-dim halves); warp 3 loads each item's V image into one of two buffers. Warp 1 (one
+//   thread) issues S(c) = Q K^T into TMEM buffer c % 2 and PV(c - 1), in whichever order their
+//   operands arrive, so the softmax of chunk c overlaps PV(c - 1) and S(c + 1). Warps 4-11 (two
+//   per TMEM lane quadrant, 64 keys each) take the softmax of chunk c, writing P as fp16 over S,
 //   then store chunk c - 1's partial while PV(c) runs.
+// * With the tile kernel's Q map, each request's leading tiles (tokens before position
+//   1.5 x 128 k, `leading_tiles`) go to the tile kernel on the same images, and the index kernel
+//   skips their tokens.
 // * Softmax of one chunk (one key block): the row maximum over the block's valid keys (row
 //   maxima of the two key halves meet in shared memory), P = 2^(s * scale * log2 e - m) <= 1 as
 //   fp16 (one PV MMA per 16 keys against the fp16 V image). The partial is O / l (the image's
